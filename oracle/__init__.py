@@ -1,0 +1,150 @@
+"""SDM forward oracle: plain CPU reference of the Sparse Delta Memory forward pass.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import this package.  The
+product library (``sparse_state_linear_sdm_gb300``) shares no code with it.
+
+What it computes follows the "Sparse Delta Memory (SDM)" technical summary
+(gist.science/it/paper/2607.07386), section "Meccanismo Core", items 1-4:
+product-key top-W / top-R slot selection through
+topk(s1 (+) s2) = topk(topk(s1) (+) topk(s2)), the gated delta write
+M_t[i] = a_t M_{t-1}[i] + b_t k_t^(i) (v_t - a_t M_{t-1}[i]) on the selected rows
+only, and a weighted read of the R selected rows after the write.  The
+arithmetic lives in ``sdm_oracle.cpp`` (fp32 selection sums, fp64 state).
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against things
+other than itself: brute force over all N slot scores, a hand-worked two-token
+example, invariants of the update equations and closed forms.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sdm_oracle.cpp")
+_SO = os.path.join(_HERE, "_build", "liboracle_sdm.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle's C++ into a shared library (host code only)."""
+    if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
+        return _SO
+    os.makedirs(os.path.dirname(_SO), exist_ok=True)
+    tmp = _SO + f".tmp{os.getpid()}"
+    cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
+           "-o", tmp, _SRC]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, i32, p = ctypes.c_longlong, ctypes.c_int, ctypes.c_void_p
+            lib.oracle_select.argtypes = [p, i64, i32, i32, p, p, i32]
+            lib.oracle_select.restype = i32
+            lib.oracle_scan.argtypes = [p, i32, i64, i32, i32, i32, i32, p, p, p, p, p, p, p, p, i32]
+            lib.oracle_scan.restype = i32
+            _lib = lib
+    return _lib
+
+
+def _threads(n_threads):
+    return int(n_threads) if n_threads else (os.cpu_count() or 1)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def select(halves, K: int, n_threads=None):
+    """Top-K slots of every item.  halves: float32 [..., 2, S] (half 0, half 1).
+
+    Returns (idx int32 [..., K], sc float32 [..., K]) ordered by (sum desc, flat asc),
+    flat = i*S + j with i from half 0.
+    """
+    h = _c(halves, np.float32)
+    S = h.shape[-1]
+    lead = h.shape[:-2]
+    n = int(np.prod(lead)) if lead else 1
+    idx = np.empty(lead + (K,), np.int32)
+    sc = np.empty(lead + (K,), np.float32)
+    rc = _load().oracle_select(h.ctypes.data, n, S, K, idx.ctypes.data, sc.ctypes.data,
+                               _threads(n_threads))
+    if rc != 0:
+        raise ValueError(f"oracle_select: bad sizes S={S} K={K}")
+    return idx, sc
+
+
+def select_bruteforce(halves, K: int):
+    """Same contract as ``select`` but by ranking all S*S slot scores directly.
+
+    Independent of the C++ selection: the N scores fp32(half0[i] + half1[j]) at
+    flat = i*S + j are ordered with numpy's lexsort (score desc, flat asc).
+    Used only on tiny inputs to pin the product-key identity.
+    """
+    h = _c(halves, np.float32)
+    S = h.shape[-1]
+    lead = h.shape[:-2]
+    flat_h = h.reshape(-1, 2, S)
+    n = flat_h.shape[0]
+    if K < 1 or K > S * S:
+        raise ValueError(f"select_bruteforce: bad sizes S={S} K={K}")
+    idx = np.empty((n, K), np.int32)
+    sc = np.empty((n, K), np.float32)
+    flat = np.arange(S * S)
+    for it in range(n):
+        scores = (flat_h[it, 0][:, None] + flat_h[it, 1][None, :]).astype(np.float32).ravel()
+        order = np.lexsort((flat, -scores))[:K]
+        idx[it] = flat[order]
+        sc[it] = scores[order]
+    return idx.reshape(lead + (K,)), sc.reshape(lead + (K,))
+
+
+def scan(M, idx_w, sc_w, idx_r, sc_r, v, alpha, beta, n_threads=None):
+    """Recurrent sparse gated-delta scan of nh independent (sequence, head) pairs.
+
+    M: float64 [nh, N, d_v], updated in place (state before -> after the T tokens).
+    idx_w/sc_w: [nh, T, W]; idx_r/sc_r: [nh, T, R]; v: [nh, T, d_v];
+    alpha/beta: [nh, T].  Returns o float64 [nh, T, d_v].
+    """
+    if not (isinstance(M, np.ndarray) and M.dtype == np.float64 and M.flags.c_contiguous):
+        raise TypeError("M must be a C-contiguous float64 array (updated in place)")
+    nh, N, dv = M.shape
+    iw, sw = _c(idx_w, np.int32), _c(sc_w, np.float32)
+    ir, sr = _c(idx_r, np.int32), _c(sc_r, np.float32)
+    vv = _c(v, np.float32)
+    a, b = _c(alpha, np.float32), _c(beta, np.float32)
+    T, W = iw.shape[1], iw.shape[2]
+    R = ir.shape[2]
+    o = np.empty((nh, T, dv), np.float64)
+    rc = _load().oracle_scan(M.ctypes.data, nh, N, dv, T, W, R, iw.ctypes.data, sw.ctypes.data,
+                             ir.ctypes.data, sr.ctypes.data, vv.ctypes.data, a.ctypes.data,
+                             b.ctypes.data, o.ctypes.data, _threads(n_threads))
+    if rc != 0:
+        raise ValueError("oracle_scan: bad sizes or slot index out of range")
+    return o
+
+
+def forward(kp, qp, v, alpha, beta, M_init, W: int, R: int, n_threads=None):
+    """Selection then scan for nh (sequence, head) pairs.
+
+    kp, qp: float32 [nh, T, 2, S]; v: [nh, T, d_v]; alpha, beta: [nh, T];
+    M_init: [nh, N, d_v] (copied to fp64; the caller's array is not modified).
+    Returns dict(idx_w, sc_w, idx_r, sc_r, o (float64), M (float64 final state)).
+    """
+    idx_w, sc_w = select(kp, W, n_threads)
+    idx_r, sc_r = select(qp, R, n_threads)
+    M = np.array(M_init, dtype=np.float64, order="C", copy=True)
+    o = scan(M, idx_w, sc_w, idx_r, sc_r, v, alpha, beta, n_threads)
+    return dict(idx_w=idx_w, sc_w=sc_w, idx_r=idx_r, sc_r=sc_r, o=o, M=M)
