@@ -1,0 +1,369 @@
+#!/usr/bin/env python3
+"""SDM forward benchmark: prints one JSON line.
+
+A step is one pass of the whole forward hot path over one batch of synthetic
+input resident in HBM: state initialisation from M_0, product-key selection, and
+the sparse gated-delta scan (planning kernel + scan kernel).  The default
+workload is B=16, H=4, T=8192, N=1,048,576 (S=1024), d_v=128, W=R=128 with bf16
+k', q', v and fp32 state (34 GB).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl ours|reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs its own batch of
+sequences (weak scaling; no collective on the data path).  `--impl reference`
+times the CPU oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SDM forward head-tokens/s on 1 GB300; achieved HBM GB/s vs roofline"
+UNIT = "head-tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+SCAN_SRC = os.path.join(ROOT, "sparse_state_linear_sdm_gb300", "csrc", "sdm_scan.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "scan_kernel_dram_traffic.json")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cols", type=int, default=0, help="force scan columns per block (0 = auto)")
+    ap.add_argument("--pd", type=int, default=0, help="force scan prefetch depth (0 = auto)")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def scan_bytes_per_head_token(cfg) -> int:
+    """Algorithmic HBM bytes of the scan per head-token: W rows gathered and scattered,
+    R rows gathered (fp32, d_v each), v, alpha and beta read, o written."""
+    elt = 2 if cfg.in_dtype == "bf16" else 4
+    return (2 * cfg.W + cfg.R) * cfg.d_v * 4 + cfg.d_v * elt + 8 + cfg.d_v * 4
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_per_launch(units: int):
+    """DRAM bytes per scan launch from the committed ncu summary, scaled from its
+    captured case by head-tokens; None if absent or taken on another kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+        with open(SCAN_SRC, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        if rec.get("source_sha256") != sha:
+            return None
+        return float(rec["dram_bytes_per_head_token"]) * units
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        self.out.flush()
+        with open(self.out.name) as f:
+            rows = [[c.strip() for c in line.split(",")] for line in f if line.strip()]
+        os.unlink(self.out.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def make_state(cfg, rank, dev, torch, sdm, wl):
+    """Inputs drawn in HBM by the device generator (rank r draws batch rows
+    r*B .. r*B+B-1 of the logical workload) and every buffer of the step."""
+    dt = torch.bfloat16 if cfg.in_dtype == "bf16" else torch.float32
+    bias = wl.half_bias(cfg)
+    bias_d = None if bias is None else torch.from_numpy(bias).to(dev)
+    inp = sdm.gen_inputs(cfg.seed, cfg.B, cfg.H, cfg.T, cfg.S, cfg.d_v, dt, cfg.alpha_lo,
+                         0 if cfg.beta_kind == "uniform" else 1, half_bias=bias_d, b_off=rank * cfg.B,
+                         device=dev)
+    st = dict(inp)
+    st["M0"] = sdm.gen_M0(cfg.seed, cfg.H, cfg.N, cfg.d_v, float(wl.M0_SCALE), device=dev)
+    st["M"] = torch.empty((cfg.B, cfg.H, cfg.N, cfg.d_v), dtype=torch.float32, device=dev)
+    sh = (cfg.B, cfg.H, cfg.T)
+    st["sel"] = (torch.empty(sh + (cfg.W,), dtype=torch.int32, device=dev),
+                 torch.empty(sh + (cfg.W,), dtype=torch.float32, device=dev),
+                 torch.empty(sh + (cfg.R,), dtype=torch.int32, device=dev),
+                 torch.empty(sh + (cfg.R,), dtype=torch.float32, device=dev))
+    st["o"] = torch.empty(sh + (cfg.d_v,), dtype=torch.float32, device=dev)
+    st["ws"] = sdm.scan_workspace(cfg.B, cfg.H, cfg.T, cfg.d_v, cfg.W, cfg.R, dev)
+    st["err"] = torch.zeros(1, dtype=torch.int32, device=dev)
+    return st
+
+
+def run_step(st, cfg, sdm, args, ev=None):
+    """One forward pass; ev = (e0, e1, e2, e3, e4) events around init / select / plan / scan."""
+    if ev:
+        ev[0].record()
+    sdm.init_state_from_M0(st["M"], st["M0"])
+    if ev:
+        ev[1].record()
+    sdm.select(st["kp"], st["qp"], cfg.W, cfg.R, out=st["sel"])
+    if ev:
+        ev[2].record()
+    sdm.scan_forward(st["M"], *st["sel"], st["v"], st["alpha"], st["beta"], o=st["o"], workspace=st["ws"],
+                     dev_err=st["err"], cols_per_cta=args.cols, prefetch_depth=args.pd,
+                     event_after_plan=ev[3] if ev else None)
+    if ev:
+        ev[4].record()
+
+
+def cpu_baseline(cfg, wl, oracle, steps=1, tokens=None):
+    """The oracle, as it stands, on a bounded sample: batch row 0, every head, the
+    first `tokens` tokens (default: all), fp64 state initialised from M_0."""
+    import numpy as np
+
+    T = cfg.T if tokens is None else min(tokens, cfg.T)
+    heads = [(0, h) for h in range(cfg.H)]
+    parts = [wl.inputs(cfg, b, b + 1, h, h + 1, 0, T) for b, h in heads]
+    host = {k: np.concatenate([p[k].reshape((1,) + p[k].shape[2:]) for p in parts]) for k in parts[0]}
+    M0 = wl.initial_state(cfg, 0, cfg.H)
+    cores = os.cpu_count() or 1
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        oracle.forward(host["kp"], host["qp"], host["v"], host["alpha"], host["beta"], M0, cfg.W, cfg.R,
+                       n_threads=cores)
+        times.append(time.perf_counter() - t0)
+    units = len(heads) * T
+    return dict(value=units / statistics.median(times), unit=UNIT, cores=cores, kind="oracle",
+                sample=f"{cfg.name}: batch row 0, all {cfg.H} heads, tokens 0..{T - 1} ({units} head-tokens), "
+                       f"fp64 state initialised from M_0, selection + scan; median of {steps}"), times, units
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from sparse_state_linear_sdm_gb300 import workloads as wl
+
+    cfg = wl.CONFIGS[args.config]
+    oracle.build()
+    tokens = min(cfg.T, 2048)
+    base, times, units = cpu_baseline(cfg, wl, oracle, steps=args.warmup + args.steps, tokens=tokens)
+    timed = times[args.warmup:]
+    value = units * len(timed) / sum(timed)
+    base["value"] = value
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(timed) / len(timed),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(cfg), "cpu_baseline": base,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(cfg):
+    return {"workload": cfg.name, "B": cfg.B, "H": cfg.H, "T": cfg.T, "N": cfg.N, "d_v": cfg.d_v, "W": cfg.W,
+            "R": cfg.R, "inputs": cfg.in_dtype, "state": "f32",
+            "l2": "inputs larger than L2 (state table and k'/q' each exceed the 129 MB L2)",
+            "step": "init_state_from_M0 + select + scan_forward (plan + scan kernels)"}
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import sparse_state_linear_sdm_gb300 as sdm
+    from sparse_state_linear_sdm_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = wl.CONFIGS[args.config]
+    st = make_state(cfg, rank, dev, torch, sdm, wl)
+    torch.cuda.synchronize(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        run_step(st, cfg, sdm, args)
+    torch.cuda.synchronize(dev)
+    if st["err"].item() != 0:
+        raise RuntimeError(f"device error flags {st['err'].item()}")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for k in range(K):
+            run_step(st, cfg, sdm, args, evs[k])
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+    barrier()
+    total_ms = evs[0][0].elapsed_time(evs[-1][4])
+    phase = {name: sum(e[i].elapsed_time(e[i + 1]) for e in evs) / K
+             for i, name in enumerate(("init_ms", "select_ms", "plan_ms", "scan_ms"))}
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    units_rank = cfg.B * cfg.H * cfg.T
+    value = world * units_rank * K / (total_ms / 1e3)
+
+    # roofline of the dominant kernel (the scan), from its own events
+    peak, peak_kind = hbm_peak()
+    alg = scan_bytes_per_head_token(cfg) * units_rank
+    achieved = alg / (phase["scan_ms"] / 1e3) / 1e9
+    shape = sdm.scan_launch_info(cfg.B, cfg.H, cfg.d_v, cfg.W, cfg.R)
+    if args.cols or args.pd:
+        shape["forced"] = {"cols_per_cta": args.cols, "prefetch_depth": args.pd}
+    traffic = traffic_per_launch(units_rank)
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic", "config": config_dict(cfg),
+            "roofline": {"kernel": "sdm scan kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                         else "fallback", "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": traffic, "algorithmic_bytes_per_launch": alg},
+            "kernels": dict(phase, scan_shape=shape, wall_ms_per_step=1e3 * t_wall / K),
+            "gpu_launches": 4 * K}
+    line["clocks"] = clk.summary()
+
+    if not args.no_e2e:
+        line["e2e"] = e2e(st, cfg, sdm, args, dev, torch, K, world)
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        import oracle
+        oracle.build()
+        line["cpu_baseline"] = cpu_baseline(cfg, wl, oracle)[0]
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def e2e(st, cfg, sdm, args, dev, torch, K, world):
+    """Same metric through the public API with the inputs in pinned host memory:
+    every step copies k', q', v, alpha, beta host->device and o device->host."""
+    import torch.distributed as dist
+
+    names = ("kp", "qp", "v", "alpha", "beta")
+    host = {k: torch.empty(st[k].shape, dtype=st[k].dtype, pin_memory=True) for k in names}
+    for k in names:
+        host[k].copy_(st[k])
+    o_host = torch.empty(st["o"].shape, dtype=torch.float32, pin_memory=True)
+    h2d = sum(host[k].numel() * host[k].element_size() for k in names)
+    d2h = o_host.numel() * 4
+    torch.cuda.synchronize(dev)
+
+    def step():
+        for k in names:
+            st[k].copy_(host[k], non_blocking=True)
+        run_step(st, cfg, sdm, args)
+        o_host.copy_(st["o"], non_blocking=True)
+
+    step()
+    torch.cuda.synchronize(dev)
+    n = max(1, min(K, 10))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    a.record()
+    for _ in range(n):
+        step()
+    b.record()
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": world * cfg.B * cfg.H * cfg.T * n / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms / n}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

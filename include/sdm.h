@@ -1,0 +1,154 @@
+/* sdm.h - C ABI of the GB300 (sm_103a) Sparse Delta Memory forward hot path.
+ *
+ * The layer (Sparse Delta Memory (SDM) technical summary,
+ * gist.science/it/paper/2607.07386, "Meccanismo Core" items 1-4):
+ *   each (sequence b, head h) owns a memory table M in R^{N x d_v}, started from a
+ *   learned M_0 ("Stato Iniziale Appreso").  At every token t the projected key k'
+ *   and query q' are split in two halves of S = sqrt(N) sub-scores each; slot
+ *   i*S + j scores half0[i] + half1[j].  The top-W slots of k' are written with
+ *     M_t[i] = alpha_t M_{t-1}[i] + beta_t k_t^(i) (v_t - alpha_t M_{t-1}[i])
+ *   (k_t^(i): softmax over the W selected write scores), every other slot is left
+ *   untouched, and the output is o_t = sum_i r_i M_t[i] over the top-R slots of q'
+ *   (r: softmax over the R selected read scores), read after the write.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     keeps no pointer after the call returns and allocates nothing.  Tensors are
+ *     dense row-major ("C order") with the shapes given below and must be 16-byte
+ *     aligned (SDM_EALIGN otherwise).
+ *   - `stream` is a cudaStream_t passed as a plain pointer (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously on it; the call returns before the
+ *     GPU finishes.
+ *   - Arguments are checked on the host before anything is launched.  A failed
+ *     check returns SDM_EINVAL / SDM_EALIGN / SDM_EUNSUPPORTED and launches
+ *     nothing.  A failed launch returns SDM_ECUDA (cudaGetLastError is consumed).
+ *   - Conditions only the GPU can see (a slot index outside [0, N), a repeated slot
+ *     in one token's write set) are OR-ed into `*dev_err` (SDM_DEV_* bits, device
+ *     memory, may be NULL) and never trap; the offending rows are skipped, so no
+ *     access leaves the caller's buffers, and the results are then unspecified.
+ *   - Floating-point inputs are expected finite; NaN sub-scores give an
+ *     unspecified selection.
+ */
+#ifndef SDM_H_
+#define SDM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SDM_OK = 0,
+  SDM_EINVAL = -1,       /* a size or dtype argument is out of range */
+  SDM_EALIGN = -2,       /* a pointer is NULL or not 16-byte aligned */
+  SDM_ECUDA = -3,        /* a CUDA launch or query failed */
+  SDM_ETIMEOUT = -4,     /* reserved: a bounded device wait ran out */
+  SDM_EBOUNDS = -5,      /* reserved: device-detected bounds error */
+  SDM_EUNSUPPORTED = -6, /* sizes valid for the method but beyond this build's limits */
+  SDM_ENOSPACE = -7      /* the workspace passed is smaller than required */
+} sdm_status;
+
+typedef enum { SDM_F32 = 0, SDM_BF16 = 1 } sdm_dtype;
+
+/* bits OR-ed into *dev_err by the device */
+#define SDM_DEV_INDEX_RANGE 1 /* a slot index was < 0 or >= N */
+#define SDM_DEV_DUP_WRITE 2   /* a slot appeared twice in one token's write set */
+
+/* Limits of this build (checked on the host, SDM_EUNSUPPORTED beyond them). */
+#define SDM_MAX_S 4096  /* sqrt(N) */
+#define SDM_MAX_K 1024  /* W and R */
+
+/* Human-readable name of a status code (static string). */
+const char* sdm_status_str(int status);
+
+/* sdm_init_state_from_M0 - start every sequence from the learned initial state
+ * ("Stato Iniziale Appreso": M_0 is a learnable parameter copied into the state).
+ *   M  [B, H, N, d_v] fp32, written: M[b, h] = M0[h] for every b.
+ *   M0 [H, N, d_v]    fp32, read only.
+ * Requires B, H >= 1, N >= 1, d_v >= 4, d_v % 4 == 0. */
+int sdm_init_state_from_M0(float* M, const float* M0, int B, int H, long long N, int d_v,
+                           void* stream);
+
+/* sdm_select - product-key slot selection ("Meccanismo Core" item 2).
+ * For every (b, h, t): halves a = kp[b,h,t,0,:], b = kp[b,h,t,1,:] (S entries each,
+ * the sub-scores themselves).  With k = min(W, S), the top-k of each half by
+ * (value desc, index asc) are combined into the k x k grid of fp32 sums
+ * a[i] + b[j] at flat slot i*S + j, and the top-W of the grid by (sum desc, flat
+ * asc) are returned: idx_w[b,h,t,:] (int32 flat slots) and sc_w[b,h,t,:] (fp32
+ * sums), best first.  This equals the top-W of all N = S*S slot scores
+ * (topk(s1 (+) s2) = topk(topk(s1) (+) topk(s2))).  The same for q' with R.
+ *   kp, qp       [B, H, T, 2, S] in_dt (SDM_F32 or SDM_BF16)
+ *   idx_w, sc_w  [B, H, T, W] written;  idx_r, sc_r [B, H, T, R] written.
+ * Requires 1 <= S <= SDM_MAX_S, 1 <= W, R <= min(S*S, SDM_MAX_K), T >= 0.
+ * Results are bit-identical from run to run. */
+int sdm_select(const void* kp, const void* qp, int in_dt, int B, int H, int T, int S, int W, int R,
+               int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, void* stream);
+
+/* Bytes of device workspace sdm_scan_forward needs for these sizes (0 when T == 0). */
+size_t sdm_scan_workspace_size(int B, int H, int T, int d_v, int W, int R);
+
+/* sdm_scan_forward - the recurrent sparse gated-delta scan ("Meccanismo Core"
+ * items 3 and 4) over T tokens of every (b, h), continuing from the state in M.
+ *   M      [B, H, N, d_v] fp32, in: state before token 0, out: state after token T-1.
+ *   idx_w, sc_w [B, H, T, W]; idx_r, sc_r [B, H, T, R] as written by sdm_select
+ *          (slots distinct within a token's write set).
+ *   v      [B, H, T, d_v] v_dt;  alpha, beta [B, H, T] fp32.
+ *   o      [B, H, T, d_v] fp32, written: o_t = sum_i softmax(sc_r[t])_i M_t[idx_r[t,i]].
+ *   workspace  device scratch of at least sdm_scan_workspace_size(...) bytes, 16-byte
+ *          aligned; its contents on entry do not matter and are clobbered.
+ *   dev_err  device int, may be NULL; SDM_DEV_* bits are OR-ed in.
+ * Calls chained on one stream continue one another exactly: running T1 tokens then
+ * T2 tokens gives bit-identical results to one call over T1 + T2 tokens.
+ * Requires d_v % 4 == 0, d_v >= 4, 1 <= W, R <= SDM_MAX_K, N >= max(W, R). */
+int sdm_scan_forward(float* M, const int32_t* idx_w, const float* sc_w, const int32_t* idx_r,
+                     const float* sc_r, const void* v, int v_dt, const float* alpha,
+                     const float* beta, int B, int H, int T, long long N, int d_v, int W, int R,
+                     float* o, void* workspace, size_t workspace_bytes, int* dev_err,
+                     void* stream);
+
+/* Same as sdm_scan_forward with the scan kernel's shape forced instead of chosen:
+ * cols_per_cta in {4, 8, 16, 32} (d_v columns owned by one thread block, d_v % cols == 0)
+ * and prefetch_depth in {1, 2, 3} (tokens of rows gathered ahead).  0 keeps the
+ * automatic choice.  The state and the slots do not depend on the shape; o may differ
+ * in the last bits (order of the read reduction).  `event_after_plan`, if not NULL, is
+ * a cudaEvent_t recorded on `stream` between the planning kernel and the scan kernel
+ * (for timing the scan kernel alone).  For tuning, tests and measurement. */
+int sdm_scan_forward_tuned(float* M, const int32_t* idx_w, const float* sc_w,
+                           const int32_t* idx_r, const float* sc_r, const void* v, int v_dt,
+                           const float* alpha, const float* beta, int B, int H, int T,
+                           long long N, int d_v, int W, int R, float* o, void* workspace,
+                           size_t workspace_bytes, int* dev_err, int cols_per_cta,
+                           int prefetch_depth, void* event_after_plan, void* stream);
+
+/* The scan kernel shape sdm_scan_forward would use (host-only query): columns per
+ * thread block, prefetch depth, thread blocks, dynamic shared memory bytes. */
+int sdm_scan_launch_info(int B, int H, int d_v, int W, int R, int* cols_per_cta,
+                         int* prefetch_depth, int* blocks, int* smem_bytes);
+
+/* sdm_gen_inputs - synthetic inputs (not part of the method): draws the box
+ * b in [b_off, b_off+B), all H heads, tokens t in [t_off, t_off+T) of a logical
+ * workload with T_total tokens per sequence, from the counter-based generator
+ * (Philox4x32-10 keyed by `seed`, Box-Muller with fixed fp32 series; bit-identical
+ * to the host generator that feeds the CPU reference).
+ *   kp, qp [B, H, T, 2, S] in_dt: N(0,1) (+ half_bias[j] on index j of every half
+ *          when half_bias, a device fp32 [S] array, is not NULL);
+ *   v [B, H, T, d_v] in_dt: N(0,1);  alpha [B, H, T] fp32: U(alpha_lo, 1);
+ *   beta [B, H, T] fp32: U(0, 1) if beta_kind == 0, sigmoid(N(0,1)) if 1.
+ * Any of kp, qp, v, alpha, beta may be NULL to skip that tensor. */
+int sdm_gen_inputs(unsigned long long seed, int B, int H, int T, int b_off, int t_off,
+                   long long T_total, int S, int d_v, int in_dt, float alpha_lo, int beta_kind,
+                   const float* half_bias, void* kp, void* qp, void* v, float* alpha,
+                   float* beta, void* stream);
+
+/* sdm_gen_M0 - synthetic learned initial state: M0 [H, N, d_v] fp32 = scale * N(0,1)
+ * from the same generator (field of M_0). */
+int sdm_gen_M0(unsigned long long seed, int H, long long N, int d_v, float scale, float* M0,
+               void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDM_H_ */

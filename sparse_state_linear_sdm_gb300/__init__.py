@@ -1,0 +1,14 @@
+"""GB300 (sm_103a) Sparse Delta Memory forward hot path.
+
+The compute lives in ``libsdm.so`` (CUDA C++, C ABI declared in include/sdm.h);
+``api`` is a thin ctypes binding for torch tensors and ``workloads`` defines the
+seeded synthetic configurations.  Importing the package does not load the
+library; the first API call does (and fails loudly if it cannot).
+"""
+from .api import (SDM_BF16, SDM_DEV_DUP_WRITE, SDM_DEV_INDEX_RANGE, SDM_F32, SDMError, forward,
+                  gen_inputs, gen_M0, init_state_from_M0, lib, library_path, scan_forward,
+                  scan_launch_info, scan_workspace, scan_workspace_size, select)
+
+__all__ = ["SDM_BF16", "SDM_DEV_DUP_WRITE", "SDM_DEV_INDEX_RANGE", "SDM_F32", "SDMError", "forward",
+           "gen_inputs", "gen_M0", "init_state_from_M0", "lib", "library_path", "scan_forward",
+           "scan_launch_info", "scan_workspace", "scan_workspace_size", "select"]

@@ -1,0 +1,230 @@
+"""Thin Python binding of the SDM C ABI (include/sdm.h) for torch tensors.
+
+Argument marshalling only: every step of the path runs in libsdm.so's CUDA
+kernels.  There is no CPU fallback: if the library is missing and cannot be built,
+or a tensor is not on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+SDM_F32, SDM_BF16 = 0, 1
+SDM_DEV_INDEX_RANGE, SDM_DEV_DUP_WRITE = 1, 2
+SDM_MAX_S, SDM_MAX_K = 4096, 1024
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SDMError(RuntimeError):
+    """A non-zero status returned by the SDM C ABI."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {lib().sdm_status_str(status).decode()} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libsdm.so (built in-tree on first use if absent or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            L = ctypes.CDLL(path)
+            p, i, ll, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_size_t
+            ull, f = ctypes.c_ulonglong, ctypes.c_float
+            L.sdm_status_str.argtypes = [i]
+            L.sdm_status_str.restype = ctypes.c_char_p
+            L.sdm_init_state_from_M0.argtypes = [p, p, i, i, ll, i, p]
+            L.sdm_select.argtypes = [p, p, i, i, i, i, i, i, i, p, p, p, p, p]
+            L.sdm_scan_workspace_size.argtypes = [i, i, i, i, i, i]
+            L.sdm_scan_workspace_size.restype = sz
+            L.sdm_scan_forward.argtypes = [p, p, p, p, p, p, i, p, p, i, i, i, ll, i, i, i, p, p, sz, p, p]
+            L.sdm_scan_forward_tuned.argtypes = [p, p, p, p, p, p, i, p, p, i, i, i, ll, i, i, i, p, p, sz,
+                                                 p, i, i, p, p]
+            L.sdm_scan_launch_info.argtypes = [i, i, i, i, i, p, p, p, p]
+            L.sdm_gen_inputs.argtypes = [ull, i, i, i, i, i, ll, i, i, i, f, i, p, p, p, p, p, p, p]
+            L.sdm_gen_M0.argtypes = [ull, i, ll, i, f, p, p]
+            for name in ("sdm_init_state_from_M0", "sdm_select", "sdm_scan_forward",
+                         "sdm_scan_forward_tuned", "sdm_scan_launch_info", "sdm_gen_inputs", "sdm_gen_M0"):
+                getattr(L, name).restype = i
+            _lib = L
+    return _lib
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def _call(fn: str, *args):
+    st = getattr(lib(), fn)(*args)
+    if st != 0:
+        raise SDMError(fn, st)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SDM_F32
+    if t.dtype == torch.bfloat16:
+        return SDM_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def init_state_from_M0(M: torch.Tensor, M0: torch.Tensor) -> torch.Tensor:
+    """M[b, h] = M0[h] for every b.  M: fp32 [B, H, N, d_v]; M0: fp32 [H, N, d_v]."""
+    _need(M, "M", torch.float32)
+    B, H, N, dv = M.shape
+    _need(M0, "M0", torch.float32, (H, N, dv))
+    _call("sdm_init_state_from_M0", _p(M), _p(M0), B, H, N, dv, _stream(M.device))
+    return M
+
+
+def select(kp: torch.Tensor, qp: torch.Tensor, W: int, R: int, out=None):
+    """Top-W slots of k' and top-R slots of q' for every (b, h, t).
+
+    kp, qp: [B, H, T, 2, S] fp32 or bf16.  Returns (idx_w int32 [B,H,T,W], sc_w fp32,
+    idx_r int32 [B,H,T,R], sc_r fp32), best first."""
+    _need(kp, "kp")
+    B, H, T, two, S = kp.shape
+    if two != 2:
+        raise ValueError("kp must be [B, H, T, 2, S]")
+    _need(qp, "qp", kp.dtype, kp.shape)
+    if out is None:
+        dev = kp.device
+        out = (torch.empty((B, H, T, W), dtype=torch.int32, device=dev),
+               torch.empty((B, H, T, W), dtype=torch.float32, device=dev),
+               torch.empty((B, H, T, R), dtype=torch.int32, device=dev),
+               torch.empty((B, H, T, R), dtype=torch.float32, device=dev))
+    idx_w, sc_w, idx_r, sc_r = out
+    _need(idx_w, "idx_w", torch.int32, (B, H, T, W))
+    _need(sc_w, "sc_w", torch.float32, (B, H, T, W))
+    _need(idx_r, "idx_r", torch.int32, (B, H, T, R))
+    _need(sc_r, "sc_r", torch.float32, (B, H, T, R))
+    _call("sdm_select", _p(kp), _p(qp), _dtype_code(kp), B, H, T, S, W, R, _p(idx_w), _p(sc_w),
+          _p(idx_r), _p(sc_r), _stream(kp.device))
+    return idx_w, sc_w, idx_r, sc_r
+
+
+def scan_workspace_size(B: int, H: int, T: int, d_v: int, W: int, R: int) -> int:
+    return int(lib().sdm_scan_workspace_size(B, H, T, d_v, W, R))
+
+
+def scan_workspace(B, H, T, d_v, W, R, device) -> torch.Tensor:
+    """A device buffer large enough for scan_forward on these sizes."""
+    return torch.empty(max(16, scan_workspace_size(B, H, T, d_v, W, R)), dtype=torch.uint8, device=device)
+
+
+def scan_forward(M, idx_w, sc_w, idx_r, sc_r, v, alpha, beta, o=None, workspace=None,
+                 dev_err=None, cols_per_cta: int = 0, prefetch_depth: int = 0, event_after_plan=None):
+    """Sparse gated-delta scan over T tokens, continuing from the state in M (updated in
+    place).  M: fp32 [B,H,N,d_v]; idx/sc from select; v: [B,H,T,d_v] fp32/bf16;
+    alpha, beta: fp32 [B,H,T].  Returns o fp32 [B,H,T,d_v].  event_after_plan: optional
+    torch.cuda.Event recorded between the planning kernel and the scan kernel."""
+    _need(M, "M", torch.float32)
+    B, H, N, dv = M.shape
+    _need(idx_w, "idx_w", torch.int32)
+    T, W = idx_w.shape[2], idx_w.shape[3]
+    _need(idx_w, "idx_w", torch.int32, (B, H, T, W))
+    _need(sc_w, "sc_w", torch.float32, (B, H, T, W))
+    R = idx_r.shape[3]
+    _need(idx_r, "idx_r", torch.int32, (B, H, T, R))
+    _need(sc_r, "sc_r", torch.float32, (B, H, T, R))
+    _need(v, "v", None, (B, H, T, dv))
+    _need(alpha, "alpha", torch.float32, (B, H, T))
+    _need(beta, "beta", torch.float32, (B, H, T))
+    if o is None:
+        o = torch.empty((B, H, T, dv), dtype=torch.float32, device=M.device)
+    _need(o, "o", torch.float32, (B, H, T, dv))
+    if workspace is None:
+        workspace = scan_workspace(B, H, T, dv, W, R, M.device)
+    _need(workspace, "workspace", torch.uint8)
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32)
+    _call("sdm_scan_forward_tuned", _p(M), _p(idx_w), _p(sc_w), _p(idx_r), _p(sc_r), _p(v),
+          _dtype_code(v), _p(alpha), _p(beta), B, H, T, N, dv, W, R, _p(o), _p(workspace),
+          workspace.numel(), _p(dev_err), int(cols_per_cta), int(prefetch_depth),
+          None if event_after_plan is None else ctypes.c_void_p(event_after_plan.cuda_event),
+          _stream(M.device))
+    return o
+
+
+def scan_launch_info(B: int, H: int, d_v: int, W: int, R: int) -> dict:
+    vals = [ctypes.c_int(0) for _ in range(4)]
+    _call("sdm_scan_launch_info", B, H, d_v, W, R, *[ctypes.byref(x) for x in vals])
+    return dict(cols_per_cta=vals[0].value, prefetch_depth=vals[1].value, blocks=vals[2].value,
+                smem_bytes=vals[3].value)
+
+
+def gen_inputs(seed: int, B: int, H: int, T: int, S: int, d_v: int, in_dtype: torch.dtype,
+               alpha_lo: float, beta_kind: int, half_bias=None, b_off: int = 0, t_off: int = 0,
+               T_total=None, device="cuda", out=None):
+    """Synthetic inputs drawn on the device (bit-identical to the host generator).
+
+    Returns dict(kp, qp [B,H,T,2,S], v [B,H,T,d_v] in_dtype, alpha, beta fp32 [B,H,T])."""
+    T_total = T if T_total is None else T_total
+    if out is None:
+        out = dict(kp=torch.empty((B, H, T, 2, S), dtype=in_dtype, device=device),
+                   qp=torch.empty((B, H, T, 2, S), dtype=in_dtype, device=device),
+                   v=torch.empty((B, H, T, d_v), dtype=in_dtype, device=device),
+                   alpha=torch.empty((B, H, T), dtype=torch.float32, device=device),
+                   beta=torch.empty((B, H, T), dtype=torch.float32, device=device))
+    for k in ("kp", "qp", "v", "alpha", "beta"):
+        if out.get(k) is not None:
+            _need(out[k], k)
+    if half_bias is not None:
+        _need(half_bias, "half_bias", torch.float32, (S,))
+    dev = next(t for t in out.values() if t is not None).device
+    _call("sdm_gen_inputs", ctypes.c_ulonglong(seed), B, H, T, b_off, t_off, T_total, S, d_v,
+          SDM_BF16 if in_dtype == torch.bfloat16 else SDM_F32,
+          ctypes.c_float(alpha_lo), int(beta_kind), _p(half_bias), _p(out.get("kp")), _p(out.get("qp")),
+          _p(out.get("v")), _p(out.get("alpha")), _p(out.get("beta")), _stream(dev))
+    return out
+
+
+def gen_M0(seed: int, H: int, N: int, d_v: int, scale: float = 0.02, device="cuda", out=None):
+    """Synthetic learned initial state M0 = scale * N(0, 1), fp32 [H, N, d_v]."""
+    if out is None:
+        out = torch.empty((H, N, d_v), dtype=torch.float32, device=device)
+    _need(out, "M0", torch.float32, (H, N, d_v))
+    _call("sdm_gen_M0", ctypes.c_ulonglong(seed), H, N, d_v, ctypes.c_float(scale), _p(out),
+          _stream(out.device))
+    return out
+
+
+def forward(kp, qp, v, alpha, beta, M0, W: int, R: int, M=None, workspace=None, dev_err=None):
+    """One SDM forward pass over a batch: state from M0, selection, scan.
+
+    Returns (o, M, (idx_w, sc_w, idx_r, sc_r))."""
+    B, H, T, _, S = kp.shape
+    dv = M0.shape[-1]
+    if M is None:
+        M = torch.empty((B, H, S * S, dv), dtype=torch.float32, device=kp.device)
+    init_state_from_M0(M, M0)
+    sel = select(kp, qp, W, R)
+    o = scan_forward(M, *sel, v, alpha, beta, workspace=workspace, dev_err=dev_err)
+    return o, M, sel

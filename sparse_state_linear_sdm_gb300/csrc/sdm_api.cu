@@ -1,0 +1,137 @@
+// C ABI entry points of the SDM forward hot path: host-side argument checks, then
+// the launchers.  Nothing here allocates device memory or keeps pointers.
+#include "sdm_internal.cuh"
+
+using namespace sdm;
+
+namespace {
+
+bool bad_dtype(int dt) { return dt != SDM_F32 && dt != SDM_BF16; }
+
+int check_scan_args(float* M, const int32_t* idx_w, const float* sc_w, const int32_t* idx_r,
+                    const float* sc_r, const void* v, int v_dt, const float* alpha,
+                    const float* beta, int B, int H, int T, long long N, int d_v, int W, int R,
+                    float* o) {
+  if (B < 1 || H < 1 || T < 0 || N < 1 || d_v < 4 || d_v % 4 || W < 1 || R < 1) return SDM_EINVAL;
+  if (bad_dtype(v_dt) || (long long)W > N || (long long)R > N) return SDM_EINVAL;
+  if (W > SDM_MAX_K || R > SDM_MAX_K || N > 0x7FFFFFFFLL) return SDM_EUNSUPPORTED;
+  if ((long long)B * H > 0x7FFFFFFFLL || (long long)T * (W + R) > 0x7FFFFFFFLL) return SDM_EUNSUPPORTED;
+  if (!aligned16(M)) return SDM_EALIGN;
+  if (T > 0 && (!aligned16(idx_w) || !aligned16(sc_w) || !aligned16(idx_r) || !aligned16(sc_r) ||
+                !aligned16(v) || !aligned16(alpha) || !aligned16(beta) || !aligned16(o)))
+    return SDM_EALIGN;
+  return SDM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sdm_status_str(int status) {
+  switch (status) {
+    case SDM_OK: return "ok";
+    case SDM_EINVAL: return "invalid argument (size or dtype out of range)";
+    case SDM_EALIGN: return "pointer is NULL or not 16-byte aligned";
+    case SDM_ECUDA: return "CUDA launch or query failed";
+    case SDM_ETIMEOUT: return "bounded device wait ran out";
+    case SDM_EBOUNDS: return "device-detected bounds error";
+    case SDM_EUNSUPPORTED: return "sizes beyond this build's limits";
+    case SDM_ENOSPACE: return "workspace smaller than required";
+    default: return "unknown status";
+  }
+}
+
+int sdm_init_state_from_M0(float* M, const float* M0, int B, int H, long long N, int d_v,
+                           void* stream) {
+  if (B < 1 || H < 1 || N < 1 || d_v < 4 || d_v % 4) return SDM_EINVAL;
+  if (!aligned16(M) || !aligned16(M0)) return SDM_EALIGN;
+  return launch_init_state(M, M0, B, H, N, d_v, as_stream(stream));
+}
+
+int sdm_select(const void* kp, const void* qp, int in_dt, int B, int H, int T, int S, int W, int R,
+               int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, void* stream) {
+  if (B < 1 || H < 1 || T < 0 || S < 1 || W < 1 || R < 1 || bad_dtype(in_dt)) return SDM_EINVAL;
+  const long long N = (long long)S * S;
+  if ((long long)W > N || (long long)R > N) return SDM_EINVAL;
+  if (S > SDM_MAX_S || W > SDM_MAX_K || R > SDM_MAX_K) return SDM_EUNSUPPORTED;
+  const long long items = (long long)B * H * T;
+  if (items == 0) return SDM_OK;
+  if (!aligned16(kp) || !aligned16(qp) || !aligned16(idx_w) || !aligned16(sc_w) ||
+      !aligned16(idx_r) || !aligned16(sc_r))
+    return SDM_EALIGN;
+  return launch_select(kp, qp, in_dt, items, S, W, R, idx_w, sc_w, idx_r, sc_r, as_stream(stream));
+}
+
+size_t sdm_scan_workspace_size(int B, int H, int T, int d_v, int W, int R) {
+  if (B < 1 || H < 1 || T < 1 || d_v < 4 || W < 1 || R < 1) return 0;
+  return size_t(B) * size_t(H) * size_t(T) * size_t(rec_layout(W, R, d_v).bytes);
+}
+
+int sdm_scan_forward_tuned(float* M, const int32_t* idx_w, const float* sc_w,
+                           const int32_t* idx_r, const float* sc_r, const void* v, int v_dt,
+                           const float* alpha, const float* beta, int B, int H, int T,
+                           long long N, int d_v, int W, int R, float* o, void* workspace,
+                           size_t workspace_bytes, int* dev_err, int cols_per_cta,
+                           int prefetch_depth, void* event_after_plan, void* stream) {
+  int st = check_scan_args(M, idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, B, H, T, N, d_v, W,
+                           R, o);
+  if (st != SDM_OK) return st;
+  if (cols_per_cta < 0 || prefetch_depth < 0 || prefetch_depth > 3) return SDM_EINVAL;
+  if (T == 0) return SDM_OK;
+  if (!aligned16(workspace)) return SDM_EALIGN;
+  if (workspace_bytes < sdm_scan_workspace_size(B, H, T, d_v, W, R)) return SDM_ENOSPACE;
+  if (dev_err && (reinterpret_cast<uintptr_t>(dev_err) & 3u)) return SDM_EALIGN;
+  ScanShape shape;
+  st = choose_scan_shape(B * H, d_v, W, R, cols_per_cta, prefetch_depth, &shape);
+  if (st != SDM_OK) return st;
+  return launch_scan(M, idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, B * H, T, N, d_v, W, R, o,
+                     workspace, dev_err, shape, reinterpret_cast<cudaEvent_t>(event_after_plan),
+                     as_stream(stream));
+}
+
+int sdm_scan_forward(float* M, const int32_t* idx_w, const float* sc_w, const int32_t* idx_r,
+                     const float* sc_r, const void* v, int v_dt, const float* alpha,
+                     const float* beta, int B, int H, int T, long long N, int d_v, int W, int R,
+                     float* o, void* workspace, size_t workspace_bytes, int* dev_err,
+                     void* stream) {
+  return sdm_scan_forward_tuned(M, idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, B, H, T, N, d_v,
+                                W, R, o, workspace, workspace_bytes, dev_err, 0, 0, nullptr, stream);
+}
+
+int sdm_scan_launch_info(int B, int H, int d_v, int W, int R, int* cols_per_cta,
+                         int* prefetch_depth, int* blocks, int* smem_bytes) {
+  if (B < 1 || H < 1 || d_v < 4 || d_v % 4 || W < 1 || R < 1) return SDM_EINVAL;
+  if (W > SDM_MAX_K || R > SDM_MAX_K) return SDM_EUNSUPPORTED;
+  ScanShape shape;
+  const int st = choose_scan_shape(B * H, d_v, W, R, 0, 0, &shape);
+  if (st != SDM_OK) return st;
+  if (cols_per_cta) *cols_per_cta = shape.cols;
+  if (prefetch_depth) *prefetch_depth = shape.pd;
+  if (blocks) *blocks = shape.blocks;
+  if (smem_bytes) *smem_bytes = shape.smem;
+  return SDM_OK;
+}
+
+int sdm_gen_inputs(unsigned long long seed, int B, int H, int T, int b_off, int t_off,
+                   long long T_total, int S, int d_v, int in_dt, float alpha_lo, int beta_kind,
+                   const float* half_bias, void* kp, void* qp, void* v, float* alpha,
+                   float* beta, void* stream) {
+  if (B < 0 || H < 1 || T < 0 || b_off < 0 || t_off < 0 || S < 1 || d_v < 1 || bad_dtype(in_dt))
+    return SDM_EINVAL;
+  if ((long long)t_off + T > T_total || (beta_kind != 0 && beta_kind != 1)) return SDM_EINVAL;
+  if (!(alpha_lo >= 0.0f && alpha_lo <= 1.0f)) return SDM_EINVAL;
+  const void* ptrs[6] = {kp, qp, v, alpha, beta, half_bias};
+  for (const void* p : ptrs)
+    if (p && (reinterpret_cast<uintptr_t>(p) & 3u)) return SDM_EALIGN;
+  return launch_gen_inputs(seed, B, H, T, b_off, t_off, T_total, S, d_v, in_dt, alpha_lo,
+                           beta_kind, half_bias, kp, qp, v, alpha, beta, as_stream(stream));
+}
+
+int sdm_gen_M0(unsigned long long seed, int H, long long N, int d_v, float scale, float* M0,
+               void* stream) {
+  if (H < 1 || N < 1 || d_v < 1) return SDM_EINVAL;
+  if (!aligned16(M0)) return SDM_EALIGN;
+  return launch_gen_M0(seed, H, N, d_v, scale, M0, as_stream(stream));
+}
+
+}  // extern "C"

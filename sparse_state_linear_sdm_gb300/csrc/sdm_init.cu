@@ -1,0 +1,41 @@
+// State initialisation from the learned initial state (Sparse Delta Memory technical
+// summary, gist.science/it/paper/2607.07386, "Stato Iniziale Appreso": M_0 is a
+// learnable parameter that every sequence starts from).
+// M[b, h] = M0[h]: each 16-byte chunk of M0 is read once and stored B times, so the
+// HBM traffic is exactly |M0| read + |M| written.  Pure bandwidth; grid sized to the
+// SM count.
+#include "sdm_internal.cuh"
+
+namespace sdm {
+namespace {
+
+__global__ void __launch_bounds__(256) init_state_kernel(float4* __restrict__ M,
+                                                         const float4* __restrict__ M0, int B,
+                                                         size_t per_batch4) {
+  const size_t stride = size_t(gridDim.x) * blockDim.x;
+  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < per_batch4; i += stride) {
+    const float4 x = __ldcs(M0 + i);
+    for (int b = 0; b < B; ++b) __stcs(M + size_t(b) * per_batch4 + i, x);
+  }
+}
+
+}  // namespace
+
+int launch_init_state(float* M, const float* M0, int B, int H, long long N, int d_v,
+                      cudaStream_t s) {
+  const size_t per_batch4 = size_t(H) * size_t(N) * size_t(d_v) / 4;
+  if (per_batch4 == 0) return SDM_OK;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SDM_ECUDA;
+  size_t blocks = size_t(sms) * 8;
+  const size_t need = (per_batch4 + 255) / 256;
+  if (blocks > need) blocks = need;
+  init_state_kernel<<<unsigned(blocks), 256, 0, s>>>(reinterpret_cast<float4*>(M),
+                                                     reinterpret_cast<const float4*>(M0), B,
+                                                     per_batch4);
+  return last_launch_status();
+}
+
+}  // namespace sdm

@@ -1,0 +1,78 @@
+// Internal declarations shared by the SDM CUDA translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/sdm.h"
+
+namespace sdm {
+
+inline bool aligned16(const void* p) {
+  return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+inline int last_launch_status() {
+  return cudaGetLastError() == cudaSuccess ? SDM_OK : SDM_ECUDA;
+}
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Per-token record the scan's planning pass writes into the workspace, one per
+// (b, h, t).  Every section starts on a 16-byte boundary so the scan can stage it
+// with 16-byte asynchronous copies:
+//   int32 slot[WRa]     write slots then read slots (W + R entries used)
+//   fp32  weight[WRa]   softmax of the write scores, then of the read scores
+//   int16 src[WRb]      where the row comes from: -1 = the table in HBM,
+//                       -2 = invalid slot (skipped), d*W + p = row p of the write
+//                       set of token t-d (0 <= d <= prefetch depth)
+//   fp32  alpha, beta, pad, pad
+//   fp32  v[d_v]
+struct RecLayout {
+  int WR, WRa, WRb;
+  int off_wts, off_src, off_ab, off_v, bytes;
+};
+
+__host__ __device__ inline RecLayout rec_layout(int W, int R, int d_v) {
+  RecLayout L;
+  L.WR = W + R;
+  L.WRa = (L.WR + 3) & ~3;
+  L.WRb = (L.WR + 7) & ~7;
+  L.off_wts = 4 * L.WRa;
+  L.off_src = 8 * L.WRa;
+  L.off_ab = L.off_src + 2 * L.WRb;
+  L.off_v = L.off_ab + 16;
+  L.bytes = L.off_v + 4 * d_v;
+  return L;
+}
+
+// Launchers (host side; arguments already validated by the entry points).
+int launch_init_state(float* M, const float* M0, int B, int H, long long N, int d_v,
+                      cudaStream_t s);
+int launch_select(const void* kp, const void* qp, int in_dt, long long items, int S, int W, int R,
+                  int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, cudaStream_t s);
+
+struct ScanShape {
+  int cols;      // d_v columns per thread block
+  int pd;        // prefetch depth (tokens)
+  int blocks;
+  int smem;      // dynamic shared memory bytes of the scan kernel
+};
+// Picks (or checks a forced) scan kernel shape.  Returns SDM_OK or SDM_EUNSUPPORTED.
+int choose_scan_shape(int BH, int d_v, int W, int R, int force_cols, int force_pd,
+                      ScanShape* out);
+int launch_scan(float* M, const int32_t* idx_w, const float* sc_w, const int32_t* idx_r,
+                const float* sc_r, const void* v, int v_dt, const float* alpha, const float* beta,
+                int BH, int T, long long N, int d_v, int W, int R, float* o, void* workspace,
+                int* dev_err, const ScanShape& shape, cudaEvent_t after_plan, cudaStream_t s);
+
+int launch_gen_inputs(unsigned long long seed, int B, int H, int T, int b_off, int t_off,
+                      long long T_total, int S, int d_v, int in_dt, float alpha_lo,
+                      int beta_kind, const float* half_bias, void* kp, void* qp, void* v,
+                      float* alpha, float* beta, cudaStream_t s);
+int launch_gen_M0(unsigned long long seed, int H, long long N, int d_v, float scale, float* M0,
+                  cudaStream_t s);
+
+}  // namespace sdm

@@ -1,0 +1,390 @@
+// Product-key slot selection (Sparse Delta Memory technical summary,
+// gist.science/it/paper/2607.07386, "Meccanismo Core" item 2):
+// topk(s1 (+) s2) = topk(topk(s1) (+) topk(s2)) without forming the N slot scores.
+//
+// One warp owns one (b, h, t, k'-or-q') task:
+//   1. each half (S sub-scores) -> its top-k, k = min(K, S), ranked by
+//      (value desc, index asc): warp radix select on a composite integer key
+//      (order-preserving value bits, then S-1-index), then a warp bitonic sort;
+//   2. outer top-K over the k x k grid of fp32 sums, ranked by (sum desc, flat asc)
+//      with flat = i*S + j.  Only the "staircase" (p+1)(q+1) <= K of the two sorted
+//      lists is scanned: every other pair is dominated by at least K pairs in exact
+//      arithmetic.  Because fp32 rounding can merge sums (and the flat tie-break
+//      need not follow the list ranks), the kernel then walks each row past the
+//      staircase while the sum can still reach the K-th key; if any pair there beats
+//      it, the selection is redone over every grid pair that can, so the result is
+//      always exactly the top-K of the full grid.
+// No tensor cores: this is compare/select work on CUDA cores.
+#include <cuda_bf16.h>
+
+#include "sdm_internal.cuh"
+
+namespace sdm {
+namespace {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+// Order-preserving map of an fp32 value to uint32 (larger value -> larger key);
+// -0 maps like +0 so the two tie on value.
+__device__ __forceinline__ uint32_t ord_key(float x) {
+  uint32_t u = __float_as_uint(x);
+  if ((u & 0x7FFFFFFFu) == 0u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float ord_decode(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+template <typename Tin>
+__device__ __forceinline__ float load_score(const Tin* p, long long i);
+template <>
+__device__ __forceinline__ float load_score<float>(const float* p, long long i) {
+  return p[i];
+}
+template <>
+__device__ __forceinline__ float load_score<uint16_t>(const uint16_t* p, long long i) {
+  return __uint_as_float(uint32_t(p[i]) << 16);  // bf16 -> fp32 is exact
+}
+
+// Warp-cooperative radix select.  key_of(i, valid) yields a distinct key for each
+// valid i in [0, n).  Returns tau such that exactly `need` valid keys are >= tau.
+// `bits` (multiple of 8) is the key width; hist is 256 warp-private counters.
+template <class KeyOf>
+__device__ uint64_t radix_threshold(const KeyOf& key_of, int n, int need, int bits,
+                                    uint32_t* hist) {
+  const int lane = threadIdx.x & 31;
+  uint64_t prefix = 0;
+  for (int shift = bits - 8; shift >= 0; shift -= 8) {
+    const uint64_t hi_mask = (shift + 8 >= 64) ? 0ull : (~0ull << (shift + 8));
+    for (int b = lane; b < 256; b += 32) hist[b] = 0u;
+    __syncwarp();
+    for (int i = lane; i < n; i += 32) {
+      bool valid;
+      const uint64_t k = key_of(i, valid);
+      if (valid && (k & hi_mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+    }
+    __syncwarp();
+    // Bins scanned from the top: lane l owns bins 255-8l ... 248-8l.
+    uint32_t c[8];
+    uint32_t s = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      c[k] = hist[255 - 8 * lane - k];
+      s += c[k];
+    }
+    uint32_t incl = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, incl, off);
+      if (lane >= off) incl += y;
+    }
+    const uint32_t excl = incl - s;
+    const bool mine = excl < uint32_t(need) && uint32_t(need) <= incl;
+    const int src = __ffs(__ballot_sync(kFull, mine)) - 1;
+    int digit = 0;
+    uint32_t above = 0, cnt = 0;
+    if (mine) {
+      uint32_t run = excl;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (cnt == 0u && run + c[k] >= uint32_t(need)) {
+          digit = 255 - 8 * lane - k;
+          above = run;
+          cnt = c[k];
+        }
+        run += c[k];
+      }
+    }
+    digit = __shfl_sync(kFull, digit, src);
+    above = __shfl_sync(kFull, above, src);
+    cnt = __shfl_sync(kFull, cnt, src);
+    prefix |= uint64_t(digit) << shift;
+    need -= int(above);
+    __syncwarp();
+    if (cnt == uint32_t(need)) break;  // the whole bucket is in: done
+  }
+  return prefix;
+}
+
+// Writes the valid keys >= tau to out[0..cap), in index order (never past cap).
+// Returns how many keys were >= tau.
+template <class KeyOf>
+__device__ int collect_at_least(const KeyOf& key_of, int n, uint64_t tau, uint64_t* out, int cap) {
+  const int lane = threadIdx.x & 31;
+  int base = 0;
+  for (int i0 = 0; i0 < n; i0 += 32) {
+    const int i = i0 + lane;
+    bool valid = false;
+    uint64_t k = 0;
+    if (i < n) k = key_of(i, valid);
+    const bool sel = valid && k >= tau;
+    const unsigned m = __ballot_sync(kFull, sel);
+    const int pos = base + __popc(m & ((1u << lane) - 1u));
+    if (sel && pos < cap) out[pos] = k;
+    base += __popc(m);
+  }
+  __syncwarp();
+  return base;
+}
+
+// Bitonic sort (descending) of buf[0..count) padded with zero keys to 32*E entries.
+// Element i lives in lane i % 32, register i / 32.
+template <int E>
+__device__ __noinline__ void sort_desc(uint64_t* buf, int count) {
+  const int lane = threadIdx.x & 31;
+  uint64_t v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = e * 32 + lane;
+    v[e] = i < count ? buf[i] : 0ull;
+  }
+  constexpr int n = 32 * E;
+#pragma unroll
+  for (int k = 2; k <= n; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j >= 32) {
+        const int je = j >> 5;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int ep = e ^ je;
+          if (ep > e) {
+            const bool desc = ((e * 32 + lane) & k) == 0;
+            const uint64_t a = v[e], b = v[ep];
+            if (desc ? (a < b) : (a > b)) {
+              v[e] = b;
+              v[ep] = a;
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const uint64_t other = __shfl_xor_sync(kFull, v[e], j);
+          const bool lower = (lane & j) == 0;
+          const bool desc = ((e * 32 + lane) & k) == 0;
+          const bool keep_max = (lower == desc);
+          v[e] = keep_max ? (v[e] > other ? v[e] : other) : (v[e] < other ? v[e] : other);
+        }
+      }
+    }
+  }
+  __syncwarp();
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = e * 32 + lane;
+    if (i < count) buf[i] = v[e];
+  }
+  __syncwarp();
+}
+
+__device__ __noinline__ void sort_desc_any(uint64_t* buf, int count) {
+  if (count <= 32) sort_desc<1>(buf, count);
+  else if (count <= 64) sort_desc<2>(buf, count);
+  else if (count <= 128) sort_desc<4>(buf, count);
+  else if (count <= 256) sort_desc<8>(buf, count);
+  else if (count <= 512) sort_desc<16>(buf, count);
+  else sort_desc<32>(buf, count);
+}
+
+__host__ __device__ inline int imin(int a, int b) { return a < b ? a : b; }
+
+__host__ __device__ inline int stair_count(int K, int kin) {
+  int c = 0;
+  for (int p = 0; p < kin; ++p) c += imin(kin, K / (p + 1));
+  return c;
+}
+
+// Shared memory of one warp: sort buffer, histogram, the two inner lists, one half.
+__host__ __device__ inline size_t select_per_warp_bytes(int kpad, int kin_max, int S) {
+  const size_t b = size_t(kpad) * 8 + 256 * 4 + size_t(kin_max) * 16 + size_t(S) * 4;
+  return (b + 15) / 16 * 16;
+}
+
+struct SelectArgs {
+  const void* kp;
+  const void* qp;
+  long long items;
+  int S, W, R;
+  int kin_max;   // max(min(W,S), min(R,S))
+  int kpad;      // max(W, R) rounded up (sort buffer entries)
+  int cnt_w, cnt_r;
+  int warps;
+  int32_t* idx_w;
+  float* sc_w;
+  int32_t* idx_r;
+  float* sc_r;
+};
+
+// Fills the staircase {(p, q): p, q < kin, (p+1)(q+1) <= K} as p << 16 | q, row by row.
+__device__ void build_stair(uint32_t* st, int K, int kin) {
+  // Row offsets are data independent: thread p computes its own with a short loop.
+  for (int p = threadIdx.x; p < kin; p += blockDim.x) {
+    int off = 0;
+    for (int r = 0; r < p; ++r) off += min(kin, K / (r + 1));
+    const int len = min(kin, K / (p + 1));
+    for (int q = 0; q < len; ++q) st[off + q] = (uint32_t(p) << 16) | uint32_t(q);
+  }
+}
+
+template <typename Tin>
+__global__ void select_kernel(SelectArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint32_t* stair_w = reinterpret_cast<uint32_t*>(smem);
+  uint32_t* stair_r = stair_w + a.cnt_w;
+  unsigned char* wbase = smem + (size_t(a.cnt_w + a.cnt_r) * 4 + 15) / 16 * 16;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = a.S;
+  const size_t per_warp = select_per_warp_bytes(a.kpad, a.kin_max, S);
+  unsigned char* wp = wbase + per_warp * warp;
+  uint64_t* buf = reinterpret_cast<uint64_t*>(wp);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(wp + size_t(a.kpad) * 8);
+  float* aval = reinterpret_cast<float*>(hist + 256);
+  float* bval = aval + a.kin_max;
+  int32_t* aidx = reinterpret_cast<int32_t*>(bval + a.kin_max);
+  int32_t* bidx = aidx + a.kin_max;
+  float* vals = reinterpret_cast<float*>(bidx + a.kin_max);
+
+  build_stair(stair_w, a.W, min(a.W, S));
+  build_stair(stair_r, a.R, min(a.R, S));
+  __syncthreads();
+
+  const long long tasks = a.items * 2;
+  for (long long task = (long long)blockIdx.x * a.warps + warp; task < tasks;
+       task += (long long)gridDim.x * a.warps) {
+    const int which = int(task & 1);
+    const long long item = task >> 1;
+    const int K = which ? a.R : a.W;
+    const int kin = min(K, S);
+    const Tin* halves = static_cast<const Tin*>(which ? a.qp : a.kp) + item * 2 * S;
+
+    // ---- 1. top-kin of each half ------------------------------------------------
+    for (int h = 0; h < 2; ++h) {
+      for (int j = lane; j < S; j += 32) vals[j] = load_score<Tin>(halves, (long long)h * S + j);
+      __syncwarp();
+      // key = value bits (16 for bf16 inputs: their low 16 bits carry no information)
+      // then S-1-index in the low 16 bits, so that key order = (value desc, index asc).
+      constexpr int vbits = sizeof(Tin) == 2 ? 16 : 32;
+      auto key_of = [&](int j, bool& valid) -> uint64_t {
+        valid = true;
+        return (uint64_t(ord_key(vals[j]) >> (32 - vbits)) << 16) | uint64_t(0xFFFFu - uint32_t(j));
+      };
+      uint64_t tau = 0;
+      if (kin < S) tau = radix_threshold(key_of, S, kin, vbits + 16, hist);
+      collect_at_least(key_of, S, tau, buf, a.kpad);
+      sort_desc_any(buf, kin);
+      float* dv = h ? bval : aval;
+      int32_t* di = h ? bidx : aidx;
+      for (int r = lane; r < kin; r += 32) {
+        const int j = min(int(0xFFFFu - uint32_t(buf[r] & 0xFFFFu)), S - 1);
+        dv[r] = vals[j];
+        di[r] = j;
+      }
+      __syncwarp();
+    }
+
+    // ---- 2. top-K of the kin x kin grid of pair sums -------------------------------
+    const uint32_t* st = which ? stair_r : stair_w;
+    const int cnt = which ? a.cnt_r : a.cnt_w;
+    auto pair_key = [&](int p, int q) -> uint64_t {
+      const float s = __fadd_rn(aval[p], bval[q]);
+      const uint32_t flat = uint32_t(aidx[p]) * uint32_t(S) + uint32_t(bidx[q]);
+      return (uint64_t(ord_key(s)) << 32) | uint64_t(0xFFFFFFFFu - flat);
+    };
+    auto stair_key = [&](int c, bool& valid) -> uint64_t {
+      valid = true;
+      const uint32_t pq = st[c];
+      return pair_key(int(pq >> 16), int(pq & 0xFFFFu));
+    };
+    uint64_t tau = 0;
+    if (cnt > K) tau = radix_threshold(stair_key, cnt, K, 64, hist);
+    collect_at_least(stair_key, cnt, tau, buf, a.kpad);
+    sort_desc_any(buf, K);
+    const uint64_t kth = buf[K - 1];
+    const uint32_t kth_sum = uint32_t(kth >> 32);
+    // Pairs right of the staircase that could still beat the K-th key.
+    bool beyond = false;
+    for (int p = lane; p < kin; p += 32) {
+      for (int q = min(kin, K / (p + 1)); q < kin; ++q) {
+        const uint64_t k = pair_key(p, q);
+        if (uint32_t(k >> 32) < kth_sum) break;  // sums only fall along a row
+        if (k > kth) beyond = true;
+      }
+    }
+    if (__any_sync(kFull, beyond)) {
+      // Rare (needs rounding merges or massive ties): redo over every grid pair whose
+      // key reaches the staircase's K-th key; the true top-K is among them.
+      auto grid_key = [&](int i, bool& valid) -> uint64_t {
+        const uint64_t k = pair_key(i / kin, i % kin);
+        valid = k >= kth;
+        return k;
+      };
+      const uint64_t tau2 = radix_threshold(grid_key, kin * kin, K, 64, hist);
+      collect_at_least(grid_key, kin * kin, tau2, buf, a.kpad);
+      sort_desc_any(buf, K);
+    }
+    int32_t* oi = (which ? a.idx_r : a.idx_w) + item * K;
+    float* os = (which ? a.sc_r : a.sc_w) + item * K;
+    for (int r = lane; r < K; r += 32) {
+      const uint64_t k = buf[r];
+      oi[r] = int32_t(0xFFFFFFFFu - uint32_t(k & 0xFFFFFFFFu));
+      os[r] = ord_decode(uint32_t(k >> 32));
+    }
+    __syncwarp();
+  }
+}
+
+}  // namespace
+
+int launch_select(const void* kp, const void* qp, int in_dt, long long items, int S, int W, int R,
+                  int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, cudaStream_t s) {
+  if (items == 0) return SDM_OK;
+  SelectArgs a;
+  a.kp = kp;
+  a.qp = qp;
+  a.items = items;
+  a.S = S;
+  a.W = W;
+  a.R = R;
+  a.kin_max = max(min(W, S), min(R, S));
+  int kmax = max(W, R);
+  a.kpad = 32;
+  while (a.kpad < kmax) a.kpad <<= 1;
+  a.cnt_w = stair_count(W, min(W, S));
+  a.cnt_r = stair_count(R, min(R, S));
+  a.idx_w = idx_w;
+  a.sc_w = sc_w;
+  a.idx_r = idx_r;
+  a.sc_r = sc_r;
+  const size_t stair_bytes = (size_t(a.cnt_w + a.cnt_r) * 4 + 15) / 16 * 16;
+  const size_t per_warp = select_per_warp_bytes(a.kpad, a.kin_max, S);
+  int dev = 0, max_smem = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SDM_ECUDA;
+  int warps = 8;
+  while (warps > 1 && stair_bytes + per_warp * warps > size_t(max_smem)) --warps;
+  if (stair_bytes + per_warp * warps > size_t(max_smem)) return SDM_EUNSUPPORTED;
+  a.warps = warps;
+  const size_t smem = stair_bytes + per_warp * warps;
+  const void* fn = in_dt == SDM_BF16 ? reinterpret_cast<const void*>(&select_kernel<uint16_t>)
+                                     : reinterpret_cast<const void*>(&select_kernel<float>);
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+    return SDM_ECUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, warps * 32, smem) != cudaSuccess)
+    return SDM_ECUDA;
+  const long long tasks = items * 2;
+  long long blocks = (tasks + warps - 1) / warps;
+  const long long cap = (long long)sms * (per_sm > 0 ? per_sm : 1) * 8;
+  if (blocks > cap) blocks = cap;
+  if (in_dt == SDM_BF16)
+    select_kernel<uint16_t><<<unsigned(blocks), warps * 32, smem, s>>>(a);
+  else
+    select_kernel<float><<<unsigned(blocks), warps * 32, smem, s>>>(a);
+  return last_launch_status();
+}
+
+}  // namespace sdm

@@ -1,0 +1,117 @@
+"""C ABI checks that need no GPU: the library builds and loads, exports every
+function include/sdm.h declares, and rejects bad arguments on the host before
+launching anything."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import sparse_state_linear_sdm_gb300 as sdm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sdm.h")
+
+EINVAL, EALIGN, EUNSUPPORTED, ENOSPACE = -1, -2, -6, -7
+
+
+def declared_functions():
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\**\s+\**(sdm_[A-Za-z_0-9]+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("sdm_init_state_from_M0", "sdm_select", "sdm_scan_forward", "sdm_scan_workspace_size",
+              "sdm_status_str"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = sdm.lib()
+    out = subprocess.run(["nm", "-D", "--defined-only", sdm.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(sdm_\w+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_status_strings():
+    lib = sdm.lib()
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
+        assert lib.sdm_status_str(code)
+    assert lib.sdm_status_str(-6) == b"sizes beyond this build's limits"
+
+
+FAKE = ctypes.c_void_p(0x10000)      # 16-byte aligned, never dereferenced on these paths
+ODD = ctypes.c_void_p(0x10004)
+
+
+def test_select_rejects_bad_arguments_without_launching():
+    lib = sdm.lib()
+    args = lambda **kw: dict(dict(kp=FAKE, qp=FAKE, dt=1, B=1, H=1, T=4, S=8, W=4, R=4), **kw)
+
+    def call(a, ptrs=(FAKE, FAKE, FAKE, FAKE)):
+        return lib.sdm_select(a["kp"], a["qp"], a["dt"], a["B"], a["H"], a["T"], a["S"], a["W"], a["R"],
+                              *ptrs, None)
+
+    assert call(args(S=0)) == EINVAL
+    assert call(args(W=0)) == EINVAL
+    assert call(args(W=65)) == EINVAL           # W > N = 64
+    assert call(args(dt=7)) == EINVAL
+    assert call(args(B=0)) == EINVAL
+    assert call(args(S=5000, W=4)) == EUNSUPPORTED
+    assert call(args(S=64, W=2000)) == EUNSUPPORTED
+    assert call(args(kp=ODD)) == EALIGN
+    assert call(args(), ptrs=(FAKE, ODD, FAKE, FAKE)) == EALIGN
+    assert call(args(T=0)) == 0                 # nothing to do
+
+
+def test_scan_rejects_bad_arguments_without_launching():
+    lib = sdm.lib()
+
+    def call(B=1, H=1, T=8, N=64, dv=16, W=4, R=4, v_dt=0, M=FAKE, ws=FAKE, ws_bytes=1 << 30, cols=0, pd=0):
+        return lib.sdm_scan_forward_tuned(M, FAKE, FAKE, FAKE, FAKE, FAKE, v_dt, FAKE, FAKE, B, H, T, N, dv, W,
+                                          R, FAKE, ws, ws_bytes, None, cols, pd, None, None)
+
+    assert call(dv=6) == EINVAL
+    assert call(dv=0) == EINVAL
+    assert call(W=65) == EINVAL
+    assert call(R=0) == EINVAL
+    assert call(v_dt=3) == EINVAL
+    assert call(pd=4) == EINVAL
+    assert call(W=1025, N=1 << 20) == EUNSUPPORTED
+    assert call(M=ODD) == EALIGN
+    assert call(ws=ODD) == EALIGN
+    assert call(ws_bytes=10) == ENOSPACE
+    assert call(T=0) == 0
+
+
+def test_workspace_size_formula():
+    lib = sdm.lib()
+    # record = slots (W+R int32) + weights (W+R fp32) + sources (W+R int16) + 16 B gates + d_v fp32
+    assert lib.sdm_scan_workspace_size(16, 4, 8192, 128, 128, 128) == 16 * 4 * 8192 * (1024 + 1024 + 512 + 16 + 512)
+    assert lib.sdm_scan_workspace_size(1, 1, 64, 16, 8, 8) == 64 * (64 + 64 + 32 + 16 + 64)
+    # W + R = 7 pads to 8 int32/fp32 and 8 int16
+    assert lib.sdm_scan_workspace_size(1, 1, 1, 4, 3, 4) == 32 + 32 + 16 + 16 + 16
+    assert lib.sdm_scan_workspace_size(1, 1, 0, 16, 8, 8) == 0
+
+
+def test_init_and_gen_reject_bad_arguments():
+    lib = sdm.lib()
+    assert lib.sdm_init_state_from_M0(FAKE, FAKE, 1, 1, 16, 6, None) == EINVAL
+    assert lib.sdm_init_state_from_M0(ODD, FAKE, 1, 1, 16, 8, None) == EALIGN
+    assert lib.sdm_gen_inputs(0, 1, 1, 4, 0, 2, 5, 8, 8, 1, ctypes.c_float(0.9), 1, None, None, None, None,
+                              None, None, None) == EINVAL   # t_off + T > T_total
+    assert lib.sdm_gen_M0(0, 1, 16, 4, ctypes.c_float(0.02), ODD, None) == EALIGN
+
+
+def test_api_requires_cuda_tensors():
+    import torch
+    x = torch.zeros(1, 1, 4, 2, 8)
+    with pytest.raises(TypeError):
+        sdm.select(x, x, 4, 4)
