@@ -47,7 +47,21 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cols", type=int, default=0, help="force scan columns per block (0 = auto)")
     ap.add_argument("--pd", type=int, default=0, help="force scan prefetch depth (0 = auto)")
+    ap.add_argument("--override", default="", help="size overrides for profiling, e.g. S=256,T=512")
     return ap.parse_args()
+
+
+def workload(args):
+    import dataclasses
+
+    from sparse_state_linear_sdm_gb300 import workloads as wl
+
+    cfg = wl.CONFIGS[args.config]
+    if args.override:
+        kv = dict(item.split("=") for item in args.override.split(","))
+        cfg = dataclasses.replace(cfg, name=cfg.name + f" (sizes overridden: {args.override})",
+                                  **{k: int(v) for k, v in kv.items()})
+    return cfg
 
 
 def dist_env():
@@ -215,7 +229,7 @@ def run_reference(args):
     import oracle
     from sparse_state_linear_sdm_gb300 import workloads as wl
 
-    cfg = wl.CONFIGS[args.config]
+    cfg = workload(args)
     oracle.build()
     tokens = min(cfg.T, 2048)
     base, times, units = cpu_baseline(cfg, wl, oracle, steps=args.warmup + args.steps, tokens=tokens)
@@ -250,7 +264,7 @@ def run_ours(args):
         dist.init_process_group("nccl", init_method="env://")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    cfg = wl.CONFIGS[args.config]
+    cfg = workload(args)
     st = make_state(cfg, rank, dev, torch, sdm, wl)
     torch.cuda.synchronize(dev)
 

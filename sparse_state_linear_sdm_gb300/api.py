@@ -165,6 +165,8 @@ def scan_forward(M, idx_w, sc_w, idx_r, sc_r, v, alpha, beta, o=None, workspace=
     _need(workspace, "workspace", torch.uint8)
     if dev_err is not None:
         _need(dev_err, "dev_err", torch.int32)
+    if event_after_plan is not None and event_after_plan.cuda_event == 0:
+        event_after_plan.record()  # torch creates its events lazily; the library records it again
     _call("sdm_scan_forward_tuned", _p(M), _p(idx_w), _p(sc_w), _p(idx_r), _p(sc_r), _p(v),
           _dtype_code(v), _p(alpha), _p(beta), B, H, T, N, dv, W, R, _p(o), _p(workspace),
           workspace.numel(), _p(dev_err), int(cols_per_cta), int(prefetch_depth),

@@ -36,17 +36,6 @@ __device__ __forceinline__ float ord_decode(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-template <typename Tin>
-__device__ __forceinline__ float load_score(const Tin* p, long long i);
-template <>
-__device__ __forceinline__ float load_score<float>(const float* p, long long i) {
-  return p[i];
-}
-template <>
-__device__ __forceinline__ float load_score<uint16_t>(const uint16_t* p, long long i) {
-  return __uint_as_float(uint32_t(p[i]) << 16);  // bf16 -> fp32 is exact
-}
-
 // Warp-cooperative radix select.  key_of(i, valid) yields a distinct key for each
 // valid i in [0, n).  Returns tau such that exactly `need` valid keys are >= tau.
 // `bits` (multiple of 8) is the key width; hist is 256 warp-private counters.
@@ -128,16 +117,114 @@ __device__ int collect_at_least(const KeyOf& key_of, int n, uint64_t tau, uint64
   return base;
 }
 
+// Selects the `need` largest of the n distinct keys in buf[0..n) and writes them,
+// unordered, to out[0..need).  buf is scratch: each radix pass keeps only the keys of
+// the bucket that holds the need-th largest, compacted in place, so only the first
+// pass touches all n keys.  Passes start at the highest bit where the keys differ.
+template <typename Key>
+__device__ void warp_topk(Key* buf, int n, int need, Key* out, uint32_t* hist) {
+  const int lane = threadIdx.x & 31;
+  if (need >= n) {
+    for (int i = lane; i < n; i += 32) out[i] = buf[i];
+    __syncwarp();
+    return;
+  }
+  Key mx = 0, mn = ~Key(0);
+  for (int i = lane; i < n; i += 32) {
+    const Key k = buf[i];
+    mx = k > mx ? k : mx;
+    mn = k < mn ? k : mn;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const Key a = __shfl_xor_sync(kFull, mx, off), b = __shfl_xor_sync(kFull, mn, off);
+    mx = a > mx ? a : mx;
+    mn = b < mn ? b : mn;
+  }
+  const Key diff = mx ^ mn;  // n >= 2 distinct keys: non-zero
+  const int top = int(sizeof(Key) * 8) - 1 -
+                  (sizeof(Key) == 8 ? __clzll((long long)diff) : __clz(int(uint32_t(diff))));
+  int shift = (top / 8) * 8;
+  int n_out = 0;
+  for (;;) {
+    for (int b = lane; b < 256; b += 32) hist[b] = 0u;
+    __syncwarp();
+    for (int i = lane; i < n; i += 32) atomicAdd(&hist[unsigned(buf[i] >> shift) & 255u], 1u);
+    __syncwarp();
+    uint32_t c[8];
+    uint32_t s = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      c[k] = hist[255 - 8 * lane - k];
+      s += c[k];
+    }
+    uint32_t incl = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, incl, off);
+      if (lane >= off) incl += y;
+    }
+    const uint32_t excl = incl - s;
+    const bool mine = excl < uint32_t(need) && uint32_t(need) <= incl;
+    const int src = __ffs(__ballot_sync(kFull, mine)) - 1;
+    int digit = 0;
+    uint32_t above = 0, cnt = 0;
+    if (mine) {
+      uint32_t run = excl;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (cnt == 0u && run + c[k] >= uint32_t(need)) {
+          digit = 255 - 8 * lane - k;
+          above = run;
+          cnt = c[k];
+        }
+        run += c[k];
+      }
+    }
+    digit = __shfl_sync(kFull, digit, src);
+    above = __shfl_sync(kFull, above, src);
+    cnt = __shfl_sync(kFull, cnt, src);
+    // Keys above the bucket are final; the bucket is compacted to the front of buf.
+    int base_up = n_out, base_eq = 0;
+    for (int i0 = 0; i0 < n; i0 += 32) {
+      const int i = i0 + lane;
+      Key k = 0;
+      unsigned dg = 0;
+      if (i < n) {
+        k = buf[i];
+        dg = unsigned(k >> shift) & 255u;
+      }
+      const bool up = i < n && int(dg) > digit, eq = i < n && int(dg) == digit;
+      const unsigned mu = __ballot_sync(kFull, up), me = __ballot_sync(kFull, eq);
+      const unsigned lt = (1u << lane) - 1u;
+      if (up) out[base_up + __popc(mu & lt)] = k;
+      if (eq) buf[base_eq + __popc(me & lt)] = k;  // positions <= i: already read
+      base_up += __popc(mu);
+      base_eq += __popc(me);
+      __syncwarp();
+    }
+    n_out += int(above);
+    need -= int(above);
+    n = int(cnt);
+    if (n == need) {
+      for (int i = lane; i < n; i += 32) out[n_out + i] = buf[i];
+      __syncwarp();
+      return;
+    }
+    shift -= 8;  // >= 2 distinct keys share the digit, so a lower digit separates them
+  }
+}
+
 // Bitonic sort (descending) of buf[0..count) padded with zero keys to 32*E entries.
 // Element i lives in lane i % 32, register i / 32.
-template <int E>
-__device__ __noinline__ void sort_desc(uint64_t* buf, int count) {
+template <typename Key, int E>
+__device__ __noinline__ void sort_desc(Key* buf, int count) {
   const int lane = threadIdx.x & 31;
-  uint64_t v[E];
+  Key v[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int i = e * 32 + lane;
-    v[e] = i < count ? buf[i] : 0ull;
+    v[e] = i < count ? buf[i] : Key(0);
   }
   constexpr int n = 32 * E;
 #pragma unroll
@@ -151,7 +238,7 @@ __device__ __noinline__ void sort_desc(uint64_t* buf, int count) {
           const int ep = e ^ je;
           if (ep > e) {
             const bool desc = ((e * 32 + lane) & k) == 0;
-            const uint64_t a = v[e], b = v[ep];
+            const Key a = v[e], b = v[ep];
             if (desc ? (a < b) : (a > b)) {
               v[e] = b;
               v[ep] = a;
@@ -161,7 +248,7 @@ __device__ __noinline__ void sort_desc(uint64_t* buf, int count) {
       } else {
 #pragma unroll
         for (int e = 0; e < E; ++e) {
-          const uint64_t other = __shfl_xor_sync(kFull, v[e], j);
+          const Key other = __shfl_xor_sync(kFull, v[e], j);
           const bool lower = (lane & j) == 0;
           const bool desc = ((e * 32 + lane) & k) == 0;
           const bool keep_max = (lower == desc);
@@ -179,13 +266,14 @@ __device__ __noinline__ void sort_desc(uint64_t* buf, int count) {
   __syncwarp();
 }
 
-__device__ __noinline__ void sort_desc_any(uint64_t* buf, int count) {
-  if (count <= 32) sort_desc<1>(buf, count);
-  else if (count <= 64) sort_desc<2>(buf, count);
-  else if (count <= 128) sort_desc<4>(buf, count);
-  else if (count <= 256) sort_desc<8>(buf, count);
-  else if (count <= 512) sort_desc<16>(buf, count);
-  else sort_desc<32>(buf, count);
+template <typename Key, int EMAX>
+__device__ void sort_desc_upto(Key* buf, int count) {
+  if (count <= 32) sort_desc<Key, 1>(buf, count);
+  else if (count <= 64 || EMAX < 4) sort_desc<Key, (EMAX < 2 ? EMAX : 2)>(buf, count);
+  else if (count <= 128 || EMAX < 8) sort_desc<Key, (EMAX < 4 ? EMAX : 4)>(buf, count);
+  else if (count <= 256 || EMAX < 16) sort_desc<Key, (EMAX < 8 ? EMAX : 8)>(buf, count);
+  else if (count <= 512 || EMAX < 32) sort_desc<Key, (EMAX < 16 ? EMAX : 16)>(buf, count);
+  else sort_desc<Key, EMAX>(buf, count);
 }
 
 __host__ __device__ inline int imin(int a, int b) { return a < b ? a : b; }
@@ -196,9 +284,42 @@ __host__ __device__ inline int stair_count(int K, int kin) {
   return c;
 }
 
-// Shared memory of one warp: sort buffer, histogram, the two inner lists, one half.
-__host__ __device__ inline size_t select_per_warp_bytes(int kpad, int kin_max, int S) {
-  const size_t b = size_t(kpad) * 8 + 256 * 4 + size_t(kin_max) * 16 + size_t(S) * 4;
+// bf16 halves use 32-bit keys (16 value bits, 16 index bits); fp32 halves 64-bit ones.
+template <typename Tin>
+struct InnerKeyOf {
+  using type = uint64_t;
+};
+template <>
+struct InnerKeyOf<uint16_t> {
+  using type = uint32_t;
+};
+
+__device__ __forceinline__ uint32_t inner_key(uint16_t u, int j) {
+  uint32_t b = u;
+  if ((b & 0x7FFFu) == 0u) b = 0u;  // -0 ranks as +0
+  const uint32_t o = (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+  return (o << 16) | (0xFFFFu - uint32_t(j));
+}
+__device__ __forceinline__ uint64_t inner_key(float x, int j) {
+  return (uint64_t(ord_key(x)) << 16) | uint64_t(0xFFFFu - uint32_t(j));
+}
+__device__ __forceinline__ float inner_value(uint32_t key) {
+  const uint32_t o = key >> 16;
+  const uint32_t b = (o & 0x8000u) ? (o & 0x7FFFu) : (~o & 0xFFFFu);
+  return __uint_as_float(b << 16);
+}
+__device__ __forceinline__ float inner_value(uint64_t key) {
+  return ord_decode(uint32_t(key >> 16));
+}
+
+// Shared memory of one warp: key buffer (one half, or the staircase candidates), the
+// selected keys, the histogram and the two inner lists.
+__host__ __device__ inline size_t select_per_warp_bytes(int kpad, int kin_max, int S, int cnt_max,
+                                                        int inner_key_bytes) {
+  size_t keys = size_t(S) * inner_key_bytes;
+  if (size_t(cnt_max) * 8 > keys) keys = size_t(cnt_max) * 8;
+  keys = (keys + 15) / 16 * 16;
+  const size_t b = keys + size_t(kpad) * 8 + 256 * 4 + size_t(kin_max) * 16;
   return (b + 15) / 16 * 16;
 }
 
@@ -208,9 +329,10 @@ struct SelectArgs {
   long long items;
   int S, W, R;
   int kin_max;   // max(min(W,S), min(R,S))
-  int kpad;      // max(W, R) rounded up (sort buffer entries)
+  int kpad;      // max(W, R, 32) rounded up to a power of two (selected-key buffer)
   int cnt_w, cnt_r;
   int warps;
+  size_t keys_bytes;  // per-warp key buffer
   int32_t* idx_w;
   float* sc_w;
   int32_t* idx_r;
@@ -228,23 +350,24 @@ __device__ void build_stair(uint32_t* st, int K, int kin) {
   }
 }
 
-template <typename Tin>
-__global__ void select_kernel(SelectArgs a) {
+template <typename Tin, int EMAX>
+__global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
+  using IKey = typename InnerKeyOf<Tin>::type;
   extern __shared__ __align__(16) unsigned char smem[];
   uint32_t* stair_w = reinterpret_cast<uint32_t*>(smem);
   uint32_t* stair_r = stair_w + a.cnt_w;
   unsigned char* wbase = smem + (size_t(a.cnt_w + a.cnt_r) * 4 + 15) / 16 * 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = a.S;
-  const size_t per_warp = select_per_warp_bytes(a.kpad, a.kin_max, S);
-  unsigned char* wp = wbase + per_warp * warp;
-  uint64_t* buf = reinterpret_cast<uint64_t*>(wp);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(wp + size_t(a.kpad) * 8);
+  const size_t per_warp = a.keys_bytes + size_t(a.kpad) * 8 + 256 * 4 + size_t(a.kin_max) * 16;
+  unsigned char* wp = wbase + (per_warp + 15) / 16 * 16 * warp;
+  unsigned char* keys = wp;
+  uint64_t* out = reinterpret_cast<uint64_t*>(wp + a.keys_bytes);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(out + a.kpad);
   float* aval = reinterpret_cast<float*>(hist + 256);
   float* bval = aval + a.kin_max;
   int32_t* aidx = reinterpret_cast<int32_t*>(bval + a.kin_max);
   int32_t* bidx = aidx + a.kin_max;
-  float* vals = reinterpret_cast<float*>(bidx + a.kin_max);
 
   build_stair(stair_w, a.W, min(a.W, S));
   build_stair(stair_r, a.R, min(a.R, S));
@@ -259,27 +382,21 @@ __global__ void select_kernel(SelectArgs a) {
     const int kin = min(K, S);
     const Tin* halves = static_cast<const Tin*>(which ? a.qp : a.kp) + item * 2 * S;
 
-    // ---- 1. top-kin of each half ------------------------------------------------
+    // ---- 1. top-kin of each half, ranked by (value desc, index asc) ---------------
     for (int h = 0; h < 2; ++h) {
-      for (int j = lane; j < S; j += 32) vals[j] = load_score<Tin>(halves, (long long)h * S + j);
+      IKey* ik = reinterpret_cast<IKey*>(keys);
+      const Tin* src = halves + (long long)h * S;
+      for (int j = lane; j < S; j += 32) ik[j] = inner_key(src[j], j);
       __syncwarp();
-      // key = value bits (16 for bf16 inputs: their low 16 bits carry no information)
-      // then S-1-index in the low 16 bits, so that key order = (value desc, index asc).
-      constexpr int vbits = sizeof(Tin) == 2 ? 16 : 32;
-      auto key_of = [&](int j, bool& valid) -> uint64_t {
-        valid = true;
-        return (uint64_t(ord_key(vals[j]) >> (32 - vbits)) << 16) | uint64_t(0xFFFFu - uint32_t(j));
-      };
-      uint64_t tau = 0;
-      if (kin < S) tau = radix_threshold(key_of, S, kin, vbits + 16, hist);
-      collect_at_least(key_of, S, tau, buf, a.kpad);
-      sort_desc_any(buf, kin);
+      IKey* io = reinterpret_cast<IKey*>(out);
+      warp_topk<IKey>(ik, S, kin, io, hist);
+      sort_desc_upto<IKey, EMAX>(io, kin);
       float* dv = h ? bval : aval;
       int32_t* di = h ? bidx : aidx;
       for (int r = lane; r < kin; r += 32) {
-        const int j = min(int(0xFFFFu - uint32_t(buf[r] & 0xFFFFu)), S - 1);
-        dv[r] = vals[j];
-        di[r] = j;
+        const IKey k = io[r];
+        dv[r] = inner_value(k);
+        di[r] = min(int(0xFFFFu - uint32_t(k & 0xFFFFu)), S - 1);
       }
       __syncwarp();
     }
@@ -292,16 +409,15 @@ __global__ void select_kernel(SelectArgs a) {
       const uint32_t flat = uint32_t(aidx[p]) * uint32_t(S) + uint32_t(bidx[q]);
       return (uint64_t(ord_key(s)) << 32) | uint64_t(0xFFFFFFFFu - flat);
     };
-    auto stair_key = [&](int c, bool& valid) -> uint64_t {
-      valid = true;
+    uint64_t* ck = reinterpret_cast<uint64_t*>(keys);
+    for (int c = lane; c < cnt; c += 32) {
       const uint32_t pq = st[c];
-      return pair_key(int(pq >> 16), int(pq & 0xFFFFu));
-    };
-    uint64_t tau = 0;
-    if (cnt > K) tau = radix_threshold(stair_key, cnt, K, 64, hist);
-    collect_at_least(stair_key, cnt, tau, buf, a.kpad);
-    sort_desc_any(buf, K);
-    const uint64_t kth = buf[K - 1];
+      ck[c] = pair_key(int(pq >> 16), int(pq & 0xFFFFu));
+    }
+    __syncwarp();
+    warp_topk<uint64_t>(ck, cnt, K, out, hist);
+    sort_desc_upto<uint64_t, EMAX>(out, K);
+    const uint64_t kth = out[K - 1];
     const uint32_t kth_sum = uint32_t(kth >> 32);
     // Pairs right of the staircase that could still beat the K-th key.
     bool beyond = false;
@@ -321,13 +437,13 @@ __global__ void select_kernel(SelectArgs a) {
         return k;
       };
       const uint64_t tau2 = radix_threshold(grid_key, kin * kin, K, 64, hist);
-      collect_at_least(grid_key, kin * kin, tau2, buf, a.kpad);
-      sort_desc_any(buf, K);
+      collect_at_least(grid_key, kin * kin, tau2, out, a.kpad);
+      sort_desc_upto<uint64_t, EMAX>(out, K);
     }
     int32_t* oi = (which ? a.idx_r : a.idx_w) + item * K;
     float* os = (which ? a.sc_r : a.sc_w) + item * K;
     for (int r = lane; r < K; r += 32) {
-      const uint64_t k = buf[r];
+      const uint64_t k = out[r];
       oi[r] = int32_t(0xFFFFFFFFu - uint32_t(k & 0xFFFFFFFFu));
       os[r] = ord_decode(uint32_t(k >> 32));
     }
@@ -348,7 +464,7 @@ int launch_select(const void* kp, const void* qp, int in_dt, long long items, in
   a.W = W;
   a.R = R;
   a.kin_max = max(min(W, S), min(R, S));
-  int kmax = max(W, R);
+  const int kmax = max(W, R);
   a.kpad = 32;
   while (a.kpad < kmax) a.kpad <<= 1;
   a.cnt_w = stair_count(W, min(W, S));
@@ -357,20 +473,30 @@ int launch_select(const void* kp, const void* qp, int in_dt, long long items, in
   a.sc_w = sc_w;
   a.idx_r = idx_r;
   a.sc_r = sc_r;
+  const int ikb = in_dt == SDM_BF16 ? 4 : 8;
+  size_t keys = size_t(S) * ikb;
+  if (size_t(max(a.cnt_w, a.cnt_r)) * 8 > keys) keys = size_t(max(a.cnt_w, a.cnt_r)) * 8;
+  a.keys_bytes = (keys + 15) / 16 * 16;
   const size_t stair_bytes = (size_t(a.cnt_w + a.cnt_r) * 4 + 15) / 16 * 16;
-  const size_t per_warp = select_per_warp_bytes(a.kpad, a.kin_max, S);
+  const size_t per_warp = select_per_warp_bytes(a.kpad, a.kin_max, S, max(a.cnt_w, a.cnt_r), ikb);
   int dev = 0, max_smem = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return SDM_ECUDA;
-  int warps = 8;
+  int warps = 4;
   while (warps > 1 && stair_bytes + per_warp * warps > size_t(max_smem)) --warps;
   if (stair_bytes + per_warp * warps > size_t(max_smem)) return SDM_EUNSUPPORTED;
   a.warps = warps;
   const size_t smem = stair_bytes + per_warp * warps;
-  const void* fn = in_dt == SDM_BF16 ? reinterpret_cast<const void*>(&select_kernel<uint16_t>)
-                                     : reinterpret_cast<const void*>(&select_kernel<float>);
+  const bool small = kmax <= 128;
+  const void* fn;
+  if (in_dt == SDM_BF16)
+    fn = small ? reinterpret_cast<const void*>(&select_kernel<uint16_t, 4>)
+               : reinterpret_cast<const void*>(&select_kernel<uint16_t, 32>);
+  else
+    fn = small ? reinterpret_cast<const void*>(&select_kernel<float, 4>)
+               : reinterpret_cast<const void*>(&select_kernel<float, 32>);
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
     return SDM_ECUDA;
   int per_sm = 0;
@@ -378,12 +504,11 @@ int launch_select(const void* kp, const void* qp, int in_dt, long long items, in
     return SDM_ECUDA;
   const long long tasks = items * 2;
   long long blocks = (tasks + warps - 1) / warps;
-  const long long cap = (long long)sms * (per_sm > 0 ? per_sm : 1) * 8;
+  const long long cap = (long long)sms * (per_sm > 0 ? per_sm : 1);
   if (blocks > cap) blocks = cap;
-  if (in_dt == SDM_BF16)
-    select_kernel<uint16_t><<<unsigned(blocks), warps * 32, smem, s>>>(a);
-  else
-    select_kernel<float><<<unsigned(blocks), warps * 32, smem, s>>>(a);
+  void* args[] = {&a};
+  if (cudaLaunchKernel(fn, dim3(unsigned(blocks)), dim3(warps * 32), args, smem, s) != cudaSuccess)
+    return SDM_ECUDA;
   return last_launch_status();
 }
 

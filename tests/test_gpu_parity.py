@@ -44,8 +44,8 @@ def test_device_generator_matches_host(ci):
         for k in ("kp", "qp", "v", "alpha", "beta"):
             assert np.array_equal(to_np(d[k][b, h]), host[k][0, 0]), (ci, k, b, h)
     M0 = device_M0(cfg)
-    h = cfg.H - 1
-    assert np.array_equal(M0[h, :4096].cpu().numpy(), wl.initial_state(cfg, h, h + 1, 0, 4096)[0])
+    h, n = cfg.H - 1, min(cfg.N, 4096)
+    assert np.array_equal(M0[h, :n].cpu().numpy(), wl.initial_state(cfg, h, h + 1, 0, n)[0])
 
 
 @pytest.mark.parametrize("ci", [0, 1, 2, 3])
