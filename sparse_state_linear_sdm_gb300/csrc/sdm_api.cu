@@ -59,7 +59,9 @@ int sdm_select(const void* kp, const void* qp, int in_dt, int B, int H, int T, i
   if (!aligned16(kp) || !aligned16(qp) || !aligned16(idx_w) || !aligned16(sc_w) ||
       !aligned16(idx_r) || !aligned16(sc_r))
     return SDM_EALIGN;
-  return launch_select(kp, qp, in_dt, items, S, W, R, idx_w, sc_w, idx_r, sc_r, as_stream(stream));
+  return in_dt == SDM_BF16
+             ? launch_select_bf16(kp, qp, items, S, W, R, idx_w, sc_w, idx_r, sc_r, as_stream(stream))
+             : launch_select_f32(kp, qp, items, S, W, R, idx_w, sc_w, idx_r, sc_r, as_stream(stream));
 }
 
 size_t sdm_scan_workspace_size(int B, int H, int T, int d_v, int W, int R) {

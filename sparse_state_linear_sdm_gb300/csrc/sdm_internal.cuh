@@ -51,8 +51,10 @@ __host__ __device__ inline RecLayout rec_layout(int W, int R, int d_v) {
 // Launchers (host side; arguments already validated by the entry points).
 int launch_init_state(float* M, const float* M0, int B, int H, long long N, int d_v,
                       cudaStream_t s);
-int launch_select(const void* kp, const void* qp, int in_dt, long long items, int S, int W, int R,
-                  int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, cudaStream_t s);
+int launch_select_bf16(const void* kp, const void* qp, long long items, int S, int W, int R,
+                       int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, cudaStream_t s);
+int launch_select_f32(const void* kp, const void* qp, long long items, int S, int W, int R,
+                      int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, cudaStream_t s);
 
 struct ScanShape {
   int cols;      // d_v columns per thread block

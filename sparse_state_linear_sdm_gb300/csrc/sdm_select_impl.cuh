@@ -15,7 +15,7 @@
 //      it, the selection is redone over every grid pair that can, so the result is
 //      always exactly the top-K of the full grid.
 // No tensor cores: this is compare/select work on CUDA cores.
-#include <cuda_bf16.h>
+#pragma once
 
 #include "sdm_internal.cuh"
 
@@ -117,73 +117,101 @@ __device__ int collect_at_least(const KeyOf& key_of, int n, uint64_t tau, uint64
   return base;
 }
 
-// Selects the `need` largest of the n distinct keys in buf[0..n) and writes them,
-// unordered, to out[0..need).  buf is scratch: each radix pass keeps only the keys of
-// the bucket that holds the need-th largest, compacted in place, so only the first
-// pass touches all n keys.  Passes start at the highest bit where the keys differ.
-template <typename Key>
-__device__ void warp_topk(Key* buf, int n, int need, Key* out, uint32_t* hist) {
+// Bucket search over a 256-bin digit histogram, from the top: the digit d with
+// above < need <= above + cnt, where above counts digits > d and cnt = hist[d].
+__device__ __forceinline__ void find_bucket(const uint32_t* hist, int need, int& digit,
+                                            uint32_t& above, uint32_t& cnt) {
   const int lane = threadIdx.x & 31;
-  if (need >= n) {
-    for (int i = lane; i < n; i += 32) out[i] = buf[i];
-    __syncwarp();
-    return;
+  uint32_t c[8];
+  uint32_t s = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    c[k] = hist[255 - 8 * lane - k];  // lane l owns bins 255-8l ... 248-8l
+    s += c[k];
   }
-  Key mx = 0, mn = ~Key(0);
-  for (int i = lane; i < n; i += 32) {
-    const Key k = buf[i];
-    mx = k > mx ? k : mx;
-    mn = k < mn ? k : mn;
+  uint32_t incl = s;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, off);
+    if (lane >= off) incl += y;
   }
+  const uint32_t excl = incl - s;
+  const bool mine = excl < uint32_t(need) && uint32_t(need) <= incl;
+  const int src = __ffs(__ballot_sync(kFull, mine)) - 1;
+  int d = 0;
+  uint32_t ab = 0, ct = 0;
+  if (mine) {
+    uint32_t run = excl;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (ct == 0u && run + c[k] >= uint32_t(need)) {
+        d = 255 - 8 * lane - k;
+        ab = run;
+        ct = c[k];
+      }
+      run += c[k];
+    }
+  }
+  digit = __shfl_sync(kFull, d, src);
+  above = __shfl_sync(kFull, ab, src);
+  cnt = __shfl_sync(kFull, ct, src);
+}
+
+template <typename Key>
+__device__ __forceinline__ int first_diff_shift(Key mx, Key mn) {
+  const Key diff = mx ^ mn;
+  const int top = int(sizeof(Key) * 8) - 1 -
+                  (sizeof(Key) == 8 ? __clzll((long long)diff) : __clz(int(uint32_t(diff))));
+  return (top / 8) * 8;
+}
+
+template <typename Key>
+__device__ __forceinline__ void warp_minmax(Key& mx, Key& mn) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     const Key a = __shfl_xor_sync(kFull, mx, off), b = __shfl_xor_sync(kFull, mn, off);
     mx = a > mx ? a : mx;
     mn = b < mn ? b : mn;
   }
-  const Key diff = mx ^ mn;  // n >= 2 distinct keys: non-zero
-  const int top = int(sizeof(Key) * 8) - 1 -
-                  (sizeof(Key) == 8 ? __clzll((long long)diff) : __clz(int(uint32_t(diff))));
-  int shift = (top / 8) * 8;
+}
+
+// Selects the `need` largest of the n distinct keys in buf[0..n) and writes them,
+// unordered, to out[0..need).  buf is scratch: each radix pass keeps only the keys of
+// the bucket that holds the need-th largest, compacted in place, so only the first
+// pass touches all n keys.  `shift` is the first digit to use (< 0: found from the
+// keys' range); with hist_ready the histogram of that digit is already in hist.  Once a
+// bucket fits in one key per lane, the next digit is the first one where its keys differ.
+template <typename Key>
+__device__ void warp_topk_from(Key* buf, int n, int need, Key* out, uint32_t* hist, int shift,
+                               bool hist_ready) {
+  const int lane = threadIdx.x & 31;
+  if (need >= n) {
+    for (int i = lane; i < n; i += 32) out[i] = buf[i];
+    __syncwarp();
+    return;
+  }
+  if (shift < 0) {
+    Key mx = 0, mn = ~Key(0);
+    for (int i = lane; i < n; i += 32) {
+      const Key k = buf[i];
+      mx = k > mx ? k : mx;
+      mn = k < mn ? k : mn;
+    }
+    warp_minmax(mx, mn);
+    shift = first_diff_shift(mx, mn);  // n >= 2 distinct keys: they differ somewhere
+  }
   int n_out = 0;
   for (;;) {
-    for (int b = lane; b < 256; b += 32) hist[b] = 0u;
-    __syncwarp();
-    for (int i = lane; i < n; i += 32) atomicAdd(&hist[unsigned(buf[i] >> shift) & 255u], 1u);
-    __syncwarp();
-    uint32_t c[8];
-    uint32_t s = 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      c[k] = hist[255 - 8 * lane - k];
-      s += c[k];
+    if (!hist_ready) {
+      for (int b = lane; b < 256; b += 32) hist[b] = 0u;
+      __syncwarp();
+      for (int i = lane; i < n; i += 32) atomicAdd(&hist[unsigned(buf[i] >> shift) & 255u], 1u);
+      __syncwarp();
     }
-    uint32_t incl = s;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const uint32_t y = __shfl_up_sync(kFull, incl, off);
-      if (lane >= off) incl += y;
-    }
-    const uint32_t excl = incl - s;
-    const bool mine = excl < uint32_t(need) && uint32_t(need) <= incl;
-    const int src = __ffs(__ballot_sync(kFull, mine)) - 1;
-    int digit = 0;
-    uint32_t above = 0, cnt = 0;
-    if (mine) {
-      uint32_t run = excl;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        if (cnt == 0u && run + c[k] >= uint32_t(need)) {
-          digit = 255 - 8 * lane - k;
-          above = run;
-          cnt = c[k];
-        }
-        run += c[k];
-      }
-    }
-    digit = __shfl_sync(kFull, digit, src);
-    above = __shfl_sync(kFull, above, src);
-    cnt = __shfl_sync(kFull, cnt, src);
+    hist_ready = false;
+    int digit;
+    uint32_t above, cnt;
+    find_bucket(hist, need, digit, above, cnt);
     // Keys above the bucket are final; the bucket is compacted to the front of buf.
     int base_up = n_out, base_eq = 0;
     for (int i0 = 0; i0 < n; i0 += 32) {
@@ -211,7 +239,14 @@ __device__ void warp_topk(Key* buf, int n, int need, Key* out, uint32_t* hist) {
       __syncwarp();
       return;
     }
-    shift -= 8;  // >= 2 distinct keys share the digit, so a lower digit separates them
+    // >= 2 distinct keys share the digit, so a lower digit separates them.
+    if (n <= 32) {
+      Key mx = buf[lane < n ? lane : 0], mn = mx;
+      warp_minmax(mx, mn);
+      shift = first_diff_shift(mx, mn);
+    } else {
+      shift -= 8;
+    }
   }
 }
 
@@ -284,14 +319,17 @@ __host__ __device__ inline int stair_count(int K, int kin) {
   return c;
 }
 
-// bf16 halves use 32-bit keys (16 value bits, 16 index bits); fp32 halves 64-bit ones.
+// bf16 halves use 32-bit keys (16 value bits, 16 index bits); fp32 halves 48-bit keys
+// (32 value bits, 16 index bits) held in 64 bits.
 template <typename Tin>
 struct InnerKeyOf {
   using type = uint64_t;
+  static constexpr int top_shift = 40;  // shift of the key's top value byte
 };
 template <>
 struct InnerKeyOf<uint16_t> {
   using type = uint32_t;
+  static constexpr int top_shift = 24;
 };
 
 __device__ __forceinline__ uint32_t inner_key(uint16_t u, int j) {
@@ -312,8 +350,104 @@ __device__ __forceinline__ float inner_value(uint64_t key) {
   return ord_decode(uint32_t(key >> 16));
 }
 
-// Shared memory of one warp: key buffer (one half, or the staircase candidates), the
-// selected keys, the histogram and the two inner lists.
+// Unpacks one 16-byte vector of sub-scores.
+template <typename Tin>
+__device__ __forceinline__ void unpack16(const uint4& q, float* v);
+template <>
+__device__ __forceinline__ void unpack16<uint16_t>(const uint4& q, float* v) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+template <>
+__device__ __forceinline__ void unpack16<float>(const uint4& q, float* v) {
+  v[0] = __uint_as_float(q.x);
+  v[1] = __uint_as_float(q.y);
+  v[2] = __uint_as_float(q.z);
+  v[3] = __uint_as_float(q.w);
+}
+__device__ __forceinline__ uint32_t inner_key_f(float v, int j, uint32_t*) {
+  return inner_key(uint16_t(__float_as_uint(v) >> 16), j);
+}
+__device__ __forceinline__ uint64_t inner_key_f(float v, int j, uint64_t*) { return inner_key(v, j); }
+
+__device__ __forceinline__ int warp_excl_scan(int v, int& total) {
+  const int lane = threadIdx.x & 31;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(kFull, incl, off);
+    if (lane >= off) incl += y;
+  }
+  total = __shfl_sync(kFull, incl, 31);
+  return incl - v;
+}
+
+// Top-kin keys of one half (S sub-scores, 16-byte aligned, S a multiple of the vector
+// width) with the whole half in registers: 16-byte loads with the top-byte histogram
+// fused in, then one split of the keys into "above the bucket" (final) and the bucket
+// (kept in cand), and compacting passes over the bucket only.  Writes the kin keys,
+// unordered, to out.
+template <typename Tin, int NV>
+__device__ void inner_topk_regs(const Tin* src, int S, int kin, typename InnerKeyOf<Tin>::type* out,
+                                typename InnerKeyOf<Tin>::type* cand, uint32_t* hist) {
+  using IKey = typename InnerKeyOf<Tin>::type;
+  constexpr int EPV = 16 / int(sizeof(Tin));
+  constexpr int TOP = InnerKeyOf<Tin>::top_shift;
+  const int lane = threadIdx.x & 31;
+  for (int b = lane; b < 256; b += 32) hist[b] = 0u;
+  __syncwarp();
+  IKey k[NV * EPV];
+  bool ok[NV];
+  const uint4* src4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const int c = lane + 32 * v;
+    ok[v] = c * EPV < S;
+    uint4 q = make_uint4(0u, 0u, 0u, 0u);
+    if (ok[v]) q = __ldg(src4 + c);
+    float f[EPV];
+    unpack16<Tin>(q, f);
+#pragma unroll
+    for (int i = 0; i < EPV; ++i) {
+      k[v * EPV + i] = inner_key_f(f[i], c * EPV + i, static_cast<IKey*>(nullptr));
+      if (ok[v]) atomicAdd(&hist[unsigned(k[v * EPV + i] >> TOP) & 255u], 1u);
+    }
+  }
+  __syncwarp();
+  int d1 = -1;
+  uint32_t a1 = 0, c1 = 0;
+  if (kin < S) find_bucket(hist, kin, d1, a1, c1);
+  // Split: digit > d1 -> out (final), digit == d1 -> cand (the bucket).
+  int na = 0, nb = 0;
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int i = 0; i < EPV; ++i) {
+      const int dg = int(unsigned(k[v * EPV + i] >> TOP) & 255u);
+      na += (ok[v] && dg > d1) ? 1 : 0;
+      nb += (ok[v] && dg == d1) ? 1 : 0;
+    }
+  int ta, tb;
+  int oa = warp_excl_scan(na, ta), ob = warp_excl_scan(nb, tb);
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int i = 0; i < EPV; ++i) {
+      const IKey key = k[v * EPV + i];
+      const int dg = int(unsigned(key >> TOP) & 255u);
+      if (ok[v] && dg > d1) out[oa++] = key;
+      else if (ok[v] && dg == d1) cand[ob++] = key;
+    }
+  __syncwarp();
+  if (kin < S) warp_topk_from<IKey>(cand, int(c1), kin - int(a1), out + a1, hist, -1, false);
+}
+
+// Shared memory of one warp: key buffer (one half, its bucket, or the staircase
+// candidates), the selected keys, the histogram and the two inner lists.
 __host__ __device__ inline size_t select_per_warp_bytes(int kpad, int kin_max, int S, int cnt_max,
                                                         int inner_key_bytes) {
   size_t keys = size_t(S) * inner_key_bytes;
@@ -350,7 +484,26 @@ __device__ void build_stair(uint32_t* st, int K, int kin) {
   }
 }
 
-template <typename Tin, int EMAX>
+// Rare path of the outer selection (needs rounding merges or massive ties): the top-K
+// over every grid pair whose key reaches `kth` (the staircase's K-th key), into out.
+__device__ __noinline__ void outer_full_grid(const float* aval, const float* bval,
+                                             const int32_t* aidx, const int32_t* bidx, int S,
+                                             int kin, int K, uint64_t kth, uint64_t* out, int kpad,
+                                             uint32_t* hist) {
+  auto grid_key = [&](int i, bool& valid) -> uint64_t {
+    const int p = i / kin, q = i % kin;
+    const float s = __fadd_rn(aval[p], bval[q]);
+    const uint32_t flat = uint32_t(aidx[p]) * uint32_t(S) + uint32_t(bidx[q]);
+    const uint64_t k = (uint64_t(ord_key(s)) << 32) | uint64_t(0xFFFFFFFFu - flat);
+    valid = k >= kth;
+    return k;
+  };
+  const uint64_t tau2 = radix_threshold(grid_key, kin * kin, K, 64, hist);
+  collect_at_least(grid_key, kin * kin, tau2, out, kpad);
+}
+
+// NV > 0: halves held in registers (NV 16-byte vectors per lane); NV == 0: any S.
+template <typename Tin, int EMAX, int NV>
 __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
   using IKey = typename InnerKeyOf<Tin>::type;
   extern __shared__ __align__(16) unsigned char smem[];
@@ -385,11 +538,15 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
     // ---- 1. top-kin of each half, ranked by (value desc, index asc) ---------------
     for (int h = 0; h < 2; ++h) {
       IKey* ik = reinterpret_cast<IKey*>(keys);
-      const Tin* src = halves + (long long)h * S;
-      for (int j = lane; j < S; j += 32) ik[j] = inner_key(src[j], j);
-      __syncwarp();
       IKey* io = reinterpret_cast<IKey*>(out);
-      warp_topk<IKey>(ik, S, kin, io, hist);
+      const Tin* src = halves + (long long)h * S;
+      if (NV > 0) {
+        inner_topk_regs<Tin, (NV > 0 ? NV : 1)>(src, S, kin, io, ik, hist);
+      } else {
+        for (int j = lane; j < S; j += 32) ik[j] = inner_key(src[j], j);
+        __syncwarp();
+        warp_topk_from<IKey>(ik, S, kin, io, hist, -1, false);
+      }
       sort_desc_upto<IKey, EMAX>(io, kin);
       float* dv = h ? bval : aval;
       int32_t* di = h ? bidx : aidx;
@@ -410,12 +567,27 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
       return (uint64_t(ord_key(s)) << 32) | uint64_t(0xFFFFFFFFu - flat);
     };
     uint64_t* ck = reinterpret_cast<uint64_t*>(keys);
+    int shift = 0;
+    if (cnt > K) {
+      // The largest staircase key is (0, 0); the smallest is the end of some row.
+      uint64_t mx = pair_key(0, 0), mn = ~0ull;
+      for (int p = lane; p < kin; p += 32) {
+        const uint64_t k = pair_key(p, min(kin, K / (p + 1)) - 1);
+        mn = k < mn ? k : mn;
+      }
+      warp_minmax(mx, mn);
+      shift = first_diff_shift(mx, mn);
+      for (int b = lane; b < 256; b += 32) hist[b] = 0u;
+      __syncwarp();
+    }
     for (int c = lane; c < cnt; c += 32) {
       const uint32_t pq = st[c];
-      ck[c] = pair_key(int(pq >> 16), int(pq & 0xFFFFu));
+      const uint64_t k = pair_key(int(pq >> 16), int(pq & 0xFFFFu));
+      ck[c] = k;
+      if (cnt > K) atomicAdd(&hist[unsigned(k >> shift) & 255u], 1u);
     }
     __syncwarp();
-    warp_topk<uint64_t>(ck, cnt, K, out, hist);
+    warp_topk_from<uint64_t>(ck, cnt, K, out, hist, shift, true);
     sort_desc_upto<uint64_t, EMAX>(out, K);
     const uint64_t kth = out[K - 1];
     const uint32_t kth_sum = uint32_t(kth >> 32);
@@ -429,15 +601,7 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
       }
     }
     if (__any_sync(kFull, beyond)) {
-      // Rare (needs rounding merges or massive ties): redo over every grid pair whose
-      // key reaches the staircase's K-th key; the true top-K is among them.
-      auto grid_key = [&](int i, bool& valid) -> uint64_t {
-        const uint64_t k = pair_key(i / kin, i % kin);
-        valid = k >= kth;
-        return k;
-      };
-      const uint64_t tau2 = radix_threshold(grid_key, kin * kin, K, 64, hist);
-      collect_at_least(grid_key, kin * kin, tau2, out, a.kpad);
+      outer_full_grid(aval, bval, aidx, bidx, S, kin, K, kth, out, a.kpad, hist);
       sort_desc_upto<uint64_t, EMAX>(out, K);
     }
     int32_t* oi = (which ? a.idx_r : a.idx_w) + item * K;
@@ -451,10 +615,10 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
   }
 }
 
-}  // namespace
-
-int launch_select(const void* kp, const void* qp, int in_dt, long long items, int S, int W, int R,
-                  int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, cudaStream_t s) {
+template <typename Tin>
+int launch_select_t(const void* kp, const void* qp, long long items, int S, int W, int R,
+                    int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, cudaStream_t s) {
+  constexpr bool kBf16 = sizeof(Tin) == 2;
   if (items == 0) return SDM_OK;
   SelectArgs a;
   a.kp = kp;
@@ -473,7 +637,7 @@ int launch_select(const void* kp, const void* qp, int in_dt, long long items, in
   a.sc_w = sc_w;
   a.idx_r = idx_r;
   a.sc_r = sc_r;
-  const int ikb = in_dt == SDM_BF16 ? 4 : 8;
+  const int ikb = kBf16 ? 4 : 8;
   size_t keys = size_t(S) * ikb;
   if (size_t(max(a.cnt_w, a.cnt_r)) * 8 > keys) keys = size_t(max(a.cnt_w, a.cnt_r)) * 8;
   a.keys_bytes = (keys + 15) / 16 * 16;
@@ -489,14 +653,18 @@ int launch_select(const void* kp, const void* qp, int in_dt, long long items, in
   if (stair_bytes + per_warp * warps > size_t(max_smem)) return SDM_EUNSUPPORTED;
   a.warps = warps;
   const size_t smem = stair_bytes + per_warp * warps;
+  // Register-resident halves: 4 vectors of 16 bytes per lane (S <= 1024 bf16 / 512 fp32),
+  // every half 16-byte aligned (the base is; S * element size must be a multiple of 16).
+  const int elt = kBf16 ? 2 : 4;
+  const bool regs = (S * elt) % 16 == 0 && S * elt <= 4 * 32 * 16;
   const bool small = kmax <= 128;
   const void* fn;
-  if (in_dt == SDM_BF16)
-    fn = small ? reinterpret_cast<const void*>(&select_kernel<uint16_t, 4>)
-               : reinterpret_cast<const void*>(&select_kernel<uint16_t, 32>);
+  if (small)
+    fn = regs ? reinterpret_cast<const void*>(&select_kernel<Tin, 4, 4>)
+              : reinterpret_cast<const void*>(&select_kernel<Tin, 4, 0>);
   else
-    fn = small ? reinterpret_cast<const void*>(&select_kernel<float, 4>)
-               : reinterpret_cast<const void*>(&select_kernel<float, 32>);
+    fn = regs ? reinterpret_cast<const void*>(&select_kernel<Tin, 32, 4>)
+              : reinterpret_cast<const void*>(&select_kernel<Tin, 32, 0>);
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
     return SDM_ECUDA;
   int per_sm = 0;
@@ -512,4 +680,5 @@ int launch_select(const void* kp, const void* qp, int in_dt, long long items, in
   return last_launch_status();
 }
 
+}  // namespace
 }  // namespace sdm
