@@ -374,76 +374,40 @@ __device__ __forceinline__ uint32_t inner_key_f(float v, int j, uint32_t*) {
 }
 __device__ __forceinline__ uint64_t inner_key_f(float v, int j, uint64_t*) { return inner_key(v, j); }
 
-__device__ __forceinline__ int warp_excl_scan(int v, int& total) {
-  const int lane = threadIdx.x & 31;
-  int incl = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(kFull, incl, off);
-    if (lane >= off) incl += y;
-  }
-  total = __shfl_sync(kFull, incl, 31);
-  return incl - v;
-}
-
-// Top-kin keys of one half (S sub-scores, 16-byte aligned, S a multiple of the vector
-// width) with the whole half in registers: 16-byte loads with the top-byte histogram
-// fused in, then one split of the keys into "above the bucket" (final) and the bucket
-// (kept in cand), and compacting passes over the bucket only.  Writes the kin keys,
-// unordered, to out.
-template <typename Tin, int NV>
-__device__ void inner_topk_regs(const Tin* src, int S, int kin, typename InnerKeyOf<Tin>::type* out,
-                                typename InnerKeyOf<Tin>::type* cand, uint32_t* hist) {
+// Keys of one half into ik[0..S) with the histogram of their top value byte: 16-byte
+// loads when every half is 16-byte aligned (vec), element loads otherwise.
+template <typename Tin>
+__device__ __forceinline__ void load_half_keys(const Tin* src, int S, bool vec,
+                                               typename InnerKeyOf<Tin>::type* ik, uint32_t* hist) {
   using IKey = typename InnerKeyOf<Tin>::type;
   constexpr int EPV = 16 / int(sizeof(Tin));
   constexpr int TOP = InnerKeyOf<Tin>::top_shift;
   const int lane = threadIdx.x & 31;
   for (int b = lane; b < 256; b += 32) hist[b] = 0u;
   __syncwarp();
-  IKey k[NV * EPV];
-  bool ok[NV];
-  const uint4* src4 = reinterpret_cast<const uint4*>(src);
+  if (vec) {
+    const uint4* src4 = reinterpret_cast<const uint4*>(src);
+    for (int c = lane; c < S / EPV; c += 32) {
+      float f[EPV];
+      unpack16<Tin>(__ldg(src4 + c), f);
+      IKey k[EPV];
 #pragma unroll
-  for (int v = 0; v < NV; ++v) {
-    const int c = lane + 32 * v;
-    ok[v] = c * EPV < S;
-    uint4 q = make_uint4(0u, 0u, 0u, 0u);
-    if (ok[v]) q = __ldg(src4 + c);
-    float f[EPV];
-    unpack16<Tin>(q, f);
+      for (int i = 0; i < EPV; ++i) {
+        k[i] = inner_key_f(f[i], c * EPV + i, static_cast<IKey*>(nullptr));
+        atomicAdd(&hist[unsigned(k[i] >> TOP) & 255u], 1u);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(ik + c * EPV);
 #pragma unroll
-    for (int i = 0; i < EPV; ++i) {
-      k[v * EPV + i] = inner_key_f(f[i], c * EPV + i, static_cast<IKey*>(nullptr));
-      if (ok[v]) atomicAdd(&hist[unsigned(k[v * EPV + i] >> TOP) & 255u], 1u);
+      for (int w = 0; w < int(EPV * sizeof(IKey) / 16); ++w) dst[w] = reinterpret_cast<const uint4*>(k)[w];
+    }
+  } else {
+    for (int j = lane; j < S; j += 32) {
+      const IKey k = inner_key(src[j], j);
+      ik[j] = k;
+      atomicAdd(&hist[unsigned(k >> TOP) & 255u], 1u);
     }
   }
   __syncwarp();
-  int d1 = -1;
-  uint32_t a1 = 0, c1 = 0;
-  if (kin < S) find_bucket(hist, kin, d1, a1, c1);
-  // Split: digit > d1 -> out (final), digit == d1 -> cand (the bucket).
-  int na = 0, nb = 0;
-#pragma unroll
-  for (int v = 0; v < NV; ++v)
-#pragma unroll
-    for (int i = 0; i < EPV; ++i) {
-      const int dg = int(unsigned(k[v * EPV + i] >> TOP) & 255u);
-      na += (ok[v] && dg > d1) ? 1 : 0;
-      nb += (ok[v] && dg == d1) ? 1 : 0;
-    }
-  int ta, tb;
-  int oa = warp_excl_scan(na, ta), ob = warp_excl_scan(nb, tb);
-#pragma unroll
-  for (int v = 0; v < NV; ++v)
-#pragma unroll
-    for (int i = 0; i < EPV; ++i) {
-      const IKey key = k[v * EPV + i];
-      const int dg = int(unsigned(key >> TOP) & 255u);
-      if (ok[v] && dg > d1) out[oa++] = key;
-      else if (ok[v] && dg == d1) cand[ob++] = key;
-    }
-  __syncwarp();
-  if (kin < S) warp_topk_from<IKey>(cand, int(c1), kin - int(a1), out + a1, hist, -1, false);
 }
 
 // Shared memory of one warp: key buffer (one half, its bucket, or the staircase
@@ -467,6 +431,7 @@ struct SelectArgs {
   int cnt_w, cnt_r;
   int warps;
   size_t keys_bytes;  // per-warp key buffer
+  bool vec;           // every half starts on a 16-byte boundary
   int32_t* idx_w;
   float* sc_w;
   int32_t* idx_r;
@@ -502,8 +467,7 @@ __device__ __noinline__ void outer_full_grid(const float* aval, const float* bva
   collect_at_least(grid_key, kin * kin, tau2, out, kpad);
 }
 
-// NV > 0: halves held in registers (NV 16-byte vectors per lane); NV == 0: any S.
-template <typename Tin, int EMAX, int NV>
+template <typename Tin, int EMAX>
 __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
   using IKey = typename InnerKeyOf<Tin>::type;
   extern __shared__ __align__(16) unsigned char smem[];
@@ -539,14 +503,8 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
     for (int h = 0; h < 2; ++h) {
       IKey* ik = reinterpret_cast<IKey*>(keys);
       IKey* io = reinterpret_cast<IKey*>(out);
-      const Tin* src = halves + (long long)h * S;
-      if (NV > 0) {
-        inner_topk_regs<Tin, (NV > 0 ? NV : 1)>(src, S, kin, io, ik, hist);
-      } else {
-        for (int j = lane; j < S; j += 32) ik[j] = inner_key(src[j], j);
-        __syncwarp();
-        warp_topk_from<IKey>(ik, S, kin, io, hist, -1, false);
-      }
+      load_half_keys<Tin>(halves + (long long)h * S, S, a.vec, ik, hist);
+      warp_topk_from<IKey>(ik, S, kin, io, hist, InnerKeyOf<Tin>::top_shift, true);
       sort_desc_upto<IKey, EMAX>(io, kin);
       float* dv = h ? bval : aval;
       int32_t* di = h ? bidx : aidx;
@@ -653,18 +611,10 @@ int launch_select_t(const void* kp, const void* qp, long long items, int S, int 
   if (stair_bytes + per_warp * warps > size_t(max_smem)) return SDM_EUNSUPPORTED;
   a.warps = warps;
   const size_t smem = stair_bytes + per_warp * warps;
-  // Register-resident halves: 4 vectors of 16 bytes per lane (S <= 1024 bf16 / 512 fp32),
-  // every half 16-byte aligned (the base is; S * element size must be a multiple of 16).
-  const int elt = kBf16 ? 2 : 4;
-  const bool regs = (S * elt) % 16 == 0 && S * elt <= 4 * 32 * 16;
-  const bool small = kmax <= 128;
-  const void* fn;
-  if (small)
-    fn = regs ? reinterpret_cast<const void*>(&select_kernel<Tin, 4, 4>)
-              : reinterpret_cast<const void*>(&select_kernel<Tin, 4, 0>);
-  else
-    fn = regs ? reinterpret_cast<const void*>(&select_kernel<Tin, 32, 4>)
-              : reinterpret_cast<const void*>(&select_kernel<Tin, 32, 0>);
+  // 16-byte loads of the halves when every half is 16-byte aligned (the base is).
+  a.vec = (S * int(sizeof(Tin))) % 16 == 0;
+  const void* fn = kmax <= 128 ? reinterpret_cast<const void*>(&select_kernel<Tin, 4>)
+                               : reinterpret_cast<const void*>(&select_kernel<Tin, 32>);
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
     return SDM_ECUDA;
   int per_sm = 0;
