@@ -154,7 +154,7 @@ def test_scan_on_oracle_selection():
     p = _random_problem(rng, B, H, T, S, dv, W, R)
     ref = _oracle_problem(p, W, R)
     d = _to_dev(p)
-    M = d["M0"][None].expand(B, H, S * S, dv).contiguous()
+    M = d["M0"][None].repeat(B, 1, 1, 1)
     sel = [torch.from_numpy(ref[k].reshape(B, H, T, -1)).cuda() for k in ("idx_w", "sc_w", "idx_r", "sc_r")]
     o = sdm.scan_forward(M, *sel, d["v"], d["alpha"], d["beta"])
     assert scaled_err(o.cpu().numpy().reshape(B * H, T, dv), ref["o"]) <= TOL
@@ -220,6 +220,26 @@ def test_forced_shapes_agree(ci):
                 assert torch.equal(M, results[0][3]), (cols, pd)
                 assert scaled_err(o.cpu().numpy(), results[0][2].cpu().numpy()) <= 1e-5, (cols, pd)
                 del results[-1]
+
+
+@pytest.mark.parametrize("dims", [(1, 1, 64, 32, 16, 8, 8), (1, 2, 97, 8, 16, 5, 7), (2, 3, 300, 16, 32, 12, 10)])
+def test_workspace_contents_do_not_matter(dims):
+    """The planning kernel writes every record field the scan reads: a workspace full of
+    garbage gives the same bits as a zeroed one."""
+    B, H, T, S, dv, W, R = dims
+    rng = np.random.default_rng(sum(dims))
+    p = _random_problem(rng, B, H, T, S, dv, W, R, torch.bfloat16)
+    d = _to_dev(p, torch.bfloat16)
+    sel = sdm.select(d["kp"], d["qp"], W, R)
+    results = []
+    for fill in (0x00, 0xFF, 0x7F):
+        ws = sdm.scan_workspace(B, H, T, dv, W, R, "cuda")
+        ws.fill_(fill)
+        M = d["M0"][None].repeat(B, 1, 1, 1)
+        o = sdm.scan_forward(M, *sel, d["v"], d["alpha"], d["beta"], workspace=ws)
+        results.append((o, M))
+    for o, M in results[1:]:
+        assert torch.equal(o, results[0][0]) and torch.equal(M, results[0][1])
 
 
 def test_device_error_flags():
