@@ -47,7 +47,8 @@ typedef enum {
   SDM_ETIMEOUT = -4,     /* reserved: a bounded device wait ran out */
   SDM_EBOUNDS = -5,      /* reserved: device-detected bounds error */
   SDM_EUNSUPPORTED = -6, /* sizes valid for the method but beyond this build's limits */
-  SDM_ENOSPACE = -7      /* the workspace passed is smaller than required */
+  SDM_ENOSPACE = -7,     /* the workspace passed is smaller than required */
+  SDM_ESCRATCH = -8      /* too large for sdm_scan_forward_noalloc's fixed scratch */
 } sdm_status;
 
 typedef enum { SDM_F32 = 0, SDM_BF16 = 1 } sdm_dtype;
@@ -121,6 +122,34 @@ int sdm_scan_forward_tuned(float* M, const int32_t* idx_w, const float* sc_w,
                            long long N, int d_v, int W, int R, float* o, void* workspace,
                            size_t workspace_bytes, int* dev_err, int cols_per_cta,
                            int prefetch_depth, void* event_after_plan, void* stream);
+
+/* Bytes of the fixed device scratch behind sdm_scan_forward_noalloc (64 MiB). */
+#define SDM_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/* sdm_scan_forward_noalloc - sdm_scan_forward without a caller-provided workspace; the
+ * paper has no counterpart: this is an interface for callers that cannot allocate device
+ * memory where they run the scan (a serving or real-time loop that forbids allocation on
+ * its request path, or a host application that owns no allocator and passes only its
+ * input and output buffers).  Same arguments, results and errors as sdm_scan_forward,
+ * minus the workspace; the library calls no cudaMalloc/cudaFree or other allocating
+ * routine for it.
+ *   - The planning records go to one fixed scratch of SDM_NOALLOC_SCRATCH_BYTES that lives
+ *     in the library's device image: every GPU that loads the library keeps that memory
+ *     until the process exits.
+ *   - Sizes whose workspace (sdm_scan_workspace_size) exceeds SDM_NOALLOC_SCRATCH_BYTES are
+ *     refused with SDM_ESCRATCH before anything is launched; e.g. with d_v = 128 and
+ *     W = R = 128 (3,088 bytes per (b, h, t)) up to 21,732 (b, h, t) triples per call.
+ *   - The first call on a device looks up the scratch's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - All calls on a device share the scratch and each one overwrites what the last left
+ *     there (nothing in it needs to start at zero).  Calls whose work overlaps on the GPU
+ *     (other streams, other host threads) race on it: keep them ordered, e.g. on one
+ *     stream. */
+int sdm_scan_forward_noalloc(float* M, const int32_t* idx_w, const float* sc_w,
+                             const int32_t* idx_r, const float* sc_r, const void* v, int v_dt,
+                             const float* alpha, const float* beta, int B, int H, int T,
+                             long long N, int d_v, int W, int R, float* o, int* dev_err,
+                             void* stream);
 
 /* The scan kernel shape sdm_scan_forward would use (host-only query): columns per
  * thread block, prefetch depth, thread blocks, dynamic shared memory bytes. */

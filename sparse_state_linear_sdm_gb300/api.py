@@ -175,6 +175,43 @@ def scan_forward(M, idx_w, sc_w, idx_r, sc_r, v, alpha, beta, o=None, workspace=
     return o
 
 
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def scan_forward_noalloc(M, idx_w, sc_w, idx_r, sc_r, v, alpha, beta, o, dev_err=None):
+    """scan_forward for callers that cannot allocate device memory where the scan runs.
+
+    Same inputs and results as scan_forward, but the library uses its own fixed device
+    scratch (NOALLOC_SCRATCH_BYTES, held on every GPU that loads the library) instead of a
+    workspace, and the output buffer o must be passed in: nothing is allocated here or in
+    the library.  Sizes whose workspace would exceed the scratch raise SDMError.  Calls
+    share the scratch, so they must not overlap on the GPU (keep them on one stream); the
+    first call on a device should come before any stream capture."""
+    L = lib()
+    f = L.sdm_scan_forward_noalloc
+    p, i, ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
+    f.argtypes = [p, p, p, p, p, p, i, p, p, i, i, i, ll, i, i, i, p, p, p]
+    f.restype = i
+    _need(M, "M", torch.float32)
+    B, H, N, dv = M.shape
+    T, W, R = idx_w.shape[2], idx_w.shape[3], idx_r.shape[3]
+    _need(idx_w, "idx_w", torch.int32, (B, H, T, W))
+    _need(sc_w, "sc_w", torch.float32, (B, H, T, W))
+    _need(idx_r, "idx_r", torch.int32, (B, H, T, R))
+    _need(sc_r, "sc_r", torch.float32, (B, H, T, R))
+    _need(v, "v", None, (B, H, T, dv))
+    _need(alpha, "alpha", torch.float32, (B, H, T))
+    _need(beta, "beta", torch.float32, (B, H, T))
+    _need(o, "o", torch.float32, (B, H, T, dv))
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32)
+    st = f(_p(M), _p(idx_w), _p(sc_w), _p(idx_r), _p(sc_r), _p(v), _dtype_code(v), _p(alpha), _p(beta),
+           B, H, T, N, dv, W, R, _p(o), _p(dev_err), _stream(M.device))
+    if st != 0:
+        raise SDMError("sdm_scan_forward_noalloc", st)
+    return o
+
+
 def scan_launch_info(B: int, H: int, d_v: int, W: int, R: int) -> dict:
     vals = [ctypes.c_int(0) for _ in range(4)]
     _call("sdm_scan_launch_info", B, H, d_v, W, R, *[ctypes.byref(x) for x in vals])
