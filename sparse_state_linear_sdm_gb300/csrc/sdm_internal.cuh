@@ -56,6 +56,13 @@ int launch_select_bf16(const void* kp, const void* qp, long long items, int S, i
 int launch_select_f32(const void* kp, const void* qp, long long items, int S, int W, int R,
                       int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, cudaStream_t s);
 
+// Planning pass of the scan (one record per (b, h, t) into `workspace`); `pd` must be the
+// prefetch depth of the scan kernel that consumes the records.
+int launch_plan(const int32_t* idx_w, const float* sc_w, const int32_t* idx_r, const float* sc_r,
+                const void* v, int v_dt, const float* alpha, const float* beta, int BH, int T,
+                long long N, int d_v, int W, int R, int pd, void* workspace, int* dev_err,
+                cudaStream_t s);
+
 struct ScanShape {
   int cols;      // d_v columns per thread block
   int pd;        // prefetch depth (tokens)

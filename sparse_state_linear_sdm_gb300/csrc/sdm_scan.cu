@@ -4,19 +4,14 @@
 //   write slots i (k_t: softmax of their scores), all other slots untouched, then
 //   o_t = sum_i r_i M_t[i] over the R read slots (r: softmax of their scores).
 //
-// Two kernels:
-//   plan  (time-parallel, one block per (b,h, chunk of tokens)): for every token and
-//         every selected slot, finds whether a token at most `pd` steps earlier (or
-//         the same token, for a read) wrote that slot, and where in its write set.
-//         Also forms both softmaxes and packs slots, weights, alpha, beta and v into
-//         one 16-byte-aligned record per token (layout in sdm_internal.cuh).
-//   scan  (one block per (b,h, slice of `cols` columns of d_v), sequential in t):
-//         the columns of the table are independent given the slots, so each block
-//         owns a column slice of one (b,h) table outright.  It gathers the rows of
-//         token t+pd from HBM with 16-byte cp.async while it updates token t; rows
-//         whose latest writer is still in that window never come from HBM: the
-//         writer pushes its updated row into the later token's staging slot
-//         (forwarding), which also serves a read of a row written by the same token.
+// The planning kernel (sdm_plan.cu) first writes one record per token (slots, weights,
+// where each row comes from).  The scan kernel here then runs one block per (b, h, slice
+// of `cols` columns of d_v), sequential in t: the columns of the table are independent
+// given the slots, so each block owns a column slice of one (b, h) table outright.  It
+// gathers the rows of token t+pd from HBM with 16-byte cp.async while it updates token t;
+// rows whose latest writer is still in that window never come from HBM: the writer
+// pushes its updated row into the later token's staging slot (forwarding), which also
+// serves a read of a row written by the same token.
 // This is gather/scatter plus axpy: no tensor cores.
 #include <cuda_bf16.h>
 
@@ -25,160 +20,8 @@
 namespace sdm {
 namespace {
 
-constexpr int kPlanThreads = 256;
 constexpr int kScanThreads = 256;
 constexpr int kScanWarps = kScanThreads / 32;
-
-// Multiplicative hash of a slot into a table of 2^log2cap entries.
-__device__ __forceinline__ uint32_t slot_hash(int32_t x, int log2cap) {
-  return (uint32_t(x) * 0x9E3779B1u) >> (32 - log2cap);
-}
-
-template <typename Tv>
-__device__ __forceinline__ float load_v(const Tv* p, size_t i);
-template <>
-__device__ __forceinline__ float load_v<float>(const float* p, size_t i) {
-  return p[i];
-}
-template <>
-__device__ __forceinline__ float load_v<uint16_t>(const uint16_t* p, size_t i) {
-  return __uint_as_float(uint32_t(p[i]) << 16);
-}
-
-struct PlanArgs {
-  const int32_t* idx_w;
-  const float* sc_w;
-  const int32_t* idx_r;
-  const float* sc_r;
-  const void* v;
-  const float* alpha;
-  const float* beta;
-  int T;
-  long long N;
-  int d_v, W, R, pd, tc;
-  int log2cap;  // hash table of 2^log2cap entries, at least twice the entries inserted
-  RecLayout L;
-  unsigned char* rec;
-  int* dev_err;
-};
-
-// Softmax of n scores with one warp, written to w[0..n): one exp per score (the
-// unnormalised values are stored first, then scaled in place).
-__device__ void warp_softmax(const float* __restrict__ s, int n, float* w) {
-  const int lane = threadIdx.x & 31;
-  float m = -INFINITY;
-  for (int i = lane; i < n; i += 32) m = fmaxf(m, s[i]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-  float z = 0.f;
-  for (int i = lane; i < n; i += 32) {
-    const float e = expf(s[i] - m);
-    w[i] = e;
-    z += e;
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, off);
-  const float inv = 1.0f / z;
-  for (int i = lane; i < n; i += 32) w[i] *= inv;  // each lane rescales what it wrote
-}
-
-constexpr unsigned long long kEmpty = ~0ull;
-
-// Shared memory of one planning block: hash table, then the chunk's write slots
-// (tokens [t0 - pd, t1)) and read slots (tokens [t0, t1)).
-__host__ __device__ inline size_t plan_smem_bytes(int log2cap, int tc, int pd, int W, int R) {
-  return (size_t(8) << log2cap) + size_t(tc + pd) * W * 4 + size_t(tc) * R * 4;
-}
-
-template <typename Tv>
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
-  // Open-addressing table of the write slots of tokens [tl, t1): one 64-bit word per
-  // entry, slot << 32 | (token - tl) << 16 | position in the write set.
-  extern __shared__ unsigned long long table[];
-  const int tid = threadIdx.x;
-  const int bh = blockIdx.y;
-  const int t0 = blockIdx.x * a.tc;
-  const int t1 = min(a.T, t0 + a.tc);
-  const int tl = max(0, t0 - a.pd);
-  const int W = a.W, R = a.R, WR = W + R;
-  const size_t tok0 = size_t(bh) * a.T;
-  const int cap = 1 << a.log2cap, mask = cap - 1;
-  int32_t* iw = reinterpret_cast<int32_t*>(table + cap);         // [(t1 - tl) * W]
-  int32_t* ir = iw + (a.tc + a.pd) * W;                          // [(t1 - t0) * R]
-
-  // Stage the slot lists with independent loads (one memory latency, not one per use).
-  {
-    const int nw = (t1 - tl) * W, nr = (t1 - t0) * R;
-    const int32_t* gw = a.idx_w + (tok0 + tl) * W;
-    const int32_t* gr = a.idx_r + (tok0 + t0) * R;
-#pragma unroll 8
-    for (int i = tid; i < nw; i += kPlanThreads) iw[i] = gw[i];
-#pragma unroll 8
-    for (int i = tid; i < nr; i += kPlanThreads) ir[i] = gr[i];
-  }
-  for (int i = tid; i < cap; i += kPlanThreads) table[i] = kEmpty;
-  __syncthreads();
-  for (int tt = tl; tt < t1; ++tt) {
-    for (int pos = tid; pos < W; pos += kPlanThreads) {
-      const int32_t x = iw[(tt - tl) * W + pos];
-      if (x < 0 || x >= a.N) continue;
-      const unsigned long long e =
-          (static_cast<unsigned long long>(uint32_t(x)) << 32) | (uint32_t(tt - tl) << 16) | uint32_t(pos);
-      uint32_t h = slot_hash(x, a.log2cap);
-      while (atomicCAS(&table[h], kEmpty, e) != kEmpty) h = (h + 1) & mask;
-    }
-  }
-  __syncthreads();
-
-  for (int u = t0; u < t1; ++u) {
-    unsigned char* rec = a.rec + (tok0 + u) * size_t(a.L.bytes);
-    for (int e = tid; e < WR; e += kPlanThreads) {
-      int32_t x = e < W ? iw[(u - tl) * W + e] : ir[(u - t0) * R + (e - W)];
-      int code = -1;
-      if (x < 0 || x >= a.N) {
-        code = -2;
-        x = 0;
-        if (a.dev_err) atomicOr(a.dev_err, SDM_DEV_INDEX_RANGE);
-      } else {
-        int best_t = -1, best_p = 0;
-        for (uint32_t h = slot_hash(x, a.log2cap);; h = (h + 1) & mask) {
-          const unsigned long long v = table[h];
-          if (v == kEmpty) break;
-          if (uint32_t(v >> 32) != uint32_t(x)) continue;
-          const int tt = tl + int((v >> 16) & 0xFFFFu), pp = int(v & 0xFFFFu);
-          if (e < W && tt == u && pp != e && a.dev_err) atomicOr(a.dev_err, SDM_DEV_DUP_WRITE);
-          const bool earlier = e < W ? tt < u : tt <= u;
-          if (earlier && tt >= u - a.pd && tt > best_t) {
-            best_t = tt;
-            best_p = pp;
-          }
-        }
-        if (best_t >= 0) code = (u - best_t) * W + best_p;
-      }
-      reinterpret_cast<int32_t*>(rec)[e] = x;
-      reinterpret_cast<int16_t*>(rec + a.L.off_src)[e] = int16_t(code);
-    }
-  }
-
-  // Weights, gates and v for each token of the chunk: one warp per token.
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int u = t0 + warp; u < t1; u += kPlanThreads / 32) {
-    unsigned char* rec = a.rec + (tok0 + u) * size_t(a.L.bytes);
-    float* wts = reinterpret_cast<float*>(rec + a.L.off_wts);
-    warp_softmax(a.sc_w + (tok0 + u) * W, W, wts);
-    warp_softmax(a.sc_r + (tok0 + u) * R, R, wts + W);
-    if (lane == 0) {
-      float* ab = reinterpret_cast<float*>(rec + a.L.off_ab);
-      ab[0] = a.alpha[tok0 + u];
-      ab[1] = a.beta[tok0 + u];
-      ab[2] = 0.f;
-      ab[3] = 0.f;
-    }
-    float* vr = reinterpret_cast<float*>(rec + a.L.off_v);
-    const Tv* vsrc = static_cast<const Tv*>(a.v) + (tok0 + u) * size_t(a.d_v);
-    for (int c = lane; c < a.d_v; c += 32) vr[c] = load_v<Tv>(vsrc, c);
-  }
-}
 
 // ---------------------------------------------------------------------------------
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
@@ -416,49 +259,9 @@ int launch_scan(float* M, const int32_t* idx_w, const float* sc_w, const int32_t
                 int* dev_err, const ScanShape& shape, cudaEvent_t after_plan, cudaStream_t s) {
   if (T == 0 || BH == 0) return SDM_OK;
   const RecLayout L = rec_layout(W, R, d_v);
-  PlanArgs pa;
-  pa.idx_w = idx_w;
-  pa.sc_w = sc_w;
-  pa.idx_r = idx_r;
-  pa.sc_r = sc_r;
-  pa.v = v;
-  pa.alpha = alpha;
-  pa.beta = beta;
-  pa.T = T;
-  pa.N = N;
-  pa.d_v = d_v;
-  pa.W = W;
-  pa.R = R;
-  pa.pd = shape.pd;
-  // Chunk of tokens per plan block: its write sets (plus pd earlier ones) fill at most
-  // half of the hash table, which keeps probe sequences short.
-  // Tokens per planning block: at most ~2048 inserted write slots, and shared memory
-  // within 96 KB (two blocks per SM); the table has at least twice the inserted entries.
-  int tc = 2048 / W - shape.pd;
-  tc = tc < 1 ? 1 : (tc > 128 ? 128 : tc);
-  auto cap_for = [&](int t) {
-    int l = 12;
-    while ((1LL << l) < 2LL * (t + shape.pd) * W) ++l;
-    return l;
-  };
-  while (tc > 1 && plan_smem_bytes(cap_for(tc), tc, shape.pd, W, R) > 96 * 1024) --tc;
-  pa.tc = tc;
-  pa.log2cap = cap_for(tc);
-  pa.L = L;
-  pa.rec = static_cast<unsigned char*>(workspace);
-  pa.dev_err = dev_err;
-  const dim3 pgrid((T + tc - 1) / tc, BH);
-  const int plan_smem = int(plan_smem_bytes(pa.log2cap, tc, shape.pd, W, R));
-  const void* pfn = v_dt == SDM_BF16 ? reinterpret_cast<const void*>(&plan_kernel<uint16_t>)
-                                     : reinterpret_cast<const void*>(&plan_kernel<float>);
-  if (cudaFuncSetAttribute(pfn, cudaFuncAttributeMaxDynamicSharedMemorySize, plan_smem) !=
-      cudaSuccess)
-    return SDM_ECUDA;
-  if (v_dt == SDM_BF16)
-    plan_kernel<uint16_t><<<pgrid, kPlanThreads, plan_smem, s>>>(pa);
-  else
-    plan_kernel<float><<<pgrid, kPlanThreads, plan_smem, s>>>(pa);
-  if (last_launch_status() != SDM_OK) return SDM_ECUDA;
+  const int st = launch_plan(idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, BH, T, N, d_v, W, R,
+                            shape.pd, workspace, dev_err, s);
+  if (st != SDM_OK) return st;
   if (after_plan && cudaEventRecord(after_plan, s) != cudaSuccess) return SDM_ECUDA;
 
   ScanArgs sa;

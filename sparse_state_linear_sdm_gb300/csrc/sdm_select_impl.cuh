@@ -250,8 +250,27 @@ __device__ void warp_topk_from(Key* buf, int n, int need, Key* out, uint32_t* hi
   }
 }
 
+// Compare-exchange of registers e and e ^ JE (JE = partner distance / 32) in one
+// bitonic step of block size k.
+template <typename Key, int E, int JE>
+__device__ __forceinline__ void cx_regs(Key (&v)[E], int k, int lane) {
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int ep = e ^ JE;
+    if (ep > e) {
+      const bool desc = ((e * 32 + lane) & k) == 0;
+      const Key a = v[e], b = v[ep];
+      if (desc ? (a < b) : (a > b)) {
+        v[e] = b;
+        v[ep] = a;
+      }
+    }
+  }
+}
+
 // Bitonic sort (descending) of buf[0..count) padded with zero keys to 32*E entries.
-// Element i lives in lane i % 32, register i / 32.
+// Element i lives in lane i % 32, register i / 32.  The stage loops stay rolled (small
+// code); only the per-register work of a step is unrolled.
 template <typename Key, int E>
 __device__ __noinline__ void sort_desc(Key* buf, int count) {
   const int lane = threadIdx.x & 31;
@@ -262,29 +281,21 @@ __device__ __noinline__ void sort_desc(Key* buf, int count) {
     v[e] = i < count ? buf[i] : Key(0);
   }
   constexpr int n = 32 * E;
-#pragma unroll
+#pragma unroll 1
   for (int k = 2; k <= n; k <<= 1) {
-#pragma unroll
+#pragma unroll 1
     for (int j = k >> 1; j > 0; j >>= 1) {
       if (j >= 32) {
-        const int je = j >> 5;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const int ep = e ^ je;
-          if (ep > e) {
-            const bool desc = ((e * 32 + lane) & k) == 0;
-            const Key a = v[e], b = v[ep];
-            if (desc ? (a < b) : (a > b)) {
-              v[e] = b;
-              v[ep] = a;
-            }
-          }
-        }
+        if (E >= 2 && j == 32) cx_regs<Key, E, (E >= 2 ? 1 : 0)>(v, k, lane);
+        else if (E >= 4 && j == 64) cx_regs<Key, E, (E >= 4 ? 2 : 0)>(v, k, lane);
+        else if (E >= 8 && j == 128) cx_regs<Key, E, (E >= 8 ? 4 : 0)>(v, k, lane);
+        else if (E >= 16 && j == 256) cx_regs<Key, E, (E >= 16 ? 8 : 0)>(v, k, lane);
+        else if (E >= 32 && j == 512) cx_regs<Key, E, (E >= 32 ? 16 : 0)>(v, k, lane);
       } else {
+        const bool lower = (lane & j) == 0;
 #pragma unroll
         for (int e = 0; e < E; ++e) {
           const Key other = __shfl_xor_sync(kFull, v[e], j);
-          const bool lower = (lane & j) == 0;
           const bool desc = ((e * 32 + lane) & k) == 0;
           const bool keep_max = (lower == desc);
           v[e] = keep_max ? (v[e] > other ? v[e] : other) : (v[e] < other ? v[e] : other);
