@@ -110,18 +110,23 @@ int sdm_scan_forward(float* M, const int32_t* idx_w, const float* sc_w, const in
                      void* stream);
 
 /* Same as sdm_scan_forward with the scan kernel's shape forced instead of chosen:
- * cols_per_cta in {4, 8, 16, 32} (d_v columns owned by one thread block, d_v % cols == 0)
- * and prefetch_depth in {1, 2, 3} (tokens of rows gathered ahead).  0 keeps the
- * automatic choice.  The state and the slots do not depend on the shape; o may differ
- * in the last bits (order of the read reduction).  `event_after_plan`, if not NULL, is
- * a cudaEvent_t recorded on `stream` between the planning kernel and the scan kernel
- * (for timing the scan kernel alone).  For tuning, tests and measurement. */
+ * cols_per_cta in {4, 8, 16, 32, 64} (d_v columns owned by one thread block,
+ * d_v % cols == 0) and prefetch_depth in {1, 2, 3} (tokens of rows gathered ahead; 64
+ * columns allow 1 or 2).  0 keeps the automatic choice.  The state and the slots do not
+ * depend on the shape; o may differ in the last bits (order of the read reduction).
+ * `wait_before_scan`, if not NULL, is a cudaEvent_t the stream waits for after the
+ * planning kernel (which does not read M) and before the scan kernel: M only has to be
+ * ready then, so work producing M (e.g. sdm_init_state_from_M0 on another stream) can
+ * overlap the selection and planning.  `event_after_plan`, if not NULL, is a cudaEvent_t
+ * recorded on `stream` right before the scan kernel (after that wait), for timing the
+ * scan kernel alone.  For tuning, tests, measurement and stream-level overlap. */
 int sdm_scan_forward_tuned(float* M, const int32_t* idx_w, const float* sc_w,
                            const int32_t* idx_r, const float* sc_r, const void* v, int v_dt,
                            const float* alpha, const float* beta, int B, int H, int T,
                            long long N, int d_v, int W, int R, float* o, void* workspace,
                            size_t workspace_bytes, int* dev_err, int cols_per_cta,
-                           int prefetch_depth, void* event_after_plan, void* stream);
+                           int prefetch_depth, void* event_after_plan, void* wait_before_scan,
+                           void* stream);
 
 /* Bytes of the fixed device scratch behind sdm_scan_forward_noalloc (64 MiB). */
 #define SDM_NOALLOC_SCRATCH_BYTES (64u << 20)

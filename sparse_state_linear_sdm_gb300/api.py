@@ -47,7 +47,7 @@ def lib() -> ctypes.CDLL:
             L.sdm_scan_workspace_size.restype = sz
             L.sdm_scan_forward.argtypes = [p, p, p, p, p, p, i, p, p, i, i, i, ll, i, i, i, p, p, sz, p, p]
             L.sdm_scan_forward_tuned.argtypes = [p, p, p, p, p, p, i, p, p, i, i, i, ll, i, i, i, p, p, sz,
-                                                 p, i, i, p, p]
+                                                 p, i, i, p, p, p]
             L.sdm_scan_launch_info.argtypes = [i, i, i, i, i, p, p, p, p]
             L.sdm_gen_inputs.argtypes = [ull, i, i, i, i, i, ll, i, i, i, f, i, p, p, p, p, p, p, p]
             L.sdm_gen_M0.argtypes = [ull, i, ll, i, f, p, p]
@@ -140,11 +140,14 @@ def scan_workspace(B, H, T, d_v, W, R, device) -> torch.Tensor:
 
 
 def scan_forward(M, idx_w, sc_w, idx_r, sc_r, v, alpha, beta, o=None, workspace=None,
-                 dev_err=None, cols_per_cta: int = 0, prefetch_depth: int = 0, event_after_plan=None):
+                 dev_err=None, cols_per_cta: int = 0, prefetch_depth: int = 0, event_after_plan=None,
+                 wait_before_scan=None):
     """Sparse gated-delta scan over T tokens, continuing from the state in M (updated in
     place).  M: fp32 [B,H,N,d_v]; idx/sc from select; v: [B,H,T,d_v] fp32/bf16;
     alpha, beta: fp32 [B,H,T].  Returns o fp32 [B,H,T,d_v].  event_after_plan: optional
-    torch.cuda.Event recorded between the planning kernel and the scan kernel."""
+    torch.cuda.Event recorded between the planning kernel and the scan kernel;
+    wait_before_scan: optional torch.cuda.Event the scan kernel (but not the planning
+    kernel, which does not read M) waits for."""
     _need(M, "M", torch.float32)
     B, H, N, dv = M.shape
     _need(idx_w, "idx_w", torch.int32)
@@ -167,10 +170,13 @@ def scan_forward(M, idx_w, sc_w, idx_r, sc_r, v, alpha, beta, o=None, workspace=
         _need(dev_err, "dev_err", torch.int32)
     if event_after_plan is not None and event_after_plan.cuda_event == 0:
         event_after_plan.record()  # torch creates its events lazily; the library records it again
+    if wait_before_scan is not None and wait_before_scan.cuda_event == 0:
+        raise ValueError("wait_before_scan must have been recorded")
     _call("sdm_scan_forward_tuned", _p(M), _p(idx_w), _p(sc_w), _p(idx_r), _p(sc_r), _p(v),
           _dtype_code(v), _p(alpha), _p(beta), B, H, T, N, dv, W, R, _p(o), _p(workspace),
           workspace.numel(), _p(dev_err), int(cols_per_cta), int(prefetch_depth),
           None if event_after_plan is None else ctypes.c_void_p(event_after_plan.cuda_event),
+          None if wait_before_scan is None else ctypes.c_void_p(wait_before_scan.cuda_event),
           _stream(M.device))
     return o
 
@@ -255,15 +261,47 @@ def gen_M0(seed: int, H: int, N: int, d_v: int, scale: float = 0.02, device="cud
     return out
 
 
-def forward(kp, qp, v, alpha, beta, M0, W: int, R: int, M=None, workspace=None, dev_err=None):
+_side_streams = {}
+
+
+def side_stream(device) -> torch.cuda.Stream:
+    """A second stream per device, used to overlap the state initialisation (HBM writes)
+    with the selection (compare/select work); created once."""
+    dev = torch.device(device)
+    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    if key not in _side_streams:
+        _side_streams[key] = torch.cuda.Stream(device=key)
+    return _side_streams[key]
+
+
+def forward(kp, qp, v, alpha, beta, M0, W: int, R: int, M=None, workspace=None, dev_err=None,
+            overlap: bool = True, out=None, o=None):
     """One SDM forward pass over a batch: state from M0, selection, scan.
 
-    Returns (o, M, (idx_w, sc_w, idx_r, sc_r))."""
+    With overlap, M is initialised on a side stream while the current stream runs the
+    selection and the planning pass; the scan kernel waits for both.  The result is the
+    same either way.  Returns (o, M, (idx_w, sc_w, idx_r, sc_r))."""
     B, H, T, _, S = kp.shape
     dv = M0.shape[-1]
     if M is None:
         M = torch.empty((B, H, S * S, dv), dtype=torch.float32, device=kp.device)
-    init_state_from_M0(M, M0)
-    sel = select(kp, qp, W, R)
-    o = scan_forward(M, *sel, v, alpha, beta, workspace=workspace, dev_err=dev_err)
+    if not overlap:
+        init_state_from_M0(M, M0)
+        sel = select(kp, qp, W, R, out=out)
+        o = scan_forward(M, *sel, v, alpha, beta, o=o, workspace=workspace, dev_err=dev_err)
+        return o, M, sel
+    main = torch.cuda.current_stream(M.device)
+    side = side_stream(M.device)
+    free = torch.cuda.Event()
+    free.record(main)                      # earlier work on M (and M0) is ordered before
+    side.wait_event(free)
+    with torch.cuda.stream(side):
+        init_state_from_M0(M, M0)
+    M.record_stream(side)
+    M0.record_stream(side)
+    init_done = torch.cuda.Event()
+    init_done.record(side)
+    sel = select(kp, qp, W, R, out=out)
+    o = scan_forward(M, *sel, v, alpha, beta, o=o, workspace=workspace, dev_err=dev_err,
+                     wait_before_scan=init_done)
     return o, M, sel

@@ -75,7 +75,8 @@ int sdm_scan_forward_tuned(float* M, const int32_t* idx_w, const float* sc_w,
                            const float* alpha, const float* beta, int B, int H, int T,
                            long long N, int d_v, int W, int R, float* o, void* workspace,
                            size_t workspace_bytes, int* dev_err, int cols_per_cta,
-                           int prefetch_depth, void* event_after_plan, void* stream) {
+                           int prefetch_depth, void* event_after_plan, void* wait_before_scan,
+                           void* stream) {
   int st = check_scan_args(M, idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, B, H, T, N, d_v, W,
                            R, o);
   if (st != SDM_OK) return st;
@@ -89,7 +90,7 @@ int sdm_scan_forward_tuned(float* M, const int32_t* idx_w, const float* sc_w,
   if (st != SDM_OK) return st;
   return launch_scan(M, idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, B * H, T, N, d_v, W, R, o,
                      workspace, dev_err, shape, reinterpret_cast<cudaEvent_t>(event_after_plan),
-                     as_stream(stream));
+                     reinterpret_cast<cudaEvent_t>(wait_before_scan), as_stream(stream));
 }
 
 int sdm_scan_forward(float* M, const int32_t* idx_w, const float* sc_w, const int32_t* idx_r,
@@ -98,7 +99,8 @@ int sdm_scan_forward(float* M, const int32_t* idx_w, const float* sc_w, const in
                      float* o, void* workspace, size_t workspace_bytes, int* dev_err,
                      void* stream) {
   return sdm_scan_forward_tuned(M, idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, B, H, T, N, d_v,
-                                W, R, o, workspace, workspace_bytes, dev_err, 0, 0, nullptr, stream);
+                                W, R, o, workspace, workspace_bytes, dev_err, 0, 0, nullptr, nullptr,
+                                stream);
 }
 
 int sdm_scan_launch_info(int B, int H, int d_v, int W, int R, int* cols_per_cta,

@@ -75,7 +75,8 @@ int choose_scan_shape(int BH, int d_v, int W, int R, int force_cols, int force_p
 int launch_scan(float* M, const int32_t* idx_w, const float* sc_w, const int32_t* idx_r,
                 const float* sc_r, const void* v, int v_dt, const float* alpha, const float* beta,
                 int BH, int T, long long N, int d_v, int W, int R, float* o, void* workspace,
-                int* dev_err, const ScanShape& shape, cudaEvent_t after_plan, cudaStream_t s);
+                int* dev_err, const ScanShape& shape, cudaEvent_t after_plan,
+                cudaEvent_t wait_before_scan, cudaStream_t s);
 
 int launch_gen_inputs(unsigned long long seed, int B, int H, int T, int b_off, int t_off,
                       long long T_total, int S, int d_v, int in_dt, float alpha_lo,

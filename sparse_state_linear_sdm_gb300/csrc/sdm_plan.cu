@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   }
   __syncthreads();
 
+  int errs = 0;  // SDM_DEV_* bits seen by this thread, reported once at the end
   for (int u = t0; u < t1; ++u) {
     unsigned char* rec = a.rec + (tok0 + u) * size_t(a.L.bytes);
     for (int e = tid; e < WR; e += kPlanThreads) {
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
       if (x < 0 || x >= a.N) {
         code = -2;
         x = 0;
-        if (a.dev_err) atomicOr(a.dev_err, SDM_DEV_INDEX_RANGE);
+        errs |= SDM_DEV_INDEX_RANGE;
       } else {
         const uint32_t fb = filter_bit(x);
         if ((filter[fb >> 5] >> (fb & 31)) & 1u) {
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
             if (v == kEmpty) break;
             if (uint32_t(v >> 32) != uint32_t(x)) continue;
             const int tt = tl + int((v >> 16) & 0xFFFFu), pp = int(v & 0xFFFFu);
-            if (e < W && tt == u && pp != e && a.dev_err) atomicOr(a.dev_err, SDM_DEV_DUP_WRITE);
+            if (e < W && tt == u && pp != e) errs |= SDM_DEV_DUP_WRITE;
             const bool earlier = e < W ? tt < u : tt <= u;
             if (earlier && tt >= u - a.pd && tt > best_t) {
               best_t = tt;
@@ -158,6 +159,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
       reinterpret_cast<int16_t*>(rec + a.L.off_src)[e] = int16_t(code);
     }
   }
+
+  if (errs && a.dev_err) atomicOr(a.dev_err, errs);
 
   // Weights, gates and v for each token of the chunk: one warp per token.
   const int warp = tid >> 5, lane = tid & 31;

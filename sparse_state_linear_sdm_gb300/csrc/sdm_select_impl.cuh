@@ -158,14 +158,6 @@ __device__ __forceinline__ void find_bucket(const uint32_t* hist, int need, int&
 }
 
 template <typename Key>
-__device__ __forceinline__ int first_diff_shift(Key mx, Key mn) {
-  const Key diff = mx ^ mn;
-  const int top = int(sizeof(Key) * 8) - 1 -
-                  (sizeof(Key) == 8 ? __clzll((long long)diff) : __clz(int(uint32_t(diff))));
-  return (top / 8) * 8;
-}
-
-template <typename Key>
 __device__ __forceinline__ void warp_minmax(Key& mx, Key& mn) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -175,15 +167,22 @@ __device__ __forceinline__ void warp_minmax(Key& mx, Key& mn) {
   }
 }
 
-// Selects the `need` largest of the n distinct keys in buf[0..n) and writes them,
-// unordered, to out[0..need).  buf is scratch: each radix pass keeps only the keys of
-// the bucket that holds the need-th largest, compacted in place, so only the first
-// pass touches all n keys.  `shift` is the first digit to use (< 0: found from the
-// keys' range); with hist_ready the histogram of that digit is already in hist.  Once a
-// bucket fits in one key per lane, the next digit is the first one where its keys differ.
+// Bits needed to hold `range` (0 for 0).
 template <typename Key>
-__device__ void warp_topk_from(Key* buf, int n, int need, Key* out, uint32_t* hist, int shift,
-                               bool hist_ready) {
+__device__ __forceinline__ int bit_length(Key range) {
+  return int(sizeof(Key) * 8) -
+         (sizeof(Key) == 8 ? __clzll((long long)range) : __clz(int(uint32_t(range))));
+}
+
+// Selects the `need` largest of the n distinct keys in buf[0..n) and writes them,
+// unordered, to out[0..need).  MSB-first radix select on the offset (key - base) with
+// 8-bit digits d = (key - base) >> shift: each pass keeps only the bucket that holds the
+// need-th largest (compacted in place in buf) and narrows the window by 8 bits, so only
+// the first pass touches all n keys.  shift < 0: base and shift are fitted to the keys'
+// range first.  With hist_ready the first pass's histogram is already in hist.
+template <typename Key>
+__device__ void warp_topk_from(Key* buf, int n, int need, Key* out, uint32_t* hist, Key base,
+                               int shift, bool hist_ready) {
   const int lane = threadIdx.x & 31;
   if (need >= n) {
     for (int i = lane; i < n; i += 32) out[i] = buf[i];
@@ -198,14 +197,17 @@ __device__ void warp_topk_from(Key* buf, int n, int need, Key* out, uint32_t* hi
       mn = k < mn ? k : mn;
     }
     warp_minmax(mx, mn);
-    shift = first_diff_shift(mx, mn);  // n >= 2 distinct keys: they differ somewhere
+    base = mn;
+    const int bits = bit_length<Key>(mx - mn);
+    shift = bits > 8 ? bits - 8 : 0;
+    hist_ready = false;
   }
   int n_out = 0;
   for (;;) {
     if (!hist_ready) {
       for (int b = lane; b < 256; b += 32) hist[b] = 0u;
       __syncwarp();
-      for (int i = lane; i < n; i += 32) atomicAdd(&hist[unsigned(buf[i] >> shift) & 255u], 1u);
+      for (int i = lane; i < n; i += 32) atomicAdd(&hist[unsigned((buf[i] - base) >> shift)], 1u);
       __syncwarp();
     }
     hist_ready = false;
@@ -217,12 +219,12 @@ __device__ void warp_topk_from(Key* buf, int n, int need, Key* out, uint32_t* hi
     for (int i0 = 0; i0 < n; i0 += 32) {
       const int i = i0 + lane;
       Key k = 0;
-      unsigned dg = 0;
+      int dg = -1;
       if (i < n) {
         k = buf[i];
-        dg = unsigned(k >> shift) & 255u;
+        dg = int((k - base) >> shift);
       }
-      const bool up = i < n && int(dg) > digit, eq = i < n && int(dg) == digit;
+      const bool up = dg > digit, eq = dg == digit;
       const unsigned mu = __ballot_sync(kFull, up), me = __ballot_sync(kFull, eq);
       const unsigned lt = (1u << lane) - 1u;
       if (up) out[base_up + __popc(mu & lt)] = k;
@@ -239,14 +241,9 @@ __device__ void warp_topk_from(Key* buf, int n, int need, Key* out, uint32_t* hi
       __syncwarp();
       return;
     }
-    // >= 2 distinct keys share the digit, so a lower digit separates them.
-    if (n <= 32) {
-      Key mx = buf[lane < n ? lane : 0], mn = mx;
-      warp_minmax(mx, mn);
-      shift = first_diff_shift(mx, mn);
-    } else {
-      shift -= 8;
-    }
+    // >= 2 distinct keys share the digit, so the window is wider than one key: narrow it.
+    base += Key(digit) << shift;
+    shift = shift >= 8 ? shift - 8 : 0;
   }
 }
 
@@ -423,10 +420,15 @@ __device__ __forceinline__ void load_half_keys(const Tin* src, int S, bool vec,
 
 // Shared memory of one warp: key buffer (one half, its bucket, or the staircase
 // candidates), the selected keys, the histogram and the two inner lists.
-__host__ __device__ inline size_t select_per_warp_bytes(int kpad, int kin_max, int S, int cnt_max,
-                                                        int inner_key_bytes) {
+__host__ __device__ inline size_t select_key_bytes(int kpad, int S, int cnt_max, int inner_key_bytes) {
   size_t keys = size_t(S) * inner_key_bytes;
   if (size_t(cnt_max) * 8 > keys) keys = size_t(cnt_max) * 8;
+  return (keys + 15) / 16 * 16;
+}
+
+__host__ __device__ inline size_t select_per_warp_bytes(int kpad, int kin_max, int S, int cnt_max,
+                                                        int inner_key_bytes) {
+  size_t keys = select_key_bytes(kpad, S, cnt_max, inner_key_bytes);
   keys = (keys + 15) / 16 * 16;
   const size_t b = keys + size_t(kpad) * 8 + 256 * 4 + size_t(kin_max) * 16;
   return (b + 15) / 16 * 16;
@@ -515,7 +517,7 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
       IKey* ik = reinterpret_cast<IKey*>(keys);
       IKey* io = reinterpret_cast<IKey*>(out);
       load_half_keys<Tin>(halves + (long long)h * S, S, a.vec, ik, hist);
-      warp_topk_from<IKey>(ik, S, kin, io, hist, InnerKeyOf<Tin>::top_shift, true);
+      warp_topk_from<IKey>(ik, S, kin, io, hist, IKey(0), InnerKeyOf<Tin>::top_shift, true);
       sort_desc_upto<IKey, EMAX>(io, kin);
       float* dv = h ? bval : aval;
       int32_t* di = h ? bidx : aidx;
@@ -537,6 +539,7 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
     };
     uint64_t* ck = reinterpret_cast<uint64_t*>(keys);
     int shift = 0;
+    uint64_t base = 0;
     if (cnt > K) {
       // The largest staircase key is (0, 0); the smallest is the end of some row.
       uint64_t mx = pair_key(0, 0), mn = ~0ull;
@@ -545,7 +548,9 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
         mn = k < mn ? k : mn;
       }
       warp_minmax(mx, mn);
-      shift = first_diff_shift(mx, mn);
+      base = mn;
+      const int bits = bit_length<uint64_t>(mx - mn);
+      shift = bits > 8 ? bits - 8 : 0;
       for (int b = lane; b < 256; b += 32) hist[b] = 0u;
       __syncwarp();
     }
@@ -553,10 +558,10 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
       const uint32_t pq = st[c];
       const uint64_t k = pair_key(int(pq >> 16), int(pq & 0xFFFFu));
       ck[c] = k;
-      if (cnt > K) atomicAdd(&hist[unsigned(k >> shift) & 255u], 1u);
+      if (cnt > K) atomicAdd(&hist[unsigned((k - base) >> shift)], 1u);
     }
     __syncwarp();
-    warp_topk_from<uint64_t>(ck, cnt, K, out, hist, shift, true);
+    warp_topk_from<uint64_t>(ck, cnt, K, out, hist, base, shift, true);
     sort_desc_upto<uint64_t, EMAX>(out, K);
     const uint64_t kth = out[K - 1];
     const uint32_t kth_sum = uint32_t(kth >> 32);
@@ -607,9 +612,7 @@ int launch_select_t(const void* kp, const void* qp, long long items, int S, int 
   a.idx_r = idx_r;
   a.sc_r = sc_r;
   const int ikb = kBf16 ? 4 : 8;
-  size_t keys = size_t(S) * ikb;
-  if (size_t(max(a.cnt_w, a.cnt_r)) * 8 > keys) keys = size_t(max(a.cnt_w, a.cnt_r)) * 8;
-  a.keys_bytes = (keys + 15) / 16 * 16;
+  a.keys_bytes = select_key_bytes(a.kpad, S, max(a.cnt_w, a.cnt_r), ikb);
   const size_t stair_bytes = (size_t(a.cnt_w + a.cnt_r) * 4 + 15) / 16 * 16;
   const size_t per_warp = select_per_warp_bytes(a.kpad, a.kin_max, S, max(a.cnt_w, a.cnt_r), ikb);
   int dev = 0, max_smem = 0, sms = 0;

@@ -76,7 +76,7 @@ def test_scan_rejects_bad_arguments_without_launching():
 
     def call(B=1, H=1, T=8, N=64, dv=16, W=4, R=4, v_dt=0, M=FAKE, ws=FAKE, ws_bytes=1 << 30, cols=0, pd=0):
         return lib.sdm_scan_forward_tuned(M, FAKE, FAKE, FAKE, FAKE, FAKE, v_dt, FAKE, FAKE, B, H, T, N, dv, W,
-                                          R, FAKE, ws, ws_bytes, None, cols, pd, None, None)
+                                          R, FAKE, ws, ws_bytes, None, cols, pd, None, None, None)
 
     assert call(dv=6) == EINVAL
     assert call(dv=0) == EINVAL
