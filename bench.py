@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--cols", type=int, default=0, help="force scan columns per block (0 = auto)")
     ap.add_argument("--pd", type=int, default=0, help="force scan prefetch depth (0 = auto)")
     ap.add_argument("--override", default="", help="size overrides for profiling, e.g. S=256,T=512")
+    ap.add_argument("--mode", choices=["forward", "decode"], default="forward",
+                    help="decode: one token per step for the batch, state resident, CUDA graph")
     return ap.parse_args()
 
 
@@ -440,10 +442,59 @@ def e2e(st, cfg, sdm, args, dev, torch, K, world):
                         "overlap step k's compute (copy stream)"}
 
 
+def run_decode(args):
+    """Single-token decode for a batch of sequences with resident state: K tokens, one
+    CUDA-graph replay (selection, planning, scan) per token."""
+    import torch
+
+    import sparse_state_linear_sdm_gb300 as sdm
+    from sparse_state_linear_sdm_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = workload(args)
+    K = max(args.steps, 50)
+    st = make_state(dataclasses_replace(cfg, T=K + args.warmup), rank, dev, torch, sdm, wl)
+    sdm.init_state_from_M0(st["M"], st["M0"])
+    step = sdm.DecodeStep(st["M"], cfg.W, cfg.R, in_dtype=st["kp"].dtype).capture()
+
+    def token(t):
+        return step(st["kp"][:, :, t:t + 1], st["qp"][:, :, t:t + 1], st["v"][:, :, t:t + 1],
+                    st["alpha"][:, :, t:t + 1], st["beta"][:, :, t:t + 1])
+
+    for t in range(args.warmup):
+        token(t)
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for t in range(args.warmup, args.warmup + K):
+        token(t)
+    b.record()
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / K
+    state_bytes = cfg.B * cfg.H * (2 * cfg.W + cfg.R) * cfg.d_v * 4
+    line = {"metric": "SDM decode head-tokens/s (one token per step, state resident)",
+            "value": cfg.B * cfg.H / (ms / 1e3), "unit": "head-tokens/s", "n_gpus": 1, "steps": K,
+            "warmup": args.warmup, "us_per_step": ms * 1e3, "higher_is_better": True, "dtype": "f32",
+            "data": "synthetic", "config": dict(config_dict(cfg), T=1, step="decode: CUDA graph of select + plan + scan"),
+            "state_bytes_per_step": state_bytes, "state_gbs": state_bytes / (ms / 1e3) / 1e9,
+            "gpu_launches": 3 * K}
+    print(json.dumps(line), flush=True)
+
+
+def dataclasses_replace(cfg, **kw):
+    import dataclasses
+
+    return dataclasses.replace(cfg, **kw)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.mode == "decode":
+        run_decode(args)
     else:
         run_ours(args)
 

@@ -305,3 +305,76 @@ def forward(kp, qp, v, alpha, beta, M0, W: int, R: int, M=None, workspace=None, 
     o = scan_forward(M, *sel, v, alpha, beta, o=o, workspace=workspace, dev_err=dev_err,
                      wait_before_scan=init_done)
     return o, M, sel
+
+
+class DecodeStep:
+    """One-token decode step for a batch of sequences with resident state, captured once
+    into a CUDA graph (selection, planning and scan kernels) and replayed per token.
+
+    The state M [B, H, N, d_v] stays in place across steps; each step takes k', q' halves
+    [B, H, 1, 2, S], v [B, H, 1, d_v] and alpha, beta [B, H, 1] (copied into the graph's
+    static input buffers) and returns o [B, H, 1, d_v] (the graph's static output buffer:
+    copy it before the next step if it must be kept).  Chaining steps gives exactly the
+    result of one scan over the same tokens."""
+
+    def __init__(self, M, W: int, R: int, in_dtype=torch.bfloat16, S=None):
+        B, H, N, dv = M.shape
+        S = int(round(N ** 0.5)) if S is None else S
+        if S * S != N:
+            raise ValueError("N must be a square")
+        dev = M.device
+        self.M, self.W, self.R = M, W, R
+        self.kp = torch.zeros((B, H, 1, 2, S), dtype=in_dtype, device=dev)
+        self.qp = torch.zeros_like(self.kp)
+        self.v = torch.zeros((B, H, 1, dv), dtype=in_dtype, device=dev)
+        self.alpha = torch.ones((B, H, 1), dtype=torch.float32, device=dev)
+        self.beta = torch.zeros((B, H, 1), dtype=torch.float32, device=dev)
+        self.sel = (torch.empty((B, H, 1, W), dtype=torch.int32, device=dev),
+                    torch.empty((B, H, 1, W), dtype=torch.float32, device=dev),
+                    torch.empty((B, H, 1, R), dtype=torch.int32, device=dev),
+                    torch.empty((B, H, 1, R), dtype=torch.float32, device=dev))
+        self.o = torch.empty((B, H, 1, dv), dtype=torch.float32, device=dev)
+        self.ws = scan_workspace(B, H, 1, dv, W, R, dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.graph = None
+
+    def _body(self):
+        select(self.kp, self.qp, self.W, self.R, out=self.sel)
+        scan_forward(self.M, *self.sel, self.v, self.alpha, self.beta, o=self.o, workspace=self.ws,
+                     dev_err=self.err)
+
+    def capture(self):
+        """Capture the step (selection, planning, scan) into a CUDA graph.  Beforehand the
+        same kernels run once on a small dummy problem with the same (B, H, d_v, W, R), so
+        that they are loaded and configured outside the capture; the real state is not
+        touched until the graph is replayed."""
+        B, H, N, dv = self.M.shape
+        dev = self.M.device
+        s = 1
+        while s * s < max(self.W, self.R):
+            s += 1
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            kp = torch.zeros((B, H, 1, 2, s), dtype=self.kp.dtype, device=dev)
+            sel = select(kp, kp, self.W, self.R)
+            Md = torch.zeros((B, H, s * s, dv), dtype=torch.float32, device=dev)
+            scan_forward(Md, *sel, self.v, self.alpha, self.beta)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize(dev)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._body()
+        return self
+
+    def __call__(self, kp, qp, v, alpha, beta):
+        self.kp.copy_(kp, non_blocking=True)
+        self.qp.copy_(qp, non_blocking=True)
+        self.v.copy_(v, non_blocking=True)
+        self.alpha.copy_(alpha, non_blocking=True)
+        self.beta.copy_(beta, non_blocking=True)
+        if self.graph is None:
+            self._body()
+        else:
+            self.graph.replay()
+        return self.o
