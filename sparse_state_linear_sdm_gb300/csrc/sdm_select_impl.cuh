@@ -180,9 +180,13 @@ __device__ __forceinline__ int bit_length(Key range) {
 // need-th largest (compacted in place in buf) and narrows the window by 8 bits, so only
 // the first pass touches all n keys.  shift < 0: base and shift are fitted to the keys'
 // range first.  With hist_ready the first pass's histogram is already in hist.
+// tie_shift >= 0 declares that the key bits below tie_shift are a position written so
+// that, among keys equal above it, larger keys come earlier in buf (and base is a
+// multiple of 1 << tie_shift): once a pass at that shift leaves a bucket of keys equal
+// above it, its first `need` keys are the largest and the search stops there.
 template <typename Key>
 __device__ void warp_topk_from(Key* buf, int n, int need, Key* out, uint32_t* hist, Key base,
-                               int shift, bool hist_ready) {
+                               int shift, bool hist_ready, int tie_shift = -1) {
   const int lane = threadIdx.x & 31;
   if (need >= n) {
     for (int i = lane; i < n; i += 32) out[i] = buf[i];
@@ -236,8 +240,9 @@ __device__ void warp_topk_from(Key* buf, int n, int need, Key* out, uint32_t* hi
     n_out += int(above);
     need -= int(above);
     n = int(cnt);
-    if (n == need) {
-      for (int i = lane; i < n; i += 32) out[n_out + i] = buf[i];
+    if (n == need || shift == tie_shift) {
+      // The bucket keeps buf's order (the compaction is stable).
+      for (int i = lane; i < need; i += 32) out[n_out + i] = buf[i];
       __syncwarp();
       return;
     }
@@ -517,7 +522,9 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
       IKey* ik = reinterpret_cast<IKey*>(keys);
       IKey* io = reinterpret_cast<IKey*>(out);
       load_half_keys<Tin>(halves + (long long)h * S, S, a.vec, ik, hist);
-      warp_topk_from<IKey>(ik, S, kin, io, hist, IKey(0), InnerKeyOf<Tin>::top_shift, true);
+      // ik is in index order and the low 16 key bits are 0xFFFF - index: equal values
+      // are already ranked by position once the value bits are resolved.
+      warp_topk_from<IKey>(ik, S, kin, io, hist, IKey(0), InnerKeyOf<Tin>::top_shift, true, 16);
       sort_desc_upto<IKey, EMAX>(io, kin);
       float* dv = h ? bval : aval;
       int32_t* di = h ? bidx : aidx;

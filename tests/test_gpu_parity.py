@@ -274,3 +274,22 @@ def test_empty_sequence_is_a_no_op():
     o = sdm.scan_forward(M, e, s, e, s, torch.empty(1, 1, 0, 8, device="cuda"),
                          torch.empty(1, 1, 0, device="cuda"), torch.empty(1, 1, 0, device="cuda"))
     assert o.shape == (1, 1, 0, 8) and torch.equal(M, before)
+
+
+def test_overlapped_forward_waits_for_earlier_work_on_the_state():
+    """forward(overlap=True) initialises M on a side stream: that stream must first wait for
+    work already queued on the caller's stream.  A delayed copy of M queued there must
+    still see the finished state, not the next call's initialisation."""
+    cfg = wl.CONFIGS[1]
+    d = device_inputs(cfg)
+    M0 = device_M0(cfg)
+    _, ref, _ = sdm.forward(d["kp"], d["qp"], d["v"], d["alpha"], d["beta"], M0, cfg.W, cfg.R, overlap=False)
+    torch.cuda.synchronize()
+    M = torch.empty_like(ref)
+    sdm.forward(d["kp"], d["qp"], d["v"], d["alpha"], d["beta"], M0, cfg.W, cfg.R, M=M)
+    torch.cuda._sleep(50_000_000)  # keeps the caller's stream busy for tens of milliseconds
+    snap = M.clone()
+    sdm.forward(d["kp"], d["qp"], d["v"], d["alpha"], d["beta"], M0, cfg.W, cfg.R, M=M)
+    torch.cuda.synchronize()
+    assert torch.equal(snap, ref)
+    assert torch.equal(M, ref)
