@@ -178,7 +178,8 @@ __device__ __forceinline__ int bit_length(Key range) {
 // unordered, to out[0..need).  MSB-first radix select on the offset (key - base) with
 // 8-bit digits d = (key - base) >> shift: each pass keeps only the bucket that holds the
 // need-th largest (compacted in place in buf) and narrows the window by 8 bits, so only
-// the first pass touches all n keys.  shift < 0: base and shift are fitted to the keys'
+// the first pass touches all n keys; a bucket of at most 32 keys is finished by ranking
+// its keys against each other.  shift < 0: base and shift are fitted to the keys'
 // range first.  With hist_ready the first pass's histogram is already in hist.
 // tie_shift >= 0 declares that the key bits below tie_shift are a position written so
 // that, among keys equal above it, larger keys come earlier in buf (and base is a
@@ -243,6 +244,19 @@ __device__ void warp_topk_from(Key* buf, int n, int need, Key* out, uint32_t* hi
     if (n == need || shift == tie_shift) {
       // The bucket keeps buf's order (the compaction is stable).
       for (int i = lane; i < need; i += 32) out[n_out + i] = buf[i];
+      __syncwarp();
+      return;
+    }
+    if (n <= 32) {
+      // Small bucket: rank its (distinct) keys directly, one per lane, instead of more
+      // 8-bit passes (ties in value or sum leave only index bits to resolve).
+      const Key mine = lane < n ? buf[lane] : Key(0);
+      int rank = 0;
+      for (int j = 0; j < n; ++j) {
+        const Key kj = __shfl_sync(kFull, mine, j);
+        rank += kj > mine ? 1 : 0;
+      }
+      if (lane < n && rank < need) out[n_out + rank] = mine;
       __syncwarp();
       return;
     }
@@ -548,15 +562,22 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
     int shift = 0;
     uint64_t base = 0;
     if (cnt > K) {
-      // The largest staircase key is (0, 0); the smallest is the end of some row.
-      uint64_t mx = pair_key(0, 0), mn = ~0ull;
+      // Digit window: (0, 0) has the largest sum and some row end the smallest (sums fall
+      // along rows and columns).  The flat tie-break can order keys of equal sums either
+      // way, so the window spans those sums with every flat: no key falls outside it.
+      uint32_t lo = ~0u;
       for (int p = lane; p < kin; p += 32) {
-        const uint64_t k = pair_key(p, min(kin, K / (p + 1)) - 1);
-        mn = k < mn ? k : mn;
+        const uint32_t k = ord_key(__fadd_rn(aval[p], bval[min(kin, K / (p + 1)) - 1]));
+        lo = k < lo ? k : lo;
       }
-      warp_minmax(mx, mn);
-      base = mn;
-      const int bits = bit_length<uint64_t>(mx - mn);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const uint32_t o = __shfl_xor_sync(kFull, lo, off);
+        lo = o < lo ? o : lo;
+      }
+      const uint64_t mx = (uint64_t(ord_key(__fadd_rn(aval[0], bval[0]))) << 32) | 0xFFFFFFFFull;
+      base = uint64_t(lo) << 32;
+      const int bits = bit_length<uint64_t>(mx - base);
       shift = bits > 8 ? bits - 8 : 0;
       for (int b = lane; b < 256; b += 32) hist[b] = 0u;
       __syncwarp();

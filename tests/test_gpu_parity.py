@@ -69,16 +69,36 @@ def _tie_heavy(rng, shape):
     return vals[rng.integers(0, len(vals), size=shape)]
 
 
+def _rounding_merges(rng, shape, kind):
+    """Halves whose fp32 pair sums collapse: one half far larger than the other, so a whole
+    row of sums rounds to one value and the flat index alone orders it (which half is the
+    large one alternates by token)."""
+    n, S = shape[2], shape[4]
+    x = np.empty(shape, np.float32)
+    for t in range(n):
+        if kind == "merge_f32":   # distinct even integers near 2^24 (fp32 spacing 2) + |u| < 1
+            big = (2.0 ** 24 + 2.0 * rng.permutation(S)).astype(np.float32)
+            small = rng.uniform(-0.9, 0.9, S).astype(np.float32)
+        else:                     # Gaussian scores at scales 1e4 and 1e-4
+            big = (1e4 * rng.standard_normal(S)).astype(np.float32)
+            small = (1e-4 * rng.standard_normal(S)).astype(np.float32)
+        x[0, 0, t, t % 2], x[0, 0, t, 1 - t % 2] = big, small
+    return x
+
+
 @pytest.mark.parametrize("S,W,R", [(1, 1, 1), (2, 4, 3), (3, 5, 9), (5, 7, 2), (8, 8, 64), (16, 40, 16),
                                    (17, 33, 5), (32, 8, 8), (64, 100, 64), (100, 128, 1), (256, 32, 200),
                                    (1024, 128, 128), (40, 1024, 512)])
-@pytest.mark.parametrize("kind", ["ties_f32", "gauss_bf16", "gauss_f32"])
+@pytest.mark.parametrize("kind", ["ties_f32", "gauss_bf16", "gauss_f32", "merge_f32", "scaled_f32"])
 def test_select_matches_oracle(S, W, R, kind):
     rng = np.random.default_rng(S * 1000 + W * 7 + R)
     n = 37
     shape = (1, 1, n, 2, S)
     if kind == "ties_f32":
         kp, qp = _tie_heavy(rng, shape), _tie_heavy(rng, shape)
+        dt = torch.float32
+    elif kind in ("merge_f32", "scaled_f32"):
+        kp, qp = _rounding_merges(rng, shape, kind), _rounding_merges(rng, shape, kind)
         dt = torch.float32
     else:
         kp = rng.standard_normal(shape).astype(np.float32)
