@@ -204,7 +204,7 @@ def make_state(cfg, rank, dev, torch, sdm, wl):
     st["o"] = torch.empty(sh + (cfg.d_v,), dtype=torch.float32, device=dev)
     st["ws"] = sdm.scan_workspace(cfg.B, cfg.H, cfg.T, cfg.d_v, cfg.W, cfg.R, dev)
     st["err"] = torch.zeros(1, dtype=torch.int32, device=dev)
-    st["side"] = torch.cuda.Stream(device=dev)
+    st["side"] = sdm.side_stream(dev)  # high priority: init shares the SMs with the selection
     return st
 
 
@@ -395,6 +395,17 @@ def e2e(st, cfg, sdm, args, dev, torch, K, world):
     copy = torch.cuda.Stream(device=dev)
     main = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
+    # This host's copy rates, alone (context for the streamed number: the loop is copy bound
+    # when h2d_bytes_per_step / H2D rate exceeds the device step).
+    rates = {}
+    for label, dst, src in (("h2d_gbs_alone", bufs[1]["kp"], host["kp"]), ("d2h_gbs_alone", o_host[1], outs[0])):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(copy):
+            a.record(copy)
+            dst.copy_(src, non_blocking=True)
+            b.record(copy)
+        torch.cuda.synchronize(dev)
+        rates[label] = round(src.numel() * src.element_size() / a.elapsed_time(b) / 1e6, 1)
 
     def run(n):
         ready = [torch.cuda.Event() for _ in range(n + 1)]
@@ -426,7 +437,7 @@ def e2e(st, cfg, sdm, args, dev, torch, K, world):
 
     run(2)
     torch.cuda.synchronize(dev)
-    n = max(2, min(K, 10))
+    n = max(2, K)  # the pipeline fill (first step's copies) is amortised over K steps
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         import torch.distributed as dist
@@ -437,7 +448,7 @@ def e2e(st, cfg, sdm, args, dev, torch, K, world):
     torch.cuda.synchronize(dev)
     ms = max_over_ranks(a.elapsed_time(b), dev)
     return {"value": whole_job_rate(cfg.B * cfg.H * cfg.T, n, world, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms / n,
+            "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms / n, **rates,
             "pipeline": "double-buffered: step k+1's host->device copies and step k's device->host copy "
                         "overlap step k's compute (copy stream)"}
 

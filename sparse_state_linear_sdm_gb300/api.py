@@ -266,11 +266,13 @@ _side_streams = {}
 
 def side_stream(device) -> torch.cuda.Stream:
     """A second stream per device, used to overlap the state initialisation (HBM writes)
-    with the selection (compare/select work); created once."""
+    with the selection (compare/select work); created once.  It has high priority: the
+    selection kernel queues many short blocks, and without priority the initialisation's
+    blocks would only get SM slots once that queue drained."""
     dev = torch.device(device)
     key = dev.index if dev.index is not None else torch.cuda.current_device()
     if key not in _side_streams:
-        _side_streams[key] = torch.cuda.Stream(device=key)
+        _side_streams[key] = torch.cuda.Stream(device=key, priority=-1)
     return _side_streams[key]
 
 

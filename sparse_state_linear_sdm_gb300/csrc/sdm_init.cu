@@ -2,8 +2,12 @@
 // summary, gist.science/it/paper/2607.07386, "Stato Iniziale Appreso": M_0 is a
 // learnable parameter that every sequence starts from).
 // M[b, h] = M0[h]: each 16-byte chunk of M0 is read once and stored B times, so the
-// HBM traffic is exactly |M0| read + |M| written.  Pure bandwidth; grid sized to the
-// SM count.
+// HBM traffic is exactly |M0| read + |M| written.  Pure bandwidth.
+//
+// The kernel is meant to run beside the selection kernel (another stream), so it takes
+// little of each SM: one block per SM (which already saturates HBM writes), and the
+// SM's shared memory left at its maximum split, so that selection blocks (tens of KB
+// of shared memory each) can start on the same SM without waiting for it to drain.
 #include "sdm_internal.cuh"
 
 namespace sdm {
@@ -29,7 +33,11 @@ int launch_init_state(float* M, const float* M0, int B, int H, long long N, int 
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return SDM_ECUDA;
-  size_t blocks = size_t(sms) * 8;
+  if (cudaFuncSetAttribute(reinterpret_cast<const void*>(&init_state_kernel),
+                           cudaFuncAttributePreferredSharedMemoryCarveout,
+                           int(cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+    return SDM_ECUDA;
+  size_t blocks = size_t(sms);
   const size_t need = (per_batch4 + 255) / 256;
   if (blocks > need) blocks = need;
   init_state_kernel<<<unsigned(blocks), 256, 0, s>>>(reinterpret_cast<float4*>(M),

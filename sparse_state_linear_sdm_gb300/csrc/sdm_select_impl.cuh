@@ -462,6 +462,7 @@ struct SelectArgs {
   int kpad;      // max(W, R, 32) rounded up to a power of two (selected-key buffer)
   int cnt_w, cnt_r;
   int warps;
+  int tpw;            // consecutive tasks per warp
   size_t keys_bytes;  // per-warp key buffer
   bool vec;           // every half starts on a 16-byte boundary
   int32_t* idx_w;
@@ -471,14 +472,30 @@ struct SelectArgs {
 };
 
 // Fills the staircase {(p, q): p, q < kin, (p+1)(q+1) <= K} as p << 16 | q, row by row.
-__device__ void build_stair(uint32_t* st, int K, int kin) {
-  // Row offsets are data independent: thread p computes its own with a short loop.
-  for (int p = threadIdx.x; p < kin; p += blockDim.x) {
-    int off = 0;
-    for (int r = 0; r < p; ++r) off += min(kin, K / (r + 1));
+// Each thread owns a run of rows; their offsets come from a block-wide prefix sum of the
+// row lengths.  tmp: one word per warp of the block.  Ends with a block barrier.
+__device__ void build_stair(uint32_t* st, int K, int kin, int* tmp) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (kin + int(blockDim.x) - 1) / int(blockDim.x);
+  const int p0 = min(kin, tid * per), p1 = min(kin, p0 + per);
+  int mine = 0;
+  for (int p = p0; p < p1; ++p) mine += min(kin, K / (p + 1));
+  int incl = mine;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(kFull, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) tmp[warp] = incl;
+  __syncthreads();
+  int off = incl - mine;
+  for (int w = 0; w < warp; ++w) off += tmp[w];
+  for (int p = p0; p < p1; ++p) {
     const int len = min(kin, K / (p + 1));
     for (int q = 0; q < len; ++q) st[off + q] = (uint32_t(p) << 16) | uint32_t(q);
+    off += len;
   }
+  __syncthreads();
 }
 
 // Rare path of the outer selection (needs rounding merges or massive ties): the top-K
@@ -518,13 +535,17 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
   int32_t* aidx = reinterpret_cast<int32_t*>(bval + a.kin_max);
   int32_t* bidx = aidx + a.kin_max;
 
-  build_stair(stair_w, a.W, min(a.W, S));
-  build_stair(stair_r, a.R, min(a.R, S));
-  __syncthreads();
+  // Warp 0's histogram is free until its first task: scratch for the staircase scans.
+  int* tmp = reinterpret_cast<int*>(wbase + a.keys_bytes + size_t(a.kpad) * 8);
+  build_stair(stair_w, a.W, min(a.W, S), tmp);
+  build_stair(stair_r, a.R, min(a.R, S), tmp);
 
+  // A short run of consecutive tasks per warp (no persistent grid): blocks that start
+  // late, e.g. behind a kernel on another stream, do not hold up the others.
   const long long tasks = a.items * 2;
-  for (long long task = (long long)blockIdx.x * a.warps + warp; task < tasks;
-       task += (long long)gridDim.x * a.warps) {
+  const long long task0 = ((long long)blockIdx.x * a.warps + warp) * a.tpw;
+  const long long task1 = task0 + a.tpw < tasks ? task0 + a.tpw : tasks;
+  for (long long task = task0; task < task1; ++task) {
     const int which = int(task & 1);
     const long long item = task >> 1;
     const int K = which ? a.R : a.W;
@@ -662,10 +683,15 @@ int launch_select_t(const void* kp, const void* qp, long long items, int S, int 
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, warps * 32, smem) != cudaSuccess)
     return SDM_ECUDA;
+  // About 64 waves of blocks: the last wave is short, and a block's staircase set-up is
+  // spread over several tasks per warp.
   const long long tasks = items * 2;
-  long long blocks = (tasks + warps - 1) / warps;
-  const long long cap = (long long)sms * (per_sm > 0 ? per_sm : 1);
-  if (blocks > cap) blocks = cap;
+  const long long resident = (long long)sms * (per_sm > 0 ? per_sm : 1) * warps;
+  long long tpw = tasks / (resident * 64);
+  tpw = tpw < 1 ? 1 : (tpw > 64 ? 64 : tpw);
+  a.tpw = int(tpw);
+  const long long blocks = (tasks + warps * tpw - 1) / (warps * tpw);
+  if (blocks > 0x7FFFFFFFLL) return SDM_EUNSUPPORTED;
   void* args[] = {&a};
   if (cudaLaunchKernel(fn, dim3(unsigned(blocks)), dim3(warps * 32), args, smem, s) != cudaSuccess)
     return SDM_ECUDA;
