@@ -413,19 +413,32 @@ __device__ __forceinline__ void load_half_keys(const Tin* src, int S, bool vec,
   for (int b = lane; b < 256; b += 32) hist[b] = 0u;
   __syncwarp();
   if (vec) {
+    // Up to four 16-byte loads per lane are issued before any is used, so their
+    // latencies overlap instead of adding up.
+    constexpr int UNR = 4;
     const uint4* src4 = reinterpret_cast<const uint4*>(src);
-    for (int c = lane; c < S / EPV; c += 32) {
-      float f[EPV];
-      unpack16<Tin>(__ldg(src4 + c), f);
-      IKey k[EPV];
+    const int nvec = S / EPV;
+    for (int c0 = lane; c0 < nvec; c0 += 32 * UNR) {
+      uint4 q[UNR];
 #pragma unroll
-      for (int i = 0; i < EPV; ++i) {
-        k[i] = inner_key_f(f[i], c * EPV + i, static_cast<IKey*>(nullptr));
-        atomicAdd(&hist[unsigned(k[i] >> TOP) & 255u], 1u);
+      for (int u = 0; u < UNR; ++u)
+        q[u] = c0 + 32 * u < nvec ? __ldg(src4 + c0 + 32 * u) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        const int c = c0 + 32 * u;
+        if (c >= nvec) break;
+        float f[EPV];
+        unpack16<Tin>(q[u], f);
+        IKey k[EPV];
+#pragma unroll
+        for (int i = 0; i < EPV; ++i) {
+          k[i] = inner_key_f(f[i], c * EPV + i, static_cast<IKey*>(nullptr));
+          atomicAdd(&hist[unsigned(k[i] >> TOP) & 255u], 1u);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(ik + c * EPV);
+#pragma unroll
+        for (int w = 0; w < int(EPV * sizeof(IKey) / 16); ++w) dst[w] = reinterpret_cast<const uint4*>(k)[w];
       }
-      uint4* dst = reinterpret_cast<uint4*>(ik + c * EPV);
-#pragma unroll
-      for (int w = 0; w < int(EPV * sizeof(IKey) / 16); ++w) dst[w] = reinterpret_cast<const uint4*>(k)[w];
     }
   } else {
     for (int j = lane; j < S; j += 32) {
