@@ -46,7 +46,11 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cols", type=int, default=0, help="force scan columns per block (0 = auto)")
-    ap.add_argument("--pd", type=int, default=0, help="force scan prefetch depth (0 = auto)")
+    ap.add_argument("--pd", type=int, default=0, help="force scan prefetch depth (0 = auto; one-stream step only)")
+    ap.add_argument("--chunks", type=int, default=0, help="token chunks of the pipelined forward (0 = auto)")
+    ap.add_argument("--pipeline", choices=["on", "off"], default="on",
+                    help="on: sdm_forward (selection of chunk c+1 overlaps the scan of chunk c); "
+                         "off: init || select, then plan and scan, one kernel after the other")
     ap.add_argument("--override", default="", help="size overrides for profiling, e.g. S=256,T=512")
     ap.add_argument("--mode", choices=["forward", "decode"], default="forward",
                     help="decode: one token per step for the batch, state resident, CUDA graph")
@@ -203,9 +207,24 @@ def make_state(cfg, rank, dev, torch, sdm, wl):
                  torch.empty(sh + (cfg.R,), dtype=torch.float32, device=dev))
     st["o"] = torch.empty(sh + (cfg.d_v,), dtype=torch.float32, device=dev)
     st["ws"] = sdm.scan_workspace(cfg.B, cfg.H, cfg.T, cfg.d_v, cfg.W, cfg.R, dev)
+    st["fws"] = sdm.forward_workspace(cfg.B, cfg.H, cfg.T, cfg.d_v, cfg.W, cfg.R, dev, 0)
     st["err"] = torch.zeros(1, dtype=torch.int32, device=dev)
     st["side"] = sdm.side_stream(dev)  # high priority: init shares the SMs with the selection
     return st
+
+
+def run_forward(st, cfg, sdm, args, inp=None, o=None, scan_ev=None):
+    """One forward pass through the public pipelined entry point (sdm_forward): state
+    from M0, selection and planning of token chunk c+1 overlapping the scan of chunk c.
+    scan_ev: 2 * chunks timing events recorded around each chunk's scan kernel."""
+    inp = st if inp is None else inp
+    o = st["o"] if o is None else o
+    if st["fws"].numel() < sdm.lib().sdm_forward_workspace_size(cfg.B, cfg.H, cfg.T, cfg.d_v, cfg.W, cfg.R,
+                                                                 args.chunks):
+        st["fws"] = sdm.forward_workspace(cfg.B, cfg.H, cfg.T, cfg.d_v, cfg.W, cfg.R, st["M"].device, args.chunks)
+    sdm.forward(inp["kp"], inp["qp"], inp["v"], inp["alpha"], inp["beta"], st["M0"], cfg.W, cfg.R, M=st["M"],
+                workspace=st["fws"], dev_err=st["err"], out=st["sel"], o=o, chunks=args.chunks,
+                scan_events=scan_ev)
 
 
 def run_step(st, cfg, sdm, args, ev=None, before_select=None, inp=None, o=None):
@@ -284,11 +303,30 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def config_dict(cfg):
+def config_dict(cfg, pipelined=True):
+    step = ("sdm_forward: state from M0, then select+plan of token chunk c+1 overlapping the scan of chunk c"
+            if pipelined else
+            "init_state_from_M0 (side stream) || select, then plan, then scan (waits for init)")
     return {"workload": cfg.name, "B": cfg.B, "H": cfg.H, "T": cfg.T, "N": cfg.N, "d_v": cfg.d_v, "W": cfg.W,
             "R": cfg.R, "inputs": cfg.in_dtype, "state": "f32",
             "l2": "inputs larger than L2 (state table and k'/q' each exceed the 129 MB L2)",
-            "step": "init_state_from_M0 (side stream) || select, then plan, then scan (waits for init)"}
+            "step": step}
+
+
+def one_stream_breakdown(st, cfg, sdm, args, torch, dev, reps=3):
+    """Each kernel's time on the one-stream step (init on a side stream || select, then plan,
+    then scan), outside the timed region: what the pipelined step overlaps."""
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    run_step(st, cfg, sdm, args)
+    evs = [[E() for _ in range(5)] for _ in range(reps)]
+    for e in evs:
+        run_step(st, cfg, sdm, args, e)
+    torch.cuda.synchronize(dev)
+    return {"init_ms": sum(e[0].elapsed_time(e[1]) for e in evs) / reps,
+            "select_ms": sum(e[0].elapsed_time(e[2]) for e in evs) / reps,
+            "plan_ms": sum(e[2].elapsed_time(e[3]) for e in evs) / reps,
+            "scan_ms": sum(e[3].elapsed_time(e[4]) for e in evs) / reps,
+            "step_ms": sum(e[0].elapsed_time(e[4]) for e in evs) / reps}
 
 
 def run_ours(args):
@@ -312,57 +350,95 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
+    pipelined = args.pipeline == "on"
+    chunks = sdm.forward_chunks(cfg.T, args.chunks) if pipelined else 1
+    E = lambda: torch.cuda.Event(enable_timing=True)
+
+    def step(k_ev=None, s_ev=None):
+        if pipelined:
+            run_forward(st, cfg, sdm, args, scan_ev=s_ev)
+        else:
+            run_step(st, cfg, sdm, args, k_ev)
+
     for _ in range(args.warmup):
-        run_step(st, cfg, sdm, args)
+        step()
     torch.cuda.synchronize(dev)
     if st["err"].item() != 0:
         raise RuntimeError(f"device error flags {st['err'].item()}")
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
-    for e in evs:      # create the events now (torch creates them lazily on first record)
-        for x in e:
-            x.record()
+    step_ev = [(E(), E()) for _ in range(K)]
+    kern_ev = [[E() for _ in range(5)] for _ in range(K)]      # one-stream step: phase events
+    scan_ev = [[E() for _ in range(2 * chunks)] for _ in range(K)]  # pipelined step: scan launches
+    for group in (step_ev, kern_ev, scan_ev):   # create the events now (torch creates them lazily)
+        for e in group:
+            for x in e:
+                x.record()
     torch.cuda.synchronize(dev)
     barrier()
     torch.cuda.synchronize(dev)
+    main = torch.cuda.current_stream(dev)
     with ClockSampler(local) as clk:
         t_wall = time.perf_counter()
         for k in range(K):
-            run_step(st, cfg, sdm, args, evs[k])
+            step_ev[k][0].record(main)
+            step(kern_ev[k], scan_ev[k])
+            step_ev[k][1].record(main)
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall
     barrier()
-    total_ms = evs[0][0].elapsed_time(evs[-1][4])
-    # init runs on the side stream from the step start; select from the step start on the
-    # main stream; plan until the scan starts; scan until the step ends.
-    phase = {"init_ms": sum(e[0].elapsed_time(e[1]) for e in evs) / K,
-             "select_ms": sum(e[0].elapsed_time(e[2]) for e in evs) / K,
-             "plan_ms": sum(e[2].elapsed_time(e[3]) for e in evs) / K,
-             "scan_ms": sum(e[3].elapsed_time(e[4]) for e in evs) / K,
-             "overlap": "init on a side stream, concurrent with select and plan"}
+    total_ms = step_ev[0][0].elapsed_time(step_ev[-1][1])
     total_ms = max_over_ranks(total_ms, dev)
     units_rank = cfg.B * cfg.H * cfg.T
     value = whole_job_rate(units_rank, K, world, total_ms)
 
-    # roofline of the dominant kernel (the scan), from its own events
+    # roofline of the dominant kernel (the scan): its launches, timed by their own events on
+    # the stream they run on
+    if pipelined:
+        launches = [e[2 * c].elapsed_time(e[2 * c + 1]) for e in scan_ev for c in range(chunks)]
+        scan_launch_ms = sum(launches) / len(launches)
+        units_launch = units_rank / chunks
+        phase = {"scan_ms_per_launch": scan_launch_ms, "scan_ms_per_step": scan_launch_ms * chunks,
+                 "chunks": chunks, "tokens_per_chunk": -(-cfg.T // chunks),
+                 "overlap": "sdm_forward: init (high-priority stream) || select+plan of chunk c+1 "
+                            "(select stream) || scan of chunk c (high-priority stream)"}
+        phase["one_stream_breakdown"] = one_stream_breakdown(st, cfg, sdm, args, torch, dev)
+        launches_per_step = 1 + 3 * chunks
+    else:
+        scan_launch_ms = sum(e[3].elapsed_time(e[4]) for e in kern_ev) / K
+        units_launch = units_rank
+        # init runs on the side stream from the step start; select from the step start on the
+        # main stream; plan until the scan starts; scan until the step ends.
+        phase = {"init_ms": sum(e[0].elapsed_time(e[1]) for e in kern_ev) / K,
+                 "select_ms": sum(e[0].elapsed_time(e[2]) for e in kern_ev) / K,
+                 "plan_ms": sum(e[2].elapsed_time(e[3]) for e in kern_ev) / K,
+                 "scan_ms": scan_launch_ms,
+                 "overlap": "init on a side stream, concurrent with select and plan"}
+        launches_per_step = 4
     peak, peak_kind = hbm_peak()
-    alg = scan_bytes_per_head_token(cfg) * units_rank
-    achieved = alg / (phase["scan_ms"] / 1e3) / 1e9
+    alg = scan_bytes_per_head_token(cfg) * units_launch
+    achieved = alg / (scan_launch_ms / 1e3) / 1e9
     shape = sdm.scan_launch_info(cfg.B, cfg.H, cfg.d_v, cfg.W, cfg.R)
-    if args.cols or args.pd:
+    if not pipelined and (args.cols or args.pd):
         shape["forced"] = {"cols_per_cta": args.cols, "prefetch_depth": args.pd}
-    traffic = traffic_per_launch(units_rank)
+    traffic = traffic_per_launch(units_launch)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32", "data": "synthetic", "config": config_dict(cfg),
+            "dtype": "f32", "data": "synthetic", "config": config_dict(cfg, pipelined),
             "roofline": {"kernel": "sdm scan kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                          else "fallback", "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": traffic, "algorithmic_bytes_per_launch": alg},
+                         "traffic": traffic, "algorithmic_bytes_per_launch": alg,
+                         "launches_per_step": chunks},
             "kernels": dict(phase, scan_shape=shape, wall_ms_per_step=1e3 * t_wall / K),
-            "gpu_launches": 4 * K}
+            "gpu_launches": launches_per_step * K}
+    if pipelined:
+        # the same kernel over the whole sequence with nothing else running (one-stream step)
+        alone_ms = phase["one_stream_breakdown"]["scan_ms"]
+        alone = scan_bytes_per_head_token(cfg) * units_rank / (alone_ms / 1e3) / 1e9
+        line["roofline"]["alone"] = {"achieved": alone, "frac": alone / peak, "ms_per_launch": alone_ms,
+                                     "note": "scan kernel over all T tokens, timed on the one-stream step"}
     line["clocks"] = clk.summary()
 
     if not args.no_e2e:
@@ -394,6 +470,7 @@ def e2e(st, cfg, sdm, args, dev, torch, K, world):
     d2h = o_host[0].numel() * 4
     copy = torch.cuda.Stream(device=dev)
     main = torch.cuda.current_stream(dev)
+    chunks = sdm.forward_chunks(cfg.T, args.chunks)
     torch.cuda.synchronize(dev)
     # This host's copy rates, alone (context for the streamed number: the loop is copy bound
     # when h2d_bytes_per_step / H2D rate exceeds the device step).
@@ -426,9 +503,16 @@ def e2e(st, cfg, sdm, args, dev, torch, K, world):
             main.wait_event(ready[k])
             if k + 1 < n:
                 h2d_step(k + 1)
-            # the inputs are free once the scan kernel starts: selection and planning read them
-            run_step(st, cfg, sdm, args, inp=bufs[k % 2], o=outs[k % 2],
-                     ev=[torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event(), free[k], torch.cuda.Event()])
+            # the inputs are free once the (last) scan kernel starts: selection and planning
+            # read them, the scan reads only the planning records
+            if args.pipeline == "on":
+                sev = [torch.cuda.Event() for _ in range(2 * chunks)]
+                sev[2 * chunks - 2] = free[k]
+                run_forward(st, cfg, sdm, args, inp=bufs[k % 2], o=outs[k % 2], scan_ev=sev)
+            else:
+                run_step(st, cfg, sdm, args, inp=bufs[k % 2], o=outs[k % 2],
+                         ev=[torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event(), free[k],
+                             torch.cuda.Event()])
             done[k].record(main)
             with torch.cuda.stream(copy):
                 copy.wait_event(done[k])

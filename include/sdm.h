@@ -161,6 +161,48 @@ int sdm_scan_forward_noalloc(float* M, const int32_t* idx_w, const float* sc_w,
 int sdm_scan_launch_info(int B, int H, int d_v, int W, int R, int* cols_per_cta,
                          int* prefetch_depth, int* blocks, int* smem_bytes);
 
+/* sdm_forward - one whole forward pass of the SDM layer over a batch of sequences
+ * ("Stato Iniziale Appreso": every sequence starts from the learned M_0; "Meccanismo
+ * Core" items 2-4: product-key selection, gated delta write, read after write), with
+ * the selection and the scan overlapped in token chunks on internal streams.  Results
+ * are bit-identical to sdm_init_state_from_M0 + sdm_select + sdm_scan_forward on one
+ * stream.
+ *   kp, qp [B, H, T, 2, S] in_dt; v [B, H, T, d_v] v_dt; alpha, beta [B, H, T] fp32.
+ *   M0     [H, N, d_v] fp32 with N = S*S, or NULL to continue from the state in M.
+ *   M      [B, H, N, d_v] fp32, out: state after token T-1.
+ *   idx_w, sc_w [B, H, T, W]; idx_r, sc_r [B, H, T, R]; o [B, H, T, d_v] fp32: written,
+ *          as by sdm_select and sdm_scan_forward.
+ *   workspace  device scratch of at least sdm_forward_workspace_size(B, H, T, d_v, W, R, 0)
+ *          bytes, 16-byte aligned, contents irrelevant.
+ *   dev_err  device int or NULL, as for sdm_scan_forward.
+ * Ordering: work enqueued on `stream` before the call runs before any of the call's work,
+ * and work enqueued on `stream` after the call sees all of its results.  The library
+ * runs the work on four streams of its own per device (created on the first call on
+ * that device) and enqueues calls on one device one at a time.  Concurrent calls that
+ * share M, the outputs or the workspace race, as with any of these entry points.
+ * Errors: the argument checks of sdm_select and sdm_scan_forward (nothing enqueued);
+ * SDM_ENOSPACE for a short workspace; SDM_ECUDA if a launch fails part-way, after
+ * which M and the outputs are unspecified. */
+size_t sdm_forward_workspace_size(int B, int H, int T, int d_v, int W, int R, int chunks);
+int sdm_forward(const void* kp, const void* qp, int in_dt, const void* v, int v_dt,
+                const float* alpha, const float* beta, const float* M0, float* M, int B, int H,
+                int T, int S, int d_v, int W, int R, int32_t* idx_w, float* sc_w, int32_t* idx_r,
+                float* sc_r, float* o, void* workspace, size_t workspace_bytes, int* dev_err,
+                void* stream);
+
+/* sdm_forward with the chunking chosen: `chunks` token chunks (0 = automatic, about 1024
+ * tokens each; the effective count is sdm_forward_chunks(T, chunks)), and, when
+ * `scan_events` is not NULL, 2 * chunks cudaEvent_t recorded right before and after each
+ * chunk's scan kernel on the stream it runs on (for timing the scan kernel).  The
+ * workspace must hold sdm_forward_workspace_size(..., chunks) bytes. */
+int sdm_forward_chunks(int T, int chunks);
+int sdm_forward_tuned(const void* kp, const void* qp, int in_dt, const void* v, int v_dt,
+                      const float* alpha, const float* beta, const float* M0, float* M, int B,
+                      int H, int T, int S, int d_v, int W, int R, int32_t* idx_w, float* sc_w,
+                      int32_t* idx_r, float* sc_r, float* o, void* workspace,
+                      size_t workspace_bytes, int* dev_err, int chunks, void* const* scan_events,
+                      void* stream);
+
 /* sdm_gen_inputs - synthetic inputs (not part of the method): draws the box
  * b in [b_off, b_off+B), all H heads, tokens t in [t_off, t_off+T) of a logical
  * workload with T_total tokens per sequence, from the counter-based generator

@@ -51,8 +51,15 @@ def lib() -> ctypes.CDLL:
             L.sdm_scan_launch_info.argtypes = [i, i, i, i, i, p, p, p, p]
             L.sdm_gen_inputs.argtypes = [ull, i, i, i, i, i, ll, i, i, i, f, i, p, p, p, p, p, p, p]
             L.sdm_gen_M0.argtypes = [ull, i, ll, i, f, p, p]
+            L.sdm_forward_workspace_size.argtypes = [i, i, i, i, i, i, i]
+            L.sdm_forward_workspace_size.restype = sz
+            L.sdm_forward_chunks.argtypes = [i, i]
+            L.sdm_forward_tuned.argtypes = [p, p, i, p, i, p, p, p, p, i, i, i, i, i, i, i, p, p, p, p, p, p,
+                                            sz, p, i, p, p]
+            L.sdm_forward.argtypes = [p, p, i, p, i, p, p, p, p, i, i, i, i, i, i, i, p, p, p, p, p, p, sz, p, p]
             for name in ("sdm_init_state_from_M0", "sdm_select", "sdm_scan_forward",
-                         "sdm_scan_forward_tuned", "sdm_scan_launch_info", "sdm_gen_inputs", "sdm_gen_M0"):
+                         "sdm_scan_forward_tuned", "sdm_scan_launch_info", "sdm_gen_inputs", "sdm_gen_M0",
+                         "sdm_forward_chunks", "sdm_forward_tuned", "sdm_forward"):
                 getattr(L, name).restype = i
             _lib = L
     return _lib
@@ -276,37 +283,75 @@ def side_stream(device) -> torch.cuda.Stream:
     return _side_streams[key]
 
 
-def forward(kp, qp, v, alpha, beta, M0, W: int, R: int, M=None, workspace=None, dev_err=None,
-            overlap: bool = True, out=None, o=None):
-    """One SDM forward pass over a batch: state from M0, selection, scan.
+def forward_chunks(T: int, chunks: int = 0) -> int:
+    """Token chunks forward() pipelines T tokens in (chunks=0: the automatic choice)."""
+    return lib().sdm_forward_chunks(T, chunks)
 
-    With overlap, M is initialised on a side stream while the current stream runs the
-    selection and the planning pass; the scan kernel waits for both.  The result is the
-    same either way.  Returns (o, M, (idx_w, sc_w, idx_r, sc_r))."""
+
+def forward_workspace(B: int, H: int, T: int, d_v: int, W: int, R: int, device, chunks: int = 0) -> torch.Tensor:
+    n = lib().sdm_forward_workspace_size(B, H, T, d_v, W, R, chunks)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def forward(kp, qp, v, alpha, beta, M0, W: int, R: int, M=None, workspace=None, dev_err=None,
+            overlap: bool = True, out=None, o=None, chunks: int = 0, scan_events=None):
+    """One SDM forward pass over a batch: state from M0 (or, with M0=None, from the state
+    already in M), selection, scan.  Returns (o, M, (idx_w, sc_w, idx_r, sc_r)).
+
+    overlap=True runs sdm_forward: the selection of token chunk c+1 overlaps the scan of
+    chunk c on the library's own streams (chunks=0: automatic).  overlap=False runs the
+    three steps one after the other on the current stream.  Both give the same bits.
+    scan_events: optional list of 2 * forward_chunks(T, chunks) torch.cuda.Event, recorded
+    around each chunk's scan kernel."""
     B, H, T, _, S = kp.shape
-    dv = M0.shape[-1]
+    dv = v.shape[-1]
     if M is None:
+        if M0 is None:
+            raise ValueError("M0=None continues from M, which must then be given")
         M = torch.empty((B, H, S * S, dv), dtype=torch.float32, device=kp.device)
     if not overlap:
-        init_state_from_M0(M, M0)
+        if M0 is not None:
+            init_state_from_M0(M, M0)
         sel = select(kp, qp, W, R, out=out)
         o = scan_forward(M, *sel, v, alpha, beta, o=o, workspace=workspace, dev_err=dev_err)
         return o, M, sel
-    main = torch.cuda.current_stream(M.device)
-    side = side_stream(M.device)
-    free = torch.cuda.Event()
-    free.record(main)                      # earlier work on M (and M0) is ordered before
-    side.wait_event(free)
-    with torch.cuda.stream(side):
-        init_state_from_M0(M, M0)
-    M.record_stream(side)
-    M0.record_stream(side)
-    init_done = torch.cuda.Event()
-    init_done.record(side)
-    sel = select(kp, qp, W, R, out=out)
-    o = scan_forward(M, *sel, v, alpha, beta, o=o, workspace=workspace, dev_err=dev_err,
-                     wait_before_scan=init_done)
-    return o, M, sel
+    _need(kp, "kp")
+    _need(qp, "qp", kp.dtype, tuple(kp.shape))
+    _need(M, "M", torch.float32, (B, H, S * S, dv))
+    if M0 is not None:
+        _need(M0, "M0", torch.float32, (H, S * S, dv))
+    _need(v, "v", None, (B, H, T, dv))
+    _need(alpha, "alpha", torch.float32, (B, H, T))
+    _need(beta, "beta", torch.float32, (B, H, T))
+    if out is None:
+        dev = kp.device
+        out = (torch.empty((B, H, T, W), dtype=torch.int32, device=dev), torch.empty((B, H, T, W), device=dev),
+               torch.empty((B, H, T, R), dtype=torch.int32, device=dev), torch.empty((B, H, T, R), device=dev))
+    idx_w, sc_w, idx_r, sc_r = out
+    _need(idx_w, "idx_w", torch.int32, (B, H, T, W))
+    _need(sc_w, "sc_w", torch.float32, (B, H, T, W))
+    _need(idx_r, "idx_r", torch.int32, (B, H, T, R))
+    _need(sc_r, "sc_r", torch.float32, (B, H, T, R))
+    if o is None:
+        o = torch.empty((B, H, T, dv), dtype=torch.float32, device=M.device)
+    _need(o, "o", torch.float32, (B, H, T, dv))
+    if workspace is None:
+        workspace = forward_workspace(B, H, T, dv, W, R, M.device, chunks)
+    _need(workspace, "workspace", torch.uint8)
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32)
+    ev_arr = None
+    if scan_events is not None:
+        if len(scan_events) != 2 * forward_chunks(T, chunks):
+            raise ValueError("scan_events needs 2 * forward_chunks(T, chunks) events")
+        for e in scan_events:
+            if e.cuda_event == 0:
+                e.record()  # torch creates its events lazily; the library records it again
+        ev_arr = (ctypes.c_void_p * len(scan_events))(*[e.cuda_event for e in scan_events])
+    _call("sdm_forward_tuned", _p(kp), _p(qp), _dtype_code(kp), _p(v), _dtype_code(v), _p(alpha), _p(beta),
+          _p(M0), _p(M), B, H, T, S, dv, W, R, _p(idx_w), _p(sc_w), _p(idx_r), _p(sc_r), _p(o),
+          _p(workspace), workspace.numel(), _p(dev_err), int(chunks), ev_arr, _stream(M.device))
+    return o, M, out
 
 
 class DecodeStep:

@@ -4,26 +4,6 @@
 
 using namespace sdm;
 
-namespace {
-
-bool bad_dtype(int dt) { return dt != SDM_F32 && dt != SDM_BF16; }
-
-int check_scan_args(float* M, const int32_t* idx_w, const float* sc_w, const int32_t* idx_r,
-                    const float* sc_r, const void* v, int v_dt, const float* alpha,
-                    const float* beta, int B, int H, int T, long long N, int d_v, int W, int R,
-                    float* o) {
-  if (B < 1 || H < 1 || T < 0 || N < 1 || d_v < 4 || d_v % 4 || W < 1 || R < 1) return SDM_EINVAL;
-  if (bad_dtype(v_dt) || (long long)W > N || (long long)R > N) return SDM_EINVAL;
-  if (W > SDM_MAX_K || R > SDM_MAX_K || N > 0x7FFFFFFFLL) return SDM_EUNSUPPORTED;
-  if ((long long)B * H > 0x7FFFFFFFLL || (long long)T * (W + R) > 0x7FFFFFFFLL) return SDM_EUNSUPPORTED;
-  if (!aligned16(M)) return SDM_EALIGN;
-  if (T > 0 && (!aligned16(idx_w) || !aligned16(sc_w) || !aligned16(idx_r) || !aligned16(sc_r) ||
-                !aligned16(v) || !aligned16(alpha) || !aligned16(beta) || !aligned16(o)))
-    return SDM_EALIGN;
-  return SDM_OK;
-}
-
-}  // namespace
 
 extern "C" {
 
@@ -51,18 +31,13 @@ int sdm_init_state_from_M0(float* M, const float* M0, int B, int H, long long N,
 
 int sdm_select(const void* kp, const void* qp, int in_dt, int B, int H, int T, int S, int W, int R,
                int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, void* stream) {
-  if (B < 1 || H < 1 || T < 0 || S < 1 || W < 1 || R < 1 || bad_dtype(in_dt)) return SDM_EINVAL;
-  const long long N = (long long)S * S;
-  if ((long long)W > N || (long long)R > N) return SDM_EINVAL;
-  if (S > SDM_MAX_S || W > SDM_MAX_K || R > SDM_MAX_K) return SDM_EUNSUPPORTED;
-  const long long items = (long long)B * H * T;
-  if (items == 0) return SDM_OK;
-  if (!aligned16(kp) || !aligned16(qp) || !aligned16(idx_w) || !aligned16(sc_w) ||
-      !aligned16(idx_r) || !aligned16(sc_r))
-    return SDM_EALIGN;
+  const int st = check_select_args(kp, qp, in_dt, B, H, T, S, W, R, idx_w, sc_w, idx_r, sc_r);
+  if (st != SDM_OK || T == 0) return st;
   return in_dt == SDM_BF16
-             ? launch_select_bf16(kp, qp, items, S, W, R, idx_w, sc_w, idx_r, sc_r, as_stream(stream))
-             : launch_select_f32(kp, qp, items, S, W, R, idx_w, sc_w, idx_r, sc_r, as_stream(stream));
+             ? launch_select_bf16(kp, qp, whole_sequences(B * H, T), S, W, R, idx_w, sc_w, idx_r,
+                                  sc_r, as_stream(stream))
+             : launch_select_f32(kp, qp, whole_sequences(B * H, T), S, W, R, idx_w, sc_w, idx_r,
+                                 sc_r, as_stream(stream));
 }
 
 size_t sdm_scan_workspace_size(int B, int H, int T, int d_v, int W, int R) {
@@ -88,8 +63,9 @@ int sdm_scan_forward_tuned(float* M, const int32_t* idx_w, const float* sc_w,
   ScanShape shape;
   st = choose_scan_shape(B * H, d_v, W, R, cols_per_cta, prefetch_depth, &shape);
   if (st != SDM_OK) return st;
-  return launch_scan(M, idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, B * H, T, N, d_v, W, R, o,
-                     workspace, dev_err, shape, reinterpret_cast<cudaEvent_t>(event_after_plan),
+  return launch_scan(M, idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, whole_sequences(B * H, T),
+                     N, d_v, W, R, o, workspace, dev_err, shape,
+                     reinterpret_cast<cudaEvent_t>(event_after_plan),
                      reinterpret_cast<cudaEvent_t>(wait_before_scan), as_stream(stream));
 }
 

@@ -20,6 +20,39 @@ inline int last_launch_status() {
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
+inline bool bad_dtype(int dt) { return dt != SDM_F32 && dt != SDM_BF16; }
+
+// Argument checks of the selection (sdm_select); pointers only matter when T > 0.
+inline int check_select_args(const void* kp, const void* qp, int in_dt, int B, int H, int T,
+                             int S, int W, int R, const void* idx_w, const void* sc_w,
+                             const void* idx_r, const void* sc_r) {
+  if (B < 1 || H < 1 || T < 0 || S < 1 || W < 1 || R < 1 || bad_dtype(in_dt)) return SDM_EINVAL;
+  const long long N = (long long)S * S;
+  if ((long long)W > N || (long long)R > N) return SDM_EINVAL;
+  if (S > SDM_MAX_S || W > SDM_MAX_K || R > SDM_MAX_K) return SDM_EUNSUPPORTED;
+  if ((long long)B * H * T > 0x3FFFFFFFFFFFLL) return SDM_EUNSUPPORTED;
+  if (T > 0 && (!aligned16(kp) || !aligned16(qp) || !aligned16(idx_w) || !aligned16(sc_w) ||
+                !aligned16(idx_r) || !aligned16(sc_r)))
+    return SDM_EALIGN;
+  return SDM_OK;
+}
+
+// Argument checks of the scan (sdm_scan_forward), workspace excluded.
+inline int check_scan_args(const float* M, const int32_t* idx_w, const float* sc_w,
+                           const int32_t* idx_r, const float* sc_r, const void* v, int v_dt,
+                           const float* alpha, const float* beta, int B, int H, int T,
+                           long long N, int d_v, int W, int R, const float* o) {
+  if (B < 1 || H < 1 || T < 0 || N < 1 || d_v < 4 || d_v % 4 || W < 1 || R < 1) return SDM_EINVAL;
+  if (bad_dtype(v_dt) || (long long)W > N || (long long)R > N) return SDM_EINVAL;
+  if (W > SDM_MAX_K || R > SDM_MAX_K || N > 0x7FFFFFFFLL) return SDM_EUNSUPPORTED;
+  if ((long long)B * H > 0x7FFFFFFFLL || (long long)T * (W + R) > 0x7FFFFFFFLL) return SDM_EUNSUPPORTED;
+  if (!aligned16(M)) return SDM_EALIGN;
+  if (T > 0 && (!aligned16(idx_w) || !aligned16(sc_w) || !aligned16(idx_r) || !aligned16(sc_r) ||
+                !aligned16(v) || !aligned16(alpha) || !aligned16(beta) || !aligned16(o)))
+    return SDM_EALIGN;
+  return SDM_OK;
+}
+
 // Per-token record the scan's planning pass writes into the workspace, one per
 // (b, h, t).  Every section starts on a 16-byte boundary so the scan can stage it
 // with 16-byte asynchronous copies:
@@ -48,20 +81,33 @@ __host__ __device__ inline RecLayout rec_layout(int W, int R, int d_v) {
   return L;
 }
 
+// Tokens [t0, t0 + Tc) of BH sequences stored with T_total tokens each: per-token
+// arrays ([BH, T_total, ...]) are read and written in place at token bh * T_total + t;
+// planning records are per window, [BH, Tc].
+struct TokenWindow {
+  int BH;
+  int Tc;
+  int T_total;
+  int t0;
+};
+inline TokenWindow whole_sequences(int BH, int T) { return TokenWindow{BH, T, T, 0}; }
+
 // Launchers (host side; arguments already validated by the entry points).
 int launch_init_state(float* M, const float* M0, int B, int H, long long N, int d_v,
                       cudaStream_t s);
-int launch_select_bf16(const void* kp, const void* qp, long long items, int S, int W, int R,
-                       int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, cudaStream_t s);
-int launch_select_f32(const void* kp, const void* qp, long long items, int S, int W, int R,
-                      int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, cudaStream_t s);
+int launch_select_bf16(const void* kp, const void* qp, const TokenWindow& win, int S, int W,
+                       int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r,
+                       cudaStream_t s);
+int launch_select_f32(const void* kp, const void* qp, const TokenWindow& win, int S, int W,
+                      int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r,
+                      cudaStream_t s);
 
-// Planning pass of the scan (one record per (b, h, t) into `workspace`); `pd` must be the
-// prefetch depth of the scan kernel that consumes the records.
+// Planning pass of the scan (one record per (b, h, t) of the window into `rec`); `pd` must
+// be the prefetch depth of the scan kernel that consumes the records.
 int launch_plan(const int32_t* idx_w, const float* sc_w, const int32_t* idx_r, const float* sc_r,
-                const void* v, int v_dt, const float* alpha, const float* beta, int BH, int T,
-                long long N, int d_v, int W, int R, int pd, void* workspace, int* dev_err,
-                cudaStream_t s);
+                const void* v, int v_dt, const float* alpha, const float* beta,
+                const TokenWindow& win, long long N, int d_v, int W, int R, int pd, void* rec,
+                int* dev_err, cudaStream_t s);
 
 struct ScanShape {
   int cols;      // d_v columns per thread block
@@ -72,10 +118,16 @@ struct ScanShape {
 // Picks (or checks a forced) scan kernel shape.  Returns SDM_OK or SDM_EUNSUPPORTED.
 int choose_scan_shape(int BH, int d_v, int W, int R, int force_cols, int force_pd,
                       ScanShape* out);
+// The scan kernel alone, over the window's records (written by launch_plan with the
+// same shape.pd); continues from the state in M.
+int launch_scan_records(float* M, const void* rec, const TokenWindow& win, long long N, int d_v,
+                        int W, int R, float* o, const ScanShape& shape, cudaStream_t s);
+// Planning pass, then (after waiting for wait_before_scan, if any, and recording
+// after_plan, if any) the scan kernel.
 int launch_scan(float* M, const int32_t* idx_w, const float* sc_w, const int32_t* idx_r,
                 const float* sc_r, const void* v, int v_dt, const float* alpha, const float* beta,
-                int BH, int T, long long N, int d_v, int W, int R, float* o, void* workspace,
-                int* dev_err, const ScanShape& shape, cudaEvent_t after_plan,
+                const TokenWindow& win, long long N, int d_v, int W, int R, float* o,
+                void* workspace, int* dev_err, const ScanShape& shape, cudaEvent_t after_plan,
                 cudaEvent_t wait_before_scan, cudaStream_t s);
 
 int launch_gen_inputs(unsigned long long seed, int B, int H, int T, int b_off, int t_off,

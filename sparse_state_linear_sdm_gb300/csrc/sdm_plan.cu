@@ -47,7 +47,9 @@ struct PlanArgs {
   const void* v;
   const float* alpha;
   const float* beta;
-  int T;
+  int T;        // tokens of the window
+  int T_total;  // tokens per sequence in the per-token input arrays
+  int t_off;    // first token of the window
   long long N;
   int d_v, W, R, pd, tc;
   int log2cap;  // hash table of 2^log2cap entries, at least twice the entries inserted
@@ -93,7 +95,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   const int t1 = min(a.T, t0 + a.tc);
   const int tl = max(0, t0 - a.pd);
   const int W = a.W, R = a.R, WR = W + R;
-  const size_t tok0 = size_t(bh) * a.T;
+  const size_t tok0 = size_t(bh) * a.T_total + a.t_off;  // inputs: token (bh, t_off + u)
+  const size_t rec0 = size_t(bh) * a.T;                   // records: (bh, u) of the window
   const int cap = 1 << a.log2cap, mask = cap - 1;
   uint32_t* filter = reinterpret_cast<uint32_t*>(table + cap);
   int32_t* iw = reinterpret_cast<int32_t*>(filter + kFilterWords);  // [(t1 - tl) * W]
@@ -128,7 +131,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
 
   int errs = 0;  // SDM_DEV_* bits seen by this thread, reported once at the end
   for (int u = t0; u < t1; ++u) {
-    unsigned char* rec = a.rec + (tok0 + u) * size_t(a.L.bytes);
+    unsigned char* rec = a.rec + (rec0 + u) * size_t(a.L.bytes);
     for (int e = tid; e < WR; e += kPlanThreads) {
       int32_t x = e < W ? iw[(u - tl) * W + e] : ir[(u - t0) * R + (e - W)];
       int code = -1;
@@ -165,7 +168,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   // Weights, gates and v for each token of the chunk: one warp per token.
   const int warp = tid >> 5, lane = tid & 31;
   for (int u = t0 + warp; u < t1; u += kPlanThreads / 32) {
-    unsigned char* rec = a.rec + (tok0 + u) * size_t(a.L.bytes);
+    unsigned char* rec = a.rec + (rec0 + u) * size_t(a.L.bytes);
     float* wts = reinterpret_cast<float*>(rec + a.L.off_wts);
     warp_softmax(a.sc_w + (tok0 + u) * W, W, wts);
     warp_softmax(a.sc_r + (tok0 + u) * R, R, wts + W);
@@ -185,9 +188,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
 }  // namespace
 
 int launch_plan(const int32_t* idx_w, const float* sc_w, const int32_t* idx_r, const float* sc_r,
-                const void* v, int v_dt, const float* alpha, const float* beta, int BH, int T,
-                long long N, int d_v, int W, int R, int pd, void* workspace, int* dev_err,
-                cudaStream_t s) {
+                const void* v, int v_dt, const float* alpha, const float* beta,
+                const TokenWindow& win, long long N, int d_v, int W, int R, int pd, void* rec,
+                int* dev_err, cudaStream_t s) {
+  const int T = win.Tc, BH = win.BH;
   if (T == 0 || BH == 0) return SDM_OK;
   PlanArgs pa;
   pa.idx_w = idx_w;
@@ -198,6 +202,8 @@ int launch_plan(const int32_t* idx_w, const float* sc_w, const int32_t* idx_r, c
   pa.alpha = alpha;
   pa.beta = beta;
   pa.T = T;
+  pa.T_total = win.T_total;
+  pa.t_off = win.t0;
   pa.N = N;
   pa.d_v = d_v;
   pa.W = W;
@@ -216,7 +222,7 @@ int launch_plan(const int32_t* idx_w, const float* sc_w, const int32_t* idx_r, c
   pa.tc = tc;
   pa.log2cap = cap_for(tc);
   pa.L = rec_layout(W, R, d_v);
-  pa.rec = static_cast<unsigned char*>(workspace);
+  pa.rec = static_cast<unsigned char*>(rec);
   pa.dev_err = dev_err;
   const dim3 grid((T + tc - 1) / tc, BH);
   const int smem = int(plan_smem_bytes(pa.log2cap, tc, pd, W, R));

@@ -40,7 +40,9 @@ struct ScanArgs {
   float* M;
   const unsigned char* rec;
   float* o;
-  int T;
+  int T;        // tokens of the window
+  int T_total;  // tokens per sequence in o
+  int t_off;    // first token of the window
   long long N;
   int d_v, W, R;
   RecLayout L;
@@ -71,7 +73,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   const int c0 = (blockIdx.x - bh * slices) * C;
   const unsigned char* recs = a.rec + size_t(bh) * T * L.bytes;
   float* Mbh = a.M + size_t(bh) * size_t(a.N) * d_v + c0;
-  float* obh = a.o + size_t(bh) * T * d_v + c0;
+  float* obh = a.o + (size_t(bh) * a.T_total + a.t_off) * d_v + c0;
   const int c4 = tid % LPR;
 
   auto issue_meta = [&](int u) {
@@ -256,37 +258,43 @@ int choose_scan_shape(int BH, int d_v, int W, int R, int force_cols, int force_p
   return SDM_OK;
 }
 
-int launch_scan(float* M, const int32_t* idx_w, const float* sc_w, const int32_t* idx_r,
-                const float* sc_r, const void* v, int v_dt, const float* alpha, const float* beta,
-                int BH, int T, long long N, int d_v, int W, int R, float* o, void* workspace,
-                int* dev_err, const ScanShape& shape, cudaEvent_t after_plan,
-                cudaEvent_t wait_before_scan, cudaStream_t s) {
-  if (T == 0 || BH == 0) return SDM_OK;
-  const RecLayout L = rec_layout(W, R, d_v);
-  const int st = launch_plan(idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, BH, T, N, d_v, W, R,
-                            shape.pd, workspace, dev_err, s);
-  if (st != SDM_OK) return st;
-  if (wait_before_scan && cudaStreamWaitEvent(s, wait_before_scan, 0) != cudaSuccess)
-    return SDM_ECUDA;
-  if (after_plan && cudaEventRecord(after_plan, s) != cudaSuccess) return SDM_ECUDA;
-
+int launch_scan_records(float* M, const void* rec, const TokenWindow& win, long long N, int d_v,
+                        int W, int R, float* o, const ScanShape& shape, cudaStream_t s) {
+  if (win.Tc == 0 || win.BH == 0) return SDM_OK;
   ScanArgs sa;
   sa.M = M;
-  sa.rec = static_cast<const unsigned char*>(workspace);
+  sa.rec = static_cast<const unsigned char*>(rec);
   sa.o = o;
-  sa.T = T;
+  sa.T = win.Tc;
+  sa.T_total = win.T_total;
+  sa.t_off = win.t0;
   sa.N = N;
   sa.d_v = d_v;
   sa.W = W;
   sa.R = R;
-  sa.L = L;
+  sa.L = rec_layout(W, R, d_v);
   ScanFn fn = scan_fn(shape.cols, shape.pd);
   if (!fn) return SDM_EUNSUPPORTED;
   if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
                            cudaFuncAttributeMaxDynamicSharedMemorySize, shape.smem) != cudaSuccess)
     return SDM_ECUDA;
-  fn<<<shape.blocks, kScanThreads, shape.smem, s>>>(sa);
+  fn<<<win.BH * (d_v / shape.cols), kScanThreads, shape.smem, s>>>(sa);
   return last_launch_status();
+}
+
+int launch_scan(float* M, const int32_t* idx_w, const float* sc_w, const int32_t* idx_r,
+                const float* sc_r, const void* v, int v_dt, const float* alpha, const float* beta,
+                const TokenWindow& win, long long N, int d_v, int W, int R, float* o,
+                void* workspace, int* dev_err, const ScanShape& shape, cudaEvent_t after_plan,
+                cudaEvent_t wait_before_scan, cudaStream_t s) {
+  if (win.Tc == 0 || win.BH == 0) return SDM_OK;
+  const int st = launch_plan(idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, win, N, d_v, W, R,
+                             shape.pd, workspace, dev_err, s);
+  if (st != SDM_OK) return st;
+  if (wait_before_scan && cudaStreamWaitEvent(s, wait_before_scan, 0) != cudaSuccess)
+    return SDM_ECUDA;
+  if (after_plan && cudaEventRecord(after_plan, s) != cudaSuccess) return SDM_ECUDA;
+  return launch_scan_records(M, workspace, win, N, d_v, W, R, o, shape, s);
 }
 
 }  // namespace sdm

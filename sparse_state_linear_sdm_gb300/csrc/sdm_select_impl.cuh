@@ -469,7 +469,8 @@ __host__ __device__ inline size_t select_per_warp_bytes(int kpad, int kin_max, i
 struct SelectArgs {
   const void* kp;
   const void* qp;
-  long long items;
+  long long items;     // (b, h, t) triples of the token window: BH * Tc
+  int Tc, T_total, t0;  // window tokens [t0, t0 + Tc) of sequences of T_total tokens
   int S, W, R;
   int kin_max;   // max(min(W,S), min(R,S))
   int kpad;      // max(W, R, 32) rounded up to a power of two (selected-key buffer)
@@ -560,7 +561,10 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
   const long long task1 = task0 + a.tpw < tasks ? task0 + a.tpw : tasks;
   for (long long task = task0; task < task1; ++task) {
     const int which = int(task & 1);
-    const long long item = task >> 1;
+    // (b, h, t) triple in the full [B, H, T_total] arrays
+    const long long wi = task >> 1;
+    const long long item =
+        a.Tc == a.T_total ? wi : (wi / a.Tc) * a.T_total + a.t0 + wi % a.Tc;
     const int K = which ? a.R : a.W;
     const int kin = min(K, S);
     const Tin* halves = static_cast<const Tin*>(which ? a.qp : a.kp) + item * 2 * S;
@@ -652,14 +656,18 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
 }
 
 template <typename Tin>
-int launch_select_t(const void* kp, const void* qp, long long items, int S, int W, int R,
+int launch_select_t(const void* kp, const void* qp, const TokenWindow& win, int S, int W, int R,
                     int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, cudaStream_t s) {
   constexpr bool kBf16 = sizeof(Tin) == 2;
+  const long long items = (long long)win.BH * win.Tc;
   if (items == 0) return SDM_OK;
   SelectArgs a;
   a.kp = kp;
   a.qp = qp;
   a.items = items;
+  a.Tc = win.Tc;
+  a.T_total = win.T_total;
+  a.t0 = win.t0;
   a.S = S;
   a.W = W;
   a.R = R;

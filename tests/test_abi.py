@@ -115,3 +115,40 @@ def test_api_requires_cuda_tensors():
     x = torch.zeros(1, 1, 4, 2, 8)
     with pytest.raises(TypeError):
         sdm.select(x, x, 4, 4)
+
+
+def test_forward_rejects_bad_arguments_without_launching():
+    lib = sdm.lib()
+
+    def call(B=1, H=1, T=8, S=8, dv=16, W=4, R=4, in_dt=1, v_dt=0, ws=FAKE, ws_bytes=1 << 30, chunks=0,
+             M0=None, kp=FAKE, M=FAKE):
+        return lib.sdm_forward_tuned(kp, FAKE, in_dt, FAKE, v_dt, FAKE, FAKE, M0, M, B, H, T, S, dv, W, R,
+                                     FAKE, FAKE, FAKE, FAKE, FAKE, ws, ws_bytes, None, chunks, None, None)
+
+    assert call(dv=6) == EINVAL
+    assert call(in_dt=3) == EINVAL
+    assert call(v_dt=3) == EINVAL
+    assert call(W=65) == EINVAL                 # more slots than N = S * S = 64
+    assert call(chunks=-1) == EINVAL
+    assert call(S=5000) == EUNSUPPORTED
+    assert call(kp=ODD) == EALIGN
+    assert call(M=ODD) == EALIGN
+    assert call(M0=ODD) == EALIGN
+    assert call(ws=ODD) == EALIGN
+    assert call(ws_bytes=16) == ENOSPACE
+
+
+def test_forward_chunking_and_workspace_sizes():
+    lib = sdm.lib()
+    assert lib.sdm_forward_chunks(8192, 0) == 8      # about 1024 tokens per chunk
+    assert lib.sdm_forward_chunks(8192, 3) == 3
+    assert lib.sdm_forward_chunks(1000, 0) == 1
+    assert lib.sdm_forward_chunks(5, 8) == 5         # never more chunks than tokens
+    assert lib.sdm_forward_chunks(0, 0) == 0
+    # one record, W = R = 10 (20 slots), d_v = 16: slots, weights, sources (padded to 8),
+    # alpha/beta block, v
+    rec = 4 * 20 + 4 * 20 + 2 * 24 + 16 + 4 * 16
+    assert rec == 288
+    # two record buffers of B*H*ceil(T/chunks) records, each rounded up to 256 bytes
+    assert lib.sdm_forward_workspace_size(2, 3, 100, 16, 10, 10, 4) == 2 * ((6 * 25 * rec + 255) // 256 * 256)
+    assert lib.sdm_forward_workspace_size(1, 1, 0, 16, 4, 4, 0) == 0
