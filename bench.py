@@ -116,6 +116,37 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+SELECT_SRC = [os.path.join(ROOT, "sparse_state_linear_sdm_gb300", "csrc", f)
+              for f in ("sdm_select_impl.cuh", "sdm_select_bf16.cu", "sdm_select_f32.cu")]
+SELECT_FILE = os.path.join(ROOT, "profiles", "select_kernel_instructions.json")
+SMS, SMSP_PER_SM = 152, 4
+
+
+def select_roofline(cfg, units: int, select_ms: float, clocks):
+    """The selection kernel is bound by instruction issue: warp-instructions per selection
+    (ncu, this workload, this kernel source) x selections / its time alone, against one
+    warp-instruction per clock per SM sub-partition at the sampled SM clock."""
+    try:
+        with open(SELECT_FILE) as f:
+            rec = json.load(f)
+        h = hashlib.sha256()
+        for p in SELECT_SRC:
+            with open(p, "rb") as f:
+                h.update(f.read())
+        if rec.get("source_sha256") != h.hexdigest() or rec.get("workload") != cfg.name:
+            return None
+        mhz = (clocks or {}).get("sm_mhz") or 2070.0
+        achieved = rec["warp_instructions_per_selection"] * 2 * units / (select_ms / 1e3) / 1e9
+        peak = SMS * SMSP_PER_SM * mhz / 1e3
+        return {"kernel": "sdm select kernel", "bound": "alu", "achieved": achieved, "peak": peak,
+                "unit": "G warp-instructions/s", "frac": achieved / peak,
+                "peak_source": f"derived: {SMS} SMs x {SMSP_PER_SM} issue slots/clock x {mhz:.0f} MHz",
+                "warp_instructions_per_selection": rec["warp_instructions_per_selection"],
+                "ms_alone": select_ms}
+    except Exception:
+        return None
+
+
 def traffic_per_launch(units: int):
     """DRAM bytes per scan launch from the committed ncu summary, scaled from its
     captured case by head-tokens; None if absent or taken on another kernel source."""
@@ -314,19 +345,28 @@ def config_dict(cfg, pipelined=True):
 
 
 def one_stream_breakdown(st, cfg, sdm, args, torch, dev, reps=3):
-    """Each kernel's time on the one-stream step (init on a side stream || select, then plan,
-    then scan), outside the timed region: what the pipelined step overlaps."""
+    """Each kernel alone, one after the other on the current stream (outside the timed
+    region): state initialisation, selection, planning, scan over the whole sequence."""
     E = lambda: torch.cuda.Event(enable_timing=True)
-    run_step(st, cfg, sdm, args)
-    evs = [[E() for _ in range(5)] for _ in range(reps)]
-    for e in evs:
-        run_step(st, cfg, sdm, args, e)
-    torch.cuda.synchronize(dev)
-    return {"init_ms": sum(e[0].elapsed_time(e[1]) for e in evs) / reps,
-            "select_ms": sum(e[0].elapsed_time(e[2]) for e in evs) / reps,
-            "plan_ms": sum(e[2].elapsed_time(e[3]) for e in evs) / reps,
-            "scan_ms": sum(e[3].elapsed_time(e[4]) for e in evs) / reps,
-            "step_ms": sum(e[0].elapsed_time(e[4]) for e in evs) / reps}
+    res = {"init_ms": [], "select_ms": [], "plan_ms": [], "scan_ms": []}
+    for r in range(reps + 1):
+        e = [E() for _ in range(5)]
+        e[0].record()
+        sdm.init_state_from_M0(st["M"], st["M0"])
+        e[1].record()
+        sdm.select(st["kp"], st["qp"], cfg.W, cfg.R, out=st["sel"])
+        e[2].record()
+        sdm.scan_forward(st["M"], *st["sel"], st["v"], st["alpha"], st["beta"], o=st["o"], workspace=st["ws"],
+                         dev_err=st["err"], event_after_plan=e[3])
+        e[4].record()
+        torch.cuda.synchronize(dev)
+        if r == 0:
+            continue
+        for i, k in enumerate(("init_ms", "select_ms", "plan_ms", "scan_ms")):
+            res[k].append(e[i].elapsed_time(e[i + 1]))
+    out = {k: sum(v) / len(v) for k, v in res.items()}
+    out["sum_ms"] = sum(out.values())
+    return out
 
 
 def run_ours(args):
@@ -402,7 +442,7 @@ def run_ours(args):
                  "chunks": chunks, "tokens_per_chunk": -(-cfg.T // chunks),
                  "overlap": "sdm_forward: init (high-priority stream) || select+plan of chunk c+1 "
                             "(select stream) || scan of chunk c (high-priority stream)"}
-        phase["one_stream_breakdown"] = one_stream_breakdown(st, cfg, sdm, args, torch, dev)
+        phase["alone"] = one_stream_breakdown(st, cfg, sdm, args, torch, dev)
         launches_per_step = 1 + 3 * chunks
     else:
         scan_launch_ms = sum(e[3].elapsed_time(e[4]) for e in kern_ev) / K
@@ -435,11 +475,13 @@ def run_ours(args):
             "gpu_launches": launches_per_step * K}
     if pipelined:
         # the same kernel over the whole sequence with nothing else running (one-stream step)
-        alone_ms = phase["one_stream_breakdown"]["scan_ms"]
+        alone_ms = phase["alone"]["scan_ms"]
         alone = scan_bytes_per_head_token(cfg) * units_rank / (alone_ms / 1e3) / 1e9
         line["roofline"]["alone"] = {"achieved": alone, "frac": alone / peak, "ms_per_launch": alone_ms,
-                                     "note": "scan kernel over all T tokens, timed on the one-stream step"}
+                                     "note": "scan kernel over all T tokens, timed alone"}
     line["clocks"] = clk.summary()
+    if pipelined:
+        line["select_roofline"] = select_roofline(cfg, units_rank, phase["alone"]["select_ms"], line["clocks"])
 
     if not args.no_e2e:
         line["e2e"] = e2e(st, cfg, sdm, args, dev, torch, K, world)
