@@ -55,6 +55,9 @@ def _load():
             lib.oracle_select.restype = i32
             lib.oracle_scan.argtypes = [p, i32, i64, i32, i32, i32, i32, p, p, p, p, p, p, p, p, i32]
             lib.oracle_scan.restype = i32
+            lib.oracle_scan_backward.argtypes = [p, i32, i64, i32, i32, i32, i32, p, p, p, p, p, p, p,
+                                                 p, p, p, p, p, p, p, i32]
+            lib.oracle_scan_backward.restype = i32
             _lib = lib
     return _lib
 
@@ -148,3 +151,51 @@ def forward(kp, qp, v, alpha, beta, M_init, W: int, R: int, n_threads=None):
     M = np.array(M_init, dtype=np.float64, order="C", copy=True)
     o = scan(M, idx_w, sc_w, idx_r, sc_r, v, alpha, beta, n_threads)
     return dict(idx_w=idx_w, sc_w=sc_w, idx_r=idx_r, sc_r=sc_r, o=o, M=M)
+
+
+def scan_backward(M_init, idx_w, sc_w, idx_r, sc_r, v, alpha, beta, dO, dMT=None, n_threads=None):
+    """Reverse-mode derivative of ``scan`` for L = sum_t <dO_t, o_t> + <dMT, M_T>, slots fixed.
+
+    M_init: [nh, N, d_v] state before token 0 (not modified); dO: [nh, T, d_v];
+    dMT: [nh, N, d_v] or None (zero).  Returns float64 dict(dv [nh,T,d_v], dalpha [nh,T],
+    dbeta [nh,T], dsc_w [nh,T,W], dsc_r [nh,T,R], dM0 [nh,N,d_v]) (dM0 per (sequence,
+    head): a learned M_0 shared by the batch receives the sum over the batch).
+    """
+    M = _c(M_init, np.float64)
+    nh, N, dv = M.shape
+    iw, sw = _c(idx_w, np.int32), _c(sc_w, np.float32)
+    ir, sr = _c(idx_r, np.int32), _c(sc_r, np.float32)
+    vv = _c(v, np.float32)
+    a, b = _c(alpha, np.float32), _c(beta, np.float32)
+    T, W = iw.shape[1], iw.shape[2]
+    R = ir.shape[2]
+    dO = _c(dO, np.float64)
+    G = np.zeros((nh, N, dv), np.float64) if dMT is None else np.array(dMT, np.float64, order="C", copy=True)
+    out = dict(dv=np.empty((nh, T, dv)), dalpha=np.empty((nh, T)), dbeta=np.empty((nh, T)),
+               dsc_w=np.empty((nh, T, W)), dsc_r=np.empty((nh, T, R)))
+    rc = _load().oracle_scan_backward(M.ctypes.data, nh, N, dv, T, W, R, iw.ctypes.data, sw.ctypes.data,
+                                      ir.ctypes.data, sr.ctypes.data, vv.ctypes.data, a.ctypes.data,
+                                      b.ctypes.data, dO.ctypes.data, G.ctypes.data, out["dv"].ctypes.data,
+                                      out["dalpha"].ctypes.data, out["dbeta"].ctypes.data,
+                                      out["dsc_w"].ctypes.data, out["dsc_r"].ctypes.data, _threads(n_threads))
+    if rc != 0:
+        raise ValueError("oracle_scan_backward: bad sizes or slot index out of range")
+    out["dM0"] = G
+    return out
+
+
+def select_backward(S: int, idx, dsc):
+    """Gradient of the selected scores with respect to the two halves they are sums of:
+    sc = half0[flat // S] + half1[flat % S], so each half entry receives the sum of dsc
+    over the selected slots that use it.  idx: int [..., K]; dsc: [..., K].
+    Returns float64 [..., 2, S]."""
+    idx = np.asarray(idx)
+    dsc = np.asarray(dsc, np.float64)
+    lead = idx.shape[:-1]
+    flat_i = idx.reshape(-1, idx.shape[-1])
+    flat_d = dsc.reshape(-1, dsc.shape[-1])
+    out = np.zeros((flat_i.shape[0], 2, S))
+    rows = np.arange(flat_i.shape[0])[:, None]
+    np.add.at(out[:, 0], (rows, flat_i // S), flat_d)
+    np.add.at(out[:, 1], (rows, flat_i % S), flat_d)
+    return out.reshape(lead + (2, S))
