@@ -52,8 +52,9 @@ def parse_args():
                     help="on: sdm_forward (selection of chunk c+1 overlaps the scan of chunk c); "
                          "off: init || select, then plan and scan, one kernel after the other")
     ap.add_argument("--override", default="", help="size overrides for profiling, e.g. S=256,T=512")
-    ap.add_argument("--mode", choices=["forward", "decode"], default="forward",
-                    help="decode: one token per step for the batch, state resident, CUDA graph")
+    ap.add_argument("--mode", choices=["forward", "decode", "backward"], default="forward",
+                    help="decode: one token per step for the batch, state resident, CUDA graph; "
+                         "backward: the training backward pass (reverse scan, score and half gradients)")
     return ap.parse_args()
 
 
@@ -620,6 +621,96 @@ def run_decode(args):
     print(json.dumps(line), flush=True)
 
 
+def backward_bytes_per_head_token(cfg) -> int:
+    """Algorithmic bytes of the backward scan per head-token: dO; the stored write rows
+    (before their update) and read rows; the adjoint rows gathered and scattered at every
+    write and read slot; v, alpha, beta; slots and scores; dv (fp32 d_v-vectors)."""
+    K = cfg.W + cfg.R
+    elt = 2 if cfg.in_dtype == "bf16" else 4
+    return cfg.d_v * 4 + K * cfg.d_v * 4 + 2 * K * cfg.d_v * 4 + cfg.d_v * elt + 8 + K * 8 + cfg.d_v * 4
+
+
+def run_backward(args):
+    """Training backward of one forward pass: with the forward's stored rows, K steps of
+    (adjoint table zeroed: no gradient on the final state; reverse scan with the finish
+    and the batch reduction into dM_0; half gradients of k' and q')."""
+    import torch
+
+    import sparse_state_linear_sdm_gb300 as sdm
+    from sparse_state_linear_sdm_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = workload(args)
+    st = make_state(cfg, rank, dev, torch, sdm, wl)
+    del st["fws"]
+    sel = st["sel"]
+    sdm.select(st["kp"], st["qp"], cfg.W, cfg.R, out=sel)
+    sdm.init_state_from_M0(st["M"], st["M0"])
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    f0, f1 = E(), E()
+    f0.record()
+    o, w_prev, r_rows = sdm.scan_forward_train(st["M"], *sel, st["v"], st["alpha"], st["beta"], o=st["o"],
+                                               workspace=st["ws"], dev_err=st["err"])
+    f1.record()
+    gen = torch.Generator(device=dev).manual_seed(cfg.seed)
+    dO = torch.randn((cfg.B, cfg.H, cfg.T, cfg.d_v), generator=gen, device=dev)
+    G = st["M"]   # the state is not needed any more: its buffer holds the adjoint
+    ws = torch.empty(sdm.lib().sdm_scan_backward_workspace_size(cfg.B, cfg.H, cfg.T, cfg.d_v, cfg.W, cfg.R),
+                     dtype=torch.uint8, device=dev)
+    dkp = torch.empty((cfg.B, cfg.H, cfg.T, 2, cfg.S), device=dev)
+    dqp = torch.empty_like(dkp)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record()
+        G.zero_()
+        if ev:
+            ev[1].record()
+        g = sdm.scan_backward(*sel, st["v"], st["alpha"], st["beta"], w_prev, r_rows, dO, G, workspace=ws)
+        if ev:
+            ev[2].record()
+        sdm.select_backward(sel[0], g["dsc_w"], cfg.S, out=dkp)
+        sdm.select_backward(sel[2], g["dsc_r"], cfg.S, out=dqp)
+        if ev:
+            ev[3].record()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    evs = [[E() for _ in range(4)] for _ in range(K)]
+    with ClockSampler(local) as clk:
+        for k in range(K):
+            step(evs[k])
+        torch.cuda.synchronize(dev)
+    total = evs[0][0].elapsed_time(evs[-1][3])
+    zero_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / K
+    scan_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / K
+    sel_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / K
+    units = cfg.B * cfg.H * cfg.T
+    peak, peak_kind = hbm_peak()
+    alg = backward_bytes_per_head_token(cfg) * units
+    achieved = alg / (scan_ms / 1e3) / 1e9
+    line = {"metric": "SDM backward head-tokens/s on 1 GB300 (reverse scan, score and half gradients)",
+            "value": whole_job_rate(units, K, world, total), "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": total / K, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": dict(config_dict(cfg), step="backward: zero the adjoint, reverse scan + finish + dM0 "
+                                                  "reduction, select backward for k' and q'"),
+            "roofline": {"kernel": "sdm_scan_backward (reverse scan, finish, batch reduction)", "bound": "hbm",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "algorithmic_bytes_per_launch": alg, "traffic": None,
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                         else "fallback"},
+            "kernels": {"forward_train_ms": f0.elapsed_time(f1), "zero_adjoint_ms": zero_ms,
+                        "scan_backward_ms": scan_ms, "select_backward_ms": sel_ms},
+            "gpu_launches": 5 * K, "clocks": clk.summary()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def dataclasses_replace(cfg, **kw):
     import dataclasses
 
@@ -632,6 +723,8 @@ def main():
         run_reference(args)
     elif args.mode == "decode":
         run_decode(args)
+    elif args.mode == "backward":
+        run_backward(args)
     else:
         run_ours(args)
 

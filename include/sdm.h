@@ -203,6 +203,53 @@ int sdm_forward_tuned(const void* kp, const void* qp, int in_dt, const void* v, 
                       size_t workspace_bytes, int* dev_err, int chunks, void* const* scan_events,
                       void* stream);
 
+/* Backward pass (training) of the scan, for the loss L = sum_t <dO_t, o_t> + <dM_T, M_T>
+ * with the selected slots held fixed (they are discrete); gradients reach v, alpha, beta,
+ * the selected write and read scores, the initial state ("Stato Iniziale Appreso": M_0 is
+ * learned) and, through sdm_select_backward, the k' / q' halves ("Meccanismo Core" item 2:
+ * a selected score is half0[i] + half1[j]).
+ *
+ * sdm_scan_forward_train - sdm_scan_forward that also stores what the backward needs:
+ *   w_prev [B, H, T, W, d_v] fp32: every write row before its update (M_{t-1}[idx_w]);
+ *   r_rows [B, H, T, R, d_v] fp32: every read row as read (M_t[idx_r]).
+ * Rows of invalid slots (dev_err SDM_DEV_INDEX_RANGE) are not stored. */
+int sdm_scan_forward_train(float* M, const int32_t* idx_w, const float* sc_w,
+                           const int32_t* idx_r, const float* sc_r, const void* v, int v_dt,
+                           const float* alpha, const float* beta, int B, int H, int T,
+                           long long N, int d_v, int W, int R, float* o, float* w_prev,
+                           float* r_rows, void* workspace, size_t workspace_bytes, int* dev_err,
+                           void* stream);
+
+/* sdm_scan_backward - the reverse-mode pass.
+ *   idx/sc, v, alpha, beta: as given to sdm_scan_forward_train; w_prev, r_rows: its outputs.
+ *   dO     [B, H, T, d_v] fp32: dL/do.
+ *   G      [B, H, N, d_v] fp32, in: dL/dM_T (zeros when the final state carries no
+ *          gradient), out: dL/dM_0 for each (b, h) (overwritten in place).
+ *   dv     [B, H, T, d_v] fp32; dalpha, dbeta [B, H, T]; dsc_w [B, H, T, W];
+ *          dsc_r [B, H, T, R]: written.
+ *   dM0    [H, N, d_v] fp32 or NULL: if given, the sum of the output G over the batch
+ *          (the gradient of an M_0 shared by the batch).
+ *   workspace  at least sdm_scan_backward_workspace_size(...) bytes, 16-byte aligned,
+ *          contents irrelevant.
+ * Requires d_v % 4 == 0 and the limits of sdm_scan_forward; slots outside [0, N) are
+ * skipped (their gradients are unspecified). */
+size_t sdm_scan_backward_workspace_size(int B, int H, int T, int d_v, int W, int R);
+int sdm_scan_backward(const int32_t* idx_w, const float* sc_w, const int32_t* idx_r,
+                      const float* sc_r, const void* v, int v_dt, const float* alpha,
+                      const float* beta, const float* w_prev, const float* r_rows,
+                      const float* dO, int B, int H, int T, long long N, int d_v, int W, int R,
+                      float* G, float* dv, float* dalpha, float* dbeta, float* dsc_w,
+                      float* dsc_r, float* dM0, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/* sdm_select_backward - gradient of the selected scores with respect to the halves:
+ * dhalves[b, h, t, 0, i] = sum of dsc over the selected slots with flat / S == i, and
+ * dhalves[b, h, t, 1, j] over those with flat % S == j.  idx, dsc [B, H, T, K] (as from
+ * sdm_select and sdm_scan_backward); dhalves [B, H, T, 2, S] fp32, overwritten.  The sums
+ * use atomic adds: their order, and so the last bits, may vary from run to run. */
+int sdm_select_backward(const int32_t* idx, const float* dsc, int B, int H, int T, int S, int K,
+                        float* dhalves, void* stream);
+
 /* sdm_gen_inputs - synthetic inputs (not part of the method): draws the box
  * b in [b_off, b_off+B), all H heads, tokens t in [t_off, t_off+T) of a logical
  * workload with T_total tokens per sequence, from the counter-based generator

@@ -6,11 +6,11 @@ seeded synthetic configurations.  Importing the package does not load the
 library; the first API call does (and fails loudly if it cannot).
 """
 from .api import (SDM_BF16, SDM_DEV_DUP_WRITE, SDM_DEV_INDEX_RANGE, SDM_F32, DecodeStep, SDMError, forward,
-                  forward_chunks, forward_workspace,
+                  forward_chunks, forward_workspace, scan_backward, scan_forward_train, select_backward,
                   gen_inputs, gen_M0, init_state_from_M0, lib, library_path, scan_forward,
                   scan_launch_info, scan_workspace, scan_workspace_size, select, side_stream)
 
 __all__ = ["SDM_BF16", "SDM_DEV_DUP_WRITE", "SDM_DEV_INDEX_RANGE", "SDM_F32", "DecodeStep", "SDMError", "forward",
-           "forward_chunks", "forward_workspace",
+           "forward_chunks", "forward_workspace", "scan_backward", "scan_forward_train", "select_backward",
            "gen_inputs", "gen_M0", "init_state_from_M0", "lib", "library_path", "scan_forward",
            "scan_launch_info", "scan_workspace", "scan_workspace_size", "select", "side_stream"]

@@ -57,9 +57,16 @@ def lib() -> ctypes.CDLL:
             L.sdm_forward_tuned.argtypes = [p, p, i, p, i, p, p, p, p, i, i, i, i, i, i, i, p, p, p, p, p, p,
                                             sz, p, i, p, p]
             L.sdm_forward.argtypes = [p, p, i, p, i, p, p, p, p, i, i, i, i, i, i, i, p, p, p, p, p, p, sz, p, p]
+            L.sdm_scan_forward_train.argtypes = [p, p, p, p, p, p, i, p, p, i, i, i, ll, i, i, i, p, p, p, p, sz, p, p]
+            L.sdm_scan_backward_workspace_size.argtypes = [i, i, i, i, i, i]
+            L.sdm_scan_backward_workspace_size.restype = sz
+            L.sdm_scan_backward.argtypes = [p, p, p, p, p, i, p, p, p, p, p, i, i, i, ll, i, i, i, p, p, p, p, p, p,
+                                            p, p, sz, p]
+            L.sdm_select_backward.argtypes = [p, p, i, i, i, i, i, p, p]
             for name in ("sdm_init_state_from_M0", "sdm_select", "sdm_scan_forward",
                          "sdm_scan_forward_tuned", "sdm_scan_launch_info", "sdm_gen_inputs", "sdm_gen_M0",
-                         "sdm_forward_chunks", "sdm_forward_tuned", "sdm_forward"):
+                         "sdm_forward_chunks", "sdm_forward_tuned", "sdm_forward", "sdm_scan_forward_train",
+                         "sdm_scan_backward", "sdm_select_backward"):
                 getattr(L, name).restype = i
             _lib = L
     return _lib
@@ -352,6 +359,68 @@ def forward(kp, qp, v, alpha, beta, M0, W: int, R: int, M=None, workspace=None, 
           _p(M0), _p(M), B, H, T, S, dv, W, R, _p(idx_w), _p(sc_w), _p(idx_r), _p(sc_r), _p(o),
           _p(workspace), workspace.numel(), _p(dev_err), int(chunks), ev_arr, _stream(M.device))
     return o, M, out
+
+
+def scan_forward_train(M, idx_w, sc_w, idx_r, sc_r, v, alpha, beta, o=None, workspace=None, dev_err=None):
+    """scan_forward that also keeps what scan_backward needs.  Returns (o, w_prev, r_rows):
+    w_prev [B,H,T,W,d_v] every write row before its update, r_rows [B,H,T,R,d_v] every read
+    row as read (fp32)."""
+    _need(M, "M", torch.float32)
+    B, H, N, dv = M.shape
+    T, W, R = idx_w.shape[2], idx_w.shape[3], idx_r.shape[3]
+    for t_, n_, dt_, sh_ in ((idx_w, "idx_w", torch.int32, (B, H, T, W)), (sc_w, "sc_w", torch.float32, (B, H, T, W)),
+                             (idx_r, "idx_r", torch.int32, (B, H, T, R)), (sc_r, "sc_r", torch.float32, (B, H, T, R)),
+                             (v, "v", None, (B, H, T, dv)), (alpha, "alpha", torch.float32, (B, H, T)),
+                             (beta, "beta", torch.float32, (B, H, T))):
+        _need(t_, n_, dt_, sh_)
+    if o is None:
+        o = torch.empty((B, H, T, dv), dtype=torch.float32, device=M.device)
+    w_prev = torch.empty((B, H, T, W, dv), dtype=torch.float32, device=M.device)
+    r_rows = torch.empty((B, H, T, R, dv), dtype=torch.float32, device=M.device)
+    if workspace is None:
+        workspace = scan_workspace(B, H, T, dv, W, R, M.device)
+    _call("sdm_scan_forward_train", _p(M), _p(idx_w), _p(sc_w), _p(idx_r), _p(sc_r), _p(v), _dtype_code(v),
+          _p(alpha), _p(beta), B, H, T, N, dv, W, R, _p(o), _p(w_prev), _p(r_rows), _p(workspace),
+          workspace.numel(), _p(dev_err), _stream(M.device))
+    return o, w_prev, r_rows
+
+
+def scan_backward(idx_w, sc_w, idx_r, sc_r, v, alpha, beta, w_prev, r_rows, dO, G, shared_M0: bool = True,
+                  workspace=None):
+    """Reverse-mode pass of the scan for L = sum_t <dO_t, o_t> + <dM_T, M_T>, slots fixed.
+    G: fp32 [B,H,N,d_v], in dL/dM_T, out dL/dM_0 per (b, h) (in place).  Returns
+    dict(dv, dalpha, dbeta, dsc_w, dsc_r, dM0) with dM0 = sum of G over the batch
+    (shared_M0) or None."""
+    _need(G, "G", torch.float32)
+    B, H, N, dv = G.shape
+    T, W, R = idx_w.shape[2], idx_w.shape[3], idx_r.shape[3]
+    _need(dO, "dO", torch.float32, (B, H, T, dv))
+    _need(w_prev, "w_prev", torch.float32, (B, H, T, W, dv))
+    _need(r_rows, "r_rows", torch.float32, (B, H, T, R, dv))
+    dev = G.device
+    out = dict(dv=torch.empty((B, H, T, dv), device=dev), dalpha=torch.empty((B, H, T), device=dev),
+               dbeta=torch.empty((B, H, T), device=dev), dsc_w=torch.empty((B, H, T, W), device=dev),
+               dsc_r=torch.empty((B, H, T, R), device=dev),
+               dM0=torch.empty((H, N, dv), device=dev) if shared_M0 else None)
+    if workspace is None:
+        n = lib().sdm_scan_backward_workspace_size(B, H, T, dv, W, R)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+    _call("sdm_scan_backward", _p(idx_w), _p(sc_w), _p(idx_r), _p(sc_r), _p(v), _dtype_code(v), _p(alpha), _p(beta),
+          _p(w_prev), _p(r_rows), _p(dO), B, H, T, N, dv, W, R, _p(G), _p(out["dv"]), _p(out["dalpha"]),
+          _p(out["dbeta"]), _p(out["dsc_w"]), _p(out["dsc_r"]), _p(out["dM0"]), _p(workspace), workspace.numel(),
+          _stream(dev))
+    return out
+
+
+def select_backward(idx, dsc, S: int, out=None):
+    """Gradient of the selected scores with respect to the halves: [B,H,T,2,S] fp32."""
+    _need(idx, "idx", torch.int32)
+    B, H, T, K = idx.shape
+    _need(dsc, "dsc", torch.float32, (B, H, T, K))
+    if out is None:
+        out = torch.empty((B, H, T, 2, S), dtype=torch.float32, device=idx.device)
+    _call("sdm_select_backward", _p(idx), _p(dsc), B, H, T, S, K, _p(out), _stream(idx.device))
+    return out
 
 
 class DecodeStep:

@@ -1,0 +1,427 @@
+// Backward pass of the sparse gated-delta scan (Sparse Delta Memory technical summary,
+// gist.science/it/paper/2607.07386, "Meccanismo Core" items 2-4; the learned initial state
+// of "Stato Iniziale Appreso" receives dL/dM_0).  Reverse mode for the loss
+// L = sum_t <dO_t, o_t> + <dM_T, M_T>, with the selected slots held fixed (they are
+// discrete).  The forward (sdm_scan_forward_train) keeps, per token, the write rows before
+// their update (w_prev) and the read rows as read (r_rows); the backward walks the tokens
+// from last to first with the adjoint G = dL/dM_t, a table like M:
+//   read   o_t = sum_j r_j M_t[ir_j]:  G[ir_j] += r_j dO_t,  dr_j = <dO_t, M_t[ir_j]>
+//   write  M_t[i] = a M_{t-1}[i] + b k_i (v_t - a M_{t-1}[i]), with G after the read:
+//          dv_t += b k_i G[i],  ge_i = <G[i], v_t - a M_{t-1}[i]>,  gm_i = <G[i], M_{t-1}[i]>,
+//          then G[i] <- a (1 - b k_i) G[i]
+//   finish dk_i = b ge_i,  da_t = sum_i (1 - b k_i) gm_i,  db_t = sum_i k_i ge_i, and the
+//          softmax backward ds_i = w_i (dw_i - sum_l w_l dw_l) for the write and read scores.
+//
+// Kernels: the reverse scan (one block per (b, h, slice of columns), sequential in t; the
+// dot products over d_v leave one partial per slice), a finish kernel (one warp per token:
+// sums the slices' partials, softmax backward), a batch reduction of G into dM_0, and the
+// selection backward (a selected score is half0[i] + half1[j]).
+#include "sdm_internal.cuh"
+
+namespace sdm {
+namespace {
+
+constexpr int kBwdThreads = 256;
+constexpr int kBwdWarps = kBwdThreads / 32;
+
+struct BwdArgs {
+  const int32_t* idx_w;
+  const float* sc_w;
+  const int32_t* idx_r;
+  const float* sc_r;
+  const void* v;
+  int v_bf16;
+  const float* alpha;
+  const float* beta;
+  const float* w_prev;
+  const float* r_rows;
+  const float* dO;
+  float* G;
+  float* dv;
+  float* part;  // [BH, T, slices, 2W + R]: ge (W), gm (W), dr (R) of one column slice
+  int T;
+  long long N;
+  int d_v, W, R;
+};
+
+__device__ __forceinline__ float4 load_v4(const void* v, int bf16, size_t i4) {
+  if (bf16) {
+    const uint2 u = reinterpret_cast<const uint2*>(v)[i4];
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+  }
+  return reinterpret_cast<const float4*>(v)[i4];
+}
+
+__device__ __forceinline__ float dot4(float4 a, float4 b) {
+  return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, a.x * b.x)));
+}
+
+// Sum over the LPR lanes that hold one row slice (lanes differing in the low bits).
+template <int LPR>
+__device__ __forceinline__ float slice_sum(float x) {
+#pragma unroll
+  for (int off = 1; off < LPR; off <<= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, off);
+  return x;
+}
+
+template <int C>
+__global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
+  constexpr int LPR = C / 4;                 // threads per row slice (one float4 each)
+  constexpr int RPP = kBwdThreads / LPR;     // row slices per pass
+  constexpr int NB = 4;                      // rows per thread per round, loaded together
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int W = a.W, R = a.R, T = a.T, d_v = a.d_v;
+  const int WRa = (W + R + 3) & ~3;
+  float* kw = reinterpret_cast<float*>(smem);        // [W] write weights of the token
+  float* rw = kw + W;                                 // [R] read weights
+  float* red = kw + WRa;                              // [warps][C]
+  int32_t* iw = reinterpret_cast<int32_t*>(red + kBwdWarps * C);  // [W]
+  int32_t* ir = iw + W;                                            // [R]
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int slices = d_v / C;
+  const int bh = blockIdx.x / slices;
+  const int sl = blockIdx.x - bh * slices;
+  const int c0 = sl * C;
+  const int c4 = tid % LPR;
+  const int PW = 2 * W + R;
+  float* Gbh = a.G + size_t(bh) * size_t(a.N) * d_v + c0;
+
+  for (int t = T - 1; t >= 0; --t) {
+    const size_t tk = size_t(bh) * T + t;
+    if (warp == 0) warp_softmax(a.sc_w + tk * W, W, kw);
+    if (warp == 1) warp_softmax(a.sc_r + tk * R, R, rw);
+    for (int i = tid; i < W; i += kBwdThreads) iw[i] = a.idx_w[tk * W + i];
+    for (int j = tid; j < R; j += kBwdThreads) ir[j] = a.idx_r[tk * R + j];
+    __syncthreads();
+    float* part = a.part + (tk * slices + sl) * PW;
+    const float4 dO4 = reinterpret_cast<const float4*>(a.dO + tk * d_v + c0)[c4];
+
+    // Read rows: dr_j (this slice's share) and G[ir_j] += r_j dO_t.  Each thread takes up
+    // to NB rows per round and loads all of them before using any (their latencies
+    // overlap); the round bound is the same for every lane (the shuffles need the whole
+    // warp), `in` marks real rows.
+    for (int jb = 0; jb < R; jb += NB * RPP) {
+      int32_t x[NB];
+      float4 gv[NB], m[NB];
+#pragma unroll
+      for (int u = 0; u < NB; ++u) {
+        const int j = jb + u * RPP + tid / LPR;
+        x[u] = j < R ? ir[j] : -1;
+        const bool ok = x[u] >= 0 && x[u] < a.N;  // uniform over the row's LPR lanes
+        gv[u] = m[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (ok) {
+          gv[u] = reinterpret_cast<const float4*>(Gbh + size_t(x[u]) * d_v)[c4];
+          m[u] = reinterpret_cast<const float4*>(a.r_rows + (tk * R + j) * d_v + c0)[c4];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < NB; ++u) {
+        const int j = jb + u * RPP + tid / LPR;
+        const float s = slice_sum<LPR>(dot4(dO4, m[u]));
+        if (j < R && c4 == 0) part[2 * W + j] = s;
+        if (x[u] >= 0 && x[u] < a.N) {
+          const float r = rw[j];
+          reinterpret_cast<float4*>(Gbh + size_t(x[u]) * d_v)[c4] =
+              make_float4(fmaf(r, dO4.x, gv[u].x), fmaf(r, dO4.y, gv[u].y), fmaf(r, dO4.z, gv[u].z),
+                          fmaf(r, dO4.w, gv[u].w));
+        }
+      }
+    }
+    __syncthreads();  // the read contributions reach G before the write rows load it
+
+    // Write rows: partial dot products, dv, and G propagated to M_{t-1} (same batching).
+    const float al = a.alpha[tk], be = a.beta[tk];
+    const float4 vv = load_v4(a.v, a.v_bf16, (tk * d_v + c0) / 4 + c4);
+    float4 dva = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int ib = 0; ib < W; ib += NB * RPP) {
+      int32_t x[NB];
+      float4 g[NB], wp[NB];
+#pragma unroll
+      for (int u = 0; u < NB; ++u) {
+        const int i = ib + u * RPP + tid / LPR;
+        x[u] = i < W ? iw[i] : -1;
+        g[u] = wp[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (x[u] >= 0 && x[u] < a.N) {
+          g[u] = reinterpret_cast<const float4*>(Gbh + size_t(x[u]) * d_v)[c4];
+          wp[u] = reinterpret_cast<const float4*>(a.w_prev + (tk * W + i) * d_v + c0)[c4];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < NB; ++u) {
+        const int i = ib + u * RPP + tid / LPR;
+        const bool in = i < W;
+        const float4 e = make_float4(fmaf(-al, wp[u].x, vv.x), fmaf(-al, wp[u].y, vv.y),
+                                     fmaf(-al, wp[u].z, vv.z), fmaf(-al, wp[u].w, vv.w));
+        const float ge = slice_sum<LPR>(dot4(g[u], e));
+        const float gm = slice_sum<LPR>(dot4(g[u], wp[u]));
+        if (in && c4 == 0) {
+          part[i] = ge;
+          part[W + i] = gm;
+        }
+        const float bk = in ? be * kw[i] : 0.f;
+        dva.x = fmaf(bk, g[u].x, dva.x);
+        dva.y = fmaf(bk, g[u].y, dva.y);
+        dva.z = fmaf(bk, g[u].z, dva.z);
+        dva.w = fmaf(bk, g[u].w, dva.w);
+        if (x[u] >= 0 && x[u] < a.N) {
+          const float sc = al * (1.f - bk);
+          reinterpret_cast<float4*>(Gbh + size_t(x[u]) * d_v)[c4] =
+              make_float4(sc * g[u].x, sc * g[u].y, sc * g[u].z, sc * g[u].w);
+        }
+      }
+    }
+    // dv_t: sum over the rows held by the other lanes and warps.
+#pragma unroll
+    for (int off = LPR; off < 32; off <<= 1) {
+      dva.x += __shfl_xor_sync(0xFFFFFFFFu, dva.x, off);
+      dva.y += __shfl_xor_sync(0xFFFFFFFFu, dva.y, off);
+      dva.z += __shfl_xor_sync(0xFFFFFFFFu, dva.z, off);
+      dva.w += __shfl_xor_sync(0xFFFFFFFFu, dva.w, off);
+    }
+    if (lane < LPR) reinterpret_cast<float4*>(red + warp * C)[lane] = dva;
+    __syncthreads();
+    if (tid < LPR) {
+      float4 s4 = reinterpret_cast<const float4*>(red)[tid];
+      for (int w = 1; w < kBwdWarps; ++w) {
+        const float4 u = reinterpret_cast<const float4*>(red + w * C)[tid];
+        s4 = make_float4(s4.x + u.x, s4.y + u.y, s4.z + u.z, s4.w + u.w);
+      }
+      reinterpret_cast<float4*>(a.dv + tk * d_v + c0)[tid] = s4;
+    }
+    __syncthreads();  // G of this token is written before the previous token loads it
+  }
+}
+
+size_t backward_smem_bytes(int C, int W, int R) {
+  const int WRa = (W + R + 3) & ~3;
+  return size_t(WRa) * 4 + size_t(kBwdWarps) * C * 4 + size_t(W + R) * 4;
+}
+
+int backward_cols(int d_v) {
+  for (int c : {32, 16, 8, 4})
+    if (d_v % c == 0) return c;
+  return 0;
+}
+
+// One warp per (b, h, t): sums the slices' partials, then the softmax backward.
+__global__ void __launch_bounds__(128) backward_finish_kernel(
+    const float* __restrict__ sc_w, const float* __restrict__ sc_r, const float* __restrict__ beta,
+    const float* __restrict__ part, int slices, int W, int R, long long items, float* dalpha,
+    float* dbeta, float* dsc_w, float* dsc_r) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* k = reinterpret_cast<float*>(smem) + size_t(warp) * 2 * (W + R);
+  float* r = k + W;
+  float* dk = r + R;
+  float* dr = dk + W;
+  const long long item = (long long)blockIdx.x * (blockDim.x >> 5) + warp;
+  if (item >= items) return;
+  warp_softmax(sc_w + item * W, W, k);
+  warp_softmax(sc_r + item * R, R, r);
+  __syncwarp();
+  const int PW = 2 * W + R;
+  const float* p = part + item * slices * PW;
+  const float be = beta[item];
+  float sa = 0.f, sb = 0.f, dotk = 0.f;
+  for (int i = lane; i < W; i += 32) {
+    float ge = 0.f, gm = 0.f;
+    for (int s = 0; s < slices; ++s) {
+      ge += p[s * PW + i];
+      gm += p[s * PW + W + i];
+    }
+    const float d = be * ge;
+    dk[i] = d;
+    dotk = fmaf(k[i], d, dotk);
+    sa = fmaf(1.f - be * k[i], gm, sa);
+    sb = fmaf(k[i], ge, sb);
+  }
+  float dotr = 0.f;
+  for (int j = lane; j < R; j += 32) {
+    float d = 0.f;
+    for (int s = 0; s < slices; ++s) d += p[s * PW + 2 * W + j];
+    dr[j] = d;
+    dotr = fmaf(r[j], d, dotr);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    sa += __shfl_xor_sync(0xFFFFFFFFu, sa, off);
+    sb += __shfl_xor_sync(0xFFFFFFFFu, sb, off);
+    dotk += __shfl_xor_sync(0xFFFFFFFFu, dotk, off);
+    dotr += __shfl_xor_sync(0xFFFFFFFFu, dotr, off);
+  }
+  __syncwarp();
+  for (int i = lane; i < W; i += 32) dsc_w[item * W + i] = k[i] * (dk[i] - dotk);
+  for (int j = lane; j < R; j += 32) dsc_r[item * R + j] = r[j] * (dr[j] - dotr);
+  if (lane == 0) {
+    dalpha[item] = sa;
+    dbeta[item] = sb;
+  }
+}
+
+// dM0[h] = sum over the batch of G[b, h].
+__global__ void reduce_batch_kernel(const float4* __restrict__ G, float4* __restrict__ dM0, int B,
+                                    size_t per_batch4) {
+  const size_t stride = size_t(gridDim.x) * blockDim.x;
+  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < per_batch4; i += stride) {
+    float4 s = G[i];
+    for (int b = 1; b < B; ++b) {
+      const float4 u = G[size_t(b) * per_batch4 + i];
+      s = make_float4(s.x + u.x, s.y + u.y, s.z + u.z, s.w + u.w);
+    }
+    dM0[i] = s;
+  }
+}
+
+// Selection backward, one warp per (b, h, t): dhalves[0][i] and dhalves[1][j] collect the
+// gradients of the selected scores that use them (flat = i * S + j).
+__global__ void __launch_bounds__(128) select_backward_kernel(const int32_t* __restrict__ idx,
+                                                              const float* __restrict__ dsc,
+                                                              long long items, int S, int K,
+                                                              float* dhalves) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long item = (long long)blockIdx.x * (blockDim.x >> 5) + warp;
+  if (item >= items) return;
+  float* dh = dhalves + item * 2 * S;
+  for (int i = lane; i < 2 * S; i += 32) dh[i] = 0.f;
+  __syncwarp();
+  for (int r = lane; r < K; r += 32) {
+    const int32_t f = idx[item * K + r];
+    if (f < 0 || f >= S * S) continue;
+    const float d = dsc[item * K + r];
+    atomicAdd(dh + f / S, d);
+    atomicAdd(dh + S + f % S, d);
+  }
+}
+
+int grid_for(size_t work, int per_block) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return -1;
+  size_t blocks = (work + per_block - 1) / per_block;
+  const size_t cap = size_t(sms) * 8;
+  return int(blocks < cap ? (blocks < 1 ? 1 : blocks) : cap);
+}
+
+}  // namespace
+}  // namespace sdm
+
+using namespace sdm;
+
+extern "C" {
+
+size_t sdm_scan_backward_workspace_size(int B, int H, int T, int d_v, int W, int R) {
+  if (B < 1 || H < 1 || T < 1 || d_v < 4 || W < 1 || R < 1) return 0;
+  const int C = backward_cols(d_v);
+  if (!C) return 0;
+  return size_t(B) * H * T * (d_v / C) * size_t(2 * W + R) * 4;
+}
+
+int sdm_scan_forward_train(float* M, const int32_t* idx_w, const float* sc_w,
+                           const int32_t* idx_r, const float* sc_r, const void* v, int v_dt,
+                           const float* alpha, const float* beta, int B, int H, int T,
+                           long long N, int d_v, int W, int R, float* o, float* w_prev,
+                           float* r_rows, void* workspace, size_t workspace_bytes, int* dev_err,
+                           void* stream) {
+  int st = check_scan_args(M, idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, B, H, T, N, d_v, W,
+                           R, o);
+  if (st != SDM_OK) return st;
+  if (T == 0) return SDM_OK;
+  if (!aligned16(w_prev) || !aligned16(r_rows) || !aligned16(workspace)) return SDM_EALIGN;
+  if (workspace_bytes < sdm_scan_workspace_size(B, H, T, d_v, W, R)) return SDM_ENOSPACE;
+  if (dev_err && (reinterpret_cast<uintptr_t>(dev_err) & 3u)) return SDM_EALIGN;
+  ScanShape shape;
+  st = choose_scan_shape(B * H, d_v, W, R, 0, 0, &shape);
+  if (st != SDM_OK) return st;
+  return launch_scan(M, idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, whole_sequences(B * H, T),
+                     N, d_v, W, R, o, workspace, dev_err, shape, nullptr, nullptr,
+                     as_stream(stream), w_prev, r_rows);
+}
+
+int sdm_scan_backward(const int32_t* idx_w, const float* sc_w, const int32_t* idx_r,
+                      const float* sc_r, const void* v, int v_dt, const float* alpha,
+                      const float* beta, const float* w_prev, const float* r_rows,
+                      const float* dO, int B, int H, int T, long long N, int d_v, int W, int R,
+                      float* G, float* dv, float* dalpha, float* dbeta, float* dsc_w,
+                      float* dsc_r, float* dM0, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  int st = check_scan_args(G, idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, B, H, T, N, d_v, W,
+                           R, dv);
+  if (st != SDM_OK) return st;
+  const int C = backward_cols(d_v);
+  if (!C) return SDM_EUNSUPPORTED;
+  cudaStream_t s = as_stream(stream);
+  const size_t per_batch4 = size_t(H) * size_t(N) * d_v / 4;
+  if (dM0 && !aligned16(dM0)) return SDM_EALIGN;
+  if (T > 0) {
+    if (!aligned16(w_prev) || !aligned16(r_rows) || !aligned16(dO) || !aligned16(dalpha) ||
+        !aligned16(dbeta) || !aligned16(dsc_w) || !aligned16(dsc_r) || !aligned16(workspace))
+      return SDM_EALIGN;
+    if (workspace_bytes < sdm_scan_backward_workspace_size(B, H, T, d_v, W, R)) return SDM_ENOSPACE;
+    BwdArgs a;
+    a.idx_w = idx_w;
+    a.sc_w = sc_w;
+    a.idx_r = idx_r;
+    a.sc_r = sc_r;
+    a.v = v;
+    a.v_bf16 = v_dt == SDM_BF16;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.w_prev = w_prev;
+    a.r_rows = r_rows;
+    a.dO = dO;
+    a.G = G;
+    a.dv = dv;
+    a.part = static_cast<float*>(workspace);
+    a.T = T;
+    a.N = N;
+    a.d_v = d_v;
+    a.W = W;
+    a.R = R;
+    const int smem = int(backward_smem_bytes(C, W, R));
+    const void* fn = C == 32   ? reinterpret_cast<const void*>(&scan_backward_kernel<32>)
+                     : C == 16 ? reinterpret_cast<const void*>(&scan_backward_kernel<16>)
+                     : C == 8  ? reinterpret_cast<const void*>(&scan_backward_kernel<8>)
+                               : reinterpret_cast<const void*>(&scan_backward_kernel<4>);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return SDM_ECUDA;
+    void* args[] = {&a};
+    if (cudaLaunchKernel(fn, dim3(unsigned(B * H * (d_v / C))), dim3(kBwdThreads), args,
+                         size_t(smem), s) != cudaSuccess)
+      return SDM_ECUDA;
+    // finish: one warp per (b, h, t)
+    const long long items = (long long)B * H * T;
+    const int fsmem = 4 * 2 * (W + R) * 4;
+    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(&backward_finish_kernel),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, fsmem) != cudaSuccess)
+      return SDM_ECUDA;
+    backward_finish_kernel<<<unsigned((items + 3) / 4), 128, fsmem, s>>>(
+        sc_w, sc_r, beta, a.part, d_v / C, W, R, items, dalpha, dbeta, dsc_w, dsc_r);
+    if (last_launch_status() != SDM_OK) return SDM_ECUDA;
+  }
+  if (dM0) {
+    const int blocks = grid_for(per_batch4, 256);
+    if (blocks < 1) return SDM_ECUDA;
+    reduce_batch_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(G),
+                                                reinterpret_cast<float4*>(dM0), B, per_batch4);
+    return last_launch_status();
+  }
+  return SDM_OK;
+}
+
+int sdm_select_backward(const int32_t* idx, const float* dsc, int B, int H, int T, int S, int K,
+                        float* dhalves, void* stream) {
+  if (B < 1 || H < 1 || T < 0 || S < 1 || K < 1 || (long long)K > (long long)S * S)
+    return SDM_EINVAL;
+  if (S > SDM_MAX_S || K > SDM_MAX_K) return SDM_EUNSUPPORTED;
+  const long long items = (long long)B * H * T;
+  if (items == 0) return SDM_OK;
+  if (!aligned16(idx) || !aligned16(dsc) || !aligned16(dhalves)) return SDM_EALIGN;
+  select_backward_kernel<<<unsigned((items + 3) / 4), 128, 0, as_stream(stream)>>>(idx, dsc, items,
+                                                                                  S, K, dhalves);
+  return last_launch_status();
+}
+
+}  // extern "C"

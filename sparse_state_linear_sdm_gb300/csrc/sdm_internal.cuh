@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstddef>
 #include <cstdint>
 
@@ -81,6 +82,28 @@ __host__ __device__ inline RecLayout rec_layout(int W, int R, int d_v) {
   return L;
 }
 
+// Softmax of n scores with one warp (max-subtracted, __expf), written to w[0..n): one exp
+// per score (the unnormalised values are stored first, then scaled in place by the lane
+// that wrote them).  Shared by the planning kernel (forward weights) and the backward
+// kernels, so both see the same weights bit for bit.
+__device__ inline void warp_softmax(const float* __restrict__ s, int n, float* w) {
+  const int lane = threadIdx.x & 31;
+  float m = -INFINITY;
+  for (int i = lane; i < n; i += 32) m = fmaxf(m, s[i]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  float z = 0.f;
+  for (int i = lane; i < n; i += 32) {
+    const float e = __expf(s[i] - m);
+    w[i] = e;
+    z += e;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, off);
+  const float inv = 1.0f / z;
+  for (int i = lane; i < n; i += 32) w[i] *= inv;
+}
+
 // Tokens [t0, t0 + Tc) of BH sequences stored with T_total tokens each: per-token
 // arrays ([BH, T_total, ...]) are read and written in place at token bh * T_total + t;
 // planning records are per window, [BH, Tc].
@@ -120,15 +143,19 @@ int choose_scan_shape(int BH, int d_v, int W, int R, int force_cols, int force_p
                       ScanShape* out);
 // The scan kernel alone, over the window's records (written by launch_plan with the
 // same shape.pd); continues from the state in M.
+// w_prev / r_rows (optional, [BH, T_total, W or R, d_v]): every write row before its update
+// and every read row as read, for the backward pass.
 int launch_scan_records(float* M, const void* rec, const TokenWindow& win, long long N, int d_v,
-                        int W, int R, float* o, const ScanShape& shape, cudaStream_t s);
+                        int W, int R, float* o, const ScanShape& shape, cudaStream_t s,
+                        float* w_prev = nullptr, float* r_rows = nullptr);
 // Planning pass, then (after waiting for wait_before_scan, if any, and recording
 // after_plan, if any) the scan kernel.
 int launch_scan(float* M, const int32_t* idx_w, const float* sc_w, const int32_t* idx_r,
                 const float* sc_r, const void* v, int v_dt, const float* alpha, const float* beta,
                 const TokenWindow& win, long long N, int d_v, int W, int R, float* o,
                 void* workspace, int* dev_err, const ScanShape& shape, cudaEvent_t after_plan,
-                cudaEvent_t wait_before_scan, cudaStream_t s);
+                cudaEvent_t wait_before_scan, cudaStream_t s, float* w_prev = nullptr,
+                float* r_rows = nullptr);
 
 int launch_gen_inputs(unsigned long long seed, int B, int H, int T, int b_off, int t_off,
                       long long T_total, int S, int d_v, int in_dt, float alpha_lo,

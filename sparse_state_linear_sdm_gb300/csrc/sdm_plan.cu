@@ -58,26 +58,6 @@ struct PlanArgs {
   int* dev_err;
 };
 
-// Softmax of n scores with one warp, written to w[0..n): one exp per score (the
-// unnormalised values are stored first, then scaled in place by the lane that wrote them).
-__device__ void warp_softmax(const float* __restrict__ s, int n, float* w) {
-  const int lane = threadIdx.x & 31;
-  float m = -INFINITY;
-  for (int i = lane; i < n; i += 32) m = fmaxf(m, s[i]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-  float z = 0.f;
-  for (int i = lane; i < n; i += 32) {
-    const float e = __expf(s[i] - m);
-    w[i] = e;
-    z += e;
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, off);
-  const float inv = 1.0f / z;
-  for (int i = lane; i < n; i += 32) w[i] *= inv;
-}
-
 // Shared memory of one planning block: hash table, filter, then the chunk's write slots
 // (tokens [t0 - pd, t1)) and read slots (tokens [t0, t1)).
 __host__ __device__ inline size_t plan_smem_bytes(int log2cap, int tc, int pd, int W, int R) {

@@ -46,6 +46,8 @@ struct ScanArgs {
   long long N;
   int d_v, W, R;
   RecLayout L;
+  float* w_prev;  // optional [BH, T_total, W, d_v]: each write row before its update
+  float* r_rows;  // optional [BH, T_total, R, d_v]: each read row as read (after the write)
 };
 
 __device__ __forceinline__ float4 f4_add(float4 a, float4 b) {
@@ -74,6 +76,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   const unsigned char* recs = a.rec + size_t(bh) * T * L.bytes;
   float* Mbh = a.M + size_t(bh) * size_t(a.N) * d_v + c0;
   float* obh = a.o + (size_t(bh) * a.T_total + a.t_off) * d_v + c0;
+  float* wsave = a.w_prev ? a.w_prev + (size_t(bh) * a.T_total + a.t_off) * W * d_v + c0 : nullptr;
+  float* rsave = a.r_rows ? a.r_rows + (size_t(bh) * a.T_total + a.t_off) * R * d_v + c0 : nullptr;
   const int c4 = tid % LPR;
 
   auto issue_meta = [&](int u) {
@@ -136,6 +140,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
       if (src[e] == -2) continue;
       float4* cell = reinterpret_cast<float4*>(rs + e * C) + c4;
       const float4 m = *cell;
+      if (wsave) *(reinterpret_cast<float4*>(wsave + (size_t(t) * W + e) * d_v) + c4) = m;
       const float kb = beta * wts[e];
       float4 r;
       float mt_;
@@ -175,6 +180,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
       if (src[W + e] == -2) continue;
       const float r = wts[W + e];
       const float4 m = reinterpret_cast<const float4*>(rs + (W + e) * C)[c4];
+      if (rsave) *(reinterpret_cast<float4*>(rsave + (size_t(t) * R + e) * d_v) + c4) = m;
       acc.x = fmaf(r, m.x, acc.x);
       acc.y = fmaf(r, m.y, acc.y);
       acc.z = fmaf(r, m.z, acc.z);
@@ -259,7 +265,8 @@ int choose_scan_shape(int BH, int d_v, int W, int R, int force_cols, int force_p
 }
 
 int launch_scan_records(float* M, const void* rec, const TokenWindow& win, long long N, int d_v,
-                        int W, int R, float* o, const ScanShape& shape, cudaStream_t s) {
+                        int W, int R, float* o, const ScanShape& shape, cudaStream_t s,
+                        float* w_prev, float* r_rows) {
   if (win.Tc == 0 || win.BH == 0) return SDM_OK;
   ScanArgs sa;
   sa.M = M;
@@ -273,6 +280,8 @@ int launch_scan_records(float* M, const void* rec, const TokenWindow& win, long 
   sa.W = W;
   sa.R = R;
   sa.L = rec_layout(W, R, d_v);
+  sa.w_prev = w_prev;
+  sa.r_rows = r_rows;
   ScanFn fn = scan_fn(shape.cols, shape.pd);
   if (!fn) return SDM_EUNSUPPORTED;
   if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
@@ -286,7 +295,7 @@ int launch_scan(float* M, const int32_t* idx_w, const float* sc_w, const int32_t
                 const float* sc_r, const void* v, int v_dt, const float* alpha, const float* beta,
                 const TokenWindow& win, long long N, int d_v, int W, int R, float* o,
                 void* workspace, int* dev_err, const ScanShape& shape, cudaEvent_t after_plan,
-                cudaEvent_t wait_before_scan, cudaStream_t s) {
+                cudaEvent_t wait_before_scan, cudaStream_t s, float* w_prev, float* r_rows) {
   if (win.Tc == 0 || win.BH == 0) return SDM_OK;
   const int st = launch_plan(idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, win, N, d_v, W, R,
                              shape.pd, workspace, dev_err, s);
@@ -294,7 +303,7 @@ int launch_scan(float* M, const int32_t* idx_w, const float* sc_w, const int32_t
   if (wait_before_scan && cudaStreamWaitEvent(s, wait_before_scan, 0) != cudaSuccess)
     return SDM_ECUDA;
   if (after_plan && cudaEventRecord(after_plan, s) != cudaSuccess) return SDM_ECUDA;
-  return launch_scan_records(M, workspace, win, N, d_v, W, R, o, shape, s);
+  return launch_scan_records(M, workspace, win, N, d_v, W, R, o, shape, s, w_prev, r_rows);
 }
 
 }  // namespace sdm

@@ -1,0 +1,153 @@
+"""Backward pass on the GPU (sdm_scan_forward_train + sdm_scan_backward +
+sdm_select_backward, through the C ABI) against the oracle's pinned backward, on the
+GPU's own selection.
+
+Tolerance, per gradient tensor (normwise): max |g - r| <= 2e-4 * (1 + max |r|).  The score
+gradients come out of a cancelling difference (softmax backward: dk - <k, dk>), so an
+elementwise relative bound would measure the cancellation, not the kernel; 2e-4 is the
+forward's fp32 bound, taken at the scale of each gradient."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_state_linear_sdm_gb300 as sdm
+from sparse_state_linear_sdm_gb300 import workloads as wl
+
+from sdm_testlib import device_inputs, device_M0, to_np
+
+pytestmark = pytest.mark.gpu
+GTOL = 2e-4
+
+
+def normwise(got, want) -> float:
+    g = np.asarray(got, np.float64)
+    w = np.asarray(want, np.float64)
+    assert g.shape == w.shape, (g.shape, w.shape)
+    return float(np.abs(g - w).max() / (1.0 + np.abs(w).max())) if g.size else 0.0
+
+
+def _random(rng, B, H, T, S, dv, vdt):
+    f = lambda *sh: rng.standard_normal(sh).astype(np.float32)
+    d = dict(kp=f(B, H, T, 2, S), qp=f(B, H, T, 2, S), v=f(B, H, T, dv),
+             alpha=rng.uniform(0.85, 1.0, (B, H, T)).astype(np.float32),
+             beta=rng.uniform(0.1, 1.0, (B, H, T)).astype(np.float32))
+    if vdt == torch.bfloat16:
+        d["v"] = wl.bf16_to_f32(wl.bf16_bits(d["v"]))
+    dev = {k: torch.from_numpy(x).cuda() for k, x in d.items()}
+    dev["v"] = dev["v"].to(vdt)
+    M0 = (0.3 * rng.standard_normal((H, S * S, dv))).astype(np.float32)
+    dO = f(B, H, T, dv)
+    dMT = f(B, H, S * S, dv)
+    return d, dev, M0, dO, dMT
+
+
+def _gpu_backward(dev, M0, dO, dMT, W, R):
+    B, H, T, _, S = dev["kp"].shape
+    dv = dev["v"].shape[-1]
+    sel = sdm.select(dev["kp"], dev["qp"], W, R)
+    M = torch.from_numpy(np.broadcast_to(M0[None], (B,) + M0.shape).copy()).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, w_prev, r_rows = sdm.scan_forward_train(M, *sel, dev["v"], dev["alpha"], dev["beta"], dev_err=err)
+    G = torch.from_numpy(dMT).cuda()
+    g = sdm.scan_backward(*sel, dev["v"], dev["alpha"], dev["beta"], w_prev, r_rows,
+                          torch.from_numpy(dO).cuda(), G)
+    dkp = sdm.select_backward(sel[0], g["dsc_w"], S)
+    dqp = sdm.select_backward(sel[2], g["dsc_r"], S)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    return sel, o, M, w_prev, r_rows, g, G, dkp, dqp
+
+
+def _oracle_backward(host_v, alpha, beta, sel, M0, dO, dMT):
+    iw, sw, ir, sr = (x.cpu().numpy() for x in sel)
+    B, H, T, W = iw.shape
+    R, N, dv = ir.shape[-1], M0.shape[1], M0.shape[2]
+    nh = B * H
+    Minit = np.broadcast_to(M0[None], (B,) + M0.shape).reshape(nh, N, dv)
+    ref = oracle.scan_backward(Minit, iw.reshape(nh, T, W), sw.reshape(nh, T, W), ir.reshape(nh, T, R),
+                               sr.reshape(nh, T, R), host_v.reshape(nh, T, dv), alpha.reshape(nh, T),
+                               beta.reshape(nh, T), dO.reshape(nh, T, dv), dMT.reshape(nh, N, dv))
+    S = int(round(np.sqrt(N)))
+    ref["dkp"] = oracle.select_backward(S, iw.reshape(nh, T, W), ref["dsc_w"])
+    ref["dqp"] = oracle.select_backward(S, ir.reshape(nh, T, R), ref["dsc_r"])
+    return ref
+
+
+def _check(g, G, dkp, dqp, ref, B, H, label):
+    nh = B * H
+    for name in ("dv", "dalpha", "dbeta", "dsc_w", "dsc_r"):
+        e = normwise(g[name].cpu().numpy().reshape(ref[name].shape), ref[name])
+        assert e <= GTOL, f"{label} {name} error {e:.3e}"
+    N, dv = ref["dM0"].shape[1:]
+    e = normwise(G.cpu().numpy().reshape(nh, N, dv), ref["dM0"])
+    assert e <= GTOL, f"{label} dM0 per (b, h) error {e:.3e}"
+    shared = ref["dM0"].reshape(B, H, N, dv).sum(axis=0)
+    e = normwise(g["dM0"].cpu().numpy(), shared)
+    assert e <= GTOL, f"{label} shared dM0 error {e:.3e}"
+    for name, x in (("dkp", dkp), ("dqp", dqp)):
+        e = normwise(x.cpu().numpy().reshape(ref[name].shape), ref[name])
+        assert e <= GTOL, f"{label} {name} error {e:.3e}"
+
+
+@pytest.mark.parametrize("B,H,T,S,dv,W,R,vdt", [
+    (1, 1, 1, 4, 4, 2, 3, torch.float32),          # one token, d_v = 4 (4-column slices)
+    (2, 2, 50, 8, 16, 6, 5, torch.float32),        # ragged W, R against the rows per pass
+    (1, 3, 97, 6, 24, 9, 20, torch.bfloat16),      # K > S, d_v = 24 (8-column slices)
+    (2, 1, 300, 16, 64, 64, 64, torch.bfloat16),   # rows rewritten and reread across tokens
+    (1, 2, 40, 4, 32, 16, 16, torch.float32),      # W = R = N: every row every token
+])
+def test_backward_matches_oracle(B, H, T, S, dv, W, R, vdt):
+    rng = np.random.default_rng(B * 1000 + T + dv)
+    host, dev, M0, dO, dMT = _random(rng, B, H, T, S, dv, vdt)
+    sel, o, M, w_prev, r_rows, g, G, dkp, dqp = _gpu_backward(dev, M0, dO, dMT, W, R)
+    ref = _oracle_backward(host["v"], host["alpha"], host["beta"], sel, M0, dO, dMT)
+    _check(g, G, dkp, dqp, ref, B, H, (B, H, T, S, dv, W, R))
+
+
+def test_forward_train_equals_forward_and_keeps_the_rows():
+    rng = np.random.default_rng(11)
+    B, H, T, S, dv, W, R = 2, 2, 64, 8, 32, 8, 8
+    host, dev, M0, dO, dMT = _random(rng, B, H, T, S, dv, torch.float32)
+    sel = sdm.select(dev["kp"], dev["qp"], W, R)
+    M1 = torch.from_numpy(np.broadcast_to(M0[None], (B,) + M0.shape).copy()).cuda()
+    M2 = M1.clone()
+    o1 = sdm.scan_forward(M1, *sel, dev["v"], dev["alpha"], dev["beta"])
+    o2, w_prev, r_rows = sdm.scan_forward_train(M2, *sel, dev["v"], dev["alpha"], dev["beta"])
+    torch.cuda.synchronize()
+    assert torch.equal(M1, M2) and torch.equal(o1, o2)
+    # token 0's write rows are M_0's rows; the read rows reproduce o
+    iw = sel[0].cpu().numpy()
+    wp = w_prev.cpu().numpy()
+    for b in range(B):
+        for h in range(H):
+            assert np.array_equal(wp[b, h, 0], M0[h][iw[b, h, 0]])
+    r = torch.softmax(sel[3].double(), dim=-1)
+    o_rows = torch.einsum("bhtr,bhtrd->bhtd", r, r_rows.double())
+    assert float((o_rows - o2.double()).abs().max()) <= 1e-5
+
+
+def test_backward_on_the_small_workload_sampled_heads():
+    """B4 H8 T2048 N=65,536 d_v=64 W=R=32, bf16 inputs: the whole backward on the GPU,
+    the oracle on two heads."""
+    cfg = wl.CONFIGS[1]
+    d = device_inputs(cfg)
+    M0 = device_M0(cfg)
+    sel = sdm.select(d["kp"], d["qp"], cfg.W, cfg.R)
+    M = torch.empty((cfg.B, cfg.H, cfg.N, cfg.d_v), device="cuda")
+    sdm.init_state_from_M0(M, M0)
+    o, w_prev, r_rows = sdm.scan_forward_train(M, *sel, d["v"], d["alpha"], d["beta"])
+    rng = np.random.default_rng(21)
+    dO = torch.from_numpy(rng.standard_normal((cfg.B, cfg.H, cfg.T, cfg.d_v)).astype(np.float32)).cuda()
+    G = torch.zeros((cfg.B, cfg.H, cfg.N, cfg.d_v), device="cuda")
+    g = sdm.scan_backward(*sel, d["v"], d["alpha"], d["beta"], w_prev, r_rows, dO, G, shared_M0=False)
+    torch.cuda.synchronize()
+    M0h = M0.cpu().numpy()
+    for b, h in ((0, 0), (cfg.B - 1, cfg.H - 1)):
+        s = lambda x: x[b, h].cpu().numpy()[None]
+        ref = oracle.scan_backward(M0h[h][None], s(sel[0]), s(sel[1]), s(sel[2]), s(sel[3]),
+                                   to_np(d["v"][b, h])[None], s(d["alpha"]), s(d["beta"]), s(dO))
+        for name in ("dv", "dalpha", "dbeta", "dsc_w", "dsc_r"):
+            e = normwise(g[name][b, h].cpu().numpy()[None], ref[name])
+            assert e <= GTOL, (name, b, h, e)
+        assert normwise(G[b, h].cpu().numpy()[None], ref["dM0"]) <= GTOL
