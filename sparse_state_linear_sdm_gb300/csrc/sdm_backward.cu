@@ -72,12 +72,13 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
   constexpr int NB = 4;                      // rows per thread per round, loaded together
   extern __shared__ __align__(16) unsigned char smem[];
   const int W = a.W, R = a.R, T = a.T, d_v = a.d_v;
-  const int WRa = (W + R + 3) & ~3;
+  const int WR = W + R, WRa = (W + R + 3) & ~3;
   float* kw = reinterpret_cast<float*>(smem);        // [W] write weights of the token
   float* rw = kw + W;                                 // [R] read weights
   float* red = kw + WRa;                              // [warps][C]
-  int32_t* iw = reinterpret_cast<int32_t*>(red + kBwdWarps * C);  // [W]
-  int32_t* ir = iw + W;                                            // [R]
+  // Two staging buffers of one token's [slots W | slots R | scores W | scores R]: the next
+  // token's (going backwards) arrive by cp.async while this one is processed.
+  int32_t* stg = reinterpret_cast<int32_t*>(red + kBwdWarps * C);  // [2][2 * WR]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int slices = d_v / C;
@@ -88,13 +89,34 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
   const int PW = 2 * W + R;
   float* Gbh = a.G + size_t(bh) * size_t(a.N) * d_v + c0;
 
+  auto stage = [&](int t) {  // 4-byte cp.async per entry into buffer t & 1
+    const size_t tk = size_t(bh) * T + t;
+    int32_t* dst = stg + (t & 1) * 2 * WR;
+    for (int e = tid; e < 2 * WR; e += kBwdThreads) {
+      const void* src = e < W ? static_cast<const void*>(a.idx_w + tk * W + e)
+                      : e < WR ? static_cast<const void*>(a.idx_r + tk * R + (e - W))
+                      : e < WR + W ? static_cast<const void*>(a.sc_w + tk * W + (e - WR))
+                                   : static_cast<const void*>(a.sc_r + tk * R + (e - WR - W));
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                       static_cast<uint32_t>(__cvta_generic_to_shared(dst + e))),
+                   "l"(src)
+                   : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  if (T > 0) stage(T - 1);
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+
   for (int t = T - 1; t >= 0; --t) {
     const size_t tk = size_t(bh) * T + t;
-    if (warp == 0) warp_softmax(a.sc_w + tk * W, W, kw);
-    if (warp == 1) warp_softmax(a.sc_r + tk * R, R, rw);
-    for (int i = tid; i < W; i += kBwdThreads) iw[i] = a.idx_w[tk * W + i];
-    for (int j = tid; j < R; j += kBwdThreads) ir[j] = a.idx_r[tk * R + j];
+    const int32_t* iw = stg + (t & 1) * 2 * WR;
+    const int32_t* ir = iw + W;
+    const float* scw = reinterpret_cast<const float*>(iw + WR);
+    if (warp == 0) warp_softmax(scw, W, kw);
+    if (warp == 1) warp_softmax(scw + W, R, rw);
     __syncthreads();
+    if (t > 0) stage(t - 1);  // the other buffer held token t+1, no longer read
     float* part = a.part + (tk * slices + sl) * PW;
     const float4 dO4 = reinterpret_cast<const float4*>(a.dO + tk * d_v + c0)[c4];
 
@@ -190,13 +212,14 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
       }
       reinterpret_cast<float4*>(a.dv + tk * d_v + c0)[tid] = s4;
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();  // G of this token is written before the previous token loads it
   }
 }
 
 size_t backward_smem_bytes(int C, int W, int R) {
   const int WRa = (W + R + 3) & ~3;
-  return size_t(WRa) * 4 + size_t(kBwdWarps) * C * 4 + size_t(W + R) * 4;
+  return size_t(WRa) * 4 + size_t(kBwdWarps) * C * 4 + size_t(4 * (W + R)) * 4;
 }
 
 int backward_cols(int d_v) {
