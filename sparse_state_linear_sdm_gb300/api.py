@@ -483,6 +483,20 @@ class DecodeStep:
             self._body()
         return self
 
+    @property
+    def inputs(self) -> dict:
+        """The step's static input buffers (kp, qp, v, alpha, beta): a producer that writes
+        a token's inputs here directly can then call run() without any copy."""
+        return dict(kp=self.kp, qp=self.qp, v=self.v, alpha=self.alpha, beta=self.beta)
+
+    def run(self):
+        """One step on the inputs already in the static buffers; returns o (static)."""
+        if self.graph is None:
+            self._body()
+        else:
+            self.graph.replay()
+        return self.o
+
     def __call__(self, kp, qp, v, alpha, beta):
         self.kp.copy_(kp, non_blocking=True)
         self.qp.copy_(qp, non_blocking=True)

@@ -28,6 +28,9 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gmem_src) : "memory");
 }
+__device__ __forceinline__ void cp_async16_s(uint32_t smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_dst), "l"(gmem_src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
@@ -97,10 +100,14 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
     const unsigned char* mt = meta + (u % QM) * meta_bytes;
     const int32_t* idx = reinterpret_cast<const int32_t*>(mt);
     const int16_t* src = reinterpret_cast<const int16_t*>(mt + L.off_src);
-    float* dst = rows + size_t(u % QR) * WR * C;
-    for (int k = tid; k < WR * LPR; k += kScanThreads) {
-      const int e = k / LPR, q = k % LPR;
-      if (src[e] == -1) cp_async16(dst + e * C + 4 * q, Mbh + size_t(idx[e]) * d_v + 4 * q);
+    // Thread tid copies 16-byte chunk c4 of rows tid / LPR + j * RPP: its destination
+    // advances by a fixed stride and its source column is fixed.
+    uint32_t sdst = static_cast<uint32_t>(
+        __cvta_generic_to_shared(rows + size_t(u % QR) * WR * C + (tid / LPR) * C + 4 * c4));
+    const float* gcol = Mbh + 4 * c4;
+#pragma unroll 4
+    for (int e = tid / LPR; e < WR; e += RPP, sdst += RPP * C * 4) {
+      if (src[e] == -1) cp_async16_s(sdst, gcol + size_t(idx[e]) * d_v);
     }
   };
 

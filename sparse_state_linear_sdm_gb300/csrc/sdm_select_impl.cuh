@@ -476,7 +476,8 @@ struct SelectArgs {
   int kpad;      // max(W, R, 32) rounded up to a power of two (selected-key buffer)
   int cnt_w, cnt_r;
   int warps;
-  int tpw;            // consecutive tasks per warp
+  int tpw;            // consecutive tasks per warp (per warp pair in pair mode)
+  int pair;           // pair mode: two warps per task, one half each (few tasks: latency)
   size_t keys_bytes;  // per-warp key buffer
   bool vec;           // every half starts on a 16-byte boundary
   int32_t* idx_w;
@@ -544,7 +545,11 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
   unsigned char* keys = wp;
   uint64_t* out = reinterpret_cast<uint64_t*>(wp + a.keys_bytes);
   uint32_t* hist = reinterpret_cast<uint32_t*>(out + a.kpad);
-  float* aval = reinterpret_cast<float*>(hist + 256);
+  // Pair mode: warps 2u and 2u+1 share a task; the inner lists live in warp 2u's region.
+  const int role = a.pair ? (warp & 1) : 0;
+  const int unit = a.pair ? (warp >> 1) : warp;
+  unsigned char* lp = a.pair ? wbase + (per_warp + 15) / 16 * 16 * (warp & ~1) : wp;
+  float* aval = reinterpret_cast<float*>(lp + a.keys_bytes + size_t(a.kpad) * 8 + 256 * 4);
   float* bval = aval + a.kin_max;
   int32_t* aidx = reinterpret_cast<int32_t*>(bval + a.kin_max);
   int32_t* bidx = aidx + a.kin_max;
@@ -557,7 +562,8 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
   // A short run of consecutive tasks per warp (no persistent grid): blocks that start
   // late, e.g. behind a kernel on another stream, do not hold up the others.
   const long long tasks = a.items * 2;
-  const long long task0 = ((long long)blockIdx.x * a.warps + warp) * a.tpw;
+  const int units = a.pair ? a.warps / 2 : a.warps;
+  const long long task0 = ((long long)blockIdx.x * units + unit) * a.tpw;
   const long long task1 = task0 + a.tpw < tasks ? task0 + a.tpw : tasks;
   for (long long task = task0; task < task1; ++task) {
     const int which = int(task & 1);
@@ -570,7 +576,7 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
     const Tin* halves = static_cast<const Tin*>(which ? a.qp : a.kp) + item * 2 * S;
 
     // ---- 1. top-kin of each half, ranked by (value desc, index asc) ---------------
-    for (int h = 0; h < 2; ++h) {
+    for (int h = role; h < (a.pair ? role + 1 : 2); ++h) {
       IKey* ik = reinterpret_cast<IKey*>(keys);
       IKey* io = reinterpret_cast<IKey*>(out);
       load_half_keys<Tin>(halves + (long long)h * S, S, a.vec, ik, hist);
@@ -586,6 +592,14 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
         di[r] = min(int(0xFFFFu - uint32_t(k & 0xFFFFu)), S - 1);
       }
       __syncwarp();
+    }
+
+    if (a.pair) {  // both halves' lists are in place; the second warp waits for the next task
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + unit) : "memory");
+      if (role) {
+        asm volatile("bar.sync %0, 64;" ::"r"(1 + unit) : "memory");
+        continue;
+      }
     }
 
     // ---- 2. top-K of the kin x kin grid of pair sums -------------------------------
@@ -652,6 +666,7 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
       os[r] = ord_decode(uint32_t(k >> 32));
     }
     __syncwarp();
+    if (a.pair) asm volatile("bar.sync %0, 64;" ::"r"(1 + unit) : "memory");  // lists free again
   }
 }
 
@@ -705,13 +720,16 @@ int launch_select_t(const void* kp, const void* qp, const TokenWindow& win, int 
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, warps * 32, smem) != cudaSuccess)
     return SDM_ECUDA;
   // About 64 waves of blocks: the last wave is short, and a block's staircase set-up is
-  // spread over several tasks per warp.
+  // spread over several tasks per warp.  With fewer tasks than resident warps (a decode
+  // step) each task gets a pair of warps instead: the two halves run side by side.
   const long long tasks = items * 2;
   const long long resident = (long long)sms * (per_sm > 0 ? per_sm : 1) * warps;
+  a.pair = tasks < resident && warps % 2 == 0 ? 1 : 0;
+  const int units = a.pair ? warps / 2 : warps;
   long long tpw = tasks / (resident * 64);
   tpw = tpw < 1 ? 1 : (tpw > 64 ? 64 : tpw);
   a.tpw = int(tpw);
-  const long long blocks = (tasks + warps * tpw - 1) / (warps * tpw);
+  const long long blocks = (tasks + units * tpw - 1) / (units * tpw);
   if (blocks > 0x7FFFFFFFLL) return SDM_EUNSUPPORTED;
   void* args[] = {&a};
   if (cudaLaunchKernel(fn, dim3(unsigned(blocks)), dim3(warps * 32), args, smem, s) != cudaSuccess)
