@@ -477,7 +477,6 @@ struct SelectArgs {
   int cnt_w, cnt_r;
   int warps;
   int tpw;            // consecutive tasks per warp (per warp pair in pair mode)
-  int pair;           // pair mode: two warps per task, one half each (few tasks: latency)
   size_t keys_bytes;  // per-warp key buffer
   bool vec;           // every half starts on a 16-byte boundary
   int32_t* idx_w;
@@ -531,7 +530,7 @@ __device__ __noinline__ void outer_full_grid(const float* aval, const float* bva
   collect_at_least(grid_key, kin * kin, tau2, out, kpad);
 }
 
-template <typename Tin, int EMAX>
+template <typename Tin, int EMAX, bool PAIR>
 __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
   using IKey = typename InnerKeyOf<Tin>::type;
   extern __shared__ __align__(16) unsigned char smem[];
@@ -546,9 +545,9 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
   uint64_t* out = reinterpret_cast<uint64_t*>(wp + a.keys_bytes);
   uint32_t* hist = reinterpret_cast<uint32_t*>(out + a.kpad);
   // Pair mode: warps 2u and 2u+1 share a task; the inner lists live in warp 2u's region.
-  const int role = a.pair ? (warp & 1) : 0;
-  const int unit = a.pair ? (warp >> 1) : warp;
-  unsigned char* lp = a.pair ? wbase + (per_warp + 15) / 16 * 16 * (warp & ~1) : wp;
+  const int role = PAIR ? (warp & 1) : 0;
+  const int unit = PAIR ? (warp >> 1) : warp;
+  unsigned char* lp = PAIR ? wbase + (per_warp + 15) / 16 * 16 * (warp & ~1) : wp;
   float* aval = reinterpret_cast<float*>(lp + a.keys_bytes + size_t(a.kpad) * 8 + 256 * 4);
   float* bval = aval + a.kin_max;
   int32_t* aidx = reinterpret_cast<int32_t*>(bval + a.kin_max);
@@ -562,7 +561,7 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
   // A short run of consecutive tasks per warp (no persistent grid): blocks that start
   // late, e.g. behind a kernel on another stream, do not hold up the others.
   const long long tasks = a.items * 2;
-  const int units = a.pair ? a.warps / 2 : a.warps;
+  const int units = PAIR ? a.warps / 2 : a.warps;
   const long long task0 = ((long long)blockIdx.x * units + unit) * a.tpw;
   const long long task1 = task0 + a.tpw < tasks ? task0 + a.tpw : tasks;
   for (long long task = task0; task < task1; ++task) {
@@ -576,7 +575,7 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
     const Tin* halves = static_cast<const Tin*>(which ? a.qp : a.kp) + item * 2 * S;
 
     // ---- 1. top-kin of each half, ranked by (value desc, index asc) ---------------
-    for (int h = role; h < (a.pair ? role + 1 : 2); ++h) {
+    for (int h = role; h < (PAIR ? role + 1 : 2); ++h) {
       IKey* ik = reinterpret_cast<IKey*>(keys);
       IKey* io = reinterpret_cast<IKey*>(out);
       load_half_keys<Tin>(halves + (long long)h * S, S, a.vec, ik, hist);
@@ -594,7 +593,7 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
       __syncwarp();
     }
 
-    if (a.pair) {  // both halves' lists are in place; the second warp waits for the next task
+    if (PAIR) {  // both halves' lists are in place; the second warp waits for the next task
       asm volatile("bar.sync %0, 64;" ::"r"(1 + unit) : "memory");
       if (role) {
         asm volatile("bar.sync %0, 64;" ::"r"(1 + unit) : "memory");
@@ -666,7 +665,7 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
       os[r] = ord_decode(uint32_t(k >> 32));
     }
     __syncwarp();
-    if (a.pair) asm volatile("bar.sync %0, 64;" ::"r"(1 + unit) : "memory");  // lists free again
+    if (PAIR) asm volatile("bar.sync %0, 64;" ::"r"(1 + unit) : "memory");  // lists free again
   }
 }
 
@@ -712,20 +711,26 @@ int launch_select_t(const void* kp, const void* qp, const TokenWindow& win, int 
   const size_t smem = stair_bytes + per_warp * warps;
   // 16-byte loads of the halves when every half is 16-byte aligned (the base is).
   a.vec = (S * int(sizeof(Tin))) % 16 == 0;
-  const void* fn = kmax <= 128 ? reinterpret_cast<const void*>(&select_kernel<Tin, 4>)
-                               : reinterpret_cast<const void*>(&select_kernel<Tin, 32>);
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+  // With fewer tasks than resident warps (a decode step) each task gets a pair of warps:
+  // the two halves run side by side.  (Occupancy is the same for both kernels.)
+  const void* fn1 = kmax <= 128 ? reinterpret_cast<const void*>(&select_kernel<Tin, 4, false>)
+                                : reinterpret_cast<const void*>(&select_kernel<Tin, 32, false>);
+  const void* fn2 = kmax <= 128 ? reinterpret_cast<const void*>(&select_kernel<Tin, 4, true>)
+                                : reinterpret_cast<const void*>(&select_kernel<Tin, 32, true>);
+  const void* fn = fn1;
+  if (cudaFuncSetAttribute(fn1, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess ||
+      cudaFuncSetAttribute(fn2, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
     return SDM_ECUDA;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, warps * 32, smem) != cudaSuccess)
     return SDM_ECUDA;
   // About 64 waves of blocks: the last wave is short, and a block's staircase set-up is
-  // spread over several tasks per warp.  With fewer tasks than resident warps (a decode
-  // step) each task gets a pair of warps instead: the two halves run side by side.
+  // spread over several tasks per warp.
   const long long tasks = items * 2;
   const long long resident = (long long)sms * (per_sm > 0 ? per_sm : 1) * warps;
-  a.pair = tasks < resident && warps % 2 == 0 ? 1 : 0;
-  const int units = a.pair ? warps / 2 : warps;
+  const bool pair = tasks < resident && warps % 2 == 0;
+  if (pair) fn = fn2;
+  const int units = pair ? warps / 2 : warps;
   long long tpw = tasks / (resident * 64);
   tpw = tpw < 1 ? 1 : (tpw > 64 ? 64 : tpw);
   a.tpw = int(tpw);
