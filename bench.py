@@ -52,9 +52,12 @@ def parse_args():
                     help="on: sdm_forward (selection of chunk c+1 overlaps the scan of chunk c); "
                          "off: init || select, then plan and scan, one kernel after the other")
     ap.add_argument("--override", default="", help="size overrides for profiling, e.g. S=256,T=512")
-    ap.add_argument("--mode", choices=["forward", "decode", "backward"], default="forward",
+    ap.add_argument("--mode", choices=["forward", "decode", "backward", "project"], default="forward",
                     help="decode: one token per step for the batch, state resident, CUDA graph; "
-                         "backward: the training backward pass (reverse scan, score and half gradients)")
+                         "backward: the training backward pass (reverse scan, score and half gradients); "
+                         "project: the projections x -> k', q' on the tensor cores")
+    ap.add_argument("--dmodel", type=int, default=0, help="feature width D of --mode project (0 = 2048)")
+    ap.add_argument("--max-ctas", type=int, default=0, help="blocks of the projection kernel (0 = one per SM)")
     return ap.parse_args()
 
 
@@ -723,6 +726,92 @@ def run_backward(args):
         print(json.dumps(line), flush=True)
 
 
+def bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def run_project(args):
+    """The projections x -> k', q' of every token of the workload: one tensor-core GEMM
+    [B*T, D] x [D, 4*H*S] per step, bf16 outputs in the selection's layout."""
+    import numpy as np
+    import torch
+
+    import sparse_state_linear_sdm_gb300 as sdm
+    from sparse_state_linear_sdm_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = workload(args)
+    D = args.dmodel or wl.PROJ_D
+    B, T, H, S = cfg.B, cfg.T, cfg.H, cfg.S
+    b0 = rank_batch_offset(rank, B)
+    xb = wl.projection_features(cfg.seed, B * world, T, D, b0 * T, (b0 + B) * T)
+    wb = wl.projection_weights(cfg.seed, H, S, D)
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    x = to_dev(xb).view(B, T, D)
+    w = to_dev(wb)
+    kp = torch.empty((B, H, T, 2, S), dtype=torch.bfloat16, device=dev)
+    qp = torch.empty_like(kp)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(args.warmup):
+        sdm.project_kq(x, w, H, S, out=(kp, qp), dev_err=err, max_ctas=args.max_ctas)
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    evs = [(E(), E()) for _ in range(K)]
+    with ClockSampler(local) as clk:
+        for a, b in evs:
+            a.record()
+            sdm.project_kq(x, w, H, S, out=(kp, qp), dev_err=err, max_ctas=args.max_ctas)
+            b.record()
+        torch.cuda.synchronize(dev)
+    if err.item() != 0:
+        raise RuntimeError(f"projection kernel reported device error bits {err.item()}")
+    total = evs[0][0].elapsed_time(evs[-1][1])
+    per = [a.elapsed_time(b) for a, b in evs]
+    ms = statistics.mean(per)
+    max_ms = max_over_ranks(total, dev)
+    flops = 2.0 * B * T * D * 4 * H * S
+    achieved = flops / (ms / 1e3) / 1e12
+    peak, peak_kind = bf16_peak()
+    line = {"metric": "SDM k'/q' projection head-tokens/s on 1 GB300 (tensor-core GEMM)",
+            "value": whole_job_rate(B * H * T, K, world, max_ms), "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": total / K, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 (fp32 accumulation)", "data": "synthetic",
+            "config": {"workload": f"{cfg.name}: x [B={B}, T={T}, D={D}] bf16 -> k', q' [B, H={H}, T, 2, S={S}] bf16",
+                       "gemm": [B * T, 4 * H * S, D], "l2": "inputs larger than L2 (x is "
+                       f"{B * T * D * 2 / 1e6:.0f} MB, outputs {2 * B * H * T * 2 * S * 2 / 1e9:.1f} GB)"},
+            "roofline": {"kernel": "sdm project_kernel (tcgen05.mma kind::f16, TMA, TMEM)", "bound": "tensor",
+                         "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                         "algorithmic_flops_per_launch": flops, "traffic": None,
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"
+                         if peak_kind == "measured" else "fallback 1.9 PFLOP/s"},
+            "kernel_ms": {"mean": ms, "min": min(per), "max": max(per)},
+            "gpu_launches": K, "clocks": clk.summary()}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        n = 32
+        xs = wl.bf16_to_f32(xb[:n])
+        ws = wl.bf16_to_f32(wb)
+        t0 = time.perf_counter()
+        reps = 0
+        while reps < 3 or time.perf_counter() - t0 < 2.0:
+            oracle.project(xs, ws, H, S)
+            reps += 1
+        dt = (time.perf_counter() - t0) / reps
+        line["cpu_baseline"] = {"value": n * H / dt, "unit": UNIT, "cores": os.cpu_count() or 1,
+                                "kind": "oracle", "sample": f"oracle.project (fp64 matmul) on {n} tokens x "
+                                f"{4 * H * S} columns x D={D}, mean of {reps}"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def dataclasses_replace(cfg, **kw):
     import dataclasses
 
@@ -737,6 +826,8 @@ def main():
         run_decode(args)
     elif args.mode == "backward":
         run_backward(args)
+    elif args.mode == "project":
+        run_project(args)
     else:
         run_ours(args)
 

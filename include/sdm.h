@@ -56,6 +56,7 @@ typedef enum { SDM_F32 = 0, SDM_BF16 = 1 } sdm_dtype;
 /* bits OR-ed into *dev_err by the device */
 #define SDM_DEV_INDEX_RANGE 1 /* a slot index was < 0 or >= N */
 #define SDM_DEV_DUP_WRITE 2   /* a slot appeared twice in one token's write set */
+#define SDM_DEV_TIMEOUT 4     /* a bounded wait inside a kernel ran out; outputs unspecified */
 
 /* Limits of this build (checked on the host, SDM_EUNSUPPORTED beyond them). */
 #define SDM_MAX_S 4096  /* sqrt(N) */
@@ -249,6 +250,31 @@ int sdm_scan_backward(const int32_t* idx_w, const float* sc_w, const int32_t* id
  * use atomic adds: their order, and so the last bits, may vary from run to run. */
 int sdm_select_backward(const int32_t* idx, const float* dsc, int B, int H, int T, int S, int K,
                         float* dhalves, void* stream);
+
+/* sdm_project_kq - the projections that produce the product keys and queries
+ * ("Meccanismo Core" item 2: the projected key k' and query q', whose two halves are the
+ * sub-scores; "Design IsoFLOP": the projections are linear layers).  One bf16 GEMM on the
+ * tensor cores (fp32 accumulation, each output rounded to bf16, nearest even):
+ *   kp[b,h,t,half,s] = sum_d x[b,t,d] * w[(h*2 + half)*S + s, d]
+ *   qp[b,h,t,half,s] = sum_d x[b,t,d] * w[H*2*S + (h*2 + half)*S + s, d]
+ *   x  [B, T, D] bf16 (raw 16-bit patterns), read only;
+ *   w  [4*H*S, D] bf16, read only: one row of D weights per output column, the k'
+ *      columns (head, half, index) first, then the q' columns in the same order;
+ *   kp, qp [B, H, T, 2, S] bf16, written (the layout sdm_select reads, in_dt SDM_BF16).
+ * The order of the fp32 accumulation is unspecified, so an output can differ from the
+ * correctly rounded sum by one bf16 unit where the sum lies near a rounding boundary.
+ * Requires B, T, H >= 1, 1 <= S <= SDM_MAX_S, D >= 8 with D % 8 == 0 (the row pitch of x
+ * and w is a multiple of 16 bytes), B*T < 2^31, 4*H*S < 2^31; x, w, kp, qp 16-byte
+ * aligned.  dev_err: device int or NULL; SDM_DEV_TIMEOUT if a wait inside the kernel ran
+ * out (then kp, qp are unspecified).  Runs as one persistent kernel with one block per
+ * SM on `stream`. */
+int sdm_project_kq(const void* x, const void* w, int B, int T, int D, int H, int S, void* kp,
+                   void* qp, int* dev_err, void* stream);
+
+/* sdm_project_kq_ctas - sdm_project_kq on at most max_ctas blocks (0: one per SM), to
+ * leave SMs to work running beside it on other streams. */
+int sdm_project_kq_ctas(const void* x, const void* w, int B, int T, int D, int H, int S,
+                        void* kp, void* qp, int* dev_err, int max_ctas, void* stream);
 
 /* sdm_gen_inputs - synthetic inputs (not part of the method): draws the box
  * b in [b_off, b_off+B), all H heads, tokens t in [t_off, t_off+T) of a logical

@@ -10,11 +10,16 @@ product-key top-W / top-R slot selection through
 topk(s1 (+) s2) = topk(topk(s1) (+) topk(s2)), the gated delta write
 M_t[i] = a_t M_{t-1}[i] + b_t k_t^(i) (v_t - a_t M_{t-1}[i]) on the selected rows
 only, and a weighted read of the R selected rows after the write.  The
-arithmetic lives in ``sdm_oracle.cpp`` (fp32 selection sums, fp64 state).
+arithmetic lives in ``sdm_oracle.cpp`` (fp32 selection sums, fp64 state).  Also the
+linear projections x -> k', q' (``project``, one fp64 library matmul) and the reverse
+mode of the scan and of the selection sums (``scan_backward``, ``select_backward``).
 
-Every function here is pinned by ``tests/test_oracle_pins.py`` against things
-other than itself: brute force over all N slot scores, a hand-worked two-token
-example, invariants of the update equations and closed forms.
+Every function here is pinned against things other than itself:
+``tests/test_oracle_pins.py`` (brute force over all N slot scores, a hand-worked
+two-token example, invariants of the update equations and closed forms),
+``tests/test_oracle_backward_pins.py`` (finite differences, an exact linearity
+identity) and ``tests/test_oracle_project_pins.py`` (one-hot features, explicit loops
+on tiny sizes, linearity).
 """
 from __future__ import annotations
 
@@ -199,3 +204,34 @@ def select_backward(S: int, idx, dsc):
     np.add.at(out[:, 0], (rows, flat_i // S), flat_d)
     np.add.at(out[:, 1], (rows, flat_i % S), flat_d)
     return out.reshape(lead + (2, S))
+
+
+def project(x, w, H: int, S: int):
+    """The key and query projections ("Meccanismo Core" item 2: k' and q' are projections of
+    the token features whose two halves are the sub-scores; "Design IsoFLOP": plain linear
+    layers).  x: [..., D] (any float values, e.g. bf16 patterns decoded to fp32);
+    w: [4*H*S, D], one row per output column: k' columns in (head, half, index) order,
+    then q' columns in the same order.
+
+    Returns float64 (kp, qp, mag), each [lead..., H, 2, S] when x is [lead..., D] with the
+    token axis moved behind the head axis for x of shape [B, T, D] (kp[b, h, t, half, s]);
+    mag = sum_d |x_d w_nd| per output (the scale of the accumulation's rounding error).
+    The products and sums are exact up to fp64 rounding (one library matmul)."""
+    x64 = np.asarray(x, np.float64)
+    w64 = np.asarray(w, np.float64)
+    if w64.shape != (4 * H * S, x64.shape[-1]):
+        raise ValueError("w must be [4*H*S, D]")
+    y = x64 @ w64.T                                   # [..., 4HS]
+    mag = np.abs(x64) @ np.abs(w64).T
+    lead = x64.shape[:-1]
+
+    def split(a):
+        a = a.reshape(lead + (2, H, 2, S))            # (k' or q', head, half, index)
+        a = np.moveaxis(a, len(lead), 0)              # [2, lead..., H, 2, S]
+        if len(lead) == 2:                            # [B, T, ...] -> [B, H, T, 2, S]
+            a = np.moveaxis(a, 3, 2)
+        return a[0], a[1]
+
+    kp, qp = split(y)
+    mk, mq = split(mag)
+    return kp, qp, (mk, mq)

@@ -1,0 +1,440 @@
+// Projection of the token features onto the product-key halves, on the tcgen05 tensor
+// cores (Sparse Delta Memory technical summary, gist.science/it/paper/2607.07386,
+// "Meccanismo Core" item 2: the projected key k' and query q' whose halves are the
+// sub-scores; "Design IsoFLOP": the projections are plain linear layers).
+//
+//   k'[b,h,t,half,s] = sum_d x[b,t,d] w[(h*2 + half)*S + s, d]
+//   q'[b,h,t,half,s] = sum_d x[b,t,d] w[H*2*S + (h*2 + half)*S + s, d]
+//
+// is one GEMM  Y[m, n] = sum_d X[m, d] W[n, d]  over the m = b*T + t token rows and the
+// n < 2*H*2S output columns: bf16 operands, fp32 accumulation, rounded to bf16 (nearest
+// even) and stored straight into the [B,H,T,2,S] layout the selection reads, so no
+// transpose pass follows.
+//
+// Kernel: persistent, one CTA per SM, 128 x 256 output tiles (all 256 columns of a tile
+// lie in one head's k' or q' when S % 128 == 0), K in steps of 64 (one 128-byte swizzle
+// atom of bf16).
+//   warp 0      TMA producer: the X tile (128 x 64) and the W tile (256 x 64), 128-byte
+//               swizzled, into a 4-stage ring of shared memory (48 KB per stage)
+//   warp 1      TMEM owner (allocates 512 columns: two 256-column fp32 accumulators) and
+//               MMA issuer (one thread): 4 x tcgen05.mma M128 N256 K16 per stage;
+//               tcgen05.commit frees the stage and, after a tile's last stage, hands the
+//               accumulator to the epilogue
+//   warps 2..5  epilogue: each warp reads its 32 TMEM lanes (= 32 rows of the tile) with
+//               tcgen05.ld, converts to bf16 and stores 16-byte pieces of the row; the
+//               other accumulator is meanwhile being filled by the next tile's MMAs
+// Tiles run m-major (the 2*H*2S / 256 column tiles of a row block back to back), so the
+// resident CTAs share a few row blocks of X and all of W in L2.
+// Every mbarrier wait is bounded in time: an expired wait raises a CTA-wide stop flag,
+// every role leaves its loop, outstanding copies and MMAs are waited for (bounded), TMEM
+// is freed and SDM_DEV_TIMEOUT is reported through dev_err.
+#include "sdm_internal.cuh"
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace sdm {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 2 * BN;
+constexpr int kNumBars = 2 * STAGES + 5;  // full[], empty[], acc_full[2], acc_empty[2], drain
+constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024 /* alignment slack */ + 256;
+constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
+// M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) |
+                            (uint32_t(BM >> 4) << 24);
+
+struct ProjArgs {
+  int Mrows, Ncols, D;
+  int T, H, S;
+  uint16_t* kp;
+  uint16_t* qp;
+  int* dev_err;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits until the barrier's phase of the given parity has completed.  Returns false when
+// the CTA's stop flag is up or the wait ran past its time limit (then it raises the flag).
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* stop) {
+  if (mbar_test(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 1; i < (1u << 28); ++i) {
+    if (mbar_test(bar, parity)) return true;
+    if ((i & 31u) == 0) {
+      if (*stop) return false;
+      if (global_ns() - t0 > kWaitNs) break;
+    }
+  }
+  *stop = 1;
+  return false;
+}
+
+// Teardown wait: only the time limit, not the stop flag.
+__device__ void mbar_wait_teardown(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 0; i < (1u << 28); ++i) {
+    if (mbar_test(bar, parity)) return;
+    if ((i & 31u) == 31u && global_ns() - t0 > kWaitNs) return;
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile in the 128-byte swizzle layout
+// written by TMA: rows of 128 bytes, 8-row atoms of 1,024 bytes stacked along M/N (stride
+// byte offset 1,024; the leading byte offset is not used by this layout), descriptor
+// version 1 at bit 46, swizzle mode 2 (128 bytes) at bits 61-63.  The K step of 16
+// elements inside the atom advances the start address by 32 bytes.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
+         (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %3, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %4, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(accumulate), "r"(kIdesc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_load32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+      " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
+      " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31},"
+      " [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(uint32_t lo, uint32_t hi) {
+  const __nv_bfloat162 p = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+  return *reinterpret_cast<const uint32_t*>(&p);
+}
+
+// Stores columns n .. n+31 of token row (b, t).  VEC: 2S % 8 == 0 and 16-byte aligned
+// outputs, so every 8-column piece lies in one (k' or q', head) block and is one 16-byte
+// store; otherwise column by column.
+template <bool VEC>
+__device__ __forceinline__ void store_cols(const ProjArgs& a, int b, int t, int n,
+                                           const uint32_t (&r)[32]) {
+  const int S2 = 2 * a.S, HS2 = a.H * S2;
+  if (VEC) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int c = n + 8 * g;
+      if (c >= a.Ncols) break;
+      const int which = c >= HS2;
+      const int rem = c - which * HS2;
+      const int h = rem / S2, cc = rem - h * S2;
+      uint16_t* dst = (which ? a.qp : a.kp) + ((size_t(b) * a.H + h) * a.T + t) * S2 + cc;
+      uint4 v;
+      v.x = pack_bf16(r[8 * g + 0], r[8 * g + 1]);
+      v.y = pack_bf16(r[8 * g + 2], r[8 * g + 3]);
+      v.z = pack_bf16(r[8 * g + 4], r[8 * g + 5]);
+      v.w = pack_bf16(r[8 * g + 6], r[8 * g + 7]);
+      *reinterpret_cast<uint4*>(dst) = v;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int c = n + j;
+      if (c >= a.Ncols) continue;
+      const int which = c >= HS2;
+      const int rem = c - which * HS2;
+      const int h = rem / S2, cc = rem - h * S2;
+      uint16_t* dst = (which ? a.qp : a.kp) + ((size_t(b) * a.H + h) * a.T + t) * S2 + cc;
+      const __nv_bfloat16 v = __float2bfloat16_rn(__uint_as_float(r[j]));
+      *dst = *reinterpret_cast<const uint16_t*>(&v);
+    }
+  }
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads, 1)
+    project_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                   ProjArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t ring = (raw + 1023u) & ~1023u;  // stage tiles on 1,024-byte swizzle atoms
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + (ring - raw) + STAGES * STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  volatile int* stop = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int FULL = 0, EMPTY = STAGES, ACC_FULL = 2 * STAGES, ACC_EMPTY = 2 * STAGES + 2,
+            DRAIN = 2 * STAGES + 4;
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NT = (a.Ncols + BN - 1) / BN;
+  const int ntiles = ((a.Mrows + BM - 1) / BM) * NT;
+  const int KB = (a.D + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar(FULL + s), 1);
+      mbar_init(bar(EMPTY + s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(ACC_FULL + i), 1);
+      mbar_init(bar(ACC_EMPTY + i), 4);  // one arrival per epilogue warp
+    }
+    mbar_init(bar(DRAIN), 1);
+    *stop = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- TMA producer ----
+      int stage = 0;
+      uint32_t phase = 0, used = 0, last_par = 0;  // per stage: ever loaded / parity of last load
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+        const int m0 = (tile / NT) * BM, n0 = (tile % NT) * BN;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(bar(EMPTY + stage), phase ^ 1u, stop)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = ring + uint32_t(stage) * STAGE_BYTES;
+          mbar_expect_tx(bar(FULL + stage), STAGE_BYTES);
+          tma_load_2d(sa, &tmX, kb * BK, m0, bar(FULL + stage));
+          tma_load_2d(sa + A_BYTES, &tmW, kb * BK, n0, bar(FULL + stage));
+          used |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {  // let every copy in flight land before the CTA's shared memory goes away
+        for (int s = 0; s < STAGES; ++s)
+          if (used & (1u << s)) mbar_wait_teardown(bar(FULL + s), (last_par >> s) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer ----
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int it = 0;
+      for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t acc_par = uint32_t(it >> 1) & 1u;
+        if (!mbar_wait(bar(ACC_EMPTY + acc), acc_par ^ 1u, stop)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + uint32_t(acc * BN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(bar(FULL + stage), phase, stop)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = ring + uint32_t(stage) * STAGE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_bf16(d, sw128_desc(sa + kk * 32), sw128_desc(sa + A_BYTES + kk * 32),
+                     (kb | kk) != 0);
+          mma_commit(bar(EMPTY + stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) mma_commit(bar(ACC_FULL + acc));
+      }
+      // Every MMA issued has finished before TMEM and shared memory are released.
+      mma_commit(bar(DRAIN));
+      mbar_wait_teardown(bar(DRAIN), 0);
+    }
+  } else {
+    // ---- epilogue: warp w reads TMEM lanes 32*(w % 4) .. +31 ----
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t acc_par = uint32_t(it >> 1) & 1u;
+      // every lane waits; the warp leaves together (tcgen05.ld needs the whole warp)
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(ACC_FULL + acc), acc_par, stop))) break;
+      tc_fence_after();
+      const int m = (tile / NT) * BM + row, n0 = (tile % NT) * BN;
+      const int b = m / a.T, t = m - b * a.T;
+      const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_load32(taddr + uint32_t(c * 32), r);
+        if (m < a.Mrows && n0 + c * 32 < a.Ncols) store_cols<VEC>(a, b, t, n0 + c * 32, r);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(ACC_EMPTY + acc));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kTmemCols)
+                 : "memory");
+  if (threadIdx.x == 0 && *stop && a.dev_err) atomicOr(a.dev_err, SDM_DEV_TIMEOUT);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] read in boxes of box_rows x 64 columns, 128-byte swizzle,
+// zero fill outside the matrix.
+bool bf16_tile_map(CUtensorMap* map, const void* base, int rows, int cols, int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
+  const cuuint32_t box[2] = {cuuint32_t(BK), cuuint32_t(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  return n;
+}
+
+}  // namespace
+
+int launch_project(const void* x, const void* w, int B, int T, int D, int H, int S, void* kp,
+                   void* qp, int* dev_err, int max_ctas, cudaStream_t s) {
+  const long long Mrows = 1LL * B * T, Ncols = 4LL * H * S;
+  if (Mrows == 0) return SDM_OK;
+  ProjArgs pa;
+  pa.Mrows = int(Mrows);
+  pa.Ncols = int(Ncols);
+  pa.D = D;
+  pa.T = T;
+  pa.H = H;
+  pa.S = S;
+  pa.kp = static_cast<uint16_t*>(kp);
+  pa.qp = static_cast<uint16_t*>(qp);
+  pa.dev_err = dev_err;
+  CUtensorMap tmX, tmW;
+  if (!bf16_tile_map(&tmX, x, int(Mrows), D, BM) || !bf16_tile_map(&tmW, w, int(Ncols), D, BN))
+    return SDM_ECUDA;
+  const long long tiles = ((Mrows + BM - 1) / BM) * ((Ncols + BN - 1) / BN);
+  if (tiles > 0x7FFFFFFFLL || Mrows > 0x7FFFFFFFLL - BM) return SDM_EUNSUPPORTED;
+  int ctas = sm_count();
+  if (ctas <= 0) return SDM_ECUDA;
+  if (max_ctas > 0 && max_ctas < ctas) ctas = max_ctas;
+  if (tiles < ctas) ctas = int(tiles);
+  const bool vec = (2 * S) % 8 == 0 && aligned16(kp) && aligned16(qp);
+  const void* fn = vec ? reinterpret_cast<const void*>(&project_kernel<true>)
+                       : reinterpret_cast<const void*>(&project_kernel<false>);
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+      cudaSuccess)
+    return SDM_ECUDA;
+  void* args[] = {&tmX, &tmW, &pa};
+  if (cudaLaunchKernel(fn, dim3(ctas), dim3(kThreads), args, size_t(kSmemBytes), s) != cudaSuccess)
+    return SDM_ECUDA;
+  return last_launch_status();
+}
+
+}  // namespace sdm

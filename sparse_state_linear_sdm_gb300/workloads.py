@@ -33,6 +33,7 @@ import threading
 import numpy as np
 
 FIELD_KP, FIELD_QP, FIELD_V, FIELD_ALPHA, FIELD_BETA, FIELD_M0 = 0, 1, 2, 3, 4, 5
+FIELD_X, FIELD_WKQ = 6, 7
 
 _MASK = np.uint64(0xFFFFFFFF)
 _PM0 = np.uint64(0xD2511F53)
@@ -328,3 +329,24 @@ def inputs(cfg: SDMConfig, b0=0, b1=None, h0=0, h1=None, t0=0, t1=None):
     return dict(kp=halves(cfg, FIELD_KP, b0, b1, h0, h1, t0, t1),
                 qp=halves(cfg, FIELD_QP, b0, b1, h0, h1, t0, t1),
                 v=values(cfg, b0, b1, h0, h1, t0, t1), alpha=alpha, beta=beta)
+
+
+# Projection workload: token features x [B, T, D] and key/query weights w [4*H*S, D].  The
+# pages give no model width; D = 2,048 is taken as a width typical of the smallest model
+# scale they train (1.4B parameters).  x ~ N(0, 1); w ~ N(0, 1/D) (the usual fan-in
+# scaling), so that each projected sub-score is ~ N(0, 1) like the selection workloads'.
+PROJ_D = 2048
+
+
+def projection_features(seed: int, B: int, T: int, D: int, m0: int = 0, m1=None):
+    """bf16 bit patterns of x rows m0 .. m1-1 (m = b*T + t) of x [B, T, D]: uint16 [m1-m0, D]."""
+    m1 = B * T if m1 is None else m1
+    z = fill_range(seed, FIELD_X, m0 * D, (m1 - m0) * D)
+    return bf16_bits(z).reshape(m1 - m0, D)
+
+
+def projection_weights(seed: int, H: int, S: int, D: int):
+    """bf16 bit patterns of w [4*H*S, D] ~ N(0, 1/D)."""
+    z = fill_range(seed, FIELD_WKQ, 0, 4 * H * S * D)
+    scale = np.float32(1.0 / math.sqrt(D))
+    return bf16_bits((z * scale).astype(np.float32)).reshape(4 * H * S, D)

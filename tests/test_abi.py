@@ -152,3 +152,20 @@ def test_forward_chunking_and_workspace_sizes():
     # two record buffers of B*H*ceil(T/chunks) records, each rounded up to 256 bytes
     assert lib.sdm_forward_workspace_size(2, 3, 100, 16, 10, 10, 4) == 2 * ((6 * 25 * rec + 255) // 256 * 256)
     assert lib.sdm_forward_workspace_size(1, 1, 0, 16, 4, 4, 0) == 0
+
+
+def test_projection_rejects_bad_arguments_without_launching():
+    L = sdm.lib()
+    L.sdm_project_kq.argtypes = [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int] * 5 + \
+        [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    ok = ctypes.c_void_p(1 << 20)   # never dereferenced: every call below fails its checks
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    call = lambda x, w, B, T, D, H, S, kp, qp: L.sdm_project_kq(x, w, B, T, D, H, S, kp, qp, None, None)
+    assert call(ok, ok, 1, 4, 12, 1, 4, ok, ok) == EINVAL        # D % 8 != 0
+    assert call(ok, ok, 1, 4, 0, 1, 4, ok, ok) == EINVAL         # D < 8
+    assert call(ok, ok, 0, 4, 64, 1, 4, ok, ok) == EINVAL        # B < 1
+    assert call(ok, ok, 1, 4, 64, 1, 0, ok, ok) == EINVAL        # S < 1
+    assert call(ok, ok, 1, 4, 64, 1, 5000, ok, ok) == EUNSUPPORTED
+    assert call(None, ok, 1, 4, 64, 1, 4, ok, ok) == EALIGN
+    assert call(ok, odd, 1, 4, 64, 1, 4, ok, ok) == EALIGN
+    assert call(ok, ok, 1, 4, 64, 1, 4, ok, odd) == EALIGN
