@@ -58,6 +58,8 @@ def parse_args():
                          "project: the projections x -> k', q' on the tensor cores")
     ap.add_argument("--dmodel", type=int, default=0, help="feature width D of --mode project (0 = 2048)")
     ap.add_argument("--max-ctas", type=int, default=0, help="blocks of the projection kernel (0 = one per SM)")
+    ap.add_argument("--pair", type=int, default=-1, choices=[-1, 0, 1],
+                    help="projection kernel: 1 clusters of two blocks sharing weight tiles, 0 single blocks, -1 auto")
     return ap.parse_args()
 
 
@@ -760,7 +762,7 @@ def run_project(args):
     qp = torch.empty_like(kp)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     for _ in range(args.warmup):
-        sdm.project_kq(x, w, H, S, out=(kp, qp), dev_err=err, max_ctas=args.max_ctas)
+        sdm.project_kq(x, w, H, S, out=(kp, qp), dev_err=err, max_ctas=args.max_ctas, pair=args.pair)
     torch.cuda.synchronize(dev)
     K = args.steps
     E = lambda: torch.cuda.Event(enable_timing=True)
@@ -768,7 +770,7 @@ def run_project(args):
     with ClockSampler(local) as clk:
         for a, b in evs:
             a.record()
-            sdm.project_kq(x, w, H, S, out=(kp, qp), dev_err=err, max_ctas=args.max_ctas)
+            sdm.project_kq(x, w, H, S, out=(kp, qp), dev_err=err, max_ctas=args.max_ctas, pair=args.pair)
             b.record()
         torch.cuda.synchronize(dev)
     if err.item() != 0:
@@ -793,6 +795,7 @@ def run_project(args):
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"
                          if peak_kind == "measured" else "fallback 1.9 PFLOP/s"},
             "kernel_ms": {"mean": ms, "min": min(per), "max": max(per)},
+            "launch": {"max_ctas": args.max_ctas, "pair": args.pair},
             "gpu_launches": K, "clocks": clk.summary()}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle

@@ -266,15 +266,19 @@ int sdm_select_backward(const int32_t* idx, const float* dsc, int B, int H, int 
  * Requires B, T, H >= 1, 1 <= S <= SDM_MAX_S, D >= 8 with D % 8 == 0 (the row pitch of x
  * and w is a multiple of 16 bytes), B*T < 2^31, 4*H*S < 2^31; x, w, kp, qp 16-byte
  * aligned.  dev_err: device int or NULL; SDM_DEV_TIMEOUT if a wait inside the kernel ran
- * out (then kp, qp are unspecified).  Runs as one persistent kernel with one block per
- * SM on `stream`. */
+ * out (then kp, qp are unspecified).  Runs as one persistent kernel on `stream`: one
+ * block per SM, in clusters of two blocks that share the weight tiles. */
 int sdm_project_kq(const void* x, const void* w, int B, int T, int D, int H, int S, void* kp,
                    void* qp, int* dev_err, void* stream);
 
-/* sdm_project_kq_ctas - sdm_project_kq on at most max_ctas blocks (0: one per SM), to
- * leave SMs to work running beside it on other streams. */
-int sdm_project_kq_ctas(const void* x, const void* w, int B, int T, int D, int H, int S,
-                        void* kp, void* qp, int* dev_err, int max_ctas, void* stream);
+/* sdm_project_kq_tuned - sdm_project_kq with its launch shape fixed by the caller:
+ *   max_ctas  at most this many blocks (0: as many as can be resident, one per SM), to leave
+ *             SMs to work running beside it on other streams;
+ *   pair      1: blocks run in clusters of two that share each weight tile (each loads half
+ *             and multicasts it to both); 0: single blocks; -1: pairs unless B*T <= 128.
+ * Results do not depend on either. */
+int sdm_project_kq_tuned(const void* x, const void* w, int B, int T, int D, int H, int S,
+                         void* kp, void* qp, int* dev_err, int max_ctas, int pair, void* stream);
 
 /* sdm_gen_inputs - synthetic inputs (not part of the method): draws the box
  * b in [b_off, b_off+B), all H heads, tokens t in [t_off, t_off+T) of a logical

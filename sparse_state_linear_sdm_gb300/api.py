@@ -63,7 +63,7 @@ def lib() -> ctypes.CDLL:
             L.sdm_scan_backward.argtypes = [p, p, p, p, p, i, p, p, p, p, p, i, i, i, ll, i, i, i, p, p, p, p, p, p,
                                             p, p, sz, p]
             L.sdm_select_backward.argtypes = [p, p, i, i, i, i, i, p, p]
-            L.sdm_project_kq_ctas.argtypes = [p, p, i, i, i, i, i, p, p, p, i, p]
+            L.sdm_project_kq_tuned.argtypes = [p, p, i, i, i, i, i, p, p, p, i, i, p]
             for name in ("sdm_init_state_from_M0", "sdm_select", "sdm_scan_forward",
                          "sdm_scan_forward_tuned", "sdm_scan_launch_info", "sdm_gen_inputs", "sdm_gen_M0",
                          "sdm_forward_chunks", "sdm_forward_tuned", "sdm_forward", "sdm_scan_forward_train",
@@ -424,12 +424,14 @@ def select_backward(idx, dsc, S: int, out=None):
     return out
 
 
-def project_kq(x, w, H: int, S: int, out=None, dev_err=None, max_ctas: int = 0):
+def project_kq(x, w, H: int, S: int, out=None, dev_err=None, max_ctas: int = 0, pair: int = -1):
     """The projections x -> k', q' on the tensor cores: one bf16 GEMM, fp32 accumulation,
     outputs rounded to bf16 in the [B, H, T, 2, S] layout ``select`` reads.
 
     x: [B, T, D] bf16; w: [4*H*S, D] bf16, one row per output column: the k' columns in
-    (head, half, index) order, then the q' columns.  Returns (kp, qp)."""
+    (head, half, index) order, then the q' columns.  max_ctas caps the blocks (0: one per
+    SM); pair 1/0/-1: clusters of two blocks sharing weight tiles / single blocks / auto.
+    Returns (kp, qp)."""
     _need(x, "x", torch.bfloat16)
     if x.dim() != 3:
         raise ValueError("x must be [B, T, D]")
@@ -441,8 +443,8 @@ def project_kq(x, w, H: int, S: int, out=None, dev_err=None, max_ctas: int = 0):
     kp, qp = out
     _need(kp, "kp", torch.bfloat16, (B, H, T, 2, S))
     _need(qp, "qp", torch.bfloat16, (B, H, T, 2, S))
-    _call("sdm_project_kq_ctas", _p(x), _p(w), B, T, D, H, S, _p(kp), _p(qp),
-          _p(dev_err) if dev_err is not None else None, int(max_ctas), _stream(x.device))
+    _call("sdm_project_kq_tuned", _p(x), _p(w), B, T, D, H, S, _p(kp), _p(qp),
+          _p(dev_err) if dev_err is not None else None, int(max_ctas), int(pair), _stream(x.device))
     return kp, qp
 
 

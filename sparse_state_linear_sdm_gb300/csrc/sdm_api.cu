@@ -40,19 +40,20 @@ int sdm_select(const void* kp, const void* qp, int in_dt, int B, int H, int T, i
                                  sc_r, as_stream(stream));
 }
 
-int sdm_project_kq_ctas(const void* x, const void* w, int B, int T, int D, int H, int S,
-                        void* kp, void* qp, int* dev_err, int max_ctas, void* stream) {
-  if (B < 1 || T < 1 || H < 1 || S < 1 || D < 8 || D % 8 || max_ctas < 0) return SDM_EINVAL;
+int sdm_project_kq_tuned(const void* x, const void* w, int B, int T, int D, int H, int S,
+                         void* kp, void* qp, int* dev_err, int max_ctas, int pair, void* stream) {
+  if (B < 1 || T < 1 || H < 1 || S < 1 || D < 8 || D % 8 || max_ctas < 0 || pair < -1 || pair > 1)
+    return SDM_EINVAL;
   if (S > SDM_MAX_S) return SDM_EUNSUPPORTED;
   if (1LL * B * T >= (1LL << 31) || 4LL * H * S >= (1LL << 31)) return SDM_EUNSUPPORTED;
   if (!aligned16(x) || !aligned16(w) || !aligned16(kp) || !aligned16(qp)) return SDM_EALIGN;
   if (dev_err && (reinterpret_cast<uintptr_t>(dev_err) & 3u)) return SDM_EALIGN;
-  return launch_project(x, w, B, T, D, H, S, kp, qp, dev_err, max_ctas, as_stream(stream));
+  return launch_project(x, w, B, T, D, H, S, kp, qp, dev_err, max_ctas, pair, as_stream(stream));
 }
 
 int sdm_project_kq(const void* x, const void* w, int B, int T, int D, int H, int S, void* kp,
                    void* qp, int* dev_err, void* stream) {
-  return sdm_project_kq_ctas(x, w, B, T, D, H, S, kp, qp, dev_err, 0, stream);
+  return sdm_project_kq_tuned(x, w, B, T, D, H, S, kp, qp, dev_err, 0, -1, stream);
 }
 
 size_t sdm_scan_workspace_size(int B, int H, int T, int d_v, int W, int R) {

@@ -158,7 +158,7 @@ int launch_scan(float* M, const int32_t* idx_w, const float* sc_w, const int32_t
                 float* r_rows = nullptr);
 
 int launch_project(const void* x, const void* w, int B, int T, int D, int H, int S, void* kp,
-                   void* qp, int* dev_err, int max_ctas, cudaStream_t s);
+                   void* qp, int* dev_err, int max_ctas, int pair, cudaStream_t s);
 int launch_gen_inputs(unsigned long long seed, int B, int H, int T, int b_off, int t_off,
                       long long T_total, int S, int d_v, int in_dt, float alpha_lo,
                       int beta_kind, const float* half_bias, void* kp, void* qp, void* v,

@@ -48,6 +48,7 @@ constexpr uint32_t kTmemCols = 2 * BN;
 constexpr int kNumBars = 2 * STAGES + 5;  // full[], empty[], acc_full[2], acc_empty[2], drain
 constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024 /* alignment slack */ + 256;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
+constexpr int kGroup = 8;  // row-tile pairs per group of the tile order
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
 // (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
@@ -128,6 +129,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// The same box multicast into the shared memory of every CTA of the cluster in cta_mask (same
+// offset), completing on the barrier at the same offset in each of them.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map, int x,
+                                                      int y, uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
+      : "memory");
+}
+
+__device__ void pause_ns(unsigned long long ns) {
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 0; i < (1u << 24) && global_ns() - t0 < ns; ++i) {
+  }
+}
+
 // Shared-memory matrix descriptor of a K-major operand tile in the 128-byte swizzle layout
 // written by TMA: rows of 128 bytes, 8-row atoms of 1,024 bytes stacked along M/N (stride
 // byte offset 1,024; the leading byte offset is not used by this layout), descriptor
@@ -149,6 +167,14 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+// Arrives on the barrier at this offset in every CTA of cta_mask once this thread's MMAs are done.
+__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
       : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
@@ -217,7 +243,32 @@ __device__ __forceinline__ void store_cols(const ProjArgs& a, int b, int t, int 
   }
 }
 
-template <bool VEC>
+// Work unit u -> (row-tile pair mp, column tile n): groups of kGroup row-tile pairs, the
+// pairs of a group fastest, then the column tiles, so that the units running at the same
+// time share a few rows of X and a few column tiles of W in L2.
+__device__ __forceinline__ void unit_coords(int u, int MP, int NT, int& mp, int& n) {
+  const int per_group = kGroup * NT;
+  const int g = u / per_group, w = u - g * per_group;
+  const int gm = min(kGroup, MP - g * kGroup);
+  n = w / gm;
+  mp = g * kGroup + (w - n * gm);
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\nbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// CL = 1: each CTA loads its whole W tile.  CL = 2: the two CTAs of a cluster take row tiles
+// 2*mp and 2*mp+1 of the same column tile; each loads one half (128 rows) of the W tile and
+// multicasts it into both CTAs' shared memory, so each SM reads 32 KB instead of 48 KB from
+// L2 per K step.  A stage is refilled only after the MMAs of both CTAs have read it: each
+// MMA thread's commit arrives on the stage's empty barrier in both CTAs.
+template <bool VEC, int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     project_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    ProjArgs a) {
@@ -232,14 +283,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = CL == 1 ? 0 : int(cluster_rank());
+  const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
   const int NT = (a.Ncols + BN - 1) / BN;
-  const int ntiles = ((a.Mrows + BM - 1) / BM) * NT;
+  const int MP = ((a.Mrows + BM - 1) / BM + CL - 1) / CL;
+  const int units = MP * NT;
   const int KB = (a.D + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar(FULL + s), 1);
-      mbar_init(bar(EMPTY + s), 1);
+      mbar_init(bar(EMPTY + s), CL);  // one commit from the MMA thread of each CTA
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(ACC_FULL + i), 1);
@@ -260,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync_all();  // the peer's barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -269,8 +324,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0, used = 0, last_par = 0;  // per stage: ever loaded / parity of last load
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
-        const int m0 = (tile / NT) * BM, n0 = (tile % NT) * BN;
+      for (int u = cid; ok && u < units; u += ncl) {
+        int mp, n;
+        unit_coords(u, MP, NT, mp, n);
+        const int m0 = (mp * CL + rank) * BM, n0 = n * BN;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(bar(EMPTY + stage), phase ^ 1u, stop)) {
             ok = false;
@@ -279,7 +336,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = ring + uint32_t(stage) * STAGE_BYTES;
           mbar_expect_tx(bar(FULL + stage), STAGE_BYTES);
           tma_load_2d(sa, &tmX, kb * BK, m0, bar(FULL + stage));
-          tma_load_2d(sa + A_BYTES, &tmW, kb * BK, n0, bar(FULL + stage));
+          if (CL == 1) {
+            tma_load_2d(sa + A_BYTES, &tmW, kb * BK, n0, bar(FULL + stage));
+            tma_load_2d(sa + A_BYTES + B_BYTES / 2, &tmW, kb * BK, n0 + BN / 2, bar(FULL + stage));
+          } else {
+            tma_load_2d_multicast(sa + A_BYTES + rank * (B_BYTES / 2), &tmW, kb * BK,
+                                  n0 + rank * (BN / 2), bar(FULL + stage), uint16_t(0x3));
+          }
           used |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -291,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {  // let every copy in flight land before the CTA's shared memory goes away
         for (int s = 0; s < STAGES; ++s)
           if (used & (1u << s)) mbar_wait_teardown(bar(FULL + s), (last_par >> s) & 1u);
+        if (CL > 1) pause_ns(200000);  // copies the peer multicast into this CTA
       }
     }
   } else if (warp == 1) {
@@ -300,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
-      for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
+      for (int u = cid; ok && u < units; u += ncl, ++it) {
         const int acc = it & 1;
         const uint32_t acc_par = uint32_t(it >> 1) & 1u;
         if (!mbar_wait(bar(ACC_EMPTY + acc), acc_par ^ 1u, stop)) break;
@@ -317,7 +381,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < BK / 16; ++kk)
             mma_bf16(d, sw128_desc(sa + kk * 32), sw128_desc(sa + A_BYTES + kk * 32),
                      (kb | kk) != 0);
-          mma_commit(bar(EMPTY + stage));
+          if (CL == 1)
+            mma_commit(bar(EMPTY + stage));
+          else
+            mma_commit_multicast(bar(EMPTY + stage), uint16_t(0x3));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -334,13 +401,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     int it = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+    for (int u = cid; u < units; u += ncl, ++it) {
       const int acc = it & 1;
       const uint32_t acc_par = uint32_t(it >> 1) & 1u;
       // every lane waits; the warp leaves together (tcgen05.ld needs the whole warp)
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(ACC_FULL + acc), acc_par, stop))) break;
       tc_fence_after();
-      const int m = (tile / NT) * BM + row, n0 = (tile % NT) * BN;
+      int mp, n;
+      unit_coords(u, MP, NT, mp, n);
+      const int m = (mp * CL + rank) * BM + row, n0 = n * BN;
       const int b = m / a.T, t = m - b * a.T;
       const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * BN);
 #pragma unroll 1
@@ -363,6 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                  "r"(kTmemCols)
                  : "memory");
   if (threadIdx.x == 0 && *stop && a.dev_err) atomicOr(a.dev_err, SDM_DEV_TIMEOUT);
+  // Neither CTA of a pair leaves while the other may still arrive on its barriers.
+  if (CL > 1) cluster_sync_all();
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -403,9 +474,11 @@ int sm_count() {
 }  // namespace
 
 int launch_project(const void* x, const void* w, int B, int T, int D, int H, int S, void* kp,
-                   void* qp, int* dev_err, int max_ctas, cudaStream_t s) {
+                   void* qp, int* dev_err, int max_ctas, int pair, cudaStream_t s) {
   const long long Mrows = 1LL * B * T, Ncols = 4LL * H * S;
   if (Mrows == 0) return SDM_OK;
+  const long long MT = (Mrows + BM - 1) / BM, NT = (Ncols + BN - 1) / BN;
+  if (MT * NT > 0x7FFFFFFFLL || Mrows > 0x7FFFFFFFLL - 2 * BM) return SDM_EUNSUPPORTED;
   ProjArgs pa;
   pa.Mrows = int(Mrows);
   pa.Ncols = int(Ncols);
@@ -417,23 +490,45 @@ int launch_project(const void* x, const void* w, int B, int T, int D, int H, int
   pa.qp = static_cast<uint16_t*>(qp);
   pa.dev_err = dev_err;
   CUtensorMap tmX, tmW;
-  if (!bf16_tile_map(&tmX, x, int(Mrows), D, BM) || !bf16_tile_map(&tmW, w, int(Ncols), D, BN))
+  if (!bf16_tile_map(&tmX, x, int(Mrows), D, BM) || !bf16_tile_map(&tmW, w, int(Ncols), D, BN / 2))
     return SDM_ECUDA;
-  const long long tiles = ((Mrows + BM - 1) / BM) * ((Ncols + BN - 1) / BN);
-  if (tiles > 0x7FFFFFFFLL || Mrows > 0x7FFFFFFFLL - BM) return SDM_EUNSUPPORTED;
-  int ctas = sm_count();
-  if (ctas <= 0) return SDM_ECUDA;
-  if (max_ctas > 0 && max_ctas < ctas) ctas = max_ctas;
-  if (tiles < ctas) ctas = int(tiles);
+  const int CL = pair < 0 ? (MT >= 2 ? 2 : 1) : (pair ? 2 : 1);
+  const long long units = ((MT + CL - 1) / CL) * NT;
   const bool vec = (2 * S) % 8 == 0 && aligned16(kp) && aligned16(qp);
-  const void* fn = vec ? reinterpret_cast<const void*>(&project_kernel<true>)
-                       : reinterpret_cast<const void*>(&project_kernel<false>);
+  const void* fn =
+      CL == 2 ? (vec ? reinterpret_cast<const void*>(&project_kernel<true, 2>)
+                     : reinterpret_cast<const void*>(&project_kernel<false, 2>))
+              : (vec ? reinterpret_cast<const void*>(&project_kernel<true, 1>)
+                     : reinterpret_cast<const void*>(&project_kernel<false, 1>));
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
       cudaSuccess)
     return SDM_ECUDA;
+  const int sms = sm_count();
+  if (sms <= 0) return SDM_ECUDA;
+  long long clusters = sms / CL;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(CL);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(clusters * CL));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = size_t(kSmemBytes);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (CL > 1) {  // a persistent grid larger than what can be resident would run in two waves
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, fn, &cfg) != cudaSuccess || active <= 0)
+      return SDM_ECUDA;
+    if (active < clusters) clusters = active;
+  }
+  if (max_ctas > 0 && max_ctas / CL < clusters) clusters = max_ctas / CL > 0 ? max_ctas / CL : 1;
+  if (units < clusters) clusters = units;
+  cfg.gridDim = dim3(unsigned(clusters * CL));
   void* args[] = {&tmX, &tmW, &pa};
-  if (cudaLaunchKernel(fn, dim3(ctas), dim3(kThreads), args, size_t(kSmemBytes), s) != cudaSuccess)
-    return SDM_ECUDA;
+  if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return SDM_ECUDA;
   return last_launch_status();
 }
 

@@ -44,30 +44,44 @@ def _check(got, want, mag, D, label):
     assert frac >= 0.95, f"{label}: only {frac:.3f} of outputs correctly rounded"
 
 
-def _run(xb, wb, H, S, max_ctas=0):
+def _run(xb, wb, H, S, max_ctas=0, pair=-1):
     x, w = _bf16_dev(xb), _bf16_dev(wb)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    kp, qp = sdm.project_kq(x, w, H, S, dev_err=err, max_ctas=max_ctas)
+    kp, qp = sdm.project_kq(x, w, H, S, dev_err=err, max_ctas=max_ctas, pair=pair)
     torch.cuda.synchronize()
     assert err.item() == 0
     return kp, qp
 
 
+@pytest.mark.parametrize("pair", [0, 1])
 @pytest.mark.parametrize("B,T,D,H,S,max_ctas", [
     (1, 1, 8, 1, 4, 0),          # one token, D < one K block, 16 output columns
     (2, 100, 72, 2, 6, 0),       # 2S % 8 != 0 (column-wise stores), ragged K block
-    (1, 300, 128, 1, 64, 0),     # one column tile, ragged row tile
+    (1, 300, 128, 1, 64, 0),     # one column tile, ragged (and, paired, empty) row tiles
     (2, 257, 512, 4, 128, 0),    # 5 x 8 tiles
-    (2, 257, 512, 4, 128, 3),    # the same on 3 blocks: ~13 tiles each, accumulators alternate
-    (1, 70, 256, 2, 64, 1),      # one block runs every tile
+    (2, 257, 512, 4, 128, 4),    # the same on 4 blocks: ~10-20 tiles each, accumulators alternate
+    (1, 70, 256, 2, 64, 2),      # one block (or one pair) runs every tile
+    (9, 300, 64, 1, 128, 0),     # several groups of row tiles in the tile order
     (1, 129, 2048, 4, 1024, 0),  # the full-size output width and depth, two row tiles
 ])
-def test_projection_matches_oracle(B, T, D, H, S, max_ctas):
+def test_projection_matches_oracle(B, T, D, H, S, max_ctas, pair):
     xb, wb = _inputs(B * 31 + T + D, B, T, D, H, S)
-    kp, qp = _run(xb, wb, H, S, max_ctas)
+    kp, qp = _run(xb, wb, H, S, max_ctas, pair)
     rk, rq, (mk, mq) = oracle.project(wl.bf16_to_f32(xb), wl.bf16_to_f32(wb), H, S)
-    _check(_f32(kp), rk, mk, D, ("kp", B, T, D, H, S, max_ctas))
-    _check(_f32(qp), rq, mq, D, ("qp", B, T, D, H, S, max_ctas))
+    _check(_f32(kp), rk, mk, D, ("kp", B, T, D, H, S, max_ctas, pair))
+    _check(_f32(qp), rq, mq, D, ("qp", B, T, D, H, S, max_ctas, pair))
+
+
+def test_pairs_and_single_blocks_agree_bit_for_bit():
+    """Both launch shapes accumulate each output in the same order (K blocks in sequence,
+    the same MMA shape), so their results are identical."""
+    B, T, D, H, S = 3, 200, 320, 2, 128
+    xb, wb = _inputs(99, B, T, D, H, S)
+    k1, q1 = _run(xb, wb, H, S, 0, 0)
+    k2, q2 = _run(xb, wb, H, S, 0, 1)
+    k3, q3 = _run(xb, wb, H, S, 6, 1)
+    assert torch.equal(k1, k2) and torch.equal(q1, q2)
+    assert torch.equal(k1, k3) and torch.equal(q1, q3)
 
 
 def test_projected_halves_select_like_the_oracle():
