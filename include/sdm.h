@@ -275,7 +275,10 @@ int sdm_project_kq(const void* x, const void* w, int B, int T, int D, int H, int
  *   max_ctas  at most this many blocks (0: as many as can be resident, one per SM), to leave
  *             SMs to work running beside it on other streams;
  *   pair      1: blocks run in clusters of two that share each weight tile (each loads half
- *             and multicasts it to both); 0: single blocks; -1: pairs unless B*T <= 128.
+ *             and multicasts it to both); 2: clusters of two whose MMAs run as one 256-row
+ *             tile across both SMs (tcgen05 cta_group::2), each block staging its own rows
+ *             of x and half of the weight tile; 0: single blocks; -1: pairs (1) unless
+ *             B*T <= 128.
  * Results do not depend on either. */
 int sdm_project_kq_tuned(const void* x, const void* w, int B, int T, int D, int H, int S,
                          void* kp, void* qp, int* dev_err, int max_ctas, int pair, void* stream);

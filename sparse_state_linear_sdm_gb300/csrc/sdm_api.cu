@@ -42,7 +42,7 @@ int sdm_select(const void* kp, const void* qp, int in_dt, int B, int H, int T, i
 
 int sdm_project_kq_tuned(const void* x, const void* w, int B, int T, int D, int H, int S,
                          void* kp, void* qp, int* dev_err, int max_ctas, int pair, void* stream) {
-  if (B < 1 || T < 1 || H < 1 || S < 1 || D < 8 || D % 8 || max_ctas < 0 || pair < -1 || pair > 1)
+  if (B < 1 || T < 1 || H < 1 || S < 1 || D < 8 || D % 8 || max_ctas < 0 || pair < -1 || pair > 2)
     return SDM_EINVAL;
   if (S > SDM_MAX_S) return SDM_EUNSUPPORTED;
   if (1LL * B * T >= (1LL << 31) || 4LL * H * S >= (1LL << 31)) return SDM_EUNSUPPORTED;

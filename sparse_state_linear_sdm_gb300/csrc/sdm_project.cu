@@ -48,7 +48,7 @@ constexpr uint32_t kTmemCols = 2 * BN;
 constexpr int kNumBars = 2 * STAGES + 5;  // full[], empty[], acc_full[2], acc_empty[2], drain
 constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024 /* alignment slack */ + 256;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
-constexpr int kGroup = 8;  // row-tile pairs per group of the tile order
+constexpr int kGroup = 32;  // row-tile pairs per group of the tile order (measured best of 1..64)
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
 // (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
@@ -436,6 +436,245 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (CL > 1) cluster_sync_all();
 }
 
+// ---- 2-SM variant: one tcgen05.mma.cta_group::2 M256 x N256 per K16 for a CTA pair ----
+//
+// The even CTA of a cluster of two (the leader) issues the MMAs for both: A rows 0-127 come
+// from its own shared memory and rows 128-255 from its peer's (same offset), the W tile's
+// rows 0-127 from the leader and 128-255 from the peer, and each CTA's TMEM receives its own
+// 128 rows of the 256 x 256 accumulator.  Each CTA stages only its own X rows and its half of
+// the W tile (32 KB per stage, 6 stages).  Both CTAs' copies complete on the leader's full
+// barrier; the leader's commits arrive on the empty and accumulator-full barriers of both
+// CTAs; the epilogue warps of both arrive on the leader's accumulator-empty barrier.
+constexpr int STAGES2 = 6;
+constexpr int STAGE2_BYTES = A_BYTES + B_BYTES / 2;
+constexpr int kSmemBytes2 = STAGES2 * STAGE2_BYTES + 1024 + 256;
+constexpr int kNumBars2 = 2 * STAGES2 + 5;
+constexpr uint32_t kIdesc2 = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) |
+                             (uint32_t((2 * BM) >> 4) << 24);
+
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait with cluster-scope acquire (barriers that the peer CTA arrives on).
+__device__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* stop) {
+  if (mbar_test_cluster(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 1; i < (1u << 28); ++i) {
+    if (mbar_test_cluster(bar, parity)) return true;
+    if ((i & 31u) == 0) {
+      if (*stop) return false;
+      if (global_ns() - t0 > kWaitNs) break;
+    }
+  }
+  *stop = 1;
+  return false;
+}
+// A box loaded into this CTA's shared memory, completing on a barrier of either CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t cluster_bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".cta_group::2 [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(cluster_bar)
+      : "memory");
+}
+__device__ __forceinline__ void mma2_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %3, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %4, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(accumulate), "r"(kIdesc2)
+      : "memory");
+}
+__device__ __forceinline__ void mma2_commit_both(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(uint16_t(0x3))
+      : "memory");
+}
+__device__ __forceinline__ void mma2_commit_local(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads, 1)
+    project_kernel_2sm(const __grid_constant__ CUtensorMap tmX,
+                       const __grid_constant__ CUtensorMap tmW, ProjArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t ring = (raw + 1023u) & ~1023u;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + (ring - raw) + STAGES2 * STAGE2_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars2);
+  volatile int* stop = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int FULL = 0, EMPTY = STAGES2, ACC_FULL = 2 * STAGES2, ACC_EMPTY = 2 * STAGES2 + 2,
+            DRAIN = 2 * STAGES2 + 4;
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int cid = blockIdx.x / 2, ncl = gridDim.x / 2;
+  const int NT = (a.Ncols + BN - 1) / BN;
+  const int MP = ((a.Mrows + BM - 1) / BM + 1) / 2;
+  const int units = MP * NT;
+  const int KB = (a.D + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES2; ++s) {
+      mbar_init(bar(FULL + s), 1);   // the leader's expect_tx; both CTAs' bytes
+      mbar_init(bar(EMPTY + s), 1);  // the leader's commit
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(ACC_FULL + i), 1);
+      mbar_init(bar(ACC_EMPTY + i), 8);  // the 4 epilogue warps of each CTA
+    }
+    mbar_init(bar(DRAIN), 1);
+    *stop = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+  }
+  if (warp == 1) {  // one warp of each CTA of the pair allocates, together
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- TMA producer (both CTAs) ----
+      int stage = 0;
+      uint32_t phase = 0, used = 0, last_par = 0;
+      bool ok = true;
+      for (int u = cid; ok && u < units; u += ncl) {
+        int mp, n;
+        unit_coords(u, MP, NT, mp, n);
+        const int m0 = (mp * 2 + int(rank)) * BM, n0 = n * BN;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_cluster(bar(EMPTY + stage), phase ^ 1u, stop)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = ring + uint32_t(stage) * STAGE2_BYTES;
+          const uint32_t full_leader = cluster_addr(bar(FULL + stage), 0);
+          if (leader) mbar_expect_tx(bar(FULL + stage), 2 * STAGE2_BYTES);
+          tma_load_2d_pair(sa, &tmX, kb * BK, m0, full_leader);
+          tma_load_2d_pair(sa + A_BYTES, &tmW, kb * BK, n0 + int(rank) * (BN / 2), full_leader);
+          used |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES2) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        if (leader)
+          for (int s = 0; s < STAGES2; ++s)
+            if (used & (1u << s)) mbar_wait_teardown(bar(FULL + s), (last_par >> s) & 1u);
+        pause_ns(200000);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---- MMA issuer (leader only) ----
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int it = 0;
+      for (int u = cid; ok && u < units; u += ncl, ++it) {
+        const int acc = it & 1;
+        const uint32_t acc_par = uint32_t(it >> 1) & 1u;
+        if (!mbar_wait_cluster(bar(ACC_EMPTY + acc), acc_par ^ 1u, stop)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + uint32_t(acc * BN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_cluster(bar(FULL + stage), phase, stop)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = ring + uint32_t(stage) * STAGE2_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma2_bf16(d, sw128_desc(sa + kk * 32), sw128_desc(sa + A_BYTES + kk * 32),
+                      (kb | kk) != 0);
+          mma2_commit_both(bar(EMPTY + stage));
+          if (++stage == STAGES2) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) mma2_commit_both(bar(ACC_FULL + acc));
+      }
+      mma2_commit_local(bar(DRAIN));
+      mbar_wait_teardown(bar(DRAIN), 0);
+    }
+  } else {
+    // ---- epilogue (both CTAs): warp w reads TMEM lanes 32*(w % 4) .. +31 ----
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    int it = 0;
+    for (int u = cid; u < units; u += ncl, ++it) {
+      const int acc = it & 1;
+      const uint32_t acc_par = uint32_t(it >> 1) & 1u;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_cluster(bar(ACC_FULL + acc), acc_par, stop))) break;
+      tc_fence_after();
+      int mp, n;
+      unit_coords(u, MP, NT, mp, n);
+      const int m = (mp * 2 + int(rank)) * BM + row, n0 = n * BN;
+      const int b = m / a.T, t = m - b * a.T;
+      const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_load32(taddr + uint32_t(c * 32), r);
+        if (m < a.Mrows && n0 + c * 32 < a.Ncols) store_cols<VEC>(a, b, t, n0 + c * 32, r);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(cluster_addr(bar(ACC_EMPTY + acc), 0));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // the leader's MMAs into both CTAs' TMEM are done before either frees it
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kTmemCols)
+                 : "memory");
+  if (threadIdx.x == 0 && *stop && a.dev_err) atomicOr(a.dev_err, SDM_DEV_TIMEOUT);
+  cluster_sync_all();
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -492,16 +731,19 @@ int launch_project(const void* x, const void* w, int B, int T, int D, int H, int
   CUtensorMap tmX, tmW;
   if (!bf16_tile_map(&tmX, x, int(Mrows), D, BM) || !bf16_tile_map(&tmW, w, int(Ncols), D, BN / 2))
     return SDM_ECUDA;
-  const int CL = pair < 0 ? (MT >= 2 ? 2 : 1) : (pair ? 2 : 1);
+  const int mode = pair < 0 ? (MT >= 2 ? 1 : 0) : pair;  // 0 single, 1 multicast pair, 2 2-SM MMA
+  const int CL = mode == 0 ? 1 : 2;
   const long long units = ((MT + CL - 1) / CL) * NT;
   const bool vec = (2 * S) % 8 == 0 && aligned16(kp) && aligned16(qp);
   const void* fn =
-      CL == 2 ? (vec ? reinterpret_cast<const void*>(&project_kernel<true, 2>)
-                     : reinterpret_cast<const void*>(&project_kernel<false, 2>))
-              : (vec ? reinterpret_cast<const void*>(&project_kernel<true, 1>)
-                     : reinterpret_cast<const void*>(&project_kernel<false, 1>));
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-      cudaSuccess)
+      mode == 2   ? (vec ? reinterpret_cast<const void*>(&project_kernel_2sm<true>)
+                         : reinterpret_cast<const void*>(&project_kernel_2sm<false>))
+      : mode == 1 ? (vec ? reinterpret_cast<const void*>(&project_kernel<true, 2>)
+                         : reinterpret_cast<const void*>(&project_kernel<false, 2>))
+                  : (vec ? reinterpret_cast<const void*>(&project_kernel<true, 1>)
+                         : reinterpret_cast<const void*>(&project_kernel<false, 1>));
+  const int smem = mode == 2 ? kSmemBytes2 : kSmemBytes;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return SDM_ECUDA;
   const int sms = sm_count();
   if (sms <= 0) return SDM_ECUDA;
@@ -514,7 +756,7 @@ int launch_project(const void* x, const void* w, int B, int T, int D, int H, int
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(clusters * CL));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = size_t(kSmemBytes);
+  cfg.dynamicSmemBytes = size_t(smem);
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;

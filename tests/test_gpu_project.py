@@ -53,7 +53,7 @@ def _run(xb, wb, H, S, max_ctas=0, pair=-1):
     return kp, qp
 
 
-@pytest.mark.parametrize("pair", [0, 1])
+@pytest.mark.parametrize("pair", [0, 1, 2])
 @pytest.mark.parametrize("B,T,D,H,S,max_ctas", [
     (1, 1, 8, 1, 4, 0),          # one token, D < one K block, 16 output columns
     (2, 100, 72, 2, 6, 0),       # 2S % 8 != 0 (column-wise stores), ragged K block
@@ -82,6 +82,18 @@ def test_pairs_and_single_blocks_agree_bit_for_bit():
     k3, q3 = _run(xb, wb, H, S, 6, 1)
     assert torch.equal(k1, k2) and torch.equal(q1, q2)
     assert torch.equal(k1, k3) and torch.equal(q1, q3)
+
+
+def test_two_sm_tiles_on_few_pairs():
+    """The 2-SM shape (tcgen05 cta_group::2) with one and three pairs: each pair runs many
+    256 x 256 tiles, so both accumulators and every stage wrap many times."""
+    B, T, D, H, S = 2, 300, 384, 2, 128
+    xb, wb = _inputs(123, B, T, D, H, S)
+    rk, rq, (mk, mq) = oracle.project(wl.bf16_to_f32(xb), wl.bf16_to_f32(wb), H, S)
+    for ctas in (2, 6):
+        kp, qp = _run(xb, wb, H, S, ctas, 2)
+        _check(_f32(kp), rk, mk, D, ("kp 2sm", ctas))
+        _check(_f32(qp), rq, mq, D, ("qp 2sm", ctas))
 
 
 def test_projected_halves_select_like_the_oracle():
