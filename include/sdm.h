@@ -267,7 +267,7 @@ int sdm_select_backward(const int32_t* idx, const float* dsc, int B, int H, int 
  * and w is a multiple of 16 bytes), B*T < 2^31, 4*H*S < 2^31; x, w, kp, qp 16-byte
  * aligned.  dev_err: device int or NULL; SDM_DEV_TIMEOUT if a wait inside the kernel ran
  * out (then kp, qp are unspecified).  Runs as one persistent kernel on `stream`: one
- * block per SM, in clusters of two blocks that share the weight tiles. */
+ * block per SM, in clusters of two blocks that compute 256 x 256 output tiles together. */
 int sdm_project_kq(const void* x, const void* w, int B, int T, int D, int H, int S, void* kp,
                    void* qp, int* dev_err, void* stream);
 
@@ -277,8 +277,8 @@ int sdm_project_kq(const void* x, const void* w, int B, int T, int D, int H, int
  *   pair      1: blocks run in clusters of two that share each weight tile (each loads half
  *             and multicasts it to both); 2: clusters of two whose MMAs run as one 256-row
  *             tile across both SMs (tcgen05 cta_group::2), each block staging its own rows
- *             of x and half of the weight tile; 0: single blocks; -1: pairs (1) unless
- *             B*T <= 128.
+ *             of x and half of the weight tile; 0: single blocks; -1: 2 unless B*T <= 128
+ *             (then 0).
  * Results do not depend on either. */
 int sdm_project_kq_tuned(const void* x, const void* w, int B, int T, int D, int H, int S,
                          void* kp, void* qp, int* dev_err, int max_ctas, int pair, void* stream);

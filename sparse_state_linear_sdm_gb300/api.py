@@ -430,7 +430,8 @@ def project_kq(x, w, H: int, S: int, out=None, dev_err=None, max_ctas: int = 0, 
 
     x: [B, T, D] bf16; w: [4*H*S, D] bf16, one row per output column: the k' columns in
     (head, half, index) order, then the q' columns.  max_ctas caps the blocks (0: one per
-    SM); pair 1/0/-1: clusters of two blocks sharing weight tiles / single blocks / auto.
+    SM); pair 2/1/0/-1: two-SM MMA tiles / clusters of two blocks sharing weight tiles /
+    single blocks / auto (2 unless there is a single row tile).
     Returns (kp, qp)."""
     _need(x, "x", torch.bfloat16)
     if x.dim() != 3:

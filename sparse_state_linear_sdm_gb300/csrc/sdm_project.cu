@@ -11,20 +11,26 @@
 // even) and stored straight into the [B,H,T,2,S] layout the selection reads, so no
 // transpose pass follows.
 //
-// Kernel: persistent, one CTA per SM, 128 x 256 output tiles (all 256 columns of a tile
-// lie in one head's k' or q' when S % 128 == 0), K in steps of 64 (one 128-byte swizzle
-// atom of bf16).
-//   warp 0      TMA producer: the X tile (128 x 64) and the W tile (256 x 64), 128-byte
-//               swizzled, into a 4-stage ring of shared memory (48 KB per stage)
-//   warp 1      TMEM owner (allocates 512 columns: two 256-column fp32 accumulators) and
-//               MMA issuer (one thread): 4 x tcgen05.mma M128 N256 K16 per stage;
-//               tcgen05.commit frees the stage and, after a tile's last stage, hands the
-//               accumulator to the epilogue
+// Kernels: persistent, one CTA per SM, K in steps of 64 (one 128-byte swizzle atom of bf16),
+// three launch shapes of the same warp roles:
+//   warp 0      TMA producer: X and W tiles, 128-byte swizzled, into a ring of stages in
+//               shared memory
+//   warp 1      TMEM owner (512 columns: two 256-column fp32 accumulators) and MMA issuer
+//               (one thread); tcgen05.commit frees a stage and, after a tile's last stage,
+//               hands the accumulator to the epilogue
 //   warps 2..5  epilogue: each warp reads its 32 TMEM lanes (= 32 rows of the tile) with
-//               tcgen05.ld, converts to bf16 and stores 16-byte pieces of the row; the
-//               other accumulator is meanwhile being filled by the next tile's MMAs
-// Tiles run m-major (the 2*H*2S / 256 column tiles of a row block back to back), so the
-// resident CTAs share a few row blocks of X and all of W in L2.
+//               tcgen05.ld, converts to bf16 and stores 16-byte pieces of the row, while the
+//               other accumulator is filled by the next tile's MMAs
+// (0) single CTAs: 128 x 256 tiles, tcgen05.mma M128 N256, 4 stages of 48 KB;
+// (1) CTA pairs that multicast halves of the shared W tile: the same MMAs, 32 KB per SM
+//     read from L2 per K step instead of 48 KB;
+// (2) the default: CTA pairs whose MMAs form one 256 x 256 tile (tcgen05.mma cta_group::2
+//     M256 N256, issued by the even CTA), each CTA staging only its 128 rows of X and half
+//     of the W tile (6 stages of 32 KB), which halves the operand bytes each SM's shared
+//     memory takes in and hands to the tensor core per flop.
+// All 256 columns of a tile lie in one head's k' or q' when S % 128 == 0.  Tiles run in
+// groups of row tiles (see unit_coords), so the CTAs running at once share rows of X and
+// column tiles of W in L2.
 // Every mbarrier wait is bounded in time: an expired wait raises a CTA-wide stop flag,
 // every role leaves its loop, outstanding copies and MMAs are waited for (bounded), TMEM
 // is freed and SDM_DEV_TIMEOUT is reported through dev_err.
@@ -731,7 +737,7 @@ int launch_project(const void* x, const void* w, int B, int T, int D, int H, int
   CUtensorMap tmX, tmW;
   if (!bf16_tile_map(&tmX, x, int(Mrows), D, BM) || !bf16_tile_map(&tmW, w, int(Ncols), D, BN / 2))
     return SDM_ECUDA;
-  const int mode = pair < 0 ? (MT >= 2 ? 1 : 0) : pair;  // 0 single, 1 multicast pair, 2 2-SM MMA
+  const int mode = pair < 0 ? (MT >= 2 ? 2 : 0) : pair;  // 0 single, 1 multicast pair, 2 2-SM MMA
   const int CL = mode == 0 ? 1 : 2;
   const long long units = ((MT + CL - 1) / CL) * NT;
   const bool vec = (2 * S) % 8 == 0 && aligned16(kp) && aligned16(qp);
