@@ -244,7 +244,7 @@ def make_state(cfg, rank, dev, torch, sdm, wl):
                  torch.empty(sh + (cfg.R,), dtype=torch.float32, device=dev))
     st["o"] = torch.empty(sh + (cfg.d_v,), dtype=torch.float32, device=dev)
     st["ws"] = sdm.scan_workspace(cfg.B, cfg.H, cfg.T, cfg.d_v, cfg.W, cfg.R, dev)
-    st["fws"] = sdm.forward_workspace(cfg.B, cfg.H, cfg.T, cfg.d_v, cfg.W, cfg.R, dev, 0)
+    st["fws"] = sdm.forward_workspace(cfg.B, cfg.H, cfg.T, cfg.S, cfg.d_v, cfg.W, cfg.R, dev, 0)
     st["err"] = torch.zeros(1, dtype=torch.int32, device=dev)
     st["side"] = sdm.side_stream(dev)  # high priority: init shares the SMs with the selection
     return st
@@ -256,9 +256,10 @@ def run_forward(st, cfg, sdm, args, inp=None, o=None, scan_ev=None):
     scan_ev: 2 * chunks timing events recorded around each chunk's scan kernel."""
     inp = st if inp is None else inp
     o = st["o"] if o is None else o
-    if st["fws"].numel() < sdm.lib().sdm_forward_workspace_size(cfg.B, cfg.H, cfg.T, cfg.d_v, cfg.W, cfg.R,
+    if st["fws"].numel() < sdm.lib().sdm_forward_workspace_size(cfg.B, cfg.H, cfg.T, cfg.S, cfg.d_v, cfg.W, cfg.R,
                                                                  args.chunks):
-        st["fws"] = sdm.forward_workspace(cfg.B, cfg.H, cfg.T, cfg.d_v, cfg.W, cfg.R, st["M"].device, args.chunks)
+        st["fws"] = sdm.forward_workspace(cfg.B, cfg.H, cfg.T, cfg.S, cfg.d_v, cfg.W, cfg.R, st["M"].device,
+                                          args.chunks)
     sdm.forward(inp["kp"], inp["qp"], inp["v"], inp["alpha"], inp["beta"], st["M0"], cfg.W, cfg.R, M=st["M"],
                 workspace=st["fws"], dev_err=st["err"], out=st["sel"], o=o, chunks=args.chunks,
                 scan_events=scan_ev)

@@ -51,7 +51,7 @@ def lib() -> ctypes.CDLL:
             L.sdm_scan_launch_info.argtypes = [i, i, i, i, i, p, p, p, p]
             L.sdm_gen_inputs.argtypes = [ull, i, i, i, i, i, ll, i, i, i, f, i, p, p, p, p, p, p, p]
             L.sdm_gen_M0.argtypes = [ull, i, ll, i, f, p, p]
-            L.sdm_forward_workspace_size.argtypes = [i, i, i, i, i, i, i]
+            L.sdm_forward_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
             L.sdm_forward_workspace_size.restype = sz
             L.sdm_forward_chunks.argtypes = [i, i]
             L.sdm_forward_tuned.argtypes = [p, p, i, p, i, p, p, p, p, i, i, i, i, i, i, i, p, p, p, p, p, p,
@@ -296,8 +296,10 @@ def forward_chunks(T: int, chunks: int = 0) -> int:
     return lib().sdm_forward_chunks(T, chunks)
 
 
-def forward_workspace(B: int, H: int, T: int, d_v: int, W: int, R: int, device, chunks: int = 0) -> torch.Tensor:
-    n = lib().sdm_forward_workspace_size(B, H, T, d_v, W, R, chunks)
+def forward_workspace(B: int, H: int, T: int, S: int, d_v: int, W: int, R: int, device,
+                      chunks: int = 0) -> torch.Tensor:
+    """Scratch for forward(): two chunks of planning records and the first-write table."""
+    n = lib().sdm_forward_workspace_size(B, H, T, S, d_v, W, R, chunks)
     return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
 
 
@@ -344,7 +346,7 @@ def forward(kp, qp, v, alpha, beta, M0, W: int, R: int, M=None, workspace=None, 
         o = torch.empty((B, H, T, dv), dtype=torch.float32, device=M.device)
     _need(o, "o", torch.float32, (B, H, T, dv))
     if workspace is None:
-        workspace = forward_workspace(B, H, T, dv, W, R, M.device, chunks)
+        workspace = forward_workspace(B, H, T, S, dv, W, R, M.device, chunks)
     _need(workspace, "workspace", torch.uint8)
     if dev_err is not None:
         _need(dev_err, "dev_err", torch.int32)

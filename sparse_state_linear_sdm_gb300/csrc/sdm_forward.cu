@@ -2,21 +2,27 @@
 // gist.science/it/paper/2607.07386, "Meccanismo Core" items 2-4 and "Stato Iniziale
 // Appreso"): state from M_0, product-key selection, planning, sparse gated-delta scan.
 //
-// The selection is compare/select work on the SM cores, the scan and the state
-// initialisation are bound by HBM.  Run one after the other they leave either the cores
-// or HBM idle, so the sequence is cut into token chunks and four streams overlap them:
+// The selection is compare/select work on the SM cores, the scan is bound by HBM.  Run one
+// after the other they leave either the cores or HBM idle, so the sequence is cut into token
+// chunks and four streams overlap them:
 //
-//   init stream (high priority)    M = M_0 broadcast
 //   select stream                  select(0), select(1), ... (full-size outputs: never waits)
-//   plan stream                    plan(c) -> record buffer c % 2, after select(c) and
-//                                  once scan(c - 2) has consumed that buffer
+//   plan stream                    first-writes(c), then plan(c) -> record buffer c % 2,
+//                                  after select(c) and once scan(c - 2) has consumed that
+//                                  buffer
 //   scan stream (high priority)    scan(c) over record buffer c % 2, after plan(c)
-//                                  (the first also after the initialisation)
+//   init stream (high priority)    M_0 into the rows no token writes, after the last
+//                                  first-writes pass (beside the remaining scans)
 //
-// The selection runs ahead while the state is initialised (the scan cannot start before
-// that) and then shares the SMs with the scans.  The scan stream has high priority so that
-// its blocks get SM slots ahead of the selection's queue of short blocks.  A chunk boundary is a fresh scan pipeline, exactly as chained calls of
-// sdm_scan_forward: the results are bit-identical to the unpipelined path.
+// Starting from M_0, the state is not copied before the scan: a row still holds M_0 until
+// the first token that writes it, so the planning pass, given each slot's first writing
+// token, sends the gathers of rows not yet written to M_0, and the rows never written get
+// M_0 at the end.  The scan starts as soon as the first chunk is selected and planned, and
+// the copy of M_0 shrinks to the rows no token touches.  Continuing from M (M_0 == NULL)
+// skips all of that.  The scan stream has high priority so that its blocks get SM slots
+// ahead of the selection's queue of short blocks.  A chunk boundary is a fresh scan
+// pipeline, exactly as chained calls of sdm_scan_forward: the results are bit-identical to
+// the unpipelined path (state copied from M_0, then one scan).
 //
 // The streams and events are created once per device and reused; calls on one device
 // are enqueued one at a time (a mutex), and the caller's stream waits for all of the
@@ -36,6 +42,7 @@ struct Pipeline {
   bool ready = false;
   cudaStream_t init = nullptr, sel = nullptr, plan = nullptr, scan = nullptr;
   cudaEvent_t start = nullptr, init_done = nullptr, plan_end = nullptr, scan_done = nullptr;
+  cudaEvent_t writes_known = nullptr;              // every chunk's first-writes pass done
   cudaEvent_t sel_done[2] = {nullptr, nullptr};    // selection of chunk c (c % 2) written
   cudaEvent_t plan_done[2] = {nullptr, nullptr};   // records of buffer i written
   cudaEvent_t buf_free[2] = {nullptr, nullptr};    // records of buffer i consumed
@@ -57,9 +64,9 @@ int pipeline_of_current_device(Pipeline** out) {
         cudaStreamCreateWithPriority(&p.plan, cudaStreamNonBlocking, least) != cudaSuccess ||
         cudaStreamCreateWithPriority(&p.scan, cudaStreamNonBlocking, greatest) != cudaSuccess)
       return SDM_ECUDA;
-    cudaEvent_t* evs[] = {&p.start,        &p.init_done,    &p.plan_end,    &p.scan_done,
+    cudaEvent_t* evs[] = {&p.start,        &p.init_done,    &p.plan_end,     &p.scan_done,
                           &p.sel_done[0],  &p.sel_done[1],  &p.plan_done[0], &p.plan_done[1],
-                          &p.buf_free[0],  &p.buf_free[1]};
+                          &p.buf_free[0],  &p.buf_free[1],  &p.writes_known};
     for (cudaEvent_t* e : evs)
       if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return SDM_ECUDA;
     p.ready = true;
@@ -83,6 +90,12 @@ size_t forward_buffer_bytes(int BH, int Tc, int d_v, int W, int R) {
   return (b + 255) / 256 * 256;
 }
 
+// First-write table: one int32 per (b, h, slot).
+size_t first_write_bytes(int BH, long long N) {
+  const size_t b = size_t(BH) * size_t(N) * 4;
+  return (b + 255) / 256 * 256;
+}
+
 }  // namespace
 }  // namespace sdm
 
@@ -90,9 +103,10 @@ using namespace sdm;
 
 extern "C" {
 
-size_t sdm_forward_workspace_size(int B, int H, int T, int d_v, int W, int R, int chunks) {
-  if (B < 1 || H < 1 || T < 1 || d_v < 4 || W < 1 || R < 1 || chunks < 0) return 0;
-  return 2 * forward_buffer_bytes(B * H, forward_chunk_tokens(T, chunks), d_v, W, R);
+size_t sdm_forward_workspace_size(int B, int H, int T, int S, int d_v, int W, int R, int chunks) {
+  if (B < 1 || H < 1 || T < 1 || S < 1 || d_v < 4 || W < 1 || R < 1 || chunks < 0) return 0;
+  return 2 * forward_buffer_bytes(B * H, forward_chunk_tokens(T, chunks), d_v, W, R) +
+         first_write_bytes(B * H, (long long)S * S);
 }
 
 int sdm_forward_chunks(int T, int chunks) {
@@ -119,7 +133,8 @@ int sdm_forward_tuned(const void* kp, const void* qp, int in_dt, const void* v, 
   cudaStream_t s = as_stream(stream);
   if (T == 0) return M0 ? launch_init_state(M, M0, B, H, N, d_v, s) : SDM_OK;
   if (!aligned16(workspace)) return SDM_EALIGN;
-  if (workspace_bytes < sdm_forward_workspace_size(B, H, T, d_v, W, R, chunks)) return SDM_ENOSPACE;
+  if (workspace_bytes < sdm_forward_workspace_size(B, H, T, S, d_v, W, R, chunks))
+    return SDM_ENOSPACE;
 
   const int BH = B * H;
   ScanShape shape;
@@ -129,6 +144,8 @@ int sdm_forward_tuned(const void* kp, const void* qp, int in_dt, const void* v, 
   const int n = (T + Tc - 1) / Tc;
   const size_t buf = forward_buffer_bytes(BH, Tc, d_v, W, R);
   void* rec[2] = {workspace, static_cast<unsigned char*>(workspace) + buf};
+  int32_t* first =
+      M0 ? reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + 2 * buf) : nullptr;
 
   std::lock_guard<std::mutex> lock(g_mu);
   Pipeline* p = nullptr;
@@ -140,12 +157,9 @@ int sdm_forward_tuned(const void* kp, const void* qp, int in_dt, const void* v, 
   SDM_CK(cudaStreamWaitEvent(p->init, p->start, 0));
   SDM_CK(cudaStreamWaitEvent(p->sel, p->start, 0));
   SDM_CK(cudaStreamWaitEvent(p->plan, p->start, 0));
-  if (M0) {
-    st = launch_init_state(M, M0, B, H, N, d_v, p->init);
-    if (st != SDM_OK) return st;
-  }
-  SDM_CK(cudaEventRecord(p->init_done, p->init));
-  SDM_CK(cudaStreamWaitEvent(p->scan, p->init_done, 0));
+  SDM_CK(cudaStreamWaitEvent(p->scan, p->start, 0));
+  if (first)
+    SDM_CK(cudaMemsetAsync(first, 0x7F, first_write_bytes(BH, N), p->plan));  // kNeverWritten
   // Enqueued chunk by chunk, so every wait on a reused event refers to its latest record.
   for (int c = 0; c < n; ++c) {
     const TokenWindow win{BH, (c + 1) * Tc <= T ? Tc : T - c * Tc, T, c * Tc};
@@ -156,19 +170,32 @@ int sdm_forward_tuned(const void* kp, const void* qp, int in_dt, const void* v, 
     if (st != SDM_OK) return st;
     SDM_CK(cudaEventRecord(p->sel_done[b], p->sel));
     SDM_CK(cudaStreamWaitEvent(p->plan, p->sel_done[b], 0));
+    if (first) {
+      st = launch_first_writes(idx_w, win, N, W, first, p->plan);
+      if (st != SDM_OK) return st;
+      if (c == n - 1) SDM_CK(cudaEventRecord(p->writes_known, p->plan));
+    }
     if (c >= 2) SDM_CK(cudaStreamWaitEvent(p->plan, p->buf_free[b], 0));  // scan(c - 2) done
     st = launch_plan(idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, win, N, d_v, W, R, shape.pd,
-                     rec[b], dev_err, p->plan);
+                     rec[b], dev_err, p->plan, first);
     if (st != SDM_OK) return st;
     SDM_CK(cudaEventRecord(p->plan_done[b], p->plan));
     SDM_CK(cudaStreamWaitEvent(p->scan, p->plan_done[b], 0));
     if (scan_events) SDM_CK(cudaEventRecord(static_cast<cudaEvent_t>(scan_events[2 * c]), p->scan));
-    st = launch_scan_records(M, rec[b], win, N, d_v, W, R, o, shape, p->scan);
+    st = launch_scan_records(M, rec[b], win, N, d_v, W, R, o, shape, p->scan, nullptr, nullptr,
+                             M0, H);
     if (st != SDM_OK) return st;
     if (scan_events)
       SDM_CK(cudaEventRecord(static_cast<cudaEvent_t>(scan_events[2 * c + 1]), p->scan));
     SDM_CK(cudaEventRecord(p->buf_free[b], p->scan));
   }
+  if (first) {  // rows no token writes: M_0, beside the scans still running (disjoint rows)
+    SDM_CK(cudaStreamWaitEvent(p->init, p->writes_known, 0));
+    st = launch_fill_unwritten(M, M0, first, B, H, N, d_v, p->init);
+    if (st != SDM_OK) return st;
+  }
+  SDM_CK(cudaEventRecord(p->init_done, p->init));
+  SDM_CK(cudaStreamWaitEvent(s, p->init_done, 0));
   // The last plan follows every selection, and the last scan every plan.
   SDM_CK(cudaEventRecord(p->plan_end, p->plan));
   SDM_CK(cudaEventRecord(p->scan_done, p->scan));

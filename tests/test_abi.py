@@ -149,9 +149,12 @@ def test_forward_chunking_and_workspace_sizes():
     # alpha/beta block, v
     rec = 4 * 20 + 4 * 20 + 2 * 24 + 16 + 4 * 16
     assert rec == 288
-    # two record buffers of B*H*ceil(T/chunks) records, each rounded up to 256 bytes
-    assert lib.sdm_forward_workspace_size(2, 3, 100, 16, 10, 10, 4) == 2 * ((6 * 25 * rec + 255) // 256 * 256)
-    assert lib.sdm_forward_workspace_size(1, 1, 0, 16, 4, 4, 0) == 0
+    # two record buffers of B*H*ceil(T/chunks) records, each rounded up to 256 bytes, then
+    # the first-write table: one int32 per (b, h, slot), S = 12 -> N = 144
+    first = (6 * 144 * 4 + 255) // 256 * 256
+    assert lib.sdm_forward_workspace_size(2, 3, 100, 12, 16, 10, 10, 4) == \
+        2 * ((6 * 25 * rec + 255) // 256 * 256) + first
+    assert lib.sdm_forward_workspace_size(1, 1, 0, 4, 16, 4, 4, 0) == 0
 
 
 def test_projection_rejects_bad_arguments_without_launching():
