@@ -197,17 +197,19 @@ int sdm_forward(const void* kp, const void* qp, int in_dt, const void* v, int v_
                 void* stream);
 
 /* sdm_forward with the chunking chosen: `chunks` token chunks (0 = automatic, about 1024
- * tokens each; the effective count is sdm_forward_chunks(T, chunks)), and, when
+ * tokens each; the effective count is sdm_forward_chunks(T, chunks)); `lead`, the chunks
+ * the selection runs ahead before the first scan starts (0..6, -1 = automatic); and, when
  * `scan_events` is not NULL, 2 * chunks cudaEvent_t recorded right before and after each
  * chunk's scan kernel on the stream it runs on (for timing the scan kernel).  The
- * workspace must hold sdm_forward_workspace_size(..., chunks) bytes. */
+ * workspace must hold sdm_forward_workspace_size(..., chunks) bytes.  Results do not
+ * depend on chunks or lead. */
 int sdm_forward_chunks(int T, int chunks);
 int sdm_forward_tuned(const void* kp, const void* qp, int in_dt, const void* v, int v_dt,
                       const float* alpha, const float* beta, const float* M0, float* M, int B,
                       int H, int T, int S, int d_v, int W, int R, int32_t* idx_w, float* sc_w,
                       int32_t* idx_r, float* sc_r, float* o, void* workspace,
-                      size_t workspace_bytes, int* dev_err, int chunks, void* const* scan_events,
-                      void* stream);
+                      size_t workspace_bytes, int* dev_err, int chunks, int lead,
+                      void* const* scan_events, void* stream);
 
 /* Backward pass (training) of the scan, for the loss L = sum_t <dO_t, o_t> + <dM_T, M_T>
  * with the selected slots held fixed (they are discrete); gradients reach v, alpha, beta,

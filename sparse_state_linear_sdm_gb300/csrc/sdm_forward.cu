@@ -37,13 +37,16 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kAutoChunkTokens = 1024;
 constexpr int kMaxChunks = 256;
+constexpr int kMaxLead = 6;         // chunks the selection may run ahead of the first scan
+constexpr int kSelRing = kMaxLead + 2;
+constexpr int kAutoLead = 2;
 
 struct Pipeline {
   bool ready = false;
   cudaStream_t init = nullptr, sel = nullptr, plan = nullptr, scan = nullptr;
   cudaEvent_t start = nullptr, init_done = nullptr, plan_end = nullptr, scan_done = nullptr;
   cudaEvent_t writes_known = nullptr;              // every chunk's first-writes pass done
-  cudaEvent_t sel_done[2] = {nullptr, nullptr};    // selection of chunk c (c % 2) written
+  cudaEvent_t sel_done[kSelRing] = {};             // selection (and first writes) of chunk c
   cudaEvent_t plan_done[2] = {nullptr, nullptr};   // records of buffer i written
   cudaEvent_t buf_free[2] = {nullptr, nullptr};    // records of buffer i consumed
 };
@@ -65,10 +68,12 @@ int pipeline_of_current_device(Pipeline** out) {
         cudaStreamCreateWithPriority(&p.scan, cudaStreamNonBlocking, greatest) != cudaSuccess)
       return SDM_ECUDA;
     cudaEvent_t* evs[] = {&p.start,        &p.init_done,    &p.plan_end,     &p.scan_done,
-                          &p.sel_done[0],  &p.sel_done[1],  &p.plan_done[0], &p.plan_done[1],
-                          &p.buf_free[0],  &p.buf_free[1],  &p.writes_known};
+                          &p.plan_done[0], &p.plan_done[1], &p.buf_free[0],  &p.buf_free[1],
+                          &p.writes_known};
     for (cudaEvent_t* e : evs)
       if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return SDM_ECUDA;
+    for (cudaEvent_t& e : p.sel_done)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return SDM_ECUDA;
     p.ready = true;
   }
   *out = &p;
@@ -119,15 +124,15 @@ int sdm_forward_tuned(const void* kp, const void* qp, int in_dt, const void* v, 
                       const float* alpha, const float* beta, const float* M0, float* M, int B,
                       int H, int T, int S, int d_v, int W, int R, int32_t* idx_w, float* sc_w,
                       int32_t* idx_r, float* sc_r, float* o, void* workspace,
-                      size_t workspace_bytes, int* dev_err, int chunks, void* const* scan_events,
-                      void* stream) {
+                      size_t workspace_bytes, int* dev_err, int chunks, int lead,
+                      void* const* scan_events, void* stream) {
   int st = check_select_args(kp, qp, in_dt, B, H, T, S, W, R, idx_w, sc_w, idx_r, sc_r);
   if (st != SDM_OK) return st;
   const long long N = (long long)S * S;
   st = check_scan_args(M, idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, B, H, T, N, d_v, W, R,
                        o);
   if (st != SDM_OK) return st;
-  if (chunks < 0) return SDM_EINVAL;
+  if (chunks < 0 || lead < -1 || lead > kMaxLead) return SDM_EINVAL;
   if (M0 && !aligned16(M0)) return SDM_EALIGN;
   if (dev_err && (reinterpret_cast<uintptr_t>(dev_err) & 3u)) return SDM_EALIGN;
   cudaStream_t s = as_stream(stream);
@@ -159,22 +164,32 @@ int sdm_forward_tuned(const void* kp, const void* qp, int in_dt, const void* v, 
   SDM_CK(cudaStreamWaitEvent(p->plan, p->start, 0));
   SDM_CK(cudaStreamWaitEvent(p->scan, p->start, 0));
   if (first)
-    SDM_CK(cudaMemsetAsync(first, 0x7F, first_write_bytes(BH, N), p->plan));  // kNeverWritten
+    SDM_CK(cudaMemsetAsync(first, 0x7F, first_write_bytes(BH, N), p->sel));  // kNeverWritten
+  // The selection runs `ld` chunks ahead of the first scan: it is issue-bound like the scan
+  // and gets few SM slots once the scans run, so it is given a head start.
+  const int ld = lead < 0 ? kAutoLead : lead;
+  auto select_chunk = [&](int c) -> int {
+    const TokenWindow win{BH, (c + 1) * Tc <= T ? Tc : T - c * Tc, T, c * Tc};
+    int r = in_dt == SDM_BF16
+                ? launch_select_bf16(kp, qp, win, S, W, R, idx_w, sc_w, idx_r, sc_r, p->sel)
+                : launch_select_f32(kp, qp, win, S, W, R, idx_w, sc_w, idx_r, sc_r, p->sel);
+    if (r != SDM_OK) return r;
+    if (first) {
+      r = launch_first_writes(idx_w, win, N, W, first, p->sel);
+      if (r != SDM_OK) return r;
+      if (c == n - 1 && cudaEventRecord(p->writes_known, p->sel) != cudaSuccess) return SDM_ECUDA;
+    }
+    return cudaEventRecord(p->sel_done[c % kSelRing], p->sel) == cudaSuccess ? SDM_OK : SDM_ECUDA;
+  };
   // Enqueued chunk by chunk, so every wait on a reused event refers to its latest record.
+  for (int c = 0; c < n && c < ld; ++c)
+    if ((st = select_chunk(c)) != SDM_OK) return st;
   for (int c = 0; c < n; ++c) {
     const TokenWindow win{BH, (c + 1) * Tc <= T ? Tc : T - c * Tc, T, c * Tc};
     const int b = c & 1;
-    st = in_dt == SDM_BF16
-             ? launch_select_bf16(kp, qp, win, S, W, R, idx_w, sc_w, idx_r, sc_r, p->sel)
-             : launch_select_f32(kp, qp, win, S, W, R, idx_w, sc_w, idx_r, sc_r, p->sel);
-    if (st != SDM_OK) return st;
-    SDM_CK(cudaEventRecord(p->sel_done[b], p->sel));
-    SDM_CK(cudaStreamWaitEvent(p->plan, p->sel_done[b], 0));
-    if (first) {
-      st = launch_first_writes(idx_w, win, N, W, first, p->plan);
-      if (st != SDM_OK) return st;
-      if (c == n - 1) SDM_CK(cudaEventRecord(p->writes_known, p->plan));
-    }
+    if (c + ld < n && (st = select_chunk(c + ld)) != SDM_OK) return st;
+    if (c == 0) SDM_CK(cudaStreamWaitEvent(p->scan, p->sel_done[(n - 1 < ld ? n - 1 : ld) % kSelRing], 0));
+    SDM_CK(cudaStreamWaitEvent(p->plan, p->sel_done[c % kSelRing], 0));
     if (c >= 2) SDM_CK(cudaStreamWaitEvent(p->plan, p->buf_free[b], 0));  // scan(c - 2) done
     st = launch_plan(idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, win, N, d_v, W, R, shape.pd,
                      rec[b], dev_err, p->plan, first);
@@ -212,7 +227,7 @@ int sdm_forward(const void* kp, const void* qp, int in_dt, const void* v, int v_
                 void* stream) {
   return sdm_forward_tuned(kp, qp, in_dt, v, v_dt, alpha, beta, M0, M, B, H, T, S, d_v, W, R,
                            idx_w, sc_w, idx_r, sc_r, o, workspace, workspace_bytes, dev_err, 0,
-                           nullptr, stream);
+                           -1, nullptr, stream);
 }
 
 }  // extern "C"

@@ -121,15 +121,18 @@ def test_forward_rejects_bad_arguments_without_launching():
     lib = sdm.lib()
 
     def call(B=1, H=1, T=8, S=8, dv=16, W=4, R=4, in_dt=1, v_dt=0, ws=FAKE, ws_bytes=1 << 30, chunks=0,
-             M0=None, kp=FAKE, M=FAKE):
+             M0=None, kp=FAKE, M=FAKE, lead=-1):
         return lib.sdm_forward_tuned(kp, FAKE, in_dt, FAKE, v_dt, FAKE, FAKE, M0, M, B, H, T, S, dv, W, R,
-                                     FAKE, FAKE, FAKE, FAKE, FAKE, ws, ws_bytes, None, chunks, None, None)
+                                     FAKE, FAKE, FAKE, FAKE, FAKE, ws, ws_bytes, None, chunks, lead, None,
+                                     None)
 
     assert call(dv=6) == EINVAL
     assert call(in_dt=3) == EINVAL
     assert call(v_dt=3) == EINVAL
     assert call(W=65) == EINVAL                 # more slots than N = S * S = 64
     assert call(chunks=-1) == EINVAL
+    assert call(lead=-2) == EINVAL
+    assert call(lead=7) == EINVAL
     assert call(S=5000) == EUNSUPPORTED
     assert call(kp=ODD) == EALIGN
     assert call(M=ODD) == EALIGN
