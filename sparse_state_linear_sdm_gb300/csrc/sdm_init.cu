@@ -45,31 +45,34 @@ __global__ void __launch_bounds__(256) first_writes_kernel(const int32_t* __rest
   }
 }
 
-// One warp per (head, 32 consecutive rows): for every sequence b, the rows whose first-write
-// entry says "never" get M_0's row (the M_0 rows are re-read from cache across b).
+// One warp per (head h, row x): lane l reads the first-write entry of sequence b = l (32
+// sequences per round), a ballot gives the sequences whose row x was never written, and the
+// M_0 row, loaded once, is stored into each of them.  Consecutive warps take consecutive
+// rows, so the entries of neighbouring rows share sectors in L2.
 __global__ void __launch_bounds__(256) fill_unwritten_kernel(float* __restrict__ M,
                                                              const float* __restrict__ M0,
                                                              const int32_t* __restrict__ first,
                                                              int B, int H, long long N, int d_v) {
   const int lane = threadIdx.x & 31;
-  const long long groups = (N + 31) / 32;
-  const long long items = groups * H;
+  const long long items = (long long)H * N;
   const long long warps = (long long)gridDim.x * (blockDim.x / 32);
   const int q4 = d_v / 4;
   for (long long it = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); it < items;
        it += warps) {
-    const int h = int(it / groups);
-    const long long x0 = (it - (long long)h * groups) * 32;
-    const float4* src = reinterpret_cast<const float4*>(M0 + (size_t(h) * N + x0) * d_v);
-    for (int b = 0; b < B; ++b) {
-      const size_t bh = size_t(b) * H + h;
-      const bool mine = x0 + lane < N && first[bh * N + x0 + lane] == kNeverWritten;
-      unsigned need = __ballot_sync(0xFFFFFFFFu, mine);
-      float4* dst = reinterpret_cast<float4*>(M + (bh * N + x0) * d_v);
-      while (need) {
-        const int r = __ffs(need) - 1;
-        need &= need - 1;
-        for (int k = lane; k < q4; k += 32) __stcs(dst + size_t(r) * q4 + k, src[size_t(r) * q4 + k]);
+    const int h = int(it / N);
+    const long long x = it - (long long)h * N;
+    const float4* src = reinterpret_cast<const float4*>(M0 + size_t(it) * d_v);
+    for (int b0 = 0; b0 < B; b0 += 32) {
+      const int b = b0 + lane;
+      const bool mine = b < B && first[(size_t(b) * H + h) * size_t(N) + size_t(x)] == kNeverWritten;
+      const unsigned need = __ballot_sync(0xFFFFFFFFu, mine);
+      if (!need) continue;
+      for (int k = lane; k < q4; k += 32) {
+        const float4 val = __ldg(src + k);
+        for (unsigned m = need; m; m &= m - 1) {
+          const size_t bh = size_t(b0 + __ffs(m) - 1) * H + h;
+          __stcs(reinterpret_cast<float4*>(M + (bh * size_t(N) + size_t(x)) * d_v) + k, val);
+        }
       }
     }
   }
@@ -108,8 +111,8 @@ int launch_fill_unwritten(float* M, const float* M0, const int32_t* first_write,
                            cudaFuncAttributePreferredSharedMemoryCarveout,
                            int(cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
     return SDM_ECUDA;
-  const long long items = (N + 31) / 32 * H;
-  long long blocks = (long long)sms * 2;
+  const long long items = (long long)H * N;
+  long long blocks = (long long)sms * 8;
   if (blocks > (items + 7) / 8) blocks = (items + 7) / 8;
   fill_unwritten_kernel<<<unsigned(blocks), 256, 0, s>>>(M, M0, first_write, B, H, N, d_v);
   return last_launch_status();
