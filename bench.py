@@ -48,8 +48,6 @@ def parse_args():
     ap.add_argument("--cols", type=int, default=0, help="force scan columns per block (0 = auto)")
     ap.add_argument("--pd", type=int, default=0, help="force scan prefetch depth (0 = auto; one-stream step only)")
     ap.add_argument("--chunks", type=int, default=0, help="token chunks of the pipelined forward (0 = auto)")
-    ap.add_argument("--lead", type=int, default=-1,
-                    help="chunks the selection runs ahead of the first scan in the pipelined forward (-1 = auto)")
     ap.add_argument("--pipeline", choices=["on", "off"], default="on",
                     help="on: sdm_forward (selection of chunk c+1 overlaps the scan of chunk c); "
                          "off: init || select, then plan and scan, one kernel after the other")
@@ -246,7 +244,7 @@ def make_state(cfg, rank, dev, torch, sdm, wl):
                  torch.empty(sh + (cfg.R,), dtype=torch.float32, device=dev))
     st["o"] = torch.empty(sh + (cfg.d_v,), dtype=torch.float32, device=dev)
     st["ws"] = sdm.scan_workspace(cfg.B, cfg.H, cfg.T, cfg.d_v, cfg.W, cfg.R, dev)
-    st["fws"] = sdm.forward_workspace(cfg.B, cfg.H, cfg.T, cfg.S, cfg.d_v, cfg.W, cfg.R, dev, 0)
+    st["fws"] = sdm.forward_workspace(cfg.B, cfg.H, cfg.T, cfg.d_v, cfg.W, cfg.R, dev, 0)
     st["err"] = torch.zeros(1, dtype=torch.int32, device=dev)
     st["side"] = sdm.side_stream(dev)  # high priority: init shares the SMs with the selection
     return st
@@ -258,13 +256,12 @@ def run_forward(st, cfg, sdm, args, inp=None, o=None, scan_ev=None):
     scan_ev: 2 * chunks timing events recorded around each chunk's scan kernel."""
     inp = st if inp is None else inp
     o = st["o"] if o is None else o
-    if st["fws"].numel() < sdm.lib().sdm_forward_workspace_size(cfg.B, cfg.H, cfg.T, cfg.S, cfg.d_v, cfg.W, cfg.R,
+    if st["fws"].numel() < sdm.lib().sdm_forward_workspace_size(cfg.B, cfg.H, cfg.T, cfg.d_v, cfg.W, cfg.R,
                                                                  args.chunks):
-        st["fws"] = sdm.forward_workspace(cfg.B, cfg.H, cfg.T, cfg.S, cfg.d_v, cfg.W, cfg.R, st["M"].device,
-                                          args.chunks)
+        st["fws"] = sdm.forward_workspace(cfg.B, cfg.H, cfg.T, cfg.d_v, cfg.W, cfg.R, st["M"].device, args.chunks)
     sdm.forward(inp["kp"], inp["qp"], inp["v"], inp["alpha"], inp["beta"], st["M0"], cfg.W, cfg.R, M=st["M"],
                 workspace=st["fws"], dev_err=st["err"], out=st["sel"], o=o, chunks=args.chunks,
-                scan_events=scan_ev, lead=args.lead)
+                scan_events=scan_ev)
 
 
 def run_step(st, cfg, sdm, args, ev=None, before_select=None, inp=None, o=None):
@@ -449,12 +446,10 @@ def run_ours(args):
         units_launch = units_rank / chunks
         phase = {"scan_ms_per_launch": scan_launch_ms, "scan_ms_per_step": scan_launch_ms * chunks,
                  "chunks": chunks, "tokens_per_chunk": -(-cfg.T // chunks),
-                 "overlap": "sdm_forward: select (+ first writes) runs `lead` chunks ahead, plan of chunk c "
-                            "|| scan of chunk c-1 (high-priority stream) gathering not-yet-written rows from M0; "
-                            "M0 into the never-written rows beside the last scans",
-                 "lead": args.lead}
+                 "overlap": "sdm_forward: init (high-priority stream) || select+plan of chunk c+1 "
+                            "(select stream) || scan of chunk c (high-priority stream)"}
         phase["alone"] = one_stream_breakdown(st, cfg, sdm, args, torch, dev)
-        launches_per_step = 1 + 4 * chunks   # per chunk select, first writes, plan, scan; one fill
+        launches_per_step = 1 + 3 * chunks
     else:
         scan_launch_ms = sum(e[3].elapsed_time(e[4]) for e in kern_ev) / K
         units_launch = units_rank

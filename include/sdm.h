@@ -173,12 +173,8 @@ int sdm_scan_launch_info(int B, int H, int d_v, int W, int R, int* cols_per_cta,
  *   M      [B, H, N, d_v] fp32, out: state after token T-1.
  *   idx_w, sc_w [B, H, T, W]; idx_r, sc_r [B, H, T, R]; o [B, H, T, d_v] fp32: written,
  *          as by sdm_select and sdm_scan_forward.
- *   workspace  device scratch of at least sdm_forward_workspace_size(B, H, T, S, d_v, W, R,
- *          0) bytes, 16-byte aligned, contents irrelevant: two chunks of planning records
- *          and a table of B*H*N int32 (each slot's first writing token).
- * Starting from M_0, the state is not copied up front: gathers of rows that no earlier
- * token wrote read M_0 directly, and M_0 is copied at the end into the rows no token
- * writes, so M ends up exactly as after sdm_init_state_from_M0 and the scan.
+ *   workspace  device scratch of at least sdm_forward_workspace_size(B, H, T, d_v, W, R, 0)
+ *          bytes, 16-byte aligned, contents irrelevant.
  *   dev_err  device int or NULL, as for sdm_scan_forward.
  * Ordering: work enqueued on `stream` before the call runs before any of the call's work,
  * and work enqueued on `stream` after the call sees all of its results.  The library
@@ -188,8 +184,7 @@ int sdm_scan_launch_info(int B, int H, int d_v, int W, int R, int* cols_per_cta,
  * Errors: the argument checks of sdm_select and sdm_scan_forward (nothing enqueued);
  * SDM_ENOSPACE for a short workspace; SDM_ECUDA if a launch fails part-way, after
  * which M and the outputs are unspecified. */
-size_t sdm_forward_workspace_size(int B, int H, int T, int S, int d_v, int W, int R,
-                                  int chunks);
+size_t sdm_forward_workspace_size(int B, int H, int T, int d_v, int W, int R, int chunks);
 int sdm_forward(const void* kp, const void* qp, int in_dt, const void* v, int v_dt,
                 const float* alpha, const float* beta, const float* M0, float* M, int B, int H,
                 int T, int S, int d_v, int W, int R, int32_t* idx_w, float* sc_w, int32_t* idx_r,
@@ -197,19 +192,17 @@ int sdm_forward(const void* kp, const void* qp, int in_dt, const void* v, int v_
                 void* stream);
 
 /* sdm_forward with the chunking chosen: `chunks` token chunks (0 = automatic, about 1024
- * tokens each; the effective count is sdm_forward_chunks(T, chunks)); `lead`, the chunks
- * the selection runs ahead before the first scan starts (0..6, -1 = automatic); and, when
+ * tokens each; the effective count is sdm_forward_chunks(T, chunks)), and, when
  * `scan_events` is not NULL, 2 * chunks cudaEvent_t recorded right before and after each
  * chunk's scan kernel on the stream it runs on (for timing the scan kernel).  The
- * workspace must hold sdm_forward_workspace_size(..., chunks) bytes.  Results do not
- * depend on chunks or lead. */
+ * workspace must hold sdm_forward_workspace_size(..., chunks) bytes. */
 int sdm_forward_chunks(int T, int chunks);
 int sdm_forward_tuned(const void* kp, const void* qp, int in_dt, const void* v, int v_dt,
                       const float* alpha, const float* beta, const float* M0, float* M, int B,
                       int H, int T, int S, int d_v, int W, int R, int32_t* idx_w, float* sc_w,
                       int32_t* idx_r, float* sc_r, float* o, void* workspace,
-                      size_t workspace_bytes, int* dev_err, int chunks, int lead,
-                      void* const* scan_events, void* stream);
+                      size_t workspace_bytes, int* dev_err, int chunks, void* const* scan_events,
+                      void* stream);
 
 /* Backward pass (training) of the scan, for the loss L = sum_t <dO_t, o_t> + <dM_T, M_T>
  * with the selected slots held fixed (they are discrete); gradients reach v, alpha, beta,

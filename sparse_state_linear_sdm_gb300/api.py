@@ -51,11 +51,11 @@ def lib() -> ctypes.CDLL:
             L.sdm_scan_launch_info.argtypes = [i, i, i, i, i, p, p, p, p]
             L.sdm_gen_inputs.argtypes = [ull, i, i, i, i, i, ll, i, i, i, f, i, p, p, p, p, p, p, p]
             L.sdm_gen_M0.argtypes = [ull, i, ll, i, f, p, p]
-            L.sdm_forward_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
+            L.sdm_forward_workspace_size.argtypes = [i, i, i, i, i, i, i]
             L.sdm_forward_workspace_size.restype = sz
             L.sdm_forward_chunks.argtypes = [i, i]
             L.sdm_forward_tuned.argtypes = [p, p, i, p, i, p, p, p, p, i, i, i, i, i, i, i, p, p, p, p, p, p,
-                                            sz, p, i, i, p, p]
+                                            sz, p, i, p, p]
             L.sdm_forward.argtypes = [p, p, i, p, i, p, p, p, p, i, i, i, i, i, i, i, p, p, p, p, p, p, sz, p, p]
             L.sdm_scan_forward_train.argtypes = [p, p, p, p, p, p, i, p, p, i, i, i, ll, i, i, i, p, p, p, p, sz, p, p]
             L.sdm_scan_backward_workspace_size.argtypes = [i, i, i, i, i, i]
@@ -296,22 +296,19 @@ def forward_chunks(T: int, chunks: int = 0) -> int:
     return lib().sdm_forward_chunks(T, chunks)
 
 
-def forward_workspace(B: int, H: int, T: int, S: int, d_v: int, W: int, R: int, device,
-                      chunks: int = 0) -> torch.Tensor:
-    """Scratch for forward(): two chunks of planning records and the first-write table."""
-    n = lib().sdm_forward_workspace_size(B, H, T, S, d_v, W, R, chunks)
+def forward_workspace(B: int, H: int, T: int, d_v: int, W: int, R: int, device, chunks: int = 0) -> torch.Tensor:
+    n = lib().sdm_forward_workspace_size(B, H, T, d_v, W, R, chunks)
     return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
 
 
 def forward(kp, qp, v, alpha, beta, M0, W: int, R: int, M=None, workspace=None, dev_err=None,
-            overlap: bool = True, out=None, o=None, chunks: int = 0, scan_events=None, lead: int = -1):
+            overlap: bool = True, out=None, o=None, chunks: int = 0, scan_events=None):
     """One SDM forward pass over a batch: state from M0 (or, with M0=None, from the state
     already in M), selection, scan.  Returns (o, M, (idx_w, sc_w, idx_r, sc_r)).
 
     overlap=True runs sdm_forward: the selection of token chunk c+1 overlaps the scan of
     chunk c on the library's own streams (chunks=0: automatic).  overlap=False runs the
     three steps one after the other on the current stream.  Both give the same bits.
-    lead: token chunks the selection runs ahead before the first scan (-1: automatic).
     scan_events: optional list of 2 * forward_chunks(T, chunks) torch.cuda.Event, recorded
     around each chunk's scan kernel."""
     B, H, T, _, S = kp.shape
@@ -347,7 +344,7 @@ def forward(kp, qp, v, alpha, beta, M0, W: int, R: int, M=None, workspace=None, 
         o = torch.empty((B, H, T, dv), dtype=torch.float32, device=M.device)
     _need(o, "o", torch.float32, (B, H, T, dv))
     if workspace is None:
-        workspace = forward_workspace(B, H, T, S, dv, W, R, M.device, chunks)
+        workspace = forward_workspace(B, H, T, dv, W, R, M.device, chunks)
     _need(workspace, "workspace", torch.uint8)
     if dev_err is not None:
         _need(dev_err, "dev_err", torch.int32)
@@ -361,7 +358,7 @@ def forward(kp, qp, v, alpha, beta, M0, W: int, R: int, M=None, workspace=None, 
         ev_arr = (ctypes.c_void_p * len(scan_events))(*[e.cuda_event for e in scan_events])
     _call("sdm_forward_tuned", _p(kp), _p(qp), _dtype_code(kp), _p(v), _dtype_code(v), _p(alpha), _p(beta),
           _p(M0), _p(M), B, H, T, S, dv, W, R, _p(idx_w), _p(sc_w), _p(idx_r), _p(sc_r), _p(o),
-          _p(workspace), workspace.numel(), _p(dev_err), int(chunks), int(lead), ev_arr, _stream(M.device))
+          _p(workspace), workspace.numel(), _p(dev_err), int(chunks), ev_arr, _stream(M.device))
     return o, M, out
 
 

@@ -60,16 +60,10 @@ inline int check_scan_args(const float* M, const int32_t* idx_w, const float* sc
 //   int32 slot[WRa]     write slots then read slots (W + R entries used)
 //   fp32  weight[WRa]   softmax of the write scores, then of the read scores
 //   int16 src[WRb]      where the row comes from: -1 = the table in HBM,
-//                       -2 = invalid slot (skipped), -3 (kSrcInitial) = M_0 (a row no
-//                       earlier token wrote, in a pass that starts from M_0 without
-//                       copying it), d*W + p = row p of the write set of token t-d
-//                       (0 <= d <= prefetch depth)
+//                       -2 = invalid slot (skipped), d*W + p = row p of the write
+//                       set of token t-d (0 <= d <= prefetch depth)
 //   fp32  alpha, beta, pad, pad
 //   fp32  v[d_v]
-constexpr int kSrcInitial = -3;
-// First-write table entry of a slot no token has written (memset byte 0x7F).
-constexpr int32_t kNeverWritten = 0x7F7F7F7F;
-
 struct RecLayout {
   int WR, WRa, WRb;
   int off_wts, off_src, off_ab, off_v, bytes;
@@ -133,20 +127,10 @@ int launch_select_f32(const void* kp, const void* qp, const TokenWindow& win, in
 
 // Planning pass of the scan (one record per (b, h, t) of the window into `rec`); `pd` must
 // be the prefetch depth of the scan kernel that consumes the records.
-// first_write (optional, [BH, N], see launch_first_writes): rows no earlier token wrote get
-// source kSrcInitial (gathered from M_0 by the scan).
 int launch_plan(const int32_t* idx_w, const float* sc_w, const int32_t* idx_r, const float* sc_r,
                 const void* v, int v_dt, const float* alpha, const float* beta,
                 const TokenWindow& win, long long N, int d_v, int W, int R, int pd, void* rec,
-                int* dev_err, cudaStream_t s, const int32_t* first_write = nullptr);
-// first_write[bh, x] = min(first_write[bh, x], t) over the window's write slots x of token
-// t (token index in the sequence); entries start at kNeverWritten.  Slots outside [0, N)
-// are skipped (the planning pass reports them).
-int launch_first_writes(const int32_t* idx_w, const TokenWindow& win, long long N, int W,
-                        int32_t* first_write, cudaStream_t s);
-// M[b, h, x] = M_0[h, x] for every row with first_write[b*H + h, x] == kNeverWritten.
-int launch_fill_unwritten(float* M, const float* M0, const int32_t* first_write, int B, int H,
-                          long long N, int d_v, cudaStream_t s);
+                int* dev_err, cudaStream_t s);
 
 struct ScanShape {
   int cols;      // d_v columns per thread block
@@ -161,11 +145,9 @@ int choose_scan_shape(int BH, int d_v, int W, int R, int force_cols, int force_p
 // same shape.pd); continues from the state in M.
 // w_prev / r_rows (optional, [BH, T_total, W or R, d_v]): every write row before its update
 // and every read row as read, for the backward pass.
-// M0 / H (optional): rows with source kSrcInitial are gathered from M0[bh % H].
 int launch_scan_records(float* M, const void* rec, const TokenWindow& win, long long N, int d_v,
                         int W, int R, float* o, const ScanShape& shape, cudaStream_t s,
-                        float* w_prev = nullptr, float* r_rows = nullptr,
-                        const float* M0 = nullptr, int H = 1);
+                        float* w_prev = nullptr, float* r_rows = nullptr);
 // Planning pass, then (after waiting for wait_before_scan, if any, and recording
 // after_plan, if any) the scan kernel.
 int launch_scan(float* M, const int32_t* idx_w, const float* sc_w, const int32_t* idx_r,

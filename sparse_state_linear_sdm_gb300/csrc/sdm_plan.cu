@@ -5,9 +5,6 @@
 // selected slot it finds whether a token at most `pd` steps earlier (or the same token,
 // for a read slot) wrote that slot, and where in that token's write set, so that the
 // sequential scan can take the freshly written row from shared memory instead of HBM.
-// With a first-write table (the pipelined pass started from M_0 without copying it), a slot
-// that no earlier token has written gets source code kSrcInitial: the scan gathers that row
-// from M_0 instead of M.
 // It also forms both softmaxes (write weights k_t^(i), read weights) and packs slots,
 // weights, sources, alpha, beta and v into one 16-byte-aligned record per token (layout
 // in sdm_internal.cuh).
@@ -59,7 +56,6 @@ struct PlanArgs {
   RecLayout L;
   unsigned char* rec;
   int* dev_err;
-  const int32_t* first_write;  // optional [BH, N]: first token (of the sequence) writing each slot
 };
 
 // Shared memory of one planning block: hash table, filter, then the chunk's write slots
@@ -124,7 +120,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
         x = 0;
         errs |= SDM_DEV_INDEX_RANGE;
       } else {
-        bool seen = false;  // an earlier writer of x among the tokens in the table
         const uint32_t fb = filter_bit(x);
         if ((filter[fb >> 5] >> (fb & 31)) & 1u) {
           int best_t = -1, best_p = 0;
@@ -135,19 +130,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
             const int tt = tl + int((v >> 16) & 0xFFFFu), pp = int(v & 0xFFFFu);
             if (e < W && tt == u && pp != e) errs |= SDM_DEV_DUP_WRITE;
             const bool earlier = e < W ? tt < u : tt <= u;
-            seen |= earlier;
             if (earlier && tt >= u - a.pd && tt > best_t) {
               best_t = tt;
               best_p = pp;
             }
           }
           if (best_t >= 0) code = (u - best_t) * W + best_p;
-        }
-        // A row no token before this one has written still holds M_0: gather it from M_0.
-        if (code == -1 && !seen && a.first_write) {
-          const int f = a.first_write[size_t(bh) * size_t(a.N) + size_t(x)];
-          const int ug = a.t_off + u;
-          if (e < W ? f >= ug : f > ug) code = kSrcInitial;
         }
       }
       reinterpret_cast<int32_t*>(rec)[e] = x;
@@ -182,7 +170,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
 int launch_plan(const int32_t* idx_w, const float* sc_w, const int32_t* idx_r, const float* sc_r,
                 const void* v, int v_dt, const float* alpha, const float* beta,
                 const TokenWindow& win, long long N, int d_v, int W, int R, int pd, void* rec,
-                int* dev_err, cudaStream_t s, const int32_t* first_write) {
+                int* dev_err, cudaStream_t s) {
   const int T = win.Tc, BH = win.BH;
   if (T == 0 || BH == 0) return SDM_OK;
   PlanArgs pa;
@@ -216,7 +204,6 @@ int launch_plan(const int32_t* idx_w, const float* sc_w, const int32_t* idx_r, c
   pa.L = rec_layout(W, R, d_v);
   pa.rec = static_cast<unsigned char*>(rec);
   pa.dev_err = dev_err;
-  pa.first_write = first_write;
   const dim3 grid((T + tc - 1) / tc, BH);
   const int smem = int(plan_smem_bytes(pa.log2cap, tc, pd, W, R));
   const void* fn = v_dt == SDM_BF16 ? reinterpret_cast<const void*>(&plan_kernel<uint16_t>)

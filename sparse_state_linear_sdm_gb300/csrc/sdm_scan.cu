@@ -51,8 +51,6 @@ struct ScanArgs {
   RecLayout L;
   float* w_prev;  // optional [BH, T_total, W, d_v]: each write row before its update
   float* r_rows;  // optional [BH, T_total, R, d_v]: each read row as read (after the write)
-  const float* M0;  // optional [H, N, d_v]: rows with source kSrcInitial come from M0[bh % H]
-  int H;
 };
 
 __device__ __forceinline__ float4 f4_add(float4 a, float4 b) {
@@ -80,7 +78,6 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   const int c0 = (blockIdx.x - bh * slices) * C;
   const unsigned char* recs = a.rec + size_t(bh) * T * L.bytes;
   float* Mbh = a.M + size_t(bh) * size_t(a.N) * d_v + c0;
-  const float* M0h = a.M0 ? a.M0 + size_t(bh % a.H) * size_t(a.N) * d_v + c0 : Mbh;
   float* obh = a.o + (size_t(bh) * a.T_total + a.t_off) * d_v + c0;
   float* wsave = a.w_prev ? a.w_prev + (size_t(bh) * a.T_total + a.t_off) * W * d_v + c0 : nullptr;
   float* rsave = a.r_rows ? a.r_rows + (size_t(bh) * a.T_total + a.t_off) * R * d_v + c0 : nullptr;
@@ -108,12 +105,9 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
     uint32_t sdst = static_cast<uint32_t>(
         __cvta_generic_to_shared(rows + size_t(u % QR) * WR * C + (tid / LPR) * C + 4 * c4));
     const float* gcol = Mbh + 4 * c4;
-    const float* g0col = M0h + 4 * c4;
 #pragma unroll 4
     for (int e = tid / LPR; e < WR; e += RPP, sdst += RPP * C * 4) {
-      const int code = src[e];
-      if (code == -1 || code == kSrcInitial)
-        cp_async16_s(sdst, (code == -1 ? gcol : g0col) + size_t(idx[e]) * d_v);
+      if (src[e] == -1) cp_async16_s(sdst, gcol + size_t(idx[e]) * d_v);
     }
   };
 
@@ -279,7 +273,7 @@ int choose_scan_shape(int BH, int d_v, int W, int R, int force_cols, int force_p
 
 int launch_scan_records(float* M, const void* rec, const TokenWindow& win, long long N, int d_v,
                         int W, int R, float* o, const ScanShape& shape, cudaStream_t s,
-                        float* w_prev, float* r_rows, const float* M0, int H) {
+                        float* w_prev, float* r_rows) {
   if (win.Tc == 0 || win.BH == 0) return SDM_OK;
   ScanArgs sa;
   sa.M = M;
@@ -295,8 +289,6 @@ int launch_scan_records(float* M, const void* rec, const TokenWindow& win, long 
   sa.L = rec_layout(W, R, d_v);
   sa.w_prev = w_prev;
   sa.r_rows = r_rows;
-  sa.M0 = M0;
-  sa.H = H > 0 ? H : 1;
   ScanFn fn = scan_fn(shape.cols, shape.pd);
   if (!fn) return SDM_EUNSUPPORTED;
   if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),

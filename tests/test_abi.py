@@ -121,18 +121,15 @@ def test_forward_rejects_bad_arguments_without_launching():
     lib = sdm.lib()
 
     def call(B=1, H=1, T=8, S=8, dv=16, W=4, R=4, in_dt=1, v_dt=0, ws=FAKE, ws_bytes=1 << 30, chunks=0,
-             M0=None, kp=FAKE, M=FAKE, lead=-1):
+             M0=None, kp=FAKE, M=FAKE):
         return lib.sdm_forward_tuned(kp, FAKE, in_dt, FAKE, v_dt, FAKE, FAKE, M0, M, B, H, T, S, dv, W, R,
-                                     FAKE, FAKE, FAKE, FAKE, FAKE, ws, ws_bytes, None, chunks, lead, None,
-                                     None)
+                                     FAKE, FAKE, FAKE, FAKE, FAKE, ws, ws_bytes, None, chunks, None, None)
 
     assert call(dv=6) == EINVAL
     assert call(in_dt=3) == EINVAL
     assert call(v_dt=3) == EINVAL
     assert call(W=65) == EINVAL                 # more slots than N = S * S = 64
     assert call(chunks=-1) == EINVAL
-    assert call(lead=-2) == EINVAL
-    assert call(lead=7) == EINVAL
     assert call(S=5000) == EUNSUPPORTED
     assert call(kp=ODD) == EALIGN
     assert call(M=ODD) == EALIGN
@@ -152,12 +149,9 @@ def test_forward_chunking_and_workspace_sizes():
     # alpha/beta block, v
     rec = 4 * 20 + 4 * 20 + 2 * 24 + 16 + 4 * 16
     assert rec == 288
-    # two record buffers of B*H*ceil(T/chunks) records, each rounded up to 256 bytes, then
-    # the first-write table: one int32 per (b, h, slot), S = 12 -> N = 144
-    first = (6 * 144 * 4 + 255) // 256 * 256
-    assert lib.sdm_forward_workspace_size(2, 3, 100, 12, 16, 10, 10, 4) == \
-        2 * ((6 * 25 * rec + 255) // 256 * 256) + first
-    assert lib.sdm_forward_workspace_size(1, 1, 0, 4, 16, 4, 4, 0) == 0
+    # two record buffers of B*H*ceil(T/chunks) records, each rounded up to 256 bytes
+    assert lib.sdm_forward_workspace_size(2, 3, 100, 16, 10, 10, 4) == 2 * ((6 * 25 * rec + 255) // 256 * 256)
+    assert lib.sdm_forward_workspace_size(1, 1, 0, 16, 4, 4, 0) == 0
 
 
 def test_projection_rejects_bad_arguments_without_launching():

@@ -110,21 +110,19 @@ def test_pipelined_forward_matches_the_oracle_on_a_small_case():
 
 
 @pytest.mark.parametrize("B,H,T,S,dv,W,R,chunks", [
-    (2, 2, 1, 32, 16, 2, 8, 0),       # one token: almost every row only gets M_0 at the end
-    (1, 3, 3, 32, 8, 2, 16, 2),       # reads of rows a later token writes first (gathered from M_0)
+    (2, 2, 1, 32, 16, 2, 8, 0),       # one token: almost every row keeps M_0
+    (1, 3, 3, 32, 8, 2, 16, 2),       # rows read before any token writes them
     (2, 1, 50, 8, 16, 4, 16, 3),      # N = 64: rows written, read, rewritten across chunks
     (1, 2, 257, 16, 32, 32, 32, 5),   # most rows written somewhere, ragged last chunk
 ])
 def test_pipelined_forward_from_M0_writes_every_row(B, H, T, S, dv, W, R, chunks):
-    """Starting from M_0 the pipelined pass never copies M_0 up front: rows are gathered from
-    M_0 until first written, and M_0 is copied into the rows no token writes at the end.  M
-    starts as NaN and the workspace as garbage, so a row that neither the scan nor the final
-    copy writes, or a gather from the wrong table, shows up."""
+    """M starts as NaN and the workspace as garbage: every row of the result must come from
+    M_0 or from the scan, exactly as on the one-stream path."""
     rng = np.random.default_rng(T * 13 + S)
     d, M0 = _random(rng, B, H, T, S, dv, torch.float32)
     ref = _run(d, M0, W, R, overlap=False)
     M = torch.full((B, H, S * S, dv), float("nan"), device="cuda")
-    ws = sdm.forward_workspace(B, H, T, S, dv, W, R, "cuda", chunks)
+    ws = sdm.forward_workspace(B, H, T, dv, W, R, "cuda", chunks)
     ws.copy_(torch.randint(0, 256, ws.shape, dtype=torch.uint8, device="cuda"))
     got = _run(d, M0, W, R, chunks=chunks, M=M, workspace=ws)
     _assert_same(got, ref, (B, H, T, S, chunks))
