@@ -251,6 +251,19 @@ int sdm_scan_backward(const int32_t* idx_w, const float* sc_w, const int32_t* id
 int sdm_select_backward(const int32_t* idx, const float* dsc, int B, int H, int T, int S, int K,
                         float* dhalves, void* stream);
 
+/* sdm_decode_step - one decode token (T = 1) for every (b, h), in a single kernel: the
+ * selection of sdm_select, then the gated delta write and the read of sdm_scan_forward,
+ * with the state resident in M ("Meccanismo Core" items 2-4 applied to one token).
+ * Arguments as for sdm_select and sdm_scan_forward with T = 1 (kp, qp [B, H, 1, 2, S];
+ * v [B, H, 1, d_v]; alpha, beta [B, H, 1]; idx/sc [B, H, 1, W or R]; o [B, H, 1, d_v]);
+ * no workspace.  Every output (slots, scores, o, M) is bit-identical to sdm_select followed
+ * by sdm_scan_forward over the same token.  Requires d_v % 32 == 0 (SDM_EUNSUPPORTED
+ * otherwise, and when the block's shared memory does not fit). */
+int sdm_decode_step(const void* kp, const void* qp, int in_dt, const void* v, int v_dt,
+                    const float* alpha, const float* beta, float* M, int B, int H, int S, int d_v,
+                    int W, int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r,
+                    float* o, int* dev_err, void* stream);
+
 /* sdm_project_kq - the projections that produce the product keys and queries
  * ("Meccanismo Core" item 2: the projected key k' and query q', whose two halves are the
  * sub-scores; "Design IsoFLOP": the projections are linear layers).  One bf16 GEMM on the

@@ -63,6 +63,7 @@ def lib() -> ctypes.CDLL:
             L.sdm_scan_backward.argtypes = [p, p, p, p, p, i, p, p, p, p, p, i, i, i, ll, i, i, i, p, p, p, p, p, p,
                                             p, p, sz, p]
             L.sdm_select_backward.argtypes = [p, p, i, i, i, i, i, p, p]
+            L.sdm_decode_step.argtypes = [p, p, i, p, i, p, p, p, i, i, i, i, i, i, p, p, p, p, p, p, p]
             L.sdm_project_kq_tuned.argtypes = [p, p, i, i, i, i, i, p, p, p, i, i, p]
             for name in ("sdm_init_state_from_M0", "sdm_select", "sdm_scan_forward",
                          "sdm_scan_forward_tuned", "sdm_scan_launch_info", "sdm_gen_inputs", "sdm_gen_M0",
@@ -449,9 +450,38 @@ def project_kq(x, w, H: int, S: int, out=None, dev_err=None, max_ctas: int = 0, 
     return kp, qp
 
 
+def decode_step(kp, qp, v, alpha, beta, M, W: int, R: int, out=None, o=None, dev_err=None):
+    """One decode token (T = 1) for every (b, h) in a single kernel: selection, planning and
+    the gated write and read on M (in place).  kp, qp [B, H, 1, 2, S]; v [B, H, 1, d_v];
+    alpha, beta [B, H, 1]; M [B, H, S*S, d_v] fp32.  Returns (o, (idx_w, sc_w, idx_r, sc_r)),
+    bit-identical to select() followed by scan_forward() on the same token."""
+    _need(kp, "kp")
+    B, H, T, two, S = kp.shape
+    if T != 1 or two != 2:
+        raise ValueError("kp must be [B, H, 1, 2, S]")
+    _need(qp, "qp", kp.dtype, tuple(kp.shape))
+    dv = v.shape[-1]
+    _need(v, "v", None, (B, H, 1, dv))
+    _need(alpha, "alpha", torch.float32, (B, H, 1))
+    _need(beta, "beta", torch.float32, (B, H, 1))
+    _need(M, "M", torch.float32, (B, H, S * S, dv))
+    if out is None:
+        dev = kp.device
+        out = (torch.empty((B, H, 1, W), dtype=torch.int32, device=dev), torch.empty((B, H, 1, W), device=dev),
+               torch.empty((B, H, 1, R), dtype=torch.int32, device=dev), torch.empty((B, H, 1, R), device=dev))
+    if o is None:
+        o = torch.empty((B, H, 1, dv), dtype=torch.float32, device=M.device)
+    _need(o, "o", torch.float32, (B, H, 1, dv))
+    _call("sdm_decode_step", _p(kp), _p(qp), _dtype_code(kp), _p(v), _dtype_code(v), _p(alpha), _p(beta),
+          _p(M), B, H, S, dv, W, R, _p(out[0]), _p(out[1]), _p(out[2]), _p(out[3]), _p(o),
+          _p(dev_err) if dev_err is not None else None, _stream(M.device))
+    return o, out
+
+
 class DecodeStep:
     """One-token decode step for a batch of sequences with resident state, captured once
-    into a CUDA graph (selection, planning and scan kernels) and replayed per token.
+    into a CUDA graph and replayed per token: the single-kernel decode_step when d_v is a
+    multiple of 32 (fused=True), else the selection, planning and scan kernels.
 
     The state M [B, H, N, d_v] stays in place across steps; each step takes k', q' halves
     [B, H, 1, 2, S], v [B, H, 1, d_v] and alpha, beta [B, H, 1] (copied into the graph's
@@ -459,8 +489,9 @@ class DecodeStep:
     copy it before the next step if it must be kept).  Chaining steps gives exactly the
     result of one scan over the same tokens."""
 
-    def __init__(self, M, W: int, R: int, in_dtype=torch.bfloat16, S=None):
+    def __init__(self, M, W: int, R: int, in_dtype=torch.bfloat16, S=None, fused=None):
         B, H, N, dv = M.shape
+        self.fused = (dv % 32 == 0) if fused is None else bool(fused)
         S = int(round(N ** 0.5)) if S is None else S
         if S * S != N:
             raise ValueError("N must be a square")
@@ -481,6 +512,10 @@ class DecodeStep:
         self.graph = None
 
     def _body(self):
+        if self.fused:
+            decode_step(self.kp, self.qp, self.v, self.alpha, self.beta, self.M, self.W, self.R,
+                        out=self.sel, o=self.o, dev_err=self.err)
+            return
         select(self.kp, self.qp, self.W, self.R, out=self.sel)
         scan_forward(self.M, *self.sel, self.v, self.alpha, self.beta, o=self.o, workspace=self.ws,
                      dev_err=self.err)
@@ -502,6 +537,8 @@ class DecodeStep:
             sel = select(kp, kp, self.W, self.R)
             Md = torch.zeros((B, H, s * s, dv), dtype=torch.float32, device=dev)
             scan_forward(Md, *sel, self.v, self.alpha, self.beta)
+            if self.fused:
+                decode_step(kp, kp, self.v, self.alpha, self.beta, Md, self.W, self.R)
         torch.cuda.current_stream(dev).wait_stream(side)
         torch.cuda.synchronize(dev)
         self.graph = torch.cuda.CUDAGraph()

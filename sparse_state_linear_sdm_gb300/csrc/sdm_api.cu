@@ -40,6 +40,21 @@ int sdm_select(const void* kp, const void* qp, int in_dt, int B, int H, int T, i
                                  sc_r, as_stream(stream));
 }
 
+int sdm_decode_step(const void* kp, const void* qp, int in_dt, const void* v, int v_dt,
+                    const float* alpha, const float* beta, float* M, int B, int H, int S, int d_v,
+                    int W, int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r,
+                    float* o, int* dev_err, void* stream) {
+  int st = check_select_args(kp, qp, in_dt, B, H, 1, S, W, R, idx_w, sc_w, idx_r, sc_r);
+  if (st != SDM_OK) return st;
+  const long long N = (long long)S * S;
+  st = check_scan_args(M, idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, B, H, 1, N, d_v, W, R,
+                       o);
+  if (st != SDM_OK) return st;
+  if (dev_err && (reinterpret_cast<uintptr_t>(dev_err) & 3u)) return SDM_EALIGN;
+  return launch_decode(kp, qp, in_dt, v, v_dt, alpha, beta, M, B * H, S, d_v, W, R, idx_w, sc_w,
+                       idx_r, sc_r, o, dev_err, as_stream(stream));
+}
+
 int sdm_project_kq_tuned(const void* x, const void* w, int B, int T, int D, int H, int S,
                          void* kp, void* qp, int* dev_err, int max_ctas, int pair, void* stream) {
   if (B < 1 || T < 1 || H < 1 || S < 1 || D < 8 || D % 8 || max_ctas < 0 || pair < -1 || pair > 2)

@@ -157,6 +157,12 @@ int launch_scan(float* M, const int32_t* idx_w, const float* sc_w, const int32_t
                 cudaEvent_t wait_before_scan, cudaStream_t s, float* w_prev = nullptr,
                 float* r_rows = nullptr);
 
+// One decode token (T = 1) of every (b, h) in one kernel: selection, planning and scan.
+// SDM_EUNSUPPORTED if d_v % 32 != 0 or the shared memory does not fit.
+int launch_decode(const void* kp, const void* qp, int in_dt, const void* v, int v_dt,
+                  const float* alpha, const float* beta, float* M, int BH, int S, int d_v, int W,
+                  int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, float* o,
+                  int* dev_err, cudaStream_t s);
 int launch_project(const void* x, const void* w, int B, int T, int D, int H, int S, void* kp,
                    void* qp, int* dev_err, int max_ctas, int pair, cudaStream_t s);
 int launch_gen_inputs(unsigned long long seed, int B, int H, int T, int b_off, int t_off,

@@ -530,40 +530,55 @@ __device__ __noinline__ void outer_full_grid(const float* aval, const float* bva
   collect_at_least(grid_key, kin * kin, tau2, out, kpad);
 }
 
+// Shared memory of a selecting block: the two staircases, then one region per warp.
+struct SelectSmem {
+  uint32_t* stair_w;
+  uint32_t* stair_r;
+  unsigned char* wbase;
+  size_t per_warp;  // bytes of one warp's region (16-byte multiple)
+};
+
+__device__ __forceinline__ SelectSmem select_smem(const SelectArgs& a, unsigned char* smem) {
+  SelectSmem m;
+  m.stair_w = reinterpret_cast<uint32_t*>(smem);
+  m.stair_r = m.stair_w + a.cnt_w;
+  m.wbase = smem + (size_t(a.cnt_w + a.cnt_r) * 4 + 15) / 16 * 16;
+  const size_t per_warp = a.keys_bytes + size_t(a.kpad) * 8 + 256 * 4 + size_t(a.kin_max) * 16;
+  m.per_warp = (per_warp + 15) / 16 * 16;
+  return m;
+}
+
+// Both staircases, built by every thread of the block (ends with a block barrier).  Warp 0's
+// histogram is free until its first task: scratch for the staircase scans.
+__device__ __forceinline__ void select_build_stairs(const SelectArgs& a, const SelectSmem& m) {
+  int* tmp = reinterpret_cast<int*>(m.wbase + a.keys_bytes + size_t(a.kpad) * 8);
+  build_stair(m.stair_w, a.W, min(a.W, a.S), tmp);
+  build_stair(m.stair_r, a.R, min(a.R, a.S), tmp);
+}
+
+// Selection tasks [task0, task1) (task = 2 * item + which, which 0: k' / top-W, 1: q' /
+// top-R) by one warp (PAIR false) or by the warp pair `unit` (PAIR true: warps 2*unit and
+// 2*unit + 1 of the block, one half each, joined by named barrier 1 + unit).
 template <typename Tin, int EMAX, bool PAIR>
-__global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
+__device__ void select_tasks(const SelectArgs& a, const SelectSmem& m, long long task0,
+                             long long task1) {
   using IKey = typename InnerKeyOf<Tin>::type;
-  extern __shared__ __align__(16) unsigned char smem[];
-  uint32_t* stair_w = reinterpret_cast<uint32_t*>(smem);
-  uint32_t* stair_r = stair_w + a.cnt_w;
-  unsigned char* wbase = smem + (size_t(a.cnt_w + a.cnt_r) * 4 + 15) / 16 * 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = a.S;
-  const size_t per_warp = a.keys_bytes + size_t(a.kpad) * 8 + 256 * 4 + size_t(a.kin_max) * 16;
-  unsigned char* wp = wbase + (per_warp + 15) / 16 * 16 * warp;
+  unsigned char* wp = m.wbase + m.per_warp * warp;
   unsigned char* keys = wp;
   uint64_t* out = reinterpret_cast<uint64_t*>(wp + a.keys_bytes);
   uint32_t* hist = reinterpret_cast<uint32_t*>(out + a.kpad);
   // Pair mode: warps 2u and 2u+1 share a task; the inner lists live in warp 2u's region.
   const int role = PAIR ? (warp & 1) : 0;
   const int unit = PAIR ? (warp >> 1) : warp;
-  unsigned char* lp = PAIR ? wbase + (per_warp + 15) / 16 * 16 * (warp & ~1) : wp;
+  unsigned char* lp = PAIR ? m.wbase + m.per_warp * (warp & ~1) : wp;
   float* aval = reinterpret_cast<float*>(lp + a.keys_bytes + size_t(a.kpad) * 8 + 256 * 4);
   float* bval = aval + a.kin_max;
   int32_t* aidx = reinterpret_cast<int32_t*>(bval + a.kin_max);
   int32_t* bidx = aidx + a.kin_max;
-
-  // Warp 0's histogram is free until its first task: scratch for the staircase scans.
-  int* tmp = reinterpret_cast<int*>(wbase + a.keys_bytes + size_t(a.kpad) * 8);
-  build_stair(stair_w, a.W, min(a.W, S), tmp);
-  build_stair(stair_r, a.R, min(a.R, S), tmp);
-
-  // A short run of consecutive tasks per warp (no persistent grid): blocks that start
-  // late, e.g. behind a kernel on another stream, do not hold up the others.
-  const long long tasks = a.items * 2;
-  const int units = PAIR ? a.warps / 2 : a.warps;
-  const long long task0 = ((long long)blockIdx.x * units + unit) * a.tpw;
-  const long long task1 = task0 + a.tpw < tasks ? task0 + a.tpw : tasks;
+  const uint32_t* stair_w = m.stair_w;
+  const uint32_t* stair_r = m.stair_r;
   for (long long task = task0; task < task1; ++task) {
     const int which = int(task & 1);
     // (b, h, t) triple in the full [B, H, T_total] arrays
@@ -667,6 +682,60 @@ __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
     __syncwarp();
     if (PAIR) asm volatile("bar.sync %0, 64;" ::"r"(1 + unit) : "memory");  // lists free again
   }
+}
+
+template <typename Tin, int EMAX, bool PAIR>
+__global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const SelectSmem m = select_smem(a, smem);
+  select_build_stairs(a, m);
+  // A short run of consecutive tasks per warp (no persistent grid): blocks that start
+  // late, e.g. behind a kernel on another stream, do not hold up the others.
+  const long long tasks = a.items * 2;
+  const int warp = threadIdx.x >> 5;
+  const int unit = PAIR ? (warp >> 1) : warp;
+  const int units = PAIR ? a.warps / 2 : a.warps;
+  const long long task0 = ((long long)blockIdx.x * units + unit) * a.tpw;
+  const long long task1 = task0 + a.tpw < tasks ? task0 + a.tpw : tasks;
+  select_tasks<Tin, EMAX, PAIR>(a, m, task0, task1);
+}
+
+// Arguments and shared-memory sizes of a selection over a token window (warps, tpw and
+// the launch shape are left to the caller).  stair_bytes: both staircases; per_warp: one
+// warp's region.
+template <typename Tin>
+void select_args(const void* kp, const void* qp, const TokenWindow& win, int S, int W, int R,
+                 int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, SelectArgs* out,
+                 size_t* stair_bytes, size_t* per_warp_bytes) {
+  constexpr bool kBf16 = sizeof(Tin) == 2;
+  SelectArgs a;
+  a.kp = kp;
+  a.qp = qp;
+  a.items = (long long)win.BH * win.Tc;
+  a.Tc = win.Tc;
+  a.T_total = win.T_total;
+  a.t0 = win.t0;
+  a.S = S;
+  a.W = W;
+  a.R = R;
+  a.kin_max = max(min(W, S), min(R, S));
+  const int kmax = max(W, R);
+  a.kpad = 32;
+  while (a.kpad < kmax) a.kpad <<= 1;
+  a.cnt_w = stair_count(W, min(W, S));
+  a.cnt_r = stair_count(R, min(R, S));
+  a.idx_w = idx_w;
+  a.sc_w = sc_w;
+  a.idx_r = idx_r;
+  a.sc_r = sc_r;
+  const int ikb = kBf16 ? 4 : 8;
+  a.keys_bytes = select_key_bytes(a.kpad, S, max(a.cnt_w, a.cnt_r), ikb);
+  a.vec = (S * int(sizeof(Tin))) % 16 == 0;
+  a.warps = 0;
+  a.tpw = 1;
+  *stair_bytes = (size_t(a.cnt_w + a.cnt_r) * 4 + 15) / 16 * 16;
+  *per_warp_bytes = select_per_warp_bytes(a.kpad, a.kin_max, S, max(a.cnt_w, a.cnt_r), ikb);
+  *out = a;
 }
 
 template <typename Tin>

@@ -39,3 +39,67 @@ def test_decode_steps_equal_one_scan(graph):
     ref = oracle_heads(cfg, host_heads(cfg, heads, 0, T))
     for k, (b, h) in enumerate(heads):
         assert scaled_err(torch.cat(outs, dim=2)[b, h].cpu().numpy(), ref["o"][k]) <= TOL
+
+
+def _token(rng, B, H, S, dv, dt):
+    f = lambda *sh: torch.from_numpy(rng.standard_normal(sh).astype(np.float32)).cuda()
+    return dict(kp=f(B, H, 1, 2, S).to(dt), qp=f(B, H, 1, 2, S).to(dt), v=f(B, H, 1, dv).to(dt),
+                alpha=torch.from_numpy(rng.uniform(0.8, 1.0, (B, H, 1)).astype(np.float32)).cuda(),
+                beta=torch.from_numpy(rng.uniform(0.0, 1.0, (B, H, 1)).astype(np.float32)).cuda())
+
+
+@pytest.mark.parametrize("B,H,S,dv,W,R,dt,steps", [
+    (2, 3, 32, 32, 16, 16, torch.bfloat16, 5),    # one 32-column slice
+    (1, 2, 64, 128, 128, 128, torch.bfloat16, 3),  # the default widths
+    (2, 1, 8, 64, 40, 64, torch.float32, 6),      # K > S; W = R = N: every row read is also written
+    (1, 1, 24, 96, 200, 150, torch.bfloat16, 2),  # K > 128 (wide sort variant); 3 slices
+    (3, 2, 16, 32, 8, 3, torch.float32, 4),
+])
+def test_fused_decode_equals_select_then_scan(B, H, S, dv, W, R, dt, steps):
+    """sdm_decode_step (one kernel) against sdm_select + sdm_scan_forward on the same token,
+    chained over several tokens: slots, scores, o and M bit for bit."""
+    rng = np.random.default_rng(B * 100 + S + dv + W)
+    M0 = torch.from_numpy((0.3 * rng.standard_normal((B, H, S * S, dv))).astype(np.float32)).cuda()
+    M1, M2 = M0.clone(), M0.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(steps):
+        x = _token(rng, B, H, S, dv, dt)
+        o1, sel1 = sdm.decode_step(x["kp"], x["qp"], x["v"], x["alpha"], x["beta"], M1, W, R, dev_err=err)
+        sel2 = sdm.select(x["kp"], x["qp"], W, R)
+        o2 = sdm.scan_forward(M2, *sel2, x["v"], x["alpha"], x["beta"])
+        torch.cuda.synchronize()
+        for a, b in zip(sel1, sel2):
+            assert torch.equal(a, b)
+        assert torch.equal(o1, o2)
+        assert torch.equal(M1, M2)
+    assert err.item() == 0
+
+
+def test_decode_step_graph_uses_one_kernel_and_matches_the_unfused_step():
+    cfg = wl.CONFIGS[1]
+    T = 6
+    d = device_inputs(cfg, T=T)
+    M0 = device_M0(cfg)
+    Ma = torch.empty((cfg.B, cfg.H, cfg.N, cfg.d_v), device="cuda")
+    sdm.init_state_from_M0(Ma, M0)
+    Mb = Ma.clone()
+    fused = sdm.DecodeStep(Ma, cfg.W, cfg.R, in_dtype=torch.bfloat16).capture()
+    plain = sdm.DecodeStep(Mb, cfg.W, cfg.R, in_dtype=torch.bfloat16, fused=False).capture()
+    assert fused.fused and not plain.fused
+    for t in range(T):
+        args = [d[k][:, :, t:t + 1] for k in ("kp", "qp", "v", "alpha", "beta")]
+        oa = fused(*args).clone()
+        ob = plain(*args).clone()
+        assert torch.equal(oa, ob)
+    torch.cuda.synchronize()
+    assert torch.equal(Ma, Mb)
+
+
+def test_decode_step_needs_whole_32_column_slices():
+    rng = np.random.default_rng(3)
+    x = _token(rng, 1, 1, 8, 24, torch.float32)
+    M = torch.zeros((1, 1, 64, 24), device="cuda")
+    with pytest.raises(sdm.SDMError):
+        sdm.decode_step(x["kp"], x["qp"], x["v"], x["alpha"], x["beta"], M, 4, 4)
+    step = sdm.DecodeStep(M, 4, 4, in_dtype=torch.float32)
+    assert not step.fused   # d_v = 24: the selection, planning and scan kernels
