@@ -257,12 +257,15 @@ int sdm_select_backward(const int32_t* idx, const float* dsc, int B, int H, int 
  * Arguments as for sdm_select and sdm_scan_forward with T = 1 (kp, qp [B, H, 1, 2, S];
  * v [B, H, 1, d_v]; alpha, beta [B, H, 1]; idx/sc [B, H, 1, W or R]; o [B, H, 1, d_v]);
  * no workspace.  Every output (slots, scores, o, M) is bit-identical to sdm_select followed
- * by sdm_scan_forward over the same token.  Requires d_v % 32 == 0 (SDM_EUNSUPPORTED
- * otherwise, and when the block's shared memory does not fit). */
+ * by sdm_scan_forward over the same token: a block covers the column slice the scan
+ * kernel would use for these sizes, so the read is summed in the same order.
+ * SDM_EUNSUPPORTED when the block's shared memory would not fit (very large W + R or S);
+ * sdm_decode_step_supported answers that on the host (SDM_OK or SDM_EUNSUPPORTED). */
 int sdm_decode_step(const void* kp, const void* qp, int in_dt, const void* v, int v_dt,
                     const float* alpha, const float* beta, float* M, int B, int H, int S, int d_v,
                     int W, int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r,
                     float* o, int* dev_err, void* stream);
+int sdm_decode_step_supported(int in_dt, int B, int H, int S, int d_v, int W, int R);
 
 /* sdm_project_kq - the projections that produce the product keys and queries
  * ("Meccanismo Core" item 2: the projected key k' and query q', whose two halves are the

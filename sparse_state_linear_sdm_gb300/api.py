@@ -64,6 +64,7 @@ def lib() -> ctypes.CDLL:
                                             p, p, sz, p]
             L.sdm_select_backward.argtypes = [p, p, i, i, i, i, i, p, p]
             L.sdm_decode_step.argtypes = [p, p, i, p, i, p, p, p, i, i, i, i, i, i, p, p, p, p, p, p, p]
+            L.sdm_decode_step_supported.argtypes = [i, i, i, i, i, i, i]
             L.sdm_project_kq_tuned.argtypes = [p, p, i, i, i, i, i, p, p, p, i, i, p]
             for name in ("sdm_init_state_from_M0", "sdm_select", "sdm_scan_forward",
                          "sdm_scan_forward_tuned", "sdm_scan_launch_info", "sdm_gen_inputs", "sdm_gen_M0",
@@ -480,8 +481,8 @@ def decode_step(kp, qp, v, alpha, beta, M, W: int, R: int, out=None, o=None, dev
 
 class DecodeStep:
     """One-token decode step for a batch of sequences with resident state, captured once
-    into a CUDA graph and replayed per token: the single-kernel decode_step when d_v is a
-    multiple of 32 (fused=True), else the selection, planning and scan kernels.
+    into a CUDA graph and replayed per token: the single-kernel decode_step (fused=True, the
+    default where its shared memory fits), else the selection, planning and scan kernels.
 
     The state M [B, H, N, d_v] stays in place across steps; each step takes k', q' halves
     [B, H, 1, 2, S], v [B, H, 1, d_v] and alpha, beta [B, H, 1] (copied into the graph's
@@ -491,8 +492,12 @@ class DecodeStep:
 
     def __init__(self, M, W: int, R: int, in_dtype=torch.bfloat16, S=None, fused=None):
         B, H, N, dv = M.shape
-        self.fused = (dv % 32 == 0) if fused is None else bool(fused)
         S = int(round(N ** 0.5)) if S is None else S
+        if fused is None:
+            code = SDM_BF16 if in_dtype == torch.bfloat16 else SDM_F32
+            with torch.cuda.device(M.device):
+                fused = lib().sdm_decode_step_supported(code, B, H, S, dv, W, R) == 0
+        self.fused = bool(fused)
         if S * S != N:
             raise ValueError("N must be a square")
         dev = M.device

@@ -55,6 +55,14 @@ int sdm_decode_step(const void* kp, const void* qp, int in_dt, const void* v, in
                        idx_r, sc_r, o, dev_err, as_stream(stream));
 }
 
+int sdm_decode_step_supported(int in_dt, int B, int H, int S, int d_v, int W, int R) {
+  if (bad_dtype(in_dt) || B < 1 || H < 1 || S < 1 || S > SDM_MAX_S || d_v < 4 || d_v % 4 ||
+      W < 1 || R < 1 || W > SDM_MAX_K || R > SDM_MAX_K || 1LL * W > 1LL * S * S ||
+      1LL * R > 1LL * S * S)
+    return SDM_EINVAL;
+  return decode_supported(in_dt, B * H, S, d_v, W, R);
+}
+
 int sdm_project_kq_tuned(const void* x, const void* w, int B, int T, int D, int H, int S,
                          void* kp, void* qp, int* dev_err, int max_ctas, int pair, void* stream) {
   if (B < 1 || T < 1 || H < 1 || S < 1 || D < 8 || D % 8 || max_ctas < 0 || pair < -1 || pair > 2)

@@ -14,19 +14,18 @@
 //      same warp routine as the planning kernel), the source of every row (HBM, or the
 //      updated row of the token's own write set for a read slot it also writes), and the
 //      device error checks.
-//   3. the scan of the token on the block's 32 columns with the scan kernel's thread
-//      mapping and arithmetic: gather, forget gate and delta update, write-back,
-//      forwarding, weighted read reduced in the same order.
+//   3. the scan of the token on the block's columns with the scan kernel's thread mapping
+//      and arithmetic: gather, forget gate and delta update, write-back, forwarding,
+//      weighted read reduced in the same order.  The column width of a block is the one
+//      the scan kernel would use for these sizes (choose_scan_shape), so the read's sum
+//      runs in the same order too.
 // So every output is bit-identical to the three-kernel path.
 #include "sdm_select_impl.cuh"
 
 namespace sdm {
 namespace {
 
-constexpr int kDecCols = 32;                   // columns of d_v per block
 constexpr int kDecThreads = 256;
-constexpr int kDecLPR = kDecCols / 4;           // threads per row slice (one float4 each)
-constexpr int kDecRPP = kDecThreads / kDecLPR;  // row slices per pass of the block
 constexpr int kDecWarps = kDecThreads / 32;
 
 struct DecodeArgs {
@@ -38,14 +37,15 @@ struct DecodeArgs {
   float* o;
   long long N;
   int d_v, W, R, slices;
+  int cols;  // columns of d_v per block (4 .. 64), as the scan kernel's shape
   size_t sel_smem;  // bytes of the selection's shared memory
   int* dev_err;
 };
 
-__host__ __device__ inline size_t decode_scan_smem(int W, int R) {
+__host__ __device__ inline size_t decode_scan_smem(int W, int R, int C) {
   const int WR = W + R, WRa = (WR + 3) & ~3;
-  return size_t(WR) * kDecCols * 4 + size_t(WRa) * 4 /* weights */ + size_t(WRa) * 4 /* slots */ +
-         size_t(WRa) * 2 /* sources */ + 16 + size_t(kDecWarps) * kDecCols * 4 /* reduction */;
+  return size_t(WR) * C * 4 + size_t(WRa) * 4 /* weights */ + size_t(WRa) * 4 /* slots */ +
+         size_t(WRa) * 2 /* sources */ + 16 + size_t(kDecWarps) * C * 4 /* reduction */;
 }
 
 template <typename Tv>
@@ -71,8 +71,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs d) {
   extern __shared__ __align__(16) unsigned char smem[];
   const SelectArgs& a = d.sel;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int C = d.cols, LPR = C / 4, RPP = kDecThreads / LPR;
   const int bh = blockIdx.x / d.slices;
-  const int c0 = (blockIdx.x - bh * d.slices) * kDecCols;
+  const int c0 = (blockIdx.x - bh * d.slices) * C;
   const int W = d.W, R = d.R, WR = W + R, d_v = d.d_v;
 
   // ---- 1. selection of token (bh, 0) -------------------------------------------------
@@ -88,19 +89,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs d) {
 
   // ---- 2. planning of the token (shared memory reused) --------------------------------
   const int WRa = (WR + 3) & ~3;
-  float* rows = reinterpret_cast<float*>(smem);        // [WR][kDecCols]
-  float* wts = rows + size_t(WR) * kDecCols;           // [WRa]
+  float* rows = reinterpret_cast<float*>(smem);        // [WR][C]
+  float* wts = rows + size_t(WR) * C;                  // [WRa]
   int32_t* idx = reinterpret_cast<int32_t*>(wts + WRa);  // [WRa]
   int16_t* src = reinterpret_cast<int16_t*>(idx + WRa);  // [WRa]
   float* red = reinterpret_cast<float*>(
-      smem + ((size_t(WR) * kDecCols * 4 + size_t(WRa) * 10 + 15) / 16 * 16));  // [warps][C]
+      smem + ((size_t(WR) * C * 4 + size_t(WRa) * 10 + 15) / 16 * 16));  // [warps][C]
   const int32_t* gw = a.idx_w + size_t(bh) * W;
   const int32_t* gr = a.idx_r + size_t(bh) * R;
   for (int e = tid; e < WR; e += kDecThreads) idx[e] = e < W ? gw[e] : gr[e - W];
   if (warp == 0) warp_softmax(a.sc_w + size_t(bh) * W, W, wts);
   if (warp == 1) warp_softmax(a.sc_r + size_t(bh) * R, R, wts + W);
   const float alpha = d.alpha[bh], beta = d.beta[bh];
-  const int c4 = tid % kDecLPR;
+  const int c4 = tid % LPR;
   const Tv* vsrc = static_cast<const Tv*>(d.v) + size_t(bh) * d_v + c0 + 4 * c4;
   const float4 vv = make_float4(v_at<Tv>(vsrc, 0), v_at<Tv>(vsrc, 1), v_at<Tv>(vsrc, 2),
                                 v_at<Tv>(vsrc, 3));
@@ -127,17 +128,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs d) {
   if (errs && d.dev_err) atomicOr(d.dev_err, errs);
   __syncthreads();
 
-  // ---- 3. the token's scan on columns c0 .. c0+31 -------------------------------------
+  // ---- 3. the token's scan on columns c0 .. c0+C-1 -------------------------------------
   float* Mbh = d.M + size_t(bh) * size_t(d.N) * d_v + c0;
-  for (int e = tid / kDecLPR; e < WR; e += kDecRPP)
-    if (src[e] == -1) cp16(rows + e * kDecCols + 4 * c4, Mbh + size_t(idx[e]) * d_v + 4 * c4);
+  for (int e = tid / LPR; e < WR; e += RPP)
+    if (src[e] == -1) cp16(rows + e * C + 4 * c4, Mbh + size_t(idx[e]) * d_v + 4 * c4);
   asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
   __syncthreads();
 
   // Forget gate and delta update of the W write rows (in shared memory and in HBM).
-  for (int e = tid / kDecLPR; e < W; e += kDecRPP) {
+  for (int e = tid / LPR; e < W; e += RPP) {
     if (src[e] == -2) continue;
-    float4* cell = reinterpret_cast<float4*>(rows + e * kDecCols) + c4;
+    float4* cell = reinterpret_cast<float4*>(rows + e * C) + c4;
     const float4 m = *cell;
     const float kb = beta * wts[e];
     float4 r;
@@ -155,43 +156,65 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs d) {
   for (int e = W + tid; e < WR; e += kDecThreads) {
     const int code = src[e];
     if (code >= 0 && code < W) {
-      const float4* from = reinterpret_cast<const float4*>(rows + code * kDecCols);
-      float4* to = reinterpret_cast<float4*>(rows + e * kDecCols);
-#pragma unroll
-      for (int q = 0; q < kDecLPR; ++q) to[q] = from[q];
+      const float4* from = reinterpret_cast<const float4*>(rows + code * C);
+      float4* to = reinterpret_cast<float4*>(rows + e * C);
+      for (int q = 0; q < LPR; ++q) to[q] = from[q];
     }
   }
   __syncthreads();
 
   // Weighted read of the R read rows (after the write), reduced in the scan kernel's order.
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int e = tid / kDecLPR; e < R; e += kDecRPP) {
+  for (int e = tid / LPR; e < R; e += RPP) {
     if (src[W + e] == -2) continue;
     const float r = wts[W + e];
-    const float4 m = reinterpret_cast<const float4*>(rows + (W + e) * kDecCols)[c4];
+    const float4 m = reinterpret_cast<const float4*>(rows + (W + e) * C)[c4];
     acc.x = fmaf(r, m.x, acc.x);
     acc.y = fmaf(r, m.y, acc.y);
     acc.z = fmaf(r, m.z, acc.z);
     acc.w = fmaf(r, m.w, acc.w);
   }
-#pragma unroll
-  for (int off = kDecLPR; off < 32; off <<= 1) {
+  for (int off = LPR; off < 32; off <<= 1) {
     acc.x += __shfl_xor_sync(0xFFFFFFFFu, acc.x, off);
     acc.y += __shfl_xor_sync(0xFFFFFFFFu, acc.y, off);
     acc.z += __shfl_xor_sync(0xFFFFFFFFu, acc.z, off);
     acc.w += __shfl_xor_sync(0xFFFFFFFFu, acc.w, off);
   }
-  if (lane < kDecLPR) reinterpret_cast<float4*>(red + warp * kDecCols)[lane] = acc;
+  if (lane < LPR) reinterpret_cast<float4*>(red + warp * C)[lane] = acc;
   __syncthreads();
-  if (tid < kDecLPR) {
+  if (tid < LPR) {
     float4 s = reinterpret_cast<const float4*>(red)[tid];
 #pragma unroll
     for (int w = 1; w < kDecWarps; ++w) {
-      const float4 t = reinterpret_cast<const float4*>(red + w * kDecCols)[tid];
+      const float4 t = reinterpret_cast<const float4*>(red + w * C)[tid];
       s = make_float4(s.x + t.x, s.y + t.y, s.z + t.z, s.w + t.w);
     }
     *(reinterpret_cast<float4*>(d.o + size_t(bh) * d_v + c0) + tid) = s;
   }
+}
+
+// Launch shape of the decode kernel: column width (the scan kernel's), blocks, shared memory.
+template <typename Tin>
+int decode_shape(int BH, int S, int d_v, int W, int R, SelectArgs* sel, int* cols, size_t* smem,
+                 size_t* sel_smem) {
+  ScanShape shape;
+  const int st = choose_scan_shape(BH, d_v, W, R, 0, 0, &shape);
+  if (st != SDM_OK) return st;
+  if (shape.cols < 4 || shape.cols > 64 || d_v % shape.cols != 0) return SDM_EUNSUPPORTED;
+  size_t stair_bytes = 0, per_warp = 0;
+  select_args<Tin>(nullptr, nullptr, whole_sequences(BH, 1), S, W, R, nullptr, nullptr, nullptr,
+                   nullptr, sel, &stair_bytes, &per_warp);
+  sel->warps = 4;
+  *cols = shape.cols;
+  *sel_smem = stair_bytes + 4 * per_warp;
+  *smem = *sel_smem;
+  const size_t scan_smem = decode_scan_smem(W, R, shape.cols);
+  if (scan_smem > *smem) *smem = scan_smem;
+  int dev = 0, max_smem = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return SDM_ECUDA;
+  return *smem > size_t(max_smem) ? SDM_EUNSUPPORTED : SDM_OK;
 }
 
 template <typename Tin>
@@ -199,12 +222,17 @@ int launch_decode_t(const void* kp, const void* qp, const void* v, int v_dt, con
                     const float* beta, float* M, int BH, int S, int d_v, int W, int R,
                     int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, float* o,
                     int* dev_err, cudaStream_t s) {
-  if (d_v % kDecCols != 0) return SDM_EUNSUPPORTED;
   DecodeArgs dargs;
-  size_t stair_bytes = 0, per_warp = 0;
-  select_args<Tin>(kp, qp, whole_sequences(BH, 1), S, W, R, idx_w, sc_w, idx_r, sc_r, &dargs.sel,
-                   &stair_bytes, &per_warp);
-  dargs.sel.warps = 4;
+  int cols = 0;
+  size_t smem = 0;
+  const int st = decode_shape<Tin>(BH, S, d_v, W, R, &dargs.sel, &cols, &smem, &dargs.sel_smem);
+  if (st != SDM_OK) return st;
+  dargs.sel.kp = kp;
+  dargs.sel.qp = qp;
+  dargs.sel.idx_w = idx_w;
+  dargs.sel.sc_w = sc_w;
+  dargs.sel.idx_r = idx_r;
+  dargs.sel.sc_r = sc_r;
   dargs.v = v;
   dargs.alpha = alpha;
   dargs.beta = beta;
@@ -214,17 +242,9 @@ int launch_decode_t(const void* kp, const void* qp, const void* v, int v_dt, con
   dargs.d_v = d_v;
   dargs.W = W;
   dargs.R = R;
-  dargs.slices = d_v / kDecCols;
-  dargs.sel_smem = stair_bytes + 4 * per_warp;
+  dargs.cols = cols;
+  dargs.slices = d_v / cols;
   dargs.dev_err = dev_err;
-  size_t smem = dargs.sel_smem;
-  const size_t scan_smem = decode_scan_smem(W, R);
-  if (scan_smem > smem) smem = scan_smem;
-  int dev = 0, max_smem = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-    return SDM_ECUDA;
-  if (smem > size_t(max_smem)) return SDM_EUNSUPPORTED;
   const bool big = W > 128 || R > 128;
   const void* fn;
   if (v_dt == SDM_BF16)
@@ -256,6 +276,14 @@ int launch_decode(const void* kp, const void* qp, int in_dt, const void* v, int 
                                          sc_w, idx_r, sc_r, o, dev_err, s)
              : launch_decode_t<float>(kp, qp, v, v_dt, alpha, beta, M, BH, S, d_v, W, R, idx_w,
                                       sc_w, idx_r, sc_r, o, dev_err, s);
+}
+
+int decode_supported(int in_dt, int BH, int S, int d_v, int W, int R) {
+  SelectArgs sel;
+  int cols = 0;
+  size_t smem = 0, sel_smem = 0;
+  return in_dt == SDM_BF16 ? decode_shape<uint16_t>(BH, S, d_v, W, R, &sel, &cols, &smem, &sel_smem)
+                           : decode_shape<float>(BH, S, d_v, W, R, &sel, &cols, &smem, &sel_smem);
 }
 
 }  // namespace sdm

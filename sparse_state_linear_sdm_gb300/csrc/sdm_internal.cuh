@@ -158,7 +158,8 @@ int launch_scan(float* M, const int32_t* idx_w, const float* sc_w, const int32_t
                 float* r_rows = nullptr);
 
 // One decode token (T = 1) of every (b, h) in one kernel: selection, planning and scan.
-// SDM_EUNSUPPORTED if d_v % 32 != 0 or the shared memory does not fit.
+// SDM_EUNSUPPORTED if its shared memory does not fit (decode_supported: the same check).
+int decode_supported(int in_dt, int BH, int S, int d_v, int W, int R);
 int launch_decode(const void* kp, const void* qp, int in_dt, const void* v, int v_dt,
                   const float* alpha, const float* beta, float* M, int BH, int S, int d_v, int W,
                   int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, float* o,

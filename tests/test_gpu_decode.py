@@ -95,11 +95,17 @@ def test_decode_step_graph_uses_one_kernel_and_matches_the_unfused_step():
     assert torch.equal(Ma, Mb)
 
 
-def test_decode_step_needs_whole_32_column_slices():
+def test_decode_step_column_slices_follow_the_scan_shape():
+    """d_v = 24: the scan kernel takes 4-column slices here, and so does the decode kernel."""
     rng = np.random.default_rng(3)
-    x = _token(rng, 1, 1, 8, 24, torch.float32)
-    M = torch.zeros((1, 1, 64, 24), device="cuda")
-    with pytest.raises(sdm.SDMError):
-        sdm.decode_step(x["kp"], x["qp"], x["v"], x["alpha"], x["beta"], M, 4, 4)
-    step = sdm.DecodeStep(M, 4, 4, in_dtype=torch.float32)
-    assert not step.fused   # d_v = 24: the selection, planning and scan kernels
+    M1 = torch.from_numpy(rng.standard_normal((1, 1, 64, 24)).astype(np.float32)).cuda()
+    M2 = M1.clone()
+    for _ in range(3):
+        x = _token(rng, 1, 1, 8, 24, torch.float32)
+        o1, s1 = sdm.decode_step(x["kp"], x["qp"], x["v"], x["alpha"], x["beta"], M1, 4, 4)
+        s2 = sdm.select(x["kp"], x["qp"], 4, 4)
+        o2 = sdm.scan_forward(M2, *s2, x["v"], x["alpha"], x["beta"])
+        torch.cuda.synchronize()
+        assert all(torch.equal(a, b) for a, b in zip(s1, s2))
+        assert torch.equal(o1, o2) and torch.equal(M1, M2)
+    assert sdm.DecodeStep(M1, 4, 4, in_dtype=torch.float32).fused
