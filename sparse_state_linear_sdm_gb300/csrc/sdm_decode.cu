@@ -66,7 +66,231 @@ __device__ __forceinline__ void cp16(float* dst, const float* src) {
                : "memory");
 }
 
-template <typename Tin, typename Tv, int EMAX>
+// ---- latency-oriented selection for one token: a team of 4 warps per task -----------
+//
+// The selection kernel gives a task one warp (or two), which suits throughput; for a single
+// token the task's latency is what counts.  Here a task gets a team of 128 threads (64 per
+// half for the inner lists): radix passes over 8-bit digits narrow the candidates (each
+// pass: histogram, the bucket holding the k-th key, compaction), and once at most 64 are
+// left they are ranked against each other; the selected keys are put in order by rank.
+// The keys are the selection kernel's (distinct: value or sum, then index or flat), so the
+// top-k sets and their order are unique and the results are bit-identical.
+
+__device__ __forceinline__ void team_bar(int bar, int nth) {
+  asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(nth) : "memory");
+}
+
+template <typename Key>
+__device__ __forceinline__ int count_greater(const Key* a, int n, Key k) {
+  int c = 0;
+  for (int j = 0; j < n; ++j) c += a[j] > k ? 1 : 0;
+  return c;
+}
+
+// The `need` largest of the n distinct keys in a[] into sel[0..need), in no order; a and b
+// (n entries each) are overwritten.  `bits`: key width (multiple of 8).  hist: 256
+// counters, ctr: 4 ints, both team-private.  Team thread t of nth (whole warps), barrier bar.
+template <typename Key>
+__device__ void team_topk(Key* a, Key* b, int n, int need, int bits, Key* sel, uint32_t* hist,
+                          int* ctr, int t, int nth, int bar) {
+  int shift = bits - 8, nsel = 0, left = need;
+  if (t == 0) ctr[0] = 0;
+  for (;;) {
+    if (n <= left) {  // every candidate is in
+      for (int i = t; i < n; i += nth) sel[nsel + i] = a[i];
+      team_bar(bar, nth);
+      return;
+    }
+    if (n <= 64 || shift < 0) {  // rank the few candidates left
+      for (int i = t; i < n; i += nth) {
+        const int r = count_greater(a, n, a[i]);
+        if (r < left) sel[nsel + r] = a[i];
+      }
+      team_bar(bar, nth);
+      return;
+    }
+    for (int i = t; i < 256; i += nth) hist[i] = 0u;
+    team_bar(bar, nth);
+    for (int i = t; i < n; i += nth) atomicAdd(&hist[unsigned(a[i] >> shift) & 255u], 1u);
+    team_bar(bar, nth);
+    if (t < 32) {  // the bucket of the left-th largest key: lane l owns bins 8l .. 8l+7
+      uint32_t own = 0;
+#pragma unroll
+      for (int d = 0; d < 8; ++d) own += hist[8 * t + d];
+      uint32_t suf = own;  // keys in the bins of lanes >= t
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_down_sync(kFull, suf, off);
+        if (t + off < 32) suf += y;
+      }
+      const unsigned ok = __ballot_sync(kFull, suf >= uint32_t(left));
+      const int L = 31 - __clz(int(ok));
+      if (t == L) {
+        uint32_t run = suf - own;
+        for (int d = 7; d >= 0; --d) {
+          const uint32_t hcount = hist[8 * t + d];
+          if (run + hcount >= uint32_t(left)) {
+            ctr[1] = 0;
+            ctr[2] = 8 * t + d;
+            ctr[3] = int(run);
+            break;
+          }
+          run += hcount;
+        }
+      }
+    }
+    team_bar(bar, nth);
+    const uint32_t bstar = uint32_t(ctr[2]);
+    const int above = ctr[3];
+    for (int i = t; i < n; i += nth) {
+      const uint32_t dg = unsigned(a[i] >> shift) & 255u;
+      if (dg > bstar)
+        sel[atomicAdd(&ctr[0], 1)] = a[i];
+      else if (dg == bstar)
+        b[atomicAdd(&ctr[1], 1)] = a[i];
+    }
+    team_bar(bar, nth);
+    nsel += above;
+    left -= above;
+    n = ctr[1];
+    Key* sw = a;
+    a = b;
+    b = sw;
+    shift -= 8;
+  }
+}
+
+// Shared memory of one team.
+struct TeamMem {
+  unsigned char* A;  // inner keys of both halves, then the staircase keys
+  unsigned char* B;  // their scratch
+  unsigned char* isel;  // inner selections [2][kin_max] inner keys
+  uint64_t* osel;       // outer selection [kpad]
+  uint64_t* oout;       // outer selection in order [kpad]
+  uint32_t* hist;       // [2][256]
+  int* ctr;             // [2][4], then a flag
+  float* aval;          // [kin_max] x 2 lists
+  float* bval;
+  int32_t* aidx;
+  int32_t* bidx;
+};
+
+__host__ __device__ inline size_t team_buf_bytes(int S, int cnt_max, int ikb) {
+  size_t x = size_t(2) * S * ikb;
+  if (size_t(cnt_max) * 8 > x) x = size_t(cnt_max) * 8;
+  return (x + 15) / 16 * 16;
+}
+__host__ __device__ inline size_t team_mem_bytes(int S, int kin_max, int kpad, int cnt_max, int ikb) {
+  const size_t buf = team_buf_bytes(S, cnt_max, ikb);
+  return 2 * buf + (size_t(2) * kin_max * ikb + 15) / 16 * 16 + size_t(2) * kpad * 8 +
+         size_t(512) * 4 + 48 + size_t(4) * kin_max * 4;
+}
+
+__device__ __forceinline__ TeamMem team_mem(unsigned char* base, int S, int kin_max, int kpad,
+                                            int cnt_max, int ikb) {
+  TeamMem m;
+  const size_t buf = team_buf_bytes(S, cnt_max, ikb);
+  m.A = base;
+  m.B = base + buf;
+  m.isel = base + 2 * buf;
+  unsigned char* q = m.isel + (size_t(2) * kin_max * ikb + 15) / 16 * 16;
+  m.osel = reinterpret_cast<uint64_t*>(q);
+  m.oout = m.osel + kpad;
+  m.hist = reinterpret_cast<uint32_t*>(m.oout + kpad);
+  m.ctr = reinterpret_cast<int*>(m.hist + 512);
+  m.aval = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(m.ctr) + 48);
+  m.bval = m.aval + kin_max;
+  m.aidx = reinterpret_cast<int32_t*>(m.bval + kin_max);
+  m.bidx = m.aidx + kin_max;
+  return m;
+}
+
+// Task `which` (0: k' / top-W, 1: q' / top-R) of token `item` by a team of 128 threads
+// (team thread t); barriers bar0 (the team), bar0 + 1 and bar0 + 2 (its two halves).
+template <typename Tin, int EMAX>
+__device__ void team_select(const SelectArgs& a, long long item, int which, const uint32_t* stair,
+                            const TeamMem& m, int t, int bar0) {
+  using IKey = typename InnerKeyOf<Tin>::type;
+  constexpr int IBITS = sizeof(Tin) == 2 ? 32 : 48;
+  const int S = a.S, K = which ? a.R : a.W, kin = min(K, S);
+  const int cnt = which ? a.cnt_r : a.cnt_w;
+  const Tin* halves = static_cast<const Tin*>(which ? a.qp : a.kp) + item * 2 * S;
+
+  // ---- inner: half h by threads 64h .. 64h+63 ----
+  {
+    const int h = t >> 6, ht = t & 63, hb = bar0 + 1 + h;
+    IKey* A = reinterpret_cast<IKey*>(m.A) + size_t(h) * S;
+    IKey* Bk = reinterpret_cast<IKey*>(m.B) + size_t(h) * S;
+    IKey* sel = reinterpret_cast<IKey*>(m.isel) + size_t(h) * a.kin_max;
+    const Tin* src = halves + size_t(h) * S;
+    for (int j = ht; j < S; j += 64) A[j] = inner_key(src[j], j);
+    team_bar(hb, 64);
+    team_topk<IKey>(A, Bk, S, kin, IBITS, sel, m.hist + 256 * h, m.ctr + 4 * h, ht, 64, hb);
+    float* dv = h ? m.bval : m.aval;
+    int32_t* di = h ? m.bidx : m.aidx;
+    for (int i = ht; i < kin; i += 64) {
+      const IKey k = sel[i];
+      const int r = count_greater(sel, kin, k);
+      dv[r] = inner_value(k);
+      di[r] = min(int(0xFFFFu - uint32_t(k & 0xFFFFu)), S - 1);
+    }
+  }
+  team_bar(bar0, 128);
+
+  // ---- outer: top-K of the staircase pairs ----
+  const float* aval = m.aval;
+  const float* bval = m.bval;
+  const int32_t* aidx = m.aidx;
+  const int32_t* bidx = m.bidx;
+  auto pair_key = [&](int p, int q) -> uint64_t {
+    const float sum = __fadd_rn(aval[p], bval[q]);
+    const uint32_t flat = uint32_t(aidx[p]) * uint32_t(S) + uint32_t(bidx[q]);
+    return (uint64_t(ord_key(sum)) << 32) | uint64_t(0xFFFFFFFFu - flat);
+  };
+  uint64_t* OA = reinterpret_cast<uint64_t*>(m.A);
+  uint64_t* OB = reinterpret_cast<uint64_t*>(m.B);
+  for (int c = t; c < cnt; c += 128) {
+    const uint32_t pq = stair[c];
+    OA[c] = pair_key(int(pq >> 16), int(pq & 0xFFFFu));
+  }
+  team_bar(bar0, 128);
+  team_topk<uint64_t>(OA, OB, cnt, K, 64, m.osel, m.hist, m.ctr, t, 128, bar0);
+  for (int i = t; i < K; i += 128) {
+    const uint64_t k = m.osel[i];
+    m.oout[count_greater(m.osel, K, k)] = k;
+  }
+  if (t == 0) m.ctr[8] = 0;
+  team_bar(bar0, 128);
+  // Pairs right of the staircase that could still beat the K-th key.
+  const uint64_t kth = m.oout[K - 1];
+  const uint32_t kth_sum = uint32_t(kth >> 32);
+  bool beyond = false;
+  for (int p = t; p < kin; p += 128) {
+    for (int q = min(kin, K / (p + 1)); q < kin; ++q) {
+      const uint64_t k = pair_key(p, q);
+      if (uint32_t(k >> 32) < kth_sum) break;  // sums only fall along a row
+      if (k > kth) beyond = true;
+    }
+  }
+  if (beyond) m.ctr[8] = 1;
+  team_bar(bar0, 128);
+  if (m.ctr[8]) {  // rare: redo over every grid pair that can reach the K-th key
+    if (t < 32) {
+      outer_full_grid(aval, bval, aidx, bidx, S, kin, K, kth, m.oout, a.kpad, m.hist);
+      sort_desc_upto<uint64_t, EMAX>(m.oout, K);
+    }
+    team_bar(bar0, 128);
+  }
+  int32_t* oi = (which ? a.idx_r : a.idx_w) + item * K;
+  float* os = (which ? a.sc_r : a.sc_w) + item * K;
+  for (int r = t; r < K; r += 128) {
+    const uint64_t k = m.oout[r];
+    oi[r] = int32_t(0xFFFFFFFFu - uint32_t(k & 0xFFFFFFFFu));
+    os[r] = ord_decode(uint32_t(k >> 32));
+  }
+}
+
+template <typename Tin, typename Tv, int EMAX, bool TEAM>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs d) {
   extern __shared__ __align__(16) unsigned char smem[];
   const SelectArgs& a = d.sel;
@@ -77,7 +301,21 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs d) {
   const int W = d.W, R = d.R, WR = W + R, d_v = d.d_v;
 
   // ---- 1. selection of token (bh, 0) -------------------------------------------------
-  {
+  if (TEAM) {  // warps 0-3: the k' task, warps 4-7: the q' task
+    constexpr int ikb = int(sizeof(typename InnerKeyOf<Tin>::type));
+    uint32_t* stair_w = reinterpret_cast<uint32_t*>(smem);
+    uint32_t* stair_r = stair_w + a.cnt_w;
+    unsigned char* tbase = smem + (size_t(a.cnt_w + a.cnt_r) * 4 + 15) / 16 * 16;
+    const int cmax = max(a.cnt_w, a.cnt_r);
+    const size_t tsize = (team_mem_bytes(a.S, a.kin_max, a.kpad, cmax, ikb) + 15) / 16 * 16;
+    const int team = warp >> 2;
+    const TeamMem m = team_mem(tbase + team * tsize, a.S, a.kin_max, a.kpad, cmax, ikb);
+    // team 0's histograms are free until its selection starts: scratch for the staircases
+    int* tmp = reinterpret_cast<int*>(team_mem(tbase, a.S, a.kin_max, a.kpad, cmax, ikb).hist);
+    build_stair(stair_w, a.W, min(a.W, a.S), tmp);
+    build_stair(stair_r, a.R, min(a.R, a.S), tmp);
+    team_select<Tin, EMAX>(a, bh, team, team ? stair_r : stair_w, m, tid & 127, 1 + 3 * team);
+  } else {  // the selection kernel's pair mode: warps 0-1 the k' task, 2-3 the q' task
     const SelectSmem m = select_smem(a, smem);
     select_build_stairs(a, m);
     if (warp < 4) {
@@ -196,7 +434,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs d) {
 // Launch shape of the decode kernel: column width (the scan kernel's), blocks, shared memory.
 template <typename Tin>
 int decode_shape(int BH, int S, int d_v, int W, int R, SelectArgs* sel, int* cols, size_t* smem,
-                 size_t* sel_smem) {
+                 size_t* sel_smem, bool* team) {
   ScanShape shape;
   const int st = choose_scan_shape(BH, d_v, W, R, 0, 0, &shape);
   if (st != SDM_OK) return st;
@@ -206,14 +444,19 @@ int decode_shape(int BH, int S, int d_v, int W, int R, SelectArgs* sel, int* col
                    nullptr, sel, &stair_bytes, &per_warp);
   sel->warps = 4;
   *cols = shape.cols;
-  *sel_smem = stair_bytes + 4 * per_warp;
-  *smem = *sel_smem;
-  const size_t scan_smem = decode_scan_smem(W, R, shape.cols);
-  if (scan_smem > *smem) *smem = scan_smem;
   int dev = 0, max_smem = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return SDM_ECUDA;
+  const size_t scan_smem = decode_scan_smem(W, R, shape.cols);
+  // Teams of 4 warps per task where their buffers fit and K <= 128, else warp pairs.
+  const int ikb = int(sizeof(typename InnerKeyOf<Tin>::type));
+  const size_t team_smem =
+      stair_bytes + 2 * ((team_mem_bytes(S, sel->kin_max, sel->kpad, max(sel->cnt_w, sel->cnt_r),
+                                         ikb) + 15) / 16 * 16);
+  *team = W <= 128 && R <= 128 && team_smem <= size_t(max_smem) && scan_smem <= size_t(max_smem);
+  *sel_smem = *team ? team_smem : stair_bytes + 4 * per_warp;
+  *smem = *sel_smem > scan_smem ? *sel_smem : scan_smem;
   return *smem > size_t(max_smem) ? SDM_EUNSUPPORTED : SDM_OK;
 }
 
@@ -225,7 +468,9 @@ int launch_decode_t(const void* kp, const void* qp, const void* v, int v_dt, con
   DecodeArgs dargs;
   int cols = 0;
   size_t smem = 0;
-  const int st = decode_shape<Tin>(BH, S, d_v, W, R, &dargs.sel, &cols, &smem, &dargs.sel_smem);
+  bool team = false;
+  const int st =
+      decode_shape<Tin>(BH, S, d_v, W, R, &dargs.sel, &cols, &smem, &dargs.sel_smem, &team);
   if (st != SDM_OK) return st;
   dargs.sel.kp = kp;
   dargs.sel.qp = qp;
@@ -248,11 +493,13 @@ int launch_decode_t(const void* kp, const void* qp, const void* v, int v_dt, con
   const bool big = W > 128 || R > 128;
   const void* fn;
   if (v_dt == SDM_BF16)
-    fn = big ? reinterpret_cast<const void*>(&decode_kernel<Tin, uint16_t, 32>)
-             : reinterpret_cast<const void*>(&decode_kernel<Tin, uint16_t, 4>);
+    fn = big    ? reinterpret_cast<const void*>(&decode_kernel<Tin, uint16_t, 32, false>)
+         : team ? reinterpret_cast<const void*>(&decode_kernel<Tin, uint16_t, 4, true>)
+                : reinterpret_cast<const void*>(&decode_kernel<Tin, uint16_t, 4, false>);
   else
-    fn = big ? reinterpret_cast<const void*>(&decode_kernel<Tin, float, 32>)
-             : reinterpret_cast<const void*>(&decode_kernel<Tin, float, 4>);
+    fn = big    ? reinterpret_cast<const void*>(&decode_kernel<Tin, float, 32, false>)
+         : team ? reinterpret_cast<const void*>(&decode_kernel<Tin, float, 4, true>)
+                : reinterpret_cast<const void*>(&decode_kernel<Tin, float, 4, false>);
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
       cudaSuccess)
     return SDM_ECUDA;
@@ -282,8 +529,10 @@ int decode_supported(int in_dt, int BH, int S, int d_v, int W, int R) {
   SelectArgs sel;
   int cols = 0;
   size_t smem = 0, sel_smem = 0;
-  return in_dt == SDM_BF16 ? decode_shape<uint16_t>(BH, S, d_v, W, R, &sel, &cols, &smem, &sel_smem)
-                           : decode_shape<float>(BH, S, d_v, W, R, &sel, &cols, &smem, &sel_smem);
+  bool team = false;
+  return in_dt == SDM_BF16
+             ? decode_shape<uint16_t>(BH, S, d_v, W, R, &sel, &cols, &smem, &sel_smem, &team)
+             : decode_shape<float>(BH, S, d_v, W, R, &sel, &cols, &smem, &sel_smem, &team);
 }
 
 }  // namespace sdm
