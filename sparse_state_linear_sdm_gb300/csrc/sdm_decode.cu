@@ -173,6 +173,8 @@ struct TeamMem {
   float* bval;
   int32_t* aidx;
   int32_t* bidx;
+  int32_t* ridx;        // the task's result: slots [kpad]
+  float* rsc;           // and scores [kpad]
 };
 
 __host__ __device__ inline size_t team_buf_bytes(int S, int cnt_max, int ikb) {
@@ -183,7 +185,7 @@ __host__ __device__ inline size_t team_buf_bytes(int S, int cnt_max, int ikb) {
 __host__ __device__ inline size_t team_mem_bytes(int S, int kin_max, int kpad, int cnt_max, int ikb) {
   const size_t buf = team_buf_bytes(S, cnt_max, ikb);
   return 2 * buf + (size_t(2) * kin_max * ikb + 15) / 16 * 16 + size_t(2) * kpad * 8 +
-         size_t(512) * 4 + 48 + size_t(4) * kin_max * 4;
+         size_t(512) * 4 + 48 + size_t(4) * kin_max * 4 + size_t(2) * kpad * 4;
 }
 
 __device__ __forceinline__ TeamMem team_mem(unsigned char* base, int S, int kin_max, int kpad,
@@ -202,6 +204,8 @@ __device__ __forceinline__ TeamMem team_mem(unsigned char* base, int S, int kin_
   m.bval = m.aval + kin_max;
   m.aidx = reinterpret_cast<int32_t*>(m.bval + kin_max);
   m.bidx = m.aidx + kin_max;
+  m.ridx = m.bidx + kin_max;
+  m.rsc = reinterpret_cast<float*>(m.ridx + kpad);
   return m;
 }
 
@@ -223,7 +227,36 @@ __device__ void team_select(const SelectArgs& a, long long item, int which, cons
     IKey* Bk = reinterpret_cast<IKey*>(m.B) + size_t(h) * S;
     IKey* sel = reinterpret_cast<IKey*>(m.isel) + size_t(h) * a.kin_max;
     const Tin* src = halves + size_t(h) * S;
-    for (int j = ht; j < S; j += 64) A[j] = inner_key(src[j], j);
+    constexpr int EPV = 16 / int(sizeof(Tin));
+    if (a.vec) {  // 16-byte loads, up to four per thread issued before any is used
+      const uint4* src4 = reinterpret_cast<const uint4*>(src);
+      const int nvec = S / EPV;
+      for (int c0 = ht; c0 < nvec; c0 += 64 * 4) {
+        uint4 q[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          q[u] = c0 + 64 * u < nvec ? __ldg(src4 + c0 + 64 * u) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = c0 + 64 * u;
+          if (c >= nvec) break;
+          float f[EPV];
+          unpack16<Tin>(q[u], f);
+#pragma unroll
+          for (int i = 0; i < EPV; ++i)
+            A[c * EPV + i] = inner_key_f(f[i], c * EPV + i, static_cast<IKey*>(nullptr));
+        }
+      }
+    } else {
+      for (int j0 = ht; j0 < S; j0 += 64 * 8) {
+        Tin q[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) q[u] = j0 + 64 * u < S ? src[j0 + 64 * u] : Tin(0);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (j0 + 64 * u < S) A[j0 + 64 * u] = inner_key(q[u], j0 + 64 * u);
+      }
+    }
     team_bar(hb, 64);
     team_topk<IKey>(A, Bk, S, kin, IBITS, sel, m.hist + 256 * h, m.ctr + 4 * h, ht, 64, hb);
     float* dv = h ? m.bval : m.aval;
@@ -285,8 +318,12 @@ __device__ void team_select(const SelectArgs& a, long long item, int which, cons
   float* os = (which ? a.sc_r : a.sc_w) + item * K;
   for (int r = t; r < K; r += 128) {
     const uint64_t k = m.oout[r];
-    oi[r] = int32_t(0xFFFFFFFFu - uint32_t(k & 0xFFFFFFFFu));
-    os[r] = ord_decode(uint32_t(k >> 32));
+    const int32_t slot = int32_t(0xFFFFFFFFu - uint32_t(k & 0xFFFFFFFFu));
+    const float sc = ord_decode(uint32_t(k >> 32));
+    oi[r] = slot;
+    os[r] = sc;
+    m.ridx[r] = slot;
+    m.rsc[r] = sc;
   }
 }
 
@@ -325,19 +362,38 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs d) {
   }
   __syncthreads();  // idx / sc of the token written (global, this block)
 
-  // ---- 2. planning of the token (shared memory reused) --------------------------------
+  // ---- 2. planning of the token -----------------------------------------------------
+  // Team selections leave their slots and scores in shared memory (the scan's buffers
+  // follow them); the warp-pair path's are read back from global memory and its shared
+  // memory is reused.
+  const int32_t* gw = a.idx_w + size_t(bh) * W;
+  const int32_t* gr = a.idx_r + size_t(bh) * R;
+  const float* sw = a.sc_w + size_t(bh) * W;
+  const float* sr = a.sc_r + size_t(bh) * R;
+  unsigned char* sbase = smem;
+  if (TEAM) {
+    constexpr int ikb = int(sizeof(typename InnerKeyOf<Tin>::type));
+    unsigned char* tbase = smem + (size_t(a.cnt_w + a.cnt_r) * 4 + 15) / 16 * 16;
+    const int cmax = max(a.cnt_w, a.cnt_r);
+    const size_t tsize = (team_mem_bytes(a.S, a.kin_max, a.kpad, cmax, ikb) + 15) / 16 * 16;
+    const TeamMem m0 = team_mem(tbase, a.S, a.kin_max, a.kpad, cmax, ikb);
+    const TeamMem m1 = team_mem(tbase + tsize, a.S, a.kin_max, a.kpad, cmax, ikb);
+    gw = m0.ridx;
+    sw = m0.rsc;
+    gr = m1.ridx;
+    sr = m1.rsc;
+    sbase = smem + d.sel_smem;
+  }
   const int WRa = (WR + 3) & ~3;
-  float* rows = reinterpret_cast<float*>(smem);        // [WR][C]
+  float* rows = reinterpret_cast<float*>(sbase);       // [WR][C]
   float* wts = rows + size_t(WR) * C;                  // [WRa]
   int32_t* idx = reinterpret_cast<int32_t*>(wts + WRa);  // [WRa]
   int16_t* src = reinterpret_cast<int16_t*>(idx + WRa);  // [WRa]
   float* red = reinterpret_cast<float*>(
-      smem + ((size_t(WR) * C * 4 + size_t(WRa) * 10 + 15) / 16 * 16));  // [warps][C]
-  const int32_t* gw = a.idx_w + size_t(bh) * W;
-  const int32_t* gr = a.idx_r + size_t(bh) * R;
+      sbase + ((size_t(WR) * C * 4 + size_t(WRa) * 10 + 15) / 16 * 16));  // [warps][C]
   for (int e = tid; e < WR; e += kDecThreads) idx[e] = e < W ? gw[e] : gr[e - W];
-  if (warp == 0) warp_softmax(a.sc_w + size_t(bh) * W, W, wts);
-  if (warp == 1) warp_softmax(a.sc_r + size_t(bh) * R, R, wts + W);
+  if (warp == 0) warp_softmax(sw, W, wts);
+  if (warp == 1) warp_softmax(sr, R, wts + W);
   const float alpha = d.alpha[bh], beta = d.beta[bh];
   const int c4 = tid % LPR;
   const Tv* vsrc = static_cast<const Tv*>(d.v) + size_t(bh) * d_v + c0 + 4 * c4;
@@ -455,8 +511,12 @@ int decode_shape(int BH, int S, int d_v, int W, int R, SelectArgs* sel, int* col
       stair_bytes + 2 * ((team_mem_bytes(S, sel->kin_max, sel->kpad, max(sel->cnt_w, sel->cnt_r),
                                          ikb) + 15) / 16 * 16);
   *team = W <= 128 && R <= 128 && team_smem <= size_t(max_smem) && scan_smem <= size_t(max_smem);
+  *team = *team && team_smem + scan_smem <= size_t(max_smem);
   *sel_smem = *team ? team_smem : stair_bytes + 4 * per_warp;
-  *smem = *sel_smem > scan_smem ? *sel_smem : scan_smem;
+  if (*team)
+    *smem = team_smem + scan_smem;  // the scan's buffers follow the team selections
+  else
+    *smem = *sel_smem > scan_smem ? *sel_smem : scan_smem;
   return *smem > size_t(max_smem) ? SDM_EUNSUPPORTED : SDM_OK;
 }
 
