@@ -5,20 +5,20 @@
 //
 // The three-kernel path (sdm_select, planning, scan) spends most of a decode step in
 // launch and dependency latency: three small grids, each waiting for the previous one's
-// writes.  Here one block per (b, h, 32-column slice of d_v) does all of it:
-//   1. the selection of (b, h): warps 0-1 take the k' task, warps 2-3 the q' task (one
-//      half each, as the selection kernel's pair mode), written to idx/sc as sdm_select
-//      does.  Every slice block of a (b, h) selects the same slots (the work is small and
-//      the blocks would otherwise wait for each other).
+// writes.  Here one block per (b, h) does all of it:
+//   1. the selection of (b, h): warps 0-3 take the k' task and warps 4-7 the q' task (teams
+//      of four warps, below; warp pairs as in the selection kernel where the teams' buffers
+//      do not fit or K > 128), written to idx/sc as sdm_select does.
 //   2. the planning of the one token: softmax of the selected write and read scores (the
 //      same warp routine as the planning kernel), the source of every row (HBM, or the
-//      updated row of the token's own write set for a read slot it also writes), and the
-//      device error checks.
-//   3. the scan of the token on the block's columns with the scan kernel's thread mapping
-//      and arithmetic: gather, forget gate and delta update, write-back, forwarding,
-//      weighted read reduced in the same order.  The column width of a block is the one
-//      the scan kernel would use for these sizes (choose_scan_shape), so the read's sum
-//      runs in the same order too.
+//      updated row of the token's own write set for a read slot it also writes, found
+//      through a small hash of the write slots), and the device error checks.
+//   3. the scan of the token, one column slice after the other, each with the scan
+//      kernel's thread mapping and arithmetic for a block of that slice: gather, forget
+//      gate and delta update, write-back, forwarding, weighted read reduced in the same
+//      order.  The slice width is the one the scan kernel would use for these sizes
+//      (choose_scan_shape), so the read's sum runs in the same order too.  The rows of as
+//      many slices as fit in shared memory are gathered at once.
 // So every output is bit-identical to the three-kernel path.
 #include "sdm_select_impl.cuh"
 
@@ -37,15 +37,19 @@ struct DecodeArgs {
   float* o;
   long long N;
   int d_v, W, R, slices;
-  int cols;  // columns of d_v per block (4 .. 64), as the scan kernel's shape
+  int cols;   // columns of d_v per slice (4 .. 64), as the scan kernel's shape
+  int group;  // slices whose rows are gathered together
   size_t sel_smem;  // bytes of the selection's shared memory
   int* dev_err;
 };
 
-__host__ __device__ inline size_t decode_scan_smem(int W, int R, int C) {
+__host__ __device__ inline size_t decode_scan_smem(int W, int R, int C, int G) {
   const int WR = W + R, WRa = (WR + 3) & ~3;
-  return size_t(WR) * C * 4 + size_t(WRa) * 4 /* weights */ + size_t(WRa) * 4 /* slots */ +
-         size_t(WRa) * 2 /* sources */ + 16 + size_t(kDecWarps) * C * 4 /* reduction */;
+  int P = 64;
+  while (P < 2 * W) P <<= 1;
+  return size_t(G) * WR * C * 4 + size_t(WRa) * 4 /* weights */ + size_t(WRa) * 4 /* slots */ +
+         size_t(WRa) * 2 /* sources */ + 16 + size_t(kDecWarps) * C * 4 /* reduction */ +
+         size_t(P) * 4 /* write-slot table */;
 }
 
 template <typename Tv>
@@ -333,8 +337,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs d) {
   const SelectArgs& a = d.sel;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int C = d.cols, LPR = C / 4, RPP = kDecThreads / LPR;
-  const int bh = blockIdx.x / d.slices;
-  const int c0 = (blockIdx.x - bh * d.slices) * C;
+  const int bh = blockIdx.x;
   const int W = d.W, R = d.R, WR = W + R, d_v = d.d_v;
 
   // ---- 1. selection of token (bh, 0) -------------------------------------------------
@@ -385,112 +388,143 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs d) {
     sbase = smem + d.sel_smem;
   }
   const int WRa = (WR + 3) & ~3;
-  float* rows = reinterpret_cast<float*>(sbase);       // [WR][C]
-  float* wts = rows + size_t(WR) * C;                  // [WRa]
-  int32_t* idx = reinterpret_cast<int32_t*>(wts + WRa);  // [WRa]
-  int16_t* src = reinterpret_cast<int16_t*>(idx + WRa);  // [WRa]
+  const int G = d.group;  // column slices gathered together
+  float* rows = reinterpret_cast<float*>(sbase);             // [G][WR][C]
+  float* wts = rows + size_t(G) * WR * C;                    // [WRa]
+  int32_t* idx = reinterpret_cast<int32_t*>(wts + WRa);      // [WRa]
+  int16_t* src = reinterpret_cast<int16_t*>(idx + WRa);      // [WRa]
   float* red = reinterpret_cast<float*>(
-      sbase + ((size_t(WR) * C * 4 + size_t(WRa) * 10 + 15) / 16 * 16));  // [warps][C]
+      sbase + ((size_t(G) * WR * C * 4 + size_t(WRa) * 10 + 15) / 16 * 16));  // [warps][C]
+  int* table = reinterpret_cast<int*>(red + kDecWarps * C);  // [P] write positions by slot
+  int lg = 6;
+  while ((1 << lg) < 2 * W) ++lg;
+  const int P = 1 << lg;
+  for (int i = tid; i < P; i += kDecThreads) table[i] = -1;
   for (int e = tid; e < WR; e += kDecThreads) idx[e] = e < W ? gw[e] : gr[e - W];
   if (warp == 0) warp_softmax(sw, W, wts);
   if (warp == 1) warp_softmax(sr, R, wts + W);
   const float alpha = d.alpha[bh], beta = d.beta[bh];
   const int c4 = tid % LPR;
-  const Tv* vsrc = static_cast<const Tv*>(d.v) + size_t(bh) * d_v + c0 + 4 * c4;
-  const float4 vv = make_float4(v_at<Tv>(vsrc, 0), v_at<Tv>(vsrc, 1), v_at<Tv>(vsrc, 2),
-                                v_at<Tv>(vsrc, 3));
   __syncthreads();
+  // Write slots into an open-addressing table (a slot met twice: a duplicate write).
   int errs = 0;
+  auto slot_hash = [&](int32_t x) { return (uint32_t(x) * 0x9E3779B1u) >> (32 - lg); };
+  for (int e = tid; e < W; e += kDecThreads) {
+    const int32_t x = idx[e];
+    if (x < 0 || x >= d.N) continue;
+    for (uint32_t h = slot_hash(x);; h = (h + 1) & uint32_t(P - 1)) {
+      const int prev = atomicCAS(&table[h], -1, e);
+      if (prev == -1) break;
+      if (idx[prev] == x) {
+        errs |= SDM_DEV_DUP_WRITE;
+        break;
+      }
+    }
+  }
+  __syncthreads();
   for (int e = tid; e < WR; e += kDecThreads) {
     const int32_t x = idx[e];
     int code = -1;
     if (x < 0 || x >= d.N) {
       code = -2;
       errs |= SDM_DEV_INDEX_RANGE;
-    } else if (e < W) {
-      for (int p = 0; p < W; ++p)
-        if (p != e && idx[p] == x) errs |= SDM_DEV_DUP_WRITE;
-    } else {
-      for (int p = 0; p < W; ++p)  // a read of a row this token writes: the updated row
+    } else if (e >= W) {  // a read of a row this token writes: the updated row
+      for (uint32_t h = slot_hash(x);; h = (h + 1) & uint32_t(P - 1)) {
+        const int p = table[h];
+        if (p == -1) break;
         if (idx[p] == x) {
           code = p;
           break;
         }
+      }
     }
     src[e] = int16_t(code);
   }
   if (errs && d.dev_err) atomicOr(d.dev_err, errs);
   __syncthreads();
 
-  // ---- 3. the token's scan on columns c0 .. c0+C-1 -------------------------------------
-  float* Mbh = d.M + size_t(bh) * size_t(d.N) * d_v + c0;
-  for (int e = tid / LPR; e < WR; e += RPP)
-    if (src[e] == -1) cp16(rows + e * C + 4 * c4, Mbh + size_t(idx[e]) * d_v + 4 * c4);
-  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-  __syncthreads();
-
-  // Forget gate and delta update of the W write rows (in shared memory and in HBM).
-  for (int e = tid / LPR; e < W; e += RPP) {
-    if (src[e] == -2) continue;
-    float4* cell = reinterpret_cast<float4*>(rows + e * C) + c4;
-    const float4 m = *cell;
-    const float kb = beta * wts[e];
-    float4 r;
-    float mt_;
-    mt_ = alpha * m.x; r.x = fmaf(kb, vv.x - mt_, mt_);
-    mt_ = alpha * m.y; r.y = fmaf(kb, vv.y - mt_, mt_);
-    mt_ = alpha * m.z; r.z = fmaf(kb, vv.z - mt_, mt_);
-    mt_ = alpha * m.w; r.w = fmaf(kb, vv.w - mt_, mt_);
-    *cell = r;
-    *(reinterpret_cast<float4*>(Mbh + size_t(idx[e]) * d_v) + c4) = r;
-  }
-  __syncthreads();
-
-  // Read rows this token also writes take the updated row.
-  for (int e = W + tid; e < WR; e += kDecThreads) {
-    const int code = src[e];
-    if (code >= 0 && code < W) {
-      const float4* from = reinterpret_cast<const float4*>(rows + code * C);
-      float4* to = reinterpret_cast<float4*>(rows + e * C);
-      for (int q = 0; q < LPR; ++q) to[q] = from[q];
+  // ---- 3. the token's scan, column slice by column slice -------------------------------
+  float* Mbh = d.M + size_t(bh) * size_t(d.N) * d_v;
+  for (int s0 = 0; s0 < d.slices; s0 += G) {
+    const int gn = min(G, d.slices - s0);
+    for (int g = 0; g < gn; ++g) {
+      float* rg = rows + size_t(g) * WR * C;
+      const float* Mc = Mbh + (s0 + g) * C;
+      for (int e = tid / LPR; e < WR; e += RPP)
+        if (src[e] == -1) cp16(rg + e * C + 4 * c4, Mc + size_t(idx[e]) * d_v + 4 * c4);
     }
-  }
-  __syncthreads();
-
-  // Weighted read of the R read rows (after the write), reduced in the scan kernel's order.
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int e = tid / LPR; e < R; e += RPP) {
-    if (src[W + e] == -2) continue;
-    const float r = wts[W + e];
-    const float4 m = reinterpret_cast<const float4*>(rows + (W + e) * C)[c4];
-    acc.x = fmaf(r, m.x, acc.x);
-    acc.y = fmaf(r, m.y, acc.y);
-    acc.z = fmaf(r, m.z, acc.z);
-    acc.w = fmaf(r, m.w, acc.w);
-  }
-  for (int off = LPR; off < 32; off <<= 1) {
-    acc.x += __shfl_xor_sync(0xFFFFFFFFu, acc.x, off);
-    acc.y += __shfl_xor_sync(0xFFFFFFFFu, acc.y, off);
-    acc.z += __shfl_xor_sync(0xFFFFFFFFu, acc.z, off);
-    acc.w += __shfl_xor_sync(0xFFFFFFFFu, acc.w, off);
-  }
-  if (lane < LPR) reinterpret_cast<float4*>(red + warp * C)[lane] = acc;
-  __syncthreads();
-  if (tid < LPR) {
-    float4 s = reinterpret_cast<const float4*>(red)[tid];
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    for (int g = 0; g < gn; ++g) {
+      const int c0 = (s0 + g) * C;
+      float* rg = rows + size_t(g) * WR * C;
+      float* Mc = Mbh + c0;
+      const Tv* vsrc = static_cast<const Tv*>(d.v) + size_t(bh) * d_v + c0 + 4 * c4;
+      const float4 vv = make_float4(v_at<Tv>(vsrc, 0), v_at<Tv>(vsrc, 1), v_at<Tv>(vsrc, 2),
+                                    v_at<Tv>(vsrc, 3));
+      // Forget gate and delta update of the W write rows (in shared memory and in HBM).
+      for (int e = tid / LPR; e < W; e += RPP) {
+        if (src[e] == -2) continue;
+        float4* cell = reinterpret_cast<float4*>(rg + e * C) + c4;
+        const float4 m = *cell;
+        const float kb = beta * wts[e];
+        float4 r;
+        float mt_;
+        mt_ = alpha * m.x; r.x = fmaf(kb, vv.x - mt_, mt_);
+        mt_ = alpha * m.y; r.y = fmaf(kb, vv.y - mt_, mt_);
+        mt_ = alpha * m.z; r.z = fmaf(kb, vv.z - mt_, mt_);
+        mt_ = alpha * m.w; r.w = fmaf(kb, vv.w - mt_, mt_);
+        *cell = r;
+        *(reinterpret_cast<float4*>(Mc + size_t(idx[e]) * d_v) + c4) = r;
+      }
+      __syncthreads();
+      // Read rows this token also writes take the updated row.
+      for (int e = W + tid; e < WR; e += kDecThreads) {
+        const int code = src[e];
+        if (code >= 0 && code < W) {
+          const float4* from = reinterpret_cast<const float4*>(rg + code * C);
+          float4* to = reinterpret_cast<float4*>(rg + e * C);
+          for (int q = 0; q < LPR; ++q) to[q] = from[q];
+        }
+      }
+      __syncthreads();
+      // Weighted read of the R read rows (after the write), in the scan kernel's order.
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int e = tid / LPR; e < R; e += RPP) {
+        if (src[W + e] == -2) continue;
+        const float r = wts[W + e];
+        const float4 m = reinterpret_cast<const float4*>(rg + (W + e) * C)[c4];
+        acc.x = fmaf(r, m.x, acc.x);
+        acc.y = fmaf(r, m.y, acc.y);
+        acc.z = fmaf(r, m.z, acc.z);
+        acc.w = fmaf(r, m.w, acc.w);
+      }
+      for (int off = LPR; off < 32; off <<= 1) {
+        acc.x += __shfl_xor_sync(0xFFFFFFFFu, acc.x, off);
+        acc.y += __shfl_xor_sync(0xFFFFFFFFu, acc.y, off);
+        acc.z += __shfl_xor_sync(0xFFFFFFFFu, acc.z, off);
+        acc.w += __shfl_xor_sync(0xFFFFFFFFu, acc.w, off);
+      }
+      if (lane < LPR) reinterpret_cast<float4*>(red + warp * C)[lane] = acc;
+      __syncthreads();
+      if (tid < LPR) {
+        float4 sum = reinterpret_cast<const float4*>(red)[tid];
 #pragma unroll
-    for (int w = 1; w < kDecWarps; ++w) {
-      const float4 t = reinterpret_cast<const float4*>(red + w * C)[tid];
-      s = make_float4(s.x + t.x, s.y + t.y, s.z + t.z, s.w + t.w);
+        for (int w = 1; w < kDecWarps; ++w) {
+          const float4 t = reinterpret_cast<const float4*>(red + w * C)[tid];
+          sum = make_float4(sum.x + t.x, sum.y + t.y, sum.z + t.z, sum.w + t.w);
+        }
+        *(reinterpret_cast<float4*>(d.o + size_t(bh) * d_v + c0) + tid) = sum;
+      }
     }
-    *(reinterpret_cast<float4*>(d.o + size_t(bh) * d_v + c0) + tid) = s;
   }
 }
 
-// Launch shape of the decode kernel: column width (the scan kernel's), blocks, shared memory.
+// Launch shape of the decode kernel: column width (the scan kernel's), slices gathered
+// together, selection variant, shared memory.
 template <typename Tin>
-int decode_shape(int BH, int S, int d_v, int W, int R, SelectArgs* sel, int* cols, size_t* smem,
-                 size_t* sel_smem, bool* team) {
+int decode_shape(int BH, int S, int d_v, int W, int R, SelectArgs* sel, int* cols, int* group,
+                 size_t* smem, size_t* sel_smem, bool* team) {
   ScanShape shape;
   const int st = choose_scan_shape(BH, d_v, W, R, 0, 0, &shape);
   if (st != SDM_OK) return st;
@@ -504,20 +538,26 @@ int decode_shape(int BH, int S, int d_v, int W, int R, SelectArgs* sel, int* col
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return SDM_ECUDA;
-  const size_t scan_smem = decode_scan_smem(W, R, shape.cols);
-  // Teams of 4 warps per task where their buffers fit and K <= 128, else warp pairs.
+  const size_t cap = size_t(max_smem);
+  const int slices = d_v / shape.cols;
+  // Teams of 4 warps per task where K <= 128 and their buffers fit beside one slice's rows,
+  // else warp pairs (whose shared memory the scan part reuses).
   const int ikb = int(sizeof(typename InnerKeyOf<Tin>::type));
   const size_t team_smem =
       stair_bytes + 2 * ((team_mem_bytes(S, sel->kin_max, sel->kpad, max(sel->cnt_w, sel->cnt_r),
                                          ikb) + 15) / 16 * 16);
-  *team = W <= 128 && R <= 128 && team_smem <= size_t(max_smem) && scan_smem <= size_t(max_smem);
-  *team = *team && team_smem + scan_smem <= size_t(max_smem);
-  *sel_smem = *team ? team_smem : stair_bytes + 4 * per_warp;
-  if (*team)
-    *smem = team_smem + scan_smem;  // the scan's buffers follow the team selections
-  else
-    *smem = *sel_smem > scan_smem ? *sel_smem : scan_smem;
-  return *smem > size_t(max_smem) ? SDM_EUNSUPPORTED : SDM_OK;
+  const size_t pair_smem = stair_bytes + 4 * per_warp;
+  *team = W <= 128 && R <= 128 && team_smem + decode_scan_smem(W, R, shape.cols, 1) <= cap;
+  *sel_smem = *team ? team_smem : pair_smem;
+  auto total = [&](int g) {
+    const size_t sc = decode_scan_smem(W, R, shape.cols, g);
+    return *team ? team_smem + sc : (pair_smem > sc ? pair_smem : sc);
+  };
+  int g = slices;  // as many slices per gather as fit
+  while (g > 1 && total(g) > cap) --g;
+  *group = g;
+  *smem = total(g);
+  return *smem > cap ? SDM_EUNSUPPORTED : SDM_OK;
 }
 
 template <typename Tin>
@@ -526,11 +566,11 @@ int launch_decode_t(const void* kp, const void* qp, const void* v, int v_dt, con
                     int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, float* o,
                     int* dev_err, cudaStream_t s) {
   DecodeArgs dargs;
-  int cols = 0;
+  int cols = 0, group = 1;
   size_t smem = 0;
   bool team = false;
-  const int st =
-      decode_shape<Tin>(BH, S, d_v, W, R, &dargs.sel, &cols, &smem, &dargs.sel_smem, &team);
+  const int st = decode_shape<Tin>(BH, S, d_v, W, R, &dargs.sel, &cols, &group, &smem,
+                                   &dargs.sel_smem, &team);
   if (st != SDM_OK) return st;
   dargs.sel.kp = kp;
   dargs.sel.qp = qp;
@@ -549,6 +589,7 @@ int launch_decode_t(const void* kp, const void* qp, const void* v, int v_dt, con
   dargs.R = R;
   dargs.cols = cols;
   dargs.slices = d_v / cols;
+  dargs.group = group;
   dargs.dev_err = dev_err;
   const bool big = W > 128 || R > 128;
   const void* fn;
@@ -563,10 +604,8 @@ int launch_decode_t(const void* kp, const void* qp, const void* v, int v_dt, con
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
       cudaSuccess)
     return SDM_ECUDA;
-  const long long blocks = (long long)BH * dargs.slices;
-  if (blocks > 0x7FFFFFFFLL) return SDM_EUNSUPPORTED;
   void* args[] = {&dargs};
-  if (cudaLaunchKernel(fn, dim3(unsigned(blocks)), dim3(kDecThreads), args, smem, s) != cudaSuccess)
+  if (cudaLaunchKernel(fn, dim3(unsigned(BH)), dim3(kDecThreads), args, smem, s) != cudaSuccess)
     return SDM_ECUDA;
   return last_launch_status();
 }
@@ -587,12 +626,13 @@ int launch_decode(const void* kp, const void* qp, int in_dt, const void* v, int 
 
 int decode_supported(int in_dt, int BH, int S, int d_v, int W, int R) {
   SelectArgs sel;
-  int cols = 0;
+  int cols = 0, group = 1;
   size_t smem = 0, sel_smem = 0;
   bool team = false;
-  return in_dt == SDM_BF16
-             ? decode_shape<uint16_t>(BH, S, d_v, W, R, &sel, &cols, &smem, &sel_smem, &team)
-             : decode_shape<float>(BH, S, d_v, W, R, &sel, &cols, &smem, &sel_smem, &team);
+  return in_dt == SDM_BF16 ? decode_shape<uint16_t>(BH, S, d_v, W, R, &sel, &cols, &group, &smem,
+                                                    &sel_smem, &team)
+                           : decode_shape<float>(BH, S, d_v, W, R, &sel, &cols, &group, &smem,
+                                                 &sel_smem, &team);
 }
 
 }  // namespace sdm
