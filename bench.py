@@ -625,6 +625,33 @@ def run_decode(args):
     b2.record()
     torch.cuda.synchronize(dev)
     ms_in_place = a2.elapsed_time(b2) / K
+    # Device time per token: one graph of G consecutive tokens (inputs already resident, one
+    # launch per token), replayed; the host's per-replay cost is then spread over G tokens.
+    G = 16
+    toks = {k: torch.stack([st[k][:, :, t:t + 1].contiguous() for t in range(G)])
+            for k in ("kp", "qp", "v", "alpha", "beta")}
+    sel_g = [torch.empty_like(x) for x in step.sel]
+    o_g = torch.empty_like(step.o)
+    chain = lambda: [sdm.decode_step(toks["kp"][g], toks["qp"][g], toks["v"][g], toks["alpha"][g],
+                                     toks["beta"][g], st["M"], cfg.W, cfg.R, out=sel_g, o=o_g)
+                     for g in range(G)] if step.fused else None
+    ms_device = None
+    if step.fused:
+        chain()
+        torch.cuda.synchronize(dev)
+        gph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gph):
+            chain()
+        gph.replay()
+        torch.cuda.synchronize(dev)
+        reps = max(K // G, 4)
+        a3, b3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a3.record()
+        for _ in range(reps):
+            gph.replay()
+        b3.record()
+        torch.cuda.synchronize(dev)
+        ms_device = a3.elapsed_time(b3) / (reps * G)
     state_bytes = cfg.B * cfg.H * (2 * cfg.W + cfg.R) * cfg.d_v * 4
     line = {"metric": "SDM decode head-tokens/s (one token per step, state resident)",
             "value": cfg.B * cfg.H / (ms / 1e3), "unit": "head-tokens/s", "n_gpus": 1, "steps": K,
@@ -632,9 +659,13 @@ def run_decode(args):
             "data": "synthetic", "config": dict(config_dict(cfg), T=1, step="decode: CUDA graph of select + plan + scan"),
             "state_bytes_per_step": state_bytes, "state_gbs": state_bytes / (ms / 1e3) / 1e9,
             "us_per_step_inputs_in_place": ms_in_place * 1e3,
+            "us_per_step_device": ms_device * 1e3 if ms_device is not None else None,
+            "decode_kernel": "one fused kernel per token" if step.fused else "select + plan + scan",
             "note": "us_per_step includes copying each token's inputs into the step's buffers (5 copies); "
-                    "us_per_step_inputs_in_place replays the graph alone on inputs already there",
-            "gpu_launches": 3 * K}
+                    "us_per_step_inputs_in_place replays the one-token graph alone on inputs already there "
+                    "(bounded by the host's graph launches); us_per_step_device replays a graph of 16 "
+                    "consecutive tokens (device time per token)",
+            "gpu_launches": (1 if step.fused else 3) * K}
     print(json.dumps(line), flush=True)
 
 

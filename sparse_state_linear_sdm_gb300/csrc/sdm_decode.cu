@@ -6,27 +6,25 @@
 // The three-kernel path (sdm_select, planning, scan) spends most of a decode step in
 // launch and dependency latency: three small grids, each waiting for the previous one's
 // writes.  Here one block per (b, h) does all of it:
-//   1. the selection of (b, h): warps 0-3 take the k' task and warps 4-7 the q' task (teams
-//      of four warps, below; warp pairs as in the selection kernel where the teams' buffers
-//      do not fit or K > 128), written to idx/sc as sdm_select does.
+//   1. the selection of (b, h): in 512-thread blocks warps 0-7 take the k' task and warps
+//      8-15 the q' task (teams, below); where the teams' buffers do not fit or K > 128,
+//      256-thread blocks with the selection kernel's warp pairs.  Written to idx/sc as
+//      sdm_select does.
 //   2. the planning of the one token: softmax of the selected write and read scores (the
 //      same warp routine as the planning kernel), the source of every row (HBM, or the
 //      updated row of the token's own write set for a read slot it also writes, found
 //      through a small hash of the write slots), and the device error checks.
-//   3. the scan of the token, one column slice after the other, each with the scan
-//      kernel's thread mapping and arithmetic for a block of that slice: gather, forget
-//      gate and delta update, write-back, forwarding, weighted read reduced in the same
-//      order.  The slice width is the one the scan kernel would use for these sizes
-//      (choose_scan_shape), so the read's sum runs in the same order too.  The rows of as
-//      many slices as fit in shared memory are gathered at once.
+//   3. the scan of the token by groups of 256 threads, each taking column slices in turn
+//      with the scan kernel's thread mapping and arithmetic for a block of that slice:
+//      gather, forget gate and delta update, write-back, forwarding, weighted read reduced
+//      in the same order.  The slice width is the one the scan kernel would use for these
+//      sizes (choose_scan_shape), so the read's sum runs in the same order too.
 // So every output is bit-identical to the three-kernel path.
 #include "sdm_select_impl.cuh"
 
 namespace sdm {
 namespace {
 
-constexpr int kDecThreads = 256;
-constexpr int kDecWarps = kDecThreads / 32;
 
 struct DecodeArgs {
   SelectArgs sel;  // one token per (b, h): items = B * H, Tc = T_total = 1
@@ -38,18 +36,18 @@ struct DecodeArgs {
   long long N;
   int d_v, W, R, slices;
   int cols;   // columns of d_v per slice (4 .. 64), as the scan kernel's shape
-  int group;  // slices whose rows are gathered together
   size_t sel_smem;  // bytes of the selection's shared memory
   int* dev_err;
 };
 
-__host__ __device__ inline size_t decode_scan_smem(int W, int R, int C, int G) {
+// Shared memory of the planning and scan parts for NG groups of 256 threads.
+__host__ __device__ inline size_t decode_scan_smem(int W, int R, int C, int NG) {
   const int WR = W + R, WRa = (WR + 3) & ~3;
   int P = 64;
   while (P < 2 * W) P <<= 1;
-  return size_t(G) * WR * C * 4 + size_t(WRa) * 4 /* weights */ + size_t(WRa) * 4 /* slots */ +
-         size_t(WRa) * 2 /* sources */ + 16 + size_t(kDecWarps) * C * 4 /* reduction */ +
-         size_t(P) * 4 /* write-slot table */;
+  return size_t(NG) * WR * C * 4 /* rows */ + size_t(NG) * 8 * C * 4 /* reductions */ +
+         size_t(WRa) * 4 /* weights */ + size_t(WRa) * 4 /* slots */ +
+         size_t((WRa + 7) & ~7) * 2 /* sources */ + size_t(P) * 4 /* write-slot table */;
 }
 
 template <typename Tv>
@@ -70,10 +68,10 @@ __device__ __forceinline__ void cp16(float* dst, const float* src) {
                : "memory");
 }
 
-// ---- latency-oriented selection for one token: a team of 4 warps per task -----------
+// ---- latency-oriented selection for one token: a team of warps per task --------------
 //
 // The selection kernel gives a task one warp (or two), which suits throughput; for a single
-// token the task's latency is what counts.  Here a task gets a team of 128 threads (64 per
+// token the task's latency is what counts.  Here a task gets a team of 256 threads (128 per
 // half for the inner lists): radix passes over 8-bit digits narrow the candidates (each
 // pass: histogram, the bucket holding the k-th key, compaction), and once at most 64 are
 // left they are ranked against each other; the selected keys are put in order by rank.
@@ -215,7 +213,7 @@ __device__ __forceinline__ TeamMem team_mem(unsigned char* base, int S, int kin_
 
 // Task `which` (0: k' / top-W, 1: q' / top-R) of token `item` by a team of 128 threads
 // (team thread t); barriers bar0 (the team), bar0 + 1 and bar0 + 2 (its two halves).
-template <typename Tin, int EMAX>
+template <typename Tin, int EMAX, int TT>
 __device__ void team_select(const SelectArgs& a, long long item, int which, const uint32_t* stair,
                             const TeamMem& m, int t, int bar0) {
   using IKey = typename InnerKeyOf<Tin>::type;
@@ -224,9 +222,10 @@ __device__ void team_select(const SelectArgs& a, long long item, int which, cons
   const int cnt = which ? a.cnt_r : a.cnt_w;
   const Tin* halves = static_cast<const Tin*>(which ? a.qp : a.kp) + item * 2 * S;
 
-  // ---- inner: half h by threads 64h .. 64h+63 ----
+  constexpr int HT = TT / 2;  // threads per half
+  // ---- inner: half h by threads HT*h .. HT*h + HT-1 ----
   {
-    const int h = t >> 6, ht = t & 63, hb = bar0 + 1 + h;
+    const int h = t / HT, ht = t % HT, hb = bar0 + 1 + h;
     IKey* A = reinterpret_cast<IKey*>(m.A) + size_t(h) * S;
     IKey* Bk = reinterpret_cast<IKey*>(m.B) + size_t(h) * S;
     IKey* sel = reinterpret_cast<IKey*>(m.isel) + size_t(h) * a.kin_max;
@@ -235,14 +234,14 @@ __device__ void team_select(const SelectArgs& a, long long item, int which, cons
     if (a.vec) {  // 16-byte loads, up to four per thread issued before any is used
       const uint4* src4 = reinterpret_cast<const uint4*>(src);
       const int nvec = S / EPV;
-      for (int c0 = ht; c0 < nvec; c0 += 64 * 4) {
+      for (int c0 = ht; c0 < nvec; c0 += HT * 4) {
         uint4 q[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          q[u] = c0 + 64 * u < nvec ? __ldg(src4 + c0 + 64 * u) : make_uint4(0u, 0u, 0u, 0u);
+          q[u] = c0 + HT * u < nvec ? __ldg(src4 + c0 + HT * u) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int c = c0 + 64 * u;
+          const int c = c0 + HT * u;
           if (c >= nvec) break;
           float f[EPV];
           unpack16<Tin>(q[u], f);
@@ -252,27 +251,27 @@ __device__ void team_select(const SelectArgs& a, long long item, int which, cons
         }
       }
     } else {
-      for (int j0 = ht; j0 < S; j0 += 64 * 8) {
+      for (int j0 = ht; j0 < S; j0 += HT * 8) {
         Tin q[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) q[u] = j0 + 64 * u < S ? src[j0 + 64 * u] : Tin(0);
+        for (int u = 0; u < 8; ++u) q[u] = j0 + HT * u < S ? src[j0 + HT * u] : Tin(0);
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          if (j0 + 64 * u < S) A[j0 + 64 * u] = inner_key(q[u], j0 + 64 * u);
+          if (j0 + HT * u < S) A[j0 + HT * u] = inner_key(q[u], j0 + HT * u);
       }
     }
-    team_bar(hb, 64);
-    team_topk<IKey>(A, Bk, S, kin, IBITS, sel, m.hist + 256 * h, m.ctr + 4 * h, ht, 64, hb);
+    team_bar(hb, HT);
+    team_topk<IKey>(A, Bk, S, kin, IBITS, sel, m.hist + 256 * h, m.ctr + 4 * h, ht, HT, hb);
     float* dv = h ? m.bval : m.aval;
     int32_t* di = h ? m.bidx : m.aidx;
-    for (int i = ht; i < kin; i += 64) {
+    for (int i = ht; i < kin; i += HT) {
       const IKey k = sel[i];
       const int r = count_greater(sel, kin, k);
       dv[r] = inner_value(k);
       di[r] = min(int(0xFFFFu - uint32_t(k & 0xFFFFu)), S - 1);
     }
   }
-  team_bar(bar0, 128);
+  team_bar(bar0, TT);
 
   // ---- outer: top-K of the staircase pairs ----
   const float* aval = m.aval;
@@ -286,23 +285,23 @@ __device__ void team_select(const SelectArgs& a, long long item, int which, cons
   };
   uint64_t* OA = reinterpret_cast<uint64_t*>(m.A);
   uint64_t* OB = reinterpret_cast<uint64_t*>(m.B);
-  for (int c = t; c < cnt; c += 128) {
+  for (int c = t; c < cnt; c += TT) {
     const uint32_t pq = stair[c];
     OA[c] = pair_key(int(pq >> 16), int(pq & 0xFFFFu));
   }
-  team_bar(bar0, 128);
-  team_topk<uint64_t>(OA, OB, cnt, K, 64, m.osel, m.hist, m.ctr, t, 128, bar0);
-  for (int i = t; i < K; i += 128) {
+  team_bar(bar0, TT);
+  team_topk<uint64_t>(OA, OB, cnt, K, 64, m.osel, m.hist, m.ctr, t, TT, bar0);
+  for (int i = t; i < K; i += TT) {
     const uint64_t k = m.osel[i];
     m.oout[count_greater(m.osel, K, k)] = k;
   }
   if (t == 0) m.ctr[8] = 0;
-  team_bar(bar0, 128);
+  team_bar(bar0, TT);
   // Pairs right of the staircase that could still beat the K-th key.
   const uint64_t kth = m.oout[K - 1];
   const uint32_t kth_sum = uint32_t(kth >> 32);
   bool beyond = false;
-  for (int p = t; p < kin; p += 128) {
+  for (int p = t; p < kin; p += TT) {
     for (int q = min(kin, K / (p + 1)); q < kin; ++q) {
       const uint64_t k = pair_key(p, q);
       if (uint32_t(k >> 32) < kth_sum) break;  // sums only fall along a row
@@ -310,17 +309,17 @@ __device__ void team_select(const SelectArgs& a, long long item, int which, cons
     }
   }
   if (beyond) m.ctr[8] = 1;
-  team_bar(bar0, 128);
+  team_bar(bar0, TT);
   if (m.ctr[8]) {  // rare: redo over every grid pair that can reach the K-th key
     if (t < 32) {
       outer_full_grid(aval, bval, aidx, bidx, S, kin, K, kth, m.oout, a.kpad, m.hist);
       sort_desc_upto<uint64_t, EMAX>(m.oout, K);
     }
-    team_bar(bar0, 128);
+    team_bar(bar0, TT);
   }
   int32_t* oi = (which ? a.idx_r : a.idx_w) + item * K;
   float* os = (which ? a.sc_r : a.sc_w) + item * K;
-  for (int r = t; r < K; r += 128) {
+  for (int r = t; r < K; r += TT) {
     const uint64_t k = m.oout[r];
     const int32_t slot = int32_t(0xFFFFFFFFu - uint32_t(k & 0xFFFFFFFFu));
     const float sc = ord_decode(uint32_t(k >> 32));
@@ -332,29 +331,44 @@ __device__ void team_select(const SelectArgs& a, long long item, int which, cons
 }
 
 template <typename Tin, typename Tv, int EMAX, bool TEAM>
-__global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs d) {
+__global__ void __launch_bounds__(TEAM ? 512 : 256, 1) decode_kernel(DecodeArgs d) {
+  constexpr int NT = TEAM ? 512 : 256;  // threads of the block
+  constexpr int NG = NT / 256;          // groups of 256 threads scanning slices side by side
   extern __shared__ __align__(16) unsigned char smem[];
   const SelectArgs& a = d.sel;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int C = d.cols, LPR = C / 4, RPP = kDecThreads / LPR;
   const int bh = blockIdx.x;
+  const int C = d.cols, LPR = C / 4, RPP = 256 / LPR;
   const int W = d.W, R = d.R, WR = W + R, d_v = d.d_v;
 
   // ---- 1. selection of token (bh, 0) -------------------------------------------------
-  if (TEAM) {  // warps 0-3: the k' task, warps 4-7: the q' task
+  const int32_t* gw = a.idx_w + size_t(bh) * W;
+  const int32_t* gr = a.idx_r + size_t(bh) * R;
+  const float* sw = a.sc_w + size_t(bh) * W;
+  const float* sr = a.sc_r + size_t(bh) * R;
+  unsigned char* sbase = smem;
+  if (TEAM) {  // warps 0-7: the k' task, warps 8-15: the q' task
     constexpr int ikb = int(sizeof(typename InnerKeyOf<Tin>::type));
     uint32_t* stair_w = reinterpret_cast<uint32_t*>(smem);
     uint32_t* stair_r = stair_w + a.cnt_w;
     unsigned char* tbase = smem + (size_t(a.cnt_w + a.cnt_r) * 4 + 15) / 16 * 16;
     const int cmax = max(a.cnt_w, a.cnt_r);
     const size_t tsize = (team_mem_bytes(a.S, a.kin_max, a.kpad, cmax, ikb) + 15) / 16 * 16;
-    const int team = warp >> 2;
-    const TeamMem m = team_mem(tbase + team * tsize, a.S, a.kin_max, a.kpad, cmax, ikb);
+    const TeamMem m0 = team_mem(tbase, a.S, a.kin_max, a.kpad, cmax, ikb);
+    const TeamMem m1 = team_mem(tbase + tsize, a.S, a.kin_max, a.kpad, cmax, ikb);
     // team 0's histograms are free until its selection starts: scratch for the staircases
-    int* tmp = reinterpret_cast<int*>(team_mem(tbase, a.S, a.kin_max, a.kpad, cmax, ikb).hist);
+    int* tmp = reinterpret_cast<int*>(m0.hist);
     build_stair(stair_w, a.W, min(a.W, a.S), tmp);
     build_stair(stair_r, a.R, min(a.R, a.S), tmp);
-    team_select<Tin, EMAX>(a, bh, team, team ? stair_r : stair_w, m, tid & 127, 1 + 3 * team);
+    const int team = warp >> 3;
+    team_select<Tin, EMAX, 256>(a, bh, team, team ? stair_r : stair_w, team ? m1 : m0, tid & 255,
+                                1 + 3 * team);
+    // the slots and scores stay in shared memory; the scan's buffers follow them
+    gw = m0.ridx;
+    sw = m0.rsc;
+    gr = m1.ridx;
+    sr = m1.rsc;
+    sbase = smem + d.sel_smem;
   } else {  // the selection kernel's pair mode: warps 0-1 the k' task, 2-3 the q' task
     const SelectSmem m = select_smem(a, smem);
     select_build_stairs(a, m);
@@ -363,53 +377,29 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs d) {
       select_tasks<Tin, EMAX, true>(a, m, task, task + 1);
     }
   }
-  __syncthreads();  // idx / sc of the token written (global, this block)
+  __syncthreads();  // the token's slots and scores are written
 
   // ---- 2. planning of the token -----------------------------------------------------
-  // Team selections leave their slots and scores in shared memory (the scan's buffers
-  // follow them); the warp-pair path's are read back from global memory and its shared
-  // memory is reused.
-  const int32_t* gw = a.idx_w + size_t(bh) * W;
-  const int32_t* gr = a.idx_r + size_t(bh) * R;
-  const float* sw = a.sc_w + size_t(bh) * W;
-  const float* sr = a.sc_r + size_t(bh) * R;
-  unsigned char* sbase = smem;
-  if (TEAM) {
-    constexpr int ikb = int(sizeof(typename InnerKeyOf<Tin>::type));
-    unsigned char* tbase = smem + (size_t(a.cnt_w + a.cnt_r) * 4 + 15) / 16 * 16;
-    const int cmax = max(a.cnt_w, a.cnt_r);
-    const size_t tsize = (team_mem_bytes(a.S, a.kin_max, a.kpad, cmax, ikb) + 15) / 16 * 16;
-    const TeamMem m0 = team_mem(tbase, a.S, a.kin_max, a.kpad, cmax, ikb);
-    const TeamMem m1 = team_mem(tbase + tsize, a.S, a.kin_max, a.kpad, cmax, ikb);
-    gw = m0.ridx;
-    sw = m0.rsc;
-    gr = m1.ridx;
-    sr = m1.rsc;
-    sbase = smem + d.sel_smem;
-  }
   const int WRa = (WR + 3) & ~3;
-  const int G = d.group;  // column slices gathered together
-  float* rows = reinterpret_cast<float*>(sbase);             // [G][WR][C]
-  float* wts = rows + size_t(G) * WR * C;                    // [WRa]
-  int32_t* idx = reinterpret_cast<int32_t*>(wts + WRa);      // [WRa]
-  int16_t* src = reinterpret_cast<int16_t*>(idx + WRa);      // [WRa]
-  float* red = reinterpret_cast<float*>(
-      sbase + ((size_t(G) * WR * C * 4 + size_t(WRa) * 10 + 15) / 16 * 16));  // [warps][C]
-  int* table = reinterpret_cast<int*>(red + kDecWarps * C);  // [P] write positions by slot
+  float* rows = reinterpret_cast<float*>(sbase);                  // [NG][WR][C]
+  float* red = rows + size_t(NG) * WR * C;                        // [NG][8][C]
+  float* wts = red + NG * 8 * C;                                  // [WRa]
+  int32_t* idx = reinterpret_cast<int32_t*>(wts + WRa);           // [WRa]
+  int16_t* src = reinterpret_cast<int16_t*>(idx + WRa);           // [WRa]
+  int* table = reinterpret_cast<int*>(src + ((WRa + 7) & ~7));    // [P] write positions by slot
   int lg = 6;
   while ((1 << lg) < 2 * W) ++lg;
   const int P = 1 << lg;
-  for (int i = tid; i < P; i += kDecThreads) table[i] = -1;
-  for (int e = tid; e < WR; e += kDecThreads) idx[e] = e < W ? gw[e] : gr[e - W];
+  for (int i = tid; i < P; i += NT) table[i] = -1;
+  for (int e = tid; e < WR; e += NT) idx[e] = e < W ? gw[e] : gr[e - W];
   if (warp == 0) warp_softmax(sw, W, wts);
   if (warp == 1) warp_softmax(sr, R, wts + W);
   const float alpha = d.alpha[bh], beta = d.beta[bh];
-  const int c4 = tid % LPR;
   __syncthreads();
   // Write slots into an open-addressing table (a slot met twice: a duplicate write).
   int errs = 0;
   auto slot_hash = [&](int32_t x) { return (uint32_t(x) * 0x9E3779B1u) >> (32 - lg); };
-  for (int e = tid; e < W; e += kDecThreads) {
+  for (int e = tid; e < W; e += NT) {
     const int32_t x = idx[e];
     if (x < 0 || x >= d.N) continue;
     for (uint32_t h = slot_hash(x);; h = (h + 1) & uint32_t(P - 1)) {
@@ -422,7 +412,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs d) {
     }
   }
   __syncthreads();
-  for (int e = tid; e < WR; e += kDecThreads) {
+  for (int e = tid; e < WR; e += NT) {
     const int32_t x = idx[e];
     int code = -1;
     if (x < 0 || x >= d.N) {
@@ -443,88 +433,85 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(DecodeArgs d) {
   if (errs && d.dev_err) atomicOr(d.dev_err, errs);
   __syncthreads();
 
-  // ---- 3. the token's scan, column slice by column slice -------------------------------
+  // ---- 3. the token's scan: group gi of 256 threads takes slices gi, gi+NG, ... ---------
+  // Each slice with the scan kernel's thread mapping for a block of that slice.
+  const int gi = tid >> 8, lt = tid & 255, lw = lt >> 5, gbar = 7 + gi;
+  float* rg = rows + size_t(gi) * WR * C;
+  float* redg = red + gi * 8 * C;
+  const int c4 = lt % LPR;
   float* Mbh = d.M + size_t(bh) * size_t(d.N) * d_v;
-  for (int s0 = 0; s0 < d.slices; s0 += G) {
-    const int gn = min(G, d.slices - s0);
-    for (int g = 0; g < gn; ++g) {
-      float* rg = rows + size_t(g) * WR * C;
-      const float* Mc = Mbh + (s0 + g) * C;
-      for (int e = tid / LPR; e < WR; e += RPP)
-        if (src[e] == -1) cp16(rg + e * C + 4 * c4, Mc + size_t(idx[e]) * d_v + 4 * c4);
-    }
+  for (int sl = gi; sl < d.slices; sl += NG) {
+    const int c0 = sl * C;
+    float* Mc = Mbh + c0;
+    for (int e = lt / LPR; e < WR; e += RPP)
+      if (src[e] == -1) cp16(rg + e * C + 4 * c4, Mc + size_t(idx[e]) * d_v + 4 * c4);
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-    __syncthreads();
-    for (int g = 0; g < gn; ++g) {
-      const int c0 = (s0 + g) * C;
-      float* rg = rows + size_t(g) * WR * C;
-      float* Mc = Mbh + c0;
-      const Tv* vsrc = static_cast<const Tv*>(d.v) + size_t(bh) * d_v + c0 + 4 * c4;
-      const float4 vv = make_float4(v_at<Tv>(vsrc, 0), v_at<Tv>(vsrc, 1), v_at<Tv>(vsrc, 2),
-                                    v_at<Tv>(vsrc, 3));
-      // Forget gate and delta update of the W write rows (in shared memory and in HBM).
-      for (int e = tid / LPR; e < W; e += RPP) {
-        if (src[e] == -2) continue;
-        float4* cell = reinterpret_cast<float4*>(rg + e * C) + c4;
-        const float4 m = *cell;
-        const float kb = beta * wts[e];
-        float4 r;
-        float mt_;
-        mt_ = alpha * m.x; r.x = fmaf(kb, vv.x - mt_, mt_);
-        mt_ = alpha * m.y; r.y = fmaf(kb, vv.y - mt_, mt_);
-        mt_ = alpha * m.z; r.z = fmaf(kb, vv.z - mt_, mt_);
-        mt_ = alpha * m.w; r.w = fmaf(kb, vv.w - mt_, mt_);
-        *cell = r;
-        *(reinterpret_cast<float4*>(Mc + size_t(idx[e]) * d_v) + c4) = r;
+    const Tv* vsrc = static_cast<const Tv*>(d.v) + size_t(bh) * d_v + c0 + 4 * c4;
+    const float4 vv = make_float4(v_at<Tv>(vsrc, 0), v_at<Tv>(vsrc, 1), v_at<Tv>(vsrc, 2),
+                                  v_at<Tv>(vsrc, 3));
+    team_bar(gbar, 256);
+    // Forget gate and delta update of the W write rows (in shared memory and in HBM).
+    for (int e = lt / LPR; e < W; e += RPP) {
+      if (src[e] == -2) continue;
+      float4* cell = reinterpret_cast<float4*>(rg + e * C) + c4;
+      const float4 m = *cell;
+      const float kb = beta * wts[e];
+      float4 r;
+      float mt_;
+      mt_ = alpha * m.x; r.x = fmaf(kb, vv.x - mt_, mt_);
+      mt_ = alpha * m.y; r.y = fmaf(kb, vv.y - mt_, mt_);
+      mt_ = alpha * m.z; r.z = fmaf(kb, vv.z - mt_, mt_);
+      mt_ = alpha * m.w; r.w = fmaf(kb, vv.w - mt_, mt_);
+      *cell = r;
+      *(reinterpret_cast<float4*>(Mc + size_t(idx[e]) * d_v) + c4) = r;
+    }
+    team_bar(gbar, 256);
+    // Read rows this token also writes take the updated row.
+    for (int e = W + lt; e < WR; e += 256) {
+      const int code = src[e];
+      if (code >= 0 && code < W) {
+        const float4* from = reinterpret_cast<const float4*>(rg + code * C);
+        float4* to = reinterpret_cast<float4*>(rg + e * C);
+        for (int q = 0; q < LPR; ++q) to[q] = from[q];
       }
-      __syncthreads();
-      // Read rows this token also writes take the updated row.
-      for (int e = W + tid; e < WR; e += kDecThreads) {
-        const int code = src[e];
-        if (code >= 0 && code < W) {
-          const float4* from = reinterpret_cast<const float4*>(rg + code * C);
-          float4* to = reinterpret_cast<float4*>(rg + e * C);
-          for (int q = 0; q < LPR; ++q) to[q] = from[q];
-        }
-      }
-      __syncthreads();
-      // Weighted read of the R read rows (after the write), in the scan kernel's order.
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int e = tid / LPR; e < R; e += RPP) {
-        if (src[W + e] == -2) continue;
-        const float r = wts[W + e];
-        const float4 m = reinterpret_cast<const float4*>(rg + (W + e) * C)[c4];
-        acc.x = fmaf(r, m.x, acc.x);
-        acc.y = fmaf(r, m.y, acc.y);
-        acc.z = fmaf(r, m.z, acc.z);
-        acc.w = fmaf(r, m.w, acc.w);
-      }
-      for (int off = LPR; off < 32; off <<= 1) {
-        acc.x += __shfl_xor_sync(0xFFFFFFFFu, acc.x, off);
-        acc.y += __shfl_xor_sync(0xFFFFFFFFu, acc.y, off);
-        acc.z += __shfl_xor_sync(0xFFFFFFFFu, acc.z, off);
-        acc.w += __shfl_xor_sync(0xFFFFFFFFu, acc.w, off);
-      }
-      if (lane < LPR) reinterpret_cast<float4*>(red + warp * C)[lane] = acc;
-      __syncthreads();
-      if (tid < LPR) {
-        float4 sum = reinterpret_cast<const float4*>(red)[tid];
+    }
+    team_bar(gbar, 256);
+    // Weighted read of the R read rows (after the write), in the scan kernel's order.
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int e = lt / LPR; e < R; e += RPP) {
+      if (src[W + e] == -2) continue;
+      const float r = wts[W + e];
+      const float4 m = reinterpret_cast<const float4*>(rg + (W + e) * C)[c4];
+      acc.x = fmaf(r, m.x, acc.x);
+      acc.y = fmaf(r, m.y, acc.y);
+      acc.z = fmaf(r, m.z, acc.z);
+      acc.w = fmaf(r, m.w, acc.w);
+    }
+    for (int off = LPR; off < 32; off <<= 1) {
+      acc.x += __shfl_xor_sync(0xFFFFFFFFu, acc.x, off);
+      acc.y += __shfl_xor_sync(0xFFFFFFFFu, acc.y, off);
+      acc.z += __shfl_xor_sync(0xFFFFFFFFu, acc.z, off);
+      acc.w += __shfl_xor_sync(0xFFFFFFFFu, acc.w, off);
+    }
+    if (lane < LPR) reinterpret_cast<float4*>(redg + lw * C)[lane] = acc;
+    team_bar(gbar, 256);
+    if (lt < LPR) {
+      float4 sum = reinterpret_cast<const float4*>(redg)[lt];
 #pragma unroll
-        for (int w = 1; w < kDecWarps; ++w) {
-          const float4 t = reinterpret_cast<const float4*>(red + w * C)[tid];
-          sum = make_float4(sum.x + t.x, sum.y + t.y, sum.z + t.z, sum.w + t.w);
-        }
-        *(reinterpret_cast<float4*>(d.o + size_t(bh) * d_v + c0) + tid) = sum;
+      for (int w = 1; w < 8; ++w) {
+        const float4 t = reinterpret_cast<const float4*>(redg + w * C)[lt];
+        sum = make_float4(sum.x + t.x, sum.y + t.y, sum.z + t.z, sum.w + t.w);
       }
+      *(reinterpret_cast<float4*>(d.o + size_t(bh) * d_v + c0) + lt) = sum;
     }
   }
 }
 
-// Launch shape of the decode kernel: column width (the scan kernel's), slices gathered
-// together, selection variant, shared memory.
+// Launch shape of the decode kernel: slice width (the scan kernel's), selection variant
+// (teams of 8 warps in 512-thread blocks, or warp pairs in 256-thread blocks), shared memory.
 template <typename Tin>
-int decode_shape(int BH, int S, int d_v, int W, int R, SelectArgs* sel, int* cols, int* group,
-                 size_t* smem, size_t* sel_smem, bool* team) {
+int decode_shape(int BH, int S, int d_v, int W, int R, SelectArgs* sel, int* cols, size_t* smem,
+                 size_t* sel_smem, bool* team) {
   ScanShape shape;
   const int st = choose_scan_shape(BH, d_v, W, R, 0, 0, &shape);
   if (st != SDM_OK) return st;
@@ -539,24 +526,20 @@ int decode_shape(int BH, int S, int d_v, int W, int R, SelectArgs* sel, int* col
       cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return SDM_ECUDA;
   const size_t cap = size_t(max_smem);
-  const int slices = d_v / shape.cols;
-  // Teams of 4 warps per task where K <= 128 and their buffers fit beside one slice's rows,
-  // else warp pairs (whose shared memory the scan part reuses).
   const int ikb = int(sizeof(typename InnerKeyOf<Tin>::type));
   const size_t team_smem =
       stair_bytes + 2 * ((team_mem_bytes(S, sel->kin_max, sel->kpad, max(sel->cnt_w, sel->cnt_r),
                                          ikb) + 15) / 16 * 16);
-  const size_t pair_smem = stair_bytes + 4 * per_warp;
-  *team = W <= 128 && R <= 128 && team_smem + decode_scan_smem(W, R, shape.cols, 1) <= cap;
-  *sel_smem = *team ? team_smem : pair_smem;
-  auto total = [&](int g) {
-    const size_t sc = decode_scan_smem(W, R, shape.cols, g);
-    return *team ? team_smem + sc : (pair_smem > sc ? pair_smem : sc);
-  };
-  int g = slices;  // as many slices per gather as fit
-  while (g > 1 && total(g) > cap) --g;
-  *group = g;
-  *smem = total(g);
+  const size_t team_total = team_smem + decode_scan_smem(W, R, shape.cols, 2);
+  *team = W <= 128 && R <= 128 && team_total <= cap;
+  if (*team) {
+    *sel_smem = team_smem;
+    *smem = team_total;  // the scan's buffers follow the team selections
+  } else {
+    *sel_smem = stair_bytes + 4 * per_warp;
+    const size_t sc = decode_scan_smem(W, R, shape.cols, 1);
+    *smem = *sel_smem > sc ? *sel_smem : sc;
+  }
   return *smem > cap ? SDM_EUNSUPPORTED : SDM_OK;
 }
 
@@ -566,11 +549,11 @@ int launch_decode_t(const void* kp, const void* qp, const void* v, int v_dt, con
                     int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, float* o,
                     int* dev_err, cudaStream_t s) {
   DecodeArgs dargs;
-  int cols = 0, group = 1;
+  int cols = 0;
   size_t smem = 0;
   bool team = false;
-  const int st = decode_shape<Tin>(BH, S, d_v, W, R, &dargs.sel, &cols, &group, &smem,
-                                   &dargs.sel_smem, &team);
+  const int st =
+      decode_shape<Tin>(BH, S, d_v, W, R, &dargs.sel, &cols, &smem, &dargs.sel_smem, &team);
   if (st != SDM_OK) return st;
   dargs.sel.kp = kp;
   dargs.sel.qp = qp;
@@ -589,7 +572,6 @@ int launch_decode_t(const void* kp, const void* qp, const void* v, int v_dt, con
   dargs.R = R;
   dargs.cols = cols;
   dargs.slices = d_v / cols;
-  dargs.group = group;
   dargs.dev_err = dev_err;
   const bool big = W > 128 || R > 128;
   const void* fn;
@@ -605,7 +587,7 @@ int launch_decode_t(const void* kp, const void* qp, const void* v, int v_dt, con
       cudaSuccess)
     return SDM_ECUDA;
   void* args[] = {&dargs};
-  if (cudaLaunchKernel(fn, dim3(unsigned(BH)), dim3(kDecThreads), args, smem, s) != cudaSuccess)
+  if (cudaLaunchKernel(fn, dim3(unsigned(BH)), dim3(team ? 512 : 256), args, smem, s) != cudaSuccess)
     return SDM_ECUDA;
   return last_launch_status();
 }
@@ -626,13 +608,12 @@ int launch_decode(const void* kp, const void* qp, int in_dt, const void* v, int 
 
 int decode_supported(int in_dt, int BH, int S, int d_v, int W, int R) {
   SelectArgs sel;
-  int cols = 0, group = 1;
+  int cols = 0;
   size_t smem = 0, sel_smem = 0;
   bool team = false;
-  return in_dt == SDM_BF16 ? decode_shape<uint16_t>(BH, S, d_v, W, R, &sel, &cols, &group, &smem,
-                                                    &sel_smem, &team)
-                           : decode_shape<float>(BH, S, d_v, W, R, &sel, &cols, &group, &smem,
-                                                 &sel_smem, &team);
+  return in_dt == SDM_BF16
+             ? decode_shape<uint16_t>(BH, S, d_v, W, R, &sel, &cols, &smem, &sel_smem, &team)
+             : decode_shape<float>(BH, S, d_v, W, R, &sel, &cols, &smem, &sel_smem, &team);
 }
 
 }  // namespace sdm
