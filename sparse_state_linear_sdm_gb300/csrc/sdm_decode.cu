@@ -113,7 +113,13 @@ __device__ void team_topk(Key* a, Key* b, int n, int need, int bits, Key* sel, u
     }
     for (int i = t; i < 256; i += nth) hist[i] = 0u;
     team_bar(bar, nth);
-    for (int i = t; i < n; i += nth) atomicAdd(&hist[unsigned(a[i] >> shift) & 255u], 1u);
+    // Equal digits of a warp are counted with one atomic (few bins take most keys).
+    for (int i0 = 0; i0 < n; i0 += nth) {
+      const int i = i0 + t;
+      const unsigned dg = i < n ? unsigned(a[i] >> shift) & 255u : 256u;
+      const unsigned same = __match_any_sync(kFull, dg);
+      if (dg < 256u && (threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(&hist[dg], unsigned(__popc(same)));
+    }
     team_bar(bar, nth);
     if (t < 32) {  // the bucket of the left-th largest key: lane l owns bins 8l .. 8l+7
       uint32_t own = 0;
@@ -144,12 +150,27 @@ __device__ void team_topk(Key* a, Key* b, int n, int need, int bits, Key* sel, u
     team_bar(bar, nth);
     const uint32_t bstar = uint32_t(ctr[2]);
     const int above = ctr[3];
-    for (int i = t; i < n; i += nth) {
-      const uint32_t dg = unsigned(a[i] >> shift) & 255u;
-      if (dg > bstar)
-        sel[atomicAdd(&ctr[0], 1)] = a[i];
-      else if (dg == bstar)
-        b[atomicAdd(&ctr[1], 1)] = a[i];
+    // Appends with one atomic per warp and list (ballot, then each lane's rank in it).
+    const unsigned lane = threadIdx.x & 31, below = (1u << lane) - 1u;
+    for (int i0 = 0; i0 < n; i0 += nth) {
+      const int i = i0 + t;
+      Key k = 0;
+      uint32_t dg = 0;
+      if (i < n) {
+        k = a[i];
+        dg = unsigned(k >> shift) & 255u;
+      }
+      const unsigned up = __ballot_sync(kFull, i < n && dg > bstar);
+      const unsigned eq = __ballot_sync(kFull, i < n && dg == bstar);
+      int base_up = 0, base_eq = 0;
+      if (lane == 0) {
+        if (up) base_up = atomicAdd(&ctr[0], __popc(up));
+        if (eq) base_eq = atomicAdd(&ctr[1], __popc(eq));
+      }
+      base_up = __shfl_sync(kFull, base_up, 0);
+      base_eq = __shfl_sync(kFull, base_eq, 0);
+      if ((up >> lane) & 1u) sel[base_up + __popc(up & below)] = k;
+      if ((eq >> lane) & 1u) b[base_eq + __popc(eq & below)] = k;
     }
     team_bar(bar, nth);
     nsel += above;
