@@ -36,16 +36,18 @@ struct DecodeArgs {
   long long N;
   int d_v, W, R, slices;
   int cols;   // columns of d_v per slice (4 .. 64), as the scan kernel's shape
+  int bufs;   // row buffers per group of 256 threads (1 or 2)
   size_t sel_smem;  // bytes of the selection's shared memory
   int* dev_err;
 };
 
-// Shared memory of the planning and scan parts for NG groups of 256 threads.
-__host__ __device__ inline size_t decode_scan_smem(int W, int R, int C, int NG) {
+// Shared memory of the planning and scan parts for NG groups of 256 threads with NB row
+// buffers each.
+__host__ __device__ inline size_t decode_scan_smem(int W, int R, int C, int NG, int NB) {
   const int WR = W + R, WRa = (WR + 3) & ~3;
   int P = 64;
   while (P < 2 * W) P <<= 1;
-  return size_t(NG) * WR * C * 4 /* rows */ + size_t(NG) * 8 * C * 4 /* reductions */ +
+  return size_t(NG) * NB * WR * C * 4 /* rows */ + size_t(NG) * 8 * C * 4 /* reductions */ +
          size_t(WRa) * 4 /* weights */ + size_t(WRa) * 4 /* slots */ +
          size_t((WRa + 7) & ~7) * 2 /* sources */ + size_t(P) * 4 /* write-slot table */;
 }
@@ -181,6 +183,53 @@ __device__ void team_topk(Key* a, Key* b, int n, int need, int bits, Key* sel, u
     b = sw;
     shift -= 8;
   }
+}
+
+// Both staircases {(p, q): p, q < kin, (p+1)(q+1) <= K} as p << 16 | q, row by row, with
+// every thread of the block: warp 0 (W) and warp 1 (R) form the rows' start offsets, then
+// each entry finds its row by binary search.  rs: (kin_w + 1) + (kin_r + 1) ints of scratch.
+__device__ void build_stairs_parallel(uint32_t* st_w, uint32_t* st_r, int W, int R, int S,
+                                      int* rs, int nt) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kw = min(W, S), kr = min(R, S);
+  int* rs_w = rs;
+  int* rs_r = rs + kw + 1;
+  if (warp < 2) {
+    const int K = warp ? R : W, kin = warp ? kr : kw;
+    int* r = warp ? rs_r : rs_w;
+    const int per = (kin + 31) / 32;
+    const int p0 = min(kin, lane * per), p1 = min(kin, p0 + per);
+    int mine = 0;
+    for (int p = p0; p < p1; ++p) mine += min(kin, K / (p + 1));
+    int incl = mine;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(kFull, incl, off);
+      if (lane >= off) incl += y;
+    }
+    int off = incl - mine;
+    for (int p = p0; p < p1; ++p) {
+      r[p] = off;
+      off += min(kin, K / (p + 1));
+    }
+    if (lane == 31) r[kin] = incl;
+  }
+  __syncthreads();
+  for (int which = 0; which < 2; ++which) {
+    const int kin = which ? kr : kw;
+    const int* r = which ? rs_r : rs_w;
+    uint32_t* st = which ? st_r : st_w;
+    const int cnt = r[kin];
+    for (int c = tid; c < cnt; c += nt) {
+      int lo = 0, hi = kin - 1;  // the last row starting at or before c
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (r[mid] <= c) lo = mid; else hi = mid - 1;
+      }
+      st[c] = (uint32_t(lo) << 16) | uint32_t(c - r[lo]);
+    }
+  }
+  __syncthreads();
 }
 
 // Shared memory of one team.
@@ -378,9 +427,7 @@ __global__ void __launch_bounds__(TEAM ? 512 : 256, 1) decode_kernel(DecodeArgs 
     const TeamMem m0 = team_mem(tbase, a.S, a.kin_max, a.kpad, cmax, ikb);
     const TeamMem m1 = team_mem(tbase + tsize, a.S, a.kin_max, a.kpad, cmax, ikb);
     // team 0's histograms are free until its selection starts: scratch for the staircases
-    int* tmp = reinterpret_cast<int*>(m0.hist);
-    build_stair(stair_w, a.W, min(a.W, a.S), tmp);
-    build_stair(stair_r, a.R, min(a.R, a.S), tmp);
+    build_stairs_parallel(stair_w, stair_r, a.W, a.R, a.S, reinterpret_cast<int*>(m0.hist), NT);
     const int team = warp >> 3;
     team_select<Tin, EMAX, 256>(a, bh, team, team ? stair_r : stair_w, team ? m1 : m0, tid & 255,
                                 1 + 3 * team);
@@ -402,8 +449,8 @@ __global__ void __launch_bounds__(TEAM ? 512 : 256, 1) decode_kernel(DecodeArgs 
 
   // ---- 2. planning of the token -----------------------------------------------------
   const int WRa = (WR + 3) & ~3;
-  float* rows = reinterpret_cast<float*>(sbase);                  // [NG][WR][C]
-  float* red = rows + size_t(NG) * WR * C;                        // [NG][8][C]
+  float* rows = reinterpret_cast<float*>(sbase);                  // [NG][bufs][WR][C]
+  float* red = rows + size_t(NG) * d.bufs * WR * C;               // [NG][8][C]
   float* wts = red + NG * 8 * C;                                  // [WRa]
   int32_t* idx = reinterpret_cast<int32_t*>(wts + WRa);           // [WRa]
   int16_t* src = reinterpret_cast<int16_t*>(idx + WRa);           // [WRa]
@@ -455,18 +502,30 @@ __global__ void __launch_bounds__(TEAM ? 512 : 256, 1) decode_kernel(DecodeArgs 
   __syncthreads();
 
   // ---- 3. the token's scan: group gi of 256 threads takes slices gi, gi+NG, ... ---------
-  // Each slice with the scan kernel's thread mapping for a block of that slice.
+  // Each slice with the scan kernel's thread mapping for a block of that slice; with two
+  // row buffers per group the next slice's rows are gathered while this one is computed.
   const int gi = tid >> 8, lt = tid & 255, lw = lt >> 5, gbar = 7 + gi;
-  float* rg = rows + size_t(gi) * WR * C;
+  const int NB = d.bufs;  // row buffers per group (1 or 2)
   float* redg = red + gi * 8 * C;
   const int c4 = lt % LPR;
   float* Mbh = d.M + size_t(bh) * size_t(d.N) * d_v;
-  for (int sl = gi; sl < d.slices; sl += NG) {
-    const int c0 = sl * C;
-    float* Mc = Mbh + c0;
+  auto gather = [&](int sl, float* rg) {
+    const float* Mc = Mbh + sl * C;
     for (int e = lt / LPR; e < WR; e += RPP)
       if (src[e] == -1) cp16(rg + e * C + 4 * c4, Mc + size_t(idx[e]) * d_v + 4 * c4);
-    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  if (gi < d.slices) gather(gi, rows + size_t(gi * NB) * WR * C);
+  for (int sl = gi, k = 0; sl < d.slices; sl += NG, ++k) {
+    const int c0 = sl * C;
+    float* Mc = Mbh + c0;
+    float* rg = rows + size_t(gi * NB + (k % NB)) * WR * C;
+    const bool ahead = NB > 1 && sl + NG < d.slices;
+    if (ahead) gather(sl + NG, rows + size_t(gi * NB + ((k + 1) % NB)) * WR * C);
+    if (ahead)
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
     const Tv* vsrc = static_cast<const Tv*>(d.v) + size_t(bh) * d_v + c0 + 4 * c4;
     const float4 vv = make_float4(v_at<Tv>(vsrc, 0), v_at<Tv>(vsrc, 1), v_at<Tv>(vsrc, 2),
                                   v_at<Tv>(vsrc, 3));
@@ -525,14 +584,20 @@ __global__ void __launch_bounds__(TEAM ? 512 : 256, 1) decode_kernel(DecodeArgs 
       }
       *(reinterpret_cast<float4*>(d.o + size_t(bh) * d_v + c0) + lt) = sum;
     }
+    if (NB == 1 && sl + NG < d.slices) {
+      team_bar(gbar, 256);  // every read of this slice's rows is done
+      gather(sl + NG, rg);
+    } else if (NB > 1) {
+      team_bar(gbar, 256);  // the buffer is gathered into again two slices later
+    }
   }
 }
 
 // Launch shape of the decode kernel: slice width (the scan kernel's), selection variant
 // (teams of 8 warps in 512-thread blocks, or warp pairs in 256-thread blocks), shared memory.
 template <typename Tin>
-int decode_shape(int BH, int S, int d_v, int W, int R, SelectArgs* sel, int* cols, size_t* smem,
-                 size_t* sel_smem, bool* team) {
+int decode_shape(int BH, int S, int d_v, int W, int R, SelectArgs* sel, int* cols, int* bufs,
+                 size_t* smem, size_t* sel_smem, bool* team) {
   ScanShape shape;
   const int st = choose_scan_shape(BH, d_v, W, R, 0, 0, &shape);
   if (st != SDM_OK) return st;
@@ -551,14 +616,18 @@ int decode_shape(int BH, int S, int d_v, int W, int R, SelectArgs* sel, int* col
   const size_t team_smem =
       stair_bytes + 2 * ((team_mem_bytes(S, sel->kin_max, sel->kpad, max(sel->cnt_w, sel->cnt_r),
                                          ikb) + 15) / 16 * 16);
-  const size_t team_total = team_smem + decode_scan_smem(W, R, shape.cols, 2);
+  const int slices = d_v / shape.cols;
+  // Two row buffers per group where there are slices to prefetch and they fit.
+  *bufs = slices > 2 && team_smem + decode_scan_smem(W, R, shape.cols, 2, 2) <= cap ? 2 : 1;
+  const size_t team_total = team_smem + decode_scan_smem(W, R, shape.cols, 2, *bufs);
   *team = W <= 128 && R <= 128 && team_total <= cap;
   if (*team) {
     *sel_smem = team_smem;
     *smem = team_total;  // the scan's buffers follow the team selections
   } else {
+    *bufs = 1;
     *sel_smem = stair_bytes + 4 * per_warp;
-    const size_t sc = decode_scan_smem(W, R, shape.cols, 1);
+    const size_t sc = decode_scan_smem(W, R, shape.cols, 1, 1);
     *smem = *sel_smem > sc ? *sel_smem : sc;
   }
   return *smem > cap ? SDM_EUNSUPPORTED : SDM_OK;
@@ -570,11 +639,11 @@ int launch_decode_t(const void* kp, const void* qp, const void* v, int v_dt, con
                     int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, float* o,
                     int* dev_err, cudaStream_t s) {
   DecodeArgs dargs;
-  int cols = 0;
+  int cols = 0, bufs = 1;
   size_t smem = 0;
   bool team = false;
-  const int st =
-      decode_shape<Tin>(BH, S, d_v, W, R, &dargs.sel, &cols, &smem, &dargs.sel_smem, &team);
+  const int st = decode_shape<Tin>(BH, S, d_v, W, R, &dargs.sel, &cols, &bufs, &smem,
+                                   &dargs.sel_smem, &team);
   if (st != SDM_OK) return st;
   dargs.sel.kp = kp;
   dargs.sel.qp = qp;
@@ -593,6 +662,7 @@ int launch_decode_t(const void* kp, const void* qp, const void* v, int v_dt, con
   dargs.R = R;
   dargs.cols = cols;
   dargs.slices = d_v / cols;
+  dargs.bufs = bufs;
   dargs.dev_err = dev_err;
   const bool big = W > 128 || R > 128;
   const void* fn;
@@ -629,12 +699,13 @@ int launch_decode(const void* kp, const void* qp, int in_dt, const void* v, int 
 
 int decode_supported(int in_dt, int BH, int S, int d_v, int W, int R) {
   SelectArgs sel;
-  int cols = 0;
+  int cols = 0, bufs = 1;
   size_t smem = 0, sel_smem = 0;
   bool team = false;
-  return in_dt == SDM_BF16
-             ? decode_shape<uint16_t>(BH, S, d_v, W, R, &sel, &cols, &smem, &sel_smem, &team)
-             : decode_shape<float>(BH, S, d_v, W, R, &sel, &cols, &smem, &sel_smem, &team);
+  return in_dt == SDM_BF16 ? decode_shape<uint16_t>(BH, S, d_v, W, R, &sel, &cols, &bufs, &smem,
+                                                    &sel_smem, &team)
+                           : decode_shape<float>(BH, S, d_v, W, R, &sel, &cols, &bufs, &smem,
+                                                 &sel_smem, &team);
 }
 
 }  // namespace sdm
