@@ -79,13 +79,6 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
   // Two staging buffers of one token's [slots W | slots R | scores W | scores R]: the next
   // token's (going backwards) arrive by cp.async while this one is processed.
   int32_t* stg = reinterpret_cast<int32_t*>(red + kBwdWarps * C);  // [2][2 * WR]
-  // The token's read slots by hash: a write row whose slot is not read by the same token
-  // can be loaded before the read phase updates G.
-  int* rtab = stg + 4 * WR;  // [P]
-  int lg = 6;
-  while ((1 << lg) < 2 * R) ++lg;
-  const int P = 1 << lg;
-  auto rhash = [&](int32_t x) { return (uint32_t(x) * 0x9E3779B1u) >> (32 - lg); };
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int slices = d_v / C;
@@ -120,52 +113,12 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
     const int32_t* iw = stg + (t & 1) * 2 * WR;
     const int32_t* ir = iw + W;
     const float* scw = reinterpret_cast<const float*>(iw + WR);
-    for (int i = tid; i < P; i += kBwdThreads) rtab[i] = -1;
     if (warp == 0) warp_softmax(scw, W, kw);
     if (warp == 1) warp_softmax(scw + W, R, rw);
     __syncthreads();
     if (t > 0) stage(t - 1);  // the other buffer held token t+1, no longer read
-    for (int j = tid; j < R; j += kBwdThreads) {
-      const int32_t x = ir[j];
-      if (x < 0 || x >= a.N) continue;
-      for (uint32_t h = rhash(x);; h = (h + 1) & uint32_t(P - 1)) {
-        const int prev = atomicCAS(&rtab[h], -1, int(x));
-        if (prev == -1 || prev == int(x)) break;
-      }
-    }
     float* part = a.part + (tk * slices + sl) * PW;
     const float4 dO4 = reinterpret_cast<const float4*>(a.dO + tk * d_v + c0)[c4];
-    const float al = a.alpha[tk], be = a.beta[tk];
-    const float4 vv = load_v4(a.v, a.v_bf16, (tk * d_v + c0) / 4 + c4);
-    __syncthreads();  // the read-slot table is complete
-    // The first round of write rows, loaded now where the token does not also read the slot
-    // (the rest after the read phase): one memory round trip per token instead of two.
-    int32_t x0[NB];
-    bool early[NB];
-    float4 g0[NB], wp0[NB];
-#pragma unroll
-    for (int u = 0; u < NB; ++u) {
-      const int i = u * RPP + tid / LPR;
-      x0[u] = i < W ? iw[i] : -1;
-      early[u] = false;
-      g0[u] = wp0[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (x0[u] >= 0 && x0[u] < a.N) {
-        bool read_too = false;
-        for (uint32_t h = rhash(x0[u]);; h = (h + 1) & uint32_t(P - 1)) {
-          const int v = rtab[h];
-          if (v == -1) break;
-          if (v == int(x0[u])) {
-            read_too = true;
-            break;
-          }
-        }
-        wp0[u] = reinterpret_cast<const float4*>(a.w_prev + (tk * W + i) * d_v + c0)[c4];
-        if (!read_too) {
-          g0[u] = reinterpret_cast<const float4*>(Gbh + size_t(x0[u]) * d_v)[c4];
-          early[u] = true;
-        }
-      }
-    }
 
     // Read rows: dr_j (this slice's share) and G[ir_j] += r_j dO_t.  Each thread takes up
     // to NB rows per round and loads all of them before using any (their latencies
@@ -201,6 +154,8 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
     __syncthreads();  // the read contributions reach G before the write rows load it
 
     // Write rows: partial dot products, dv, and G propagated to M_{t-1} (same batching).
+    const float al = a.alpha[tk], be = a.beta[tk];
+    const float4 vv = load_v4(a.v, a.v_bf16, (tk * d_v + c0) / 4 + c4);
     float4 dva = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int ib = 0; ib < W; ib += NB * RPP) {
       int32_t x[NB];
@@ -208,14 +163,6 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
 #pragma unroll
       for (int u = 0; u < NB; ++u) {
         const int i = ib + u * RPP + tid / LPR;
-        if (ib == 0) {  // loaded before the read phase, except rows the token also reads
-          x[u] = x0[u];
-          g[u] = g0[u];
-          wp[u] = wp0[u];
-          if (!early[u] && x[u] >= 0 && x[u] < a.N)
-            g[u] = reinterpret_cast<const float4*>(Gbh + size_t(x[u]) * d_v)[c4];
-          continue;
-        }
         x[u] = i < W ? iw[i] : -1;
         g[u] = wp[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (x[u] >= 0 && x[u] < a.N) {
@@ -272,9 +219,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
 
 size_t backward_smem_bytes(int C, int W, int R) {
   const int WRa = (W + R + 3) & ~3;
-  int P = 64;
-  while (P < 2 * R) P <<= 1;
-  return size_t(WRa) * 4 + size_t(kBwdWarps) * C * 4 + size_t(4 * (W + R)) * 4 + size_t(P) * 4;
+  return size_t(WRa) * 4 + size_t(kBwdWarps) * C * 4 + size_t(4 * (W + R)) * 4;
 }
 
 int backward_cols(int d_v) {
