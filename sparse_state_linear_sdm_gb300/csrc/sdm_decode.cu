@@ -530,113 +530,59 @@ __global__ void __launch_bounds__(TEAM ? 512 : 256, 1) decode_kernel(DecodeArgs 
     const float4 vv = make_float4(v_at<Tv>(vsrc, 0), v_at<Tv>(vsrc, 1), v_at<Tv>(vsrc, 2),
                                   v_at<Tv>(vsrc, 3));
     team_bar(gbar, 256);
-    if (C >= 32) {
-      // The scan kernel's mapping for 32- and 64-column slices: warp lw owns column quads
-      // q0 .. q0+QPW-1 of every row, its lanes take rows lane, lane+32, ...
-      const int QPW = C / 32, q0 = lw * QPW;
-      for (int e = lane; e < W; e += 32) {
-        if (src[e] == -2) continue;
-        const float kb = beta * wts[e];
-        float* Mrow = Mc + size_t(idx[e]) * d_v;
-        for (int q = 0; q < QPW; ++q) {
-          const Tv* vq = static_cast<const Tv*>(d.v) + size_t(bh) * d_v + c0 + 4 * (q0 + q);
-          const float4 vv2 = make_float4(v_at<Tv>(vq, 0), v_at<Tv>(vq, 1), v_at<Tv>(vq, 2),
-                                         v_at<Tv>(vq, 3));
-          float4* cell = reinterpret_cast<float4*>(rg + e * C) + q0 + q;
-          const float4 m = *cell;
-          float4 r;
-          float mt_;
-          mt_ = alpha * m.x; r.x = fmaf(kb, vv2.x - mt_, mt_);
-          mt_ = alpha * m.y; r.y = fmaf(kb, vv2.y - mt_, mt_);
-          mt_ = alpha * m.z; r.z = fmaf(kb, vv2.z - mt_, mt_);
-          mt_ = alpha * m.w; r.w = fmaf(kb, vv2.w - mt_, mt_);
-          *cell = r;
-          *(reinterpret_cast<float4*>(Mrow) + q0 + q) = r;
-        }
+    // Forget gate and delta update of the W write rows (in shared memory and in HBM).
+    for (int e = lt / LPR; e < W; e += RPP) {
+      if (src[e] == -2) continue;
+      float4* cell = reinterpret_cast<float4*>(rg + e * C) + c4;
+      const float4 m = *cell;
+      const float kb = beta * wts[e];
+      float4 r;
+      float mt_;
+      mt_ = alpha * m.x; r.x = fmaf(kb, vv.x - mt_, mt_);
+      mt_ = alpha * m.y; r.y = fmaf(kb, vv.y - mt_, mt_);
+      mt_ = alpha * m.z; r.z = fmaf(kb, vv.z - mt_, mt_);
+      mt_ = alpha * m.w; r.w = fmaf(kb, vv.w - mt_, mt_);
+      *cell = r;
+      *(reinterpret_cast<float4*>(Mc + size_t(idx[e]) * d_v) + c4) = r;
+    }
+    team_bar(gbar, 256);
+    // Read rows this token also writes take the updated row.
+    for (int e = W + lt; e < WR; e += 256) {
+      const int code = src[e];
+      if (code >= 0 && code < W) {
+        const float4* from = reinterpret_cast<const float4*>(rg + code * C);
+        float4* to = reinterpret_cast<float4*>(rg + e * C);
+        for (int q = 0; q < LPR; ++q) to[q] = from[q];
       }
-      __syncwarp();
-      for (int e = W + lane; e < WR; e += 32) {
-        const int code = src[e];
-        if (code >= 0 && code < W)
-          for (int q = 0; q < QPW; ++q)
-            reinterpret_cast<float4*>(rg + e * C)[q0 + q] =
-                reinterpret_cast<const float4*>(rg + code * C)[q0 + q];
+    }
+    team_bar(gbar, 256);
+    // Weighted read of the R read rows (after the write), in the scan kernel's order.
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int e = lt / LPR; e < R; e += RPP) {
+      if (src[W + e] == -2) continue;
+      const float r = wts[W + e];
+      const float4 m = reinterpret_cast<const float4*>(rg + (W + e) * C)[c4];
+      acc.x = fmaf(r, m.x, acc.x);
+      acc.y = fmaf(r, m.y, acc.y);
+      acc.z = fmaf(r, m.z, acc.z);
+      acc.w = fmaf(r, m.w, acc.w);
+    }
+    for (int off = LPR; off < 32; off <<= 1) {
+      acc.x += __shfl_xor_sync(0xFFFFFFFFu, acc.x, off);
+      acc.y += __shfl_xor_sync(0xFFFFFFFFu, acc.y, off);
+      acc.z += __shfl_xor_sync(0xFFFFFFFFu, acc.z, off);
+      acc.w += __shfl_xor_sync(0xFFFFFFFFu, acc.w, off);
+    }
+    if (lane < LPR) reinterpret_cast<float4*>(redg + lw * C)[lane] = acc;
+    team_bar(gbar, 256);
+    if (lt < LPR) {
+      float4 sum = reinterpret_cast<const float4*>(redg)[lt];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) {
+        const float4 t = reinterpret_cast<const float4*>(redg + w * C)[lt];
+        sum = make_float4(sum.x + t.x, sum.y + t.y, sum.z + t.z, sum.w + t.w);
       }
-      __syncwarp();
-      for (int q = 0; q < QPW; ++q) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int e = lane; e < R; e += 32) {
-          if (src[W + e] == -2) continue;
-          const float r = wts[W + e];
-          const float4 m = reinterpret_cast<const float4*>(rg + (W + e) * C)[q0 + q];
-          acc.x = fmaf(r, m.x, acc.x);
-          acc.y = fmaf(r, m.y, acc.y);
-          acc.z = fmaf(r, m.z, acc.z);
-          acc.w = fmaf(r, m.w, acc.w);
-        }
-        for (int off = 16; off > 0; off >>= 1) {
-          acc.x += __shfl_xor_sync(0xFFFFFFFFu, acc.x, off);
-          acc.y += __shfl_xor_sync(0xFFFFFFFFu, acc.y, off);
-          acc.z += __shfl_xor_sync(0xFFFFFFFFu, acc.z, off);
-          acc.w += __shfl_xor_sync(0xFFFFFFFFu, acc.w, off);
-        }
-        if (lane == 0) *(reinterpret_cast<float4*>(d.o + size_t(bh) * d_v + c0) + q0 + q) = acc;
-      }
-    } else {
-      // Forget gate and delta update of the W write rows (in shared memory and in HBM).
-      for (int e = lt / LPR; e < W; e += RPP) {
-        if (src[e] == -2) continue;
-        float4* cell = reinterpret_cast<float4*>(rg + e * C) + c4;
-        const float4 m = *cell;
-        const float kb = beta * wts[e];
-        float4 r;
-        float mt_;
-        mt_ = alpha * m.x; r.x = fmaf(kb, vv.x - mt_, mt_);
-        mt_ = alpha * m.y; r.y = fmaf(kb, vv.y - mt_, mt_);
-        mt_ = alpha * m.z; r.z = fmaf(kb, vv.z - mt_, mt_);
-        mt_ = alpha * m.w; r.w = fmaf(kb, vv.w - mt_, mt_);
-        *cell = r;
-        *(reinterpret_cast<float4*>(Mc + size_t(idx[e]) * d_v) + c4) = r;
-      }
-      team_bar(gbar, 256);
-      // Read rows this token also writes take the updated row.
-      for (int e = W + lt; e < WR; e += 256) {
-        const int code = src[e];
-        if (code >= 0 && code < W) {
-          const float4* from = reinterpret_cast<const float4*>(rg + code * C);
-          float4* to = reinterpret_cast<float4*>(rg + e * C);
-          for (int q = 0; q < LPR; ++q) to[q] = from[q];
-        }
-      }
-      team_bar(gbar, 256);
-      // Weighted read of the R read rows (after the write), in the scan kernel's order.
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int e = lt / LPR; e < R; e += RPP) {
-        if (src[W + e] == -2) continue;
-        const float r = wts[W + e];
-        const float4 m = reinterpret_cast<const float4*>(rg + (W + e) * C)[c4];
-        acc.x = fmaf(r, m.x, acc.x);
-        acc.y = fmaf(r, m.y, acc.y);
-        acc.z = fmaf(r, m.z, acc.z);
-        acc.w = fmaf(r, m.w, acc.w);
-      }
-      for (int off = LPR; off < 32; off <<= 1) {
-        acc.x += __shfl_xor_sync(0xFFFFFFFFu, acc.x, off);
-        acc.y += __shfl_xor_sync(0xFFFFFFFFu, acc.y, off);
-        acc.z += __shfl_xor_sync(0xFFFFFFFFu, acc.z, off);
-        acc.w += __shfl_xor_sync(0xFFFFFFFFu, acc.w, off);
-      }
-      if (lane < LPR) reinterpret_cast<float4*>(redg + lw * C)[lane] = acc;
-      team_bar(gbar, 256);
-      if (lt < LPR) {
-        float4 sum = reinterpret_cast<const float4*>(redg)[lt];
-  #pragma unroll
-        for (int w = 1; w < 8; ++w) {
-          const float4 t = reinterpret_cast<const float4*>(redg + w * C)[lt];
-          sum = make_float4(sum.x + t.x, sum.y + t.y, sum.z + t.z, sum.w + t.w);
-        }
-        *(reinterpret_cast<float4*>(d.o + size_t(bh) * d_v + c0) + lt) = sum;
-      }
+      *(reinterpret_cast<float4*>(d.o + size_t(bh) * d_v + c0) + lt) = sum;
     }
     if (NB == 1 && sl + NG < d.slices) {
       team_bar(gbar, 256);  // every read of this slice's rows is done

@@ -212,177 +212,6 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   cp_async_wait<0>();
 }
 
-// The same scan with each warp owning QPW column quads (4 columns each) of the slice for
-// every row (C = 32 * QPW): the write, the forwarding and the read of a token are then
-// warp-local, and one block barrier per token is left (the records are shared by the warps
-// of the block).  A warp's lanes take rows lane, lane + 32, ...; the read is summed per lane
-// over its rows and then across the warp.
-template <int C, int PD>
-__global__ void __launch_bounds__(kScanThreads) scan_kernel_wc(ScanArgs a) {
-  constexpr int QPW = C / 32;  // float4 column quads per warp
-  constexpr int MD = 2 * PD;
-  constexpr int QM = MD + 1;
-  constexpr int QR = PD + 1;
-  extern __shared__ __align__(16) unsigned char smem[];
-  const int W = a.W, R = a.R, WR = W + R, T = a.T, d_v = a.d_v;
-  const RecLayout L = a.L;
-  const int meta_bytes = L.off_v + 4 * C;
-  float* rows = reinterpret_cast<float*>(smem);                               // [QR][WR][C]
-  unsigned char* meta = smem + size_t(QR) * WR * C * 4;                        // [QM][meta_bytes]
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int slices = d_v / C;
-  const int bh = blockIdx.x / slices;
-  const int c0 = (blockIdx.x - bh * slices) * C;
-  const unsigned char* recs = a.rec + size_t(bh) * T * L.bytes;
-  float* Mbh = a.M + size_t(bh) * size_t(a.N) * d_v + c0;
-  float* obh = a.o + (size_t(bh) * a.T_total + a.t_off) * d_v + c0;
-  float* wsave = a.w_prev ? a.w_prev + (size_t(bh) * a.T_total + a.t_off) * W * d_v + c0 : nullptr;
-  float* rsave = a.r_rows ? a.r_rows + (size_t(bh) * a.T_total + a.t_off) * R * d_v + c0 : nullptr;
-  const int q0 = warp * QPW;  // this warp's first column quad
-
-  auto issue_meta = [&](int u) {
-    if (u >= T) return;
-    const unsigned char* src = recs + size_t(u) * L.bytes;
-    unsigned char* dst = meta + (u % QM) * meta_bytes;
-    const int n_main = L.off_v / 16;
-    for (int k = tid; k < n_main + C / 4; k += kScanThreads) {
-      if (k < n_main)
-        cp_async16(dst + 16 * k, src + 16 * k);
-      else
-        cp_async16(dst + L.off_v + 16 * (k - n_main), src + L.off_v + 4 * c0 + 16 * (k - n_main));
-    }
-  };
-  auto issue_rows = [&](int u) {  // this warp's column quads of the rows of token u
-    if (u >= T) return;
-    const unsigned char* mt = meta + (u % QM) * meta_bytes;
-    const int32_t* idx = reinterpret_cast<const int32_t*>(mt);
-    const int16_t* src = reinterpret_cast<const int16_t*>(mt + L.off_src);
-    float* ru = rows + size_t(u % QR) * WR * C;
-    for (int e = lane; e < WR; e += 32) {
-      if (src[e] != -1) continue;
-      const float* g = Mbh + size_t(idx[e]) * d_v;
-#pragma unroll
-      for (int q = 0; q < QPW; ++q) cp_async16(ru + e * C + 4 * (q0 + q), g + 4 * (q0 + q));
-    }
-  };
-
-  // Prologue: records of tokens [0, PD), then what iterations -PD .. -1 would have issued
-  // (record u + MD and rows u + PD for u = -PD .. -1): records PD .. MD-1, rows 0 .. PD-1.
-  for (int u = 0; u < PD; ++u) issue_meta(u);
-  cp_async_commit();
-  cp_async_wait<0>();
-  __syncthreads();
-  for (int j = 0; j < PD; ++j) {
-    issue_meta(PD + j);
-    cp_async_commit();
-    issue_rows(j);
-    cp_async_commit();
-  }
-
-  for (int t = 0; t < T; ++t) {
-    // Groups newer than rows(t): 2 (PD - 1) from iterations t-PD+1 .. t-1.  record(t+PD)
-    // came in the same iteration as rows(t), before it.
-    cp_async_wait<2 * PD - 2>();
-    __syncthreads();  // rows(t) and record(t+PD) visible; every warp is past token t-1
-    issue_meta(t + MD);
-    cp_async_commit();
-    issue_rows(t + PD);
-    cp_async_commit();
-
-    const unsigned char* mt = meta + (t % QM) * meta_bytes;
-    const int32_t* idx = reinterpret_cast<const int32_t*>(mt);
-    const float* wts = reinterpret_cast<const float*>(mt + L.off_wts);
-    const int16_t* src = reinterpret_cast<const int16_t*>(mt + L.off_src);
-    const float alpha = reinterpret_cast<const float*>(mt + L.off_ab)[0];
-    const float beta = reinterpret_cast<const float*>(mt + L.off_ab)[1];
-    float4 vv[QPW];
-#pragma unroll
-    for (int q = 0; q < QPW; ++q) vv[q] = reinterpret_cast<const float4*>(mt + L.off_v)[q0 + q];
-    float* rs = rows + size_t(t % QR) * WR * C;
-
-    // Forget gate and delta update of the W write rows (in shared memory and in HBM).
-    for (int e = lane; e < W; e += 32) {
-      if (src[e] == -2) continue;
-      const float kb = beta * wts[e];
-      float* Mrow = Mbh + size_t(idx[e]) * d_v;
-#pragma unroll
-      for (int q = 0; q < QPW; ++q) {
-        float4* cell = reinterpret_cast<float4*>(rs + e * C) + q0 + q;
-        const float4 m = *cell;
-        if (wsave) *(reinterpret_cast<float4*>(wsave + (size_t(t) * W + e) * d_v) + q0 + q) = m;
-        float4 r;
-        float mt_;
-        mt_ = alpha * m.x; r.x = fmaf(kb, vv[q].x - mt_, mt_);
-        mt_ = alpha * m.y; r.y = fmaf(kb, vv[q].y - mt_, mt_);
-        mt_ = alpha * m.z; r.z = fmaf(kb, vv[q].z - mt_, mt_);
-        mt_ = alpha * m.w; r.w = fmaf(kb, vv[q].w - mt_, mt_);
-        *cell = r;
-        *(reinterpret_cast<float4*>(Mrow) + q0 + q) = r;
-      }
-    }
-    __syncwarp();
-
-    // Forwarding: rows of tokens t .. t+PD whose latest writer is token t.
-#pragma unroll
-    for (int d = 0; d <= PD; ++d) {
-      const int u = t + d;
-      if (u >= T) break;
-      const unsigned char* mu = meta + (u % QM) * meta_bytes;
-      const int16_t* su = reinterpret_cast<const int16_t*>(mu + L.off_src);
-      float* ru = rows + size_t(u % QR) * WR * C;
-      const int lo = d * W;
-      for (int e = (d == 0 ? W : 0) + lane; e < WR; e += 32) {
-        const int code = su[e];
-        if (code >= lo && code < lo + W) {
-#pragma unroll
-          for (int q = 0; q < QPW; ++q)
-            reinterpret_cast<float4*>(ru + e * C)[q0 + q] =
-                reinterpret_cast<const float4*>(rs + (code - lo) * C)[q0 + q];
-        }
-      }
-    }
-    __syncwarp();
-
-    // Weighted read of the R read rows (after the write): per lane over its rows, then
-    // across the warp.
-    float4 acc[QPW];
-#pragma unroll
-    for (int q = 0; q < QPW; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int e = lane; e < R; e += 32) {
-      if (src[W + e] == -2) continue;
-      const float r = wts[W + e];
-#pragma unroll
-      for (int q = 0; q < QPW; ++q) {
-        const float4 m = reinterpret_cast<const float4*>(rs + (W + e) * C)[q0 + q];
-        if (rsave) *(reinterpret_cast<float4*>(rsave + (size_t(t) * R + e) * d_v) + q0 + q) = m;
-        acc[q].x = fmaf(r, m.x, acc[q].x);
-        acc[q].y = fmaf(r, m.y, acc[q].y);
-        acc[q].z = fmaf(r, m.z, acc[q].z);
-        acc[q].w = fmaf(r, m.w, acc[q].w);
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < QPW; ++q) {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        acc[q].x += __shfl_xor_sync(0xFFFFFFFFu, acc[q].x, off);
-        acc[q].y += __shfl_xor_sync(0xFFFFFFFFu, acc[q].y, off);
-        acc[q].z += __shfl_xor_sync(0xFFFFFFFFu, acc[q].z, off);
-        acc[q].w += __shfl_xor_sync(0xFFFFFFFFu, acc[q].w, off);
-      }
-    }
-    if (lane < QPW) {
-      float4 outv = acc[0];
-#pragma unroll
-      for (int q = 1; q < QPW; ++q)
-        if (lane == q) outv = acc[q];
-      *(reinterpret_cast<float4*>(obh + size_t(t) * d_v) + q0 + lane) = outv;
-    }
-  }
-  cp_async_wait<0>();
-}
-
 size_t scan_smem_bytes(int cols, int pd, int W, int R, int d_v) {
   const RecLayout L = rec_layout(W, R, d_v);
   const size_t meta_bytes = size_t(L.off_v) + 4 * size_t(cols);
@@ -393,11 +222,6 @@ size_t scan_smem_bytes(int cols, int pd, int W, int R, int d_v) {
 using ScanFn = void (*)(ScanArgs);
 
 ScanFn scan_fn(int cols, int pd) {
-  // 32- and 64-column slices: warp-owned column quads (one block barrier per token).
-  if (cols == 32 && pd == 1) return &scan_kernel_wc<32, 1>;
-  if (cols == 32 && pd == 2) return &scan_kernel_wc<32, 2>;
-  if (cols == 64 && pd == 1) return &scan_kernel_wc<64, 1>;
-  if (cols == 64 && pd == 2) return &scan_kernel_wc<64, 2>;
 #define SDM_SCAN_CASE(Cc, Pp) \
   if (cols == Cc && pd == Pp) return &scan_kernel<Cc, Pp>;
   SDM_SCAN_CASE(4, 1) SDM_SCAN_CASE(4, 2) SDM_SCAN_CASE(4, 3)
