@@ -328,60 +328,6 @@ __device__ __noinline__ void sort_desc(Key* buf, int count) {
   __syncwarp();
 }
 
-// Stable descending sort of the n bf16 inner keys in a[] by their 16 value bits (key bits
-// 16..31): two LSD passes of 8 bits, each a counting sort whose equal digits keep their
-// order (a row of 32 keys at a time; lanes with the same digit are ranked by lane).  Keys
-// of equal value therefore stay in their input order.  b: scratch of n keys; cnt: 256
-// counters.  The result is back in a[].
-__device__ void sort_value16_desc(uint32_t* a, int n, uint32_t* b, uint32_t* cnt) {
-  const int lane = threadIdx.x & 31;
-  const unsigned below = (1u << lane) - 1u;
-  for (int pass = 0; pass < 2; ++pass) {
-    const int shift = 16 + 8 * pass;
-    for (int i = lane; i < 256; i += 32) cnt[i] = 0u;
-    __syncwarp();
-    for (int i = lane; i < n; i += 32) atomicAdd(&cnt[(a[i] >> shift) & 255u], 1u);
-    __syncwarp();
-    // cnt[d] <- number of keys with a larger digit (lane l owns digits 255-8l .. 248-8l)
-    uint32_t c[8], s = 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      c[k] = cnt[255 - 8 * lane - k];
-      s += c[k];
-    }
-    uint32_t incl = s;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const uint32_t y = __shfl_up_sync(kFull, incl, off);
-      if (lane >= off) incl += y;
-    }
-    uint32_t run = incl - s;
-    __syncwarp();
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      cnt[255 - 8 * lane - k] = run;
-      run += c[k];
-    }
-    __syncwarp();
-    for (int i0 = 0; i0 < n; i0 += 32) {
-      const int i = i0 + lane;
-      const bool valid = i < n;
-      const uint32_t k = valid ? a[i] : 0u;
-      const unsigned d = valid ? (k >> shift) & 255u : 256u;
-      const unsigned same = __match_any_sync(kFull, d);
-      const int leader = __ffs(same) - 1;
-      uint32_t base = 0;
-      if (valid && lane == leader) base = atomicAdd(&cnt[d], uint32_t(__popc(same)));
-      base = __shfl_sync(kFull, base, leader);
-      if (valid) b[base + __popc(same & below)] = k;
-    }
-    __syncwarp();
-    uint32_t* t = a;
-    a = b;
-    b = t;
-  }
-}
-
 template <typename Key, int EMAX>
 __device__ void sort_desc_upto(Key* buf, int count) {
   if (count <= 32) sort_desc<Key, 1>(buf, count);
@@ -651,12 +597,7 @@ __device__ void select_tasks(const SelectArgs& a, const SelectSmem& m, long long
       // ik is in index order and the low 16 key bits are 0xFFFF - index: equal values
       // are already ranked by position once the value bits are resolved.
       warp_topk_from<IKey>(ik, S, kin, io, hist, IKey(0), InnerKeyOf<Tin>::top_shift, true, 16);
-      // The winners come out as value-range groups, each in index order, so a stable sort by
-      // value gives (value desc, index asc); for bf16 keys two 8-bit counting passes do it.
-      if constexpr (sizeof(IKey) == 4)
-        sort_value16_desc(reinterpret_cast<uint32_t*>(io), kin, reinterpret_cast<uint32_t*>(ik), hist);
-      else
-        sort_desc_upto<IKey, EMAX>(io, kin);
+      sort_desc_upto<IKey, EMAX>(io, kin);
       float* dv = h ? bval : aval;
       int32_t* di = h ? bidx : aidx;
       for (int r = lane; r < kin; r += 32) {
