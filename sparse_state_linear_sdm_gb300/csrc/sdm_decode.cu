@@ -84,11 +84,20 @@ __device__ __forceinline__ void team_bar(int bar, int nth) {
   asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(nth) : "memory");
 }
 
+// How many of a[0..n) are larger than k: four independent counts, so that the loads of a
+// step overlap instead of following each other.
 template <typename Key>
 __device__ __forceinline__ int count_greater(const Key* a, int n, Key k) {
-  int c = 0;
-  for (int j = 0; j < n; ++j) c += a[j] > k ? 1 : 0;
-  return c;
+  int c0 = 0, c1 = 0, c2 = 0, c3 = 0, j = 0;
+  for (; j + 4 <= n; j += 4) {
+    const Key x0 = a[j], x1 = a[j + 1], x2 = a[j + 2], x3 = a[j + 3];
+    c0 += x0 > k ? 1 : 0;
+    c1 += x1 > k ? 1 : 0;
+    c2 += x2 > k ? 1 : 0;
+    c3 += x3 > k ? 1 : 0;
+  }
+  for (; j < n; ++j) c0 += a[j] > k ? 1 : 0;
+  return c0 + c1 + c2 + c3;
 }
 
 // The `need` largest of the n distinct keys in a[] into sel[0..need), in no order; a and b
