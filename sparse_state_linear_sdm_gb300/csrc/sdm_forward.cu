@@ -54,7 +54,7 @@ int pipeline_of_current_device(Pipeline** out) {
     if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return SDM_ECUDA;
     if (cudaStreamCreateWithPriority(&p.init, cudaStreamNonBlocking, greatest) != cudaSuccess ||
         cudaStreamCreateWithPriority(&p.sel, cudaStreamNonBlocking, least) != cudaSuccess ||
-        cudaStreamCreateWithPriority(&p.plan, cudaStreamNonBlocking, least) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&p.plan, cudaStreamNonBlocking, greatest) != cudaSuccess ||
         cudaStreamCreateWithPriority(&p.scan, cudaStreamNonBlocking, greatest) != cudaSuccess)
       return SDM_ECUDA;
     cudaEvent_t* evs[] = {&p.start,        &p.init_done,    &p.plan_end,    &p.scan_done,
