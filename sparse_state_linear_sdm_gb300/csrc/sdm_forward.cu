@@ -8,8 +8,10 @@
 //
 //   init stream (high priority)    M = M_0 broadcast
 //   select stream                  select(0), select(1), ... (full-size outputs: never waits)
-//   plan stream                    plan(c) -> record buffer c % 2, after select(c) and
-//                                  once scan(c - 2) has consumed that buffer
+//   plan stream (high priority)    plan(c) -> record buffer c % 2, after select(c) and
+//                                  once scan(c - 2) has consumed that buffer (at low
+//                                  priority its small grid waited behind the selection's
+//                                  blocks and held up the scans)
 //   scan stream (high priority)    scan(c) over record buffer c % 2, after plan(c)
 //                                  (the first also after the initialisation)
 //
