@@ -446,8 +446,9 @@ def run_ours(args):
         units_launch = units_rank / chunks
         phase = {"scan_ms_per_launch": scan_launch_ms, "scan_ms_per_step": scan_launch_ms * chunks,
                  "chunks": chunks, "tokens_per_chunk": -(-cfg.T // chunks),
-                 "overlap": "sdm_forward: init (high-priority stream) || select+plan of chunk c+1 "
-                            "(select stream) || scan of chunk c (high-priority stream)"}
+                 "overlap": "sdm_forward: init (high-priority stream) || select of chunk c+1 "
+                            "(low-priority stream) then its plan (high-priority stream) || "
+                            "scan of chunk c (high-priority stream)"}
         phase["alone"] = one_stream_breakdown(st, cfg, sdm, args, torch, dev)
         launches_per_step = 1 + 3 * chunks
     else:
