@@ -31,7 +31,7 @@ namespace sdm {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kAutoChunkTokens = 1024;
+constexpr int kAutoChunkTokens = 512;
 constexpr int kMaxChunks = 256;
 
 struct Pipeline {

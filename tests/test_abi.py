@@ -140,9 +140,10 @@ def test_forward_rejects_bad_arguments_without_launching():
 
 def test_forward_chunking_and_workspace_sizes():
     lib = sdm.lib()
-    assert lib.sdm_forward_chunks(8192, 0) == 8      # about 1024 tokens per chunk
+    assert lib.sdm_forward_chunks(8192, 0) == 16     # about 512 tokens per chunk
     assert lib.sdm_forward_chunks(8192, 3) == 3
-    assert lib.sdm_forward_chunks(1000, 0) == 1
+    assert lib.sdm_forward_chunks(1000, 0) == 2
+    assert lib.sdm_forward_chunks(500, 0) == 1
     assert lib.sdm_forward_chunks(5, 8) == 5         # never more chunks than tokens
     assert lib.sdm_forward_chunks(0, 0) == 0
     # one record, W = R = 10 (20 slots), d_v = 16: slots, weights, sources (padded to 8),
