@@ -299,6 +299,19 @@ int sdm_project_kq(const void* x, const void* w, int B, int T, int D, int H, int
 int sdm_project_kq_tuned(const void* x, const void* w, int B, int T, int D, int H, int S,
                          void* kp, void* qp, int* dev_err, int max_ctas, int pair, void* stream);
 
+/* sdm_test_bounded_wait - test of the timeout path of the projection kernel's waits (not
+ * part of the method): one warp waits once, with the same bounded mbarrier wait, on a
+ * barrier of its own:
+ *   mode 0  on a phase that nothing completes: the wait gives up after limit_ns;
+ *   mode 1  on a phase already completed by its own arrival: returns at once;
+ *   mode 2  with the block's stop flag already raised: gives up at once.
+ * When the wait gave up, SDM_DEV_TIMEOUT is OR-ed into *dev_err (device int, required), as
+ * the projection kernel does.  elapsed_ns (device, 8-byte aligned, or NULL) receives the
+ * wait's duration from the global timer.  limit_ns <= 10^9; SDM_EINVAL otherwise.  The
+ * kernel issues no copies, so nothing is left in flight and the context stays usable. */
+int sdm_test_bounded_wait(int mode, unsigned long long limit_ns, int* dev_err,
+                          unsigned long long* elapsed_ns, void* stream);
+
 /* sdm_gen_inputs - synthetic inputs (not part of the method): draws the box
  * b in [b_off, b_off+B), all H heads, tokens t in [t_off, t_off+T) of a logical
  * workload with T_total tokens per sequence, from the counter-based generator

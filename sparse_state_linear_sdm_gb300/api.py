@@ -66,6 +66,7 @@ def lib() -> ctypes.CDLL:
             L.sdm_decode_step.argtypes = [p, p, i, p, i, p, p, p, i, i, i, i, i, i, p, p, p, p, p, p, p]
             L.sdm_decode_step_supported.argtypes = [i, i, i, i, i, i, i]
             L.sdm_project_kq_tuned.argtypes = [p, p, i, i, i, i, i, p, p, p, i, i, p]
+            L.sdm_test_bounded_wait.argtypes = [i, ull, p, p, p]
             for name in ("sdm_init_state_from_M0", "sdm_select", "sdm_scan_forward",
                          "sdm_scan_forward_tuned", "sdm_scan_launch_info", "sdm_gen_inputs", "sdm_gen_M0",
                          "sdm_forward_chunks", "sdm_forward_tuned", "sdm_forward", "sdm_scan_forward_train",
@@ -449,6 +450,19 @@ def project_kq(x, w, H: int, S: int, out=None, dev_err=None, max_ctas: int = 0, 
     _call("sdm_project_kq_tuned", _p(x), _p(w), B, T, D, H, S, _p(kp), _p(qp),
           _p(dev_err) if dev_err is not None else None, int(max_ctas), int(pair), _stream(x.device))
     return kp, qp
+
+
+def bounded_wait_check(mode: int, limit_ns: int, device="cuda"):
+    """Runs one bounded mbarrier wait of the projection kernel's kind on one warp (mode 0: a
+    phase nothing completes, 1: a completed phase, 2: the stop flag already raised) and
+    returns (dev_err, elapsed_ns): the error word it reported (SDM_DEV_TIMEOUT when the wait
+    gave up) and the wait's duration on the global timer.  Synchronises the device."""
+    dev_err = torch.zeros(1, dtype=torch.int32, device=device)
+    elapsed = torch.zeros(1, dtype=torch.int64, device=device)
+    _call("sdm_test_bounded_wait", int(mode), ctypes.c_ulonglong(limit_ns), _p(dev_err), _p(elapsed),
+          _stream(dev_err.device))
+    torch.cuda.synchronize(dev_err.device)
+    return int(dev_err.item()), int(elapsed.item())
 
 
 def decode_step(kp, qp, v, alpha, beta, M, W: int, R: int, out=None, o=None, dev_err=None):

@@ -79,6 +79,14 @@ int sdm_project_kq(const void* x, const void* w, int B, int T, int D, int H, int
   return sdm_project_kq_tuned(x, w, B, T, D, H, S, kp, qp, dev_err, 0, -1, stream);
 }
 
+int sdm_test_bounded_wait(int mode, unsigned long long limit_ns, int* dev_err,
+                          unsigned long long* elapsed_ns, void* stream) {
+  if (mode < 0 || mode > 2 || limit_ns > 1000000000ull || !dev_err) return SDM_EINVAL;
+  if (reinterpret_cast<uintptr_t>(dev_err) & 3u) return SDM_EALIGN;
+  if (elapsed_ns && (reinterpret_cast<uintptr_t>(elapsed_ns) & 7u)) return SDM_EALIGN;
+  return launch_bounded_wait(mode, limit_ns, dev_err, elapsed_ns, as_stream(stream));
+}
+
 size_t sdm_scan_workspace_size(int B, int H, int T, int d_v, int W, int R) {
   if (B < 1 || H < 1 || T < 1 || d_v < 4 || W < 1 || R < 1) return 0;
   return size_t(B) * size_t(H) * size_t(T) * size_t(rec_layout(W, R, d_v).bytes);

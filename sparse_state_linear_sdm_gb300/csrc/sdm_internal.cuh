@@ -166,6 +166,10 @@ int launch_decode(const void* kp, const void* qp, int in_dt, const void* v, int 
                   int* dev_err, cudaStream_t s);
 int launch_project(const void* x, const void* w, int B, int T, int D, int H, int S, void* kp,
                    void* qp, int* dev_err, int max_ctas, int pair, cudaStream_t s);
+// One bounded mbarrier wait of the projection kernel's kind on a single warp (mode 0: never
+// completed, 1: completed, 2: stop flag already up); see sdm_test_bounded_wait.
+int launch_bounded_wait(int mode, unsigned long long limit_ns, int* dev_err,
+                        unsigned long long* elapsed_ns, cudaStream_t s);
 int launch_gen_inputs(unsigned long long seed, int B, int H, int T, int b_off, int t_off,
                       long long T_total, int S, int d_v, int in_dt, float alpha_lo,
                       int beta_kind, const float* half_bias, void* kp, void* qp, void* v,

@@ -103,18 +103,40 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 
 // Waits until the barrier's phase of the given parity has completed.  Returns false when
 // the CTA's stop flag is up or the wait ran past its time limit (then it raises the flag).
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* stop) {
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* stop,
+                          unsigned long long limit_ns = kWaitNs) {
   if (mbar_test(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t i = 1; i < (1u << 28); ++i) {
     if (mbar_test(bar, parity)) return true;
     if ((i & 31u) == 0) {
       if (*stop) return false;
-      if (global_ns() - t0 > kWaitNs) break;
+      if (global_ns() - t0 > limit_ns) break;
     }
   }
   *stop = 1;
   return false;
+}
+
+// One bounded wait of mbar_wait on a barrier of its own, for checking the timeout path
+// without a kernel that can hang: mode 0 waits on a phase that nothing completes (the wait
+// runs out after limit_ns), mode 1 on a phase its own arrival has completed, mode 2 with
+// the stop flag already raised (as when another role of the CTA gave up first).  Like the
+// projection kernel, it reports SDM_DEV_TIMEOUT through dev_err when the stop flag is up at
+// the end.  One warp; no copies or MMAs are issued, so nothing is in flight at exit.
+__global__ void bounded_wait_kernel(int mode, unsigned long long limit_ns, int* dev_err,
+                                    unsigned long long* elapsed_ns) {
+  __shared__ __align__(8) uint64_t bar_mem;
+  __shared__ int stop;
+  if (threadIdx.x != 0) return;
+  const uint32_t bar = smem_u32(&bar_mem);
+  stop = mode == 2 ? 1 : 0;
+  mbar_init(bar, 1);  // initialised, arrived on and waited on by this one thread
+  if (mode == 1) mbar_arrive(bar);
+  const unsigned long long t0 = global_ns();
+  mbar_wait(bar, 0, &stop, limit_ns);
+  if (elapsed_ns) *elapsed_ns = global_ns() - t0;
+  if (stop && dev_err) atomicOr(dev_err, SDM_DEV_TIMEOUT);
 }
 
 // Teardown wait: only the time limit, not the stop flag.
@@ -777,6 +799,12 @@ int launch_project(const void* x, const void* w, int B, int T, int D, int H, int
   cfg.gridDim = dim3(unsigned(clusters * CL));
   void* args[] = {&tmX, &tmW, &pa};
   if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return SDM_ECUDA;
+  return last_launch_status();
+}
+
+int launch_bounded_wait(int mode, unsigned long long limit_ns, int* dev_err,
+                        unsigned long long* elapsed_ns, cudaStream_t s) {
+  bounded_wait_kernel<<<1, 32, 0, s>>>(mode, limit_ns, dev_err, elapsed_ns);
   return last_launch_status();
 }
 

@@ -170,3 +170,15 @@ def test_projection_rejects_bad_arguments_without_launching():
     assert call(None, ok, 1, 4, 64, 1, 4, ok, ok) == EALIGN
     assert call(ok, odd, 1, 4, 64, 1, 4, ok, ok) == EALIGN
     assert call(ok, ok, 1, 4, 64, 1, 4, ok, odd) == EALIGN
+
+
+def test_bounded_wait_check_rejects_bad_arguments_without_launching():
+    L = sdm.lib()
+    ok = ctypes.c_void_p(1 << 20)   # never dereferenced: every call below fails its checks
+    call = lambda mode, limit, err, el=None: L.sdm_test_bounded_wait(mode, limit, err, el, None)
+    assert call(3, 1000, ok) == EINVAL                  # unknown mode
+    assert call(-1, 1000, ok) == EINVAL
+    assert call(0, 10 ** 9 + 1, ok) == EINVAL           # limit above one second
+    assert call(0, 1000, None) == EINVAL                # the error word is required
+    assert call(0, 1000, ctypes.c_void_p((1 << 20) + 2)) == EALIGN
+    assert call(0, 1000, ok, ctypes.c_void_p((1 << 20) + 4)) == EALIGN

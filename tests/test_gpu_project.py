@@ -148,3 +148,24 @@ def test_projection_rejects_bad_arguments():
     w = torch.zeros((4 * 1 * 4, 12), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(sdm.SDMError):
         sdm.project_kq(x, w, 1, 4)
+
+
+def test_bounded_wait_runs_out_and_reports_a_timeout():
+    """The projection kernel's mbarrier wait, on a phase that nothing completes, gives up
+    after its limit and reports SDM_DEV_TIMEOUT; on a completed phase it returns at once
+    without an error; with the block's stop flag already raised it gives up at once.  The
+    context stays usable: a projection afterwards is still correct."""
+    limit = 1_000_000                                        # 1 ms
+    err, ns = sdm.bounded_wait_check(0, limit)
+    assert err == sdm.SDM_DEV_TIMEOUT
+    assert limit <= ns < limit + 200_000_000, ns
+    err, ns = sdm.bounded_wait_check(1, limit)
+    assert err == 0 and ns < limit, (err, ns)
+    err, ns = sdm.bounded_wait_check(2, 500_000_000)         # left by the flag, not the timer
+    assert err == sdm.SDM_DEV_TIMEOUT and ns < 100_000_000, (err, ns)
+    B, T, D, H, S = 1, 64, 64, 1, 32
+    xb, wb = _inputs(5, B, T, D, H, S)
+    kp, qp = _run(xb, wb, H, S)
+    rk, rq, (mk, mq) = oracle.project(wl.bf16_to_f32(xb), wl.bf16_to_f32(wb), H, S)
+    _check(_f32(kp), rk, mk, D, "kp after the timeouts")
+    _check(_f32(qp), rq, mq, D, "qp after the timeouts")
