@@ -7,7 +7,7 @@ the sparse gated-delta scan (planning kernel + scan kernel).  The default
 workload is B=16, H=4, T=8192, N=1,048,576 (S=1024), d_v=128, W=R=128 with bf16
 k', q', v and fp32 state (34 GB).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--seed S] [--impl ours|reference]
 
 With N > 1 (launched by torch.distributed.run) every rank runs its own batch of
 sequences (weak scaling; no collective on the data path).  `--impl reference`
@@ -42,6 +42,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", type=int, default=3)
+    ap.add_argument("--seed", type=int, default=None, help="generator seed (default: the workload's own)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -69,6 +70,8 @@ def workload(args):
     from sparse_state_linear_sdm_gb300 import workloads as wl
 
     cfg = wl.CONFIGS[args.config]
+    if args.seed is not None and args.seed != cfg.seed:
+        cfg = dataclasses.replace(cfg, name=cfg.name + f" (seed {args.seed})", seed=args.seed)
     if args.override:
         kv = dict(item.split("=") for item in args.override.split(","))
         cfg = dataclasses.replace(cfg, name=cfg.name + f" (sizes overridden: {args.override})",
