@@ -37,33 +37,43 @@ _lock = threading.Lock()
 _lib = None
 
 
+def compile_library(src: str, so: str) -> str:
+    """Compile a C++ source of the oracle into a shared library at ``so`` (host code only)."""
+    os.makedirs(os.path.dirname(so), exist_ok=True)
+    tmp = so + f".tmp{os.getpid()}"
+    cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
+           "-o", tmp, src]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, so)
+    return so
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle's C++ into a shared library (host code only)."""
     if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
         return _SO
-    os.makedirs(os.path.dirname(_SO), exist_ok=True)
-    tmp = _SO + f".tmp{os.getpid()}"
-    cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
-           "-o", tmp, _SRC]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, _SO)
-    return _SO
+    return compile_library(_SRC, _SO)
+
+
+def open_library(path: str) -> ctypes.CDLL:
+    """Load a compiled oracle library and declare its entry points."""
+    lib = ctypes.CDLL(path)
+    i64, i32, p = ctypes.c_longlong, ctypes.c_int, ctypes.c_void_p
+    lib.oracle_select.argtypes = [p, i64, i32, i32, p, p, i32]
+    lib.oracle_select.restype = i32
+    lib.oracle_scan.argtypes = [p, i32, i64, i32, i32, i32, i32, p, p, p, p, p, p, p, p, i32]
+    lib.oracle_scan.restype = i32
+    lib.oracle_scan_backward.argtypes = [p, i32, i64, i32, i32, i32, i32, p, p, p, p, p, p, p,
+                                         p, p, p, p, p, p, p, i32]
+    lib.oracle_scan_backward.restype = i32
+    return lib
 
 
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            i64, i32, p = ctypes.c_longlong, ctypes.c_int, ctypes.c_void_p
-            lib.oracle_select.argtypes = [p, i64, i32, i32, p, p, i32]
-            lib.oracle_select.restype = i32
-            lib.oracle_scan.argtypes = [p, i32, i64, i32, i32, i32, i32, p, p, p, p, p, p, p, p, i32]
-            lib.oracle_scan.restype = i32
-            lib.oracle_scan_backward.argtypes = [p, i32, i64, i32, i32, i32, i32, p, p, p, p, p, p, p,
-                                                 p, p, p, p, p, p, p, i32]
-            lib.oracle_scan_backward.restype = i32
-            _lib = lib
+            _lib = open_library(build())
     return _lib
 
 
