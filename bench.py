@@ -156,6 +156,27 @@ def select_roofline(cfg, units: int, select_ms: float, clocks):
         return None
 
 
+PROJECT_SRC = os.path.join(ROOT, "sparse_state_linear_sdm_gb300", "csrc", "sdm_project.cu")
+PROJECT_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "project_kernel_dram_traffic.json")
+
+
+def project_traffic(gemm, args):
+    """DRAM bytes per projection launch from the committed ncu record, when it was taken on
+    this kernel source, this GEMM shape and the default launch shape; else None."""
+    try:
+        with open(PROJECT_TRAFFIC_FILE) as f:
+            rec = json.load(f)
+        with open(PROJECT_SRC, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        if rec.get("source_sha256") != sha or list(rec.get("gemm", [])) != list(gemm):
+            return None
+        if args.max_ctas != 0 or args.pair != -1:
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def traffic_per_launch(units: int):
     """DRAM bytes per scan launch from the committed ncu summary, scaled from its
     captured case by head-tokens; None if absent or taken on another kernel source."""
@@ -826,7 +847,9 @@ def run_project(args):
                        f"{B * T * D * 2 / 1e6:.0f} MB, outputs {2 * B * H * T * 2 * S * 2 / 1e9:.1f} GB)"},
             "roofline": {"kernel": "sdm project_kernel (tcgen05.mma kind::f16, TMA, TMEM)", "bound": "tensor",
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                         "algorithmic_flops_per_launch": flops, "traffic": None,
+                         "algorithmic_flops_per_launch": flops,
+                         "traffic": project_traffic([B * T, 4 * H * S, D], args),
+                         "algorithmic_bytes_per_launch": 2.0 * (B * T * D + 4 * H * S * D + B * T * 4 * H * S),
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"
                          if peak_kind == "measured" else "fallback 1.9 PFLOP/s"},
             "kernel_ms": {"mean": ms, "min": min(per), "max": max(per)},
