@@ -41,7 +41,8 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", type=int, default=3)
+    ap.add_argument("--config", default="3",
+                    help="workload: a name from workloads.CONFIGS or its position (default 3, B16H4-T8192-N1M-dv128-W128)")
     ap.add_argument("--seed", type=int, default=None, help="generator seed (default: the workload's own)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -69,7 +70,7 @@ def workload(args):
 
     from sparse_state_linear_sdm_gb300 import workloads as wl
 
-    cfg = wl.CONFIGS[args.config]
+    cfg = wl.CONFIGS[int(args.config)] if str(args.config).isdigit() else wl.by_name(args.config)
     if args.seed is not None and args.seed != cfg.seed:
         cfg = dataclasses.replace(cfg, name=cfg.name + f" (seed {args.seed})", seed=args.seed)
     if args.override:

@@ -235,16 +235,28 @@ class SDMConfig:
         return self.B * self.H * self.T
 
 
-CONFIGS = [
-    SDMConfig("tiny-B1H1-T64-N1024-dv16-W8", 1, 1, 64, 32, 16, 8, 8, "f32", 0.9, "uniform", False, 0),
-    SDMConfig("B4H8-T2048-N65536-dv64-W32", 4, 8, 2048, 256, 64, 32, 32, "bf16", 0.95, "sigmoid", False, 1),
-    SDMConfig("B8H16-T4096-N262144-dv64-W64-hot", 8, 16, 4096, 512, 64, 64, 64, "bf16", 0.95, "sigmoid",
-              True, 2),
-    SDMConfig("B16H4-T8192-N1M-dv128-W128", 16, 4, 8192, 1024, 128, 128, 128, "bf16", 0.97, "sigmoid",
-              False, 3),
-    SDMConfig("stream-B1H4-T1M-N1M-dv128-W128", 1, 4, 1 << 20, 1024, 128, 128, 128, "bf16", 0.97,
-              "sigmoid", False, 4, chunk=65536),
-]
+TINY_F32 = SDMConfig("tiny-B1H1-T64-N1024-dv16-W8", 1, 1, 64, 32, 16, 8, 8, "f32", 0.9, "uniform",
+                     False, 0)
+B4H8_T2048 = SDMConfig("B4H8-T2048-N65536-dv64-W32", 4, 8, 2048, 256, 64, 32, 32, "bf16", 0.95,
+                       "sigmoid", False, 1)
+B8H16_T4096_HOT = SDMConfig("B8H16-T4096-N262144-dv64-W64-hot", 8, 16, 4096, 512, 64, 64, 64, "bf16",
+                            0.95, "sigmoid", True, 2)
+B16H4_T8192 = SDMConfig("B16H4-T8192-N1M-dv128-W128", 16, 4, 8192, 1024, 128, 128, 128, "bf16", 0.97,
+                        "sigmoid", False, 3)
+STREAM_B1H4_T1M = SDMConfig("stream-B1H4-T1M-N1M-dv128-W128", 1, 4, 1 << 20, 1024, 128, 128, 128, "bf16",
+                            0.97, "sigmoid", False, 4, chunk=65536)
+
+# The workloads in a fixed order (bench.py --config I picks one by position; the seed of
+# each is its position).
+CONFIGS = [TINY_F32, B4H8_T2048, B8H16_T4096_HOT, B16H4_T8192, STREAM_B1H4_T1M]
+
+
+def by_name(name: str) -> SDMConfig:
+    """The workload with this name."""
+    for c in CONFIGS:
+        if c.name == name:
+            return c
+    raise KeyError(name)
 
 
 def half_bias(cfg: SDMConfig):

@@ -130,7 +130,7 @@ def test_forward_train_equals_forward_and_keeps_the_rows():
 def test_backward_on_the_small_workload_sampled_heads():
     """B4 H8 T2048 N=65,536 d_v=64 W=R=32, bf16 inputs: the whole backward on the GPU,
     the oracle on two heads."""
-    cfg = wl.CONFIGS[1]
+    cfg = wl.B4H8_T2048
     d = device_inputs(cfg)
     M0 = device_M0(cfg)
     sel = sdm.select(d["kp"], d["qp"], cfg.W, cfg.R)

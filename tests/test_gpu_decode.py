@@ -15,7 +15,7 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("graph", [False, True])
 def test_decode_steps_equal_one_scan(graph):
-    cfg = wl.CONFIGS[1]
+    cfg = wl.B4H8_T2048
     T = 48
     d = device_inputs(cfg, T=T)
     M0 = device_M0(cfg)
@@ -76,7 +76,7 @@ def test_fused_decode_equals_select_then_scan(B, H, S, dv, W, R, dt, steps):
 
 
 def test_decode_step_graph_uses_one_kernel_and_matches_the_unfused_step():
-    cfg = wl.CONFIGS[1]
+    cfg = wl.B4H8_T2048
     T = 6
     d = device_inputs(cfg, T=T)
     M0 = device_M0(cfg)

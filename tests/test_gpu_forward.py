@@ -29,9 +29,8 @@ def _assert_same(a, b, label):
     assert torch.equal(o1, o2), (label, "o")
 
 
-@pytest.mark.parametrize("ci", [1, 2])
-def test_pipelined_forward_equals_one_stream_path(ci):
-    cfg = wl.CONFIGS[ci]
+@pytest.mark.parametrize("cfg", [wl.B4H8_T2048, wl.B8H16_T4096_HOT], ids=lambda c: c.name)
+def test_pipelined_forward_equals_one_stream_path(cfg):
     d = device_inputs(cfg)
     M0 = device_M0(cfg)
     ref = _run(d, M0, cfg.W, cfg.R, overlap=False)
@@ -65,7 +64,7 @@ def test_pipelined_forward_ragged_and_small(B, H, T, S, dv, W, R, dt, chunks):
 
 def test_pipelined_forward_continues_from_the_state_in_M():
     """M0=None continues from M: two calls over T1 and T2 tokens equal one call over both."""
-    cfg = wl.CONFIGS[1]
+    cfg = wl.B4H8_T2048
     d = device_inputs(cfg)
     M0 = device_M0(cfg)
     o_all, M_all, _ = _run(d, M0, cfg.W, cfg.R, chunks=3)
@@ -78,7 +77,7 @@ def test_pipelined_forward_continues_from_the_state_in_M():
 
 
 def test_pipelined_forward_scan_events_bracket_each_scan_kernel():
-    cfg = wl.CONFIGS[1]
+    cfg = wl.B4H8_T2048
     d = device_inputs(cfg)
     M0 = device_M0(cfg)
     n = sdm.forward_chunks(cfg.T, 4)

@@ -20,11 +20,16 @@ from sdm_testlib import (TOL, check_against_oracle, device_inputs, device_M0, ho
 pytestmark = pytest.mark.gpu
 
 SAMPLED_HEADS = {
-    0: [(0, 0)],
-    1: [(0, 0), (1, 3), (2, 5), (3, 7)],
-    2: [(0, 0), (3, 9), (7, 15)],
-    3: [(0, 0), (15, 3)],
+    wl.TINY_F32.name: [(0, 0)],
+    wl.B4H8_T2048.name: [(0, 0), (1, 3), (2, 5), (3, 7)],
+    wl.B8H16_T4096_HOT.name: [(0, 0), (3, 9), (7, 15)],
+    wl.B16H4_T8192.name: [(0, 0), (15, 3)],
 }
+FULL_SIZE = [wl.TINY_F32, wl.B4H8_T2048, wl.B8H16_T4096_HOT, wl.B16H4_T8192]
+
+
+def _name(cfg):
+    return cfg.name
 
 
 @pytest.fixture(autouse=True)
@@ -34,24 +39,22 @@ def _free_memory():
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("ci", [0, 1, 2, 3])
-def test_device_generator_matches_host(ci):
-    cfg = wl.CONFIGS[ci]
+@pytest.mark.parametrize("cfg", FULL_SIZE, ids=_name)
+def test_device_generator_matches_host(cfg):
     T = min(cfg.T, 256)
     d = device_inputs(cfg, T=T)
-    for b, h in SAMPLED_HEADS[ci]:
+    for b, h in SAMPLED_HEADS[cfg.name]:
         host = wl.inputs(cfg, b, b + 1, h, h + 1, 0, T)
         for k in ("kp", "qp", "v", "alpha", "beta"):
-            assert np.array_equal(to_np(d[k][b, h]), host[k][0, 0]), (ci, k, b, h)
+            assert np.array_equal(to_np(d[k][b, h]), host[k][0, 0]), (cfg.name, k, b, h)
     M0 = device_M0(cfg)
     h, n = cfg.H - 1, min(cfg.N, 4096)
     assert np.array_equal(M0[h, :n].cpu().numpy(), wl.initial_state(cfg, h, h + 1, 0, n)[0])
 
 
-@pytest.mark.parametrize("ci", [0, 1, 2, 3])
-def test_config_end_to_end(ci):
-    cfg = wl.CONFIGS[ci]
-    heads = SAMPLED_HEADS[ci]
+@pytest.mark.parametrize("cfg", FULL_SIZE, ids=_name)
+def test_config_end_to_end(cfg):
+    heads = SAMPLED_HEADS[cfg.name]
     d = device_inputs(cfg)
     M0 = device_M0(cfg)
     dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -182,7 +185,7 @@ def test_scan_on_oracle_selection():
 
 
 def test_invariants_on_gpu():
-    cfg = wl.CONFIGS[1]
+    cfg = wl.B4H8_T2048
     d = device_inputs(cfg, T=512)
     M0 = device_M0(cfg)
     # alpha = 1, beta = 0: the state is bit-identical to M0 afterwards
@@ -199,7 +202,7 @@ def test_invariants_on_gpu():
 
 
 def test_chunked_scan_is_bit_identical():
-    cfg = wl.CONFIGS[2]   # hot slots: forwarding across the chunk boundary matters
+    cfg = wl.B8H16_T4096_HOT   # hot slots: forwarding across the chunk boundary matters
     T = 700
     d = device_inputs(cfg, T=T)
     M0 = device_M0(cfg)
@@ -219,12 +222,11 @@ def test_chunked_scan_is_bit_identical():
     assert torch.equal(o1, o2)
 
 
-@pytest.mark.parametrize("ci", [1, 2])
-def test_forced_shapes_agree(ci):
+@pytest.mark.parametrize("cfg", [wl.B4H8_T2048, wl.B8H16_T4096_HOT], ids=_name)
+def test_forced_shapes_agree(cfg):
     """Every (columns per block, prefetch depth) gives the same state bit for bit
     (the per-row arithmetic does not depend on the shape) and the same outputs up to
     the order of the read reduction."""
-    cfg = wl.CONFIGS[ci]
     T = 400
     d = device_inputs(cfg, T=T)
     M0 = device_M0(cfg)
@@ -300,7 +302,7 @@ def test_overlapped_forward_waits_for_earlier_work_on_the_state():
     """forward(overlap=True) initialises M on a side stream: that stream must first wait for
     work already queued on the caller's stream.  A delayed copy of M queued there must
     still see the finished state, not the next call's initialisation."""
-    cfg = wl.CONFIGS[1]
+    cfg = wl.B4H8_T2048
     d = device_inputs(cfg)
     M0 = device_M0(cfg)
     _, ref, _ = sdm.forward(d["kp"], d["qp"], d["v"], d["alpha"], d["beta"], M0, cfg.W, cfg.R, overlap=False)

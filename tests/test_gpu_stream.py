@@ -19,7 +19,7 @@ from sdm_testlib import TOL, device_M0, scaled_err, to_np
 
 pytestmark = pytest.mark.gpu
 
-CFG = wl.CONFIGS[4]
+CFG = wl.STREAM_B1H4_T1M
 
 
 def _chunk(t_off, T):

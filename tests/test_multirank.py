@@ -27,7 +27,7 @@ def _worker(rank, world, port, out):
         assert bench.dist_env()[:2] == (rank, world)
         ms = 10.0 + 7.0 * rank                     # rank 1 is the slow one
         m = bench.max_over_ranks(ms, "cpu")
-        cfg = wl.CONFIGS[1]
+        cfg = wl.B4H8_T2048
         b0 = bench.rank_batch_offset(rank, cfg.B)
         kp = wl.halves(cfg, wl.FIELD_KP, b0, b0 + 1, 0, 1, 0, 4)
         out[rank] = (m, b0, float(kp.sum()))
@@ -43,7 +43,7 @@ def test_two_ranks_share_max_time_and_disjoint_batches():
     mp.start_processes(_worker, args=(world, _free_port(), out), nprocs=world, start_method="spawn")
     (m0, b00, s0), (m1, b01, s1) = out[0], out[1]
     assert m0 == m1 == 17.0
-    assert (b00, b01) == (0, wl.CONFIGS[1].B)
+    assert (b00, b01) == (0, wl.B4H8_T2048.B)
     assert s0 != s1                                  # different sequences per rank
     # whole-job throughput: both ranks' units over the slowest rank's time
     assert bench.whole_job_rate(1000, 5, world, 17.0) == pytest.approx(2 * 1000 * 5 / 0.017)

@@ -43,7 +43,7 @@ def test_normal_and_uniform_statistics():
 
 
 def test_boxes_are_consistent_slices():
-    cfg = wl.CONFIGS[1]
+    cfg = wl.B4H8_T2048
     full = wl.inputs(cfg, 0, 2, 0, 3, 0, 40)
     part = wl.inputs(cfg, 1, 2, 2, 3, 10, 30)
     for k in full:
@@ -53,12 +53,12 @@ def test_boxes_are_consistent_slices():
 
 
 def test_config_distributions():
-    c0 = wl.CONFIGS[0]
+    c0 = wl.TINY_F32
     inp = wl.inputs(c0)
     assert inp["kp"].shape == (1, 1, 64, 2, 32) and inp["kp"].dtype == np.float32
     assert inp["alpha"].min() > 0.9 and inp["alpha"].max() <= 1.0
     assert inp["beta"].min() > 0 and inp["beta"].max() <= 1.0
-    c2 = wl.CONFIGS[2]
+    c2 = wl.B8H16_T4096_HOT
     x = wl.inputs(c2, 0, 1, 0, 1, 0, 64)
     # bf16 configs hold bf16-exact values; hot bias lifts the low indices
     kp = x["kp"]
@@ -73,7 +73,7 @@ def test_tiny_config_identity_matches_bruteforce():
     """The tiny configuration has fp32 sub-scores, where a rounding merge could in
     principle let topk(topk (+) topk) differ from the top-K of all N scores.  On
     its fixed seed it does not: both agree on every token."""
-    cfg = wl.CONFIGS[0]
+    cfg = wl.TINY_F32
     inp = wl.inputs(cfg)
     for key, K in (("kp", cfg.W), ("qp", cfg.R)):
         i1, s1 = oracle.select(inp[key], K)
