@@ -7,7 +7,8 @@
 // or HBM idle, so the sequence is cut into token chunks and four streams overlap them:
 //
 //   init stream (high priority)    M = M_0 broadcast
-//   select stream                  select(0), select(1), ... (full-size outputs: never waits)
+//   select stream                  the staircase table (once), then select(0), select(1), ...
+//                                  (full-size outputs: never waits)
 //   plan stream (high priority)    plan(c) -> record buffer c % 2, after select(c) and
 //                                  once scan(c - 2) has consumed that buffer (at low
 //                                  priority its small grid waited behind the selection's
@@ -20,6 +21,10 @@
 // its blocks get SM slots ahead of the selection's queue of short blocks.  A chunk boundary is a fresh scan pipeline, exactly as chained calls of
 // sdm_scan_forward: the results are bit-identical to the unpipelined path.
 //
+// The selection blocks read the staircases (the pair-index table of the outer top-K) from a
+// table built once per call at the end of the workspace, instead of each block building its
+// own in shared memory: with a chunk's few tasks per block that build was a noticeable share
+// of the selection.
 // The streams and events are created once per device and reused; calls on one device
 // are enqueued one at a time (a mutex), and the caller's stream waits for all of the
 // call's work before anything enqueued after the call runs.
@@ -94,7 +99,9 @@ extern "C" {
 
 size_t sdm_forward_workspace_size(int B, int H, int T, int d_v, int W, int R, int chunks) {
   if (B < 1 || H < 1 || T < 1 || d_v < 4 || W < 1 || R < 1 || chunks < 0) return 0;
-  return 2 * forward_buffer_bytes(B * H, forward_chunk_tokens(T, chunks), d_v, W, R);
+  // two record buffers, then both staircases (sized for min(K, S) = K, the largest)
+  return 2 * forward_buffer_bytes(B * H, forward_chunk_tokens(T, chunks), d_v, W, R) +
+         (size_t(stair_table_words(W, R, 1 << 20)) * 4 + 255) / 256 * 256;
 }
 
 int sdm_forward_chunks(int T, int chunks) {
@@ -131,6 +138,7 @@ int sdm_forward_tuned(const void* kp, const void* qp, int in_dt, const void* v, 
   const int n = (T + Tc - 1) / Tc;
   const size_t buf = forward_buffer_bytes(BH, Tc, d_v, W, R);
   void* rec[2] = {workspace, static_cast<unsigned char*>(workspace) + buf};
+  uint32_t* stairs = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(workspace) + 2 * buf);
 
   std::lock_guard<std::mutex> lock(g_mu);
   Pipeline* p = nullptr;
@@ -142,6 +150,8 @@ int sdm_forward_tuned(const void* kp, const void* qp, int in_dt, const void* v, 
   SDM_CK(cudaStreamWaitEvent(p->init, p->start, 0));
   SDM_CK(cudaStreamWaitEvent(p->sel, p->start, 0));
   SDM_CK(cudaStreamWaitEvent(p->plan, p->start, 0));
+  st = launch_stair_table(stairs, W, R, S, p->sel);
+  if (st != SDM_OK) return st;
   if (M0) {
     st = launch_init_state(M, M0, B, H, N, d_v, p->init);
     if (st != SDM_OK) return st;
@@ -153,8 +163,8 @@ int sdm_forward_tuned(const void* kp, const void* qp, int in_dt, const void* v, 
     const TokenWindow win{BH, (c + 1) * Tc <= T ? Tc : T - c * Tc, T, c * Tc};
     const int b = c & 1;
     st = in_dt == SDM_BF16
-             ? launch_select_bf16(kp, qp, win, S, W, R, idx_w, sc_w, idx_r, sc_r, p->sel)
-             : launch_select_f32(kp, qp, win, S, W, R, idx_w, sc_w, idx_r, sc_r, p->sel);
+             ? launch_select_bf16(kp, qp, win, S, W, R, idx_w, sc_w, idx_r, sc_r, p->sel, stairs)
+             : launch_select_f32(kp, qp, win, S, W, R, idx_w, sc_w, idx_r, sc_r, p->sel, stairs);
     if (st != SDM_OK) return st;
     SDM_CK(cudaEventRecord(p->sel_done[b], p->sel));
     SDM_CK(cudaStreamWaitEvent(p->plan, p->sel_done[b], 0));

@@ -118,12 +118,15 @@ inline TokenWindow whole_sequences(int BH, int T) { return TokenWindow{BH, T, T,
 // Launchers (host side; arguments already validated by the entry points).
 int launch_init_state(float* M, const float* M0, int B, int H, long long N, int d_v,
                       cudaStream_t s);
+// Both staircases of a (W, R, S) selection into out (stair_table_words 32-bit words).
+int stair_table_words(int W, int R, int S);
+int launch_stair_table(uint32_t* out, int W, int R, int S, cudaStream_t s);
 int launch_select_bf16(const void* kp, const void* qp, const TokenWindow& win, int S, int W,
                        int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r,
-                       cudaStream_t s);
+                       cudaStream_t s, const uint32_t* stair_g = nullptr);
 int launch_select_f32(const void* kp, const void* qp, const TokenWindow& win, int S, int W,
                       int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r,
-                      cudaStream_t s);
+                      cudaStream_t s, const uint32_t* stair_g = nullptr);
 
 // Planning pass of the scan (one record per (b, h, t) of the window into `rec`); `pd` must
 // be the prefetch depth of the scan kernel that consumes the records.

@@ -479,6 +479,8 @@ struct SelectArgs {
   int tpw;            // consecutive tasks per warp (per warp pair in pair mode)
   size_t keys_bytes;  // per-warp key buffer
   bool vec;           // every half starts on a 16-byte boundary
+  const uint32_t* stair_g;  // both staircases prebuilt in device memory (write, then read),
+                            // or nullptr: every block builds them in its shared memory
   int32_t* idx_w;
   float* sc_w;
   int32_t* idx_r;
@@ -540,9 +542,15 @@ struct SelectSmem {
 
 __device__ __forceinline__ SelectSmem select_smem(const SelectArgs& a, unsigned char* smem) {
   SelectSmem m;
-  m.stair_w = reinterpret_cast<uint32_t*>(smem);
-  m.stair_r = m.stair_w + a.cnt_w;
-  m.wbase = smem + (size_t(a.cnt_w + a.cnt_r) * 4 + 15) / 16 * 16;
+  if (a.stair_g) {
+    m.stair_w = const_cast<uint32_t*>(a.stair_g);
+    m.stair_r = m.stair_w + a.cnt_w;
+    m.wbase = smem;
+  } else {
+    m.stair_w = reinterpret_cast<uint32_t*>(smem);
+    m.stair_r = m.stair_w + a.cnt_w;
+    m.wbase = smem + (size_t(a.cnt_w + a.cnt_r) * 4 + 15) / 16 * 16;
+  }
   const size_t per_warp = a.keys_bytes + size_t(a.kpad) * 8 + 256 * 4 + size_t(a.kin_max) * 16;
   m.per_warp = (per_warp + 15) / 16 * 16;
   return m;
@@ -688,7 +696,7 @@ template <typename Tin, int EMAX, bool PAIR>
 __global__ void __launch_bounds__(128) select_kernel(SelectArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const SelectSmem m = select_smem(a, smem);
-  select_build_stairs(a, m);
+  if (!a.stair_g) select_build_stairs(a, m);
   // A short run of consecutive tasks per warp (no persistent grid): blocks that start
   // late, e.g. behind a kernel on another stream, do not hold up the others.
   const long long tasks = a.items * 2;
@@ -733,6 +741,7 @@ void select_args(const void* kp, const void* qp, const TokenWindow& win, int S, 
   a.vec = (S * int(sizeof(Tin))) % 16 == 0;
   a.warps = 0;
   a.tpw = 1;
+  a.stair_g = nullptr;
   *stair_bytes = (size_t(a.cnt_w + a.cnt_r) * 4 + 15) / 16 * 16;
   *per_warp_bytes = select_per_warp_bytes(a.kpad, a.kin_max, S, max(a.cnt_w, a.cnt_r), ikb);
   *out = a;
@@ -740,7 +749,8 @@ void select_args(const void* kp, const void* qp, const TokenWindow& win, int S, 
 
 template <typename Tin>
 int launch_select_t(const void* kp, const void* qp, const TokenWindow& win, int S, int W, int R,
-                    int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, cudaStream_t s) {
+                    int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, cudaStream_t s,
+                    const uint32_t* stair_g) {
   constexpr bool kBf16 = sizeof(Tin) == 2;
   const long long items = (long long)win.BH * win.Tc;
   if (items == 0) return SDM_OK;
@@ -766,7 +776,8 @@ int launch_select_t(const void* kp, const void* qp, const TokenWindow& win, int 
   a.sc_r = sc_r;
   const int ikb = kBf16 ? 4 : 8;
   a.keys_bytes = select_key_bytes(a.kpad, S, max(a.cnt_w, a.cnt_r), ikb);
-  const size_t stair_bytes = (size_t(a.cnt_w + a.cnt_r) * 4 + 15) / 16 * 16;
+  a.stair_g = stair_g;
+  const size_t stair_bytes = stair_g ? 0 : (size_t(a.cnt_w + a.cnt_r) * 4 + 15) / 16 * 16;
   const size_t per_warp = select_per_warp_bytes(a.kpad, a.kin_max, S, max(a.cnt_w, a.cnt_r), ikb);
   int dev = 0, max_smem = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -809,6 +820,13 @@ int launch_select_t(const void* kp, const void* qp, const TokenWindow& win, int 
   if (cudaLaunchKernel(fn, dim3(unsigned(blocks)), dim3(warps * 32), args, smem, s) != cudaSuccess)
     return SDM_ECUDA;
   return last_launch_status();
+}
+
+// Both staircases into out: the write staircase, then the read staircase (one block).
+__global__ void stair_table_kernel(uint32_t* out, int W, int R, int S) {
+  __shared__ int tmp[32];
+  build_stair(out, W, min(W, S), tmp);
+  build_stair(out + stair_count(W, min(W, S)), R, min(R, S), tmp);
 }
 
 }  // namespace

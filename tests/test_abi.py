@@ -150,8 +150,14 @@ def test_forward_chunking_and_workspace_sizes():
     # alpha/beta block, v
     rec = 4 * 20 + 4 * 20 + 2 * 24 + 16 + 4 * 16
     assert rec == 288
-    # two record buffers of B*H*ceil(T/chunks) records, each rounded up to 256 bytes
-    assert lib.sdm_forward_workspace_size(2, 3, 100, 16, 10, 10, 4) == 2 * ((6 * 25 * rec + 255) // 256 * 256)
+    # the staircase of the outer top-K: pairs (p, q) of the two inner lists with
+    # (p + 1)(q + 1) <= K (sized for inner lists of K entries); one table for W, one for R
+    stair = sum(1 for p in range(10) for q in range(10) if (p + 1) * (q + 1) <= 10)
+    assert stair == 27
+    # two record buffers of B*H*ceil(T/chunks) records, each rounded up to 256 bytes, then
+    # both staircases (4 bytes per pair) rounded up to 256 bytes
+    assert lib.sdm_forward_workspace_size(2, 3, 100, 16, 10, 10, 4) == \
+        2 * ((6 * 25 * rec + 255) // 256 * 256) + (2 * stair * 4 + 255) // 256 * 256
     assert lib.sdm_forward_workspace_size(1, 1, 0, 16, 4, 4, 0) == 0
 
 
