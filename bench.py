@@ -471,11 +471,12 @@ def run_ours(args):
         units_launch = units_rank / chunks
         phase = {"scan_ms_per_launch": scan_launch_ms, "scan_ms_per_step": scan_launch_ms * chunks,
                  "chunks": chunks, "tokens_per_chunk": -(-cfg.T // chunks),
-                 "overlap": "sdm_forward: init (high-priority stream) || select of chunk c+1 "
-                            "(low-priority stream) then its plan (high-priority stream) || "
-                            "scan of chunk c (high-priority stream)"}
+                 "overlap": "sdm_forward: init (high-priority stream) || staircase table once, then "
+                            "select of chunk c+1 (low-priority stream) then its plan (high-priority "
+                            "stream) || scan of chunk c (high-priority stream)"}
         phase["alone"] = one_stream_breakdown(st, cfg, sdm, args, torch, dev)
-        launches_per_step = 1 + 3 * chunks
+        # init, the staircase table, then select, plan and scan per chunk
+        launches_per_step = 2 + 3 * chunks
     else:
         scan_launch_ms = sum(e[3].elapsed_time(e[4]) for e in kern_ev) / K
         units_launch = units_rank
