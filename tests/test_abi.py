@@ -111,10 +111,31 @@ def test_init_and_gen_reject_bad_arguments():
 
 
 def test_api_requires_cuda_tensors():
+    """Every entry point of the binding refuses host tensors before doing anything: there is
+    no CPU path to fall back to."""
     import torch
-    x = torch.zeros(1, 1, 4, 2, 8)
-    with pytest.raises(TypeError):
-        sdm.select(x, x, 4, 4)
+    B, H, T, S, dv, W, R = 1, 1, 4, 8, 8, 4, 4
+    kp = torch.zeros(B, H, T, 2, S)
+    v = torch.zeros(B, H, T, dv)
+    ab = torch.zeros(B, H, T)
+    M = torch.zeros(B, H, S * S, dv)
+    M0 = torch.zeros(H, S * S, dv)
+    iw = torch.zeros(B, H, T, W, dtype=torch.int32)
+    sw = torch.zeros(B, H, T, W)
+    calls = [
+        lambda: sdm.select(kp, kp, W, R),
+        lambda: sdm.init_state_from_M0(M, M0),
+        lambda: sdm.scan_forward(M, iw, sw, iw, sw, v, ab, ab),
+        lambda: sdm.forward(kp, kp, v, ab, ab, M0, W, R),
+        lambda: sdm.forward(kp, kp, v, ab, ab, M0, W, R, overlap=False),
+        lambda: sdm.decode_step(kp[:, :, :1], kp[:, :, :1], v[:, :, :1], ab[:, :, :1], ab[:, :, :1], M, W, R),
+        lambda: sdm.project_kq(torch.zeros(B, T, 16, dtype=torch.bfloat16),
+                               torch.zeros(4 * H * S, 16, dtype=torch.bfloat16), H, S),
+        lambda: sdm.select_backward(iw, sw, S),
+    ]
+    for call in calls:
+        with pytest.raises(TypeError, match="must be a CUDA tensor"):
+            call()
 
 
 def test_forward_rejects_bad_arguments_without_launching():
