@@ -60,8 +60,8 @@ def parse_args():
                          "project: the projections x -> k', q' on the tensor cores")
     ap.add_argument("--dmodel", type=int, default=0, help="feature width D of --mode project (0 = 2048)")
     ap.add_argument("--max-ctas", type=int, default=0, help="blocks of the projection kernel (0 = one per SM)")
-    ap.add_argument("--pair", type=int, default=-1, choices=[-1, 0, 1, 2],
-                    help="projection kernel: 1 clusters of two blocks sharing weight tiles, 2 two-SM MMA, 0 single blocks, -1 auto")
+    ap.add_argument("--pair", type=int, default=-1, choices=[-1, 0, 2],
+                    help="projection kernel: 2 two-SM MMA, 0 single blocks, -1 auto")
     return ap.parse_args()
 
 

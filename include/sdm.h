@@ -59,8 +59,9 @@ typedef enum { SDM_F32 = 0, SDM_BF16 = 1 } sdm_dtype;
 #define SDM_DEV_TIMEOUT 4     /* a bounded wait inside a kernel ran out; outputs unspecified */
 
 /* Limits of this build (checked on the host, SDM_EUNSUPPORTED beyond them). */
-#define SDM_MAX_S 4096  /* sqrt(N) */
-#define SDM_MAX_K 1024  /* W and R */
+#define SDM_MAX_S 4096   /* sqrt(N) */
+#define SDM_MAX_K 1024   /* W and R */
+#define SDM_MAX_DV 65536 /* d_v of the scan entry points */
 
 /* Human-readable name of a status code (static string). */
 const char* sdm_status_str(int status);
@@ -88,7 +89,8 @@ int sdm_init_state_from_M0(float* M, const float* M0, int B, int H, long long N,
 int sdm_select(const void* kp, const void* qp, int in_dt, int B, int H, int T, int S, int W, int R,
                int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, void* stream);
 
-/* Bytes of device workspace sdm_scan_forward needs for these sizes (0 when T == 0). */
+/* Bytes of device workspace sdm_scan_forward needs for these sizes (0 when T == 0 or a size
+ * is below its minimum; SIZE_MAX when the product does not fit in a size_t). */
 size_t sdm_scan_workspace_size(int B, int H, int T, int d_v, int W, int R);
 
 /* sdm_scan_forward - the recurrent sparse gated-delta scan ("Meccanismo Core"
@@ -103,7 +105,7 @@ size_t sdm_scan_workspace_size(int B, int H, int T, int d_v, int W, int R);
  *   dev_err  device int, may be NULL; SDM_DEV_* bits are OR-ed in.
  * Calls chained on one stream continue one another exactly: running T1 tokens then
  * T2 tokens gives bit-identical results to one call over T1 + T2 tokens.
- * Requires d_v % 4 == 0, d_v >= 4, 1 <= W, R <= SDM_MAX_K, N >= max(W, R). */
+ * Requires d_v % 4 == 0, 4 <= d_v <= SDM_MAX_DV, 1 <= W, R <= SDM_MAX_K, N >= max(W, R). */
 int sdm_scan_forward(float* M, const int32_t* idx_w, const float* sc_w, const int32_t* idx_r,
                      const float* sc_r, const void* v, int v_dt, const float* alpha,
                      const float* beta, int B, int H, int T, long long N, int d_v, int W, int R,
@@ -138,7 +140,10 @@ int sdm_scan_forward_tuned(float* M, const int32_t* idx_w, const float* sc_w,
  * its request path, or a host application that owns no allocator and passes only its
  * input and output buffers).  Same arguments, results and errors as sdm_scan_forward,
  * minus the workspace; the library calls no cudaMalloc/cudaFree or other allocating
- * routine for it.
+ * routine for it.  The host checks run in this order, before anything is launched: the
+ * argument checks of sdm_scan_forward (SDM_EINVAL, SDM_EUNSUPPORTED, SDM_EALIGN), then a
+ * workspace size that does not fit in a size_t (SDM_EUNSUPPORTED), then the scratch
+ * size (SDM_ESCRATCH).
  *   - The planning records go to one fixed scratch of SDM_NOALLOC_SCRATCH_BYTES that lives
  *     in the library's device image: every GPU that loads the library keeps that memory
  *     until the process exits.
@@ -146,7 +151,10 @@ int sdm_scan_forward_tuned(float* M, const int32_t* idx_w, const float* sc_w,
  *     refused with SDM_ESCRATCH before anything is launched; e.g. with d_v = 128 and
  *     W = R = 128 (3,088 bytes per (b, h, t)) up to 21,732 (b, h, t) triples per call.
  *   - The first call on a device looks up the scratch's device address (once per device,
- *     with that device current); make that first call before any stream capture.
+ *     with that device current); make that first call before any stream capture.  The
+ *     address is kept for the life of the process: after a cudaDeviceReset of a device
+ *     the library's device image is loaded anew, so do not call this entry point on that
+ *     device again in the same process.
  *   - All calls on a device share the scratch and each one overwrites what the last left
  *     there (nothing in it needs to start at zero).  Calls whose work overlaps on the GPU
  *     (other streams, other host threads) race on it: keep them ordered, e.g. on one
@@ -290,11 +298,10 @@ int sdm_project_kq(const void* x, const void* w, int B, int T, int D, int H, int
 /* sdm_project_kq_tuned - sdm_project_kq with its launch shape fixed by the caller:
  *   max_ctas  at most this many blocks (0: as many as can be resident, one per SM), to leave
  *             SMs to work running beside it on other streams;
- *   pair      1: blocks run in clusters of two that share each weight tile (each loads half
- *             and multicasts it to both); 2: clusters of two whose MMAs run as one 256-row
- *             tile across both SMs (tcgen05 cta_group::2), each block staging its own rows
- *             of x and half of the weight tile; 0: single blocks; -1: 2 unless B*T <= 128
- *             (then 0).
+ *   pair      2: clusters of two blocks whose MMAs run as one 256-row tile across both SMs
+ *             (tcgen05 cta_group::2), each block staging its own rows of x and half of the
+ *             weight tile; 0: single blocks (128 x 256 tiles); -1: 2 unless B*T <= 128
+ *             (then 0).  Any other value: SDM_EINVAL.
  * Results do not depend on either. */
 int sdm_project_kq_tuned(const void* x, const void* w, int B, int T, int D, int H, int S,
                          void* kp, void* qp, int* dev_err, int max_ctas, int pair, void* stream);

@@ -7,6 +7,7 @@ or a tensor is not on a CUDA device, the call raises.
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 import threading
 
@@ -80,6 +81,37 @@ def library_path() -> str:
     return _build.LIB
 
 
+def _first_cuda_tensor(values):
+    for a in values:
+        if isinstance(a, torch.Tensor):
+            if a.is_cuda:
+                return a
+        elif isinstance(a, (tuple, list)):
+            t = _first_cuda_tensor(a)
+            if t is not None:
+                return t
+        elif isinstance(a, dict):
+            t = _first_cuda_tensor(a.values())
+            if t is not None:
+                return t
+    return None
+
+
+def _on_tensor_device(fn):
+    """Runs fn with the device of its first CUDA tensor argument current, so the library
+    (which launches on the current device and looks up per-device state there) works on
+    the tensors' GPU whatever device the caller had current.  _need then rejects tensors
+    of one call that sit on different devices."""
+    @functools.wraps(fn)
+    def wrapped(*args, **kwargs):
+        t = _first_cuda_tensor(list(args) + list(kwargs.values()))
+        if t is None:
+            return fn(*args, **kwargs)
+        with torch.cuda.device(t.device):
+            return fn(*args, **kwargs)
+    return wrapped
+
+
 def _call(fn: str, *args):
     st = getattr(lib(), fn)(*args)
     if st != 0:
@@ -105,6 +137,9 @@ def _dtype_code(t: torch.Tensor) -> int:
 def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, but the call runs on cuda:{torch.cuda.current_device()}: "
+                         "every tensor of one call must be on the same device")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
@@ -113,6 +148,7 @@ def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
+@_on_tensor_device
 def init_state_from_M0(M: torch.Tensor, M0: torch.Tensor) -> torch.Tensor:
     """M[b, h] = M0[h] for every b.  M: fp32 [B, H, N, d_v]; M0: fp32 [H, N, d_v]."""
     _need(M, "M", torch.float32)
@@ -122,6 +158,7 @@ def init_state_from_M0(M: torch.Tensor, M0: torch.Tensor) -> torch.Tensor:
     return M
 
 
+@_on_tensor_device
 def select(kp: torch.Tensor, qp: torch.Tensor, W: int, R: int, out=None):
     """Top-W slots of k' and top-R slots of q' for every (b, h, t).
 
@@ -157,6 +194,7 @@ def scan_workspace(B, H, T, d_v, W, R, device) -> torch.Tensor:
     return torch.empty(max(16, scan_workspace_size(B, H, T, d_v, W, R)), dtype=torch.uint8, device=device)
 
 
+@_on_tensor_device
 def scan_forward(M, idx_w, sc_w, idx_r, sc_r, v, alpha, beta, o=None, workspace=None,
                  dev_err=None, cols_per_cta: int = 0, prefetch_depth: int = 0, event_after_plan=None,
                  wait_before_scan=None):
@@ -202,6 +240,7 @@ def scan_forward(M, idx_w, sc_w, idx_r, sc_r, v, alpha, beta, o=None, workspace=
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
+@_on_tensor_device
 def scan_forward_noalloc(M, idx_w, sc_w, idx_r, sc_r, v, alpha, beta, o, dev_err=None):
     """scan_forward for callers that cannot allocate device memory where the scan runs.
 
@@ -243,6 +282,7 @@ def scan_launch_info(B: int, H: int, d_v: int, W: int, R: int) -> dict:
                 smem_bytes=vals[3].value)
 
 
+@_on_tensor_device
 def gen_inputs(seed: int, B: int, H: int, T: int, S: int, d_v: int, in_dtype: torch.dtype,
                alpha_lo: float, beta_kind: int, half_bias=None, b_off: int = 0, t_off: int = 0,
                T_total=None, device="cuda", out=None):
@@ -256,26 +296,29 @@ def gen_inputs(seed: int, B: int, H: int, T: int, S: int, d_v: int, in_dtype: to
                    v=torch.empty((B, H, T, d_v), dtype=in_dtype, device=device),
                    alpha=torch.empty((B, H, T), dtype=torch.float32, device=device),
                    beta=torch.empty((B, H, T), dtype=torch.float32, device=device))
-    for k in ("kp", "qp", "v", "alpha", "beta"):
-        if out.get(k) is not None:
-            _need(out[k], k)
-    if half_bias is not None:
-        _need(half_bias, "half_bias", torch.float32, (S,))
     dev = next(t for t in out.values() if t is not None).device
-    _call("sdm_gen_inputs", ctypes.c_ulonglong(seed), B, H, T, b_off, t_off, T_total, S, d_v,
-          SDM_BF16 if in_dtype == torch.bfloat16 else SDM_F32,
-          ctypes.c_float(alpha_lo), int(beta_kind), _p(half_bias), _p(out.get("kp")), _p(out.get("qp")),
-          _p(out.get("v")), _p(out.get("alpha")), _p(out.get("beta")), _stream(dev))
+    with torch.cuda.device(dev):
+        for k in ("kp", "qp", "v", "alpha", "beta"):
+            if out.get(k) is not None:
+                _need(out[k], k)
+        if half_bias is not None:
+            _need(half_bias, "half_bias", torch.float32, (S,))
+        _call("sdm_gen_inputs", ctypes.c_ulonglong(seed), B, H, T, b_off, t_off, T_total, S, d_v,
+              SDM_BF16 if in_dtype == torch.bfloat16 else SDM_F32,
+              ctypes.c_float(alpha_lo), int(beta_kind), _p(half_bias), _p(out.get("kp")), _p(out.get("qp")),
+              _p(out.get("v")), _p(out.get("alpha")), _p(out.get("beta")), _stream(dev))
     return out
 
 
+@_on_tensor_device
 def gen_M0(seed: int, H: int, N: int, d_v: int, scale: float = 0.02, device="cuda", out=None):
     """Synthetic learned initial state M0 = scale * N(0, 1), fp32 [H, N, d_v]."""
     if out is None:
         out = torch.empty((H, N, d_v), dtype=torch.float32, device=device)
-    _need(out, "M0", torch.float32, (H, N, d_v))
-    _call("sdm_gen_M0", ctypes.c_ulonglong(seed), H, N, d_v, ctypes.c_float(scale), _p(out),
-          _stream(out.device))
+    with torch.cuda.device(out.device):
+        _need(out, "M0", torch.float32, (H, N, d_v))
+        _call("sdm_gen_M0", ctypes.c_ulonglong(seed), H, N, d_v, ctypes.c_float(scale), _p(out),
+              _stream(out.device))
     return out
 
 
@@ -304,6 +347,7 @@ def forward_workspace(B: int, H: int, T: int, d_v: int, W: int, R: int, device, 
     return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
 
 
+@_on_tensor_device
 def forward(kp, qp, v, alpha, beta, M0, W: int, R: int, M=None, workspace=None, dev_err=None,
             overlap: bool = True, out=None, o=None, chunks: int = 0, scan_events=None):
     """One SDM forward pass over a batch: state from M0 (or, with M0=None, from the state
@@ -365,6 +409,7 @@ def forward(kp, qp, v, alpha, beta, M0, W: int, R: int, M=None, workspace=None, 
     return o, M, out
 
 
+@_on_tensor_device
 def scan_forward_train(M, idx_w, sc_w, idx_r, sc_r, v, alpha, beta, o=None, workspace=None, dev_err=None):
     """scan_forward that also keeps what scan_backward needs.  Returns (o, w_prev, r_rows):
     w_prev [B,H,T,W,d_v] every write row before its update, r_rows [B,H,T,R,d_v] every read
@@ -389,6 +434,7 @@ def scan_forward_train(M, idx_w, sc_w, idx_r, sc_r, v, alpha, beta, o=None, work
     return o, w_prev, r_rows
 
 
+@_on_tensor_device
 def scan_backward(idx_w, sc_w, idx_r, sc_r, v, alpha, beta, w_prev, r_rows, dO, G, shared_M0: bool = True,
                   workspace=None):
     """Reverse-mode pass of the scan for L = sum_t <dO_t, o_t> + <dM_T, M_T>, slots fixed.
@@ -416,6 +462,7 @@ def scan_backward(idx_w, sc_w, idx_r, sc_r, v, alpha, beta, w_prev, r_rows, dO, 
     return out
 
 
+@_on_tensor_device
 def select_backward(idx, dsc, S: int, out=None):
     """Gradient of the selected scores with respect to the halves: [B,H,T,2,S] fp32."""
     _need(idx, "idx", torch.int32)
@@ -427,14 +474,15 @@ def select_backward(idx, dsc, S: int, out=None):
     return out
 
 
+@_on_tensor_device
 def project_kq(x, w, H: int, S: int, out=None, dev_err=None, max_ctas: int = 0, pair: int = -1):
     """The projections x -> k', q' on the tensor cores: one bf16 GEMM, fp32 accumulation,
     outputs rounded to bf16 in the [B, H, T, 2, S] layout ``select`` reads.
 
     x: [B, T, D] bf16; w: [4*H*S, D] bf16, one row per output column: the k' columns in
     (head, half, index) order, then the q' columns.  max_ctas caps the blocks (0: one per
-    SM); pair 2/1/0/-1: two-SM MMA tiles / clusters of two blocks sharing weight tiles /
-    single blocks / auto (2 unless there is a single row tile).
+    SM); pair 2/0/-1: two-SM MMA tiles / single blocks / auto (2 unless there is a single
+    row tile).
     Returns (kp, qp)."""
     _need(x, "x", torch.bfloat16)
     if x.dim() != 3:
@@ -459,12 +507,14 @@ def bounded_wait_check(mode: int, limit_ns: int, device="cuda"):
     gave up) and the wait's duration on the global timer.  Synchronises the device."""
     dev_err = torch.zeros(1, dtype=torch.int32, device=device)
     elapsed = torch.zeros(1, dtype=torch.int64, device=device)
-    _call("sdm_test_bounded_wait", int(mode), ctypes.c_ulonglong(limit_ns), _p(dev_err), _p(elapsed),
-          _stream(dev_err.device))
+    with torch.cuda.device(dev_err.device):
+        _call("sdm_test_bounded_wait", int(mode), ctypes.c_ulonglong(limit_ns), _p(dev_err), _p(elapsed),
+              _stream(dev_err.device))
     torch.cuda.synchronize(dev_err.device)
     return int(dev_err.item()), int(elapsed.item())
 
 
+@_on_tensor_device
 def decode_step(kp, qp, v, alpha, beta, M, W: int, R: int, out=None, o=None, dev_err=None):
     """One decode token (T = 1) for every (b, h) in a single kernel: selection, planning and
     the gated write and read on M (in place).  kp, qp [B, H, 1, 2, S]; v [B, H, 1, d_v];

@@ -65,7 +65,8 @@ int sdm_decode_step_supported(int in_dt, int B, int H, int S, int d_v, int W, in
 
 int sdm_project_kq_tuned(const void* x, const void* w, int B, int T, int D, int H, int S,
                          void* kp, void* qp, int* dev_err, int max_ctas, int pair, void* stream) {
-  if (B < 1 || T < 1 || H < 1 || S < 1 || D < 8 || D % 8 || max_ctas < 0 || pair < -1 || pair > 2)
+  if (B < 1 || T < 1 || H < 1 || S < 1 || D < 8 || D % 8 || max_ctas < 0 ||
+      (pair != -1 && pair != 0 && pair != 2))
     return SDM_EINVAL;
   if (S > SDM_MAX_S) return SDM_EUNSUPPORTED;
   if (1LL * B * T >= (1LL << 31) || 4LL * H * S >= (1LL << 31)) return SDM_EUNSUPPORTED;
@@ -89,7 +90,8 @@ int sdm_test_bounded_wait(int mode, unsigned long long limit_ns, int* dev_err,
 
 size_t sdm_scan_workspace_size(int B, int H, int T, int d_v, int W, int R) {
   if (B < 1 || H < 1 || T < 1 || d_v < 4 || W < 1 || R < 1) return 0;
-  return size_t(B) * size_t(H) * size_t(T) * size_t(rec_layout(W, R, d_v).bytes);
+  size_t bytes = 0;
+  return scan_workspace_bytes(B, H, T, d_v, W, R, &bytes) ? bytes : SIZE_MAX;
 }
 
 int sdm_scan_forward_tuned(float* M, const int32_t* idx_w, const float* sc_w,

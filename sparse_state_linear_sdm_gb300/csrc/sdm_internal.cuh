@@ -45,7 +45,8 @@ inline int check_scan_args(const float* M, const int32_t* idx_w, const float* sc
                            long long N, int d_v, int W, int R, const float* o) {
   if (B < 1 || H < 1 || T < 0 || N < 1 || d_v < 4 || d_v % 4 || W < 1 || R < 1) return SDM_EINVAL;
   if (bad_dtype(v_dt) || (long long)W > N || (long long)R > N) return SDM_EINVAL;
-  if (W > SDM_MAX_K || R > SDM_MAX_K || N > 0x7FFFFFFFLL) return SDM_EUNSUPPORTED;
+  if (W > SDM_MAX_K || R > SDM_MAX_K || d_v > SDM_MAX_DV || N > 0x7FFFFFFFLL)
+    return SDM_EUNSUPPORTED;
   if ((long long)B * H > 0x7FFFFFFFLL || (long long)T * (W + R) > 0x7FFFFFFFLL) return SDM_EUNSUPPORTED;
   if (!aligned16(M)) return SDM_EALIGN;
   if (T > 0 && (!aligned16(idx_w) || !aligned16(sc_w) || !aligned16(idx_r) || !aligned16(sc_r) ||
@@ -80,6 +81,22 @@ __host__ __device__ inline RecLayout rec_layout(int W, int R, int d_v) {
   L.off_v = L.off_ab + 16;
   L.bytes = L.off_v + 4 * d_v;
   return L;
+}
+
+// Bytes of the scan's record workspace, B * H * T records, computed in 64 bits for sizes
+// that no check has bounded yet (W, R, d_v taken up to INT_MAX).  False when the product
+// does not fit in a size_t.
+inline bool scan_workspace_bytes(int B, int H, int T, int d_v, int W, int R, size_t* out) {
+  const unsigned long long WR = (unsigned long long)W + (unsigned long long)R;
+  const unsigned long long rec = 8 * ((WR + 3) & ~3ull) + 2 * ((WR + 7) & ~7ull) + 16 +
+                                 4 * (unsigned long long)d_v;  // rec_layout(W, R, d_v).bytes
+  unsigned long long n = 0;
+  if (__builtin_mul_overflow((unsigned long long)B, (unsigned long long)H, &n) ||
+      __builtin_mul_overflow(n, (unsigned long long)T, &n) || __builtin_mul_overflow(n, rec, &n) ||
+      n > (unsigned long long)SIZE_MAX)
+    return false;
+  *out = size_t(n);
+  return true;
 }
 
 // Softmax of n scores with one warp (max-subtracted, __expf), written to w[0..n): one exp

@@ -11,7 +11,10 @@
 // loaded keeps SDM_NOALLOC_SCRATCH_BYTES of device memory reserved for it until the
 // process exits.  Host code must not use the array's name as a pointer (on the host it
 // only stands for the symbol); its device address is looked up once per device with
-// cudaGetSymbolAddress, the first time the entry point runs on that device, and cached.
+// cudaGetSymbolAddress, the first time the entry point runs on that device, and cached for
+// the life of the process (a cudaDeviceReset reloads the device image, after which the
+// cached address is stale: the header tells callers not to use this entry point on that
+// device again).
 #include <mutex>
 
 #include "sdm_internal.cuh"
@@ -46,12 +49,18 @@ extern "C" int sdm_scan_forward_noalloc(float* M, const int32_t* idx_w, const fl
                                         int v_dt, const float* alpha, const float* beta, int B,
                                         int H, int T, long long N, int d_v, int W, int R,
                                         float* o, int* dev_err, void* stream) {
-  // Too large for the fixed scratch: refuse before touching anything.
-  if (sdm_scan_workspace_size(B, H, T, d_v, W, R) > size_t(SDM_NOALLOC_SCRATCH_BYTES))
-    return SDM_ESCRATCH;
+  // Every check runs on the host before anything is launched: the arguments as
+  // sdm_scan_forward checks them, then the record bytes against the fixed scratch.
+  int st = sdm::check_scan_args(M, idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, B, H, T, N,
+                                d_v, W, R, o);
+  if (st != SDM_OK) return st;
+  if (dev_err && (reinterpret_cast<uintptr_t>(dev_err) & 3u)) return SDM_EALIGN;
+  size_t need = 0;
+  if (T > 0 && !sdm::scan_workspace_bytes(B, H, T, d_v, W, R, &need)) return SDM_EUNSUPPORTED;
+  if (need > size_t(SDM_NOALLOC_SCRATCH_BYTES)) return SDM_ESCRATCH;
   void* ws = nullptr;
-  if (T > 0 && B >= 1 && H >= 1) {
-    const int st = scratch_address(&ws);
+  if (T > 0) {
+    st = scratch_address(&ws);
     if (st != SDM_OK) return st;
   }
   // The planning kernel writes every record field the scan kernel reads, so nothing in

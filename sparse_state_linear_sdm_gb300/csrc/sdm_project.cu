@@ -12,7 +12,7 @@
 // transpose pass follows.
 //
 // Kernels: persistent, one CTA per SM, K in steps of 64 (one 128-byte swizzle atom of bf16),
-// three launch shapes of the same warp roles:
+// two launch shapes of the same warp roles:
 //   warp 0      TMA producer: X and W tiles, 128-byte swizzled, into a ring of stages in
 //               shared memory
 //   warp 1      TMEM owner (512 columns: two 256-column fp32 accumulators) and MMA issuer
@@ -22,8 +22,6 @@
 //               tcgen05.ld, converts to bf16 and stores 16-byte pieces of the row, while the
 //               other accumulator is filled by the next tile's MMAs
 // (0) single CTAs: 128 x 256 tiles, tcgen05.mma M128 N256, 4 stages of 48 KB;
-// (1) CTA pairs that multicast halves of the shared W tile: the same MMAs, 32 KB per SM
-//     read from L2 per K step instead of 48 KB;
 // (2) the default: CTA pairs whose MMAs form one 256 x 256 tile (tcgen05.mma cta_group::2
 //     M256 N256, issued by the even CTA), each CTA staging only its 128 rows of X and half
 //     of the W tile (6 stages of 32 KB), which halves the operand bytes each SM's shared
@@ -157,17 +155,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// The same box multicast into the shared memory of every CTA of the cluster in cta_mask (same
-// offset), completing on the barrier at the same offset in each of them.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map, int x,
-                                                      int y, uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
 __device__ void pause_ns(unsigned long long ns) {
   const unsigned long long t0 = global_ns();
   for (uint32_t i = 0; i < (1u << 24) && global_ns() - t0 < ns; ++i) {
@@ -195,14 +182,6 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-// Arrives on the barrier at this offset in every CTA of cta_mask once this thread's MMAs are done.
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(cta_mask)
       : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
@@ -291,12 +270,9 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;\nbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
-// CL = 1: each CTA loads its whole W tile.  CL = 2: the two CTAs of a cluster take row tiles
-// 2*mp and 2*mp+1 of the same column tile; each loads one half (128 rows) of the W tile and
-// multicasts it into both CTAs' shared memory, so each SM reads 32 KB instead of 48 KB from
-// L2 per K step.  A stage is refilled only after the MMAs of both CTAs have read it: each
-// MMA thread's commit arrives on the stage's empty barrier in both CTAs.
-template <bool VEC, int CL>
+// Single CTAs: each loads its X rows and its whole W tile per stage; work units are
+// (row tile, column tile) pairs.
+template <bool VEC>
 __global__ void __launch_bounds__(kThreads, 1)
     project_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    ProjArgs a) {
@@ -311,17 +287,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rank = CL == 1 ? 0 : int(cluster_rank());
-  const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
+  const int cid = blockIdx.x, ncl = gridDim.x;
   const int NT = (a.Ncols + BN - 1) / BN;
-  const int MP = ((a.Mrows + BM - 1) / BM + CL - 1) / CL;
+  const int MP = (a.Mrows + BM - 1) / BM;
   const int units = MP * NT;
   const int KB = (a.D + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar(FULL + s), 1);
-      mbar_init(bar(EMPTY + s), CL);  // one commit from the MMA thread of each CTA
+      mbar_init(bar(EMPTY + s), 1);  // the MMA thread's commit
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(ACC_FULL + i), 1);
@@ -342,7 +317,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync_all();  // the peer's barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -355,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = cid; ok && u < units; u += ncl) {
         int mp, n;
         unit_coords(u, MP, NT, mp, n);
-        const int m0 = (mp * CL + rank) * BM, n0 = n * BN;
+        const int m0 = mp * BM, n0 = n * BN;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(bar(EMPTY + stage), phase ^ 1u, stop)) {
             ok = false;
@@ -364,13 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = ring + uint32_t(stage) * STAGE_BYTES;
           mbar_expect_tx(bar(FULL + stage), STAGE_BYTES);
           tma_load_2d(sa, &tmX, kb * BK, m0, bar(FULL + stage));
-          if (CL == 1) {
-            tma_load_2d(sa + A_BYTES, &tmW, kb * BK, n0, bar(FULL + stage));
-            tma_load_2d(sa + A_BYTES + B_BYTES / 2, &tmW, kb * BK, n0 + BN / 2, bar(FULL + stage));
-          } else {
-            tma_load_2d_multicast(sa + A_BYTES + rank * (B_BYTES / 2), &tmW, kb * BK,
-                                  n0 + rank * (BN / 2), bar(FULL + stage), uint16_t(0x3));
-          }
+          tma_load_2d(sa + A_BYTES, &tmW, kb * BK, n0, bar(FULL + stage));
+          tma_load_2d(sa + A_BYTES + B_BYTES / 2, &tmW, kb * BK, n0 + BN / 2, bar(FULL + stage));
           used |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -382,7 +351,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {  // let every copy in flight land before the CTA's shared memory goes away
         for (int s = 0; s < STAGES; ++s)
           if (used & (1u << s)) mbar_wait_teardown(bar(FULL + s), (last_par >> s) & 1u);
-        if (CL > 1) pause_ns(200000);  // copies the peer multicast into this CTA
       }
     }
   } else if (warp == 1) {
@@ -409,10 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < BK / 16; ++kk)
             mma_bf16(d, sw128_desc(sa + kk * 32), sw128_desc(sa + A_BYTES + kk * 32),
                      (kb | kk) != 0);
-          if (CL == 1)
-            mma_commit(bar(EMPTY + stage));
-          else
-            mma_commit_multicast(bar(EMPTY + stage), uint16_t(0x3));
+          mma_commit(bar(EMPTY + stage));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -437,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       int mp, n;
       unit_coords(u, MP, NT, mp, n);
-      const int m = (mp * CL + rank) * BM + row, n0 = n * BN;
+      const int m = mp * BM + row, n0 = n * BN;
       const int b = m / a.T, t = m - b * a.T;
       const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * BN);
 #pragma unroll 1
@@ -460,8 +425,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                  "r"(kTmemCols)
                  : "memory");
   if (threadIdx.x == 0 && *stop && a.dev_err) atomicOr(a.dev_err, SDM_DEV_TIMEOUT);
-  // Neither CTA of a pair leaves while the other may still arrive on its barriers.
-  if (CL > 1) cluster_sync_all();
 }
 
 // ---- 2-SM variant: one tcgen05.mma.cta_group::2 M256 x N256 per K16 for a CTA pair ----
@@ -759,17 +722,15 @@ int launch_project(const void* x, const void* w, int B, int T, int D, int H, int
   CUtensorMap tmX, tmW;
   if (!bf16_tile_map(&tmX, x, int(Mrows), D, BM) || !bf16_tile_map(&tmW, w, int(Ncols), D, BN / 2))
     return SDM_ECUDA;
-  const int mode = pair < 0 ? (MT >= 2 ? 2 : 0) : pair;  // 0 single, 1 multicast pair, 2 2-SM MMA
+  const int mode = pair < 0 ? (MT >= 2 ? 2 : 0) : pair;  // 0 single CTAs, 2 2-SM MMA pairs
+  if (mode != 0 && mode != 2) return SDM_EINVAL;
   const int CL = mode == 0 ? 1 : 2;
   const long long units = ((MT + CL - 1) / CL) * NT;
   const bool vec = (2 * S) % 8 == 0 && aligned16(kp) && aligned16(qp);
-  const void* fn =
-      mode == 2   ? (vec ? reinterpret_cast<const void*>(&project_kernel_2sm<true>)
-                         : reinterpret_cast<const void*>(&project_kernel_2sm<false>))
-      : mode == 1 ? (vec ? reinterpret_cast<const void*>(&project_kernel<true, 2>)
-                         : reinterpret_cast<const void*>(&project_kernel<false, 2>))
-                  : (vec ? reinterpret_cast<const void*>(&project_kernel<true, 1>)
-                         : reinterpret_cast<const void*>(&project_kernel<false, 1>));
+  const void* fn = mode == 2 ? (vec ? reinterpret_cast<const void*>(&project_kernel_2sm<true>)
+                                    : reinterpret_cast<const void*>(&project_kernel_2sm<false>))
+                             : (vec ? reinterpret_cast<const void*>(&project_kernel<true>)
+                                    : reinterpret_cast<const void*>(&project_kernel<false>));
   const int smem = mode == 2 ? kSmemBytes2 : kSmemBytes;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return SDM_ECUDA;

@@ -108,7 +108,7 @@ def test_projection_traffic_record_gated_by_shape_and_launch(tmp_path, monkeypat
     default = types.SimpleNamespace(max_ctas=0, pair=-1)
     assert bench.project_traffic([131072, 16384, 2048], default) == 9.5e9
     assert bench.project_traffic([16384, 16384, 2048], default) is None
-    assert bench.project_traffic([131072, 16384, 2048], types.SimpleNamespace(max_ctas=0, pair=1)) is None
+    assert bench.project_traffic([131072, 16384, 2048], types.SimpleNamespace(max_ctas=0, pair=0)) is None
     assert bench.project_traffic([131072, 16384, 2048], types.SimpleNamespace(max_ctas=76, pair=-1)) is None
     rec["source_sha256"] = "0" * 64
     path.write_text(json.dumps(rec))

@@ -53,7 +53,7 @@ def _run(xb, wb, H, S, max_ctas=0, pair=-1):
     return kp, qp
 
 
-@pytest.mark.parametrize("pair", [0, 1, 2])
+@pytest.mark.parametrize("pair", [0, 2])
 @pytest.mark.parametrize("B,T,D,H,S,max_ctas", [
     (1, 1, 8, 1, 4, 0),          # one token, D < one K block, 16 output columns
     (2, 100, 72, 2, 6, 0),       # 2S % 8 != 0 (column-wise stores), ragged K block
@@ -72,16 +72,17 @@ def test_projection_matches_oracle(B, T, D, H, S, max_ctas, pair):
     _check(_f32(qp), rq, mq, D, ("qp", B, T, D, H, S, max_ctas, pair))
 
 
-def test_pairs_and_single_blocks_agree_bit_for_bit():
-    """Both launch shapes accumulate each output in the same order (K blocks in sequence,
-    the same MMA shape), so their results are identical."""
+def test_block_counts_agree_bit_for_bit():
+    """Every block count accumulates each output in the same order (K blocks in sequence,
+    the same MMA shape), so the results are identical; the same for the 2-SM shape."""
     B, T, D, H, S = 3, 200, 320, 2, 128
     xb, wb = _inputs(99, B, T, D, H, S)
     k1, q1 = _run(xb, wb, H, S, 0, 0)
-    k2, q2 = _run(xb, wb, H, S, 0, 1)
-    k3, q3 = _run(xb, wb, H, S, 6, 1)
+    k2, q2 = _run(xb, wb, H, S, 5, 0)
+    k3, q3 = _run(xb, wb, H, S, 0, 2)
+    k4, q4 = _run(xb, wb, H, S, 6, 2)
     assert torch.equal(k1, k2) and torch.equal(q1, q2)
-    assert torch.equal(k1, k3) and torch.equal(q1, q3)
+    assert torch.equal(k3, k4) and torch.equal(q3, q4)
 
 
 def test_two_sm_tiles_on_few_pairs():

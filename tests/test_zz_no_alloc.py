@@ -76,10 +76,27 @@ def test_noalloc_matches_workspace_scan_on_two_calls(first, second):
 
 def test_noalloc_refuses_problems_beyond_its_scratch():
     f = _entry()
-    fake = ctypes.c_void_p(0x10000)  # never touched: the size check comes first
+    fake = ctypes.c_void_p(0x10000)  # never touched: every check runs on the host first
     B, H, T, dv, W, R = 8, 8, 512, 128, 128, 128
     need = sdm.scan_workspace_size(B, H, T, dv, W, R)
     assert need > SCRATCH_BYTES
     st = f(fake, fake, fake, fake, fake, fake, 1, fake, fake, B, H, T, 1 << 20, dv, W, R, fake, None, None)
     assert st == SDM_ESCRATCH
     assert b"no-allocation scratch" in sdm.lib().sdm_status_str(st)
+
+
+def test_noalloc_python_wrapper_matches_workspace_scan():
+    """The binding's scan_forward_noalloc (argument checks, the device made current for
+    the call) gives the workspace scan's results on two calls in a row."""
+    for k, (B, H, T, S, dv, W, R) in enumerate(((1, 2, 150, 16, 16, 6, 9), (2, 1, 40, 8, 32, 4, 4))):
+        sel, v, alpha, beta, M0 = _problem(200 + k, B, H, T, S, dv, W, R)
+        M_ref = M0[None].repeat(B, 1, 1, 1)
+        o_ref = sdm.scan_forward(M_ref, *sel, v, alpha, beta)
+        M = M0[None].repeat(B, 1, 1, 1)
+        o = torch.full((B, H, T, dv), float("nan"), device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        sdm.scan_forward_noalloc(M, *sel, v, alpha, beta, o, dev_err=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        assert _scaled_err(o, o_ref) <= TOL, f"call {k}: outputs differ"
+        assert _scaled_err(M, M_ref) <= TOL, f"call {k}: final state differs"
