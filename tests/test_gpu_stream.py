@@ -4,8 +4,10 @@ across chunks (constant state, arbitrarily long sequences: "Significato e
 Rivendicazioni" of the Sparse Delta Memory technical summary).
 
 The oracle recomputes one head over the whole first chunk (every output and the final
-state of that head); selection is pure per token, so tokens of the last chunk are checked
-too; properties that hold at any length cover the rest (chunked = unchunked, bit for bit).
+state of that head) and, at depth, over the whole last chunk: started from the GPU's state
+of that head after 983,040 tokens, every output of the last 65,536 tokens and the state
+after the 1,048,576th token are compared; properties that hold at any length cover the
+rest (chunked = unchunked, bit for bit).
 """
 import numpy as np
 import pytest
@@ -46,21 +48,24 @@ def test_stream_generator_chunks_match_the_whole_sequence():
         assert np.array_equal(to_np(d[k][0, 3]), host[k][0, 0]), k
 
 
-def test_stream_first_chunk_against_oracle_and_last_chunk_selection():
+def test_stream_first_and_last_chunk_against_oracle():
     C = CFG.chunk
+    n_chunks = CFG.T // C
     M0 = device_M0(CFG)
     M = torch.empty((1, CFG.H, CFG.N, CFG.d_v), device="cuda")
     sdm.init_state_from_M0(M, M0)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     ws = sdm.scan_workspace(1, CFG.H, C, CFG.d_v, CFG.W, CFG.R, "cuda")
     first = None
-    for c in range(CFG.T // C):
+    for c in range(n_chunks):
         d = _chunk(c * C, C)
         sel = sdm.select(d["kp"], d["qp"], CFG.W, CFG.R)
+        if c == n_chunks - 1:
+            M_deep = M[0, 0].cpu()   # head 0's state after (n_chunks - 1) * C tokens
         o = sdm.scan_forward(M, *sel, d["v"], d["alpha"], d["beta"], workspace=ws, dev_err=err)
         if c == 0:
             first = (o[0, 0].cpu(), M[0, 0].cpu(), sel[0][0, 0].cpu(), sel[2][0, 0].cpu())
-        last = (sel, d)
+        last = (sel, d, o[0, 0].cpu(), M[0, 0].cpu())
     torch.cuda.synchronize()
     assert err.item() == 0
     assert torch.isfinite(M).all()
@@ -75,8 +80,20 @@ def test_stream_first_chunk_against_oracle_and_last_chunk_selection():
     assert scaled_err(o0.numpy(), ref["o"][0]) <= TOL
     assert scaled_err(M00.numpy(), ref["M"][0]) <= TOL
 
-    # selection of the last tokens of the last chunk (pure per token)
-    sel, d = last
+    # head 0 over the whole last chunk, from the GPU's state after (n_chunks - 1) * C tokens
+    sel, d, o_last, M_last = last
+    t0 = (n_chunks - 1) * C
+    host = wl.inputs(CFG, 0, 1, 0, 1, t0, CFG.T)
+    ref = oracle.forward(host["kp"][0], host["qp"][0], host["v"][0], host["alpha"][0], host["beta"][0],
+                         M_deep.numpy()[None], CFG.W, CFG.R)
+    assert np.array_equal(sel[0][0, 0].cpu().numpy(), ref["idx_w"][0])
+    assert np.array_equal(sel[2][0, 0].cpu().numpy(), ref["idx_r"][0])
+    assert np.array_equal(sel[1][0, 0].cpu().numpy(), ref["sc_w"][0])
+    assert np.array_equal(sel[3][0, 0].cpu().numpy(), ref["sc_r"][0])
+    assert scaled_err(o_last.numpy(), ref["o"][0]) <= TOL
+    assert scaled_err(M_last.numpy(), ref["M"][0]) <= TOL
+
+    # selection of the last tokens of another head (pure per token)
     h, n = 2, 64
     kp = wl.halves(CFG, wl.FIELD_KP, 0, 1, h, h + 1, CFG.T - n, CFG.T)[0, 0]
     qp = wl.halves(CFG, wl.FIELD_QP, 0, 1, h, h + 1, CFG.T - n, CFG.T)[0, 0]
