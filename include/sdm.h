@@ -89,6 +89,19 @@ int sdm_init_state_from_M0(float* M, const float* M0, int B, int H, long long N,
 int sdm_select(const void* kp, const void* qp, int in_dt, int B, int H, int T, int S, int W, int R,
                int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, void* stream);
 
+/* sdm_select with the kernel chosen (same results, bit for bit, on every path):
+ *   path 0  automatic: for bf16 halves with S % 8 == 0, S <= 1024 and W, R <= 128 the
+ *           counting selection (one histogram of exact values per half, whose prefix sums
+ *           place every selected key; a half or an outer top-K whose largest values do not
+ *           fit its 256-bin window falls back to the general steps), else the general one;
+ *   path 1  the general selection (radix select on composite keys, then a bitonic sort);
+ *   path 2  the counting selection; SDM_EUNSUPPORTED outside its limits (fp32 halves
+ *           included).
+ * Any other path: SDM_EINVAL.  For tests and measurement. */
+int sdm_select_tuned(const void* kp, const void* qp, int in_dt, int B, int H, int T, int S, int W,
+                     int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, int path,
+                     void* stream);
+
 /* Bytes of device workspace sdm_scan_forward needs for these sizes (0 when T == 0 or a size
  * is below its minimum; SIZE_MAX when the product does not fit in a size_t). */
 size_t sdm_scan_workspace_size(int B, int H, int T, int d_v, int W, int R);

@@ -44,6 +44,7 @@ def lib() -> ctypes.CDLL:
             L.sdm_status_str.restype = ctypes.c_char_p
             L.sdm_init_state_from_M0.argtypes = [p, p, i, i, ll, i, p]
             L.sdm_select.argtypes = [p, p, i, i, i, i, i, i, i, p, p, p, p, p]
+            L.sdm_select_tuned.argtypes = [p, p, i, i, i, i, i, i, i, p, p, p, p, i, p]
             L.sdm_scan_workspace_size.argtypes = [i, i, i, i, i, i]
             L.sdm_scan_workspace_size.restype = sz
             L.sdm_scan_forward.argtypes = [p, p, p, p, p, p, i, p, p, i, i, i, ll, i, i, i, p, p, sz, p, p]
@@ -68,7 +69,7 @@ def lib() -> ctypes.CDLL:
             L.sdm_decode_step_supported.argtypes = [i, i, i, i, i, i, i]
             L.sdm_project_kq_tuned.argtypes = [p, p, i, i, i, i, i, p, p, p, i, i, p]
             L.sdm_test_bounded_wait.argtypes = [i, ull, p, p, p]
-            for name in ("sdm_init_state_from_M0", "sdm_select", "sdm_scan_forward",
+            for name in ("sdm_init_state_from_M0", "sdm_select", "sdm_select_tuned", "sdm_scan_forward",
                          "sdm_scan_forward_tuned", "sdm_scan_launch_info", "sdm_gen_inputs", "sdm_gen_M0",
                          "sdm_forward_chunks", "sdm_forward_tuned", "sdm_forward", "sdm_scan_forward_train",
                          "sdm_scan_backward", "sdm_select_backward"):
@@ -158,12 +159,16 @@ def init_state_from_M0(M: torch.Tensor, M0: torch.Tensor) -> torch.Tensor:
     return M
 
 
+SELECT_AUTO, SELECT_GENERAL, SELECT_COUNTING = 0, 1, 2
+
+
 @_on_tensor_device
-def select(kp: torch.Tensor, qp: torch.Tensor, W: int, R: int, out=None):
+def select(kp: torch.Tensor, qp: torch.Tensor, W: int, R: int, out=None, path: int = SELECT_AUTO):
     """Top-W slots of k' and top-R slots of q' for every (b, h, t).
 
     kp, qp: [B, H, T, 2, S] fp32 or bf16.  Returns (idx_w int32 [B,H,T,W], sc_w fp32,
-    idx_r int32 [B,H,T,R], sc_r fp32), best first."""
+    idx_r int32 [B,H,T,R], sc_r fp32), best first.  path: SELECT_AUTO, or force the
+    general or the counting kernel (the same results, bit for bit)."""
     _need(kp, "kp")
     B, H, T, two, S = kp.shape
     if two != 2:
@@ -180,8 +185,8 @@ def select(kp: torch.Tensor, qp: torch.Tensor, W: int, R: int, out=None):
     _need(sc_w, "sc_w", torch.float32, (B, H, T, W))
     _need(idx_r, "idx_r", torch.int32, (B, H, T, R))
     _need(sc_r, "sc_r", torch.float32, (B, H, T, R))
-    _call("sdm_select", _p(kp), _p(qp), _dtype_code(kp), B, H, T, S, W, R, _p(idx_w), _p(sc_w),
-          _p(idx_r), _p(sc_r), _stream(kp.device))
+    _call("sdm_select_tuned", _p(kp), _p(qp), _dtype_code(kp), B, H, T, S, W, R, _p(idx_w), _p(sc_w),
+          _p(idx_r), _p(sc_r), int(path), _stream(kp.device))
     return idx_w, sc_w, idx_r, sc_r
 
 

@@ -29,15 +29,25 @@ int sdm_init_state_from_M0(float* M, const float* M0, int B, int H, long long N,
   return launch_init_state(M, M0, B, H, N, d_v, as_stream(stream));
 }
 
-int sdm_select(const void* kp, const void* qp, int in_dt, int B, int H, int T, int S, int W, int R,
-               int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, void* stream) {
+int sdm_select_tuned(const void* kp, const void* qp, int in_dt, int B, int H, int T, int S, int W,
+                     int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, int path,
+                     void* stream) {
   const int st = check_select_args(kp, qp, in_dt, B, H, T, S, W, R, idx_w, sc_w, idx_r, sc_r);
-  if (st != SDM_OK || T == 0) return st;
+  if (st != SDM_OK) return st;
+  if (path < kSelectAuto || path > kSelectCounting) return SDM_EINVAL;
+  if (in_dt != SDM_BF16 && path == kSelectCounting) return SDM_EUNSUPPORTED;
+  if (T == 0) return SDM_OK;
   return in_dt == SDM_BF16
              ? launch_select_bf16(kp, qp, whole_sequences(B * H, T), S, W, R, idx_w, sc_w, idx_r,
-                                  sc_r, as_stream(stream))
+                                  sc_r, as_stream(stream), nullptr, path)
              : launch_select_f32(kp, qp, whole_sequences(B * H, T), S, W, R, idx_w, sc_w, idx_r,
                                  sc_r, as_stream(stream));
+}
+
+int sdm_select(const void* kp, const void* qp, int in_dt, int B, int H, int T, int S, int W, int R,
+               int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, void* stream) {
+  return sdm_select_tuned(kp, qp, in_dt, B, H, T, S, W, R, idx_w, sc_w, idx_r, sc_r, kSelectAuto,
+                          stream);
 }
 
 int sdm_decode_step(const void* kp, const void* qp, int in_dt, const void* v, int v_dt,

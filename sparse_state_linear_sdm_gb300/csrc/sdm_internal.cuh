@@ -138,9 +138,13 @@ int launch_init_state(float* M, const float* M0, int B, int H, long long N, int 
 // Both staircases of a (W, R, S) selection into out (stair_table_words 32-bit words).
 int stair_table_words(int W, int R, int S);
 int launch_stair_table(uint32_t* out, int W, int R, int S, cudaStream_t s);
+// Selection kernels of bf16 halves: kSelectAuto = the counting selection where its limits
+// hold, else the general one; kSelectGeneral / kSelectCounting force one (the latter
+// returns SDM_EUNSUPPORTED outside its limits).
+constexpr int kSelectAuto = 0, kSelectGeneral = 1, kSelectCounting = 2;
 int launch_select_bf16(const void* kp, const void* qp, const TokenWindow& win, int S, int W,
                        int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r,
-                       cudaStream_t s, const uint32_t* stair_g = nullptr);
+                       cudaStream_t s, const uint32_t* stair_g = nullptr, int path = kSelectAuto);
 int launch_select_f32(const void* kp, const void* qp, const TokenWindow& win, int S, int W,
                       int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r,
                       cudaStream_t s, const uint32_t* stair_g = nullptr);
