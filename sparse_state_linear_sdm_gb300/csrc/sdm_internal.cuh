@@ -121,6 +121,32 @@ __device__ inline void warp_softmax(const float* __restrict__ s, int n, float* w
   for (int i = lane; i < n; i += 32) w[i] *= inv;
 }
 
+// warp_softmax of n <= 32 * E scores held in registers (lane l holds scores l, l + 32, ...;
+// entries past n are -inf), with the same operations in the same order, so the weights are
+// bit-identical to warp_softmax's.
+template <int E>
+__device__ inline void warp_softmax_regs(const float (&s)[E], int n, float* w) {
+  const int lane = threadIdx.x & 31;
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < E; ++j)
+    if (lane + 32 * j < n) m = fmaxf(m, s[j]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  float z = 0.f, e[E];
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    e[j] = lane + 32 * j < n ? __expf(s[j] - m) : 0.f;
+    if (lane + 32 * j < n) z += e[j];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, off);
+  const float inv = 1.0f / z;
+#pragma unroll
+  for (int j = 0; j < E; ++j)
+    if (lane + 32 * j < n) w[lane + 32 * j] = e[j] * inv;
+}
+
 // Tokens [t0, t0 + Tc) of BH sequences stored with T_total tokens each: per-token
 // arrays ([BH, T_total, ...]) are read and written in place at token bh * T_total + t;
 // planning records are per window, [BH, Tc].
