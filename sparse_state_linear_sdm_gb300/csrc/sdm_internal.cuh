@@ -63,7 +63,8 @@ inline int check_scan_args(const float* M, const int32_t* idx_w, const float* sc
 //   int16 src[WRb]      where the row comes from: -1 = the table in HBM,
 //                       -2 = invalid slot (skipped), d*W + p = row p of the write
 //                       set of token t-d (0 <= d <= prefetch depth)
-//   fp32  alpha, beta, pad, pad
+//   fp32  alpha, beta; int32 forwarding mask (bit d set: a slot of this token takes the
+//         updated row of a write of token t-d); pad
 //   fp32  v[d_v]
 struct RecLayout {
   int WR, WRa, WRb;

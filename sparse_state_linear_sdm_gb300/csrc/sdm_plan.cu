@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(kPlanMaxWarps * 32) plan_kernel(PlanArgs a) {
 
   unsigned char* rec = a.rec + (size_t(bh) * a.T + u) * size_t(a.L.bytes);
   const int me = u - first;  // this token's index in the table
+  int fmask = 0;             // bit d: some slot takes a row written d tokens earlier
   for (int e = lane; e < WR; e += 32) {
     int32_t x = e < W ? a.idx_w[(tok0 + u) * W + e] : a.idx_r[(tok0 + u) * R + (e - W)];
     int code = -1;
@@ -122,12 +123,16 @@ __global__ void __launch_bounds__(kPlanMaxWarps * 32) plan_kernel(PlanArgs a) {
           best_p = pp;
         }
       }
-      if (best_t >= 0) code = (me - best_t) * W + best_p;
+      if (best_t >= 0) {
+        code = (me - best_t) * W + best_p;
+        fmask |= 1 << (me - best_t);
+      }
     }
     reinterpret_cast<int32_t*>(rec)[e] = x;
     reinterpret_cast<int16_t*>(rec + a.L.off_src)[e] = int16_t(code);
   }
   errs = __reduce_or_sync(0xFFFFFFFFu, errs);
+  fmask = __reduce_or_sync(0xFFFFFFFFu, fmask);
   if (errs && lane == 0 && a.dev_err) atomicOr(a.dev_err, errs);
 
   // Weights, gates and v.
@@ -143,7 +148,7 @@ __global__ void __launch_bounds__(kPlanMaxWarps * 32) plan_kernel(PlanArgs a) {
     float* ab = reinterpret_cast<float*>(rec + a.L.off_ab);
     ab[0] = a.alpha[tok0 + u];
     ab[1] = a.beta[tok0 + u];
-    ab[2] = 0.f;
+    reinterpret_cast<int*>(ab)[2] = fmask;
     ab[3] = 0.f;
   }
   float* vr = reinterpret_cast<float*>(rec + a.L.off_v);

@@ -141,6 +141,14 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
     const float beta = reinterpret_cast<const float*>(mt + L.off_ab)[1];
     const float4 vv = reinterpret_cast<const float4*>(mt + L.off_v)[c4];
     float* rs = rows + size_t(t % QR) * WR * C;
+    // Does a slot of tokens t .. t+PD take a row this token writes?  (bit u - t of record u's
+    // forwarding mask; the same answer in every thread.)  Without one, the read rows do not
+    // depend on this token's writes and the forwarding step and its barriers are skipped.
+    int fwd = 0;
+#pragma unroll
+    for (int d = 0; d <= PD; ++d)
+      if (t + d < T)
+        fwd |= (reinterpret_cast<const int*>(meta + ((t + d) % QM) * meta_bytes + L.off_ab)[2] >> d) & 1;
 
     // Forget gate and delta update of the W write rows (in shared memory and in HBM).
     for (int e = tid / LPR; e < W; e += RPP) {
@@ -158,9 +166,10 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
       *cell = r;
       *(reinterpret_cast<float4*>(Mbh + size_t(idx[e]) * d_v) + c4) = r;
     }
-    __syncthreads();
 
     // Forwarding: rows of tokens t .. t+PD whose latest writer is token t.
+    if (fwd) {
+    __syncthreads();
 #pragma unroll
     for (int d = 0; d <= PD; ++d) {
       const int u = t + d;
@@ -180,6 +189,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
       }
     }
     __syncthreads();
+    }
 
     // Weighted read of the R read rows (after the write).
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
