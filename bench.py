@@ -998,6 +998,7 @@ def run_project(args):
             "kernel_ms": {"mean": ms, "min": min(per), "max": max(per)},
             "launch": {"max_ctas": args.max_ctas, "pair": args.pair},
             "gpu_launches": K, "clocks": clk.summary()}
+    line["fused"] = project_select_timing(sdm, torch, x, w, kp, qp, cfg, H, S, K, args.warmup, dev, ms, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         n = 32
@@ -1014,6 +1015,46 @@ def run_project(args):
                                 f"{4 * H * S} columns x D={D}, mean of {reps}"}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def project_select_timing(sdm, torch, x, w, kp, qp, cfg, H, S, K, warmup, dev, project_ms, peak):
+    """The projections fused with the selection (sdm_project_select: k', q' never in device
+    memory) against the unfused pair (sdm_project_kq, then sdm_select on its output), each
+    timed over K launches after `warmup`; the two must give the same slots and scores."""
+    W, R = cfg.W, cfg.R
+    B, T = x.shape[0], x.shape[1]
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    sel = sdm.select(kp, qp, W, R)
+    ws = sdm.project_select_workspace(B, T, H, S, W, R, dev)
+    fused = sdm.project_select(x, w, H, S, W, R, workspace=ws)
+    torch.cuda.synchronize(dev)
+    same = all(torch.equal(a, b) for a, b in zip(fused, sel))
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        evs = [(E(), E()) for _ in range(K)]
+        for a, b in evs:
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize(dev)
+        return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    sel_ms = timed(lambda: sdm.select(kp, qp, W, R, out=sel))
+    fused_ms = timed(lambda: sdm.project_select(x, w, H, S, W, R, out=fused, workspace=ws))
+    kq_bytes = 2 * kp.numel() * kp.element_size()
+    lists_bytes = sdm.lib().sdm_project_select_workspace_size(B, T, H, S, W, R)
+    flops = 2.0 * B * T * x.shape[2] * 4 * H * S
+    return {"project_select_ms": fused_ms, "project_ms": project_ms, "select_ms": sel_ms,
+            "unfused_ms": project_ms + sel_ms, "bit_identical_to_unfused": same,
+            "fused_tflops": flops / (fused_ms / 1e3) / 1e12, "peak_tflops": peak,
+            "kq_bytes_not_written": kq_bytes, "inner_list_bytes": lists_bytes,
+            "note": "fused: one kernel projects on the tensor cores and takes each half's top-k on "
+                    "chip (per-half lists, 4 B per entry, written instead of k' and q'), then the "
+                    "outer top-K kernel; unfused: sdm_project_kq writes k', q' (bf16) and sdm_select "
+                    "reads them back"}
 
 
 def dataclasses_replace(cfg, **kw):

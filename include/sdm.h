@@ -319,6 +319,27 @@ int sdm_project_kq(const void* x, const void* w, int B, int T, int D, int H, int
 int sdm_project_kq_tuned(const void* x, const void* w, int B, int T, int D, int H, int S,
                          void* kp, void* qp, int* dev_err, int max_ctas, int pair, void* stream);
 
+/* sdm_project_select - the projections fused with the selection ("Meccanismo Core" item 2:
+ * the projected k' and q', whose halves are the sub-scores, and the top-k of each half;
+ * "Design IsoFLOP": the projections are linear layers).  The same results as
+ * sdm_project_kq followed by sdm_select on its output, bit for bit, without k' and q' ever
+ * being written to device memory: one kernel computes the projections on the tensor cores
+ * (tcgen05, fp32 accumulation in the same order as sdm_project_kq) and, on chip, rounds each
+ * half to bf16 and takes its top-min(K, S) by (value desc, index asc); a second kernel takes
+ * the outer top-K over each task's two lists.
+ *   x  [B, T, D] bf16, w [4*H*S, D] bf16: as for sdm_project_kq;
+ *   idx_w, sc_w [B, H, T, W]; idx_r, sc_r [B, H, T, R]: written, as by sdm_select.
+ *   workspace  device scratch of at least sdm_project_select_workspace_size(B, T, H, S, W, R)
+ *          bytes (the per-half lists, 4 bytes per entry, and the staircase table), 16-byte
+ *          aligned, contents irrelevant.
+ *   dev_err  device int or NULL: SDM_DEV_TIMEOUT if a wait inside the kernel ran out.
+ * Requires the limits of sdm_project_kq and, for this kernel, S % 128 == 0, S <= 1024 and
+ * W, R <= 128 (SDM_EUNSUPPORTED otherwise); SDM_ENOSPACE for a short workspace. */
+size_t sdm_project_select_workspace_size(int B, int T, int H, int S, int W, int R);
+int sdm_project_select(const void* x, const void* w, int B, int T, int D, int H, int S, int W,
+                       int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r,
+                       void* workspace, size_t workspace_bytes, int* dev_err, void* stream);
+
 /* sdm_test_bounded_wait - test of the timeout path of the projection kernel's waits (not
  * part of the method): one warp waits once, with the same bounded mbarrier wait, on a
  * barrier of its own:

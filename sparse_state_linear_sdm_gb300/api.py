@@ -69,10 +69,13 @@ def lib() -> ctypes.CDLL:
             L.sdm_decode_step_supported.argtypes = [i, i, i, i, i, i, i]
             L.sdm_project_kq_tuned.argtypes = [p, p, i, i, i, i, i, p, p, p, i, i, p]
             L.sdm_test_bounded_wait.argtypes = [i, ull, p, p, p]
+            L.sdm_project_select_workspace_size.argtypes = [i, i, i, i, i, i]
+            L.sdm_project_select_workspace_size.restype = sz
+            L.sdm_project_select.argtypes = [p, p, i, i, i, i, i, i, i, p, p, p, p, p, sz, p, p]
             for name in ("sdm_init_state_from_M0", "sdm_select", "sdm_select_tuned", "sdm_scan_forward",
                          "sdm_scan_forward_tuned", "sdm_scan_launch_info", "sdm_gen_inputs", "sdm_gen_M0",
                          "sdm_forward_chunks", "sdm_forward_tuned", "sdm_forward", "sdm_scan_forward_train",
-                         "sdm_scan_backward", "sdm_select_backward"):
+                         "sdm_scan_backward", "sdm_select_backward", "sdm_project_select"):
                 getattr(L, name).restype = i
             _lib = L
     return _lib
@@ -503,6 +506,43 @@ def project_kq(x, w, H: int, S: int, out=None, dev_err=None, max_ctas: int = 0, 
     _call("sdm_project_kq_tuned", _p(x), _p(w), B, T, D, H, S, _p(kp), _p(qp),
           _p(dev_err) if dev_err is not None else None, int(max_ctas), int(pair), _stream(x.device))
     return kp, qp
+
+
+def project_select_workspace(B: int, T: int, H: int, S: int, W: int, R: int, device) -> torch.Tensor:
+    n = lib().sdm_project_select_workspace_size(B, T, H, S, W, R)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+@_on_tensor_device
+def project_select(x, w, H: int, S: int, W: int, R: int, out=None, workspace=None, dev_err=None):
+    """The projections x -> k', q' fused with the selection: the top-W slots of k' and the
+    top-R slots of q' for every (b, h, t), as select(*project_kq(x, w, H, S), W, R) gives them,
+    without k' and q' in device memory.  x: [B, T, D] bf16; w: [4*H*S, D] bf16.
+    Returns (idx_w, sc_w, idx_r, sc_r)."""
+    _need(x, "x", torch.bfloat16)
+    if x.dim() != 3:
+        raise ValueError("x must be [B, T, D]")
+    B, T, D = x.shape
+    _need(w, "w", torch.bfloat16, (4 * H * S, D))
+    dev = x.device
+    if out is None:
+        out = (torch.empty((B, H, T, W), dtype=torch.int32, device=dev),
+               torch.empty((B, H, T, W), dtype=torch.float32, device=dev),
+               torch.empty((B, H, T, R), dtype=torch.int32, device=dev),
+               torch.empty((B, H, T, R), dtype=torch.float32, device=dev))
+    idx_w, sc_w, idx_r, sc_r = out
+    _need(idx_w, "idx_w", torch.int32, (B, H, T, W))
+    _need(sc_w, "sc_w", torch.float32, (B, H, T, W))
+    _need(idx_r, "idx_r", torch.int32, (B, H, T, R))
+    _need(sc_r, "sc_r", torch.float32, (B, H, T, R))
+    if workspace is None:
+        workspace = project_select_workspace(B, T, H, S, W, R, dev)
+    _need(workspace, "workspace", torch.uint8)
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32)
+    _call("sdm_project_select", _p(x), _p(w), B, T, D, H, S, W, R, _p(idx_w), _p(sc_w), _p(idx_r), _p(sc_r),
+          _p(workspace), workspace.numel(), _p(dev_err), _stream(dev))
+    return idx_w, sc_w, idx_r, sc_r
 
 
 def bounded_wait_check(mode: int, limit_ns: int, device="cuda"):

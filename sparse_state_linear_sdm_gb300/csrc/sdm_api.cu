@@ -73,6 +73,27 @@ int sdm_decode_step_supported(int in_dt, int B, int H, int S, int d_v, int W, in
   return decode_supported(in_dt, B * H, S, d_v, W, R);
 }
 
+size_t sdm_project_select_workspace_size(int B, int T, int H, int S, int W, int R) {
+  if (B < 1 || T < 1 || H < 1 || S < 1 || W < 1 || R < 1) return 0;
+  return project_select_workspace(B, T, H, S, W, R);
+}
+
+int sdm_project_select(const void* x, const void* w, int B, int T, int D, int H, int S, int W,
+                       int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r,
+                       void* workspace, size_t workspace_bytes, int* dev_err, void* stream) {
+  if (B < 1 || T < 1 || H < 1 || S < 1 || D < 8 || D % 8 || W < 1 || R < 1) return SDM_EINVAL;
+  if (1LL * W > 1LL * S * S || 1LL * R > 1LL * S * S) return SDM_EINVAL;
+  if (S % 128 || S > 1024 || W > 128 || R > 128) return SDM_EUNSUPPORTED;
+  if (1LL * B * T >= (1LL << 31) || 4LL * H * S >= (1LL << 31)) return SDM_EUNSUPPORTED;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(idx_w) || !aligned16(sc_w) || !aligned16(idx_r) ||
+      !aligned16(sc_r) || !aligned16(workspace))
+    return SDM_EALIGN;
+  if (dev_err && (reinterpret_cast<uintptr_t>(dev_err) & 3u)) return SDM_EALIGN;
+  if (workspace_bytes < project_select_workspace(B, T, H, S, W, R)) return SDM_ENOSPACE;
+  return launch_project_select(x, w, B, T, D, H, S, W, R, idx_w, sc_w, idx_r, sc_r, workspace,
+                               dev_err, as_stream(stream));
+}
+
 int sdm_project_kq_tuned(const void* x, const void* w, int B, int T, int D, int H, int S,
                          void* kp, void* qp, int* dev_err, int max_ctas, int pair, void* stream) {
   if (B < 1 || T < 1 || H < 1 || S < 1 || D < 8 || D % 8 || max_ctas < 0 ||

@@ -217,6 +217,11 @@ int launch_decode(const void* kp, const void* qp, int in_dt, const void* v, int 
                   int* dev_err, cudaStream_t s);
 int launch_project(const void* x, const void* w, int B, int T, int D, int H, int S, void* kp,
                    void* qp, int* dev_err, int max_ctas, int pair, cudaStream_t s);
+// Projections fused with the inner top-k of every half, then the outer top-K (two kernels).
+size_t project_select_workspace(int B, int T, int H, int S, int W, int R);
+int launch_project_select(const void* x, const void* w, int B, int T, int D, int H, int S, int W,
+                          int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r,
+                          void* workspace, int* dev_err, cudaStream_t s);
 // One bounded mbarrier wait of the projection kernel's kind on a single warp (mode 0: never
 // completed, 1: completed, 2: stop flag already up); see sdm_test_bounded_wait.
 int launch_bounded_wait(int mode, unsigned long long limit_ns, int* dev_err,

@@ -33,6 +33,7 @@
 // every role leaves its loop, outstanding copies and MMAs are waited for (bounded), TMEM
 // is freed and SDM_DEV_TIMEOUT is reported through dev_err.
 #include "sdm_internal.cuh"
+#include "sdm_select_count.cuh"
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -701,6 +702,319 @@ int sm_count() {
   return n;
 }
 
+
+// ---- projection fused with the inner top-k of every half ----------------------------------
+//
+// "Meccanismo Core" item 2 of the same summary takes the top-k of each half of k' and q';
+// here they are taken on chip, straight from the projection's accumulators, so k' and q'
+// never reach HBM: only each half's top-kin list (kin = min(W or R, S) packed entries,
+// bf16 value << 16 | index) is written, and the outer top-K over the lists' staircase runs
+// in a second kernel (outer_kernel below).
+//
+// Transposed tiles: a work unit is (a block of FT = 64 tokens, one half g), g = (which * H +
+// h) * 2 + half, whose S sub-scores are rows [g*S, g*S + S) of W.  The unit's S x 64 outputs
+// (sub-scores x tokens) accumulate in TMEM, M-tile mt (128 sub-scores, the MMA's M) in
+// columns [64 mt, 64 mt + 64) (S = 1024 fills all 512 columns), so a token's whole half is on
+// chip when the K loop ends.  Per K step of 64 the X tile (64 tokens x 64, the MMA's B) is
+// loaded once and used by the S/128 MMAs (M128 N64 K16 x 4) of the step; the W tiles stream
+// through their own ring.  The epilogue warps then read the accumulators in groups of FG = 8
+// tokens, round them to bf16 (nearest even, as the unfused kernel stores them) into a
+// staging buffer [8][S] in shared memory, and select each token's top-kin there with the
+// counting selection (inner_count_smem; the general path on its rare fallback), two tokens
+// per warp.  The accumulation order of every output is the unfused kernel's (K blocks in
+// sequence, the same MMA K steps), so the lists are those of sdm_select on sdm_project_kq's
+// output.  The MMAs of the next unit wait until the epilogue has read the accumulators.
+constexpr int FT = 64;                    // tokens per unit (the MMA's N)
+constexpr int FG = 8;                     // tokens per epilogue group
+constexpr int F_A_BYTES = 128 * BK * 2;   // 16 KB: W tile (128 sub-scores x 64)
+constexpr int F_B_BYTES = FT * BK * 2;    // 8 KB: X tile (64 tokens x 64)
+constexpr int F_ASTAGES = 6, F_BSTAGES = 3;
+constexpr int F_EPI_WARPS = 4;
+constexpr uint32_t kIdescF = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(FT >> 3) << 17) |
+                             (uint32_t(128 >> 4) << 24);
+// barriers: a_full, a_empty, b_full, b_empty, acc_full, tmem_empty, drain
+constexpr int F_NUM_BARS = 2 * F_ASTAGES + 2 * F_BSTAGES + 3;
+
+struct FusedArgs {
+  int Mrows, D, T, H, S, W, R;
+  int kp_stride;       // entries per list (max(min(W, S), min(R, S)))
+  int units;           // token blocks x 4H halves
+  size_t sel_per_warp; // bytes of one selecting warp's region
+  size_t sel_keys_bytes;
+  int sel_kpad;
+  uint32_t* lists;     // [B*T][H][2][2][kp_stride]: (b, h, t, which, half)
+  int* dev_err;
+};
+
+__device__ __forceinline__ void mma_bf16_f(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %3, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %4, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(accumulate), "r"(kIdescF)
+      : "memory");
+}
+
+// 8 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_load8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void epi_barrier() {  // the four epilogue warps
+  asm volatile("bar.sync 1, %0;" ::"n"(F_EPI_WARPS * 32) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    project_select_kernel(const __grid_constant__ CUtensorMap tmX,
+                          const __grid_constant__ CUtensorMap tmW, FusedArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t ring = (raw + 1023u) & ~1023u;  // tiles on 1,024-byte swizzle atoms
+  const uint32_t a_ring = ring, b_ring = ring + F_ASTAGES * F_A_BYTES;
+  unsigned char* gen = smem_raw + (ring - raw) + F_ASTAGES * F_A_BYTES + F_BSTAGES * F_B_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gen);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + F_NUM_BARS);
+  volatile int* stop = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* epi_ok = reinterpret_cast<int*>(tmem_slot + 2);   // [F_EPI_WARPS]
+  uint16_t* staging = reinterpret_cast<uint16_t*>(gen + 256);  // [FG][S]
+  unsigned char* selw = gen + 256 + size_t(FG) * a.S * 2;      // per selecting warp
+  const int AF = 0, AE = F_ASTAGES, BF = 2 * F_ASTAGES, BE = 2 * F_ASTAGES + F_BSTAGES,
+            ACC_FULL = 2 * F_ASTAGES + 2 * F_BSTAGES, TMEM_EMPTY = ACC_FULL + 1, DRAIN = ACC_FULL + 2;
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = a.S, MT = S / 128, KB = (a.D + BK - 1) / BK, halves = 4 * a.H;
+  const uint32_t tmem_cols = MT * FT <= 32 ? 32u : uint32_t(MT * FT);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < F_ASTAGES; ++i) {
+      mbar_init(bar(AF + i), 1);
+      mbar_init(bar(AE + i), 1);
+    }
+    for (int i = 0; i < F_BSTAGES; ++i) {
+      mbar_init(bar(BF + i), 1);
+      mbar_init(bar(BE + i), 1);
+    }
+    mbar_init(bar(ACC_FULL), 1);
+    mbar_init(bar(TMEM_EMPTY), F_EPI_WARPS);
+    mbar_init(bar(DRAIN), 1);
+    *stop = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- TMA producer: per K step the X tile, then the MT W tiles ----
+      int as = 0, bs = 0;
+      uint32_t aph = 0, bph = 0, a_used = 0, a_par = 0, b_used = 0, b_par = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
+        const int tb = u / halves, g = u - tb * halves;
+        for (int kb = 0; ok && kb < KB; ++kb) {
+          if (!mbar_wait(bar(BE + bs), bph ^ 1u, stop)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(bar(BF + bs), F_B_BYTES);
+          tma_load_2d(b_ring + uint32_t(bs) * F_B_BYTES, &tmX, kb * BK, tb * FT, bar(BF + bs));
+          b_used |= 1u << bs;
+          b_par = (b_par & ~(1u << bs)) | (bph << bs);
+          if (++bs == F_BSTAGES) {
+            bs = 0;
+            bph ^= 1u;
+          }
+          for (int mt = 0; mt < MT; ++mt) {
+            if (!mbar_wait(bar(AE + as), aph ^ 1u, stop)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(bar(AF + as), F_A_BYTES);
+            tma_load_2d(a_ring + uint32_t(as) * F_A_BYTES, &tmW, kb * BK, g * S + mt * 128, bar(AF + as));
+            a_used |= 1u << as;
+            a_par = (a_par & ~(1u << as)) | (aph << as);
+            if (++as == F_ASTAGES) {
+              as = 0;
+              aph ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) {  // let every copy in flight land before the CTA's shared memory goes away
+        for (int i = 0; i < F_ASTAGES; ++i)
+          if (a_used & (1u << i)) mbar_wait_teardown(bar(AF + i), (a_par >> i) & 1u);
+        for (int i = 0; i < F_BSTAGES; ++i)
+          if (b_used & (1u << i)) mbar_wait_teardown(bar(BF + i), (b_par >> i) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer ----
+      int as = 0, bs = 0, it = 0;
+      uint32_t aph = 0, bph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x, ++it) {
+        if (!mbar_wait(bar(TMEM_EMPTY), (uint32_t(it) & 1u) ^ 1u, stop)) break;
+        tc_fence_after();
+        for (int kb = 0; ok && kb < KB; ++kb) {
+          if (!mbar_wait(bar(BF + bs), bph, stop)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sb = b_ring + uint32_t(bs) * F_B_BYTES;
+          for (int mt = 0; mt < MT; ++mt) {
+            if (!mbar_wait(bar(AF + as), aph, stop)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = a_ring + uint32_t(as) * F_A_BYTES;
+            const uint32_t d = tmem_base + uint32_t(mt * FT);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              mma_bf16_f(d, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), (kb | kk) != 0);
+            mma_commit(bar(AE + as));
+            if (++as == F_ASTAGES) {
+              as = 0;
+              aph ^= 1u;
+            }
+          }
+          if (!ok) break;
+          mma_commit(bar(BE + bs));
+          if (++bs == F_BSTAGES) {
+            bs = 0;
+            bph ^= 1u;
+          }
+        }
+        if (ok) mma_commit(bar(ACC_FULL));
+      }
+      mma_commit(bar(DRAIN));
+      mbar_wait_teardown(bar(DRAIN), 0);
+    }
+  } else {
+    // ---- epilogue and selection: warp q reads TMEM lanes 32q .. 32q+31 ----
+    const int q = warp & 3;         // TMEM lane quadrant of this warp
+    const int sw = warp - 2;        // 0..3: this warp's selecting slot
+    const CountSmem m = count_smem(selw + a.sel_per_warp * sw, a.sel_keys_bytes, a.sel_kpad,
+                                   a.kp_stride);
+    int it = 0;
+    for (int u = blockIdx.x; u < a.units; u += gridDim.x, ++it) {
+      // The four warps agree on whether the accumulators are ready (each waits; any that gave
+      // up makes all leave), so no warp is left behind at a named barrier.
+      const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(bar(ACC_FULL), uint32_t(it) & 1u, stop));
+      if (lane == 0) epi_ok[sw] = got ? 1 : 0;
+      epi_barrier();
+      const bool all = epi_ok[0] && epi_ok[1] && epi_ok[2] && epi_ok[3];
+      epi_barrier();
+      if (!all) break;
+      tc_fence_after();
+      const int tb = u / halves, g = u - tb * halves;
+      const int which = g / (2 * a.H), h = (g >> 1) % a.H, half = g & 1;
+      const int kin = min(which ? a.R : a.W, S);
+#pragma unroll 1
+      for (int grp = 0; grp < FT / FG; ++grp) {
+        // tokens grp*8 .. grp*8+7 of the block: this warp's 32 sub-scores of every M-tile
+#pragma unroll 1
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t r[8];
+          tmem_load8(tmem_base + (uint32_t(q * 32) << 16) + uint32_t(mt * FT + grp * FG), r);
+          const int col = mt * 128 + q * 32 + lane;
+#pragma unroll
+          for (int n = 0; n < FG; ++n) {
+            const __nv_bfloat16 v = __float2bfloat16_rn(__uint_as_float(r[n]));
+            staging[n * S + col] = *reinterpret_cast<const uint16_t*>(&v);
+          }
+        }
+        epi_barrier();
+#pragma unroll 1
+        for (int n = sw; n < FG; n += F_EPI_WARPS) {
+          const int mrow = tb * FT + grp * FG + n;  // token b*T + t
+          if (mrow < a.Mrows) {
+            const uint16_t* row = staging + n * S;
+            uint32_t* lst = m.la;
+            if (!inner_count_smem(row, S, kin, m, lst)) inner_general_smem(row, S, kin, m, lst);
+            const int b = mrow / a.T, t = mrow - b * a.T;
+            uint32_t* dst = a.lists + ((((size_t(b) * a.H + h) * a.T + t) * 2 + which) * 2 + half) *
+                                          size_t(a.kp_stride);
+            for (int i = lane; i < kin; i += 32) dst[i] = lst[i];
+            __syncwarp();
+          }
+        }
+        epi_barrier();  // the staging buffer is free again
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(TMEM_EMPTY));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(tmem_cols)
+                 : "memory");
+  if (threadIdx.x == 0 && *stop && a.dev_err) atomicOr(a.dev_err, SDM_DEV_TIMEOUT);
+}
+
+// Outer top-K of every (b, h, t, k' or q') task from the inner lists (one warp per task).
+struct OuterArgs {
+  const uint32_t* lists;
+  long long items;  // B * H * T
+  int S, W, R, kp_stride;
+  int cnt_w, cnt_r, kpad, warps;
+  size_t per_warp, keys_bytes;
+  const uint32_t* stair;  // both staircases (write, then read)
+  int32_t* idx_w;
+  float* sc_w;
+  int32_t* idx_r;
+  float* sc_r;
+};
+
+__global__ void __launch_bounds__(128, 6) outer_kernel(OuterArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long task = (long long)blockIdx.x * a.warps + warp;
+  if (task >= 2 * a.items) return;
+  const CountSmem m = count_smem(smem + a.per_warp * warp, a.keys_bytes, a.kpad, a.kp_stride);
+  const int which = int(task & 1);
+  const long long item = task >> 1;  // (b * H + h) * T + t
+  const int K = which ? a.R : a.W, kin = min(K, a.S);
+  const uint32_t* src = a.lists + (size_t(item) * 2 + which) * 2 * size_t(a.kp_stride);
+  for (int i = lane; i < kin; i += 32) {
+    m.la[i] = src[i];
+    m.lb[i] = src[a.kp_stride + i];
+  }
+  __syncwarp();
+  outer_task(m, which ? a.stair + a.cnt_w : a.stair, which ? a.cnt_r : a.cnt_w, K, kin, a.S,
+             a.kpad, (which ? a.idx_r : a.idx_w) + item * K, (which ? a.sc_r : a.sc_w) + item * K);
+}
+
+// Bytes of the lists region of the fused projection's workspace.
+size_t fused_lists_bytes(int B, int T, int H, int S, int W, int R) {
+  const size_t kp = size_t(max(min(W, S), min(R, S)));
+  return (size_t(B) * T * H * 4 * kp * 4 + 255) / 256 * 256;
+}
+
 }  // namespace
 
 int launch_project(const void* x, const void* w, int B, int T, int D, int H, int S, void* kp,
@@ -760,6 +1074,93 @@ int launch_project(const void* x, const void* w, int B, int T, int D, int H, int
   cfg.gridDim = dim3(unsigned(clusters * CL));
   void* args[] = {&tmX, &tmW, &pa};
   if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return SDM_ECUDA;
+  return last_launch_status();
+}
+
+size_t project_select_workspace(int B, int T, int H, int S, int W, int R) {
+  return fused_lists_bytes(B, T, H, S, W, R) +
+         (size_t(stair_table_words(W, R, S)) * 4 + 255) / 256 * 256;
+}
+
+int launch_project_select(const void* x, const void* w, int B, int T, int D, int H, int S, int W,
+                          int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r,
+                          void* workspace, int* dev_err, cudaStream_t s) {
+  const long long Mrows = 1LL * B * T;
+  if (Mrows == 0) return SDM_OK;
+  if (S % 128 || S > kCountMaxS || W > kCountMaxK || R > kCountMaxK) return SDM_EUNSUPPORTED;
+  const long long blocks_t = (Mrows + FT - 1) / FT;
+  if (blocks_t * 4 * H > 0x7FFFFFFFLL || Mrows > 0x7FFFFFFFLL - FT) return SDM_EUNSUPPORTED;
+  FusedArgs fa;
+  fa.Mrows = int(Mrows);
+  fa.D = D;
+  fa.T = T;
+  fa.H = H;
+  fa.S = S;
+  fa.W = W;
+  fa.R = R;
+  fa.kp_stride = max(min(W, S), min(R, S));
+  fa.units = int(blocks_t * 4 * H);
+  fa.sel_kpad = 32;
+  while (fa.sel_kpad < max(W, R)) fa.sel_kpad <<= 1;
+  fa.sel_keys_bytes = (size_t(S) * 4 + 15) / 16 * 16;
+  fa.sel_per_warp = (count_per_warp_bytes(fa.sel_keys_bytes, fa.sel_kpad, fa.kp_stride) + 15) / 16 * 16;
+  fa.lists = static_cast<uint32_t*>(workspace);
+  fa.dev_err = dev_err;
+  CUtensorMap tmX, tmW;
+  if (!bf16_tile_map(&tmX, x, int(Mrows), D, FT) || !bf16_tile_map(&tmW, w, 4 * H * S, D, 128))
+    return SDM_ECUDA;
+  const size_t smem = size_t(F_ASTAGES) * F_A_BYTES + size_t(F_BSTAGES) * F_B_BYTES + 1024 + 256 +
+                      size_t(FG) * S * 2 + size_t(F_EPI_WARPS) * fa.sel_per_warp;
+  int dev = 0, max_smem = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return SDM_ECUDA;
+  if (smem > size_t(max_smem)) return SDM_EUNSUPPORTED;
+  const void* fn = reinterpret_cast<const void*>(&project_select_kernel);
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+    return SDM_ECUDA;
+  const int sms = sm_count();
+  if (sms <= 0) return SDM_ECUDA;
+  const int grid = fa.units < sms ? fa.units : sms;
+  void* args[] = {&tmX, &tmW, &fa};
+  if (cudaLaunchKernel(fn, dim3(unsigned(grid)), dim3(kThreads), args, smem, s) != cudaSuccess)
+    return SDM_ECUDA;
+  if (last_launch_status() != SDM_OK) return SDM_ECUDA;
+
+  // The outer top-K from the lists, with both staircases in the workspace after them.
+  uint32_t* stair = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(workspace) +
+                                                fused_lists_bytes(B, T, H, S, W, R));
+  int st = launch_stair_table(stair, W, R, S, s);
+  if (st != SDM_OK) return st;
+  OuterArgs oa;
+  oa.lists = fa.lists;
+  oa.items = Mrows * H;
+  oa.S = S;
+  oa.W = W;
+  oa.R = R;
+  oa.kp_stride = fa.kp_stride;
+  oa.cnt_w = stair_count(W, min(W, S));
+  oa.cnt_r = stair_count(R, min(R, S));
+  oa.kpad = fa.sel_kpad;
+  oa.warps = 4;
+  oa.keys_bytes = select_key_bytes(oa.kpad, S, max(oa.cnt_w, oa.cnt_r), 4);
+  oa.per_warp = (count_per_warp_bytes(oa.keys_bytes, oa.kpad, oa.kp_stride) + 15) / 16 * 16;
+  oa.stair = stair;
+  oa.idx_w = idx_w;
+  oa.sc_w = sc_w;
+  oa.idx_r = idx_r;
+  oa.sc_r = sc_r;
+  const size_t osmem = oa.per_warp * oa.warps;
+  const void* ofn = reinterpret_cast<const void*>(&outer_kernel);
+  if (cudaFuncSetAttribute(ofn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(osmem)) != cudaSuccess ||
+      cudaFuncSetAttribute(ofn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           int(cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+    return SDM_ECUDA;
+  const long long oblocks = (2 * oa.items + oa.warps - 1) / oa.warps;
+  if (oblocks > 0x7FFFFFFFLL) return SDM_EUNSUPPORTED;
+  void* oargs[] = {&oa};
+  if (cudaLaunchKernel(ofn, dim3(unsigned(oblocks)), dim3(oa.warps * 32), oargs, osmem, s) != cudaSuccess)
+    return SDM_ECUDA;
   return last_launch_status();
 }
 

@@ -208,6 +208,9 @@ __device__ __forceinline__ void count_finish(Key* dst, const Key* tmp, const uin
   __syncwarp();
 }
 
+__device__ bool inner_count_raw(const uint4* raw, int S, int kin, int top, const CountSmem& m,
+                                uint32_t* lst);
+
 // Top-kin of one bf16 half (S values, 16-byte aligned, S % 8 == 0, S <= kCountMaxS) by
 // (value desc, index asc), packed into lst[0..kin); the half's 16-byte chunks are kept in
 // the keys region between passes.  Returns false when the half's largest
@@ -238,6 +241,33 @@ __device__ bool inner_count(const uint16_t* src, int S, int kin, const CountSmem
   const int mxl = max(int(int16_t(mx2 & 0xFFFFu)), int(int16_t(mx2 >> 16)));
   const int top = __reduce_max_sync(kFull, mxl);
   if (top < 256) return false;
+  __syncwarp();
+  return inner_count_raw(raw, S, kin, top, m, lst);
+}
+
+// inner_count on a half already in shared memory (16-byte aligned, S % 8 == 0, S <=
+// kCountMaxS); the same result.
+__device__ bool inner_count_smem(const uint16_t* half, int S, int kin, const CountSmem& m,
+                                 uint32_t* lst) {
+  const int lane = threadIdx.x & 31;
+  const uint4* raw = reinterpret_cast<const uint4*>(half);
+  uint32_t mx2 = 0x80008000u;
+  for (int c = lane; c < (S >> 3); c += 32) {
+    const uint4 q = raw[c];
+    mx2 = __vmaxs2(__vmaxs2(mx2, q.x), __vmaxs2(q.y, __vmaxs2(q.z, q.w)));
+  }
+  const int mxl = max(int(int16_t(mx2 & 0xFFFFu)), int(int16_t(mx2 >> 16)));
+  const int top = __reduce_max_sync(kFull, mxl);
+  if (top < 256) return false;
+  return inner_count_raw(raw, S, kin, top, m, lst);
+}
+
+// Steps 2-5 of inner_count on the half's 16-byte chunks `raw` (shared memory), whose largest
+// pattern is top >= 256.
+__device__ bool inner_count_raw(const uint4* raw, int S, int kin, int top, const CountSmem& m,
+                                uint32_t* lst) {
+  const int lane = threadIdx.x & 31;
+  const int nvec = S >> 3;
   uint32_t* bins = m.bins;
   const uint32_t junk = 256u + uint32_t(lane);
   reinterpret_cast<uint4*>(bins)[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
@@ -290,6 +320,26 @@ __device__ __noinline__ void inner_general(const uint16_t* src, int S, int kin, 
   uint32_t* ik = reinterpret_cast<uint32_t*>(m.keys);
   uint32_t* io = reinterpret_cast<uint32_t*>(m.out);
   load_half_keys<uint16_t>(src, S, vec, ik, m.bins);
+  warp_topk_from<uint32_t>(ik, S, kin, io, m.bins, 0u, InnerKeyOf<uint16_t>::top_shift, true, 16);
+  sort_desc_upto<uint32_t, 4>(io, kin);
+  for (int r = lane; r < kin; r += 32) lst[r] = pack_inner(io[r]);
+  __syncwarp();
+}
+
+// inner_general on a half already in shared memory.
+__device__ __noinline__ void inner_general_smem(const uint16_t* half, int S, int kin,
+                                                const CountSmem& m, uint32_t* lst) {
+  const int lane = threadIdx.x & 31;
+  uint32_t* ik = reinterpret_cast<uint32_t*>(m.keys);
+  uint32_t* io = reinterpret_cast<uint32_t*>(m.out);
+  for (int b = lane; b < 256; b += 32) m.bins[b] = 0u;
+  __syncwarp();
+  for (int j = lane; j < S; j += 32) {
+    const uint32_t k = inner_key(half[j], j);
+    ik[j] = k;
+    atomicAdd(&m.bins[k >> InnerKeyOf<uint16_t>::top_shift], 1u);
+  }
+  __syncwarp();
   warp_topk_from<uint32_t>(ik, S, kin, io, m.bins, 0u, InnerKeyOf<uint16_t>::top_shift, true, 16);
   sort_desc_upto<uint32_t, 4>(io, kin);
   for (int r = lane; r < kin; r += 32) lst[r] = pack_inner(io[r]);
@@ -379,6 +429,59 @@ __device__ __noinline__ void outer_general(const CountSmem& m, const uint32_t* s
   sort_desc_upto<uint64_t, 4>(out, K);
 }
 
+// The outer top-K of one task over the packed lists m.la, m.lb (each the top-kin of a half,
+// in order): slots and scores, best first, to oi[0..K) and os[0..K).
+__device__ void outer_task(const CountSmem& m, const uint32_t* st, int cnt, int K, int kin, int S,
+                           int kpad, int32_t* oi, float* os) {
+  const int lane = threadIdx.x & 31;
+  uint64_t* out = reinterpret_cast<uint64_t*>(m.out);
+  // The smallest row-end sum and the largest sum (both lists are in descending order),
+  // and the exponent span of the lists' nonzero values.
+  uint32_t lo = ~0u, emax = 0u, emin = 0xFFu;
+  bool neg = false;
+  for (int p = lane; p < kin; p += 32) {
+    const float s = __fadd_rn(entry_value(m.la[p]), entry_value(m.lb[min(kin, K / (p + 1)) - 1]));
+    neg = neg || !(s > 0.0f);
+    lo = min(lo, __float_as_uint(s));
+    const uint32_t xa = entry_exp(m.la[p]), xb = entry_exp(m.lb[p]);
+    emax = max(emax, max(xa, xb));
+    if (xa) emin = min(emin, xa);
+    if (xb) emin = min(emin, xb);
+  }
+  lo = __reduce_min_sync(kFull, lo);
+  emax = __reduce_max_sync(kFull, emax);
+  emin = __reduce_min_sync(kFull, emin);
+  const bool any_neg = __any_sync(kFull, neg);
+  const uint32_t hi = __float_as_uint(__fadd_rn(entry_value(m.la[0]), entry_value(m.lb[0])));
+  bool done = false;
+  if (cnt > K && !any_neg) done = outer_count(m, st, cnt, K, kin, S, lo, hi);
+  if (!done) outer_general(m, st, cnt, K, S);
+  // Pairs right of the staircase that could still beat the K-th key: possible only when
+  // fp32 rounding merges sums, i.e. when the values' exponents span more than 15.
+  if (emax > emin + 15u) {
+    const uint64_t kth = out[K - 1];
+    const uint32_t kth_sum = uint32_t(kth >> 32);
+    bool beyond = false;
+    for (int p = lane; p < kin; p += 32) {
+      for (int q = min(kin, K / (p + 1)); q < kin; ++q) {
+        const uint64_t k = packed_pair_key(m.la, m.lb, p, q, S);
+        if (uint32_t(k >> 32) < kth_sum) break;  // sums only fall along a row
+        if (k > kth) beyond = true;
+      }
+    }
+    if (__any_sync(kFull, beyond)) {
+      packed_full_grid(m.la, m.lb, S, kin, K, kth, out, kpad, m.bins);
+      sort_desc_upto<uint64_t, 4>(out, K);
+    }
+  }
+  for (int r = lane; r < K; r += 32) {
+    const uint64_t k = out[r];
+    oi[r] = int32_t(0xFFFFFFFFu - uint32_t(k & 0xFFFFFFFFu));
+    os[r] = ord_decode(uint32_t(k >> 32));
+  }
+  __syncwarp();
+}
+
 struct CountArgs {
   const void* kp;
   const void* qp;
@@ -399,10 +502,9 @@ struct CountArgs {
 // 1: q' / top-R).
 __device__ void count_tasks(const CountArgs& a, const uint32_t* stair_w, const uint32_t* stair_r,
                             unsigned char* wbase, long long task0, long long task1) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   const int S = a.S;
   const CountSmem m = count_smem(wbase + a.per_warp * warp, a.keys_bytes, a.kpad, a.kin_max);
-  uint64_t* out = reinterpret_cast<uint64_t*>(m.out);
   for (long long task = task0; task < task1; ++task) {
     const int which = int(task & 1);
     const long long wi = task >> 1;
@@ -417,55 +519,8 @@ __device__ void count_tasks(const CountArgs& a, const uint32_t* stair_w, const u
     if (!inner_count(halves + S, S, kin, m, m.lb)) inner_general(halves + S, S, kin, true, m, m.lb);
 
     // ---- 2. top-K of the kin x kin grid of pair sums over the staircase -----------------
-    const uint32_t* st = which ? stair_r : stair_w;
-    const int cnt = which ? a.cnt_r : a.cnt_w;
-    // The smallest row-end sum and the largest sum (both lists are in descending order),
-    // and the exponent span of the lists' nonzero values.
-    uint32_t lo = ~0u, emax = 0u, emin = 0xFFu;
-    bool neg = false;
-    for (int p = lane; p < kin; p += 32) {
-      const float s = __fadd_rn(entry_value(m.la[p]), entry_value(m.lb[min(kin, K / (p + 1)) - 1]));
-      neg = neg || !(s > 0.0f);
-      lo = min(lo, __float_as_uint(s));
-      const uint32_t xa = entry_exp(m.la[p]), xb = entry_exp(m.lb[p]);
-      emax = max(emax, max(xa, xb));
-      if (xa) emin = min(emin, xa);
-      if (xb) emin = min(emin, xb);
-    }
-    lo = __reduce_min_sync(kFull, lo);
-    emax = __reduce_max_sync(kFull, emax);
-    emin = __reduce_min_sync(kFull, emin);
-    const bool any_neg = __any_sync(kFull, neg);
-    const uint32_t hi = __float_as_uint(__fadd_rn(entry_value(m.la[0]), entry_value(m.lb[0])));
-    bool done = false;
-    if (cnt > K && !any_neg) done = outer_count(m, st, cnt, K, kin, S, lo, hi);
-    if (!done) outer_general(m, st, cnt, K, S);
-    // Pairs right of the staircase that could still beat the K-th key: possible only when
-    // fp32 rounding merges sums, i.e. when the values' exponents span more than 15.
-    if (emax > emin + 15u) {
-      const uint64_t kth = out[K - 1];
-      const uint32_t kth_sum = uint32_t(kth >> 32);
-      bool beyond = false;
-      for (int p = lane; p < kin; p += 32) {
-        for (int q = min(kin, K / (p + 1)); q < kin; ++q) {
-          const uint64_t k = packed_pair_key(m.la, m.lb, p, q, S);
-          if (uint32_t(k >> 32) < kth_sum) break;  // sums only fall along a row
-          if (k > kth) beyond = true;
-        }
-      }
-      if (__any_sync(kFull, beyond)) {
-        packed_full_grid(m.la, m.lb, S, kin, K, kth, out, a.kpad, m.bins);
-        sort_desc_upto<uint64_t, 4>(out, K);
-      }
-    }
-    int32_t* oi = (which ? a.idx_r : a.idx_w) + item * K;
-    float* os = (which ? a.sc_r : a.sc_w) + item * K;
-    for (int r = lane; r < K; r += 32) {
-      const uint64_t k = out[r];
-      oi[r] = int32_t(0xFFFFFFFFu - uint32_t(k & 0xFFFFFFFFu));
-      os[r] = ord_decode(uint32_t(k >> 32));
-    }
-    __syncwarp();
+    outer_task(m, which ? stair_r : stair_w, which ? a.cnt_r : a.cnt_w, K, kin, S, a.kpad,
+               (which ? a.idx_r : a.idx_w) + item * K, (which ? a.sc_r : a.sc_w) + item * K);
   }
 }
 
