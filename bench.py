@@ -127,23 +127,30 @@ def hbm_peak():
 
 
 SELECT_SRC = [os.path.join(ROOT, "sparse_state_linear_sdm_gb300", "csrc", f)
-              for f in ("sdm_select_impl.cuh", "sdm_select_bf16.cu", "sdm_select_f32.cu")]
+              for f in ("sdm_select_impl.cuh", "sdm_select_count.cuh", "sdm_select_bf16.cu",
+                        "sdm_select_f32.cu")]
 SELECT_FILE = os.path.join(ROOT, "profiles", "select_kernel_instructions.json")
 SMS, SMSP_PER_SM = 152, 4
 
 
+def select_source_sha() -> str:
+    h = hashlib.sha256()
+    for p in SELECT_SRC:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def select_roofline(cfg, units: int, select_ms: float, clocks):
     """The selection kernel is bound by instruction issue: warp-instructions per selection
-    (ncu, this workload, this kernel source) x selections / its time alone, against one
-    warp-instruction per clock per SM sub-partition at the sampled SM clock."""
+    (ncu, a selection of the same S, W, R and input dtype on inputs of the same distribution,
+    this kernel source) x selections / its time alone, against one warp-instruction per clock
+    per SM sub-partition at the sampled SM clock."""
     try:
         with open(SELECT_FILE) as f:
             rec = json.load(f)
-        h = hashlib.sha256()
-        for p in SELECT_SRC:
-            with open(p, "rb") as f:
-                h.update(f.read())
-        if rec.get("source_sha256") != h.hexdigest() or rec.get("workload") != cfg.name:
+        key = (cfg.S, cfg.W, cfg.R, cfg.in_dtype)
+        if rec.get("source_sha256") != select_source_sha() or tuple(rec.get("shape", ())) != key:
             return None
         mhz = (clocks or {}).get("sm_mhz") or 2070.0
         achieved = rec["warp_instructions_per_selection"] * 2 * units / (select_ms / 1e3) / 1e9

@@ -120,8 +120,9 @@ def test_select_roofline_from_the_instruction_record(tmp_path, monkeypatch):
     for p in bench.SELECT_SRC:
         with open(p, "rb") as f:
             h.update(f.read())
+    assert h.hexdigest() == bench.select_source_sha()
     cfg = wl.B16H4_T8192
-    rec = {"warp_instructions_per_selection": 10_000.0, "workload": cfg.name,
+    rec = {"warp_instructions_per_selection": 10_000.0, "shape": [cfg.S, cfg.W, cfg.R, cfg.in_dtype],
            "source_sha256": h.hexdigest()}
     path = tmp_path / "sel.json"
     path.write_text(json.dumps(rec))
@@ -133,8 +134,9 @@ def test_select_roofline_from_the_instruction_record(tmp_path, monkeypatch):
     assert got["peak"] == pytest.approx(152 * 4 * 2000.0 / 1e3)
     assert got["frac"] == pytest.approx(got["achieved"] / got["peak"])
     assert got["bound"] == "alu"
-    # another workload, or another source, has no record
+    # another shape, or another source, has no record; the stream workload shares the shape
     assert bench.select_roofline(wl.B4H8_T2048, units, 12.0, None) is None
+    assert bench.select_roofline(wl.STREAM_B1H4_T1M, units, 12.0, None) is not None
     rec["source_sha256"] = "0" * 64
     path.write_text(json.dumps(rec))
     assert bench.select_roofline(cfg, units, 12.0, None) is None
