@@ -888,7 +888,7 @@ def run_backward(args):
     def step(ev=None):
         if ev:
             ev[0].record()
-        G.zero_()
+        sdm.fill_state(G, 0.0)
         if ev:
             ev[1].record()
         g = sdm.scan_backward(*sel, st["v"], st["alpha"], st["beta"], w_prev, r_rows, dO, G, workspace=ws)
@@ -929,7 +929,7 @@ def run_backward(args):
                          else "fallback"},
             "kernels": {"forward_train_ms": f0.elapsed_time(f1), "zero_adjoint_ms": zero_ms,
                         "scan_backward_ms": scan_ms, "select_backward_ms": sel_ms},
-            "gpu_launches": 5 * K, "clocks": clk.summary()}
+            "gpu_launches": 6 * K, "clocks": clk.summary()}
     if rank == 0:
         print(json.dumps(line), flush=True)
 

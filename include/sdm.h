@@ -74,6 +74,12 @@ const char* sdm_status_str(int status);
 int sdm_init_state_from_M0(float* M, const float* M0, int B, int H, long long N, int d_v,
                            void* stream);
 
+/* sdm_fill_state - every entry of a state-shaped table set to `value` (not the method itself:
+ * the backward pass's adjoint table starts at zero when the final state carries no gradient,
+ * see sdm_scan_backward).  M [B, H, N, d_v] fp32, written with streaming stores.
+ * Requires B, H >= 1, N >= 1, d_v >= 4, d_v % 4 == 0. */
+int sdm_fill_state(float* M, float value, int B, int H, long long N, int d_v, void* stream);
+
 /* sdm_select - product-key slot selection ("Meccanismo Core" item 2).
  * For every (b, h, t): halves a = kp[b,h,t,0,:], b = kp[b,h,t,1,:] (S entries each,
  * the sub-scores themselves).  With k = min(W, S), the top-k of each half by

@@ -69,13 +69,15 @@ def lib() -> ctypes.CDLL:
             L.sdm_decode_step_supported.argtypes = [i, i, i, i, i, i, i]
             L.sdm_project_kq_tuned.argtypes = [p, p, i, i, i, i, i, p, p, p, i, i, p]
             L.sdm_test_bounded_wait.argtypes = [i, ull, p, p, p]
+            L.sdm_fill_state.argtypes = [p, f, i, i, ll, i, p]
             L.sdm_project_select_workspace_size.argtypes = [i, i, i, i, i, i]
             L.sdm_project_select_workspace_size.restype = sz
             L.sdm_project_select.argtypes = [p, p, i, i, i, i, i, i, i, p, p, p, p, p, sz, p, p]
             for name in ("sdm_init_state_from_M0", "sdm_select", "sdm_select_tuned", "sdm_scan_forward",
                          "sdm_scan_forward_tuned", "sdm_scan_launch_info", "sdm_gen_inputs", "sdm_gen_M0",
                          "sdm_forward_chunks", "sdm_forward_tuned", "sdm_forward", "sdm_scan_forward_train",
-                         "sdm_scan_backward", "sdm_select_backward", "sdm_project_select"):
+                         "sdm_scan_backward", "sdm_select_backward", "sdm_project_select",
+                         "sdm_fill_state"):
                 getattr(L, name).restype = i
             _lib = L
     return _lib
@@ -159,6 +161,16 @@ def init_state_from_M0(M: torch.Tensor, M0: torch.Tensor) -> torch.Tensor:
     B, H, N, dv = M.shape
     _need(M0, "M0", torch.float32, (H, N, dv))
     _call("sdm_init_state_from_M0", _p(M), _p(M0), B, H, N, dv, _stream(M.device))
+    return M
+
+
+@_on_tensor_device
+def fill_state(M: torch.Tensor, value: float = 0.0) -> torch.Tensor:
+    """Every entry of M (fp32 [B, H, N, d_v]) set to value, e.g. the backward pass's adjoint
+    table cleared when the final state carries no gradient."""
+    _need(M, "M", torch.float32)
+    B, H, N, dv = M.shape
+    _call("sdm_fill_state", _p(M), ctypes.c_float(value), B, H, N, dv, _stream(M.device))
     return M
 
 

@@ -29,6 +29,12 @@ int sdm_init_state_from_M0(float* M, const float* M0, int B, int H, long long N,
   return launch_init_state(M, M0, B, H, N, d_v, as_stream(stream));
 }
 
+int sdm_fill_state(float* M, float value, int B, int H, long long N, int d_v, void* stream) {
+  if (B < 1 || H < 1 || N < 1 || d_v < 4 || d_v % 4) return SDM_EINVAL;
+  if (!aligned16(M)) return SDM_EALIGN;
+  return launch_fill_state(M, value, B, H, N, d_v, as_stream(stream));
+}
+
 int sdm_select_tuned(const void* kp, const void* qp, int in_dt, int B, int H, int T, int S, int W,
                      int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, int path,
                      void* stream) {

@@ -73,14 +73,14 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int W = a.W, R = a.R, T = a.T, d_v = a.d_v;
   const int WR = W + R, WRa = (W + R + 3) & ~3;
-  float* kw = reinterpret_cast<float*>(smem);        // [W] write weights of the token
-  float* rw = kw + W;                                 // [R] read weights
-  float* red = kw + WRa;                              // [warps][C]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float* kw = reinterpret_cast<float*>(smem);  // [W] write weights of the token
+  float* rw = kw + W;                           // [R] read weights
+  float* red = kw + WRa;                        // [2][warps][C], by token parity
   // Two staging buffers of one token's [slots W | slots R | scores W | scores R]: the next
   // token's (going backwards) arrive by cp.async while this one is processed.
-  int32_t* stg = reinterpret_cast<int32_t*>(red + kBwdWarps * C);  // [2][2 * WR]
+  int32_t* stg = reinterpret_cast<int32_t*>(red + 2 * kBwdWarps * C);  // [2][2 * WR]
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int slices = d_v / C;
   const int bh = blockIdx.x / slices;
   const int sl = blockIdx.x - bh * slices;
@@ -202,24 +202,26 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
       dva.z += __shfl_xor_sync(0xFFFFFFFFu, dva.z, off);
       dva.w += __shfl_xor_sync(0xFFFFFFFFu, dva.w, off);
     }
-    if (lane < LPR) reinterpret_cast<float4*>(red + warp * C)[lane] = dva;
+    float* rd = red + (t & 1) * kBwdWarps * C;
+    if (lane < LPR) reinterpret_cast<float4*>(rd + warp * C)[lane] = dva;
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    // G of this token is written before the previous token loads it; the next token's slots
+    // and scores and this token's dv partials are visible.
     __syncthreads();
     if (tid < LPR) {
-      float4 s4 = reinterpret_cast<const float4*>(red)[tid];
+      float4 s4 = reinterpret_cast<const float4*>(rd)[tid];
       for (int w = 1; w < kBwdWarps; ++w) {
-        const float4 u = reinterpret_cast<const float4*>(red + w * C)[tid];
+        const float4 u = reinterpret_cast<const float4*>(rd + w * C)[tid];
         s4 = make_float4(s4.x + u.x, s4.y + u.y, s4.z + u.z, s4.w + u.w);
       }
       reinterpret_cast<float4*>(a.dv + tk * d_v + c0)[tid] = s4;
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    __syncthreads();  // G of this token is written before the previous token loads it
   }
 }
 
 size_t backward_smem_bytes(int C, int W, int R) {
   const int WRa = (W + R + 3) & ~3;
-  return size_t(WRa) * 4 + size_t(kBwdWarps) * C * 4 + size_t(4 * (W + R)) * 4;
+  return size_t(WRa) * 4 + size_t(2 * kBwdWarps) * C * 4 + size_t(4 * (W + R)) * 4;
 }
 
 int backward_cols(int d_v) {

@@ -12,8 +12,10 @@
 //             u = f 2^e with f in [sqrt(1/2), sqrt(2));
 //     sin/cos on [0, pi/2): Taylor series to degree 13 / 14 after an exact quadrant
 //             split of the 24-bit angle;
-//     exp x = 2^n p(r), n = floor(x log2 e + 1/2), r = x - n ln2 (two-part ln2),
-//             p = Taylor series to degree 8.
+//     exp x = 2^n p(r), n = floor(x log2 e + 1/2), r = (x - n ln2_hi) - n ln2_lo
+//             (ln2 split into a high part with trailing zero bits, so n ln2_hi is exact,
+//             and the rest: the argument reduction of Cody and Waite, "Software Manual
+//             for the Elementary Functions", 1980), p = Taylor series to degree 8.
 #include "sdm_internal.cuh"
 
 namespace sdm {

@@ -23,7 +23,29 @@ __global__ void __launch_bounds__(256) init_state_kernel(float4* __restrict__ M,
   }
 }
 
+// Every float of a state-shaped table set to `value` (streaming stores, 16 bytes a thread).
+__global__ void __launch_bounds__(256) fill_state_kernel(float4* __restrict__ M, float value,
+                                                         size_t n4) {
+  const size_t stride = size_t(gridDim.x) * blockDim.x;
+  const float4 x = make_float4(value, value, value, value);
+  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) __stcs(M + i, x);
+}
+
 }  // namespace
+
+int launch_fill_state(float* M, float value, int B, int H, long long N, int d_v, cudaStream_t s) {
+  const size_t n4 = size_t(B) * size_t(H) * size_t(N) * size_t(d_v) / 4;
+  if (n4 == 0) return SDM_OK;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SDM_ECUDA;
+  size_t blocks = size_t(sms) * 16;
+  const size_t need = (n4 + 255) / 256;
+  if (blocks > need) blocks = need;
+  fill_state_kernel<<<unsigned(blocks), 256, 0, s>>>(reinterpret_cast<float4*>(M), value, n4);
+  return last_launch_status();
+}
 
 int launch_init_state(float* M, const float* M0, int B, int H, long long N, int d_v,
                       cudaStream_t s) {

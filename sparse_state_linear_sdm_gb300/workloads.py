@@ -18,7 +18,10 @@ Generator ("counter-based", one draw per tensor element):
     correctly-rounded fp32 +, -, *, / and sqrt, so that any IEEE machine gives the
     same bits.  ln u = e ln2 + 2 atanh((f-1)/(f+1)) for u = f 2^e,
     f in [sqrt(1/2), sqrt(2)); cos/sin are Taylor series on [0, pi/2) after an
-    exact quadrant split of k; exp is 2^n times a Taylor series on |r| <= ln2/2.
+    exact quadrant split of k; exp is 2^n times a Taylor series on |r| <= ln2/2,
+    with r = (x - n ln2_hi) - n ln2_lo: ln2 split in a high part with trailing zero
+    bits (so n ln2_hi is exact) and the rest, the argument reduction of Cody and
+    Waite ("Software Manual for the Elementary Functions", 1980).
   * bf16 fields are rounded from fp32 to nearest-even.
 """
 from __future__ import annotations

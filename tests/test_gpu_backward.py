@@ -151,3 +151,14 @@ def test_backward_on_the_small_workload_sampled_heads():
             e = normwise(g[name][b, h].cpu().numpy()[None], ref[name])
             assert e <= GTOL, (name, b, h, e)
         assert normwise(G[b, h].cpu().numpy()[None], ref["dM0"]) <= GTOL
+
+
+def test_fill_state_sets_every_entry():
+    """sdm_fill_state (the adjoint table cleared before the reverse pass) writes every entry."""
+    M = torch.full((2, 3, 1000, 16), float("nan"), device="cuda")
+    sdm.fill_state(M, 0.0)
+    torch.cuda.synchronize()
+    assert torch.equal(M, torch.zeros_like(M))
+    sdm.fill_state(M, 1.5)
+    torch.cuda.synchronize()
+    assert bool((M == 1.5).all())
