@@ -262,10 +262,15 @@ int choose_scan_shape(int BH, int d_v, int W, int R, int force_cols, int force_p
     if (!force_cols && ci + 1 < 5 && d_v % col_opts[ci + 1] == 0 &&
         (long long)BH * (d_v / c) * 2 < 3LL * sms)
       continue;
-    // One token of rows in flight per block measured fastest (pd 1: 18.8 ms, pd 2: 19.1 ms
-    // on B16 H4 T8192 N=2^20 d_v=128 W=R=128); deeper pipelines only add shared memory.
-    for (int pd = 1; pd <= 2 && !best_cols; ++pd) {
-      const int p = force_pd ? force_pd : pd;
+    // One token of rows in flight per block measured fastest when the blocks fill the GPU
+    // (pd 1: 18.8 ms, pd 2: 19.1 ms on B16 H4 T8192 N=2^20 d_v=128 W=R=128); with fewer
+    // blocks than SMs each block's chain of gathers sets the pace, and two tokens in flight
+    // measured faster (B1 H4 N=2^20 d_v=128 W=R=128, 4-column slices: 0.93 against 1.00 us
+    // per token).
+    const int pd0 = (long long)BH * (d_v / c) < sms ? 2 : 1;
+    const int pds[2] = {pd0, 3 - pd0};
+    for (int k = 0; k < 2 && !best_cols; ++k) {
+      const int p = force_pd ? force_pd : pds[k];
       if (scan_smem_bytes(c, p, W, R, d_v) <= size_t(max_smem)) {
         best_cols = c;
         best_pd = p;
