@@ -853,10 +853,31 @@ def backward_bytes_per_head_token(cfg) -> int:
     return cfg.d_v * 4 + K * cfg.d_v * 4 + 2 * K * cfg.d_v * 4 + cfg.d_v * elt + 8 + K * 8 + cfg.d_v * 4
 
 
+def zero_adjoint_slots(sel, N, torch):
+    """Under a zero final adjoint: the write slots and read slots whose adjoint row is still
+    zero (no later read selects the row; a read at the same token comes after the token's
+    writes).  Counted with torch on the device from the slots alone (measurement only)."""
+    iw, ir = sel[0], sel[2]
+    B, H, T, W = iw.shape
+    R = ir.shape[3]
+    dev = iw.device
+    tr = torch.arange(T, device=dev).repeat_interleave(R)
+    t = torch.arange(T, device=dev)[:, None]
+    zw = zr = 0
+    for b in range(B):
+        for h in range(H):
+            last = torch.full((N,), -1, dtype=torch.int64, device=dev)
+            last.scatter_reduce_(0, ir[b, h].reshape(-1).long(), tr, reduce="amax")
+            zr += int((last[ir[b, h].long()] == t).sum())
+            zw += int((last[iw[b, h].long()] < t).sum())
+    return zw, zr
+
+
 def run_backward(args):
     """Training backward of one forward pass: with the forward's stored rows, K steps of
-    (adjoint table zeroed: no gradient on the final state; reverse scan with the finish
-    and the batch reduction into dM_0; half gradients of k' and q')."""
+    (reverse scan with a zero final adjoint -- the loss reads the outputs only -- with the
+    finish and the batch reduction into dM_0; half gradients of k' and q').  The same
+    steps with the adjoint table cleared and the full reverse scan are timed beside it."""
     import torch
 
     import sparse_state_linear_sdm_gb300 as sdm
@@ -880,18 +901,20 @@ def run_backward(args):
     gen = torch.Generator(device=dev).manual_seed(cfg.seed)
     dO = torch.randn((cfg.B, cfg.H, cfg.T, cfg.d_v), generator=gen, device=dev)
     G = st["M"]   # the state is not needed any more: its buffer holds the adjoint
-    ws = torch.empty(sdm.lib().sdm_scan_backward_workspace_size(cfg.B, cfg.H, cfg.T, cfg.d_v, cfg.W, cfg.R),
+    ws = torch.empty(sdm.backward_workspace_size(cfg.B, cfg.H, cfg.T, cfg.N, cfg.d_v, cfg.W, cfg.R, True),
                      dtype=torch.uint8, device=dev)
     dkp = torch.empty((cfg.B, cfg.H, cfg.T, 2, cfg.S), device=dev)
     dqp = torch.empty_like(dkp)
 
-    def step(ev=None):
+    def step(final_zero, ev=None):
         if ev:
             ev[0].record()
-        sdm.fill_state(G, 0.0)
+        if not final_zero:
+            sdm.fill_state(G, 0.0)
         if ev:
             ev[1].record()
-        g = sdm.scan_backward(*sel, st["v"], st["alpha"], st["beta"], w_prev, r_rows, dO, G, workspace=ws)
+        g = sdm.scan_backward(*sel, st["v"], st["alpha"], st["beta"], w_prev, r_rows, dO, G, workspace=ws,
+                              final_zero=final_zero)
         if ev:
             ev[2].record()
         sdm.select_backward(sel[0], g["dsc_w"], cfg.S, out=dkp)
@@ -899,37 +922,57 @@ def run_backward(args):
         if ev:
             ev[3].record()
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    K = args.steps
-    evs = [[E() for _ in range(4)] for _ in range(K)]
-    with ClockSampler(local) as clk:
-        for k in range(K):
-            step(evs[k])
+    def timed(final_zero):
+        for _ in range(args.warmup):
+            step(final_zero)
         torch.cuda.synchronize(dev)
-    total = evs[0][0].elapsed_time(evs[-1][3])
-    zero_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / K
-    scan_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / K
-    sel_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / K
+        evs = [[E() for _ in range(4)] for _ in range(args.steps)]
+        with ClockSampler(local) as clk:
+            for k in range(args.steps):
+                step(final_zero, evs[k])
+            torch.cuda.synchronize(dev)
+        K = args.steps
+        return dict(total=evs[0][0].elapsed_time(evs[-1][3]),
+                    zero_ms=sum(e[0].elapsed_time(e[1]) for e in evs) / K,
+                    scan_ms=sum(e[1].elapsed_time(e[2]) for e in evs) / K,
+                    sel_ms=sum(e[2].elapsed_time(e[3]) for e in evs) / K), clk
+
+    lazy, clk = timed(True)
+    full, _ = timed(False)
+    K = args.steps
     units = cfg.B * cfg.H * cfg.T
     peak, peak_kind = hbm_peak()
-    alg = backward_bytes_per_head_token(cfg) * units
-    achieved = alg / (scan_ms / 1e3) / 1e9
+    row = cfg.d_v * 4
+    zw, zr = zero_adjoint_slots(sel, cfg.N, torch)
+    # A zero read slot skips its adjoint load; a zero write slot its adjoint load and store
+    # and its stored row's load; every token reads its words of zero bits.
+    alg_full = backward_bytes_per_head_token(cfg) * units
+    alg = alg_full - zr * row - 3 * zw * row + units * 4 * ((cfg.W + cfg.R + 31) // 32)
+    achieved = alg / (lazy["scan_ms"] / 1e3) / 1e9
+    achieved_full = alg_full / (full["scan_ms"] / 1e3) / 1e9
+    slots_w, slots_r = units * cfg.W, units * cfg.R
     line = {"metric": "SDM backward head-tokens/s on 1 GB300 (reverse scan, score and half gradients)",
-            "value": whole_job_rate(units, K, world, total), "unit": UNIT, "n_gpus": world, "steps": K,
-            "warmup": args.warmup, "ms_per_step": total / K, "higher_is_better": True, "scaling": "weak",
+            "value": whole_job_rate(units, K, world, lazy["total"]), "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": lazy["total"] / K, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": dict(config_dict(cfg), step="backward: zero the adjoint, reverse scan + finish + dM0 "
-                                                  "reduction, select backward for k' and q'"),
-            "roofline": {"kernel": "sdm_scan_backward (reverse scan, finish, batch reduction)", "bound": "hbm",
-                         "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "config": dict(config_dict(cfg), step="backward with a zero final adjoint (dL/dM_T = 0): reverse "
+                                                  "scan + finish + dM0 reduction (sdm_scan_backward_ex, "
+                                                  "SDM_BWD_FINAL_ZERO), select backward for k' and q'"),
+            "roofline": {"kernel": "sdm_scan_backward_ex (zero-slot passes, reverse scan, finish, batch reduction)",
+                         "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "algorithmic_bytes_per_launch": alg, "traffic": None,
+                         "note": "bytes of the reverse scan with the zero slots' rows left out, over the whole "
+                                 "call's time",
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                          else "fallback"},
-            "kernels": {"forward_train_ms": f0.elapsed_time(f1), "zero_adjoint_ms": zero_ms,
-                        "scan_backward_ms": scan_ms, "select_backward_ms": sel_ms},
-            "gpu_launches": 6 * K, "clocks": clk.summary()}
+            "kernels": {"forward_train_ms": f0.elapsed_time(f1), "scan_backward_ms": lazy["scan_ms"],
+                        "select_backward_ms": lazy["sel_ms"],
+                        "zero_slots": {"write": zw / slots_w, "read": zr / slots_r},
+                        "cleared_adjoint": {"ms_per_step": full["total"] / K, "fill_ms": full["zero_ms"],
+                                            "scan_backward_ms": full["scan_ms"], "select_backward_ms": full["sel_ms"],
+                                            "algorithmic_bytes_per_launch": alg_full,
+                                            "achieved_gbs": achieved_full, "frac": achieved_full / peak}},
+            "gpu_launches": 8 * K, "clocks": clk.summary()}
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -262,6 +262,31 @@ int sdm_scan_forward_train(float* M, const int32_t* idx_w, const float* sc_w,
  * Requires d_v % 4 == 0 and the limits of sdm_scan_forward; slots outside [0, N) are
  * skipped (their gradients are unspecified). */
 size_t sdm_scan_backward_workspace_size(int B, int H, int T, int d_v, int W, int R);
+
+/* sdm_scan_backward_ex - sdm_scan_backward with flags (0: the same call).
+ *   SDM_BWD_FINAL_ZERO: dL/dM_T is zero (the loss reads the outputs only).  G's contents on
+ *          entry are ignored (it need not be cleared); on exit it holds dL/dM_0 for each
+ *          (b, h) as without the flag, with G cleared: exactly equal values (a zero's sign
+ *          may differ).  Knowing that the adjoint starts at zero, the pass finds, per slot,
+ *          whether the adjoint row there is still zero (no later read selects the row) and
+ *          skips that row's loads and, for a write slot, its store.  Three more kernels
+ *          (the last token reading each row, one bit per slot) run first; with T = 0 every
+ *          row of G is set to zero.
+ *   workspace  at least sdm_scan_backward_workspace_size_ex(B, H, T, N, d_v, W, R, flags)
+ *          bytes (with the flag: 4 bytes per (b, h, row) and 4 per 32 slots of a token more),
+ *          16-byte aligned, contents irrelevant.
+ * Unknown flag bits: SDM_EINVAL (and a workspace size of 0).  Two read slots of one token
+ * naming the same row give unspecified gradients, as in sdm_scan_backward. */
+#define SDM_BWD_FINAL_ZERO 1u
+size_t sdm_scan_backward_workspace_size_ex(int B, int H, int T, long long N, int d_v, int W, int R,
+                                           unsigned flags);
+int sdm_scan_backward_ex(const int32_t* idx_w, const float* sc_w, const int32_t* idx_r,
+                         const float* sc_r, const void* v, int v_dt, const float* alpha,
+                         const float* beta, const float* w_prev, const float* r_rows,
+                         const float* dO, int B, int H, int T, long long N, int d_v, int W, int R,
+                         float* G, float* dv, float* dalpha, float* dbeta, float* dsc_w,
+                         float* dsc_r, float* dM0, unsigned flags, void* workspace,
+                         size_t workspace_bytes, void* stream);
 int sdm_scan_backward(const int32_t* idx_w, const float* sc_w, const int32_t* idx_r,
                       const float* sc_r, const void* v, int v_dt, const float* alpha,
                       const float* beta, const float* w_prev, const float* r_rows,

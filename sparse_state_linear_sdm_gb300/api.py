@@ -64,6 +64,10 @@ def lib() -> ctypes.CDLL:
             L.sdm_scan_backward_workspace_size.restype = sz
             L.sdm_scan_backward.argtypes = [p, p, p, p, p, i, p, p, p, p, p, i, i, i, ll, i, i, i, p, p, p, p, p, p,
                                             p, p, sz, p]
+            L.sdm_scan_backward_workspace_size_ex.argtypes = [i, i, i, ll, i, i, i, ctypes.c_uint]
+            L.sdm_scan_backward_workspace_size_ex.restype = sz
+            L.sdm_scan_backward_ex.argtypes = [p, p, p, p, p, i, p, p, p, p, p, i, i, i, ll, i, i, i, p, p, p, p,
+                                               p, p, p, ctypes.c_uint, p, sz, p]
             L.sdm_select_backward.argtypes = [p, p, i, i, i, i, i, p, p]
             L.sdm_decode_step.argtypes = [p, p, i, p, i, p, p, p, i, i, i, i, i, i, p, p, p, p, p, p, p]
             L.sdm_decode_step_supported.argtypes = [i, i, i, i, i, i, i]
@@ -76,7 +80,7 @@ def lib() -> ctypes.CDLL:
             for name in ("sdm_init_state_from_M0", "sdm_select", "sdm_select_tuned", "sdm_scan_forward",
                          "sdm_scan_forward_tuned", "sdm_scan_launch_info", "sdm_gen_inputs", "sdm_gen_M0",
                          "sdm_forward_chunks", "sdm_forward_tuned", "sdm_forward", "sdm_scan_forward_train",
-                         "sdm_scan_backward", "sdm_select_backward", "sdm_project_select",
+                         "sdm_scan_backward", "sdm_scan_backward_ex", "sdm_select_backward", "sdm_project_select",
                          "sdm_fill_state"):
                 getattr(L, name).restype = i
             _lib = L
@@ -454,13 +458,24 @@ def scan_forward_train(M, idx_w, sc_w, idx_r, sc_r, v, alpha, beta, o=None, work
     return o, w_prev, r_rows
 
 
+BWD_FINAL_ZERO = 1  # sdm_scan_backward_ex flag: dL/dM_T = 0, G's entry contents ignored
+
+
+def backward_workspace_size(B: int, H: int, T: int, N: int, d_v: int, W: int, R: int,
+                            final_zero: bool = False) -> int:
+    """Bytes of workspace scan_backward needs (sdm_scan_backward_workspace_size_ex)."""
+    return int(lib().sdm_scan_backward_workspace_size_ex(B, H, T, N, d_v, W, R,
+                                                         BWD_FINAL_ZERO if final_zero else 0))
+
+
 @_on_tensor_device
 def scan_backward(idx_w, sc_w, idx_r, sc_r, v, alpha, beta, w_prev, r_rows, dO, G, shared_M0: bool = True,
-                  workspace=None):
+                  workspace=None, final_zero: bool = False):
     """Reverse-mode pass of the scan for L = sum_t <dO_t, o_t> + <dM_T, M_T>, slots fixed.
-    G: fp32 [B,H,N,d_v], in dL/dM_T, out dL/dM_0 per (b, h) (in place).  Returns
-    dict(dv, dalpha, dbeta, dsc_w, dsc_r, dM0) with dM0 = sum of G over the batch
-    (shared_M0) or None."""
+    G: fp32 [B,H,N,d_v], in dL/dM_T, out dL/dM_0 per (b, h) (in place).  final_zero: dM_T
+    is zero and G's entry contents are ignored (it need not be cleared; the pass skips the
+    adjoint rows it knows to be zero).  Returns dict(dv, dalpha, dbeta, dsc_w, dsc_r, dM0)
+    with dM0 = sum of G over the batch (shared_M0) or None."""
     _need(G, "G", torch.float32)
     B, H, N, dv = G.shape
     T, W, R = idx_w.shape[2], idx_w.shape[3], idx_r.shape[3]
@@ -473,12 +488,12 @@ def scan_backward(idx_w, sc_w, idx_r, sc_r, v, alpha, beta, w_prev, r_rows, dO, 
                dsc_r=torch.empty((B, H, T, R), device=dev),
                dM0=torch.empty((H, N, dv), device=dev) if shared_M0 else None)
     if workspace is None:
-        n = lib().sdm_scan_backward_workspace_size(B, H, T, dv, W, R)
+        n = backward_workspace_size(B, H, T, N, dv, W, R, final_zero)
         workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
-    _call("sdm_scan_backward", _p(idx_w), _p(sc_w), _p(idx_r), _p(sc_r), _p(v), _dtype_code(v), _p(alpha), _p(beta),
-          _p(w_prev), _p(r_rows), _p(dO), B, H, T, N, dv, W, R, _p(G), _p(out["dv"]), _p(out["dalpha"]),
-          _p(out["dbeta"]), _p(out["dsc_w"]), _p(out["dsc_r"]), _p(out["dM0"]), _p(workspace), workspace.numel(),
-          _stream(dev))
+    _call("sdm_scan_backward_ex", _p(idx_w), _p(sc_w), _p(idx_r), _p(sc_r), _p(v), _dtype_code(v), _p(alpha),
+          _p(beta), _p(w_prev), _p(r_rows), _p(dO), B, H, T, N, dv, W, R, _p(G), _p(out["dv"]), _p(out["dalpha"]),
+          _p(out["dbeta"]), _p(out["dsc_w"]), _p(out["dsc_r"]), _p(out["dM0"]),
+          BWD_FINAL_ZERO if final_zero else 0, _p(workspace), workspace.numel(), _stream(dev))
     return out
 
 

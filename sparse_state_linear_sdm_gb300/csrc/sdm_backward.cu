@@ -16,6 +16,19 @@
 // dot products over d_v leave one partial per slice), a finish kernel (one warp per token:
 // sums the slices' partials, softmax backward), a batch reduction of G into dM_0, and the
 // selection backward (a selected score is half0[i] + half1[j]).
+//
+// Zero final adjoint (SDM_BWD_FINAL_ZERO, dL/dM_T = 0, the usual training loss on the
+// outputs alone).  Going backwards, a row's adjoint stays exactly zero until a read of the
+// row adds r_j dO_t; a write only scales it.  So the adjoint row seen at a slot is zero iff
+// no read of that row comes later in the forward order (a read at the same token comes
+// after the token's writes).  Two passes find this before the reverse scan: the last token
+// that reads each row (an atomic maximum per read slot into a per-(b, h) table), then one
+// bit per slot.  The reverse scan then skips, at a zero slot, the adjoint load and, for a
+// write slot, the stored row's load and the adjoint store (the row stays zero); every
+// non-zero row it loads was stored earlier in the same pass.  G's contents on entry are
+// never read; the batch reduction writes zeros to the rows no slot reads.  Every product
+// and sum that remains is the one the full pass forms, and the skipped terms are exact
+// zeros, so the outputs equal the full pass's with G cleared (up to the sign of zeros).
 #include "sdm_internal.cuh"
 
 namespace sdm {
@@ -39,6 +52,8 @@ struct BwdArgs {
   float* G;
   float* dv;
   float* part;  // [BH, T, slices, 2W + R]: ge (W), gm (W), dr (R) of one column slice
+  const uint32_t* zflags;  // [BH, T, NW]: bit e = slot e of [write | read] sees a zero adjoint
+  int NW;                  // words of zflags per token; 0: G is the full adjoint on entry
   int T;
   long long N;
   int d_v, W, R;
@@ -77,9 +92,10 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
   float* kw = reinterpret_cast<float*>(smem);  // [W] write weights of the token
   float* rw = kw + W;                           // [R] read weights
   float* red = kw + WRa;                        // [2][warps][C], by token parity
-  // Two staging buffers of one token's [slots W | slots R | scores W | scores R]: the next
-  // token's (going backwards) arrive by cp.async while this one is processed.
-  int32_t* stg = reinterpret_cast<int32_t*>(red + 2 * kBwdWarps * C);  // [2][2 * WR]
+  // Two staging buffers of one token's [slots W | slots R | scores W | scores R | zero bits]:
+  // the next token's (going backwards) arrive by cp.async while this one is processed.
+  const int SB = 2 * WR + a.NW;
+  int32_t* stg = reinterpret_cast<int32_t*>(red + 2 * kBwdWarps * C);  // [2][SB]
 
   const int slices = d_v / C;
   const int bh = blockIdx.x / slices;
@@ -91,12 +107,13 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
 
   auto stage = [&](int t) {  // 4-byte cp.async per entry into buffer t & 1
     const size_t tk = size_t(bh) * T + t;
-    int32_t* dst = stg + (t & 1) * 2 * WR;
-    for (int e = tid; e < 2 * WR; e += kBwdThreads) {
+    int32_t* dst = stg + (t & 1) * SB;
+    for (int e = tid; e < SB; e += kBwdThreads) {
       const void* src = e < W ? static_cast<const void*>(a.idx_w + tk * W + e)
                       : e < WR ? static_cast<const void*>(a.idx_r + tk * R + (e - W))
                       : e < WR + W ? static_cast<const void*>(a.sc_w + tk * W + (e - WR))
-                                   : static_cast<const void*>(a.sc_r + tk * R + (e - WR - W));
+                      : e < 2 * WR ? static_cast<const void*>(a.sc_r + tk * R + (e - WR - W))
+                                   : static_cast<const void*>(a.zflags + tk * a.NW + (e - 2 * WR));
       asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
                        static_cast<uint32_t>(__cvta_generic_to_shared(dst + e))),
                    "l"(src)
@@ -110,9 +127,11 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
 
   for (int t = T - 1; t >= 0; --t) {
     const size_t tk = size_t(bh) * T + t;
-    const int32_t* iw = stg + (t & 1) * 2 * WR;
+    const int32_t* iw = stg + (t & 1) * SB;
     const int32_t* ir = iw + W;
     const float* scw = reinterpret_cast<const float*>(iw + WR);
+    const uint32_t* zb = reinterpret_cast<const uint32_t*>(iw + 2 * WR);
+    auto zero_at = [&](int e) { return a.NW != 0 && ((zb[e >> 5] >> (e & 31)) & 1u) != 0; };
     if (warp == 0) warp_softmax(scw, W, kw);
     if (warp == 1) warp_softmax(scw + W, R, rw);
     __syncthreads();
@@ -134,7 +153,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
         const bool ok = x[u] >= 0 && x[u] < a.N;  // uniform over the row's LPR lanes
         gv[u] = m[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (ok) {
-          gv[u] = reinterpret_cast<const float4*>(Gbh + size_t(x[u]) * d_v)[c4];
+          if (!zero_at(W + j)) gv[u] = reinterpret_cast<const float4*>(Gbh + size_t(x[u]) * d_v)[c4];
           m[u] = reinterpret_cast<const float4*>(a.r_rows + (tk * R + j) * d_v + c0)[c4];
         }
       }
@@ -164,6 +183,8 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
       for (int u = 0; u < NB; ++u) {
         const int i = ib + u * RPP + tid / LPR;
         x[u] = i < W ? iw[i] : -1;
+        // A zero adjoint row contributes nothing and stays zero: no loads, no store.
+        if (x[u] >= 0 && x[u] < a.N && zero_at(i)) x[u] = -1;
         g[u] = wp[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (x[u] >= 0 && x[u] < a.N) {
           g[u] = reinterpret_cast<const float4*>(Gbh + size_t(x[u]) * d_v)[c4];
@@ -219,9 +240,60 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
   }
 }
 
-size_t backward_smem_bytes(int C, int W, int R) {
+size_t backward_smem_bytes(int C, int W, int R, int NW) {
   const int WRa = (W + R + 3) & ~3;
-  return size_t(WRa) * 4 + size_t(2 * kBwdWarps) * C * 4 + size_t(4 * (W + R)) * 4;
+  return size_t(WRa) * 4 + size_t(2 * kBwdWarps) * C * 4 + size_t(2 * (2 * (W + R) + NW)) * 4;
+}
+
+// --- zero final adjoint: which slots see a zero adjoint row ---------------------------
+
+__global__ void fill_words_kernel(int32_t* __restrict__ p, int32_t value, size_t n) {
+  const size_t stride = size_t(gridDim.x) * blockDim.x;
+  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) p[i] = value;
+}
+
+// One warp per (b, h, t): last[bh][x] = max(last[bh][x], t) for every read slot x.
+__global__ void __launch_bounds__(256) last_read_kernel(const int32_t* __restrict__ idx_r, int T,
+                                                        int R, long long N, long long tokens,
+                                                        int32_t* __restrict__ last) {
+  const long long tok = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (tok >= tokens) return;
+  const long long bh = tok / T;
+  const int t = int(tok - bh * T);
+  int32_t* lb = last + bh * N;
+  for (int j = threadIdx.x & 31; j < R; j += 32) {
+    const int32_t x = idx_r[tok * R + j];
+    if (x >= 0 && x < N) atomicMax(lb + x, t);
+  }
+}
+
+// One warp per (b, h, t): bit e of the token's [write | read] slots is set when the adjoint
+// row at that slot is zero: a write slot whose row no read at token >= t selects, a read
+// slot whose row no read after t selects.  Slots outside [0, N) get 0.
+__global__ void __launch_bounds__(256) zero_flags_kernel(const int32_t* __restrict__ idx_w,
+                                                         const int32_t* __restrict__ idx_r, int T,
+                                                         int W, int R, long long N, long long tokens,
+                                                         const int32_t* __restrict__ last, int NW,
+                                                         uint32_t* __restrict__ zflags) {
+  const long long tok = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (tok >= tokens) return;
+  const int lane = threadIdx.x & 31;
+  const long long bh = tok / T;
+  const int t = int(tok - bh * T);
+  const int32_t* lb = last + bh * N;
+  for (int e0 = 0; e0 < W + R; e0 += 32) {
+    const int e = e0 + lane;
+    bool z = false;
+    if (e < W + R) {
+      const int32_t x = e < W ? idx_w[tok * W + e] : idx_r[tok * R + (e - W)];
+      if (x >= 0 && x < N) {
+        const int32_t l = lb[x];
+        z = e < W ? l < t : l == t;
+      }
+    }
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, z);
+    if (lane == 0) zflags[tok * NW + (e0 >> 5)] = m;
+  }
 }
 
 int backward_cols(int d_v) {
@@ -285,6 +357,47 @@ __global__ void __launch_bounds__(128) backward_finish_kernel(
   }
 }
 
+// Zero final adjoint: rows that no read selects hold no adjoint (G was never written
+// there), so they are set to zero, and dM0[h] (if given) = sum over the batch of G[b, h]
+// with those rows taken as zero, in the batch order of reduce_batch_kernel.  One warp per
+// (h, row), lanes over the row's float4 pieces.
+__global__ void __launch_bounds__(256) reduce_batch_zero_kernel(float4* __restrict__ G,
+                                                                float4* __restrict__ dM0,
+                                                                const int32_t* __restrict__ last,
+                                                                int B, long long rows, int dv4) {
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  const int lane = threadIdx.x & 31;
+  for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
+       row += warps) {
+    for (int c = lane; c < dv4; c += 32) {
+      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+      // Eight batch rows at a time: their table entries, then their loads, then the sums,
+      // so that the loads are in flight together.
+      for (int b0 = 0; b0 < B; b0 += 8) {
+        int32_t l[8];
+        float4 u[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          l[k] = b0 + k < B ? last[size_t(b0 + k) * size_t(rows) + size_t(row)] : 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          u[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (b0 + k < B && l[k] >= 0) u[k] = G[(size_t(b0 + k) * size_t(rows) + size_t(row)) * dv4 + c];
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int b = b0 + k;
+          if (b < B) {
+            if (l[k] < 0) __stcs(G + (size_t(b) * size_t(rows) + size_t(row)) * dv4 + c, u[k]);
+            s = b == 0 ? u[k] : make_float4(s.x + u[k].x, s.y + u[k].y, s.z + u[k].z, s.w + u[k].w);
+          }
+        }
+      }
+      if (dM0) dM0[size_t(row) * dv4 + c] = s;
+    }
+  }
+}
+
 // dM0[h] = sum over the batch of G[b, h].
 __global__ void reduce_batch_kernel(const float4* __restrict__ G, float4* __restrict__ dM0, int B,
                                     size_t per_batch4) {
@@ -320,6 +433,33 @@ __global__ void __launch_bounds__(128) select_backward_kernel(const int32_t* __r
   }
 }
 
+// Workspace of the reverse pass: [part | last-read table | zero bits], each piece 16-byte
+// aligned; the last two only with SDM_BWD_FINAL_ZERO.  0 on overflow or bad sizes.
+struct BwdWorkspace {
+  size_t part, last, zflags, total;
+};
+
+bool backward_workspace(int B, int H, int T, long long N, int d_v, int W, int R, unsigned flags,
+                        BwdWorkspace* ws) {
+  if (B < 1 || H < 1 || T < 0 || N < 1 || d_v < 4 || W < 1 || R < 1) return false;
+  const int C = backward_cols(d_v);
+  if (!C) return false;
+  auto up16 = [](size_t x) { return (x + 15) & ~size_t(15); };
+  const size_t lim = size_t(1) << 62;
+  const double approx = double(B) * H * (double(T) * (d_v / C) * (2.0 * W + R) * 4 + double(N) * 4 +
+                                         double(T) * ((W + R + 31) / 32) * 4);
+  if (approx > double(lim)) return false;
+  const size_t bh = size_t(B) * size_t(H);
+  ws->part = up16(bh * size_t(T) * size_t(d_v / C) * size_t(2 * W + R) * 4);
+  ws->last = ws->zflags = 0;
+  if (flags & SDM_BWD_FINAL_ZERO) {
+    ws->last = up16(bh * size_t(N) * 4);
+    ws->zflags = up16(bh * size_t(T) * size_t((W + R + 31) / 32) * 4);
+  }
+  ws->total = ws->part + ws->last + ws->zflags;
+  return true;
+}
+
 int grid_for(size_t work, int per_block) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -338,10 +478,16 @@ using namespace sdm;
 extern "C" {
 
 size_t sdm_scan_backward_workspace_size(int B, int H, int T, int d_v, int W, int R) {
-  if (B < 1 || H < 1 || T < 1 || d_v < 4 || W < 1 || R < 1) return 0;
-  const int C = backward_cols(d_v);
-  if (!C) return 0;
-  return size_t(B) * H * T * (d_v / C) * size_t(2 * W + R) * 4;
+  if (T < 1) return 0;
+  BwdWorkspace ws;
+  return backward_workspace(B, H, T, 1, d_v, W, R, 0u, &ws) ? ws.total : 0;
+}
+
+size_t sdm_scan_backward_workspace_size_ex(int B, int H, int T, long long N, int d_v, int W, int R,
+                                           unsigned flags) {
+  if (flags & ~unsigned(SDM_BWD_FINAL_ZERO)) return 0;
+  BwdWorkspace ws;
+  return backward_workspace(B, H, T, N, d_v, W, R, flags, &ws) ? ws.total : 0;
 }
 
 int sdm_scan_forward_train(float* M, const int32_t* idx_w, const float* sc_w,
@@ -372,6 +518,20 @@ int sdm_scan_backward(const int32_t* idx_w, const float* sc_w, const int32_t* id
                       float* G, float* dv, float* dalpha, float* dbeta, float* dsc_w,
                       float* dsc_r, float* dM0, void* workspace, size_t workspace_bytes,
                       void* stream) {
+  return sdm_scan_backward_ex(idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, w_prev, r_rows, dO, B,
+                              H, T, N, d_v, W, R, G, dv, dalpha, dbeta, dsc_w, dsc_r, dM0, 0u,
+                              workspace, workspace_bytes, stream);
+}
+
+int sdm_scan_backward_ex(const int32_t* idx_w, const float* sc_w, const int32_t* idx_r,
+                         const float* sc_r, const void* v, int v_dt, const float* alpha,
+                         const float* beta, const float* w_prev, const float* r_rows,
+                         const float* dO, int B, int H, int T, long long N, int d_v, int W, int R,
+                         float* G, float* dv, float* dalpha, float* dbeta, float* dsc_w,
+                         float* dsc_r, float* dM0, unsigned flags, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (flags & ~unsigned(SDM_BWD_FINAL_ZERO)) return SDM_EINVAL;
+  const bool zero_final = (flags & SDM_BWD_FINAL_ZERO) != 0;
   int st = check_scan_args(G, idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, B, H, T, N, d_v, W,
                            R, dv);
   if (st != SDM_OK) return st;
@@ -380,11 +540,35 @@ int sdm_scan_backward(const int32_t* idx_w, const float* sc_w, const int32_t* id
   cudaStream_t s = as_stream(stream);
   const size_t per_batch4 = size_t(H) * size_t(N) * d_v / 4;
   if (dM0 && !aligned16(dM0)) return SDM_EALIGN;
+  BwdWorkspace ws;
+  if (!backward_workspace(B, H, T, N, d_v, W, R, flags, &ws)) return SDM_EUNSUPPORTED;
+  if ((T > 0 || zero_final) && !aligned16(workspace)) return SDM_EALIGN;
+  if ((T > 0 || zero_final) && workspace_bytes < ws.total) return SDM_ENOSPACE;
+  unsigned char* wsb = static_cast<unsigned char*>(workspace);
+  int32_t* last = zero_final ? reinterpret_cast<int32_t*>(wsb + ws.part) : nullptr;
+  uint32_t* zflags = zero_final ? reinterpret_cast<uint32_t*>(wsb + ws.part + ws.last) : nullptr;
+  const int NW = zero_final ? (W + R + 31) / 32 : 0;
+  const long long tokens = (long long)B * H * T;
+  if (zero_final) {
+    const size_t n = size_t(B) * size_t(H) * size_t(N);
+    const int blocks = grid_for(n, 256);
+    if (blocks < 1) return SDM_ECUDA;
+    fill_words_kernel<<<blocks, 256, 0, s>>>(last, -1, n);
+    if (last_launch_status() != SDM_OK) return SDM_ECUDA;
+    if (tokens > 0) {
+      const long long tb = (tokens + 7) / 8;
+      if (tb > 0x7FFFFFFFLL) return SDM_EUNSUPPORTED;
+      last_read_kernel<<<unsigned(tb), 256, 0, s>>>(idx_r, T, R, N, tokens, last);
+      if (last_launch_status() != SDM_OK) return SDM_ECUDA;
+      zero_flags_kernel<<<unsigned(tb), 256, 0, s>>>(idx_w, idx_r, T, W, R, N, tokens, last, NW,
+                                                     zflags);
+      if (last_launch_status() != SDM_OK) return SDM_ECUDA;
+    }
+  }
   if (T > 0) {
     if (!aligned16(w_prev) || !aligned16(r_rows) || !aligned16(dO) || !aligned16(dalpha) ||
-        !aligned16(dbeta) || !aligned16(dsc_w) || !aligned16(dsc_r) || !aligned16(workspace))
+        !aligned16(dbeta) || !aligned16(dsc_w) || !aligned16(dsc_r))
       return SDM_EALIGN;
-    if (workspace_bytes < sdm_scan_backward_workspace_size(B, H, T, d_v, W, R)) return SDM_ENOSPACE;
     BwdArgs a;
     a.idx_w = idx_w;
     a.sc_w = sc_w;
@@ -399,13 +583,15 @@ int sdm_scan_backward(const int32_t* idx_w, const float* sc_w, const int32_t* id
     a.dO = dO;
     a.G = G;
     a.dv = dv;
-    a.part = static_cast<float*>(workspace);
+    a.part = reinterpret_cast<float*>(wsb);
+    a.zflags = zflags;
+    a.NW = NW;
     a.T = T;
     a.N = N;
     a.d_v = d_v;
     a.W = W;
     a.R = R;
-    const int smem = int(backward_smem_bytes(C, W, R));
+    const int smem = int(backward_smem_bytes(C, W, R, NW));
     const void* fn = C == 32   ? reinterpret_cast<const void*>(&scan_backward_kernel<32>)
                      : C == 16 ? reinterpret_cast<const void*>(&scan_backward_kernel<16>)
                      : C == 8  ? reinterpret_cast<const void*>(&scan_backward_kernel<8>)
@@ -417,7 +603,7 @@ int sdm_scan_backward(const int32_t* idx_w, const float* sc_w, const int32_t* id
                          size_t(smem), s) != cudaSuccess)
       return SDM_ECUDA;
     // finish: one warp per (b, h, t)
-    const long long items = (long long)B * H * T;
+    const long long items = tokens;
     const int fsmem = 4 * 2 * (W + R) * 4;
     if (cudaFuncSetAttribute(reinterpret_cast<const void*>(&backward_finish_kernel),
                              cudaFuncAttributeMaxDynamicSharedMemorySize, fsmem) != cudaSuccess)
@@ -425,6 +611,15 @@ int sdm_scan_backward(const int32_t* idx_w, const float* sc_w, const int32_t* id
     backward_finish_kernel<<<unsigned((items + 3) / 4), 128, fsmem, s>>>(
         sc_w, sc_r, beta, a.part, d_v / C, W, R, items, dalpha, dbeta, dsc_w, dsc_r);
     if (last_launch_status() != SDM_OK) return SDM_ECUDA;
+  }
+  if (zero_final) {
+    const long long rows = (long long)H * N;
+    const int blocks = grid_for(size_t(rows), 8);
+    if (blocks < 1) return SDM_ECUDA;
+    reduce_batch_zero_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<float4*>(G),
+                                                     reinterpret_cast<float4*>(dM0), last, B, rows,
+                                                     d_v / 4);
+    return last_launch_status();
   }
   if (dM0) {
     const int blocks = grid_for(per_batch4, 256);

@@ -209,3 +209,31 @@ def test_bounded_wait_check_rejects_bad_arguments_without_launching():
     assert call(0, 1000, None) == EINVAL                # the error word is required
     assert call(0, 1000, ctypes.c_void_p((1 << 20) + 2)) == EALIGN
     assert call(0, 1000, ok, ctypes.c_void_p((1 << 20) + 4)) == EALIGN
+
+
+def test_backward_flags_and_workspace_sizes():
+    """sdm_scan_backward_ex: the zero-final-adjoint flag's workspace (part | last-read table |
+    zero bits, each rounded to 16 bytes), unknown flags refused, size checks before launching."""
+    lib = sdm.lib()
+    B, H, T, N, dv, W, R = 2, 3, 10, 64, 16, 5, 7
+    part = B * H * T * 1 * (2 * W + R) * 4            # d_v = 16: one 16-column slice per (b, h)
+    assert lib.sdm_scan_backward_workspace_size(B, H, T, dv, W, R) == part
+    assert lib.sdm_scan_backward_workspace_size_ex(B, H, T, N, dv, W, R, 0) == part
+    up16 = lambda x: (x + 15) // 16 * 16
+    assert lib.sdm_scan_backward_workspace_size_ex(B, H, T, N, dv, W, R, 1) == (
+        up16(part) + up16(B * H * N * 4) + up16(B * H * T * 1 * 4))
+    assert lib.sdm_scan_backward_workspace_size_ex(1, 1, 5, 64, 8, 40, 33, 1) == (
+        up16(5 * 1 * 113 * 4) + up16(64 * 4) + up16(5 * 3 * 4))   # W + R = 73: three words
+    assert lib.sdm_scan_backward_workspace_size_ex(B, H, T, N, dv, W, R, 2) == 0
+    assert lib.sdm_scan_backward_workspace_size_ex(B, H, 0, N, dv, W, R, 1) == up16(B * H * N * 4)
+
+    def call(flags=1, ws=FAKE, ws_bytes=1 << 30, dv_=dv, G=FAKE):
+        return lib.sdm_scan_backward_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE, B, H, T, N,
+                                        dv_, W, R, G, FAKE, FAKE, FAKE, FAKE, FAKE, None, flags, ws, ws_bytes, None)
+
+    assert call(flags=2) == EINVAL
+    assert call(flags=3) == EINVAL
+    assert call(dv_=6) == EINVAL
+    assert call(ws=ODD) == EALIGN
+    assert call(G=ODD) == EALIGN
+    assert call(ws_bytes=up16(part)) == ENOSPACE      # the zero flag needs the table and the bits

@@ -20,6 +20,28 @@ def test_scan_bytes_per_head_token():
     assert bench.scan_bytes_per_head_token(wl.TINY_F32) == 1_672
 
 
+def test_zero_adjoint_slots_brute_force():
+    """The zero-adjoint slot counts behind the backward's roofline bytes, against a brute
+    force over every slot: a write slot at t is zero when no read at t' >= t selects its
+    row, a read slot when no read at t' > t does."""
+    import numpy as np
+    import torch
+    rng = np.random.default_rng(5)
+    B, H, T, W, R, N = 2, 3, 30, 4, 5, 24
+    iw = rng.integers(0, N, (B, H, T, W)).astype(np.int32)
+    ir = np.stack([[[rng.choice(N, R, replace=False) for _ in range(T)] for _ in range(H)] for _ in range(B)])
+    ir = ir.astype(np.int32)
+    sel = (torch.from_numpy(iw), None, torch.from_numpy(ir), None)
+    zw = zr = 0
+    for b in range(B):
+        for h in range(H):
+            for t in range(T):
+                zw += sum(all(x not in ir[b, h, u] for u in range(t, T)) for x in iw[b, h, t])
+                zr += sum(all(x not in ir[b, h, u] for u in range(t + 1, T)) for x in ir[b, h, t])
+    assert bench.zero_adjoint_slots(sel, N, torch) == (zw, zr)
+    assert 0 < zw < B * H * T * W and 0 < zr < B * H * T * R
+
+
 def test_whole_job_rate_counts_every_rank_over_the_slowest_time():
     # 2 ranks x 1000 units x 5 steps in 250 ms
     assert bench.whole_job_rate(1000, 5, 2, 250.0) == pytest.approx(40_000.0)

@@ -127,9 +127,57 @@ def test_forward_train_equals_forward_and_keeps_the_rows():
     assert float((o_rows - o2.double()).abs().max()) <= 1e-5
 
 
-def test_backward_on_the_small_workload_sampled_heads():
+OUTPUTS = ("dv", "dalpha", "dbeta", "dsc_w", "dsc_r", "dM0")
+
+
+@pytest.mark.parametrize("B,H,T,S,dv,W,R,vdt", [
+    (1, 1, 1, 4, 4, 2, 3, torch.float32),          # one token: every slot's adjoint is zero
+    (2, 2, 50, 8, 16, 6, 5, torch.float32),
+    (1, 3, 97, 6, 24, 9, 20, torch.bfloat16),
+    (2, 1, 300, 16, 64, 64, 64, torch.bfloat16),   # rows rewritten and reread across tokens
+    (1, 2, 40, 4, 32, 16, 16, torch.float32),      # W = R = N: only the last token's read slots are zero
+    (3, 1, 70, 12, 8, 40, 33, torch.float32),      # W + R = 73: three words of zero bits, ragged
+])
+def test_final_zero_equals_the_cleared_adjoint(B, H, T, S, dv, W, R, vdt):
+    """sdm_scan_backward_ex with SDM_BWD_FINAL_ZERO, G filled with NaN on entry, gives the
+    values of the full pass with G cleared (torch.equal: equal values, a zero's sign aside),
+    twice in a row on one workspace (the previous call's table and bits are stale)."""
+    rng = np.random.default_rng(7 * T + W + R)
+    host, dev, M0, dO, dMT = _random(rng, B, H, T, S, dv, vdt)
+    sel = sdm.select(dev["kp"], dev["qp"], W, R)
+    M = torch.from_numpy(np.broadcast_to(M0[None], (B,) + M0.shape).copy()).cuda()
+    o, w_prev, r_rows = sdm.scan_forward_train(M, *sel, dev["v"], dev["alpha"], dev["beta"])
+    dO_d = torch.from_numpy(dO).cuda()
+    N = S * S
+    G_ref = torch.zeros((B, H, N, dv), device="cuda")
+    ref = sdm.scan_backward(*sel, dev["v"], dev["alpha"], dev["beta"], w_prev, r_rows, dO_d, G_ref)
+    ws = torch.empty(sdm.backward_workspace_size(B, H, T, N, dv, W, R, True), dtype=torch.uint8, device="cuda")
+    for rep in range(2):
+        G = torch.full((B, H, N, dv), float("nan"), device="cuda")
+        got = sdm.scan_backward(*sel, dev["v"], dev["alpha"], dev["beta"], w_prev, r_rows, dO_d, G, workspace=ws,
+                                final_zero=True)
+        torch.cuda.synchronize()
+        for name in OUTPUTS:
+            assert torch.equal(got[name], ref[name]), (rep, name)
+        assert torch.equal(G, G_ref), rep
+
+
+def test_final_zero_with_no_tokens_clears_the_adjoint():
+    B, H, N, dv, W, R = 2, 2, 64, 8, 4, 4
+    e = lambda *sh, dt=torch.float32: torch.empty(sh, dtype=dt, device="cuda")
+    sel = (e(B, H, 0, W, dt=torch.int32), e(B, H, 0, W), e(B, H, 0, R, dt=torch.int32), e(B, H, 0, R))
+    G = torch.full((B, H, N, dv), float("nan"), device="cuda")
+    g = sdm.scan_backward(*sel, e(B, H, 0, dv), e(B, H, 0), e(B, H, 0), e(B, H, 0, W, dv), e(B, H, 0, R, dv),
+                          e(B, H, 0, dv), G, final_zero=True)
+    torch.cuda.synchronize()
+    assert torch.equal(G, torch.zeros_like(G))
+    assert torch.equal(g["dM0"], torch.zeros_like(g["dM0"]))
+
+
+@pytest.mark.parametrize("final_zero", [False, True])
+def test_backward_on_the_small_workload_sampled_heads(final_zero):
     """B4 H8 T2048 N=65,536 d_v=64 W=R=32, bf16 inputs: the whole backward on the GPU,
-    the oracle on two heads."""
+    the oracle on two heads (dL/dM_T = 0; with final_zero, G starts as NaN and is ignored)."""
     cfg = wl.B4H8_T2048
     d = device_inputs(cfg)
     M0 = device_M0(cfg)
@@ -139,8 +187,9 @@ def test_backward_on_the_small_workload_sampled_heads():
     o, w_prev, r_rows = sdm.scan_forward_train(M, *sel, d["v"], d["alpha"], d["beta"])
     rng = np.random.default_rng(21)
     dO = torch.from_numpy(rng.standard_normal((cfg.B, cfg.H, cfg.T, cfg.d_v)).astype(np.float32)).cuda()
-    G = torch.zeros((cfg.B, cfg.H, cfg.N, cfg.d_v), device="cuda")
-    g = sdm.scan_backward(*sel, d["v"], d["alpha"], d["beta"], w_prev, r_rows, dO, G, shared_M0=False)
+    G = torch.full((cfg.B, cfg.H, cfg.N, cfg.d_v), float("nan") if final_zero else 0.0, device="cuda")
+    g = sdm.scan_backward(*sel, d["v"], d["alpha"], d["beta"], w_prev, r_rows, dO, G, shared_M0=False,
+                          final_zero=final_zero)
     torch.cuda.synchronize()
     M0h = M0.cpu().numpy()
     for b, h in ((0, 0), (cfg.B - 1, cfg.H - 1)):
