@@ -384,6 +384,21 @@ int sdm_project_select(const void* x, const void* w, int B, int T, int D, int H,
 int sdm_test_bounded_wait(int mode, unsigned long long limit_ns, int* dev_err,
                           unsigned long long* elapsed_ns, void* stream);
 
+/* sdm_test_project_stall - test of the projection kernel's stop and drain path (not part of
+ * the method): sdm_project_kq_tuned(..., max_ctas 0, pair) in which the copy-issuing thread
+ * of cluster rank stall_cta (0 or, with pair 2, 1) stops issuing after stall_step K steps,
+ * as if its copies could not be issued, and every wait inside the kernel gives up after
+ * wait_ns.  The waits for the missing copies then run out, the blocks stop, wait for every
+ * copy they (and, in a pair, the peer block) issued to land, free their tensor memory and
+ * OR SDM_DEV_TIMEOUT into *dev_err (device int, required); kp, qp are unspecified.  With
+ * pair 2 one rank's producer runs ahead of the other's, so the pair's drain meets phases
+ * only one of them issued.  Requires the arguments of sdm_project_kq, pair 0 or 2 (2: B*T >
+ * 128), 10^5 <= wait_ns <= 10^9 (SDM_EINVAL otherwise).  Nothing waits longer than wait_ns
+ * for something that cannot happen, so the call returns and the context stays usable. */
+int sdm_test_project_stall(const void* x, const void* w, int B, int T, int D, int H, int S,
+                           void* kp, void* qp, int pair, int stall_cta, int stall_step,
+                           unsigned long long wait_ns, int* dev_err, void* stream);
+
 /* sdm_gen_inputs - synthetic inputs (not part of the method): draws the box
  * b in [b_off, b_off+B), all H heads, tokens t in [t_off, t_off+T) of a logical
  * workload with T_total tokens per sequence, from the counter-based generator

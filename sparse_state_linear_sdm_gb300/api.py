@@ -73,6 +73,7 @@ def lib() -> ctypes.CDLL:
             L.sdm_decode_step_supported.argtypes = [i, i, i, i, i, i, i]
             L.sdm_project_kq_tuned.argtypes = [p, p, i, i, i, i, i, p, p, p, i, i, p]
             L.sdm_test_bounded_wait.argtypes = [i, ull, p, p, p]
+            L.sdm_test_project_stall.argtypes = [p, p, i, i, i, i, i, p, p, i, i, i, ull, p, p]
             L.sdm_fill_state.argtypes = [p, f, i, i, ll, i, p]
             L.sdm_project_select_workspace_size.argtypes = [i, i, i, i, i, i]
             L.sdm_project_select_workspace_size.restype = sz
@@ -81,7 +82,7 @@ def lib() -> ctypes.CDLL:
                          "sdm_scan_forward_tuned", "sdm_scan_launch_info", "sdm_gen_inputs", "sdm_gen_M0",
                          "sdm_forward_chunks", "sdm_forward_tuned", "sdm_forward", "sdm_scan_forward_train",
                          "sdm_scan_backward", "sdm_scan_backward_ex", "sdm_select_backward", "sdm_project_select",
-                         "sdm_fill_state"):
+                         "sdm_fill_state", "sdm_test_project_stall"):
                 getattr(L, name).restype = i
             _lib = L
     return _lib
@@ -584,6 +585,24 @@ def bounded_wait_check(mode: int, limit_ns: int, device="cuda"):
               _stream(dev_err.device))
     torch.cuda.synchronize(dev_err.device)
     return int(dev_err.item()), int(elapsed.item())
+
+
+@_on_tensor_device
+def project_stall_check(x, w, H: int, S: int, pair: int, stall_cta: int, stall_step: int, wait_ns: int):
+    """The projection kernel with the copy-issuing thread of cluster rank `stall_cta` stopping
+    after `stall_step` K steps and every wait limited to wait_ns (sdm_test_project_stall):
+    the kernel must stop, drain its copies and report.  Returns the error word (the
+    SDM_DEV_TIMEOUT bit set when it stopped).  Synchronises the device."""
+    _need(x, "x", torch.bfloat16)
+    _need(w, "w", torch.bfloat16)
+    B, T, D = x.shape
+    kp = torch.empty((B, H, T, 2, S), dtype=torch.bfloat16, device=x.device)
+    qp = torch.empty_like(kp)
+    dev_err = torch.zeros(1, dtype=torch.int32, device=x.device)
+    _call("sdm_test_project_stall", _p(x), _p(w), B, T, D, H, S, _p(kp), _p(qp), int(pair), int(stall_cta),
+          int(stall_step), ctypes.c_ulonglong(wait_ns), _p(dev_err), _stream(x.device))
+    torch.cuda.synchronize(x.device)
+    return int(dev_err.item())
 
 
 @_on_tensor_device

@@ -117,6 +117,22 @@ int sdm_project_kq(const void* x, const void* w, int B, int T, int D, int H, int
   return sdm_project_kq_tuned(x, w, B, T, D, H, S, kp, qp, dev_err, 0, -1, stream);
 }
 
+int sdm_test_project_stall(const void* x, const void* w, int B, int T, int D, int H, int S,
+                           void* kp, void* qp, int pair, int stall_cta, int stall_step,
+                           unsigned long long wait_ns, int* dev_err, void* stream) {
+  if (B < 1 || T < 1 || H < 1 || S < 1 || D < 8 || D % 8 || (pair != 0 && pair != 2) ||
+      stall_cta < 0 || stall_cta > (pair == 2 ? 1 : 0) || stall_step < 0 || wait_ns < 100000ull ||
+      wait_ns > 1000000000ull || !dev_err)
+    return SDM_EINVAL;
+  if (S > SDM_MAX_S) return SDM_EUNSUPPORTED;
+  if (1LL * B * T >= (1LL << 31) || 4LL * H * S >= (1LL << 31)) return SDM_EUNSUPPORTED;
+  if (pair == 2 && 1LL * B * T <= 128) return SDM_EUNSUPPORTED;  // one row tile: no pair
+  if (!aligned16(x) || !aligned16(w) || !aligned16(kp) || !aligned16(qp)) return SDM_EALIGN;
+  if (reinterpret_cast<uintptr_t>(dev_err) & 3u) return SDM_EALIGN;
+  const ProjectStall stall{stall_cta, stall_step, wait_ns};
+  return launch_project(x, w, B, T, D, H, S, kp, qp, dev_err, 0, pair, as_stream(stream), &stall);
+}
+
 int sdm_test_bounded_wait(int mode, unsigned long long limit_ns, int* dev_err,
                           unsigned long long* elapsed_ns, void* stream) {
   if (mode < 0 || mode > 2 || limit_ns > 1000000000ull || !dev_err) return SDM_EINVAL;

@@ -360,38 +360,71 @@ __global__ void __launch_bounds__(128) backward_finish_kernel(
 // Zero final adjoint: rows that no read selects hold no adjoint (G was never written
 // there), so they are set to zero, and dM0[h] (if given) = sum over the batch of G[b, h]
 // with those rows taken as zero, in the batch order of reduce_batch_kernel.  One warp per
-// (h, row), lanes over the row's float4 pieces.
+// group of 32 rows of (h, row): lane j first reads row j's table entry of every batch row
+// (coalesced) into a bit mask, so that the G loads that follow depend on no other load;
+// then the lanes cover the group's float4 pieces.  B <= 32 (the host takes the plain loop
+// of reduce_batch_zero_wide_kernel beyond).
 __global__ void __launch_bounds__(256) reduce_batch_zero_kernel(float4* __restrict__ G,
                                                                 float4* __restrict__ dM0,
                                                                 const int32_t* __restrict__ last,
                                                                 int B, long long rows, int dv4) {
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
   const int lane = threadIdx.x & 31;
-  for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
-       row += warps) {
-    for (int c = lane; c < dv4; c += 32) {
+  const long long groups = (rows + 31) / 32;
+  for (long long g = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); g < groups;
+       g += warps) {
+    const long long row0 = g * 32;
+    const int nrows = int(min(32LL, rows - row0));
+    uint32_t bits = 0;  // bit b: batch row b reads row row0 + lane
+    if (lane < nrows)
+      for (int b = 0; b < B; ++b)
+        bits |= uint32_t(last[size_t(b) * size_t(rows) + size_t(row0 + lane)] >= 0) << b;
+    for (int e0 = 0; e0 < 32 * dv4; e0 += 32) {
+      const int e = e0 + lane, r = e / dv4, c = e - r * dv4;
+      const uint32_t m = __shfl_sync(0xFFFFFFFFu, bits, r & 31);
+      if (r >= nrows) continue;
+      const size_t row = size_t(row0 + r);
       float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-      // Eight batch rows at a time: their table entries, then their loads, then the sums,
-      // so that the loads are in flight together.
       for (int b0 = 0; b0 < B; b0 += 8) {
-        int32_t l[8];
         float4 u[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          l[k] = b0 + k < B ? last[size_t(b0 + k) * size_t(rows) + size_t(row)] : 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           u[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (b0 + k < B && l[k] >= 0) u[k] = G[(size_t(b0 + k) * size_t(rows) + size_t(row)) * dv4 + c];
+          if (b0 + k < B && ((m >> (b0 + k)) & 1u)) u[k] = G[(size_t(b0 + k) * size_t(rows) + row) * dv4 + c];
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int b = b0 + k;
           if (b < B) {
-            if (l[k] < 0) __stcs(G + (size_t(b) * size_t(rows) + size_t(row)) * dv4 + c, u[k]);
+            if (!((m >> b) & 1u)) __stcs(G + (size_t(b) * size_t(rows) + row) * dv4 + c, u[k]);
             s = b == 0 ? u[k] : make_float4(s.x + u[k].x, s.y + u[k].y, s.z + u[k].z, s.w + u[k].w);
           }
         }
+      }
+      if (dM0) dM0[row * dv4 + c] = s;
+    }
+  }
+}
+
+// The same for any B: one warp per (h, row), the table entry read before each load.
+__global__ void __launch_bounds__(256) reduce_batch_zero_wide_kernel(float4* __restrict__ G,
+                                                                     float4* __restrict__ dM0,
+                                                                     const int32_t* __restrict__ last,
+                                                                     int B, long long rows, int dv4) {
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  const int lane = threadIdx.x & 31;
+  for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
+       row += warps) {
+    for (int c = lane; c < dv4; c += 32) {
+      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int b = 0; b < B; ++b) {
+        const size_t rb = size_t(b) * size_t(rows) + size_t(row);
+        float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (last[rb] >= 0)
+          u = G[rb * dv4 + c];
+        else
+          __stcs(G + rb * dv4 + c, u);
+        s = b == 0 ? u : make_float4(s.x + u.x, s.y + u.y, s.z + u.z, s.w + u.w);
       }
       if (dM0) dM0[size_t(row) * dv4 + c] = s;
     }
@@ -614,11 +647,16 @@ int sdm_scan_backward_ex(const int32_t* idx_w, const float* sc_w, const int32_t*
   }
   if (zero_final) {
     const long long rows = (long long)H * N;
-    const int blocks = grid_for(size_t(rows), 8);
+    const int blocks = grid_for(size_t(B <= 32 ? (rows + 31) / 32 : rows), 8);
     if (blocks < 1) return SDM_ECUDA;
-    reduce_batch_zero_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<float4*>(G),
-                                                     reinterpret_cast<float4*>(dM0), last, B, rows,
-                                                     d_v / 4);
+    if (B <= 32)
+      reduce_batch_zero_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<float4*>(G),
+                                                       reinterpret_cast<float4*>(dM0), last, B, rows,
+                                                       d_v / 4);
+    else
+      reduce_batch_zero_wide_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<float4*>(G),
+                                                            reinterpret_cast<float4*>(dM0), last, B,
+                                                            rows, d_v / 4);
     return last_launch_status();
   }
   if (dM0) {

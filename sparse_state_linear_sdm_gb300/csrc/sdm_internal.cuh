@@ -216,8 +216,16 @@ int launch_decode(const void* kp, const void* qp, int in_dt, const void* v, int 
                   const float* alpha, const float* beta, float* M, int BH, int S, int d_v, int W,
                   int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, float* o,
                   int* dev_err, cudaStream_t s);
+// Tests of the projection kernels' timeout path: the producer of cluster rank `cta` (0 for
+// the single-CTA kernel) stops issuing copies after `step` K steps, and every wait gives up
+// after wait_ns, so that the kernel stops, drains and reports SDM_DEV_TIMEOUT.
+struct ProjectStall {
+  int cta, step;
+  unsigned long long wait_ns;
+};
 int launch_project(const void* x, const void* w, int B, int T, int D, int H, int S, void* kp,
-                   void* qp, int* dev_err, int max_ctas, int pair, cudaStream_t s);
+                   void* qp, int* dev_err, int max_ctas, int pair, cudaStream_t s,
+                   const ProjectStall* stall = nullptr);
 // Projections fused with the inner top-k of every half, then the outer top-K (two kernels).
 size_t project_select_workspace(int B, int T, int H, int S, int W, int R);
 int launch_project_select(const void* x, const void* w, int B, int T, int D, int H, int S, int W,

@@ -67,6 +67,9 @@ struct ProjArgs {
   uint16_t* kp;
   uint16_t* qp;
   int* dev_err;
+  unsigned long long wait_ns;  // time limit of every wait (kWaitNs outside tests)
+  int stall_cta;               // tests only: this cluster rank's producer stops issuing after
+  int stall_step;              // stall_step K steps (-1: never), so that a wait runs out
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -88,6 +91,11 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Counts `bytes` of the current phase's transactions as done without a copy.
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
 }
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -154,12 +162,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
-}
-
-__device__ void pause_ns(unsigned long long ns) {
-  const unsigned long long t0 = global_ns();
-  for (uint32_t i = 0; i < (1u << 24) && global_ns() - t0 < ns; ++i) {
-  }
 }
 
 // Shared-memory matrix descriptor of a K-major operand tile in the 128-byte swizzle layout
@@ -321,21 +323,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  uint32_t used = 0, last_par = 0;  // producer: per stage, ever loaded / parity of its last load
   if (warp == 0) {
     if (lane == 0) {
       // ---- TMA producer ----
-      int stage = 0;
-      uint32_t phase = 0, used = 0, last_par = 0;  // per stage: ever loaded / parity of last load
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
       bool ok = true;
       for (int u = cid; ok && u < units; u += ncl) {
         int mp, n;
         unit_coords(u, MP, NT, mp, n);
         const int m0 = mp * BM, n0 = n * BN;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(bar(EMPTY + stage), phase ^ 1u, stop)) {
+          if (a.stall_cta == 0 && issued >= a.stall_step) {
             ok = false;
             break;
           }
+          if (!mbar_wait(bar(EMPTY + stage), phase ^ 1u, stop, a.wait_ns)) {
+            ok = false;
+            break;
+          }
+          ++issued;
           const uint32_t sa = ring + uint32_t(stage) * STAGE_BYTES;
           mbar_expect_tx(bar(FULL + stage), STAGE_BYTES);
           tma_load_2d(sa, &tmX, kb * BK, m0, bar(FULL + stage));
@@ -349,10 +357,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!ok) {  // let every copy in flight land before the CTA's shared memory goes away
-        for (int s = 0; s < STAGES; ++s)
-          if (used & (1u << s)) mbar_wait_teardown(bar(FULL + s), (last_par >> s) & 1u);
-      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -364,11 +368,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = cid; ok && u < units; u += ncl, ++it) {
         const int acc = it & 1;
         const uint32_t acc_par = uint32_t(it >> 1) & 1u;
-        if (!mbar_wait(bar(ACC_EMPTY + acc), acc_par ^ 1u, stop)) break;
+        if (!mbar_wait(bar(ACC_EMPTY + acc), acc_par ^ 1u, stop, a.wait_ns)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + uint32_t(acc * BN);
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(bar(FULL + stage), phase, stop)) {
+          if (!mbar_wait(bar(FULL + stage), phase, stop, a.wait_ns)) {
             ok = false;
             break;
           }
@@ -399,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int acc = it & 1;
       const uint32_t acc_par = uint32_t(it >> 1) & 1u;
       // every lane waits; the warp leaves together (tcgen05.ld needs the whole warp)
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(ACC_FULL + acc), acc_par, stop))) break;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(ACC_FULL + acc), acc_par, stop, a.wait_ns))) break;
       tc_fence_after();
       int mp, n;
       unit_coords(u, MP, NT, mp, n);
@@ -425,6 +429,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"(kTmemCols)
                  : "memory");
+  // After a stop, whichever role raised it, every copy issued lands before the CTA's shared
+  // memory goes away: the last phase of each stage the producer loaded has completed.
+  if (warp == 0 && lane == 0 && *stop)
+    for (int s = 0; s < STAGES; ++s)
+      if (used & (1u << s)) mbar_wait_teardown(bar(FULL + s), (last_par >> s) & 1u);
   if (threadIdx.x == 0 && *stop && a.dev_err) atomicOr(a.dev_err, SDM_DEV_TIMEOUT);
 }
 
@@ -439,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // CTAs; the epilogue warps of both arrive on the leader's accumulator-empty barrier.
 constexpr int STAGES2 = 6;
 constexpr int STAGE2_BYTES = A_BYTES + B_BYTES / 2;
-constexpr int kSmemBytes2 = STAGES2 * STAGE2_BYTES + 1024 + 256;
+constexpr int kSmemBytes2 = STAGES2 * STAGE2_BYTES + 1024 + 256;  // + barriers, flags, counts
 constexpr int kNumBars2 = 2 * STAGES2 + 5;
 constexpr uint32_t kIdesc2 = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) |
                              (uint32_t((2 * BM) >> 4) << 24);
@@ -463,18 +472,29 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
       : "memory");
   return ok != 0;
 }
-// mbar_wait with cluster-scope acquire (barriers that the peer CTA arrives on).
-__device__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* stop) {
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t cluster_addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+// mbar_wait with cluster-scope acquire (barriers that the peer CTA arrives on).  Giving up
+// raises the stop flags of both CTAs of the pair (peer_stop: the peer's flag).
+__device__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* stop,
+                                  uint32_t peer_stop, unsigned long long limit_ns) {
   if (mbar_test_cluster(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t i = 1; i < (1u << 28); ++i) {
     if (mbar_test_cluster(bar, parity)) return true;
     if ((i & 31u) == 0) {
       if (*stop) return false;
-      if (global_ns() - t0 > kWaitNs) break;
+      if (global_ns() - t0 > limit_ns) break;
     }
   }
   *stop = 1;
+  st_cluster_u32(peer_stop, 1u);
   return false;
 }
 // A box loaded into this CTA's shared memory, completing on a barrier of either CTA of the pair.
@@ -517,6 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + (ring - raw) + STAGES2 * STAGE2_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars2);
   volatile int* stop = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // Copies this CTA's producer issued per stage (read by the leader after a stop).
+  volatile uint32_t* issued = tmem_slot + 2;
   const int FULL = 0, EMPTY = STAGES2, ACC_FULL = 2 * STAGES2, ACC_EMPTY = 2 * STAGES2 + 2,
             DRAIN = 2 * STAGES2 + 4;
   auto bar = [&](int i) { return smem_u32(bars + i); };
@@ -524,6 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const bool leader = rank == 0;
+  const uint32_t peer_stop = cluster_addr(smem_u32(const_cast<int*>(stop)), rank ^ 1u);
   const int cid = blockIdx.x / 2, ncl = gridDim.x / 2;
   const int NT = (a.Ncols + BN - 1) / BN;
   const int MP = ((a.Mrows + BM - 1) / BM + 1) / 2;
@@ -541,6 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(DRAIN), 1);
     *stop = 0;
+    for (int s = 0; s < STAGES2; ++s) issued[s] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
@@ -561,36 +585,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---- TMA producer (both CTAs) ----
-      int stage = 0;
-      uint32_t phase = 0, used = 0, last_par = 0;
+      int stage = 0, steps = 0;
+      uint32_t phase = 0;
       bool ok = true;
       for (int u = cid; ok && u < units; u += ncl) {
         int mp, n;
         unit_coords(u, MP, NT, mp, n);
         const int m0 = (mp * 2 + int(rank)) * BM, n0 = n * BN;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_cluster(bar(EMPTY + stage), phase ^ 1u, stop)) {
+          if (int(rank) == a.stall_cta && steps >= a.stall_step) {
             ok = false;
             break;
           }
+          if (!mbar_wait_cluster(bar(EMPTY + stage), phase ^ 1u, stop, peer_stop, a.wait_ns)) {
+            ok = false;
+            break;
+          }
+          ++steps;
           const uint32_t sa = ring + uint32_t(stage) * STAGE2_BYTES;
           const uint32_t full_leader = cluster_addr(bar(FULL + stage), 0);
           if (leader) mbar_expect_tx(bar(FULL + stage), 2 * STAGE2_BYTES);
           tma_load_2d_pair(sa, &tmX, kb * BK, m0, full_leader);
           tma_load_2d_pair(sa + A_BYTES, &tmW, kb * BK, n0 + int(rank) * (BN / 2), full_leader);
-          used |= 1u << stage;
-          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          issued[stage] = issued[stage] + 1u;
           if (++stage == STAGES2) {
             stage = 0;
             phase ^= 1u;
           }
         }
-      }
-      if (!ok) {
-        if (leader)
-          for (int s = 0; s < STAGES2; ++s)
-            if (used & (1u << s)) mbar_wait_teardown(bar(FULL + s), (last_par >> s) & 1u);
-        pause_ns(200000);
       }
     }
   } else if (warp == 1) {
@@ -603,11 +625,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = cid; ok && u < units; u += ncl, ++it) {
         const int acc = it & 1;
         const uint32_t acc_par = uint32_t(it >> 1) & 1u;
-        if (!mbar_wait_cluster(bar(ACC_EMPTY + acc), acc_par ^ 1u, stop)) break;
+        if (!mbar_wait_cluster(bar(ACC_EMPTY + acc), acc_par ^ 1u, stop, peer_stop, a.wait_ns)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + uint32_t(acc * BN);
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_cluster(bar(FULL + stage), phase, stop)) {
+          if (!mbar_wait_cluster(bar(FULL + stage), phase, stop, peer_stop, a.wait_ns)) {
             ok = false;
             break;
           }
@@ -636,7 +658,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = cid; u < units; u += ncl, ++it) {
       const int acc = it & 1;
       const uint32_t acc_par = uint32_t(it >> 1) & 1u;
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait_cluster(bar(ACC_FULL + acc), acc_par, stop))) break;
+      if (!__all_sync(0xFFFFFFFFu,
+                      mbar_wait_cluster(bar(ACC_FULL + acc), acc_par, stop, peer_stop, a.wait_ns)))
+        break;
       tc_fence_after();
       int mp, n;
       unit_coords(u, MP, NT, mp, n);
@@ -657,14 +681,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();  // the leader's MMAs into both CTAs' TMEM are done before either frees it
+  // Every role of both CTAs has finished: the leader's MMAs into both CTAs' TMEM are done
+  // before either frees it, and both producers' copy counts and stop flags are final.
+  cluster_sync_all();
   tc_fence_after();
   if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"(kTmemCols)
                  : "memory");
+  if (leader && warp == 0 && lane == 0 && *stop) {
+    // After a stop, every copy either CTA issued lands before the pair's shared memory goes
+    // away.  All copies of a stage complete on the leader's full barrier, which the leader
+    // arms with both CTAs' bytes; per stage the two producers issued the same number of
+    // copies or one more than the other (each is at most one round of stages ahead of the
+    // MMAs, which need both halves).  The leader arms a phase only the peer issued with the
+    // peer's bytes, counts the peer's missing bytes of a phase only it issued as done, and
+    // waits for the last phase of each stage.
+    const uint32_t peer_issued = cluster_addr(smem_u32(const_cast<uint32_t*>(issued)), 1u);
+    for (int s = 0; s < STAGES2; ++s) {
+      const uint32_t lc = issued[s], pc = ld_cluster_u32(peer_issued + 4u * uint32_t(s));
+      if (pc == lc + 1u) {
+        mbar_expect_tx(bar(FULL + s), STAGE2_BYTES);
+        mbar_wait_teardown(bar(FULL + s), lc & 1u);
+      } else if (lc == pc + 1u) {
+        mbar_complete_tx(bar(FULL + s), STAGE2_BYTES);
+        mbar_wait_teardown(bar(FULL + s), (lc - 1u) & 1u);
+      } else if (lc == pc && lc > 0u) {
+        mbar_wait_teardown(bar(FULL + s), (lc - 1u) & 1u);
+      }
+    }
+  }
   if (threadIdx.x == 0 && *stop && a.dev_err) atomicOr(a.dev_err, SDM_DEV_TIMEOUT);
-  cluster_sync_all();
+  cluster_sync_all();  // the peer's shared memory outlives the leader's drain
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -820,11 +868,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // Producer: per stage, ever loaded / parity of its last load (read again after a stop).
+  uint32_t a_used = 0, a_par = 0, b_used = 0, b_par = 0;
   if (warp == 0) {
     if (lane == 0) {
       // ---- TMA producer: per K step the X tile, then the MT W tiles ----
       int as = 0, bs = 0;
-      uint32_t aph = 0, bph = 0, a_used = 0, a_par = 0, b_used = 0, b_par = 0;
+      uint32_t aph = 0, bph = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < a.units; u += gridDim.x) {
         const int tb = u / halves, g = u - tb * halves;
@@ -856,12 +906,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-      }
-      if (!ok) {  // let every copy in flight land before the CTA's shared memory goes away
-        for (int i = 0; i < F_ASTAGES; ++i)
-          if (a_used & (1u << i)) mbar_wait_teardown(bar(AF + i), (a_par >> i) & 1u);
-        for (int i = 0; i < F_BSTAGES; ++i)
-          if (b_used & (1u << i)) mbar_wait_teardown(bar(BF + i), (b_par >> i) & 1u);
       }
     }
   } else if (warp == 1) {
@@ -973,6 +1017,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"(tmem_cols)
                  : "memory");
+  // After a stop, whichever role raised it, every copy issued lands before the CTA's shared
+  // memory goes away.
+  if (warp == 0 && lane == 0 && *stop) {
+    for (int i = 0; i < F_ASTAGES; ++i)
+      if (a_used & (1u << i)) mbar_wait_teardown(bar(AF + i), (a_par >> i) & 1u);
+    for (int i = 0; i < F_BSTAGES; ++i)
+      if (b_used & (1u << i)) mbar_wait_teardown(bar(BF + i), (b_par >> i) & 1u);
+  }
   if (threadIdx.x == 0 && *stop && a.dev_err) atomicOr(a.dev_err, SDM_DEV_TIMEOUT);
 }
 
@@ -1018,7 +1070,8 @@ size_t fused_lists_bytes(int B, int T, int H, int S, int W, int R) {
 }  // namespace
 
 int launch_project(const void* x, const void* w, int B, int T, int D, int H, int S, void* kp,
-                   void* qp, int* dev_err, int max_ctas, int pair, cudaStream_t s) {
+                   void* qp, int* dev_err, int max_ctas, int pair, cudaStream_t s,
+                   const ProjectStall* stall) {
   const long long Mrows = 1LL * B * T, Ncols = 4LL * H * S;
   if (Mrows == 0) return SDM_OK;
   const long long MT = (Mrows + BM - 1) / BM, NT = (Ncols + BN - 1) / BN;
@@ -1033,6 +1086,9 @@ int launch_project(const void* x, const void* w, int B, int T, int D, int H, int
   pa.kp = static_cast<uint16_t*>(kp);
   pa.qp = static_cast<uint16_t*>(qp);
   pa.dev_err = dev_err;
+  pa.wait_ns = stall ? stall->wait_ns : kWaitNs;
+  pa.stall_cta = stall ? stall->cta : -1;
+  pa.stall_step = stall ? stall->step : 0;
   CUtensorMap tmX, tmW;
   if (!bf16_tile_map(&tmX, x, int(Mrows), D, BM) || !bf16_tile_map(&tmW, w, int(Ncols), D, BN / 2))
     return SDM_ECUDA;

@@ -237,3 +237,21 @@ def test_backward_flags_and_workspace_sizes():
     assert call(ws=ODD) == EALIGN
     assert call(G=ODD) == EALIGN
     assert call(ws_bytes=up16(part)) == ENOSPACE      # the zero flag needs the table and the bits
+
+
+def test_project_stall_rejects_bad_arguments_without_launching():
+    lib = sdm.lib()
+
+    def call(B=2, T=300, pair=2, cta=1, step=3, wait=1_000_000, err=FAKE):
+        return lib.sdm_test_project_stall(FAKE, FAKE, B, T, 64, 1, 32, FAKE, FAKE, pair, cta, step,
+                                          ctypes.c_ulonglong(wait), err, None)
+
+    assert call(pair=1) == EINVAL
+    assert call(pair=0, cta=1) == EINVAL
+    assert call(cta=2) == EINVAL
+    assert call(step=-1) == EINVAL
+    assert call(wait=10) == EINVAL
+    assert call(wait=2_000_000_000) == EINVAL
+    assert call(err=None) == EINVAL
+    assert call(B=1, T=100) == EUNSUPPORTED       # one row tile: no pair
+    assert call(err=ctypes.c_void_p(0x10002)) == EALIGN   # dev_err is an int

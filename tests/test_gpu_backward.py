@@ -137,6 +137,7 @@ OUTPUTS = ("dv", "dalpha", "dbeta", "dsc_w", "dsc_r", "dM0")
     (2, 1, 300, 16, 64, 64, 64, torch.bfloat16),   # rows rewritten and reread across tokens
     (1, 2, 40, 4, 32, 16, 16, torch.float32),      # W = R = N: only the last token's read slots are zero
     (3, 1, 70, 12, 8, 40, 33, torch.float32),      # W + R = 73: three words of zero bits, ragged
+    (33, 1, 6, 4, 8, 3, 2, torch.float32),         # B > 32: the reduction without per-group masks
 ])
 def test_final_zero_equals_the_cleared_adjoint(B, H, T, S, dv, W, R, vdt):
     """sdm_scan_backward_ex with SDM_BWD_FINAL_ZERO, G filled with NaN on entry, gives the

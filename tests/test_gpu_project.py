@@ -170,3 +170,31 @@ def test_bounded_wait_runs_out_and_reports_a_timeout():
     rk, rq, (mk, mq) = oracle.project(wl.bf16_to_f32(xb), wl.bf16_to_f32(wb), H, S)
     _check(_f32(kp), rk, mk, D, "kp after the timeouts")
     _check(_f32(qp), rq, mq, D, "qp after the timeouts")
+
+
+@pytest.mark.parametrize("pair,cta,step", [
+    (0, 0, 3),    # single blocks: the MMAs wait for a copy that is never issued
+    (2, 1, 0),    # pairs: the peer never issues; the leader's phases miss the peer's half
+    (2, 1, 9),    # ... after 9 K steps: the leader runs up to a round of stages ahead
+    (2, 0, 3),    # the leader stops issuing; the peer issues phases the leader never armed
+    (2, 0, 9),
+])
+def test_stalled_producer_stops_drains_and_reports(pair, cta, step):
+    """A producer that stops issuing copies part-way (sdm_test_project_stall, 1 ms wait
+    limit): the waits for its copies run out, the blocks stop, drain every copy in flight
+    (in a pair, the phases only one block issued too) and report SDM_DEV_TIMEOUT, well
+    inside the 2 s limit of a drain wait that never completes.  A projection afterwards is
+    still correct."""
+    import time
+    B, T, D, H, S = 2, 300, 1024, 2, 128      # 16 K steps per tile
+    xb, wb = _inputs(77, B, T, D, H, S)
+    x, w = _bf16_dev(xb).view(B, T, D), _bf16_dev(wb)
+    t0 = time.perf_counter()
+    err = sdm.project_stall_check(x, w, H, S, pair, cta, step, 1_000_000)
+    elapsed = time.perf_counter() - t0
+    assert err & sdm.SDM_DEV_TIMEOUT, err
+    assert elapsed < 1.5, elapsed
+    kp, qp = _run(xb, wb, H, S, 0, pair)
+    rk, rq, (mk, mq) = oracle.project(wl.bf16_to_f32(xb), wl.bf16_to_f32(wb), H, S)
+    _check(_f32(kp), rk, mk, D, ("kp after a stall", pair, cta, step))
+    _check(_f32(qp), rq, mq, D, ("qp after a stall", pair, cta, step))
