@@ -379,14 +379,26 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+L2_BYTES = 129e6
+
+
+def l2_note(cfg) -> str:
+    """Which of the step's inputs exceed the 129 MB L2 (no flush between timed steps)."""
+    elt = 2 if cfg.in_dtype == "bf16" else 4
+    parts = {"state table": cfg.B * cfg.H * cfg.N * cfg.d_v * 4,
+             "k' and q'": 2 * cfg.B * cfg.H * cfg.T * 2 * cfg.S * elt}
+    big = [f"{k} {v / 1e6:.0f} MB" for k, v in parts.items() if v > L2_BYTES]
+    small = [f"{k} {v / 1e6:.0f} MB" for k, v in parts.items() if v <= L2_BYTES]
+    note = "no L2 flush; larger than the 129 MB L2: " + (", ".join(big) if big else "none")
+    return note + ("; within it: " + ", ".join(small) if small else "")
+
+
 def config_dict(cfg, pipelined=True):
     step = ("sdm_forward: state from M0, then select+plan of token chunk c+1 overlapping the scan of chunk c"
             if pipelined else
             "init_state_from_M0 (side stream) || select, then plan, then scan (waits for init)")
     return {"workload": cfg.name, "B": cfg.B, "H": cfg.H, "T": cfg.T, "N": cfg.N, "d_v": cfg.d_v, "W": cfg.W,
-            "R": cfg.R, "inputs": cfg.in_dtype, "state": "f32",
-            "l2": "inputs larger than L2 (state table and k'/q' each exceed the 129 MB L2)",
-            "step": step}
+            "R": cfg.R, "inputs": cfg.in_dtype, "state": "f32", "l2": l2_note(cfg), "step": step}
 
 
 def one_stream_breakdown(st, cfg, sdm, args, torch, dev, reps=3):

@@ -247,11 +247,6 @@ size_t backward_smem_bytes(int C, int W, int R, int NW) {
 
 // --- zero final adjoint: which slots see a zero adjoint row ---------------------------
 
-__global__ void fill_words_kernel(int32_t* __restrict__ p, int32_t value, size_t n) {
-  const size_t stride = size_t(gridDim.x) * blockDim.x;
-  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) p[i] = value;
-}
-
 // One warp per (b, h, t): last[bh][x] = max(last[bh][x], t) for every read slot x.
 __global__ void __launch_bounds__(256) last_read_kernel(const int32_t* __restrict__ idx_r, int T,
                                                         int R, long long N, long long tokens,
@@ -583,11 +578,8 @@ int sdm_scan_backward_ex(const int32_t* idx_w, const float* sc_w, const int32_t*
   const int NW = zero_final ? (W + R + 31) / 32 : 0;
   const long long tokens = (long long)B * H * T;
   if (zero_final) {
-    const size_t n = size_t(B) * size_t(H) * size_t(N);
-    const int blocks = grid_for(n, 256);
-    if (blocks < 1) return SDM_ECUDA;
-    fill_words_kernel<<<blocks, 256, 0, s>>>(last, -1, n);
-    if (last_launch_status() != SDM_OK) return SDM_ECUDA;
+    if (launch_fill_words(last, -1, size_t(B) * size_t(H) * size_t(N), s) != SDM_OK)
+      return SDM_ECUDA;
     if (tokens > 0) {
       const long long tb = (tokens + 7) / 8;
       if (tb > 0x7FFFFFFFLL) return SDM_EUNSUPPORTED;

@@ -31,7 +31,31 @@ __global__ void __launch_bounds__(256) fill_state_kernel(float4* __restrict__ M,
   for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) __stcs(M + i, x);
 }
 
+__global__ void __launch_bounds__(256) fill_words_kernel(int32_t* __restrict__ p, int32_t value,
+                                                         size_t n) {
+  const size_t stride = size_t(gridDim.x) * blockDim.x;
+  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) p[i] = value;
+}
+
+int grid_cap(size_t work, int per_block) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return -1;
+  size_t blocks = (work + per_block - 1) / per_block;
+  const size_t cap = size_t(sms) * 8;
+  return int(blocks < cap ? (blocks < 1 ? 1 : blocks) : cap);
+}
+
 }  // namespace
+
+int launch_fill_words(int32_t* p, int32_t value, size_t n, cudaStream_t s) {
+  if (n == 0) return SDM_OK;
+  const int blocks = grid_cap(n, 256);
+  if (blocks < 1) return SDM_ECUDA;
+  fill_words_kernel<<<blocks, 256, 0, s>>>(p, value, n);
+  return last_launch_status();
+}
 
 int launch_fill_state(float* M, float value, int B, int H, long long N, int d_v, cudaStream_t s) {
   const size_t n4 = size_t(B) * size_t(H) * size_t(N) * size_t(d_v) / 4;

@@ -163,6 +163,7 @@ inline TokenWindow whole_sequences(int BH, int T) { return TokenWindow{BH, T, T,
 int launch_init_state(float* M, const float* M0, int B, int H, long long N, int d_v,
                       cudaStream_t s);
 int launch_fill_state(float* M, float value, int B, int H, long long N, int d_v, cudaStream_t s);
+int launch_fill_words(int32_t* p, int32_t value, size_t n, cudaStream_t s);
 // Both staircases of a (W, R, S) selection into out (stair_table_words 32-bit words).
 int stair_table_words(int W, int R, int S);
 int launch_stair_table(uint32_t* out, int W, int R, int S, cudaStream_t s);
