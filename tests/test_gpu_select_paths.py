@@ -4,9 +4,10 @@ selected key) and the general one (radix select on composite keys, then a bitoni
 Both are forced through sdm_select_tuned and compared with the oracle's top-k, bit for bit
 (slots and scores), on inputs that take every branch of the counting kernel: Gaussian
 halves (the window holds the top-k), halves with hot indices (the hot-slot workload's
-bias), tie-heavy halves (many keys share a value: per-bin ordering, and more than 32 keys
-at the cut: the fallback), widely spread halves (the top-k leave the 256-code window: the
-fallback), constant halves (every key ties) and halves of negative values only.
+bias), halves whose top-k lie 4-8 binades below a few outliers (the 256-code window holds
+too few keys: the fallback), tie-heavy halves (many keys share a value: per-bin ordering,
+and more than 32 keys at the cut: the fallback), widely spread halves (the top-k leave the
+window: the fallback), constant halves (every key ties) and halves of negative values only.
 """
 import numpy as np
 import pytest
@@ -29,6 +30,10 @@ def _halves(rng, kind, shape):
         x = rng.standard_normal(shape)
     elif kind == "hot":
         x = rng.standard_normal(shape) + 2.0 * np.exp(-np.arange(S) / 16.0)
+    elif kind == "outlier":  # a few entries far above the rest
+        x = 0.1 * rng.standard_normal(shape) * np.exp2(rng.integers(-2, 3, size=shape[:-1] + (1,)))
+        idx = rng.integers(0, S, size=shape[:-1] + (3,))
+        np.put_along_axis(x, idx, 8.0, axis=-1)
     elif kind == "ties":
         vals = np.array([-2.0, -1.0, -0.5, -0.0, 0.0, 0.5, 1.0, 1.5, 2.0])
         x = vals[rng.integers(0, len(vals), size=shape)]
@@ -45,7 +50,7 @@ def _halves(rng, kind, shape):
 
 SHAPES = [(8, 8, 8), (8, 64, 64), (16, 40, 16), (24, 100, 128), (32, 8, 8), (64, 100, 64),
           (256, 32, 128), (512, 64, 64), (1024, 128, 128), (1024, 1, 128), (1024, 128, 5)]
-KINDS = ["gauss", "hot", "ties", "spread", "const", "negative"]
+KINDS = ["gauss", "hot", "outlier", "ties", "spread", "const", "negative"]
 
 
 @pytest.mark.parametrize("S,W,R", SHAPES)
