@@ -191,6 +191,8 @@ struct ScanShape {
   int blocks;
   int smem;      // dynamic shared memory bytes of the scan kernel
 };
+// Dynamic shared memory of the scan kernel for a column slice and prefetch depth.
+size_t scan_smem_bytes(int cols, int pd, int W, int R, int d_v);
 // Picks (or checks a forced) scan kernel shape.  Returns SDM_OK or SDM_EUNSUPPORTED.
 int choose_scan_shape(int BH, int d_v, int W, int R, int force_cols, int force_pd,
                       ScanShape* out);

@@ -222,12 +222,6 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   cp_async_wait<0>();
 }
 
-size_t scan_smem_bytes(int cols, int pd, int W, int R, int d_v) {
-  const RecLayout L = rec_layout(W, R, d_v);
-  const size_t meta_bytes = size_t(L.off_v) + 4 * size_t(cols);
-  return size_t(pd + 1) * (W + R) * cols * 4 + size_t(2 * pd + 1) * meta_bytes +
-         size_t(kScanWarps) * cols * 4;
-}
 
 using ScanFn = void (*)(ScanArgs);
 
@@ -245,45 +239,11 @@ ScanFn scan_fn(int cols, int pd) {
 
 }  // namespace
 
-int choose_scan_shape(int BH, int d_v, int W, int R, int force_cols, int force_pd,
-                      ScanShape* out) {
-  int dev = 0, max_smem = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return SDM_ECUDA;
-  const int col_opts[5] = {64, 32, 16, 8, 4};
-  int best_cols = 0, best_pd = 0;
-  for (int ci = force_cols ? 0 : 1; ci < 5 && !best_cols; ++ci) {
-    const int c = col_opts[ci];
-    if (force_cols && c != force_cols) continue;
-    if (d_v % c) continue;
-    // Prefer wide (128-byte) row slices while that still gives ~1.5 blocks per SM.
-    if (!force_cols && ci + 1 < 5 && d_v % col_opts[ci + 1] == 0 &&
-        (long long)BH * (d_v / c) * 2 < 3LL * sms)
-      continue;
-    // One token of rows in flight per block measured fastest when the blocks fill the GPU
-    // (pd 1: 18.8 ms, pd 2: 19.1 ms on B16 H4 T8192 N=2^20 d_v=128 W=R=128); with fewer
-    // blocks than SMs each block's chain of gathers sets the pace, and two tokens in flight
-    // measured faster (B1 H4 N=2^20 d_v=128 W=R=128, 4-column slices: 0.93 against 1.00 us
-    // per token).
-    const int pd0 = (long long)BH * (d_v / c) < sms ? 2 : 1;
-    const int pds[2] = {pd0, 3 - pd0};
-    for (int k = 0; k < 2 && !best_cols; ++k) {
-      const int p = force_pd ? force_pd : pds[k];
-      if (scan_smem_bytes(c, p, W, R, d_v) <= size_t(max_smem)) {
-        best_cols = c;
-        best_pd = p;
-      }
-      if (force_pd) break;
-    }
-  }
-  if (!best_cols) return SDM_EUNSUPPORTED;
-  out->cols = best_cols;
-  out->pd = best_pd;
-  out->blocks = BH * (d_v / best_cols);
-  out->smem = int(scan_smem_bytes(best_cols, best_pd, W, R, d_v));
-  return SDM_OK;
+size_t scan_smem_bytes(int cols, int pd, int W, int R, int d_v) {
+  const RecLayout L = rec_layout(W, R, d_v);
+  const size_t meta_bytes = size_t(L.off_v) + 4 * size_t(cols);
+  return size_t(pd + 1) * (W + R) * cols * 4 + size_t(2 * pd + 1) * meta_bytes +
+         size_t(kScanWarps) * cols * 4;
 }
 
 int launch_scan_records(float* M, const void* rec, const TokenWindow& win, long long N, int d_v,
