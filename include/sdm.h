@@ -258,7 +258,8 @@ int sdm_scan_forward_train(float* M, const int32_t* idx_w, const float* sc_w,
  *   dM0    [H, N, d_v] fp32 or NULL: if given, the sum of the output G over the batch
  *          (the gradient of an M_0 shared by the batch).
  *   workspace  at least sdm_scan_backward_workspace_size(...) bytes, 16-byte aligned,
- *          contents irrelevant.
+ *          contents irrelevant (per (b, h, t): the column slices' partial sums and the
+ *          softmax weights of the token's scores, formed by a parallel pass first).
  * Requires d_v % 4 == 0 and the limits of sdm_scan_forward; slots outside [0, N) are
  * skipped (their gradients are unspecified). */
 size_t sdm_scan_backward_workspace_size(int B, int H, int T, int d_v, int W, int R);

@@ -52,6 +52,7 @@ struct BwdArgs {
   float* G;
   float* dv;
   float* part;  // [BH, T, slices, 2W + R]: ge (W), gm (W), dr (R) of one column slice
+  const float* wts;  // [BH, T, W + R]: softmax of the write, then of the read scores
   const uint32_t* zflags;  // [BH, T, NW]: bit e = slot e of [write | read] sees a zero adjoint
   int NW;                  // words of zflags per token; 0: G is the full adjoint on entry
   int T;
@@ -89,11 +90,10 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
   const int W = a.W, R = a.R, T = a.T, d_v = a.d_v;
   const int WR = W + R, WRa = (W + R + 3) & ~3;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float* kw = reinterpret_cast<float*>(smem);  // [W] write weights of the token
-  float* rw = kw + W;                           // [R] read weights
-  float* red = kw + WRa;                        // [2][warps][C], by token parity
-  // Two staging buffers of one token's [slots W | slots R | scores W | scores R | zero bits]:
-  // the next token's (going backwards) arrive by cp.async while this one is processed.
+  float* red = reinterpret_cast<float*>(smem) + WRa;  // [2][warps][C], by token parity
+  // Two staging buffers of one token's [slots W | slots R | weights W | weights R | zero
+  // bits] (the weights from the softmax pass): the next token's (going backwards) arrive by
+  // cp.async while this one is processed.
   const int SB = 2 * WR + a.NW;
   int32_t* stg = reinterpret_cast<int32_t*>(red + 2 * kBwdWarps * C);  // [2][SB]
 
@@ -111,8 +111,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
     for (int e = tid; e < SB; e += kBwdThreads) {
       const void* src = e < W ? static_cast<const void*>(a.idx_w + tk * W + e)
                       : e < WR ? static_cast<const void*>(a.idx_r + tk * R + (e - W))
-                      : e < WR + W ? static_cast<const void*>(a.sc_w + tk * W + (e - WR))
-                      : e < 2 * WR ? static_cast<const void*>(a.sc_r + tk * R + (e - WR - W))
+                      : e < 2 * WR ? static_cast<const void*>(a.wts + tk * WR + (e - WR))
                                    : static_cast<const void*>(a.zflags + tk * a.NW + (e - 2 * WR));
       asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
                        static_cast<uint32_t>(__cvta_generic_to_shared(dst + e))),
@@ -129,13 +128,11 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
     const size_t tk = size_t(bh) * T + t;
     const int32_t* iw = stg + (t & 1) * SB;
     const int32_t* ir = iw + W;
-    const float* scw = reinterpret_cast<const float*>(iw + WR);
+    const float* kw = reinterpret_cast<const float*>(iw + WR);  // the token's write weights
+    const float* rw = kw + W;                                    // and read weights
     const uint32_t* zb = reinterpret_cast<const uint32_t*>(iw + 2 * WR);
     auto zero_at = [&](int e) { return a.NW != 0 && ((zb[e >> 5] >> (e & 31)) & 1u) != 0; };
-    if (warp == 0) warp_softmax(scw, W, kw);
-    if (warp == 1) warp_softmax(scw + W, R, rw);
-    __syncthreads();
-    if (t > 0) stage(t - 1);  // the other buffer held token t+1, no longer read
+    if (t > 0) stage(t - 1);  // the other buffer held token t+1, retired at its last barrier
     float* part = a.part + (tk * slices + sl) * PW;
     const float4 dO4 = reinterpret_cast<const float4*>(a.dO + tk * d_v + c0)[c4];
 
@@ -245,6 +242,20 @@ size_t backward_smem_bytes(int C, int W, int R, int NW) {
   return size_t(WRa) * 4 + size_t(2 * kBwdWarps) * C * 4 + size_t(2 * (2 * (W + R) + NW)) * 4;
 }
 
+// Softmax of every token's write and read scores, one warp per (b, h, t), with the routine
+// the planning kernel and the finish kernel use: the reverse scan stages these weights with
+// the slots instead of forming them on its sequential path.
+__global__ void __launch_bounds__(256) bwd_weights_kernel(const float* __restrict__ sc_w,
+                                                          const float* __restrict__ sc_r, int W,
+                                                          int R, long long tokens,
+                                                          float* __restrict__ wts) {
+  const long long tok = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (tok >= tokens) return;
+  float* out = wts + tok * (W + R);
+  warp_softmax(sc_w + tok * W, W, out);
+  warp_softmax(sc_r + tok * R, R, out + W);
+}
+
 // --- zero final adjoint: which slots see a zero adjoint row ---------------------------
 
 // One warp per (b, h, t): last[bh][x] = max(last[bh][x], t) for every read slot x.
@@ -297,9 +308,10 @@ int backward_cols(int d_v) {
   return 0;
 }
 
-// One warp per (b, h, t): sums the slices' partials, then the softmax backward.
+// One warp per (b, h, t): sums the slices' partials, then the softmax backward with the
+// weights of the softmax pass (wts [items, W + R]).
 __global__ void __launch_bounds__(128) backward_finish_kernel(
-    const float* __restrict__ sc_w, const float* __restrict__ sc_r, const float* __restrict__ beta,
+    const float* __restrict__ wts, const float* __restrict__ beta,
     const float* __restrict__ part, int slices, int W, int R, long long items, float* dalpha,
     float* dbeta, float* dsc_w, float* dsc_r) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -310,8 +322,7 @@ __global__ void __launch_bounds__(128) backward_finish_kernel(
   float* dr = dk + W;
   const long long item = (long long)blockIdx.x * (blockDim.x >> 5) + warp;
   if (item >= items) return;
-  warp_softmax(sc_w + item * W, W, k);
-  warp_softmax(sc_r + item * R, R, r);
+  for (int i = lane; i < W + R; i += 32) k[i] = wts[item * (W + R) + i];  // k then r
   __syncwarp();
   const int PW = 2 * W + R;
   const float* p = part + item * slices * PW;
@@ -461,10 +472,10 @@ __global__ void __launch_bounds__(128) select_backward_kernel(const int32_t* __r
   }
 }
 
-// Workspace of the reverse pass: [part | last-read table | zero bits], each piece 16-byte
-// aligned; the last two only with SDM_BWD_FINAL_ZERO.  0 on overflow or bad sizes.
+// Workspace of the reverse pass: [part | weights | last-read table | zero bits], each piece
+// 16-byte aligned; the last two only with SDM_BWD_FINAL_ZERO.  0 on overflow or bad sizes.
 struct BwdWorkspace {
-  size_t part, last, zflags, total;
+  size_t part, wts, last, zflags, total;
 };
 
 bool backward_workspace(int B, int H, int T, long long N, int d_v, int W, int R, unsigned flags,
@@ -475,16 +486,18 @@ bool backward_workspace(int B, int H, int T, long long N, int d_v, int W, int R,
   auto up16 = [](size_t x) { return (x + 15) & ~size_t(15); };
   const size_t lim = size_t(1) << 62;
   const double approx = double(B) * H * (double(T) * (d_v / C) * (2.0 * W + R) * 4 + double(N) * 4 +
-                                         double(T) * ((W + R + 31) / 32) * 4);
+                                         double(T) * ((W + R + 31) / 32) * 4 +
+                                         double(T) * (W + R) * 4);
   if (approx > double(lim)) return false;
   const size_t bh = size_t(B) * size_t(H);
   ws->part = up16(bh * size_t(T) * size_t(d_v / C) * size_t(2 * W + R) * 4);
+  ws->wts = up16(bh * size_t(T) * size_t(W + R) * 4);
   ws->last = ws->zflags = 0;
   if (flags & SDM_BWD_FINAL_ZERO) {
     ws->last = up16(bh * size_t(N) * 4);
     ws->zflags = up16(bh * size_t(T) * size_t((W + R + 31) / 32) * 4);
   }
-  ws->total = ws->part + ws->last + ws->zflags;
+  ws->total = ws->part + ws->wts + ws->last + ws->zflags;
   return true;
 }
 
@@ -573,8 +586,10 @@ int sdm_scan_backward_ex(const int32_t* idx_w, const float* sc_w, const int32_t*
   if ((T > 0 || zero_final) && !aligned16(workspace)) return SDM_EALIGN;
   if ((T > 0 || zero_final) && workspace_bytes < ws.total) return SDM_ENOSPACE;
   unsigned char* wsb = static_cast<unsigned char*>(workspace);
-  int32_t* last = zero_final ? reinterpret_cast<int32_t*>(wsb + ws.part) : nullptr;
-  uint32_t* zflags = zero_final ? reinterpret_cast<uint32_t*>(wsb + ws.part + ws.last) : nullptr;
+  float* wts = reinterpret_cast<float*>(wsb + ws.part);
+  int32_t* last = zero_final ? reinterpret_cast<int32_t*>(wsb + ws.part + ws.wts) : nullptr;
+  uint32_t* zflags =
+      zero_final ? reinterpret_cast<uint32_t*>(wsb + ws.part + ws.wts + ws.last) : nullptr;
   const int NW = zero_final ? (W + R + 31) / 32 : 0;
   const long long tokens = (long long)B * H * T;
   if (zero_final) {
@@ -594,6 +609,10 @@ int sdm_scan_backward_ex(const int32_t* idx_w, const float* sc_w, const int32_t*
     if (!aligned16(w_prev) || !aligned16(r_rows) || !aligned16(dO) || !aligned16(dalpha) ||
         !aligned16(dbeta) || !aligned16(dsc_w) || !aligned16(dsc_r))
       return SDM_EALIGN;
+    const long long wb = (tokens + 7) / 8;
+    if (wb > 0x7FFFFFFFLL) return SDM_EUNSUPPORTED;
+    bwd_weights_kernel<<<unsigned(wb), 256, 0, s>>>(sc_w, sc_r, W, R, tokens, wts);
+    if (last_launch_status() != SDM_OK) return SDM_ECUDA;
     BwdArgs a;
     a.idx_w = idx_w;
     a.sc_w = sc_w;
@@ -609,6 +628,7 @@ int sdm_scan_backward_ex(const int32_t* idx_w, const float* sc_w, const int32_t*
     a.G = G;
     a.dv = dv;
     a.part = reinterpret_cast<float*>(wsb);
+    a.wts = wts;
     a.zflags = zflags;
     a.NW = NW;
     a.T = T;
@@ -634,7 +654,7 @@ int sdm_scan_backward_ex(const int32_t* idx_w, const float* sc_w, const int32_t*
                              cudaFuncAttributeMaxDynamicSharedMemorySize, fsmem) != cudaSuccess)
       return SDM_ECUDA;
     backward_finish_kernel<<<unsigned((items + 3) / 4), 128, fsmem, s>>>(
-        sc_w, sc_r, beta, a.part, d_v / C, W, R, items, dalpha, dbeta, dsc_w, dsc_r);
+        wts, beta, a.part, d_v / C, W, R, items, dalpha, dbeta, dsc_w, dsc_r);
     if (last_launch_status() != SDM_OK) return SDM_ECUDA;
   }
   if (zero_final) {
