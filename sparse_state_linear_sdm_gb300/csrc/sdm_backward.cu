@@ -53,8 +53,13 @@ struct BwdArgs {
   float* dv;
   float* part;  // [BH, T, slices, 2W + R]: ge (W), gm (W), dr (R) of one column slice
   const float* wts;  // [BH, T, W + R]: softmax of the write, then of the read scores
-  const uint32_t* zflags;  // [BH, T, NW]: bit e = slot e of [write | read] sees a zero adjoint
-  int NW;                  // words of zflags per token; 0: G is the full adjoint on entry
+  // [BH, T, NW + NS] per token: NW words, bit e = slot e of [write | read] sees a zero
+  // adjoint (all 0 unless dL/dM_T = 0); then NS words, bit i = write slot i's row is also a
+  // read slot of the same token (its adjoint is the read phase's update: loaded after it).
+  const uint32_t* flags;
+  int NW, NS, NF;  // NF: words per token, NW + NS padded to a multiple of 4
+  bool zero_final;
+  bool vec16;  // W, R multiples of 4 and the slot arrays 16-byte aligned: 16-byte staging
   int T;
   long long N;
   int d_v, W, R;
@@ -67,6 +72,13 @@ __device__ __forceinline__ float4 load_v4(const void* v, int bf16, size_t i4) {
                        __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
   }
   return reinterpret_cast<const float4*>(v)[i4];
+}
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+               "l"(gmem_src)
+               : "memory");
 }
 
 __device__ __forceinline__ float dot4(float4 a, float4 b) {
@@ -94,7 +106,8 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
   // Two staging buffers of one token's [slots W | slots R | weights W | weights R | zero
   // bits] (the weights from the softmax pass): the next token's (going backwards) arrive by
   // cp.async while this one is processed.
-  const int SB = 2 * WR + a.NW;
+  const int NF = a.NF;
+  const int SB = 2 * WR + NF;
   int32_t* stg = reinterpret_cast<int32_t*>(red + 2 * kBwdWarps * C);  // [2][SB]
 
   const int slices = d_v / C;
@@ -105,14 +118,26 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
   const int PW = 2 * W + R;
   float* Gbh = a.G + size_t(bh) * size_t(a.N) * d_v + c0;
 
-  auto stage = [&](int t) {  // 4-byte cp.async per entry into buffer t & 1
+  auto stage = [&](int t) {  // into buffer t & 1
     const size_t tk = size_t(bh) * T + t;
     int32_t* dst = stg + (t & 1) * SB;
+    if (a.vec16) {  // the four segments are contiguous per token: 16-byte copies
+      const int n1 = W / 4, n2 = n1 + R / 4, n3 = n2 + WR / 4, n4 = n3 + NF / 4;
+      for (int q = tid; q < n4; q += kBwdThreads) {
+        const void* src = q < n1 ? static_cast<const void*>(a.idx_w + tk * W + 4 * q)
+                        : q < n2 ? static_cast<const void*>(a.idx_r + tk * R + 4 * (q - n1))
+                        : q < n3 ? static_cast<const void*>(a.wts + tk * WR + 4 * (q - n2))
+                                 : static_cast<const void*>(a.flags + tk * NF + 4 * (q - n3));
+        cp_async16(dst + 4 * q, src);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      return;
+    }
     for (int e = tid; e < SB; e += kBwdThreads) {
       const void* src = e < W ? static_cast<const void*>(a.idx_w + tk * W + e)
                       : e < WR ? static_cast<const void*>(a.idx_r + tk * R + (e - W))
                       : e < 2 * WR ? static_cast<const void*>(a.wts + tk * WR + (e - WR))
-                                   : static_cast<const void*>(a.zflags + tk * a.NW + (e - 2 * WR));
+                                   : static_cast<const void*>(a.flags + tk * NF + (e - 2 * WR));
       asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
                        static_cast<uint32_t>(__cvta_generic_to_shared(dst + e))),
                    "l"(src)
@@ -131,9 +156,32 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
     const float* kw = reinterpret_cast<const float*>(iw + WR);  // the token's write weights
     const float* rw = kw + W;                                    // and read weights
     const uint32_t* zb = reinterpret_cast<const uint32_t*>(iw + 2 * WR);
-    auto zero_at = [&](int e) { return a.NW != 0 && ((zb[e >> 5] >> (e & 31)) & 1u) != 0; };
+    const uint32_t* sb = zb + a.NW;
+    auto zero_at = [&](int e) { return a.zero_final && ((zb[e >> 5] >> (e & 31)) & 1u) != 0; };
+    auto same_at = [&](int i) { return ((sb[i >> 5] >> (i & 31)) & 1u) != 0; };
     if (t > 0) stage(t - 1);  // the other buffer held token t+1, retired at its last barrier
     float* part = a.part + (tk * slices + sl) * PW;
+
+    // The write phase's first round of rows, loaded now so that their latency overlaps the
+    // read phase's: a write row's adjoint depends on this token's reads only when one of its
+    // read slots names the same row (marked by the flags pass; loaded after the barrier).
+    // A zero adjoint row contributes nothing and stays zero: no loads, no store.
+    int32_t xw[NB];
+    float4 g0[NB], wp0[NB];
+    bool late[NB];
+#pragma unroll
+    for (int u = 0; u < NB; ++u) {
+      const int i = u * RPP + tid / LPR;
+      xw[u] = i < W ? iw[i] : -1;
+      if (xw[u] >= 0 && xw[u] < a.N && zero_at(i)) xw[u] = -1;
+      const bool ok = xw[u] >= 0 && xw[u] < a.N;
+      late[u] = ok && same_at(i);
+      g0[u] = wp0[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ok) {
+        if (!late[u]) g0[u] = reinterpret_cast<const float4*>(Gbh + size_t(xw[u]) * d_v)[c4];
+        wp0[u] = reinterpret_cast<const float4*>(a.w_prev + (tk * W + i) * d_v + c0)[c4];
+      }
+    }
     const float4 dO4 = reinterpret_cast<const float4*>(a.dO + tk * d_v + c0)[c4];
 
     // Read rows: dr_j (this slice's share) and G[ir_j] += r_j dO_t.  Each thread takes up
@@ -176,16 +224,24 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
     for (int ib = 0; ib < W; ib += NB * RPP) {
       int32_t x[NB];
       float4 g[NB], wp[NB];
+      if (ib == 0) {
 #pragma unroll
-      for (int u = 0; u < NB; ++u) {
-        const int i = ib + u * RPP + tid / LPR;
-        x[u] = i < W ? iw[i] : -1;
-        // A zero adjoint row contributes nothing and stays zero: no loads, no store.
-        if (x[u] >= 0 && x[u] < a.N && zero_at(i)) x[u] = -1;
-        g[u] = wp[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (x[u] >= 0 && x[u] < a.N) {
-          g[u] = reinterpret_cast<const float4*>(Gbh + size_t(x[u]) * d_v)[c4];
-          wp[u] = reinterpret_cast<const float4*>(a.w_prev + (tk * W + i) * d_v + c0)[c4];
+        for (int u = 0; u < NB; ++u) {
+          x[u] = xw[u];
+          g[u] = late[u] ? reinterpret_cast<const float4*>(Gbh + size_t(xw[u]) * d_v)[c4] : g0[u];
+          wp[u] = wp0[u];
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < NB; ++u) {
+          const int i = ib + u * RPP + tid / LPR;
+          x[u] = i < W ? iw[i] : -1;
+          if (x[u] >= 0 && x[u] < a.N && zero_at(i)) x[u] = -1;
+          g[u] = wp[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (x[u] >= 0 && x[u] < a.N) {
+            g[u] = reinterpret_cast<const float4*>(Gbh + size_t(x[u]) * d_v)[c4];
+            wp[u] = reinterpret_cast<const float4*>(a.w_prev + (tk * W + i) * d_v + c0)[c4];
+          }
         }
       }
 #pragma unroll
@@ -237,9 +293,9 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
   }
 }
 
-size_t backward_smem_bytes(int C, int W, int R, int NW) {
+size_t backward_smem_bytes(int C, int W, int R, int NF) {
   const int WRa = (W + R + 3) & ~3;
-  return size_t(WRa) * 4 + size_t(2 * kBwdWarps) * C * 4 + size_t(2 * (2 * (W + R) + NW)) * 4;
+  return size_t(WRa) * 4 + size_t(2 * kBwdWarps) * C * 4 + size_t(2 * (2 * (W + R) + NF)) * 4;
 }
 
 // Softmax of every token's write and read scores, one warp per (b, h, t), with the routine
@@ -273,24 +329,44 @@ __global__ void __launch_bounds__(256) last_read_kernel(const int32_t* __restric
   }
 }
 
-// One warp per (b, h, t): bit e of the token's [write | read] slots is set when the adjoint
-// row at that slot is zero: a write slot whose row no read at token >= t selects, a read
-// slot whose row no read after t selects.  Slots outside [0, N) get 0.
-__global__ void __launch_bounds__(256) zero_flags_kernel(const int32_t* __restrict__ idx_w,
-                                                         const int32_t* __restrict__ idx_r, int T,
-                                                         int W, int R, long long N, long long tokens,
-                                                         const int32_t* __restrict__ last, int NW,
-                                                         uint32_t* __restrict__ zflags) {
-  const long long tok = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+// One warp per (b, h, t).  Zero bits (when last is given, dL/dM_T = 0): bit e of the
+// token's [write | read] slots is set when the adjoint row at that slot is zero: a write
+// slot whose row no read at token >= t selects, a read slot whose row no read after t
+// selects.  Same-token bits: bit i when write slot i's row is also one of the token's read
+// slots (through a hash of the read slots in the warp's shared memory, at most half full).
+// Slots outside [0, N) get 0.
+__global__ void __launch_bounds__(256) bwd_flags_kernel(const int32_t* __restrict__ idx_w,
+                                                        const int32_t* __restrict__ idx_r, int T,
+                                                        int W, int R, long long N, long long tokens,
+                                                        const int32_t* __restrict__ last, int NW,
+                                                        int NS, int NF, int log2cap,
+                                                        uint32_t* __restrict__ flags) {
+  extern __shared__ int32_t tabs[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long tok = (long long)blockIdx.x * (blockDim.x >> 5) + warp;
   if (tok >= tokens) return;
-  const int lane = threadIdx.x & 31;
+  const int cap = 1 << log2cap;
+  int32_t* tab = tabs + size_t(warp) * cap;
   const long long bh = tok / T;
   const int t = int(tok - bh * T);
-  const int32_t* lb = last + bh * N;
+  uint32_t* out = flags + tok * NF;
+  auto hash = [&](int32_t x) { return (uint32_t(x) * 0x9E3779B1u) >> (32 - log2cap); };
+  for (int i = lane; i < cap; i += 32) tab[i] = -1;
+  __syncwarp();
+  for (int j = lane; j < R; j += 32) {
+    const int32_t x = idx_r[tok * R + j];
+    if (x < 0 || x >= N) continue;
+    for (uint32_t h = hash(x);; h = (h + 1) & uint32_t(cap - 1)) {
+      const int32_t prev = atomicCAS(&tab[h], -1, x);
+      if (prev == -1 || prev == x) break;
+    }
+  }
+  __syncwarp();
+  const int32_t* lb = last ? last + bh * N : nullptr;
   for (int e0 = 0; e0 < W + R; e0 += 32) {
     const int e = e0 + lane;
     bool z = false;
-    if (e < W + R) {
+    if (lb && e < W + R) {
       const int32_t x = e < W ? idx_w[tok * W + e] : idx_r[tok * R + (e - W)];
       if (x >= 0 && x < N) {
         const int32_t l = lb[x];
@@ -298,7 +374,25 @@ __global__ void __launch_bounds__(256) zero_flags_kernel(const int32_t* __restri
       }
     }
     const unsigned m = __ballot_sync(0xFFFFFFFFu, z);
-    if (lane == 0) zflags[tok * NW + (e0 >> 5)] = m;
+    if (lane == 0) out[e0 >> 5] = m;
+  }
+  for (int i0 = 0; i0 < W; i0 += 32) {
+    const int i = i0 + lane;
+    bool same = false;
+    if (i < W) {
+      const int32_t x = idx_w[tok * W + i];
+      if (x >= 0 && x < N)
+        for (uint32_t h = hash(x);; h = (h + 1) & uint32_t(cap - 1)) {
+          const int32_t v = tab[h];
+          if (v == -1) break;
+          if (v == x) {
+            same = true;
+            break;
+          }
+        }
+    }
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, same);
+    if (lane == 0) out[NW + (i0 >> 5)] = m;
   }
 }
 
@@ -475,8 +569,13 @@ __global__ void __launch_bounds__(128) select_backward_kernel(const int32_t* __r
 // Workspace of the reverse pass: [part | weights | last-read table | zero bits], each piece
 // 16-byte aligned; the last two only with SDM_BWD_FINAL_ZERO.  0 on overflow or bad sizes.
 struct BwdWorkspace {
-  size_t part, wts, last, zflags, total;
+  size_t part, wts, flags, last, total;
 };
+
+// Flag words per token (zero bits, then same-token bits), padded to 16 bytes.
+inline int bwd_flag_words(int W, int R) {
+  return ((W + R + 31) / 32 + (W + 31) / 32 + 3) & ~3;
+}
 
 bool backward_workspace(int B, int H, int T, long long N, int d_v, int W, int R, unsigned flags,
                         BwdWorkspace* ws) {
@@ -486,18 +585,15 @@ bool backward_workspace(int B, int H, int T, long long N, int d_v, int W, int R,
   auto up16 = [](size_t x) { return (x + 15) & ~size_t(15); };
   const size_t lim = size_t(1) << 62;
   const double approx = double(B) * H * (double(T) * (d_v / C) * (2.0 * W + R) * 4 + double(N) * 4 +
-                                         double(T) * ((W + R + 31) / 32) * 4 +
+                                         double(T) * bwd_flag_words(W, R) * 4 +
                                          double(T) * (W + R) * 4);
   if (approx > double(lim)) return false;
   const size_t bh = size_t(B) * size_t(H);
   ws->part = up16(bh * size_t(T) * size_t(d_v / C) * size_t(2 * W + R) * 4);
   ws->wts = up16(bh * size_t(T) * size_t(W + R) * 4);
-  ws->last = ws->zflags = 0;
-  if (flags & SDM_BWD_FINAL_ZERO) {
-    ws->last = up16(bh * size_t(N) * 4);
-    ws->zflags = up16(bh * size_t(T) * size_t((W + R + 31) / 32) * 4);
-  }
-  ws->total = ws->part + ws->wts + ws->last + ws->zflags;
+  ws->flags = up16(bh * size_t(T) * size_t(bwd_flag_words(W, R)) * 4);
+  ws->last = (flags & SDM_BWD_FINAL_ZERO) ? up16(bh * size_t(N) * 4) : 0;
+  ws->total = ws->part + ws->wts + ws->flags + ws->last;
   return true;
 }
 
@@ -587,10 +683,10 @@ int sdm_scan_backward_ex(const int32_t* idx_w, const float* sc_w, const int32_t*
   if ((T > 0 || zero_final) && workspace_bytes < ws.total) return SDM_ENOSPACE;
   unsigned char* wsb = static_cast<unsigned char*>(workspace);
   float* wts = reinterpret_cast<float*>(wsb + ws.part);
-  int32_t* last = zero_final ? reinterpret_cast<int32_t*>(wsb + ws.part + ws.wts) : nullptr;
-  uint32_t* zflags =
-      zero_final ? reinterpret_cast<uint32_t*>(wsb + ws.part + ws.wts + ws.last) : nullptr;
-  const int NW = zero_final ? (W + R + 31) / 32 : 0;
+  uint32_t* fl = reinterpret_cast<uint32_t*>(wsb + ws.part + ws.wts);
+  int32_t* last =
+      zero_final ? reinterpret_cast<int32_t*>(wsb + ws.part + ws.wts + ws.flags) : nullptr;
+  const int NW = (W + R + 31) / 32, NS = (W + 31) / 32;
   const long long tokens = (long long)B * H * T;
   if (zero_final) {
     if (launch_fill_words(last, -1, size_t(B) * size_t(H) * size_t(N), s) != SDM_OK)
@@ -600,10 +696,17 @@ int sdm_scan_backward_ex(const int32_t* idx_w, const float* sc_w, const int32_t*
       if (tb > 0x7FFFFFFFLL) return SDM_EUNSUPPORTED;
       last_read_kernel<<<unsigned(tb), 256, 0, s>>>(idx_r, T, R, N, tokens, last);
       if (last_launch_status() != SDM_OK) return SDM_ECUDA;
-      zero_flags_kernel<<<unsigned(tb), 256, 0, s>>>(idx_w, idx_r, T, W, R, N, tokens, last, NW,
-                                                     zflags);
-      if (last_launch_status() != SDM_OK) return SDM_ECUDA;
     }
+  }
+  if (tokens > 0) {
+    int l = 5;
+    while ((1 << l) < 2 * R) ++l;
+    const int warps = int(min(size_t(8), size_t(48 * 1024) / (size_t(4) << l)));
+    const long long fb = (tokens + warps - 1) / warps;
+    if (fb > 0x7FFFFFFFLL || warps < 1) return SDM_EUNSUPPORTED;
+    bwd_flags_kernel<<<unsigned(fb), warps * 32, size_t(warps) * (size_t(4) << l), s>>>(
+        idx_w, idx_r, T, W, R, N, tokens, last, NW, NS, bwd_flag_words(W, R), l, fl);
+    if (last_launch_status() != SDM_OK) return SDM_ECUDA;
   }
   if (T > 0) {
     if (!aligned16(w_prev) || !aligned16(r_rows) || !aligned16(dO) || !aligned16(dalpha) ||
@@ -629,14 +732,18 @@ int sdm_scan_backward_ex(const int32_t* idx_w, const float* sc_w, const int32_t*
     a.dv = dv;
     a.part = reinterpret_cast<float*>(wsb);
     a.wts = wts;
-    a.zflags = zflags;
+    a.flags = fl;
     a.NW = NW;
+    a.NS = NS;
+    a.NF = bwd_flag_words(W, R);
+    a.vec16 = W % 4 == 0 && R % 4 == 0 && aligned16(idx_w) && aligned16(idx_r);
+    a.zero_final = zero_final;
     a.T = T;
     a.N = N;
     a.d_v = d_v;
     a.W = W;
     a.R = R;
-    const int smem = int(backward_smem_bytes(C, W, R, NW));
+    const int smem = int(backward_smem_bytes(C, W, R, a.NF));
     const void* fn = C == 32   ? reinterpret_cast<const void*>(&scan_backward_kernel<32>)
                      : C == 16 ? reinterpret_cast<const void*>(&scan_backward_kernel<16>)
                      : C == 8  ? reinterpret_cast<const void*>(&scan_backward_kernel<8>)

@@ -219,12 +219,13 @@ def test_backward_flags_and_workspace_sizes():
     up16 = lambda x: (x + 15) // 16 * 16
     part = B * H * T * 1 * (2 * W + R) * 4            # d_v = 16: one 16-column slice per (b, h)
     wts = B * H * T * (W + R) * 4                     # the softmax weights of every token
-    assert lib.sdm_scan_backward_workspace_size(B, H, T, dv, W, R) == up16(part) + up16(wts)
-    assert lib.sdm_scan_backward_workspace_size_ex(B, H, T, N, dv, W, R, 0) == up16(part) + up16(wts)
-    assert lib.sdm_scan_backward_workspace_size_ex(B, H, T, N, dv, W, R, 1) == (
-        up16(part) + up16(wts) + up16(B * H * N * 4) + up16(B * H * T * 1 * 4))
+    flags = B * H * T * 4 * 4                         # per token: zero bits (W + R), same-token bits (W), padded to 16 B
+    base = up16(part) + up16(wts) + up16(flags)
+    assert lib.sdm_scan_backward_workspace_size(B, H, T, dv, W, R) == base
+    assert lib.sdm_scan_backward_workspace_size_ex(B, H, T, N, dv, W, R, 0) == base
+    assert lib.sdm_scan_backward_workspace_size_ex(B, H, T, N, dv, W, R, 1) == base + up16(B * H * N * 4)
     assert lib.sdm_scan_backward_workspace_size_ex(1, 1, 5, 64, 8, 40, 33, 1) == (
-        up16(5 * 1 * 113 * 4) + up16(5 * 73 * 4) + up16(64 * 4) + up16(5 * 3 * 4))   # three words
+        up16(5 * 1 * 113 * 4) + up16(5 * 73 * 4) + up16(5 * 8 * 4) + up16(64 * 4))   # W + R = 73: 3 + 2 words
     assert lib.sdm_scan_backward_workspace_size_ex(B, H, T, N, dv, W, R, 2) == 0
     assert lib.sdm_scan_backward_workspace_size_ex(B, H, 0, N, dv, W, R, 1) == up16(B * H * N * 4)
 
@@ -237,7 +238,7 @@ def test_backward_flags_and_workspace_sizes():
     assert call(dv_=6) == EINVAL
     assert call(ws=ODD) == EALIGN
     assert call(G=ODD) == EALIGN
-    assert call(ws_bytes=up16(part) + up16(wts)) == ENOSPACE      # the zero flag needs the table and the bits
+    assert call(ws_bytes=base) == ENOSPACE      # the zero flag needs the table
 
 
 def test_project_stall_rejects_bad_arguments_without_launching():
