@@ -150,21 +150,36 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
       if (t + d < T)
         fwd |= (reinterpret_cast<const int*>(meta + ((t + d) % QM) * meta_bytes + L.off_ab)[2] >> d) & 1;
 
-    // Forget gate and delta update of the W write rows (in shared memory and in HBM).
-    for (int e = tid / LPR; e < W; e += RPP) {
-      if (src[e] == -2) continue;
-      float4* cell = reinterpret_cast<float4*>(rs + e * C) + c4;
-      const float4 m = *cell;
-      if (wsave) *(reinterpret_cast<float4*>(wsave + (size_t(t) * W + e) * d_v) + c4) = m;
-      const float kb = beta * wts[e];
-      float4 r;
-      float mt_;
-      mt_ = alpha * m.x; r.x = fmaf(kb, vv.x - mt_, mt_);
-      mt_ = alpha * m.y; r.y = fmaf(kb, vv.y - mt_, mt_);
-      mt_ = alpha * m.z; r.z = fmaf(kb, vv.z - mt_, mt_);
-      mt_ = alpha * m.w; r.w = fmaf(kb, vv.w - mt_, mt_);
-      *cell = r;
-      *(reinterpret_cast<float4*>(Mbh + size_t(idx[e]) * d_v) + c4) = r;
+    // Forget gate and delta update of the W write rows (in shared memory and in HBM).  A
+    // thread's rows are distinct, so four of them are read before any is written back: their
+    // shared-memory latencies overlap instead of forming one chain.
+    for (int e0 = tid / LPR; e0 < W; e0 += 4 * RPP) {
+      float4 m[4];
+      float kb[4];
+      bool ok[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int e = e0 + k * RPP;
+        ok[k] = e < W && src[e] != -2;
+        if (ok[k]) {
+          m[k] = reinterpret_cast<const float4*>(rs + e * C)[c4];
+          kb[k] = beta * wts[e];
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (!ok[k]) continue;
+        const int e = e0 + k * RPP;
+        if (wsave) *(reinterpret_cast<float4*>(wsave + (size_t(t) * W + e) * d_v) + c4) = m[k];
+        float4 r;
+        float mt_;
+        mt_ = alpha * m[k].x; r.x = fmaf(kb[k], vv.x - mt_, mt_);
+        mt_ = alpha * m[k].y; r.y = fmaf(kb[k], vv.y - mt_, mt_);
+        mt_ = alpha * m[k].z; r.z = fmaf(kb[k], vv.z - mt_, mt_);
+        mt_ = alpha * m[k].w; r.w = fmaf(kb[k], vv.w - mt_, mt_);
+        reinterpret_cast<float4*>(rs + e * C)[c4] = r;
+        *(reinterpret_cast<float4*>(Mbh + size_t(idx[e]) * d_v) + c4) = r;
+      }
     }
 
     // Forwarding: rows of tokens t .. t+PD whose latest writer is token t.
@@ -193,15 +208,29 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
 
     // Weighted read of the R read rows (after the write).
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int e = tid / LPR; e < R; e += RPP) {
-      if (src[W + e] == -2) continue;
-      const float r = wts[W + e];
-      const float4 m = reinterpret_cast<const float4*>(rs + (W + e) * C)[c4];
-      if (rsave) *(reinterpret_cast<float4*>(rsave + (size_t(t) * R + e) * d_v) + c4) = m;
-      acc.x = fmaf(r, m.x, acc.x);
-      acc.y = fmaf(r, m.y, acc.y);
-      acc.z = fmaf(r, m.z, acc.z);
-      acc.w = fmaf(r, m.w, acc.w);
+    for (int e0 = tid / LPR; e0 < R; e0 += 4 * RPP) {  // four rows read, then summed in order
+      float4 m[4];
+      float r[4];
+      bool ok[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int e = e0 + k * RPP;
+        ok[k] = e < R && src[W + e] != -2;
+        if (ok[k]) {
+          r[k] = wts[W + e];
+          m[k] = reinterpret_cast<const float4*>(rs + (W + e) * C)[c4];
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (!ok[k]) continue;
+        if (rsave)
+          *(reinterpret_cast<float4*>(rsave + (size_t(t) * R + e0 + k * RPP) * d_v) + c4) = m[k];
+        acc.x = fmaf(r[k], m[k].x, acc.x);
+        acc.y = fmaf(r[k], m[k].y, acc.y);
+        acc.z = fmaf(r[k], m[k].z, acc.z);
+        acc.w = fmaf(r[k], m[k].w, acc.w);
+      }
     }
 #pragma unroll
     for (int off = LPR; off < 32; off <<= 1) {
