@@ -100,9 +100,9 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
   constexpr int NB = 4;                      // rows per thread per round, loaded together
   extern __shared__ __align__(16) unsigned char smem[];
   const int W = a.W, R = a.R, T = a.T, d_v = a.d_v;
-  const int WR = W + R, WRa = (W + R + 3) & ~3;
+  const int WR = W + R;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float* red = reinterpret_cast<float*>(smem) + WRa;  // [2][warps][C], by token parity
+  float* red = reinterpret_cast<float*>(smem);  // [2][warps][C], by token parity
   // Two staging buffers of one token's [slots W | slots R | weights W | weights R | zero
   // bits] (the weights from the softmax pass): the next token's (going backwards) arrive by
   // cp.async while this one is processed.
@@ -294,8 +294,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_backward_kernel(BwdArgs a) {
 }
 
 size_t backward_smem_bytes(int C, int W, int R, int NF) {
-  const int WRa = (W + R + 3) & ~3;
-  return size_t(WRa) * 4 + size_t(2 * kBwdWarps) * C * 4 + size_t(2 * (2 * (W + R) + NF)) * 4;
+  return size_t(2 * kBwdWarps) * C * 4 + size_t(2 * (2 * (W + R) + NF)) * 4;
 }
 
 // Softmax of every token's write and read scores, one warp per (b, h, t), with the routine
