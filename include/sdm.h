@@ -46,7 +46,7 @@ typedef enum {
   SDM_ECUDA = -3,        /* a CUDA launch or query failed */
   SDM_ETIMEOUT = -4,     /* reserved: a bounded device wait ran out */
   SDM_EBOUNDS = -5,      /* reserved: device-detected bounds error */
-  SDM_EUNSUPPORTED = -6, /* sizes valid for the method but beyond this build's limits */
+  SDM_EUNSUPPORTED = -6, /* sizes valid for the method but beyond the library's limits */
   SDM_ENOSPACE = -7,     /* the workspace passed is smaller than required */
   SDM_ESCRATCH = -8      /* too large for sdm_scan_forward_noalloc's fixed scratch */
 } sdm_status;
@@ -58,7 +58,7 @@ typedef enum { SDM_F32 = 0, SDM_BF16 = 1 } sdm_dtype;
 #define SDM_DEV_DUP_WRITE 2   /* a slot appeared twice in one token's write set */
 #define SDM_DEV_TIMEOUT 4     /* a bounded wait inside a kernel ran out; outputs unspecified */
 
-/* Limits of this build (checked on the host, SDM_EUNSUPPORTED beyond them). */
+/* Limits of the library (checked on the host, SDM_EUNSUPPORTED beyond them). */
 #define SDM_MAX_S 4096   /* sqrt(N) */
 #define SDM_MAX_K 1024   /* W and R */
 #define SDM_MAX_DV 65536 /* d_v of the scan entry points */

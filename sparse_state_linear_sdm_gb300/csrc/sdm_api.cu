@@ -15,7 +15,7 @@ const char* sdm_status_str(int status) {
     case SDM_ECUDA: return "CUDA launch or query failed";
     case SDM_ETIMEOUT: return "bounded device wait ran out";
     case SDM_EBOUNDS: return "device-detected bounds error";
-    case SDM_EUNSUPPORTED: return "sizes beyond this build's limits";
+    case SDM_EUNSUPPORTED: return "sizes beyond the library's limits";
     case SDM_ENOSPACE: return "workspace smaller than required";
     case SDM_ESCRATCH: return "problem too large for the fixed no-allocation scratch";
     default: return "unknown status";

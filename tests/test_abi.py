@@ -44,7 +44,7 @@ def test_status_strings():
     lib = sdm.lib()
     for code in (0, -1, -2, -3, -4, -5, -6, -7):
         assert lib.sdm_status_str(code)
-    assert lib.sdm_status_str(-6) == b"sizes beyond this build's limits"
+    assert lib.sdm_status_str(-6) == b"sizes beyond the library's limits"
 
 
 FAKE = ctypes.c_void_p(0x10000)      # 16-byte aligned, never dereferenced on these paths
