@@ -91,7 +91,8 @@ def _rounding_merges(rng, shape, kind):
 
 @pytest.mark.parametrize("S,W,R", [(1, 1, 1), (2, 4, 3), (3, 5, 9), (5, 7, 2), (8, 8, 64), (16, 40, 16),
                                    (17, 33, 5), (32, 8, 8), (64, 100, 64), (100, 128, 1), (256, 32, 200),
-                                   (1024, 128, 128), (40, 1024, 512)])
+                                   (1024, 128, 128), (40, 1024, 512),
+                                   (4096, 1024, 7)])   # the library's limits: S = 4096, K = 1024
 @pytest.mark.parametrize("kind", ["ties_f32", "gauss_bf16", "gauss_f32", "merge_f32", "scaled_f32"])
 def test_select_matches_oracle(S, W, R, kind):
     rng = np.random.default_rng(S * 1000 + W * 7 + R)
@@ -156,6 +157,7 @@ def _oracle_problem(p, W, R):
     (2, 2, 300, 8, 32, 5, 3, torch.float32),       # many collisions across tokens
     (1, 1, 200, 16, 64, 64, 64, torch.bfloat16),   # plan chunks span, hash-heavy
     (3, 1, 129, 32, 16, 8, 8, torch.float32),
+    (1, 1, 24, 32, 8, 1024, 1024, torch.float32),  # W = R = N = 1024, the slot limit: every row each token
 ])
 def test_scan_edge_cases(B, H, T, S, dv, W, R, vdt):
     rng = np.random.default_rng(B * 100 + T)
