@@ -261,7 +261,9 @@ int sdm_scan_forward_train(float* M, const int32_t* idx_w, const float* sc_w,
  *          contents irrelevant (per (b, h, t): the column slices' partial sums and the
  *          softmax weights of the token's scores, formed by a parallel pass first).
  * Requires d_v % 4 == 0 and the limits of sdm_scan_forward; slots outside [0, N) are
- * skipped (their gradients are unspecified). */
+ * skipped (their gradients are unspecified).  A token's write slots are distinct, and so
+ * are its read slots (as sdm_select gives them); a repeated slot within either set gives
+ * unspecified gradients. */
 size_t sdm_scan_backward_workspace_size(int B, int H, int T, int d_v, int W, int R);
 
 /* sdm_scan_backward_ex - sdm_scan_backward with flags (0: the same call).
