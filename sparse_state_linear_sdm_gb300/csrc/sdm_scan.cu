@@ -150,9 +150,25 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
       if (t + d < T)
         fwd |= (reinterpret_cast<const int*>(meta + ((t + d) % QM) * meta_bytes + L.off_ab)[2] >> d) & 1;
 
-    // Forget gate and delta update of the W write rows (in shared memory and in HBM).  A
-    // thread's rows are distinct, so four of them are read before any is written back: their
-    // shared-memory latencies overlap instead of forming one chain.
+    // Forget gate and delta update of the W write rows (in shared memory and in HBM).
+    if (C <= 16 && W <= RPP) {  // narrow slices, at most one row per thread: no batching
+      const int e = tid / LPR;
+      if (e < W && src[e] != -2) {
+        const float4 m = reinterpret_cast<const float4*>(rs + e * C)[c4];
+        const float kb = beta * wts[e];
+        if (wsave) *(reinterpret_cast<float4*>(wsave + (size_t(t) * W + e) * d_v) + c4) = m;
+        float4 r;
+        float mt_;
+        mt_ = alpha * m.x; r.x = fmaf(kb, vv.x - mt_, mt_);
+        mt_ = alpha * m.y; r.y = fmaf(kb, vv.y - mt_, mt_);
+        mt_ = alpha * m.z; r.z = fmaf(kb, vv.z - mt_, mt_);
+        mt_ = alpha * m.w; r.w = fmaf(kb, vv.w - mt_, mt_);
+        reinterpret_cast<float4*>(rs + e * C)[c4] = r;
+        *(reinterpret_cast<float4*>(Mbh + size_t(idx[e]) * d_v) + c4) = r;
+      }
+    } else
+    // A thread's rows are distinct, so four of them are read before any is written back:
+    // their shared-memory latencies overlap instead of forming one chain.
     for (int e0 = tid / LPR; e0 < W; e0 += 4 * RPP) {
       float4 m[4];
       float kb[4];
@@ -208,6 +224,18 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
 
     // Weighted read of the R read rows (after the write).
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (C <= 16 && R <= RPP) {  // narrow slices, at most one row per thread
+      const int e = tid / LPR;
+      if (e < R && src[W + e] != -2) {
+        const float r = wts[W + e];
+        const float4 m = reinterpret_cast<const float4*>(rs + (W + e) * C)[c4];
+        if (rsave) *(reinterpret_cast<float4*>(rsave + (size_t(t) * R + e) * d_v) + c4) = m;
+        acc.x = fmaf(r, m.x, acc.x);
+        acc.y = fmaf(r, m.y, acc.y);
+        acc.z = fmaf(r, m.z, acc.z);
+        acc.w = fmaf(r, m.w, acc.w);
+      }
+    } else
     for (int e0 = tid / LPR; e0 < R; e0 += 4 * RPP) {  // four rows read, then summed in order
       float4 m[4];
       float r[4];
