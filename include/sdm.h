@@ -218,8 +218,9 @@ int sdm_forward(const void* kp, const void* qp, int in_dt, const void* v, int v_
                 float* sc_r, float* o, void* workspace, size_t workspace_bytes, int* dev_err,
                 void* stream);
 
-/* sdm_forward with the chunking chosen: `chunks` token chunks (0 = automatic, about 512
- * tokens each; the effective count is sdm_forward_chunks(T, chunks)), and, when
+/* sdm_forward with the chunking chosen: `chunks` token chunks (0 = automatic: about 512
+ * tokens each, 1024 when T >= 8192; the effective count is sdm_forward_chunks(T, chunks)),
+ * and, when
  * `scan_events` is not NULL, 2 * chunks cudaEvent_t recorded right before and after each
  * chunk's scan kernel on the stream it runs on (for timing the scan kernel).  The
  * workspace must hold sdm_forward_workspace_size(..., chunks) bytes. */

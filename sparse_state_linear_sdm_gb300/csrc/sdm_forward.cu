@@ -36,7 +36,13 @@ namespace sdm {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kAutoChunkTokens = 512;
+// Automatic chunk size: 512 tokens, or 1024 from 8192 tokens on.  Every chunk's scan launch
+// has a fixed cost and the first chunk's selection and planning run before any scan; with 8
+// or more chunks of 1024 that head start is amortised and the fewer launches win (B16 H4
+// T8192: 25.74-25.79 ms against 26.12-26.15 with 512; 65,536-token calls of the 1M-token
+// stream: 946 against 958 ms), with shorter sequences 512 (B4 H8 T2048: 2.03 against 2.06
+// ms; B8 H16 T4096: 11.01 against 11.19 ms).
+inline int auto_chunk_tokens(int T) { return T >= 8192 ? 1024 : 512; }
 constexpr int kMaxChunks = 256;
 
 struct Pipeline {
@@ -78,7 +84,8 @@ int pipeline_of_current_device(Pipeline** out) {
 // Tokens per chunk for a chunk-count request (0 = automatic, about kAutoChunkTokens).
 int forward_chunk_tokens(int T, int chunks) {
   if (T <= 0) return 0;
-  int n = chunks > 0 ? chunks : (T + kAutoChunkTokens - 1) / kAutoChunkTokens;
+  const int auto_tokens = auto_chunk_tokens(T);
+  int n = chunks > 0 ? chunks : (T + auto_tokens - 1) / auto_tokens;
   if (n > kMaxChunks) n = kMaxChunks;
   if (n > T) n = T;
   if (n < 1) n = 1;

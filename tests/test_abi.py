@@ -161,7 +161,9 @@ def test_forward_rejects_bad_arguments_without_launching():
 
 def test_forward_chunking_and_workspace_sizes():
     lib = sdm.lib()
-    assert lib.sdm_forward_chunks(8192, 0) == 16     # about 512 tokens per chunk
+    assert lib.sdm_forward_chunks(8192, 0) == 8      # 1024 tokens per chunk from T = 8192 on
+    assert lib.sdm_forward_chunks(8191, 0) == 16     # about 512 tokens per chunk below
+    assert lib.sdm_forward_chunks(65536, 0) == 64
     assert lib.sdm_forward_chunks(8192, 3) == 3
     assert lib.sdm_forward_chunks(1000, 0) == 2
     assert lib.sdm_forward_chunks(500, 0) == 1
