@@ -198,18 +198,21 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
       }
     }
 
-    // Forwarding: rows of tokens t .. t+PD whose latest writer is token t.
+    // Forwarding: rows of tokens t+1 .. t+PD whose latest writer is token t are copied into
+    // those tokens' staging slots (their first barrier orders the copies); a read slot of
+    // this token that names a row it writes reads the updated row where the write left it.
+    // Both need the write phase's rows from every thread: one barrier.
     if (fwd) {
     __syncthreads();
 #pragma unroll
-    for (int d = 0; d <= PD; ++d) {
+    for (int d = 1; d <= PD; ++d) {
       const int u = t + d;
       if (u >= T) break;
       const unsigned char* mu = meta + (u % QM) * meta_bytes;
       const int16_t* su = reinterpret_cast<const int16_t*>(mu + L.off_src);
       float* ru = rows + size_t(u % QR) * WR * C;
       const int lo = d * W;
-      for (int e = (d == 0 ? W : 0) + tid; e < WR; e += kScanThreads) {
+      for (int e = tid; e < WR; e += kScanThreads) {
         const int code = su[e];
         if (code >= lo && code < lo + W) {
           const float4* from = reinterpret_cast<const float4*>(rs + (code - lo) * C);
@@ -219,16 +222,17 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
         }
       }
     }
-    __syncthreads();
     }
 
     // Weighted read of the R read rows (after the write).
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (C <= 16 && R <= RPP) {  // narrow slices, at most one row per thread
       const int e = tid / LPR;
-      if (e < R && src[W + e] != -2) {
+      const int code = e < R ? src[W + e] : -2;
+      if (code != -2) {
         const float r = wts[W + e];
-        const float4 m = reinterpret_cast<const float4*>(rs + (W + e) * C)[c4];
+        const int row = code >= 0 && code < W ? code : W + e;  // this token's write row
+        const float4 m = reinterpret_cast<const float4*>(rs + row * C)[c4];
         if (rsave) *(reinterpret_cast<float4*>(rsave + (size_t(t) * R + e) * d_v) + c4) = m;
         acc.x = fmaf(r, m.x, acc.x);
         acc.y = fmaf(r, m.y, acc.y);
@@ -243,10 +247,12 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int e = e0 + k * RPP;
-        ok[k] = e < R && src[W + e] != -2;
+        const int code = e < R ? src[W + e] : -2;
+        ok[k] = code != -2;
         if (ok[k]) {
           r[k] = wts[W + e];
-          m[k] = reinterpret_cast<const float4*>(rs + (W + e) * C)[c4];
+          const int row = code >= 0 && code < W ? code : W + e;  // this token's write row
+          m[k] = reinterpret_cast<const float4*>(rs + row * C)[c4];
         }
       }
 #pragma unroll
