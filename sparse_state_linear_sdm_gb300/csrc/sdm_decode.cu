@@ -16,7 +16,8 @@
 //      through a small hash of the write slots), and the device error checks.
 //   3. the scan of the token by groups of 256 threads, each taking column slices in turn
 //      with the scan kernel's thread mapping and arithmetic for a block of that slice:
-//      gather, forget gate and delta update, write-back, forwarding, weighted read reduced
+//      gather, forget gate and delta update, write-back, weighted read (a read slot the
+//      token also writes taking the updated row in place) reduced
 //      in the same order.  The slice width is the one the scan kernel would use for these
 //      sizes (choose_scan_shape), so the read's sum runs in the same order too.
 // So every output is bit-identical to the three-kernel path.
@@ -555,22 +556,15 @@ __global__ void __launch_bounds__(TEAM ? 512 : 256, 1) decode_kernel(DecodeArgs 
       *(reinterpret_cast<float4*>(Mc + size_t(idx[e]) * d_v) + c4) = r;
     }
     team_bar(gbar, 256);
-    // Read rows this token also writes take the updated row.
-    for (int e = W + lt; e < WR; e += 256) {
-      const int code = src[e];
-      if (code >= 0 && code < W) {
-        const float4* from = reinterpret_cast<const float4*>(rg + code * C);
-        float4* to = reinterpret_cast<float4*>(rg + e * C);
-        for (int q = 0; q < LPR; ++q) to[q] = from[q];
-      }
-    }
-    team_bar(gbar, 256);
-    // Weighted read of the R read rows (after the write), in the scan kernel's order.
+    // Weighted read of the R read rows (after the write), in the scan kernel's order; a read
+    // of a row this token also writes takes the updated row where the write left it.
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int e = lt / LPR; e < R; e += RPP) {
-      if (src[W + e] == -2) continue;
+      const int code = src[W + e];
+      if (code == -2) continue;
       const float r = wts[W + e];
-      const float4 m = reinterpret_cast<const float4*>(rg + (W + e) * C)[c4];
+      const int row = code >= 0 && code < W ? code : W + e;
+      const float4 m = reinterpret_cast<const float4*>(rg + row * C)[c4];
       acc.x = fmaf(r, m.x, acc.x);
       acc.y = fmaf(r, m.y, acc.y);
       acc.z = fmaf(r, m.z, acc.z);
