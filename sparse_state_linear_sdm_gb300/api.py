@@ -640,10 +640,12 @@ class DecodeStep:
     default where its shared memory fits), else the selection, planning and scan kernels.
 
     The state M [B, H, N, d_v] stays in place across steps; each step takes k', q' halves
-    [B, H, 1, 2, S], v [B, H, 1, d_v] and alpha, beta [B, H, 1] (copied into the graph's
-    static input buffers) and returns o [B, H, 1, d_v] (the graph's static output buffer:
-    copy it before the next step if it must be kept).  Chaining steps gives exactly the
-    result of one scan over the same tokens."""
+    [B, H, 1, 2, S], v [B, H, 1, d_v] and alpha, beta [B, H, 1] and returns o [B, H, 1, d_v]
+    (the step's static output buffer: copy it before the next step if it must be kept).
+    With the single kernel, inputs laid out as the static buffers (contiguous, same dtypes,
+    on M's device) are read where they are: one launch, no copy.  Otherwise they are copied
+    into the static buffers and the graph (or the unfused kernels) runs on those.  Chaining
+    steps gives exactly the result of one scan over the same tokens."""
 
     def __init__(self, M, W: int, R: int, in_dtype=torch.bfloat16, S=None, fused=None):
         B, H, N, dv = M.shape
@@ -670,6 +672,9 @@ class DecodeStep:
         self.ws = scan_workspace(B, H, 1, dv, W, R, dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.graph = None
+        # Fixed arguments of the single-kernel launch on the caller's tensors.
+        self._fixed_out = tuple(_p(t) for t in self.sel) + (_p(self.o), _p(self.err))
+        self._sizes = (B, H, S, dv, W, R)
 
     def _body(self):
         if self.fused:
@@ -720,7 +725,26 @@ class DecodeStep:
             self.graph.replay()
         return self.o
 
+    def _direct(self, kp, qp, v, alpha, beta) -> bool:
+        """The single kernel launched on the caller's tensors where they are laid out as the
+        static buffers (no copy); False where they are not."""
+        if not self.fused:
+            return False
+        for x, buf in ((kp, self.kp), (qp, self.qp), (v, self.v), (alpha, self.alpha), (beta, self.beta)):
+            if (not isinstance(x, torch.Tensor) or x.dtype != buf.dtype or x.shape != buf.shape
+                    or x.device != buf.device or not x.is_contiguous()):
+                return False
+        dev = self.M.device
+        if torch.cuda.current_device() != dev.index:
+            with torch.cuda.device(dev):
+                return self._direct(kp, qp, v, alpha, beta)
+        _call("sdm_decode_step", _p(kp), _p(qp), _dtype_code(kp), _p(v), _dtype_code(v), _p(alpha), _p(beta),
+              _p(self.M), *self._sizes, *self._fixed_out, _stream(dev))
+        return True
+
     def __call__(self, kp, qp, v, alpha, beta):
+        if self._direct(kp, qp, v, alpha, beta):
+            return self.o
         self.kp.copy_(kp, non_blocking=True)
         self.qp.copy_(qp, non_blocking=True)
         self.v.copy_(v, non_blocking=True)

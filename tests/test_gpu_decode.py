@@ -13,8 +13,12 @@ from sdm_testlib import TOL, device_inputs, device_M0, host_heads, oracle_heads,
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("graph", [False, True])
-def test_decode_steps_equal_one_scan(graph):
+@pytest.mark.parametrize("graph,contiguous", [(False, False), (True, False), (True, True)],
+                         ids=["copies", "copies+graph", "direct"])
+def test_decode_steps_equal_one_scan(graph, contiguous):
+    """Token slices of [B, H, T, ...] inputs are strided: they are copied into the step's
+    buffers (then the captured graph or a plain launch runs).  Contiguous per-token inputs
+    are read where they are by one launch of the single kernel."""
     cfg = wl.B4H8_T2048
     T = 48
     d = device_inputs(cfg, T=T)
@@ -23,12 +27,16 @@ def test_decode_steps_equal_one_scan(graph):
     M = torch.empty_like(M_ref)
     sdm.init_state_from_M0(M, M0)
     step = sdm.DecodeStep(M, cfg.W, cfg.R, in_dtype=torch.bfloat16)
+    assert step.fused
     if graph:
         step.capture()
     outs = []
     for t in range(T):
-        o = step(d["kp"][:, :, t:t + 1], d["qp"][:, :, t:t + 1], d["v"][:, :, t:t + 1],
-                 d["alpha"][:, :, t:t + 1], d["beta"][:, :, t:t + 1])
+        args = [d[k][:, :, t:t + 1] for k in ("kp", "qp", "v", "alpha", "beta")]
+        if contiguous:
+            args = [a.contiguous() for a in args]
+        assert all(a.is_contiguous() for a in args) == contiguous
+        o = step(*args)
         outs.append(o.clone())
     torch.cuda.synchronize()
     assert step.err.item() == 0
