@@ -672,9 +672,13 @@ class DecodeStep:
         self.ws = scan_workspace(B, H, 1, dv, W, R, dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.graph = None
-        # Fixed arguments of the single-kernel launch on the caller's tensors.
-        self._fixed_out = tuple(_p(t) for t in self.sel) + (_p(self.o), _p(self.err))
-        self._sizes = (B, H, S, dv, W, R)
+        # Fixed arguments of the single-kernel launch on the caller's tensors (plain integer
+        # addresses: ctypes converts them for the c_void_p parameters).
+        self._fn = lib().sdm_decode_step
+        self._codes = (_dtype_code(self.kp), _dtype_code(self.v))
+        self._tail = (M.data_ptr(), B, H, S, dv, W, R) + tuple(t.data_ptr() for t in self.sel) + (
+            self.o.data_ptr(), self.err.data_ptr())
+        self._bufs = (self.kp, self.qp, self.v, self.alpha, self.beta)
 
     def _body(self):
         if self.fused:
@@ -730,7 +734,7 @@ class DecodeStep:
         static buffers (no copy); False where they are not."""
         if not self.fused:
             return False
-        for x, buf in ((kp, self.kp), (qp, self.qp), (v, self.v), (alpha, self.alpha), (beta, self.beta)):
+        for x, buf in zip((kp, qp, v, alpha, beta), self._bufs):
             if (not isinstance(x, torch.Tensor) or x.dtype != buf.dtype or x.shape != buf.shape
                     or x.device != buf.device or not x.is_contiguous()):
                 return False
@@ -738,8 +742,11 @@ class DecodeStep:
         if torch.cuda.current_device() != dev.index:
             with torch.cuda.device(dev):
                 return self._direct(kp, qp, v, alpha, beta)
-        _call("sdm_decode_step", _p(kp), _p(qp), _dtype_code(kp), _p(v), _dtype_code(v), _p(alpha), _p(beta),
-              _p(self.M), *self._sizes, *self._fixed_out, _stream(dev))
+        st = self._fn(kp.data_ptr(), qp.data_ptr(), self._codes[0], v.data_ptr(), self._codes[1],
+                      alpha.data_ptr(), beta.data_ptr(), *self._tail,
+                      torch.cuda.current_stream(dev).cuda_stream)
+        if st != 0:
+            raise SDMError("sdm_decode_step", st)
         return True
 
     def __call__(self, kp, qp, v, alpha, beta):
