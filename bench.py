@@ -282,10 +282,11 @@ def make_state(cfg, rank, dev, torch, sdm, wl):
     return st
 
 
-def run_forward(st, cfg, sdm, args, inp=None, o=None, scan_ev=None):
+def run_forward(st, cfg, sdm, args, inp=None, o=None, scan_ev=None, input_ev=None):
     """One forward pass through the public pipelined entry point (sdm_forward): state
     from M0, selection and planning of token chunk c+1 overlapping the scan of chunk c.
-    scan_ev: 2 * chunks timing events recorded around each chunk's scan kernel."""
+    scan_ev: 2 * chunks timing events recorded around each chunk's scan kernel.
+    input_ev: chunks events, chunk c's inputs ready (sdm_forward_streamed)."""
     inp = st if inp is None else inp
     o = st["o"] if o is None else o
     if st["fws"].numel() < sdm.lib().sdm_forward_workspace_size(cfg.B, cfg.H, cfg.T, cfg.d_v, cfg.W, cfg.R,
@@ -293,7 +294,7 @@ def run_forward(st, cfg, sdm, args, inp=None, o=None, scan_ev=None):
         st["fws"] = sdm.forward_workspace(cfg.B, cfg.H, cfg.T, cfg.d_v, cfg.W, cfg.R, st["M"].device, args.chunks)
     sdm.forward(inp["kp"], inp["qp"], inp["v"], inp["alpha"], inp["beta"], st["M0"], cfg.W, cfg.R, M=st["M"],
                 workspace=st["fws"], dev_err=st["err"], out=st["sel"], o=o, chunks=args.chunks,
-                scan_events=scan_ev)
+                scan_events=scan_ev, input_events=input_ev)
 
 
 def run_step(st, cfg, sdm, args, ev=None, before_select=None, inp=None, o=None):
@@ -559,7 +560,10 @@ def e2e(st, cfg, sdm, args, dev, torch, K, world):
     step copies its k', q', v, alpha, beta host->device and its o device->host inside the
     timed region.  Streamed like a serving loop: device inputs and outputs are double
     buffered, so step k+1's host->device copies (on a copy stream) overlap step k's
-    compute, and step k's device->host copy overlaps step k+1."""
+    compute, and step k's device->host copy overlaps step k+1.  With the pipelined pass a
+    step's inputs are copied token window by token window (one window per chunk) and each
+    chunk's selection waits only for its own window (sdm_forward_streamed), so the first
+    step starts on its first window instead of the whole batch."""
     names = ("kp", "qp", "v", "alpha", "beta")
     host = {k: torch.empty(st[k].shape, dtype=st[k].dtype, pin_memory=True) for k in names}
     for k in names:
@@ -585,8 +589,12 @@ def e2e(st, cfg, sdm, args, dev, torch, K, world):
         torch.cuda.synchronize(dev)
         rates[label] = round(src.numel() * src.element_size() / a.elapsed_time(b) / 1e6, 1)
 
+    pipelined = args.pipeline == "on"
+    Tc = -(-cfg.T // chunks)
+
     def run(n):
         ready = [torch.cuda.Event() for _ in range(n + 1)]
+        window = [[torch.cuda.Event() for _ in range(chunks)] for _ in range(n + 1)]
         free = [torch.cuda.Event() for _ in range(n)]       # inputs of step k consumed
         done = [torch.cuda.Event() for _ in range(n)]       # o of step k written
         copy.wait_stream(main)
@@ -595,13 +603,21 @@ def e2e(st, cfg, sdm, args, dev, torch, K, world):
             with torch.cuda.stream(copy):
                 if k >= 2:
                     copy.wait_event(free[k - 2])
-                for name in names:
-                    bufs[k % 2][name].copy_(host[name], non_blocking=True)
+                if pipelined:
+                    for c in range(chunks):
+                        t0, t1 = c * Tc, min(cfg.T, (c + 1) * Tc)
+                        for name in names:
+                            sdm.copy_token_window(bufs[k % 2][name], host[name], t0, t1, stream=copy)
+                        window[k][c].record(copy)
+                else:
+                    for name in names:
+                        bufs[k % 2][name].copy_(host[name], non_blocking=True)
                 ready[k].record(copy)
 
         h2d_step(0)
         for k in range(n):
-            main.wait_event(ready[k])
+            if not pipelined:
+                main.wait_event(ready[k])
             if k + 1 < n:
                 h2d_step(k + 1)
             # the inputs are free once the (last) scan kernel starts: selection and planning
@@ -609,7 +625,8 @@ def e2e(st, cfg, sdm, args, dev, torch, K, world):
             if args.pipeline == "on":
                 sev = [torch.cuda.Event() for _ in range(2 * chunks)]
                 sev[2 * chunks - 2] = free[k]
-                run_forward(st, cfg, sdm, args, inp=bufs[k % 2], o=outs[k % 2], scan_ev=sev)
+                run_forward(st, cfg, sdm, args, inp=bufs[k % 2], o=outs[k % 2], scan_ev=sev,
+                            input_ev=window[k])
             else:
                 run_step(st, cfg, sdm, args, inp=bufs[k % 2], o=outs[k % 2],
                          ev=[torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event(), free[k],
@@ -635,6 +652,10 @@ def e2e(st, cfg, sdm, args, dev, torch, K, world):
     return {"value": whole_job_rate(cfg.B * cfg.H * cfg.T, n, world, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms / n, **rates,
             "pipeline": "double-buffered: step k+1's host->device copies and step k's device->host copy "
+                        "overlap step k's compute (copy stream); inputs copied token window by window, "
+                        "each chunk's selection waiting for its own window (sdm_forward_streamed)"
+                        if pipelined else
+                        "double-buffered: step k+1's host->device copies and step k's device->host copy "
                         "overlap step k's compute (copy stream)"}
 
 

@@ -225,6 +225,27 @@ int sdm_forward(const void* kp, const void* qp, int in_dt, const void* v, int v_
  * chunk's scan kernel on the stream it runs on (for timing the scan kernel).  The
  * workspace must hold sdm_forward_workspace_size(..., chunks) bytes. */
 int sdm_forward_chunks(int T, int chunks);
+/* sdm_forward_tuned whose inputs may still be arriving: when `input_ready` is not NULL it
+ * holds sdm_forward_chunks(T, chunks) cudaEvent_t (an entry may be NULL), and the selection
+ * and planning of token chunk c (tokens c*Tc .. c*Tc+Tc-1 of every (b, h), Tc =
+ * ceil(T / chunks)) start only after input_ready[c] (its latest record at the time of the
+ * call) has completed; the state initialisation does not wait.  So a caller copying a
+ * batch's inputs token window by token window (sdm_copy_rows_async) lets the pass start on
+ * the first window.  The events are only waited on, never recorded; the rest is
+ * sdm_forward_tuned. */
+int sdm_forward_streamed(const void* kp, const void* qp, int in_dt, const void* v, int v_dt,
+                         const float* alpha, const float* beta, const float* M0, float* M, int B,
+                         int H, int T, int S, int d_v, int W, int R, int32_t* idx_w, float* sc_w,
+                         int32_t* idx_r, float* sc_r, float* o, void* workspace,
+                         size_t workspace_bytes, int* dev_err, int chunks,
+                         void* const* scan_events, void* const* input_ready, void* stream);
+/* sdm_copy_rows_async - `rows` rows of `row_bytes` bytes from src (rows `src_pitch` bytes
+ * apart) to dst (rows `dst_pitch` bytes apart), asynchronously on `stream`; either side may
+ * be device memory or pinned host memory (the direction follows from the addresses).  One
+ * token window of a [B, H, T, ...] input for every (b, h) is B*H such rows.  SDM_EINVAL for
+ * null pointers or a pitch below row_bytes; nothing to do for zero rows or bytes. */
+int sdm_copy_rows_async(void* dst, size_t dst_pitch, const void* src, size_t src_pitch,
+                        size_t row_bytes, size_t rows, void* stream);
 int sdm_forward_tuned(const void* kp, const void* qp, int in_dt, const void* v, int v_dt,
                       const float* alpha, const float* beta, const float* M0, float* M, int B,
                       int H, int T, int S, int d_v, int W, int R, int32_t* idx_w, float* sc_w,

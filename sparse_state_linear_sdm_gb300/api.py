@@ -59,6 +59,9 @@ def lib() -> ctypes.CDLL:
             L.sdm_forward_tuned.argtypes = [p, p, i, p, i, p, p, p, p, i, i, i, i, i, i, i, p, p, p, p, p, p,
                                             sz, p, i, p, p]
             L.sdm_forward.argtypes = [p, p, i, p, i, p, p, p, p, i, i, i, i, i, i, i, p, p, p, p, p, p, sz, p, p]
+            L.sdm_forward_streamed.argtypes = [p, p, i, p, i, p, p, p, p, i, i, i, i, i, i, i, p, p, p, p, p,
+                                               p, sz, p, i, p, p, p]
+            L.sdm_copy_rows_async.argtypes = [p, sz, p, sz, sz, sz, p]
             L.sdm_scan_forward_train.argtypes = [p, p, p, p, p, p, i, p, p, i, i, i, ll, i, i, i, p, p, p, p, sz, p, p]
             L.sdm_scan_backward_workspace_size.argtypes = [i, i, i, i, i, i]
             L.sdm_scan_backward_workspace_size.restype = sz
@@ -374,7 +377,8 @@ def forward_workspace(B: int, H: int, T: int, d_v: int, W: int, R: int, device, 
 
 @_on_tensor_device
 def forward(kp, qp, v, alpha, beta, M0, W: int, R: int, M=None, workspace=None, dev_err=None,
-            overlap: bool = True, out=None, o=None, chunks: int = 0, scan_events=None):
+            overlap: bool = True, out=None, o=None, chunks: int = 0, scan_events=None,
+            input_events=None):
     """One SDM forward pass over a batch: state from M0 (or, with M0=None, from the state
     already in M), selection, scan.  Returns (o, M, (idx_w, sc_w, idx_r, sc_r)).
 
@@ -382,7 +386,10 @@ def forward(kp, qp, v, alpha, beta, M0, W: int, R: int, M=None, workspace=None, 
     chunk c on the library's own streams (chunks=0: automatic).  overlap=False runs the
     three steps one after the other on the current stream.  Both give the same bits.
     scan_events: optional list of 2 * forward_chunks(T, chunks) torch.cuda.Event, recorded
-    around each chunk's scan kernel."""
+    around each chunk's scan kernel.  input_events: optional list of forward_chunks(T, chunks)
+    torch.cuda.Event (or None entries), already recorded: chunk c's selection and planning
+    wait for input_events[c] (sdm_forward_streamed), e.g. its token window's copy
+    (copy_token_window); the state initialisation does not wait."""
     B, H, T, _, S = kp.shape
     dv = v.shape[-1]
     if M is None:
@@ -428,10 +435,43 @@ def forward(kp, qp, v, alpha, beta, M0, W: int, R: int, M=None, workspace=None, 
             if e.cuda_event == 0:
                 e.record()  # torch creates its events lazily; the library records it again
         ev_arr = (ctypes.c_void_p * len(scan_events))(*[e.cuda_event for e in scan_events])
-    _call("sdm_forward_tuned", _p(kp), _p(qp), _dtype_code(kp), _p(v), _dtype_code(v), _p(alpha), _p(beta),
-          _p(M0), _p(M), B, H, T, S, dv, W, R, _p(idx_w), _p(sc_w), _p(idx_r), _p(sc_r), _p(o),
-          _p(workspace), workspace.numel(), _p(dev_err), int(chunks), ev_arr, _stream(M.device))
+    in_arr = None
+    if input_events is not None:
+        if not overlap:
+            raise ValueError("input_events needs the pipelined pass (overlap=True)")
+        if len(input_events) != forward_chunks(T, chunks):
+            raise ValueError("input_events needs forward_chunks(T, chunks) events")
+        in_arr = (ctypes.c_void_p * len(input_events))(
+            *[None if e is None or e.cuda_event == 0 else e.cuda_event for e in input_events])
+    _call("sdm_forward_streamed", _p(kp), _p(qp), _dtype_code(kp), _p(v), _dtype_code(v), _p(alpha),
+          _p(beta), _p(M0), _p(M), B, H, T, S, dv, W, R, _p(idx_w), _p(sc_w), _p(idx_r), _p(sc_r), _p(o),
+          _p(workspace), workspace.numel(), _p(dev_err), int(chunks), ev_arr, in_arr, _stream(M.device))
     return o, M, out
+
+
+def copy_token_window(dst, src, t0: int, t1: int, stream=None):
+    """Copy tokens t0 .. t1-1 of every (b, h) from src to dst, both [B, H, T, ...] contiguous
+    with the same shape and dtype, one on the GPU and the other pinned host memory (or both on
+    the GPU): one strided copy of B*H rows (sdm_copy_rows_async) on `stream` (default: the
+    current stream of the GPU tensor's device)."""
+    if dst.shape != src.shape or dst.dtype != src.dtype:
+        raise ValueError("dst and src must have the same shape and dtype")
+    if not (dst.is_contiguous() and src.is_contiguous()):
+        raise ValueError("dst and src must be contiguous")
+    if dst.dim() < 3 or not 0 <= t0 <= t1 <= dst.shape[2]:
+        raise ValueError("need [B, H, T, ...] tensors and 0 <= t0 <= t1 <= T")
+    if not (dst.is_cuda or src.is_cuda):
+        raise ValueError("one side must be on the GPU")
+    for t in (dst, src):
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError("host tensors must be pinned")
+    dev = dst.device if dst.is_cuda else src.device
+    tok = dst.element_size() * (dst[0, 0, 0].numel() if dst.shape[2] > 0 else 0)
+    pitch = tok * dst.shape[2]
+    off = tok * t0
+    s = torch.cuda.current_stream(dev) if stream is None else stream
+    _call("sdm_copy_rows_async", ctypes.c_void_p(dst.data_ptr() + off), pitch, ctypes.c_void_p(src.data_ptr() + off),
+          pitch, tok * (t1 - t0), dst.shape[0] * dst.shape[1], ctypes.c_void_p(s.cuda_stream))
 
 
 @_on_tensor_device

@@ -117,12 +117,12 @@ int sdm_forward_chunks(int T, int chunks) {
   return Tc > 0 ? (T + Tc - 1) / Tc : 0;
 }
 
-int sdm_forward_tuned(const void* kp, const void* qp, int in_dt, const void* v, int v_dt,
-                      const float* alpha, const float* beta, const float* M0, float* M, int B,
-                      int H, int T, int S, int d_v, int W, int R, int32_t* idx_w, float* sc_w,
-                      int32_t* idx_r, float* sc_r, float* o, void* workspace,
-                      size_t workspace_bytes, int* dev_err, int chunks, void* const* scan_events,
-                      void* stream) {
+int sdm_forward_streamed(const void* kp, const void* qp, int in_dt, const void* v, int v_dt,
+                         const float* alpha, const float* beta, const float* M0, float* M, int B,
+                         int H, int T, int S, int d_v, int W, int R, int32_t* idx_w, float* sc_w,
+                         int32_t* idx_r, float* sc_r, float* o, void* workspace,
+                         size_t workspace_bytes, int* dev_err, int chunks,
+                         void* const* scan_events, void* const* input_ready, void* stream) {
   int st = check_select_args(kp, qp, in_dt, B, H, T, S, W, R, idx_w, sc_w, idx_r, sc_r);
   if (st != SDM_OK) return st;
   const long long N = (long long)S * S;
@@ -169,6 +169,9 @@ int sdm_forward_tuned(const void* kp, const void* qp, int in_dt, const void* v, 
   for (int c = 0; c < n; ++c) {
     const TokenWindow win{BH, (c + 1) * Tc <= T ? Tc : T - c * Tc, T, c * Tc};
     const int b = c & 1;
+    // The chunk's k', q', v, alpha, beta may still be arriving (a copy per token window).
+    if (input_ready && input_ready[c])
+      SDM_CK(cudaStreamWaitEvent(p->sel, static_cast<cudaEvent_t>(input_ready[c]), 0));
     st = in_dt == SDM_BF16
              ? launch_select_bf16(kp, qp, win, S, W, R, idx_w, sc_w, idx_r, sc_r, p->sel, stairs)
              : launch_select_f32(kp, qp, win, S, W, R, idx_w, sc_w, idx_r, sc_r, p->sel, stairs);
@@ -194,6 +197,27 @@ int sdm_forward_tuned(const void* kp, const void* qp, int in_dt, const void* v, 
   SDM_CK(cudaStreamWaitEvent(s, p->plan_end, 0));
   SDM_CK(cudaStreamWaitEvent(s, p->scan_done, 0));
 #undef SDM_CK
+  return SDM_OK;
+}
+
+int sdm_forward_tuned(const void* kp, const void* qp, int in_dt, const void* v, int v_dt,
+                      const float* alpha, const float* beta, const float* M0, float* M, int B,
+                      int H, int T, int S, int d_v, int W, int R, int32_t* idx_w, float* sc_w,
+                      int32_t* idx_r, float* sc_r, float* o, void* workspace,
+                      size_t workspace_bytes, int* dev_err, int chunks, void* const* scan_events,
+                      void* stream) {
+  return sdm_forward_streamed(kp, qp, in_dt, v, v_dt, alpha, beta, M0, M, B, H, T, S, d_v, W, R,
+                              idx_w, sc_w, idx_r, sc_r, o, workspace, workspace_bytes, dev_err,
+                              chunks, scan_events, nullptr, stream);
+}
+
+int sdm_copy_rows_async(void* dst, size_t dst_pitch, const void* src, size_t src_pitch,
+                        size_t row_bytes, size_t rows, void* stream) {
+  if (rows == 0 || row_bytes == 0) return SDM_OK;
+  if (!dst || !src || dst_pitch < row_bytes || src_pitch < row_bytes) return SDM_EINVAL;
+  if (cudaMemcpy2DAsync(dst, dst_pitch, src, src_pitch, row_bytes, rows, cudaMemcpyDefault,
+                        as_stream(stream)) != cudaSuccess)
+    return SDM_ECUDA;
   return SDM_OK;
 }
 

@@ -157,6 +157,20 @@ def test_forward_rejects_bad_arguments_without_launching():
     assert call(M0=ODD) == EALIGN
     assert call(ws=ODD) == EALIGN
     assert call(ws_bytes=16) == ENOSPACE
+    # the streamed variant checks the same arguments before it looks at its events
+    streamed = lib.sdm_forward_streamed(FAKE, FAKE, 1, FAKE, 0, FAKE, FAKE, None, FAKE, 1, 1, 8, 8, 6, 4, 4,
+                                        FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, None, 0, None, None, None)
+    assert streamed == EINVAL                  # d_v = 6
+
+
+def test_copy_rows_checks_its_arguments_without_copying():
+    lib = sdm.lib()
+    assert lib.sdm_copy_rows_async(None, 64, FAKE, 64, 64, 2, None) == EINVAL
+    assert lib.sdm_copy_rows_async(FAKE, 64, None, 64, 64, 2, None) == EINVAL
+    assert lib.sdm_copy_rows_async(FAKE, 32, FAKE, 64, 64, 2, None) == EINVAL   # pitch below the row
+    assert lib.sdm_copy_rows_async(FAKE, 64, FAKE, 32, 64, 2, None) == EINVAL
+    assert lib.sdm_copy_rows_async(FAKE, 64, FAKE, 64, 64, 0, None) == 0        # nothing to copy
+    assert lib.sdm_copy_rows_async(FAKE, 64, FAKE, 64, 0, 2, None) == 0
 
 
 def test_forward_chunking_and_workspace_sizes():

@@ -125,3 +125,51 @@ def test_pipelined_forward_from_M0_writes_every_row(B, H, T, S, dv, W, R, chunks
     ws.copy_(torch.randint(0, 256, ws.shape, dtype=torch.uint8, device="cuda"))
     got = _run(d, M0, W, R, chunks=chunks, M=M, workspace=ws)
     _assert_same(got, ref, (B, H, T, S, chunks))
+
+
+NAMES = ("kp", "qp", "v", "alpha", "beta")
+
+
+def test_copy_token_window_moves_exactly_its_tokens():
+    cfg = wl.B4H8_T2048
+    d = device_inputs(cfg, T=100)
+    host = {k: d[k].cpu().pin_memory() for k in NAMES}
+    for k in NAMES:
+        dst = torch.full_like(d[k], -7.0)
+        sdm.copy_token_window(dst, host[k], 30, 77)       # host -> device
+        sdm.copy_token_window(dst, d[k], 0, 5)            # device -> device
+        torch.cuda.synchronize()
+        assert torch.equal(dst[:, :, 30:77], d[k][:, :, 30:77]), k
+        assert torch.equal(dst[:, :, 0:5], d[k][:, :, 0:5]), k
+        assert bool((dst[:, :, 5:30] == -7.0).all()) and bool((dst[:, :, 77:] == -7.0).all()), k
+        back = torch.zeros_like(host[k]).pin_memory()
+        sdm.copy_token_window(back, dst, 30, 77)          # device -> host
+        torch.cuda.synchronize()
+        assert torch.equal(back[:, :, 30:77], host[k][:, :, 30:77]), k
+
+
+@pytest.mark.parametrize("chunks", [3, 4])
+def test_inputs_arriving_window_by_window(chunks):
+    """The batch's inputs copied from pinned host memory one token window at a time on a
+    copy stream, the pass waiting for each window's copy before its chunk's selection
+    (sdm_forward_streamed): the same bits as with the inputs resident."""
+    cfg = wl.B4H8_T2048
+    d = device_inputs(cfg)
+    M0 = device_M0(cfg)
+    ref = _run(d, M0, cfg.W, cfg.R, chunks=chunks)
+    host = {k: d[k].cpu().pin_memory() for k in NAMES}
+    dst = {k: torch.full_like(d[k], float("nan")) for k in NAMES}
+    torch.cuda.synchronize()
+    n = sdm.forward_chunks(cfg.T, chunks)
+    Tc = -(-cfg.T // n)
+    copy = torch.cuda.Stream()
+    evs = []
+    for c in range(n):
+        for k in NAMES:
+            sdm.copy_token_window(dst[k], host[k], c * Tc, min(cfg.T, (c + 1) * Tc), stream=copy)
+        e = torch.cuda.Event()
+        e.record(copy)
+        evs.append(e)
+    got = _run(dst, M0, cfg.W, cfg.R, chunks=chunks, input_events=evs)
+    _assert_same(got, ref, ("window by window", chunks))
+
