@@ -965,7 +965,7 @@ def run_backward(args):
         if ev:
             ev[1].record()
         g = sdm.scan_backward(*sel, st["v"], st["alpha"], st["beta"], w_prev, r_rows, dO, G, workspace=ws,
-                              final_zero=final_zero)
+                              final_zero=final_zero, dm0_only=final_zero)
         if ev:
             ev[2].record()
         sdm.select_backward(sel[0], g["dsc_w"], cfg.S, out=dkp)

@@ -303,6 +303,12 @@ size_t sdm_scan_backward_workspace_size(int B, int H, int T, int d_v, int W, int
  * Unknown flag bits: SDM_EINVAL (and a workspace size of 0).  Two read slots of one token
  * naming the same row give unspecified gradients, as in sdm_scan_backward. */
 #define SDM_BWD_FINAL_ZERO 1u
+/*   SDM_BWD_DM0_ONLY (with SDM_BWD_FINAL_ZERO): the caller needs the batch's dM0 but not G
+ *          per (b, h): the rows of G that no slot reads are left as they were instead of
+ *          being set to zero (G's contents on exit unspecified; dM0 and the other outputs
+ *          are those of the call without the flag).  dM0 must not be NULL (SDM_EINVAL).
+ *          Without SDM_BWD_FINAL_ZERO the flag changes nothing. */
+#define SDM_BWD_DM0_ONLY 2u
 size_t sdm_scan_backward_workspace_size_ex(int B, int H, int T, long long N, int d_v, int W, int R,
                                            unsigned flags);
 int sdm_scan_backward_ex(const int32_t* idx_w, const float* sc_w, const int32_t* idx_r,

@@ -500,6 +500,7 @@ def scan_forward_train(M, idx_w, sc_w, idx_r, sc_r, v, alpha, beta, o=None, work
 
 
 BWD_FINAL_ZERO = 1  # sdm_scan_backward_ex flag: dL/dM_T = 0, G's entry contents ignored
+BWD_DM0_ONLY = 2    # with BWD_FINAL_ZERO: dM0 wanted, G per (b, h) not (unread rows left as they were)
 
 
 def backward_workspace_size(B: int, H: int, T: int, N: int, d_v: int, W: int, R: int,
@@ -511,12 +512,14 @@ def backward_workspace_size(B: int, H: int, T: int, N: int, d_v: int, W: int, R:
 
 @_on_tensor_device
 def scan_backward(idx_w, sc_w, idx_r, sc_r, v, alpha, beta, w_prev, r_rows, dO, G, shared_M0: bool = True,
-                  workspace=None, final_zero: bool = False):
+                  workspace=None, final_zero: bool = False, dm0_only: bool = False):
     """Reverse-mode pass of the scan for L = sum_t <dO_t, o_t> + <dM_T, M_T>, slots fixed.
     G: fp32 [B,H,N,d_v], in dL/dM_T, out dL/dM_0 per (b, h) (in place).  final_zero: dM_T
     is zero and G's entry contents are ignored (it need not be cleared; the pass skips the
-    adjoint rows it knows to be zero).  Returns dict(dv, dalpha, dbeta, dsc_w, dsc_r, dM0)
-    with dM0 = sum of G over the batch (shared_M0) or None."""
+    adjoint rows it knows to be zero).  dm0_only (with final_zero and shared_M0): only the
+    batch's dM0 is wanted, so the rows of G no slot reads are not zeroed (G unspecified on
+    exit).  Returns dict(dv, dalpha, dbeta, dsc_w, dsc_r, dM0) with dM0 = sum of G over the
+    batch (shared_M0) or None."""
     _need(G, "G", torch.float32)
     B, H, N, dv = G.shape
     T, W, R = idx_w.shape[2], idx_w.shape[3], idx_r.shape[3]
@@ -534,7 +537,8 @@ def scan_backward(idx_w, sc_w, idx_r, sc_r, v, alpha, beta, w_prev, r_rows, dO, 
     _call("sdm_scan_backward_ex", _p(idx_w), _p(sc_w), _p(idx_r), _p(sc_r), _p(v), _dtype_code(v), _p(alpha),
           _p(beta), _p(w_prev), _p(r_rows), _p(dO), B, H, T, N, dv, W, R, _p(G), _p(out["dv"]), _p(out["dalpha"]),
           _p(out["dbeta"]), _p(out["dsc_w"]), _p(out["dsc_r"]), _p(out["dM0"]),
-          BWD_FINAL_ZERO if final_zero else 0, _p(workspace), workspace.numel(), _stream(dev))
+          (BWD_FINAL_ZERO if final_zero else 0) | (BWD_DM0_ONLY if dm0_only else 0), _p(workspace),
+          workspace.numel(), _stream(dev))
     return out
 
 

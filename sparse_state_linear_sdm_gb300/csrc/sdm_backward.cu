@@ -466,7 +466,8 @@ __global__ void __launch_bounds__(128) backward_finish_kernel(
 __global__ void __launch_bounds__(256) reduce_batch_zero_kernel(float4* __restrict__ G,
                                                                 float4* __restrict__ dM0,
                                                                 const int32_t* __restrict__ last,
-                                                                int B, long long rows, int dv4) {
+                                                                int B, long long rows, int dv4,
+                                                                bool write_zeros) {
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
   const int lane = threadIdx.x & 31;
   const long long groups = (rows + 31) / 32;
@@ -495,7 +496,7 @@ __global__ void __launch_bounds__(256) reduce_batch_zero_kernel(float4* __restri
         for (int k = 0; k < 8; ++k) {
           const int b = b0 + k;
           if (b < B) {
-            if (!((m >> b) & 1u)) __stcs(G + (size_t(b) * size_t(rows) + row) * dv4 + c, u[k]);
+            if (write_zeros && !((m >> b) & 1u)) __stcs(G + (size_t(b) * size_t(rows) + row) * dv4 + c, u[k]);
             s = b == 0 ? u[k] : make_float4(s.x + u[k].x, s.y + u[k].y, s.z + u[k].z, s.w + u[k].w);
           }
         }
@@ -509,7 +510,8 @@ __global__ void __launch_bounds__(256) reduce_batch_zero_kernel(float4* __restri
 __global__ void __launch_bounds__(256) reduce_batch_zero_wide_kernel(float4* __restrict__ G,
                                                                      float4* __restrict__ dM0,
                                                                      const int32_t* __restrict__ last,
-                                                                     int B, long long rows, int dv4) {
+                                                                     int B, long long rows, int dv4,
+                                                                     bool write_zeros) {
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
   const int lane = threadIdx.x & 31;
   for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
@@ -521,7 +523,7 @@ __global__ void __launch_bounds__(256) reduce_batch_zero_wide_kernel(float4* __r
         float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
         if (last[rb] >= 0)
           u = G[rb * dv4 + c];
-        else
+        else if (write_zeros)
           __stcs(G + rb * dv4 + c, u);
         s = b == 0 ? u : make_float4(s.x + u.x, s.y + u.y, s.z + u.z, s.w + u.w);
       }
@@ -621,7 +623,7 @@ size_t sdm_scan_backward_workspace_size(int B, int H, int T, int d_v, int W, int
 
 size_t sdm_scan_backward_workspace_size_ex(int B, int H, int T, long long N, int d_v, int W, int R,
                                            unsigned flags) {
-  if (flags & ~unsigned(SDM_BWD_FINAL_ZERO)) return 0;
+  if (flags & ~unsigned(SDM_BWD_FINAL_ZERO | SDM_BWD_DM0_ONLY)) return 0;
   BwdWorkspace ws;
   return backward_workspace(B, H, T, N, d_v, W, R, flags, &ws) ? ws.total : 0;
 }
@@ -666,8 +668,10 @@ int sdm_scan_backward_ex(const int32_t* idx_w, const float* sc_w, const int32_t*
                          float* G, float* dv, float* dalpha, float* dbeta, float* dsc_w,
                          float* dsc_r, float* dM0, unsigned flags, void* workspace,
                          size_t workspace_bytes, void* stream) {
-  if (flags & ~unsigned(SDM_BWD_FINAL_ZERO)) return SDM_EINVAL;
+  if (flags & ~unsigned(SDM_BWD_FINAL_ZERO | SDM_BWD_DM0_ONLY)) return SDM_EINVAL;
   const bool zero_final = (flags & SDM_BWD_FINAL_ZERO) != 0;
+  const bool dm0_only = (flags & SDM_BWD_DM0_ONLY) != 0;
+  if (dm0_only && !dM0) return SDM_EINVAL;
   int st = check_scan_args(G, idx_w, sc_w, idx_r, sc_r, v, v_dt, alpha, beta, B, H, T, N, d_v, W,
                            R, dv);
   if (st != SDM_OK) return st;
@@ -770,11 +774,11 @@ int sdm_scan_backward_ex(const int32_t* idx_w, const float* sc_w, const int32_t*
     if (B <= 32)
       reduce_batch_zero_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<float4*>(G),
                                                        reinterpret_cast<float4*>(dM0), last, B, rows,
-                                                       d_v / 4);
+                                                       d_v / 4, !dm0_only);
     else
       reduce_batch_zero_wide_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<float4*>(G),
                                                             reinterpret_cast<float4*>(dM0), last, B,
-                                                            rows, d_v / 4);
+                                                            rows, d_v / 4, !dm0_only);
     return last_launch_status();
   }
   if (dM0) {

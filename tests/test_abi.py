@@ -242,15 +242,20 @@ def test_backward_flags_and_workspace_sizes():
     assert lib.sdm_scan_backward_workspace_size_ex(B, H, T, N, dv, W, R, 1) == base + up16(B * H * N * 4)
     assert lib.sdm_scan_backward_workspace_size_ex(1, 1, 5, 64, 8, 40, 33, 1) == (
         up16(5 * 1 * 113 * 4) + up16(5 * 73 * 4) + up16(5 * 8 * 4) + up16(64 * 4))   # W + R = 73: 3 + 2 words
-    assert lib.sdm_scan_backward_workspace_size_ex(B, H, T, N, dv, W, R, 2) == 0
+    assert lib.sdm_scan_backward_workspace_size_ex(B, H, T, N, dv, W, R, 2) == base      # dM0 only: no table
+    assert lib.sdm_scan_backward_workspace_size_ex(B, H, T, N, dv, W, R, 3) == base + up16(B * H * N * 4)
+    assert lib.sdm_scan_backward_workspace_size_ex(B, H, T, N, dv, W, R, 4) == 0         # unknown bit
     assert lib.sdm_scan_backward_workspace_size_ex(B, H, 0, N, dv, W, R, 1) == up16(B * H * N * 4)
 
-    def call(flags=1, ws=FAKE, ws_bytes=1 << 30, dv_=dv, G=FAKE):
+    def call(flags=1, ws=FAKE, ws_bytes=1 << 30, dv_=dv, G=FAKE, dM0=None):
         return lib.sdm_scan_backward_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE, B, H, T, N,
-                                        dv_, W, R, G, FAKE, FAKE, FAKE, FAKE, FAKE, None, flags, ws, ws_bytes, None)
+                                        dv_, W, R, G, FAKE, FAKE, FAKE, FAKE, FAKE, dM0, flags, ws, ws_bytes, None)
 
-    assert call(flags=2) == EINVAL
+    assert call(flags=2) == EINVAL              # dM0 only without a dM0
     assert call(flags=3) == EINVAL
+    assert call(flags=4) == EINVAL              # unknown bit
+    assert call(flags=5, dM0=FAKE) == EINVAL
+    assert call(flags=3, dM0=FAKE, ws_bytes=base) == ENOSPACE
     assert call(dv_=6) == EINVAL
     assert call(ws=ODD) == EALIGN
     assert call(G=ODD) == EALIGN

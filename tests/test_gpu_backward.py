@@ -161,6 +161,17 @@ def test_final_zero_equals_the_cleared_adjoint(B, H, T, S, dv, W, R, vdt):
         for name in OUTPUTS:
             assert torch.equal(got[name], ref[name]), (rep, name)
         assert torch.equal(G, G_ref), rep
+    # dM0 only: the same outputs; rows of G no slot reads stay as they were (NaN here), and
+    # those are exactly the rows whose gradient is zero
+    G = torch.full((B, H, N, dv), float("nan"), device="cuda")
+    got = sdm.scan_backward(*sel, dev["v"], dev["alpha"], dev["beta"], w_prev, r_rows, dO_d, G, workspace=ws,
+                            final_zero=True, dm0_only=True)
+    torch.cuda.synchronize()
+    for name in OUTPUTS:
+        assert torch.equal(got[name], ref[name]), ("dm0_only", name)
+    left = torch.isnan(G)
+    assert torch.equal(G[~left], G_ref[~left])
+    assert bool((G_ref[left] == 0).all())
 
 
 def test_final_zero_with_no_tokens_clears_the_adjoint():
