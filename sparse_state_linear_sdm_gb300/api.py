@@ -8,6 +8,7 @@ from __future__ import annotations
 
 import ctypes
 import functools
+import math
 import os
 import threading
 
@@ -466,7 +467,7 @@ def copy_token_window(dst, src, t0: int, t1: int, stream=None):
         if not t.is_cuda and not t.is_pinned():
             raise ValueError("host tensors must be pinned")
     dev = dst.device if dst.is_cuda else src.device
-    tok = dst.element_size() * (dst[0, 0, 0].numel() if dst.shape[2] > 0 else 0)
+    tok = dst.element_size() * math.prod(dst.shape[3:])  # bytes of one token of one (b, h)
     pitch = tok * dst.shape[2]
     off = tok * t0
     s = torch.cuda.current_stream(dev) if stream is None else stream
