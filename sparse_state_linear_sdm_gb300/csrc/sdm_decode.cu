@@ -40,6 +40,7 @@ struct DecodeArgs {
   int bufs;   // row buffers per group of 256 threads (1 or 2)
   size_t sel_smem;  // bytes of the selection's shared memory
   int* dev_err;
+  int parts;  // blocks per (b, h): each repeats the selection and takes its share of the slices
 };
 
 // Shared memory of the planning and scan parts for NG groups of 256 threads with NB row
@@ -295,7 +296,7 @@ __device__ __forceinline__ TeamMem team_mem(unsigned char* base, int S, int kin_
 // (team thread t); barriers bar0 (the team), bar0 + 1 and bar0 + 2 (its two halves).
 template <typename Tin, int EMAX, int TT>
 __device__ void team_select(const SelectArgs& a, long long item, int which, const uint32_t* stair,
-                            const TeamMem& m, int t, int bar0) {
+                            const TeamMem& m, int t, int bar0, bool write_out = true) {
   using IKey = typename InnerKeyOf<Tin>::type;
   constexpr int IBITS = sizeof(Tin) == 2 ? 32 : 48;
   const int S = a.S, K = which ? a.R : a.W, kin = min(K, S);
@@ -403,8 +404,10 @@ __device__ void team_select(const SelectArgs& a, long long item, int which, cons
     const uint64_t k = m.oout[r];
     const int32_t slot = int32_t(0xFFFFFFFFu - uint32_t(k & 0xFFFFFFFFu));
     const float sc = ord_decode(uint32_t(k >> 32));
-    oi[r] = slot;
-    os[r] = sc;
+    if (write_out) {
+      oi[r] = slot;
+      os[r] = sc;
+    }
     m.ridx[r] = slot;
     m.rsc[r] = sc;
   }
@@ -417,7 +420,10 @@ __global__ void __launch_bounds__(TEAM ? 512 : 256, 1) decode_kernel(DecodeArgs 
   extern __shared__ __align__(16) unsigned char smem[];
   const SelectArgs& a = d.sel;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x;
+  // d.parts blocks per (b, h) (the team path only): each selects and plans the token, part 0
+  // writes the selection's outputs, and part p scans slices p*NG .. p*NG+NG-1, then every
+  // parts*NG-th one after them.
+  const int bh = blockIdx.x / d.parts, part = blockIdx.x - bh * d.parts;
   const int C = d.cols, LPR = C / 4, RPP = 256 / LPR;
   const int W = d.W, R = d.R, WR = W + R, d_v = d.d_v;
 
@@ -440,7 +446,7 @@ __global__ void __launch_bounds__(TEAM ? 512 : 256, 1) decode_kernel(DecodeArgs 
     build_stairs_parallel(stair_w, stair_r, a.W, a.R, a.S, reinterpret_cast<int*>(m0.hist), NT);
     const int team = warp >> 3;
     team_select<Tin, EMAX, 256>(a, bh, team, team ? stair_r : stair_w, team ? m1 : m0, tid & 255,
-                                1 + 3 * team);
+                                1 + 3 * team, part == 0);
     // the slots and scores stay in shared memory; the scan's buffers follow them
     gw = m0.ridx;
     sw = m0.rsc;
@@ -525,13 +531,14 @@ __global__ void __launch_bounds__(TEAM ? 512 : 256, 1) decode_kernel(DecodeArgs 
       if (src[e] == -1) cp16(rg + e * C + 4 * c4, Mc + size_t(idx[e]) * d_v + 4 * c4);
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
-  if (gi < d.slices) gather(gi, rows + size_t(gi * NB) * WR * C);
-  for (int sl = gi, k = 0; sl < d.slices; sl += NG, ++k) {
+  const int sl0 = part * NG + gi, sstep = d.parts * NG;
+  if (sl0 < d.slices) gather(sl0, rows + size_t(gi * NB) * WR * C);
+  for (int sl = sl0, k = 0; sl < d.slices; sl += sstep, ++k) {
     const int c0 = sl * C;
     float* Mc = Mbh + c0;
     float* rg = rows + size_t(gi * NB + (k % NB)) * WR * C;
-    const bool ahead = NB > 1 && sl + NG < d.slices;
-    if (ahead) gather(sl + NG, rows + size_t(gi * NB + ((k + 1) % NB)) * WR * C);
+    const bool ahead = NB > 1 && sl + sstep < d.slices;
+    if (ahead) gather(sl + sstep, rows + size_t(gi * NB + ((k + 1) % NB)) * WR * C);
     if (ahead)
       asm volatile("cp.async.wait_group 1;" ::: "memory");
     else
@@ -587,9 +594,9 @@ __global__ void __launch_bounds__(TEAM ? 512 : 256, 1) decode_kernel(DecodeArgs 
       }
       *(reinterpret_cast<float4*>(d.o + size_t(bh) * d_v + c0) + lt) = sum;
     }
-    if (NB == 1 && sl + NG < d.slices) {
+    if (NB == 1 && sl + sstep < d.slices) {
       team_bar(gbar, 256);  // every read of this slice's rows is done
-      gather(sl + NG, rg);
+      gather(sl + sstep, rg);
     } else if (NB > 1) {
       team_bar(gbar, 256);  // the buffer is gathered into again two slices later
     }
@@ -667,6 +674,13 @@ int launch_decode_t(const void* kp, const void* qp, const void* v, int v_dt, con
   dargs.slices = d_v / cols;
   dargs.bufs = bufs;
   dargs.dev_err = dev_err;
+  // Two blocks per (b, h) when the slices take more than one round of the block's groups and
+  // both blocks still find an SM of their own: the selection is repeated, the rounds halve.
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SDM_ECUDA;
+  dargs.parts = team && dargs.slices > 2 && 2LL * BH <= sms ? 2 : 1;
   const bool big = W > 128 || R > 128;
   const void* fn;
   if (v_dt == SDM_BF16)
@@ -681,7 +695,8 @@ int launch_decode_t(const void* kp, const void* qp, const void* v, int v_dt, con
       cudaSuccess)
     return SDM_ECUDA;
   void* args[] = {&dargs};
-  if (cudaLaunchKernel(fn, dim3(unsigned(BH)), dim3(team ? 512 : 256), args, smem, s) != cudaSuccess)
+  if (cudaLaunchKernel(fn, dim3(unsigned(BH * dargs.parts)), dim3(team ? 512 : 256), args, smem, s) !=
+      cudaSuccess)
     return SDM_ECUDA;
   return last_launch_status();
 }
