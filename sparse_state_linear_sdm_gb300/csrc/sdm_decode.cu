@@ -41,7 +41,22 @@ struct DecodeArgs {
   size_t sel_smem;  // bytes of the selection's shared memory
   int* dev_err;
   int parts;  // blocks per (b, h): each repeats the selection and takes its share of the slices
+  int pair;   // 1: the two blocks of a (b, h) form a cluster, block r selects task r (k', q')
+              // with all its threads and the two exchange their slots and scores
 };
+
+// The blocks of a cluster meet (every thread of both; their shared memory writes before are
+// visible to the other block after).
+__device__ __forceinline__ void decode_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// A word of the other block's shared memory, at the address this block's copy has.
+__device__ __forceinline__ uint32_t decode_peer_load(const void* local, uint32_t peer) {
+  uint32_t addr = static_cast<uint32_t>(__cvta_generic_to_shared(local)), remote, v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(peer));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+  return v;
+}
 
 // Shared memory of the planning and scan parts for NG groups of 256 threads with NB row
 // buffers each.
@@ -444,14 +459,31 @@ __global__ void __launch_bounds__(TEAM ? 512 : 256, 1) decode_kernel(DecodeArgs 
     const TeamMem m1 = team_mem(tbase + tsize, a.S, a.kin_max, a.kpad, cmax, ikb);
     // team 0's histograms are free until its selection starts: scratch for the staircases
     build_stairs_parallel(stair_w, stair_r, a.W, a.R, a.S, reinterpret_cast<int*>(m0.hist), NT);
-    const int team = warp >> 3;
-    team_select<Tin, EMAX, 256>(a, bh, team, team ? stair_r : stair_w, team ? m1 : m0, tid & 255,
-                                1 + 3 * team, part == 0);
-    // the slots and scores stay in shared memory; the scan's buffers follow them
-    gw = m0.ridx;
-    sw = m0.rsc;
-    gr = m1.ridx;
-    sr = m1.rsc;
+    if (d.pair) {
+      // Block `part` of the cluster takes task `part` (0: k', 1: q') with every thread; the
+      // other task's slots and scores are then copied from the other block into m1.
+      team_select<Tin, EMAX, NT>(a, bh, part, part ? stair_r : stair_w, m0, tid, 1, true);
+      decode_cluster_sync();  // both tasks' results are in place
+      const int Kp = part ? W : R;  // the other task's slot count
+      for (int i = tid; i < Kp; i += NT) {
+        m1.ridx[i] = int32_t(decode_peer_load(m0.ridx + i, uint32_t(part ^ 1)));
+        m1.rsc[i] = __uint_as_float(decode_peer_load(m0.rsc + i, uint32_t(part ^ 1)));
+      }
+      decode_cluster_sync();  // neither block's results are read by the other after this
+      gw = part ? m1.ridx : m0.ridx;
+      sw = part ? m1.rsc : m0.rsc;
+      gr = part ? m0.ridx : m1.ridx;
+      sr = part ? m0.rsc : m1.rsc;
+    } else {
+      const int team = warp >> 3;
+      team_select<Tin, EMAX, 256>(a, bh, team, team ? stair_r : stair_w, team ? m1 : m0,
+                                  tid & 255, 1 + 3 * team, part == 0);
+      // the slots and scores stay in shared memory; the scan's buffers follow them
+      gw = m0.ridx;
+      sw = m0.rsc;
+      gr = m1.ridx;
+      sr = m1.rsc;
+    }
     sbase = smem + d.sel_smem;
   } else {  // the selection kernel's pair mode: warps 0-1 the k' task, 2-3 the q' task
     const SelectSmem m = select_smem(a, smem);
@@ -680,7 +712,8 @@ int launch_decode_t(const void* kp, const void* qp, const void* v, int v_dt, con
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return SDM_ECUDA;
-  dargs.parts = team && dargs.slices > 2 && 2LL * BH <= sms ? 2 : 1;
+  dargs.pair = team && 2LL * BH <= sms ? 1 : 0;
+  dargs.parts = dargs.pair || (team && dargs.slices > 2 && 2LL * BH <= sms) ? 2 : 1;
   const bool big = W > 128 || R > 128;
   const void* fn;
   if (v_dt == SDM_BF16)
@@ -695,9 +728,19 @@ int launch_decode_t(const void* kp, const void* qp, const void* v, int v_dt, con
       cudaSuccess)
     return SDM_ECUDA;
   void* args[] = {&dargs};
-  if (cudaLaunchKernel(fn, dim3(unsigned(BH * dargs.parts)), dim3(team ? 512 : 256), args, smem, s) !=
-      cudaSuccess)
-    return SDM_ECUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(BH * dargs.parts));
+  cfg.blockDim = dim3(team ? 512 : 256);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(dargs.pair ? 2 : 1);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return SDM_ECUDA;
   return last_launch_status();
 }
 
