@@ -565,12 +565,13 @@ def e2e(st, cfg, sdm, args, dev, torch, K, world):
     chunk's selection waits only for its own window (sdm_forward_streamed), so the first
     step starts on its first window instead of the whole batch."""
     names = ("kp", "qp", "v", "alpha", "beta")
-    host = {k: torch.empty(st[k].shape, dtype=st[k].dtype, pin_memory=True) for k in names}
+    # page-locked host buffers on huge pages (sdm.pinned_empty), as a serving loop would keep them
+    host = {k: sdm.pinned_empty(st[k].shape, st[k].dtype, dev) for k in names}
     for k in names:
         host[k].copy_(st[k])
     bufs = [{k: st[k] for k in names}, {k: torch.empty_like(st[k]) for k in names}]
     outs = [st["o"], torch.empty_like(st["o"])]
-    o_host = [torch.empty(st["o"].shape, dtype=torch.float32, pin_memory=True) for _ in range(2)]
+    o_host = [sdm.pinned_empty(st["o"].shape, torch.float32, dev) for _ in range(2)]
     h2d = sum(host[k].numel() * host[k].element_size() for k in names)
     d2h = o_host[0].numel() * 4
     copy = torch.cuda.Stream(device=dev)

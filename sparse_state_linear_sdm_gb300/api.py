@@ -450,6 +450,54 @@ def forward(kp, qp, v, alpha, beta, M0, W: int, R: int, M=None, workspace=None, 
     return o, M, out
 
 
+_HUGE = 1 << 21  # transparent huge page size asked for (the register call takes any size)
+
+
+def pinned_empty(shape, dtype, device=None) -> torch.Tensor:
+    """Page-locked host memory for staging copies to and from the GPU (copy_token_window,
+    Tensor.copy_).  The pages are asked for as transparent huge pages where the OS allows,
+    then registered with CUDA: the copy engines then need few address translations, which
+    keeps host-device copies at full rate while the GPU is busy even when the host's memory is
+    fragmented (small pinned pages there slowed a streamed loop's copies several-fold).  Falls
+    back to torch's pinned allocator where that is not possible.  The registration and the
+    mapping go with the last reference to the buffer."""
+    import mmap
+    import weakref
+
+    import numpy as np
+
+    shape = tuple(int(x) for x in shape)
+    nbytes = int(np.prod(shape, dtype=np.int64)) * torch.empty((), dtype=dtype).element_size()
+    madv = getattr(mmap, "MADV_HUGEPAGE", None)
+    if nbytes == 0 or madv is None or not hasattr(mmap, "MAP_ANONYMOUS"):
+        return torch.empty(shape, dtype=dtype, pin_memory=True)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    size = (nbytes + _HUGE - 1) // _HUGE * _HUGE + _HUGE  # room to start on a huge-page boundary
+    mm = mmap.mmap(-1, size, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+    try:
+        mm.madvise(madv)
+    except OSError:
+        pass
+    raw = np.frombuffer(mm, dtype=np.uint8)
+    skip = (-raw.ctypes.data) % _HUGE
+    buf = raw[skip:skip + nbytes]
+    buf[:] = 0  # fault the pages in before they are locked
+    with torch.cuda.device(dev):
+        rc = int(torch.cuda.cudart().cudaHostRegister(buf.ctypes.data, nbytes, 0))
+    if rc != 0:
+        del buf, raw
+        mm.close()
+        return torch.empty(shape, dtype=dtype, pin_memory=True)
+    ptr = buf.ctypes.data
+
+    def release(ptr=ptr, mm=mm, dev=dev):
+        with torch.cuda.device(dev):
+            torch.cuda.cudart().cudaHostUnregister(ptr)
+
+    weakref.finalize(buf, release)  # buf lives as long as the tensor's storage
+    return torch.from_numpy(buf).view(dtype).view(shape)
+
+
 def copy_token_window(dst, src, t0: int, t1: int, stream=None):
     """Copy tokens t0 .. t1-1 of every (b, h) from src to dst, both [B, H, T, ...] contiguous
     with the same shape and dtype, one on the GPU and the other pinned host memory (or both on

@@ -148,6 +148,20 @@ def test_copy_token_window_moves_exactly_its_tokens():
         assert torch.equal(back[:, :, 30:77], host[k][:, :, 30:77]), k
 
 
+def test_pinned_empty_is_page_locked_and_round_trips():
+    x = torch.randn(3, 5, 77, 9, device="cuda")
+    h = sdm.pinned_empty(x.shape, x.dtype)
+    assert h.is_pinned() and h.shape == x.shape and h.dtype == x.dtype
+    h.copy_(x, non_blocking=True)
+    y = torch.empty_like(x)
+    y.copy_(h, non_blocking=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y, x)
+    b = sdm.pinned_empty((4, 2, 10, 2, 8), torch.bfloat16)
+    assert b.is_pinned() and b.dtype == torch.bfloat16
+    del h, b  # the registration goes with the buffers
+
+
 @pytest.mark.parametrize("chunks", [3, 4])
 def test_inputs_arriving_window_by_window(chunks):
     """The batch's inputs copied from pinned host memory one token window at a time on a
@@ -157,7 +171,9 @@ def test_inputs_arriving_window_by_window(chunks):
     d = device_inputs(cfg)
     M0 = device_M0(cfg)
     ref = _run(d, M0, cfg.W, cfg.R, chunks=chunks)
-    host = {k: d[k].cpu().pin_memory() for k in NAMES}
+    host = {k: sdm.pinned_empty(d[k].shape, d[k].dtype) for k in NAMES}
+    for k in NAMES:
+        host[k].copy_(d[k])
     dst = {k: torch.full_like(d[k], float("nan")) for k in NAMES}
     torch.cuda.synchronize()
     n = sdm.forward_chunks(cfg.T, chunks)
