@@ -494,7 +494,8 @@ def pinned_empty(shape, dtype, device=None) -> torch.Tensor:
         with torch.cuda.device(dev):
             torch.cuda.cudart().cudaHostUnregister(ptr)
 
-    weakref.finalize(buf, release)  # buf lives as long as the tensor's storage
+    fin = weakref.finalize(buf, release)  # buf lives as long as the tensor's storage
+    fin.atexit = False  # at interpreter exit the process teardown releases it
     return torch.from_numpy(buf).view(dtype).view(shape)
 
 
