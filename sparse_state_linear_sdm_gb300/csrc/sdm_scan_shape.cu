@@ -31,7 +31,8 @@ int choose_scan_shape(int BH, int d_v, int W, int R, int force_cols, int force_p
     // (pd 1: 18.8 ms, pd 2: 19.1 ms on B16 H4 T8192 N=2^20 d_v=128 W=R=128) and for short
     // tokens (B4 H8 W=R=32, 128 blocks: 1.75 against 1.86 ms); with fewer blocks than SMs
     // and many rows per token each block's gathers set the pace, and two tokens in flight
-    // measured faster (B1 H4 N=2^20 W=R=128, 128 blocks: 0.93 against 0.99 us per token).
+    // measured faster (B1 H4 N=2^20 W=R=128, 128 blocks of 4 columns: 0.86 us per token
+    // against 0.95 with one token and 0.93 with three; 8 columns 0.94-0.98, 16 columns 1.31).
     const int pd0 = (long long)BH * (d_v / c) < sms && W + R >= 128 ? 2 : 1;
     const int pds[2] = {pd0, 3 - pd0};
     for (int k = 0; k < 2 && !best_cols; ++k) {
