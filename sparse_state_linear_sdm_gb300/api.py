@@ -460,7 +460,8 @@ def pinned_empty(shape, dtype, device=None) -> torch.Tensor:
     keeps host-device copies at full rate while the GPU is busy even when the host's memory is
     fragmented (small pinned pages there slowed a streamed loop's copies several-fold).  Falls
     back to torch's pinned allocator where that is not possible.  The registration and the
-    mapping go with the last reference to the buffer."""
+    mapping go with the last reference to the buffer (after the device has finished its
+    work, so a copy still in flight never meets unlocked pages)."""
     import mmap
     import weakref
 
@@ -492,6 +493,8 @@ def pinned_empty(shape, dtype, device=None) -> torch.Tensor:
 
     def release(ptr=ptr, mm=mm, dev=dev):
         with torch.cuda.device(dev):
+            # copies still in flight from or to these pages finish before they are unlocked
+            torch.cuda.synchronize(dev)
             torch.cuda.cudart().cudaHostUnregister(ptr)
 
     fin = weakref.finalize(buf, release)  # buf lives as long as the tensor's storage
