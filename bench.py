@@ -856,7 +856,8 @@ def run_decode(args):
     sel_g = [torch.empty_like(x) for x in step.sel]
     o_g = torch.empty_like(step.o)
     chain = lambda: [sdm.decode_step(toks["kp"][g], toks["qp"][g], toks["v"][g], toks["alpha"][g],
-                                     toks["beta"][g], st["M"], cfg.W, cfg.R, out=sel_g, o=o_g)
+                                     toks["beta"][g], st["M"], cfg.W, cfg.R, out=sel_g, o=o_g,
+                                     table=step.table)
                      for g in range(G)] if step.fused else None
     ms_device = None
     if step.fused:

@@ -350,6 +350,25 @@ int sdm_decode_step(const void* kp, const void* qp, int in_dt, const void* v, in
                     float* o, int* dev_err, void* stream);
 int sdm_decode_step_supported(int in_dt, int B, int H, int S, int d_v, int W, int R);
 
+/* The staircase table of a decode step: for the write task and then the read task, the pairs
+ * (p, q) of ranks in the two sorted inner top-k lists whose rank product (p+1)(q+1) is at most
+ * K (W or R), the only pairs that can hold one of the K largest sums ("Meccanismo Core" item
+ * 2).  It depends on W, R and S alone, so a caller stepping one shape token after token builds
+ * it once and passes it to every step instead of each step's blocks building it.
+ * sdm_decode_table_words - its size in 32-bit words (-1 for sizes sdm_decode_step rejects).
+ * sdm_decode_table - writes it into `table` (caller-owned device memory of at least that many
+ *   words, 4-byte aligned) on `stream`.  SDM_EINVAL for a null table or rejected sizes.
+ * sdm_decode_step_tabled - sdm_decode_step whose blocks read the staircases from `table` (as
+ *   written by sdm_decode_table for the same W, R and S, and not written while the step runs;
+ *   NULL: the blocks build them, as sdm_decode_step does).  The same bits either way. */
+int sdm_decode_table_words(int W, int R, int S);
+int sdm_decode_table(uint32_t* table, int W, int R, int S, void* stream);
+int sdm_decode_step_tabled(const void* kp, const void* qp, int in_dt, const void* v, int v_dt,
+                           const float* alpha, const float* beta, float* M, int B, int H, int S,
+                           int d_v, int W, int R, int32_t* idx_w, float* sc_w, int32_t* idx_r,
+                           float* sc_r, float* o, int* dev_err, const uint32_t* table,
+                           void* stream);
+
 /* sdm_project_kq - the projections that produce the product keys and queries
  * ("Meccanismo Core" item 2: the projected key k' and query q', whose two halves are the
  * sub-scores; "Design IsoFLOP": the projections are linear layers).  One bf16 GEMM on the

@@ -75,6 +75,9 @@ def lib() -> ctypes.CDLL:
             L.sdm_select_backward.argtypes = [p, p, i, i, i, i, i, p, p]
             L.sdm_decode_step.argtypes = [p, p, i, p, i, p, p, p, i, i, i, i, i, i, p, p, p, p, p, p, p]
             L.sdm_decode_step_supported.argtypes = [i, i, i, i, i, i, i]
+            L.sdm_decode_table_words.argtypes = [i, i, i]
+            L.sdm_decode_table.argtypes = [p, i, i, i, p]
+            L.sdm_decode_step_tabled.argtypes = [p, p, i, p, i, p, p, p, i, i, i, i, i, i, p, p, p, p, p, p, p, p]
             L.sdm_project_kq_tuned.argtypes = [p, p, i, i, i, i, i, p, p, p, i, i, p]
             L.sdm_test_bounded_wait.argtypes = [i, ull, p, p, p]
             L.sdm_test_project_stall.argtypes = [p, p, i, i, i, i, i, p, p, i, i, i, ull, p, p]
@@ -86,7 +89,8 @@ def lib() -> ctypes.CDLL:
                          "sdm_scan_forward_tuned", "sdm_scan_launch_info", "sdm_gen_inputs", "sdm_gen_M0",
                          "sdm_forward_chunks", "sdm_forward_tuned", "sdm_forward", "sdm_scan_forward_train",
                          "sdm_scan_backward", "sdm_scan_backward_ex", "sdm_select_backward", "sdm_project_select",
-                         "sdm_fill_state", "sdm_test_project_stall"):
+                         "sdm_fill_state", "sdm_test_project_stall", "sdm_decode_table_words",
+                         "sdm_decode_table", "sdm_decode_step_tabled"):
                 getattr(L, name).restype = i
             _lib = L
     return _lib
@@ -702,12 +706,26 @@ def project_stall_check(x, w, H: int, S: int, pair: int, stall_cta: int, stall_s
     return int(dev_err.item())
 
 
+def decode_table(W: int, R: int, S: int, device="cuda") -> torch.Tensor:
+    """The staircase table of a (W, R, S) decode step (int32 words on `device`), built once
+    by sdm_decode_table; decode_step(table=...) then reads it instead of building it."""
+    n = lib().sdm_decode_table_words(W, R, S)
+    if n < 0:
+        raise ValueError("sizes not supported by the decode step")
+    dev = torch.device(device)
+    t = torch.empty(n, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _call("sdm_decode_table", _p(t), W, R, S, _stream(dev))
+    return t
+
+
 @_on_tensor_device
-def decode_step(kp, qp, v, alpha, beta, M, W: int, R: int, out=None, o=None, dev_err=None):
+def decode_step(kp, qp, v, alpha, beta, M, W: int, R: int, out=None, o=None, dev_err=None, table=None):
     """One decode token (T = 1) for every (b, h) in a single kernel: selection, planning and
     the gated write and read on M (in place).  kp, qp [B, H, 1, 2, S]; v [B, H, 1, d_v];
     alpha, beta [B, H, 1]; M [B, H, S*S, d_v] fp32.  Returns (o, (idx_w, sc_w, idx_r, sc_r)),
-    bit-identical to select() followed by scan_forward() on the same token."""
+    bit-identical to select() followed by scan_forward() on the same token.  table: the
+    step's staircase table from decode_table(W, R, S) (optional; the same bits)."""
     _need(kp, "kp")
     B, H, T, two, S = kp.shape
     if T != 1 or two != 2:
@@ -725,9 +743,13 @@ def decode_step(kp, qp, v, alpha, beta, M, W: int, R: int, out=None, o=None, dev
     if o is None:
         o = torch.empty((B, H, 1, dv), dtype=torch.float32, device=M.device)
     _need(o, "o", torch.float32, (B, H, 1, dv))
-    _call("sdm_decode_step", _p(kp), _p(qp), _dtype_code(kp), _p(v), _dtype_code(v), _p(alpha), _p(beta),
-          _p(M), B, H, S, dv, W, R, _p(out[0]), _p(out[1]), _p(out[2]), _p(out[3]), _p(o),
-          _p(dev_err) if dev_err is not None else None, _stream(M.device))
+    if table is not None:
+        n = lib().sdm_decode_table_words(W, R, S)
+        _need(table, "table", torch.int32, (n,))
+    _call("sdm_decode_step_tabled", _p(kp), _p(qp), _dtype_code(kp), _p(v), _dtype_code(v), _p(alpha),
+          _p(beta), _p(M), B, H, S, dv, W, R, _p(out[0]), _p(out[1]), _p(out[2]), _p(out[3]), _p(o),
+          _p(dev_err) if dev_err is not None else None, _p(table) if table is not None else None,
+          _stream(M.device))
     return o, out
 
 
@@ -768,19 +790,21 @@ class DecodeStep:
         self.o = torch.empty((B, H, 1, dv), dtype=torch.float32, device=dev)
         self.ws = scan_workspace(B, H, 1, dv, W, R, dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        # the staircase table of this shape, built once for every step
+        self.table = decode_table(W, R, S, dev) if self.fused else None
         self.graph = None
         # Fixed arguments of the single-kernel launch on the caller's tensors (plain integer
         # addresses: ctypes converts them for the c_void_p parameters).
-        self._fn = lib().sdm_decode_step
+        self._fn = lib().sdm_decode_step_tabled
         self._codes = (_dtype_code(self.kp), _dtype_code(self.v))
         self._tail = (M.data_ptr(), B, H, S, dv, W, R) + tuple(t.data_ptr() for t in self.sel) + (
-            self.o.data_ptr(), self.err.data_ptr())
+            self.o.data_ptr(), self.err.data_ptr(), self.table.data_ptr() if self.fused else None)
         self._bufs = (self.kp, self.qp, self.v, self.alpha, self.beta)
 
     def _body(self):
         if self.fused:
             decode_step(self.kp, self.qp, self.v, self.alpha, self.beta, self.M, self.W, self.R,
-                        out=self.sel, o=self.o, dev_err=self.err)
+                        out=self.sel, o=self.o, dev_err=self.err, table=self.table)
             return
         select(self.kp, self.qp, self.W, self.R, out=self.sel)
         scan_forward(self.M, *self.sel, self.v, self.alpha, self.beta, o=self.o, workspace=self.ws,
@@ -843,7 +867,7 @@ class DecodeStep:
                       alpha.data_ptr(), beta.data_ptr(), *self._tail,
                       torch.cuda.current_stream(dev).cuda_stream)
         if st != 0:
-            raise SDMError("sdm_decode_step", st)
+            raise SDMError("sdm_decode_step_tabled", st)
         return True
 
     def __call__(self, kp, qp, v, alpha, beta):

@@ -60,6 +60,28 @@ int sdm_decode_step(const void* kp, const void* qp, int in_dt, const void* v, in
                     const float* alpha, const float* beta, float* M, int B, int H, int S, int d_v,
                     int W, int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r,
                     float* o, int* dev_err, void* stream) {
+  return sdm_decode_step_tabled(kp, qp, in_dt, v, v_dt, alpha, beta, M, B, H, S, d_v, W, R, idx_w,
+                                sc_w, idx_r, sc_r, o, dev_err, nullptr, stream);
+}
+
+int sdm_decode_table_words(int W, int R, int S) {
+  if (W < 1 || R < 1 || S < 1 || S > SDM_MAX_S || W > SDM_MAX_K || R > SDM_MAX_K) return -1;
+  return stair_table_words(W, R, S);
+}
+
+int sdm_decode_table(uint32_t* table, int W, int R, int S, void* stream) {
+  if (sdm_decode_table_words(W, R, S) < 0) return SDM_EINVAL;
+  if (!table) return SDM_EINVAL;
+  if (reinterpret_cast<uintptr_t>(table) & 3u) return SDM_EALIGN;
+  return launch_stair_table(table, W, R, S, as_stream(stream));
+}
+
+int sdm_decode_step_tabled(const void* kp, const void* qp, int in_dt, const void* v, int v_dt,
+                           const float* alpha, const float* beta, float* M, int B, int H, int S,
+                           int d_v, int W, int R, int32_t* idx_w, float* sc_w, int32_t* idx_r,
+                           float* sc_r, float* o, int* dev_err, const uint32_t* table,
+                           void* stream) {
+  if (table && (reinterpret_cast<uintptr_t>(table) & 3u)) return SDM_EALIGN;
   int st = check_select_args(kp, qp, in_dt, B, H, 1, S, W, R, idx_w, sc_w, idx_r, sc_r);
   if (st != SDM_OK) return st;
   const long long N = (long long)S * S;
@@ -68,7 +90,7 @@ int sdm_decode_step(const void* kp, const void* qp, int in_dt, const void* v, in
   if (st != SDM_OK) return st;
   if (dev_err && (reinterpret_cast<uintptr_t>(dev_err) & 3u)) return SDM_EALIGN;
   return launch_decode(kp, qp, in_dt, v, v_dt, alpha, beta, M, B * H, S, d_v, W, R, idx_w, sc_w,
-                       idx_r, sc_r, o, dev_err, as_stream(stream));
+                       idx_r, sc_r, o, dev_err, as_stream(stream), table);
 }
 
 int sdm_decode_step_supported(int in_dt, int B, int H, int S, int d_v, int W, int R) {

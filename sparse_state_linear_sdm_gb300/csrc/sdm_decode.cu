@@ -50,12 +50,12 @@ struct DecodeArgs {
 __device__ __forceinline__ void decode_cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// A word of the other block's shared memory, at the address this block's copy has.
-__device__ __forceinline__ uint32_t decode_peer_load(const void* local, uint32_t peer) {
-  uint32_t addr = static_cast<uint32_t>(__cvta_generic_to_shared(local)), remote, v;
+// A word into the other block's shared memory, at the address this block's copy has (made
+// visible to the other block by the next cluster barrier).
+__device__ __forceinline__ void decode_peer_store(const void* local, uint32_t peer, uint32_t v) {
+  uint32_t addr = static_cast<uint32_t>(__cvta_generic_to_shared(local)), remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(peer));
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
-  return v;
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
 }
 
 // Shared memory of the planning and scan parts for NG groups of 256 threads with NB row
@@ -307,11 +307,14 @@ __device__ __forceinline__ TeamMem team_mem(unsigned char* base, int S, int kin_
   return m;
 }
 
-// Task `which` (0: k' / top-W, 1: q' / top-R) of token `item` by a team of 128 threads
+// Task `which` (0: k' / top-W, 1: q' / top-R) of token `item` by a team of TT threads
 // (team thread t); barriers bar0 (the team), bar0 + 1 and bar0 + 2 (its two halves).
+// peer >= 0: the slots and scores are also stored into the cluster block `peer`'s copy of
+// push_idx / push_sc.
 template <typename Tin, int EMAX, int TT>
 __device__ void team_select(const SelectArgs& a, long long item, int which, const uint32_t* stair,
-                            const TeamMem& m, int t, int bar0, bool write_out = true) {
+                            const TeamMem& m, int t, int bar0, bool write_out = true, int peer = -1,
+                            int32_t* push_idx = nullptr, float* push_sc = nullptr) {
   using IKey = typename InnerKeyOf<Tin>::type;
   constexpr int IBITS = sizeof(Tin) == 2 ? 32 : 48;
   const int S = a.S, K = which ? a.R : a.W, kin = min(K, S);
@@ -415,6 +418,9 @@ __device__ void team_select(const SelectArgs& a, long long item, int which, cons
   }
   int32_t* oi = (which ? a.idx_r : a.idx_w) + item * K;
   float* os = (which ? a.sc_r : a.sc_w) + item * K;
+  // the other block has started (its arrive at the kernel's start) before anything is stored
+  // into its shared memory
+  if (peer >= 0) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   for (int r = t; r < K; r += TT) {
     const uint64_t k = m.oout[r];
     const int32_t slot = int32_t(0xFFFFFFFFu - uint32_t(k & 0xFFFFFFFFu));
@@ -425,6 +431,10 @@ __device__ void team_select(const SelectArgs& a, long long item, int which, cons
     }
     m.ridx[r] = slot;
     m.rsc[r] = sc;
+    if (peer >= 0) {
+      decode_peer_store(push_idx + r, uint32_t(peer), uint32_t(slot));
+      decode_peer_store(push_sc + r, uint32_t(peer), __float_as_uint(sc));
+    }
   }
 }
 
@@ -441,6 +451,9 @@ __global__ void __launch_bounds__(TEAM ? 512 : 256, 1) decode_kernel(DecodeArgs 
   const int bh = blockIdx.x / d.parts, part = blockIdx.x - bh * d.parts;
   const int C = d.cols, LPR = C / 4, RPP = 256 / LPR;
   const int W = d.W, R = d.R, WR = W + R, d_v = d.d_v;
+  // cluster pair: this block has started (waited on before the other block stores into it)
+  if (TEAM && d.pair) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  const float alpha = d.alpha[bh], beta = d.beta[bh];
 
   // ---- 1. selection of token (bh, 0) -------------------------------------------------
   const int32_t* gw = a.idx_w + size_t(bh) * W;
@@ -457,19 +470,20 @@ __global__ void __launch_bounds__(TEAM ? 512 : 256, 1) decode_kernel(DecodeArgs 
     const size_t tsize = (team_mem_bytes(a.S, a.kin_max, a.kpad, cmax, ikb) + 15) / 16 * 16;
     const TeamMem m0 = team_mem(tbase, a.S, a.kin_max, a.kpad, cmax, ikb);
     const TeamMem m1 = team_mem(tbase + tsize, a.S, a.kin_max, a.kpad, cmax, ikb);
-    // team 0's histograms are free until its selection starts: scratch for the staircases
-    build_stairs_parallel(stair_w, stair_r, a.W, a.R, a.S, reinterpret_cast<int*>(m0.hist), NT);
+    if (a.stair_g) {  // prebuilt by the caller (sdm_decode_table)
+      stair_w = const_cast<uint32_t*>(a.stair_g);
+      stair_r = stair_w + a.cnt_w;
+    } else {  // team 0's histograms are free until its selection starts: scratch for them
+      build_stairs_parallel(stair_w, stair_r, a.W, a.R, a.S, reinterpret_cast<int*>(m0.hist), NT);
+    }
     if (d.pair) {
-      // Block `part` of the cluster takes task `part` (0: k', 1: q') with every thread; the
-      // other task's slots and scores are then copied from the other block into m1.
-      team_select<Tin, EMAX, NT>(a, bh, part, part ? stair_r : stair_w, m0, tid, 1, true);
-      decode_cluster_sync();  // both tasks' results are in place
-      const int Kp = part ? W : R;  // the other task's slot count
-      for (int i = tid; i < Kp; i += NT) {
-        m1.ridx[i] = int32_t(decode_peer_load(m0.ridx + i, uint32_t(part ^ 1)));
-        m1.rsc[i] = __uint_as_float(decode_peer_load(m0.rsc + i, uint32_t(part ^ 1)));
-      }
-      decode_cluster_sync();  // neither block's results are read by the other after this
+      // Block `part` of the cluster takes task `part` (0: k', 1: q') with every thread and
+      // stores its slots and scores into its own m0 and the other block's m1 (which the
+      // selection does not use); one cluster barrier then makes both blocks' stores visible,
+      // and no block touches the other's shared memory after it.
+      team_select<Tin, EMAX, NT>(a, bh, part, part ? stair_r : stair_w, m0, tid, 1, true,
+                                 part ^ 1, m1.ridx, m1.rsc);
+      decode_cluster_sync();
       gw = part ? m1.ridx : m0.ridx;
       sw = part ? m1.rsc : m0.rsc;
       gr = part ? m0.ridx : m1.ridx;
@@ -487,7 +501,7 @@ __global__ void __launch_bounds__(TEAM ? 512 : 256, 1) decode_kernel(DecodeArgs 
     sbase = smem + d.sel_smem;
   } else {  // the selection kernel's pair mode: warps 0-1 the k' task, 2-3 the q' task
     const SelectSmem m = select_smem(a, smem);
-    select_build_stairs(a, m);
+    if (!a.stair_g) select_build_stairs(a, m);
     if (warp < 4) {
       const long long task = 2LL * bh + (warp >> 1);
       select_tasks<Tin, EMAX, true>(a, m, task, task + 1);
@@ -510,7 +524,6 @@ __global__ void __launch_bounds__(TEAM ? 512 : 256, 1) decode_kernel(DecodeArgs 
   for (int e = tid; e < WR; e += NT) idx[e] = e < W ? gw[e] : gr[e - W];
   if (warp == 0) warp_softmax(sw, W, wts);
   if (warp == 1) warp_softmax(sr, R, wts + W);
-  const float alpha = d.alpha[bh], beta = d.beta[bh];
   __syncthreads();
   // Write slots into an open-addressing table (a slot met twice: a duplicate write).
   int errs = 0;
@@ -679,7 +692,7 @@ template <typename Tin>
 int launch_decode_t(const void* kp, const void* qp, const void* v, int v_dt, const float* alpha,
                     const float* beta, float* M, int BH, int S, int d_v, int W, int R,
                     int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, float* o,
-                    int* dev_err, cudaStream_t s) {
+                    int* dev_err, cudaStream_t s, const uint32_t* stairs) {
   DecodeArgs dargs;
   int cols = 0, bufs = 1;
   size_t smem = 0;
@@ -693,6 +706,7 @@ int launch_decode_t(const void* kp, const void* qp, const void* v, int v_dt, con
   dargs.sel.sc_w = sc_w;
   dargs.sel.idx_r = idx_r;
   dargs.sel.sc_r = sc_r;
+  dargs.sel.stair_g = stairs;
   dargs.v = v;
   dargs.alpha = alpha;
   dargs.beta = beta;
@@ -749,13 +763,13 @@ int launch_decode_t(const void* kp, const void* qp, const void* v, int v_dt, con
 int launch_decode(const void* kp, const void* qp, int in_dt, const void* v, int v_dt,
                   const float* alpha, const float* beta, float* M, int BH, int S, int d_v, int W,
                   int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, float* o,
-                  int* dev_err, cudaStream_t s) {
+                  int* dev_err, cudaStream_t s, const uint32_t* stairs) {
   if (BH == 0) return SDM_OK;
   return in_dt == SDM_BF16
              ? launch_decode_t<uint16_t>(kp, qp, v, v_dt, alpha, beta, M, BH, S, d_v, W, R, idx_w,
-                                         sc_w, idx_r, sc_r, o, dev_err, s)
+                                         sc_w, idx_r, sc_r, o, dev_err, s, stairs)
              : launch_decode_t<float>(kp, qp, v, v_dt, alpha, beta, M, BH, S, d_v, W, R, idx_w,
-                                      sc_w, idx_r, sc_r, o, dev_err, s);
+                                      sc_w, idx_r, sc_r, o, dev_err, s, stairs);
 }
 
 int decode_supported(int in_dt, int BH, int S, int d_v, int W, int R) {

@@ -218,7 +218,7 @@ int decode_supported(int in_dt, int BH, int S, int d_v, int W, int R);
 int launch_decode(const void* kp, const void* qp, int in_dt, const void* v, int v_dt,
                   const float* alpha, const float* beta, float* M, int BH, int S, int d_v, int W,
                   int R, int32_t* idx_w, float* sc_w, int32_t* idx_r, float* sc_r, float* o,
-                  int* dev_err, cudaStream_t s);
+                  int* dev_err, cudaStream_t s, const uint32_t* stairs = nullptr);
 // Tests of the projection kernels' timeout path: the producer of cluster rank `cta` (0 for
 // the single-CTA kernel) stops issuing copies after `step` K steps, and every wait gives up
 // after wait_ns, so that the kernel stops, drains and reports SDM_DEV_TIMEOUT.

@@ -278,3 +278,27 @@ def test_project_stall_rejects_bad_arguments_without_launching():
     assert call(err=None) == EINVAL
     assert call(B=1, T=100) == EUNSUPPORTED       # one row tile: no pair
     assert call(err=ctypes.c_void_p(0x10002)) == EALIGN   # dev_err is an int
+
+
+def _stair_words(K, S):
+    """Pairs (p, q) of ranks in two sorted lists of min(K, S) keys with (p+1)(q+1) <= K."""
+    kin = min(K, S)
+    return sum(1 for p in range(kin) for q in range(kin) if (p + 1) * (q + 1) <= K)
+
+
+def test_decode_table_sizes_and_argument_checks():
+    lib = sdm.lib()
+    for W, R, S in ((128, 128, 1024), (8, 8, 32), (5, 7, 2), (1, 1, 1), (128, 64, 16), (1024, 3, 4096)):
+        assert lib.sdm_decode_table_words(W, R, S) == _stair_words(W, S) + _stair_words(R, S), (W, R, S)
+    for W, R, S in ((0, 8, 32), (8, 0, 32), (8, 8, 0), (8, 8, 4097), (1025, 8, 64)):
+        assert lib.sdm_decode_table_words(W, R, S) == -1
+    assert lib.sdm_decode_table(None, 8, 8, 32, None) == EINVAL
+    assert lib.sdm_decode_table(FAKE, 0, 8, 32, None) == EINVAL
+    assert lib.sdm_decode_table(ctypes.c_void_p(0x10002), 8, 8, 32, None) == EALIGN
+    # a misaligned table is refused before anything else is looked at
+    odd_table = ctypes.c_void_p(0x10001)
+    assert lib.sdm_decode_step_tabled(FAKE, FAKE, 1, FAKE, 1, FAKE, FAKE, FAKE, 1, 1, 8, 16, 4, 4,
+                                      FAKE, FAKE, FAKE, FAKE, FAKE, None, odd_table, None) == EALIGN
+    # otherwise the checks of sdm_decode_step apply
+    assert lib.sdm_decode_step_tabled(FAKE, FAKE, 1, FAKE, 1, FAKE, FAKE, FAKE, 0, 1, 8, 16, 4, 4,
+                                      FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None) == EINVAL

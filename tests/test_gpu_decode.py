@@ -62,24 +62,32 @@ def _token(rng, B, H, S, dv, dt):
     (2, 1, 8, 64, 40, 64, torch.float32, 6),      # K > S; W = R = N: every row read is also written
     (1, 1, 24, 96, 200, 150, torch.bfloat16, 2),  # K > 128 (wide sort variant); 3 slices
     (3, 2, 16, 32, 8, 3, torch.float32, 4),
+    (16, 8, 32, 32, 16, 16, torch.bfloat16, 2),   # more sequence-heads than SM pairs: no clusters
 ])
 def test_fused_decode_equals_select_then_scan(B, H, S, dv, W, R, dt, steps):
     """sdm_decode_step (one kernel) against sdm_select + sdm_scan_forward on the same token,
-    chained over several tokens: slots, scores, o and M bit for bit."""
+    chained over several tokens: slots, scores, o and M bit for bit; the step given the
+    prebuilt staircase table (decode_table) too."""
     rng = np.random.default_rng(B * 100 + S + dv + W)
     M0 = torch.from_numpy((0.3 * rng.standard_normal((B, H, S * S, dv))).astype(np.float32)).cuda()
-    M1, M2 = M0.clone(), M0.clone()
+    M1, M2, M3 = M0.clone(), M0.clone(), M0.clone()
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    table = sdm.decode_table(W, R, S)
     for _ in range(steps):
         x = _token(rng, B, H, S, dv, dt)
         o1, sel1 = sdm.decode_step(x["kp"], x["qp"], x["v"], x["alpha"], x["beta"], M1, W, R, dev_err=err)
         sel2 = sdm.select(x["kp"], x["qp"], W, R)
         o2 = sdm.scan_forward(M2, *sel2, x["v"], x["alpha"], x["beta"])
+        o3, sel3 = sdm.decode_step(x["kp"], x["qp"], x["v"], x["alpha"], x["beta"], M3, W, R, dev_err=err,
+                                   table=table)
         torch.cuda.synchronize()
-        for a, b in zip(sel1, sel2):
+        for a, b, c in zip(sel1, sel2, sel3):
             assert torch.equal(a, b)
+            assert torch.equal(c, b)
         assert torch.equal(o1, o2)
+        assert torch.equal(o3, o2)
         assert torch.equal(M1, M2)
+        assert torch.equal(M3, M2)
     assert err.item() == 0
 
 
