@@ -555,6 +555,29 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def huge_page_share(tensors):
+    """Share of the host tensors' resident bytes that sit on transparent huge pages (from
+    /proc/self/smaps; None where that cannot be read)."""
+    import re
+    spans = [(t.data_ptr(), t.data_ptr() + t.numel() * t.element_size()) for t in tensors]
+    huge = rss = 0
+    cur = False
+    try:
+        with open("/proc/self/smaps") as f:
+            for line in f:
+                m = re.match(r"([0-9a-f]+)-([0-9a-f]+) ", line)
+                if m:
+                    lo, hi = int(m.group(1), 16), int(m.group(2), 16)
+                    cur = any(a < hi and b > lo for a, b in spans)
+                elif cur and line.startswith("AnonHugePages:"):
+                    huge += int(line.split()[1]) * 1024
+                elif cur and line.startswith("Rss:"):
+                    rss += int(line.split()[1]) * 1024
+    except OSError:
+        return None
+    return round(huge / rss, 3) if rss else None
+
+
 def e2e(st, cfg, sdm, args, dev, torch, K, world):
     """Same metric through the public API with the inputs in pinned host memory: every
     step copies its k', q', v, alpha, beta host->device and its o device->host inside the
@@ -652,6 +675,7 @@ def e2e(st, cfg, sdm, args, dev, torch, K, world):
     ms = max_over_ranks(a.elapsed_time(b), dev)
     return {"value": whole_job_rate(cfg.B * cfg.H * cfg.T, n, world, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms / n, **rates,
+            "host_huge_page_share": huge_page_share(list(host.values()) + o_host),
             "pipeline": "double-buffered: step k+1's host->device copies and step k's device->host copy "
                         "overlap step k's compute (copy stream); inputs copied token window by window, "
                         "each chunk's selection waiting for its own window (sdm_forward_streamed)"

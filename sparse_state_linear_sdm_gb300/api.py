@@ -454,7 +454,15 @@ def forward(kp, qp, v, alpha, beta, M0, W: int, R: int, M=None, workspace=None, 
     return o, M, out
 
 
-_HUGE = 1 << 21  # transparent huge page size asked for (the register call takes any size)
+def _huge_page_bytes() -> int:
+    """The size of a transparent huge page on this host (2 MB with 4 KB base pages, 512 MB
+    with 64 KB ones); 2 MB where the kernel does not say."""
+    try:
+        with open("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size") as f:
+            n = int(f.read().strip())
+        return n if n > 0 and n & (n - 1) == 0 else 1 << 21
+    except (OSError, ValueError):
+        return 1 << 21
 
 
 def pinned_empty(shape, dtype, device=None) -> torch.Tensor:
@@ -474,19 +482,23 @@ def pinned_empty(shape, dtype, device=None) -> torch.Tensor:
     shape = tuple(int(x) for x in shape)
     nbytes = int(np.prod(shape, dtype=np.int64)) * torch.empty((), dtype=dtype).element_size()
     madv = getattr(mmap, "MADV_HUGEPAGE", None)
-    if nbytes == 0 or madv is None or not hasattr(mmap, "MAP_ANONYMOUS"):
+    huge = _huge_page_bytes()
+    # A huge page covers only a whole, aligned stretch of the mapping, so the buffer starts on
+    # a huge-page boundary and its pages are whole huge pages; buffers under a quarter of one
+    # (where that rounding would waste most of the page) take torch's pinned allocator.
+    if nbytes < huge // 4 or madv is None or not hasattr(mmap, "MAP_ANONYMOUS"):
         return torch.empty(shape, dtype=dtype, pin_memory=True)
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
-    size = (nbytes + _HUGE - 1) // _HUGE * _HUGE + _HUGE  # room to start on a huge-page boundary
+    size = (nbytes + huge - 1) // huge * huge + huge  # room to start on a huge-page boundary
     mm = mmap.mmap(-1, size, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
     try:
         mm.madvise(madv)
     except OSError:
         pass
     raw = np.frombuffer(mm, dtype=np.uint8)
-    skip = (-raw.ctypes.data) % _HUGE
+    skip = (-raw.ctypes.data) % huge
     buf = raw[skip:skip + nbytes]
-    buf[:] = 0  # fault the pages in before they are locked
+    raw[skip:skip + (nbytes + huge - 1) // huge * huge] = 0  # fault whole huge pages in, then lock
     with torch.cuda.device(dev):
         rc = int(torch.cuda.cudart().cudaHostRegister(buf.ctypes.data, nbytes, 0))
     if rc != 0:

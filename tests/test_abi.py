@@ -302,3 +302,9 @@ def test_decode_table_sizes_and_argument_checks():
     # otherwise the checks of sdm_decode_step apply
     assert lib.sdm_decode_step_tabled(FAKE, FAKE, 1, FAKE, 1, FAKE, FAKE, FAKE, 0, 1, 8, 16, 4, 4,
                                       FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None) == EINVAL
+
+
+def test_huge_page_size_is_a_power_of_two():
+    from sparse_state_linear_sdm_gb300 import api
+    n = api._huge_page_bytes()
+    assert n >= 1 << 21 and n & (n - 1) == 0

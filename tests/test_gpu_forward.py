@@ -162,6 +162,24 @@ def test_pinned_empty_is_page_locked_and_round_trips():
     del h, b  # the registration goes with the buffers
 
 
+def test_pinned_empty_large_buffer_on_huge_page_boundary():
+    """A buffer of at least a quarter of the host's huge page takes the huge-page path: it
+    starts on a huge-page boundary, is page-locked and round-trips through the GPU."""
+    from sparse_state_linear_sdm_gb300 import api
+    huge = api._huge_page_bytes()
+    n = (huge // 4 + (1 << 20)) // 4
+    h = sdm.pinned_empty((n,), torch.float32)
+    assert h.is_pinned() and h.numel() == n
+    assert h.data_ptr() % huge == 0
+    x = torch.arange(n, dtype=torch.float32, device="cuda")
+    h.copy_(x, non_blocking=True)
+    y = torch.empty_like(x)
+    y.copy_(h, non_blocking=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y, x)
+    del h
+
+
 @pytest.mark.parametrize("chunks", [3, 4])
 def test_inputs_arriving_window_by_window(chunks):
     """The batch's inputs copied from pinned host memory one token window at a time on a
