@@ -812,6 +812,10 @@ class DecodeStep:
         self._tail = (M.data_ptr(), B, H, S, dv, W, R) + tuple(t.data_ptr() for t in self.sel) + (
             self.o.data_ptr(), self.err.data_ptr(), self.table.data_ptr() if self.fused else None)
         self._bufs = (self.kp, self.qp, self.v, self.alpha, self.beta)
+        # what a caller's input must match to be read in place (checked cheaply per call)
+        self._sig = tuple((b.dtype, tuple(b.shape)) for b in self._bufs)
+        self._dev_index = dev.index
+        self._raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
     def _body(self):
         if self.fused:
@@ -867,17 +871,18 @@ class DecodeStep:
         static buffers (no copy); False where they are not."""
         if not self.fused:
             return False
-        for x, buf in zip((kp, qp, v, alpha, beta), self._bufs):
-            if (not isinstance(x, torch.Tensor) or x.dtype != buf.dtype or x.shape != buf.shape
-                    or x.device != buf.device or not x.is_contiguous()):
+        idx = self._dev_index
+        for x, (dt, shape) in zip((kp, qp, v, alpha, beta), self._sig):
+            if (not isinstance(x, torch.Tensor) or x.dtype is not dt or x.shape != shape
+                    or x.get_device() != idx or not x.is_contiguous()):
                 return False
-        dev = self.M.device
-        if torch.cuda.current_device() != dev.index:
-            with torch.cuda.device(dev):
+        if torch.cuda.current_device() != idx:
+            with torch.cuda.device(self.M.device):
                 return self._direct(kp, qp, v, alpha, beta)
+        stream = (self._raw_stream(idx) if self._raw_stream is not None
+                  else torch.cuda.current_stream(self.M.device).cuda_stream)
         st = self._fn(kp.data_ptr(), qp.data_ptr(), self._codes[0], v.data_ptr(), self._codes[1],
-                      alpha.data_ptr(), beta.data_ptr(), *self._tail,
-                      torch.cuda.current_stream(dev).cuda_stream)
+                      alpha.data_ptr(), beta.data_ptr(), *self._tail, stream)
         if st != 0:
             raise SDMError("sdm_decode_step_tabled", st)
         return True
