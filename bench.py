@@ -838,9 +838,12 @@ def run_decode(args):
     # Each token's inputs as a producer would hand them over: contiguous tensors of their
     # own (staged before timing).  The single kernel reads them where they are.
     per_token = {k: torch.stack([st[k][:, :, t:t + 1] for t in range(args.warmup + K)]) for k in names}
+    # the tensor objects too (a producer hands each token's own tensors over; no slicing in
+    # the timed loop)
+    token_args = [[per_token[k][t] for k in names] for t in range(args.warmup + K)]
 
     def token(t):
-        return step(*[per_token[k][t] for k in names])
+        return step(*token_args[t])
 
     def token_strided(t):  # slices of the [B, H, T, ...] inputs: copied into the step's buffers
         return step(*[st[k][:, :, t:t + 1] for k in names])
@@ -910,7 +913,8 @@ def run_decode(args):
             "us_per_step_strided_inputs": ms_strided * 1e3,
             "us_per_step_device": ms_device * 1e3 if ms_device is not None else None,
             "decode_kernel": "one fused kernel per token" if step.fused else "select + plan + scan",
-            "note": "us_per_step: DecodeStep called per token on that token's own contiguous inputs "
+            "note": "us_per_step: DecodeStep called per token on that token's own contiguous inputs (tensor "
+                    "objects staged before timing) "
                     "(one launch of the single kernel, which reads them where they are); "
                     "us_per_step_strided_inputs: called on slices of the [B, H, T, ...] inputs, which are "
                     "copied into the step's buffers (5 copies) before the captured graph runs; "
