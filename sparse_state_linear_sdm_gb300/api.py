@@ -10,6 +10,7 @@ import ctypes
 import functools
 import math
 import os
+import sys
 import threading
 
 import torch
@@ -498,7 +499,13 @@ def pinned_empty(shape, dtype, device=None) -> torch.Tensor:
     raw = np.frombuffer(mm, dtype=np.uint8)
     skip = (-raw.ctypes.data) % huge
     buf = raw[skip:skip + nbytes]
-    raw[skip:skip + (nbytes + huge - 1) // huge * huge] = 0  # fault whole huge pages in, then lock
+    span = (nbytes + huge - 1) // huge * huge
+    raw[skip:skip + span] = 0  # fault whole huge pages in
+    if sys.platform.startswith("linux"):
+        try:  # MADV_COLLAPSE: put what did not come as huge pages onto huge pages, before locking
+            mm.madvise(25, skip, span)
+        except (OSError, ValueError):
+            pass
     with torch.cuda.device(dev):
         rc = int(torch.cuda.cudart().cudaHostRegister(buf.ctypes.data, nbytes, 0))
     if rc != 0:
