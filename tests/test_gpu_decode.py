@@ -125,3 +125,37 @@ def test_decode_step_column_slices_follow_the_scan_shape():
         assert all(torch.equal(a, b) for a, b in zip(s1, s2))
         assert torch.equal(o1, o2) and torch.equal(M1, M2)
     assert sdm.DecodeStep(M1, 4, 4, in_dtype=torch.float32).fused
+
+
+def test_decode_at_the_benchmark_size():
+    """The decode step at the size its benchmark runs (B=16, H=4, N=2^20, d_v=128,
+    W=R=128, bf16 inputs: clusters of two blocks, the staircase table): three tokens through
+    DecodeStep against select + scan_forward on a copy of the state, bit for bit, and o of
+    two sequence-heads against the oracle."""
+    cfg = wl.B16H4_T8192
+    T = 3
+    d = device_inputs(cfg, T=T)
+    M0 = device_M0(cfg)
+    M1 = torch.empty((cfg.B, cfg.H, cfg.N, cfg.d_v), dtype=torch.float32, device="cuda")
+    sdm.init_state_from_M0(M1, M0)
+    M2 = M1.clone()
+    step = sdm.DecodeStep(M1, cfg.W, cfg.R, in_dtype=torch.bfloat16)
+    assert step.fused and step.table is not None
+    outs = []
+    for t in range(T):
+        args = [d[k][:, :, t:t + 1].contiguous() for k in ("kp", "qp", "v", "alpha", "beta")]
+        outs.append(step(*args).clone())
+        sel = sdm.select(args[0], args[1], cfg.W, cfg.R)
+        o2 = sdm.scan_forward(M2, *sel, *args[2:])
+        torch.cuda.synchronize()
+        for a, b in zip(step.sel, sel):
+            assert torch.equal(a, b)
+        assert torch.equal(outs[-1], o2)
+    assert step.err.item() == 0
+    assert torch.equal(M1, M2)
+    del M2
+    heads = [(0, 0), (15, 3)]
+    ref = oracle_heads(cfg, host_heads(cfg, heads, 0, T))
+    o = torch.cat(outs, dim=2)
+    for k, (b, h) in enumerate(heads):
+        assert scaled_err(o[b, h].cpu().numpy(), ref["o"][k]) <= TOL
