@@ -223,3 +223,44 @@ def test_fill_state_sets_every_entry():
     sdm.fill_state(M, 1.5)
     torch.cuda.synchronize()
     assert bool((M == 1.5).all())
+
+
+def test_backward_at_the_benchmark_size():
+    """B16 H4 T8192 N=2^20 d_v=128 W=R=128, bf16 inputs, as the backward benchmark runs it
+    (zero final adjoint, dM0 only, M_0 shared across the batch): the gradients of two sampled
+    sequence-heads against the oracle; dM0 bit for bit equal to the mode that also writes
+    each sequence's dL/dM_0, whose sampled sequence-heads match the oracle's dM0."""
+    cfg = wl.B16H4_T8192
+    d = device_inputs(cfg)
+    M0 = device_M0(cfg)
+    sel = sdm.select(d["kp"], d["qp"], cfg.W, cfg.R)
+    del d["kp"], d["qp"]
+    M = torch.empty((cfg.B, cfg.H, cfg.N, cfg.d_v), device="cuda")
+    sdm.init_state_from_M0(M, M0)
+    o, w_prev, r_rows = sdm.scan_forward_train(M, *sel, d["v"], d["alpha"], d["beta"])
+    del o
+    rng = np.random.default_rng(23)
+    dO = torch.from_numpy(rng.standard_normal((cfg.B, cfg.H, cfg.T, cfg.d_v)).astype(np.float32)).cuda()
+    M.fill_(float("nan"))  # the adjoint table: ignored with a zero final adjoint
+    G = M
+    g = sdm.scan_backward(*sel, d["v"], d["alpha"], d["beta"], w_prev, r_rows, dO, G, shared_M0=True,
+                          final_zero=True, dm0_only=True)
+    torch.cuda.synchronize()
+    heads = ((0, 0), (cfg.B - 1, cfg.H - 1))
+    M0h = M0.cpu().numpy()
+    refs = {}
+    for b, h in heads:
+        s = lambda x: x[b, h].cpu().numpy()[None]
+        refs[b, h] = oracle.scan_backward(M0h[h][None], s(sel[0]), s(sel[1]), s(sel[2]), s(sel[3]),
+                                          to_np(d["v"][b, h])[None], s(d["alpha"]), s(d["beta"]), s(dO))
+        for name in ("dv", "dalpha", "dbeta", "dsc_w", "dsc_r"):
+            e = normwise(g[name][b, h].cpu().numpy()[None], refs[b, h][name])
+            assert e <= GTOL, (name, b, h, e)
+    dM0 = g["dM0"].clone()
+    G.fill_(float("nan"))
+    g2 = sdm.scan_backward(*sel, d["v"], d["alpha"], d["beta"], w_prev, r_rows, dO, G, shared_M0=True,
+                           final_zero=True)
+    torch.cuda.synchronize()
+    assert torch.equal(g2["dM0"], dM0)
+    for b, h in heads:
+        assert normwise(G[b, h].cpu().numpy()[None], refs[b, h]["dM0"]) <= GTOL
