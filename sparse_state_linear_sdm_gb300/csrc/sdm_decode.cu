@@ -125,6 +125,10 @@ __device__ void team_topk(Key* a, Key* b, int n, int need, int bits, Key* sel, u
                           int* ctr, int t, int nth, int bar) {
   int shift = bits - 8, nsel = 0, left = need;
   if (t == 0) ctr[0] = 0;
+  // the histogram is cleared here for the first pass and, for each later one, while the
+  // previous pass appends (no pass reads it after its bucket search)
+  for (int i = t; i < 256; i += nth) hist[i] = 0u;
+  team_bar(bar, nth);
   for (;;) {
     if (n <= left) {  // every candidate is in
       for (int i = t; i < n; i += nth) sel[nsel + i] = a[i];
@@ -139,8 +143,6 @@ __device__ void team_topk(Key* a, Key* b, int n, int need, int bits, Key* sel, u
       team_bar(bar, nth);
       return;
     }
-    for (int i = t; i < 256; i += nth) hist[i] = 0u;
-    team_bar(bar, nth);
     // Equal digits of a warp are counted with one atomic (few bins take most keys).
     for (int i0 = 0; i0 < n; i0 += nth) {
       const int i = i0 + t;
@@ -178,6 +180,7 @@ __device__ void team_topk(Key* a, Key* b, int n, int need, int bits, Key* sel, u
     team_bar(bar, nth);
     const uint32_t bstar = uint32_t(ctr[2]);
     const int above = ctr[3];
+    for (int i = t; i < 256; i += nth) hist[i] = 0u;  // for the next pass
     // Appends with one atomic per warp and list (ballot, then each lane's rank in it).
     const unsigned lane = threadIdx.x & 31, below = (1u << lane) - 1u;
     for (int i0 = 0; i0 < n; i0 += nth) {
